@@ -1,0 +1,256 @@
+"""CPU oracle for the CSA2 decode/prefill path -- TEST INFRASTRUCTURE.
+
+Only the tests, the package's smoke check and the benchmark's CPU-baseline leg may
+import this package.  The product library never loads it, and it shares no code
+with the CUDA sources: the arithmetic lives in ``csa2_oracle.c`` (plain loops,
+exact integers, fp64), selection here uses a library sort.
+
+What it computes, step by step (DeepSeek-V4.1-Flash report, aipaper.jasonlin.tech):
+  1. MXFP4 codec for indexer q/k and the main KV (report §2.4.4; OCP MX v1.0 rule).
+  2. Indexer score of every candidate position, s = sum_h w_h ReLU(q_h . k), with the
+     per-head dot rounded once to float32 and the head sum a float32 fma chain
+     (the kernel's precision, since these floats decide indices).
+  3. Top-K (K = 512, report §4.2.1): full sort by (-score, position); emitted in
+     ascending position order, padded with -1.
+  4. Hierarchical pool (report §2.3.2): block score = max score of the block's visible
+     positions (8 per block); top 2,048 blocks by (-score, block id); ascending, -1 pad.
+  5. Reindex (report §2.3.2; review page, notes on the official code: scores over the
+     full range, then a candidate mask): only pool positions compete.
+  6. Core attention in fp64 over the selected main-KV entries (dequantised) followed by
+     the SWA keys in [max(s, i-W+1), i] (report §2.3.1, §3.2.2).
+
+Parity of the attention values at scale is pinned only by closed forms, library
+special cases and invariants (see tests); the pages print no attention outputs.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "csa2_oracle.c")
+_OUT_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_OUT_DIR, "libcsa2_oracle.so")
+_lib = None
+_lock = threading.Lock()
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (plain C11 + OpenMP)."""
+    os.makedirs(_OUT_DIR, exist_ok=True)
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fopenmp", "-ffp-contract=off",
+                               "-fno-fast-math", "-shared", "-fPIC", _SRC, "-o", tmp, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _L():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            I64 = ctypes.c_int64
+            I = ctypes.c_int
+            lib.orc_quant_mxfp4.argtypes = [P, I64, I64, P, P]
+            lib.orc_dequant_mxfp4.argtypes = [P, P, I64, I64, P]
+            lib.orc_head_dots.argtypes = [I, I, P, P, P, P, P, I64, P]
+            lib.orc_index_scores.argtypes = [I, I, P, P, P, P, P, P, I64, P]
+            lib.orc_attention.argtypes = [I64, I, I, I, P, P, P, ctypes.c_double, P, P]
+            lib.orc_num_threads.restype = I
+            _lib = lib
+    return _lib
+
+
+def _p(a: np.ndarray):
+    assert a.flags.c_contiguous
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def num_threads() -> int:
+    return int(_L().orc_num_threads())
+
+
+# ---------------------------------------------------------------- MXFP4 codec
+def quant_mxfp4(x: np.ndarray):
+    """x [..., D] (float32/float64 holding exact values), D % 32 == 0 ->
+    (codes uint8 [..., D/2], scales uint8 [..., D/32])."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    D = x.shape[-1]
+    assert D % 32 == 0
+    rows = x.size // D
+    codes = np.empty(x.shape[:-1] + (D // 2,), np.uint8)
+    scales = np.empty(x.shape[:-1] + (D // 32,), np.uint8)
+    _L().orc_quant_mxfp4(_p(x), rows, D, _p(codes), _p(scales))
+    return codes, scales
+
+
+def dequant_mxfp4(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.uint8)
+    D = codes.shape[-1] * 2
+    rows = codes.size // (D // 2)
+    y = np.empty(codes.shape[:-1] + (D,), np.float64)
+    _L().orc_dequant_mxfp4(_p(codes), _p(scales), rows, D, _p(y))
+    return y
+
+
+# ---------------------------------------------------------------- scoring
+def head_dots(qc, qs, kc, ks, pos) -> np.ndarray:
+    """Per-head float32 dots D [npos, H] of one quantised query ([H, d/2], [H, d/32])
+    against key rows ``pos`` of a cache (kc [N, d/2], ks [N, d/32])."""
+    qc = np.ascontiguousarray(qc, np.uint8); qs = np.ascontiguousarray(qs, np.uint8)
+    kc = np.ascontiguousarray(kc, np.uint8); ks = np.ascontiguousarray(ks, np.uint8)
+    pos = np.ascontiguousarray(pos, np.int64)
+    H, d = qc.shape[0], qc.shape[1] * 2
+    out = np.empty((pos.size, H), np.float32)
+    _L().orc_head_dots(H, d, _p(qc), _p(qs), _p(kc), _p(ks), _p(pos), pos.size, _p(out))
+    return out
+
+
+def index_scores(qc, qs, w, kc, ks, pos) -> np.ndarray:
+    """float32 indexer scores of one quantised query at key rows ``pos``."""
+    qc = np.ascontiguousarray(qc, np.uint8); qs = np.ascontiguousarray(qs, np.uint8)
+    kc = np.ascontiguousarray(kc, np.uint8); ks = np.ascontiguousarray(ks, np.uint8)
+    w = np.ascontiguousarray(w, np.float32)
+    pos = np.ascontiguousarray(pos, np.int64)
+    H, d = qc.shape[0], qc.shape[1] * 2
+    out = np.empty(pos.size, np.float32)
+    _L().orc_index_scores(H, d, _p(qc), _p(qs), _p(w), _p(kc), _p(ks), _p(pos), pos.size,
+                          _p(out))
+    return out
+
+
+def n_visible(q_pos: int, ratio_m: int, n_keys: int) -> int:
+    """Entries a query at token position q_pos can see: entry j covers tokens
+    [j*m, j*m + m - 1] with no overlap (report §2.3), and only complete entries are
+    visible: (j + 1) * m - 1 <= q_pos."""
+    return int(min(n_keys, max(0, (q_pos + 1) // ratio_m)))
+
+
+# ---------------------------------------------------------------- selection
+def _order_desc(scores: np.ndarray, pos: np.ndarray) -> np.ndarray:
+    """Permutation sorting by (score descending, position ascending).
+
+    Floats compare by value (-0 == +0); a NaN score ranks below every number."""
+    s = scores.astype(np.float64)
+    key = np.where(np.isnan(s), np.inf, -s)
+    return np.lexsort((pos, key))
+
+
+def topk(scores: np.ndarray, pos: np.ndarray, k: int) -> np.ndarray:
+    """The k best (score, position) pairs; positions returned ascending, -1 padded."""
+    out = np.full(k, -1, np.int32)
+    if pos.size:
+        sel = pos[_order_desc(scores, pos)[:k]]
+        sel = np.sort(sel)
+        out[: sel.size] = sel
+    return out
+
+
+def block_candidates(scores: np.ndarray, n_vis: int, block: int, nb: int) -> np.ndarray:
+    """Top-nb blocks of ``block`` positions by max visible position score.
+
+    ``scores`` holds the scores of positions 0..n_vis-1; a partial last block uses its
+    visible positions only.  Block ids returned ascending, -1 padded."""
+    out = np.full(nb, -1, np.int32)
+    nblk = (n_vis + block - 1) // block
+    if nblk == 0:
+        return out
+    pad = np.full(nblk * block, -np.inf, np.float64)
+    s = scores[:n_vis].astype(np.float64)
+    pad[:n_vis] = np.where(np.isnan(s), -np.inf, s)
+    bscore = pad.reshape(nblk, block).max(axis=1)
+    # a block whose visible scores are all NaN ranks lowest, like a NaN position
+    allnan = np.zeros(nblk * block, bool)
+    allnan[:n_vis] = np.isnan(s)
+    allnan[n_vis:] = True
+    bscore = np.where(allnan.reshape(nblk, block).all(axis=1), np.nan, bscore)
+    sel = np.arange(nblk)[_order_desc(bscore.astype(np.float32), np.arange(nblk))[:nb]]
+    sel = np.sort(sel)
+    out[: sel.size] = sel
+    return out
+
+
+def pool_positions(block_ids: np.ndarray, block: int, n_vis: int) -> np.ndarray:
+    """Positions covered by the pool's blocks, restricted to the visible range."""
+    b = block_ids[block_ids >= 0].astype(np.int64)
+    p = (b[:, None] * block + np.arange(block)[None, :]).reshape(-1)
+    return np.sort(p[p < n_vis])
+
+
+# ---------------------------------------------------------------- layer flows
+def quant_query(q_f32: np.ndarray):
+    """Indexer q [H, d] (exact bf16 values) -> MXFP4 (codes [H, d/2], scales [H, d/32])."""
+    return quant_mxfp4(q_f32)
+
+
+def full_indexer(q_f32, w, kc, ks, q_pos, ratio_m, k=512, block=8, nb=2048,
+                 want_blocks=False):
+    """Full-mode indexer for one query: scores every visible position, Top-K, and
+    (for the decoder's first Full layer) the block pool."""
+    qc, qs = quant_query(q_f32)
+    nvis = n_visible(q_pos, ratio_m, kc.shape[0])
+    pos = np.arange(nvis, dtype=np.int64)
+    s = index_scores(qc, qs, w, kc, ks, pos)
+    idx = topk(s, pos, k)
+    blocks = block_candidates(s, nvis, block, nb) if want_blocks else None
+    return idx, blocks, s
+
+
+def reindex_indexer(q_f32, w, kc, ks, q_pos, ratio_m, pool_blocks, k=512, block=8):
+    """Reindex-mode indexer for one query: only positions of the pool compete."""
+    qc, qs = quant_query(q_f32)
+    nvis = n_visible(q_pos, ratio_m, kc.shape[0])
+    pos = pool_positions(np.asarray(pool_blocks), block, nvis)
+    s = index_scores(qc, qs, w, kc, ks, pos)
+    return topk(s, pos, k), s, pos
+
+
+def swa_keys_range(q_pos: int, swa_pos0: int, n_slots: int, window: int, swa_start: int):
+    """Slots of an SWA buffer (slot j holds token swa_pos0 + j) that a query at q_pos
+    attends: tokens in [max(s, i - W + 1, 0), i] (report §3.2.2)."""
+    lo = max(swa_start, q_pos - window + 1, 0)
+    j0 = max(lo - swa_pos0, 0)
+    j1 = min(q_pos - swa_pos0, n_slots - 1)
+    return j0, j1          # inclusive; empty when j1 < j0
+
+
+def attention_rows(q_rows, key_lists, sm_scale, d_v):
+    """fp64 attention: q_rows [R, H, d_qk] float64, key_lists: list of [n_j, d_qk]
+    float64 arrays -> (out [R, H, d_v], lse [R, H])."""
+    q_rows = np.ascontiguousarray(q_rows, np.float64)
+    R, H, dqk = q_rows.shape
+    off = np.zeros(R + 1, np.int64)
+    for r, kl in enumerate(key_lists):
+        off[r + 1] = off[r] + kl.shape[0]
+    keys = (np.concatenate(key_lists, axis=0) if off[-1] > 0
+            else np.zeros((1, dqk), np.float64))
+    keys = np.ascontiguousarray(keys, np.float64)
+    out = np.empty((R, H, d_v), np.float64)
+    lse = np.empty((R, H), np.float64)
+    _L().orc_attention(R, H, dqk, d_v, _p(q_rows), _p(off), _p(keys), float(sm_scale),
+                       _p(out), _p(lse))
+    return out, lse
+
+
+def gather_keys(idx, kv_codes, kv_scales, swa_f64, q_pos, swa_pos0, window, swa_start):
+    """Key list of one query: dequantised main-KV rows for idx >= 0 (in idx order,
+    duplicates kept, out-of-range indices dropped), then its SWA slots in order."""
+    n = kv_codes.shape[0]
+    sel = [int(i) for i in np.asarray(idx).reshape(-1) if 0 <= int(i) < n]
+    parts = []
+    if sel:
+        parts.append(dequant_mxfp4(kv_codes[sel], kv_scales[sel]))
+    if swa_f64 is not None:
+        j0, j1 = swa_keys_range(q_pos, swa_pos0, swa_f64.shape[0], window, swa_start)
+        if j1 >= j0:
+            parts.append(swa_f64[j0:j1 + 1])
+    d = kv_codes.shape[1] * 2
+    return np.concatenate(parts, 0) if parts else np.zeros((0, d), np.float64)

@@ -1,0 +1,329 @@
+/*
+ * csa2_oracle.c -- plain, slow CPU oracle for the CSA2 decode/prefill path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product library links, loads or calls
+ * this file; only the tests, the package's smoke check and the benchmark's CPU
+ * baseline leg do.  It shares no code, header, table or constant with the CUDA
+ * sources.
+ *
+ * Sources (DeepSeek-V4.1-Flash: Pushing the Limits of KV Cache Compression):
+ *   - report page (aipaper.jasonlin.tech) §2.3: CSA2 indexer scores main-KV entries
+ *     from indexer Q and indexer K and keeps the Top-K per query; each query attends
+ *     the selected entries together with the layer's SWA KV.
+ *   - report §2.4.4: indexer queries and keys use the OCP MXFP4 format; cached values
+ *     are dequantised before attention.
+ *   - report §3.2.2: a query at position i attends SWA keys in [max(s, i-W+1), i].
+ *   - review page (papers.chlience.com), "四位缓存" ledger: indexer K carries one 8-bit
+ *     scale per 32 channels.
+ * The score formula  s = sum_h w_h * ReLU(q_h . k)  is the one the workload
+ * definition states; the pages print none.
+ *
+ * Precision: everything here is exact or fp64 except where a float32 value decides
+ * an index (the indexer score), which is computed in the float32 precision the GPU
+ * kernel uses:
+ *   D_h = RN32(exact q_h . k)          one rounding of the exact dyadic dot
+ *   s   = fma32(w_{H-1}, R_{H-1}, ... fma32(w_0, R_0, +0))     R_h = max(D_h, 0)
+ * Build: gcc -O2 -std=c11 -fopenmp -ffp-contract=off -shared -fPIC.
+ */
+#include <stdint.h>
+#include <string.h>
+#include <math.h>
+#include <limits.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ------------------------------------------------------------------------- */
+/* MXFP4 codec (OCP Microscaling Formats v1.0: E2M1 elements, E8M0 scale per  */
+/* block of 32).  Report §2.4.4 names the format; the steps below are the     */
+/* OCP conversion: X = floor(log2(amax)) - emax_elem with emax_elem = 2 for  */
+/* E2M1, elements = RNE(x / 2^X) saturated to +-6.                            */
+/* ------------------------------------------------------------------------- */
+
+/* E2M1 magnitude of code bits 0..2 (1 sign bit, 2 exponent bits, 1 mantissa bit). */
+static double e2m1_magnitude(int code3)
+{
+    int e = (code3 >> 1) & 3, m = code3 & 1;
+    if (e == 0) return m ? 0.5 : 0.0;                  /* subnormal: m * 2^-1 */
+    return ldexp(1.0 + 0.5 * m, e - 1);                /* normal: (1 + m/2) * 2^(e-1) */
+}
+
+/* Nearest E2M1 magnitude to v >= 0, ties to the even code, saturating at 6. */
+static int e2m1_round_magnitude(double v)
+{
+    if (v >= 6.0) return 7;
+    for (int c = 0; c < 7; ++c) {
+        double lo = e2m1_magnitude(c), hi = e2m1_magnitude(c + 1);
+        if (v <= hi) {
+            double mid = 0.5 * (lo + hi);               /* exact in double */
+            if (v < mid) return c;
+            if (v > mid) return c + 1;
+            return (c % 2 == 0) ? c : c + 1;
+        }
+    }
+    return 7;
+}
+
+/* floor(log2(a)) for finite a > 0: frexp gives a = f * 2^e with f in [0.5, 1). */
+static int floor_log2(double a)
+{
+    int e;
+    frexp(a, &e);
+    return e - 1;
+}
+
+/* Quantise rows of doubles (each an exact bf16/fp32 value) to MXFP4.
+ * codes: [rows, cols/2], element 2i in the low nibble; scales: [rows, cols/32] = X + 127.
+ * An all-zero block gets X = 0.  The sign bit of every element is the sign bit of x. */
+void orc_quant_mxfp4(const double *x, int64_t rows, int64_t cols,
+                     uint8_t *codes, uint8_t *scales)
+{
+    int64_t nblk = cols / 32;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t b = 0; b < nblk; ++b) {
+            const double *xb = x + r * cols + b * 32;
+            double amax = 0.0;
+            for (int i = 0; i < 32; ++i) amax = fmax(amax, fabs(xb[i]));
+            int X = 0;
+            if (amax > 0.0) {
+                X = floor_log2(amax) - 2;
+                if (X < -127) X = -127;
+                if (X > 127) X = 127;
+            }
+            scales[r * nblk + b] = (uint8_t)(X + 127);
+            for (int i = 0; i < 32; ++i) {
+                double v = ldexp(fabs(xb[i]), -X);       /* exact */
+                int c = e2m1_round_magnitude(v) | (signbit(xb[i]) ? 8 : 0);
+                uint8_t *p = &codes[r * (cols / 2) + b * 16 + i / 2];
+                if (i % 2 == 0) *p = (uint8_t)c;
+                else *p = (uint8_t)(*p | (c << 4));
+            }
+        }
+    }
+}
+
+/* Dequantise MXFP4 rows to doubles: sign * magnitude(code) * 2^(scale - 127). */
+void orc_dequant_mxfp4(const uint8_t *codes, const uint8_t *scales, int64_t rows,
+                       int64_t cols, double *y)
+{
+    int64_t nblk = cols / 32;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t i = 0; i < cols; ++i) {
+            int byte = codes[r * (cols / 2) + i / 2];
+            int c = (i % 2 == 0) ? (byte & 15) : (byte >> 4);
+            double m = ldexp(e2m1_magnitude(c & 7), (int)scales[r * nblk + i / 32] - 127);
+            y[r * cols + i] = (c & 8) ? -m : m;
+        }
+}
+
+/* ------------------------------------------------------------------------- */
+/* Exact dot product of two MXFP4 vectors, rounded once to float32.           */
+/* Twice an E2M1 magnitude is an integer, so each block of 32 contributes     */
+/*   I_b * 2^(Xq_b + Xk_b - 2),  I_b = sum (2 q_i)(2 k_i)  (|I_b| <= 4608).     */
+/* ------------------------------------------------------------------------- */
+
+static int e2m1_twice_signed(int code)
+{
+    int t = (int)(2.0 * e2m1_magnitude(code & 7));
+    return (code & 8) ? -t : t;
+}
+
+/* Wide two's-complement fixed point for sums whose exponents are far apart.
+ * Bit 0 has weight 2^BIG_E0; 24 limbs of 32 bits cover every exponent a product of
+ * two E8M0-scaled blocks can have (-258 .. 252) plus carries. */
+#define BIG_LIMBS 24
+#define BIG_E0 (-320)
+
+static void big_add(uint32_t *acc, int64_t m, int e)
+{
+    uint32_t t[BIG_LIMBS];
+    memset(t, 0, sizeof t);
+    uint64_t mag = (uint64_t)(m < 0 ? -m : m);
+    int sh = e - BIG_E0;
+    for (int bit = 0; bit < 64; ++bit)
+        if ((mag >> bit) & 1u) {
+            int pos = sh + bit;
+            t[pos / 32] |= 1u << (pos % 32);
+        }
+    if (m < 0) {                                       /* two's complement negate */
+        uint64_t carry = 1;
+        for (int i = 0; i < BIG_LIMBS; ++i) {
+            uint64_t v = (uint64_t)(uint32_t)~t[i] + carry;
+            t[i] = (uint32_t)v;
+            carry = v >> 32;
+        }
+    }
+    uint64_t carry = 0;
+    for (int i = 0; i < BIG_LIMBS; ++i) {
+        uint64_t v = (uint64_t)acc[i] + t[i] + carry;
+        acc[i] = (uint32_t)v;
+        carry = v >> 32;
+    }
+}
+
+static int big_bit(const uint32_t *a, int i)
+{
+    return (i >= 0 && i < 32 * BIG_LIMBS) ? (int)((a[i / 32] >> (i % 32)) & 1u) : 0;
+}
+
+/* Round sign * mag * 2^BIG_E0 to float32, round-to-nearest-even, with IEEE
+ * subnormals and overflow to infinity. */
+static float big_round_f32(const uint32_t *acc_in)
+{
+    uint32_t a[BIG_LIMBS];
+    memcpy(a, acc_in, sizeof a);
+    int neg = (int)(a[BIG_LIMBS - 1] >> 31);
+    if (neg) {
+        uint64_t carry = 1;
+        for (int i = 0; i < BIG_LIMBS; ++i) {
+            uint64_t v = (uint64_t)(uint32_t)~a[i] + carry;
+            a[i] = (uint32_t)v;
+            carry = v >> 32;
+        }
+    }
+    int top = -1;
+    for (int i = 32 * BIG_LIMBS - 1; i >= 0; --i)
+        if (big_bit(a, i)) { top = i; break; }
+    if (top < 0) return 0.0f;
+    int lsb = top - 23;                                /* keep 24 significant bits */
+    if (lsb + BIG_E0 < -149) lsb = -149 - BIG_E0;      /* subnormal: lsb weight 2^-149 */
+    uint64_t M = 0;
+    for (int i = top; i >= lsb; --i) M = (M << 1) | (uint64_t)big_bit(a, i);
+    int round = big_bit(a, lsb - 1), sticky = 0;
+    for (int i = lsb - 2; i >= 0; --i) sticky |= big_bit(a, i);
+    if (round && (sticky || (M & 1u))) M += 1;
+    double v = ldexp((double)M, lsb + BIG_E0);         /* exact; float cast below is */
+    float f = (float)v;                                /* exact or overflows to inf  */
+    return neg ? -f : f;
+}
+
+/* RN32 of sum_b I[b] * 2^e[b] (nb terms). */
+static float dyadic_sum_to_f32(int nb, const int64_t *I, const int *e)
+{
+    int emin = INT_MAX, emax = INT_MIN, any = 0;
+    for (int b = 0; b < nb; ++b)
+        if (I[b] != 0) {
+            any = 1;
+            if (e[b] < emin) emin = e[b];
+            if (e[b] > emax) emax = e[b];
+        }
+    if (!any) return 0.0f;
+    int grow = 0;
+    while ((1 << grow) < nb) ++grow;
+    if ((emax - emin) + 13 + grow <= 53) {
+        /* every partial sum is an integer multiple of 2^emin below 2^53 of it: exact */
+        double s = 0.0;
+        for (int b = 0; b < nb; ++b) s += ldexp((double)I[b], e[b]);
+        return (float)s;                               /* one RNE rounding */
+    }
+    uint32_t acc[BIG_LIMBS];
+    memset(acc, 0, sizeof acc);
+    for (int b = 0; b < nb; ++b)
+        if (I[b] != 0) big_add(acc, I[b], e[b]);
+    return big_round_f32(acc);
+}
+
+/* D = RN32(qhat . khat) for one head and one key row, both MXFP4 of dim d. */
+static float exact_dot_f32(int d, const uint8_t *qc, const uint8_t *qs,
+                           const uint8_t *kc, const uint8_t *ks)
+{
+    int nb = d / 32;
+    int64_t I[64];
+    int e[64];
+    for (int b = 0; b < nb; ++b) {
+        int64_t acc = 0;
+        for (int i = 0; i < 32; ++i) {
+            int j = b * 32 + i;
+            int cq = (j % 2 == 0) ? (qc[j / 2] & 15) : (qc[j / 2] >> 4);
+            int ck = (j % 2 == 0) ? (kc[j / 2] & 15) : (kc[j / 2] >> 4);
+            acc += (int64_t)e2m1_twice_signed(cq) * e2m1_twice_signed(ck);
+        }
+        I[b] = acc;
+        e[b] = ((int)qs[b] - 127) + ((int)ks[b] - 127) - 2;
+    }
+    return dyadic_sum_to_f32(nb, I, e);
+}
+
+/* Per-head dots D_h (float32) of one quantised query against listed key rows.
+ * qc [H, d/2], qs [H, d/32]; key row p at kc + p*d/2, ks + p*d/32; out [npos, H]. */
+void orc_head_dots(int H, int d, const uint8_t *qc, const uint8_t *qs,
+                   const uint8_t *kc, const uint8_t *ks, const int64_t *pos, int64_t npos,
+                   float *out)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < npos; ++i)
+        for (int h = 0; h < H; ++h)
+            out[i * H + h] = exact_dot_f32(d, qc + (int64_t)h * (d / 2), qs + (int64_t)h * (d / 32),
+                                           kc + pos[i] * (d / 2), ks + pos[i] * (d / 32));
+}
+
+/* Indexer score of one query against listed key rows:
+ *   s = fma32 chain over h = 0..H-1 of (w_h, max(D_h, 0)), starting from +0. */
+void orc_index_scores(int H, int d, const uint8_t *qc, const uint8_t *qs, const float *w,
+                      const uint8_t *kc, const uint8_t *ks, const int64_t *pos, int64_t npos,
+                      float *out)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < npos; ++i) {
+        float s = 0.0f;
+        for (int h = 0; h < H; ++h) {
+            float D = exact_dot_f32(d, qc + (int64_t)h * (d / 2), qs + (int64_t)h * (d / 32),
+                                    kc + pos[i] * (d / 2), ks + pos[i] * (d / 32));
+            float R = D > 0.0f ? D : 0.0f;
+            s = fmaf(w[h], R, s);
+        }
+        out[i] = s;
+    }
+}
+
+/* ------------------------------------------------------------------------- */
+/* Core attention in fp64 over an explicit key list per query row.            */
+/* logits l_j = sm_scale * q_h . k_j (all d_qk dims); p = softmax(l);         */
+/* o_h = sum_j p_j * k_j[0:d_v]; lse_h = max_j l_j + log(sum_j exp(l_j - max)).*/
+/* A row with no keys gets o = 0 and lse = -inf.                              */
+/* ------------------------------------------------------------------------- */
+void orc_attention(int64_t nrows, int H, int dqk, int dv, const double *q,
+                   const int64_t *key_off, const double *keys, double sm_scale,
+                   double *out, double *lse)
+{
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < nrows; ++r) {
+        int64_t k0 = key_off[r], nk = key_off[r + 1] - key_off[r];
+        for (int h = 0; h < H; ++h) {
+            const double *qh = q + (r * H + h) * (int64_t)dqk;
+            double *oh = out + (r * H + h) * (int64_t)dv;
+            for (int c = 0; c < dv; ++c) oh[c] = 0.0;
+            if (nk == 0) { lse[r * H + h] = -INFINITY; continue; }
+            double mx = -INFINITY;
+            for (int64_t j = 0; j < nk; ++j) {
+                const double *kj = keys + (k0 + j) * (int64_t)dqk;
+                double l = 0.0;
+                for (int c = 0; c < dqk; ++c) l += qh[c] * kj[c];
+                l *= sm_scale;
+                if (l > mx) mx = l;
+            }
+            double z = 0.0;
+            for (int64_t j = 0; j < nk; ++j) {
+                const double *kj = keys + (k0 + j) * (int64_t)dqk;
+                double l = 0.0;
+                for (int c = 0; c < dqk; ++c) l += qh[c] * kj[c];
+                double p = exp(l * sm_scale - mx);
+                z += p;
+                for (int c = 0; c < dv; ++c) oh[c] += p * kj[c];
+            }
+            for (int c = 0; c < dv; ++c) oh[c] /= z;
+            lse[r * H + h] = mx + log(z);
+        }
+    }
+}
+
+int orc_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

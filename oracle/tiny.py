@@ -1,0 +1,132 @@
+"""Brute-force exact reference for tiny inputs (TEST INFRASTRUCTURE).
+
+Written independently of ``csa2_oracle.c`` with Python ``fractions.Fraction`` so
+that it can pin the C oracle: every value here is an exact rational, every
+rounding an explicit integer round-half-even.  Slow by design: only for inputs
+of a few dozen positions.
+
+Format facts used (DeepSeek-V4.1-Flash report, aipaper.jasonlin.tech, §2.4.4:
+indexer queries and keys in OCP MXFP4): E2M1 = 1 sign bit, 2 exponent bits with
+bias 1, 1 mantissa bit; E8M0 scale = 2^(byte - 127); blocks of 32.
+"""
+from __future__ import annotations
+
+from fractions import Fraction
+from typing import List, Sequence
+
+import numpy as np
+
+TWO = Fraction(2)
+
+
+def e2m1_value(code: int) -> Fraction:
+    """Value of a 4-bit E2M1 code from its bit fields."""
+    s = -1 if code & 8 else 1
+    e = (code >> 1) & 3
+    m = code & 1
+    if e == 0:
+        mag = Fraction(m, 2)                       # subnormal: 0.m * 2^(1-1)
+    else:
+        mag = (1 + Fraction(m, 2)) * TWO ** (e - 1)
+    return s * mag
+
+
+def floor_log2(a: Fraction) -> int:
+    """Largest k with 2^k <= a (a > 0)."""
+    k = a.numerator.bit_length() - a.denominator.bit_length()
+    while TWO ** k > a:
+        k -= 1
+    while TWO ** (k + 1) <= a:
+        k += 1
+    return k
+
+
+def quant_block(xs: Sequence[Fraction], signs: Sequence[bool]):
+    """OCP MXFP4 of one block of 32 exact values -> (scale byte, [codes]).
+
+    ``signs`` carries the sign bit of each input (so -0.0 keeps it)."""
+    amax = max(abs(x) for x in xs)
+    X = 0 if amax == 0 else min(127, max(-127, floor_log2(amax) - 2))
+    codes = []
+    grid = [abs(e2m1_value(c)) for c in range(8)]
+    for x, neg in zip(xs, signs):
+        v = abs(x) / TWO ** X
+        if v >= 6:
+            c = 7
+        else:
+            best = min(range(8), key=lambda c: (abs(v - grid[c]), c % 2))   # ties -> even code
+            c = best
+        codes.append(c | (8 if neg else 0))
+    return X + 127, codes
+
+
+def rn32(x: Fraction) -> np.float32:
+    """Round an exact rational to float32 (nearest, ties to even; subnormals; inf)."""
+    if x == 0:
+        return np.float32(0.0)
+    neg = x < 0
+    a = -x if neg else x
+    e = floor_log2(a)
+    q = max(e, -126) - 23                           # weight of the last kept bit
+    scaled = a / TWO ** q
+    n = scaled.numerator // scaled.denominator
+    rem = scaled - n
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and n % 2 == 1):
+        n += 1
+    val = n * TWO ** q
+    if val >= TWO ** 128:
+        f = np.float32(np.inf)
+    else:
+        f = np.float32(float(val))                  # exactly representable
+    return -f if neg else f
+
+
+def fma32(a: np.float32, b: np.float32, c: np.float32) -> np.float32:
+    """float32 fused multiply-add: one rounding of the exact a*b + c.
+
+    Infinite or NaN operands give the IEEE special result (no rounding involved)."""
+    if not (np.isfinite(a) and np.isfinite(b) and np.isfinite(c)):
+        with np.errstate(invalid="ignore", over="ignore"):
+            return np.float32(np.float64(a) * np.float64(b) + np.float64(c))
+    return rn32(Fraction(float(a)) * Fraction(float(b)) + Fraction(float(c)))
+
+
+def dequant(codes: List[int], scale_byte: int) -> List[Fraction]:
+    sc = TWO ** (scale_byte - 127)
+    return [e2m1_value(c) * sc for c in codes]
+
+
+def unpack_codes(packed: np.ndarray) -> List[int]:
+    """uint8 [D/2] -> D codes, element 2i from the low nibble."""
+    out = []
+    for byte in packed.tolist():
+        out.append(byte & 15)
+        out.append(byte >> 4)
+    return out
+
+
+def exact_vector(codes_packed: np.ndarray, scales: np.ndarray) -> List[Fraction]:
+    codes = unpack_codes(codes_packed)
+    vals = []
+    for b, sb in enumerate(scales.tolist()):
+        vals += dequant(codes[32 * b: 32 * b + 32], sb)
+    return vals
+
+
+def score(qc, qs, w, kc, ks) -> np.float32:
+    """s = fma32 chain over heads of (w_h, max(RN32(q_h . k), 0))."""
+    kv = exact_vector(kc, ks)
+    s = np.float32(0.0)
+    for h in range(qc.shape[0]):
+        qv = exact_vector(qc[h], qs[h])
+        D = rn32(sum((a * b for a, b in zip(qv, kv)), Fraction(0)))
+        R = D if D > 0 else np.float32(0.0)
+        s = fma32(np.float32(w[h]), R, s)
+    return s
+
+
+def topk_positions(scores: Sequence[float], positions: Sequence[int], k: int) -> List[int]:
+    """k best by (score descending, position ascending); returned ascending, -1 padded."""
+    order = sorted(range(len(positions)), key=lambda i: (-float(scores[i]), positions[i]))
+    sel = sorted(positions[i] for i in order[:k])
+    return sel + [-1] * (k - len(sel))

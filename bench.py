@@ -1,0 +1,352 @@
+"""Benchmark of the CSA2 decode hot path on one GB300 (or N independent replicas).
+
+Default workload: Full-mode decode layer, batch 32, 65,536 global positions per sequence,
+indexer 32 heads x 128 (MXFP4 K), main KV 512 + 64 dims (MXFP4), 64 heads, Top-512,
+SWA 128 (bf16).  One step = the whole path for one new token per sequence:
+  csa2_quant_fp4  (write the token's main-KV and indexer-K rows into the caches)
+  csa2_index_score (indexer query quantised inside; every visible position scored)
+  csa2_topk        (Top-512, ascending)
+  csa2_sparse_attn (gather + dequantise 512 entries, + 128 SWA keys, 64-head attention)
+metric: decode tokens/s per layer (batch / step time); roofline of the dominant kernel
+(the indexer scan) in achieved HBM GB/s.
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--extra]
+Under torchrun each rank runs its own replica (the path has no exchange step).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from fp4_kv_cache_gb300 import synth  # noqa: E402
+
+METRIC = "CSA2 decode tokens/s per layer (Full mode, 64K ctx)"
+WORKLOAD = "full_decode_64k"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def _kernel_bytes(w):
+    """Algorithmic bytes of the indexer scan per launch: MXFP4 K codes + scales of every
+    visible position (68 B at d_i = 128), the bf16 indexer query and the head weights.
+    Score materialisation is overhead and not counted."""
+    per_pos = w.idx_dim // 2 + w.idx_dim // 32
+    return w.batch * w.n_keys * per_pos + w.batch * w.n_q * w.idx_heads * (w.idx_dim * 2 + 4)
+
+
+def _step_bytes(w):
+    """Algorithmic bytes of a whole step (what the method must move)."""
+    kv_row = w.d_qk // 2 + w.d_qk // 32
+    idx_bytes = _kernel_bytes(w)
+    attn = w.batch * w.n_q * (w.topk * (kv_row + 4) + w.window * w.d_qk * 2
+                              + w.heads * w.d_qk * 2 + w.heads * w.d_v * 2)
+    write = w.batch * (w.d_qk * 2 + kv_row + w.idx_dim * 2 + w.idx_dim // 2 + w.idx_dim // 32)
+    return idx_bytes + attn + write
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ CPU baseline (oracle)
+def oracle_sample(w, rows):
+    """Run the CPU oracle over `rows` sequences of the workload: indexer over every
+    visible position, Top-512, fp64 attention.  Returns (seconds, tokens)."""
+    import oracle
+    f32 = synth.bf16_to_f32
+    qi, ww, qa = synth.gen_queries(w, rows)
+    qpos = synth.q_positions(w)
+    n_slots, pos0 = synth.swa_layout(w)
+    inputs = []
+    for i, b in enumerate(rows):   # inputs prepared outside the timed region
+        kc, ks = oracle.quant_mxfp4(f32(synth.gen_index_keys(w, b, qi[i], ww[i])))
+        kv = f32(synth.gen_main_kv(w, b))
+        swa = f32(synth.gen_swa(w, b)).astype(np.float64)
+        inputs.append((kc, ks, kv, swa))
+    t0 = time.perf_counter()
+    for i, b in enumerate(rows):
+        kc, ks, kv, swa = inputs[i]
+        for t in range(w.n_q):
+            idx, _, _ = oracle.full_indexer(f32(qi[i, t]), ww[i, t], kc, ks, int(qpos[b, t]),
+                                            w.ratio_m, w.topk)
+            sel = idx[idx >= 0]
+            vc, vs = oracle.quant_mxfp4(kv[sel])
+            keys = oracle.gather_keys(np.arange(sel.size), vc, vs, swa, int(qpos[b, t]), pos0,
+                                      w.window, 0)
+            oracle.attention_rows(f32(qa[i, t])[None].astype(np.float64), [keys],
+                                  1.0 / math.sqrt(w.d_qk), w.d_v)
+    return time.perf_counter() - t0, len(rows) * w.n_q
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import oracle
+    w = synth.WORKLOADS[WORKLOAD]
+    for _ in range(args.warmup):
+        oracle_sample(w, [0])
+    times = []
+    for s in range(args.steps):
+        dt, tok = oracle_sample(w, [s % w.batch])
+        times.append(dt)
+    tps = args.steps / sum(times)
+    cores = oracle.num_threads()
+    sample = "1 of 32 sequences per step: oracle indexer over 65,536 positions, Top-512, fp64 attention"
+    line = {"impl": "reference", "metric": METRIC, "value": tps, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000 * sum(times) / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "global_batch": 1, "seq_len": w.n_keys,
+                       "parallelism": "cpu-oracle"},
+            "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_gpu(args):
+    import torch
+    from fp4_kv_cache_gb300 import csa2, workload
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    w = synth.WORKLOADS[WORKLOAD]
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    dw = workload.build(w, device=dev, d_status=st)
+    B, T = w.batch, w.n_q
+    stream = torch.cuda.current_stream(dev)
+
+    # the token being decoded: its main-KV / indexer-K rows (float) to write into the caches
+    rng = np.random.default_rng([w.seed, 1000])
+    new_kv = workload.bf16_tensor(synth.f32_to_bf16_bits(
+        rng.standard_normal((B, w.d_qk), dtype=np.float32)), dev)
+    new_k = workload.bf16_tensor(synth.f32_to_bf16_bits(
+        rng.standard_normal((B, w.idx_dim), dtype=np.float32)), dev)
+    last = w.n_keys - 1        # the decoded token's slot (the query sits at position N - 1)
+    new_kvc, new_kvs = dw["kv_codes"][:, last], dw["kv_scales"][:, last]
+    new_kc, new_ks = dw["k_codes"][:, last], dw["k_scales"][:, last]
+    # preallocated outputs
+    scores = torch.empty((B, T, w.n_keys), dtype=torch.float32, device=dev)
+    row_len = torch.empty((B, T), dtype=torch.int32, device=dev)
+    idx = torch.empty((B, T, w.topk), dtype=torch.int32, device=dev)
+    out = torch.empty((B, T, w.heads, w.d_v), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, T, w.heads), dtype=torch.float32, device=dev)
+    iargs = csa2.make_index_args(dw["q_idx"], dw["w_idx"], dw["k_codes"], dw["k_scales"],
+                                 dw["q_pos"], w.ratio_m)
+    aargs = csa2.make_attn_args(dw["q_attn"], dw["kv_codes"], dw["kv_scales"], idx, dw["swa"],
+                                dw["swa_pos0"], dw["q_pos"], None, w.window, dw.sm_scale, w.d_v)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    launches_per_step = 5
+
+    def step(k_ev=None):
+        # cache write: the new token's main-KV and indexer-K rows, quantised in place
+        csa2.csa2_quant_fp4(new_kv, new_kvc, new_kvs, st)
+        csa2.csa2_quant_fp4(new_k, new_kc, new_ks, st)
+        if k_ev:
+            k_ev[0].record(stream)
+        csa2.csa2_index_score(iargs, scores, row_len, st)
+        if k_ev:
+            k_ev[1].record(stream)
+        csa2.csa2_topk(scores, w.topk, idx, row_len, d_status=st)
+        csa2.csa2_sparse_attn(aargs, out, lse, st)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if int(st.item()) != 0:
+        raise RuntimeError(f"device status {int(st.item())}")
+
+    # ---- device-timed steps: inputs resident in HBM, L2 flushed between steps (untimed)
+    t_steps, t_kern = [], []
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clocks:
+        for _ in range(args.steps):
+            flush.fill_(1)
+            e0, e1, k_ev = ev(), ev(), (ev(), ev())
+            e0.record(stream)
+            step(k_ev)
+            e1.record(stream)
+            t_steps.append((e0, e1))
+            t_kern.append(k_ev)
+        torch.cuda.synchronize(dev)
+    ms_steps = [a.elapsed_time(b) for a, b in t_steps]
+    ms_kern = [a.elapsed_time(b) for a, b in t_kern]
+    ms_step = sum(ms_steps) / len(ms_steps)
+    ms_k = sum(ms_kern) / len(ms_kern)
+
+    # ---- end to end through the public API from pinned host buffers
+    h_qi = dw["q_idx"].cpu().pin_memory()
+    h_w = dw["w_idx"].cpu().pin_memory()
+    h_qa = dw["q_attn"].cpu().pin_memory()
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = h_qi.numel() * 2 + h_w.numel() * 4 + h_qa.numel() * 2
+    d2h = h_out.numel() * 2
+    for _ in range(2):
+        dw["q_idx"].copy_(h_qi, non_blocking=True)
+        step()
+    torch.cuda.synchronize(dev)
+    e2e_ms = []
+    for _ in range(args.steps):
+        flush.fill_(1)
+        e0, e1 = ev(), ev()
+        e0.record(stream)
+        dw["q_idx"].copy_(h_qi, non_blocking=True)
+        dw["w_idx"].copy_(h_w, non_blocking=True)
+        dw["q_attn"].copy_(h_qa, non_blocking=True)
+        step()
+        h_out.copy_(out, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        e2e_ms.append(e0.elapsed_time(e1))
+    e2e_step = sum(e2e_ms) / len(e2e_ms)
+    if int(st.item()) != 0:
+        raise RuntimeError(f"device status {int(st.item())}")
+
+    # ---- max over ranks
+    if dist:
+        t = torch.tensor([ms_step, ms_k, e2e_step], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step, ms_k, e2e_step = t.tolist()
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return 0
+
+    peak, peak_kind = _peaks()
+    kb = _kernel_bytes(w)
+    achieved = kb / (ms_k * 1e-3) / 1e9
+    tokens = B * T * world
+    line = {
+        "metric": METRIC, "value": tokens / (ms_step * 1e-3), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp4-e2m1/f32",
+        "data": "synthetic (seeded N(0,1) caches quantised to MXFP4, U(0,1) head weights, 1% planted)",
+        "config": {"workload": WORKLOAD, "global_batch": B * world, "seq_len": w.n_keys,
+                   "parallelism": f"replicas{world}", "topk": w.topk, "window": w.window,
+                   "indexer": f"{w.idx_heads}x{w.idx_dim}", "heads": w.heads,
+                   "d_qk": w.d_qk, "d_v": w.d_v,
+                   "l2": "flushed between timed steps (256 MiB write, untimed)"},
+        "achieved_gbs_step": _step_bytes(w) / (ms_step * 1e-3) / 1e9,
+        "roofline": {"bound": "hbm", "kernel": "csa2_index_score", "achieved": achieved,
+                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "algorithmic_bytes": kb, "ms": ms_k},
+        "e2e": {"value": tokens / (e2e_step * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_step},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks.summary(),
+    }
+    if not args.no_cpu_baseline:
+        import oracle
+        dt, tok = oracle_sample(w, [0, 1])
+        line["cpu_baseline"] = {"value": tok / dt, "unit": "tokens/s", "cores": oracle.num_threads(),
+                                "kind": "oracle",
+                                "sample": "2 of 32 sequences: oracle indexer over 65,536 positions, "
+                                          "Top-512, fp64 attention"}
+    print(json.dumps(line))
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,199 @@
+// api.cu -- extern "C" entry points of libcsa2.so (declared in include/csa2.h).
+//
+// Host-side validation happens here, before any launch; the kernels live in quant.cu,
+// index_score.cu, topk.cu and attn.cu.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/csa2.h"
+#include "internal.h"
+
+using namespace csa2;
+
+namespace {
+
+inline bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+inline csa2_status from_cuda(cudaError_t e) { return e == cudaSuccess ? CSA2_OK : CSA2_ERR_CUDA; }
+
+inline cudaStream_t as_stream(csa2_stream s) { return reinterpret_cast<cudaStream_t>(s); }
+
+bool index_args_ok(const csa2_index_args *a)
+{
+    if (!a) return false;
+    if (a->batch < 0 || a->n_q < 0 || a->n_keys < 0 || a->n_keys >= (int64_t(1) << 31)) return false;
+    if ((int64_t)a->batch * a->n_q > 65535) return false;
+    if (a->n_heads < 1 || a->n_heads > 64) return false;
+    if (a->head_dim != 32 && a->head_dim != 64 && a->head_dim != 128) return false;
+    if (a->ratio_m < 1) return false;
+    if (a->mode != CSA2_INDEX_FULL && a->mode != CSA2_INDEX_POOL) return false;
+    if (a->block < 1 || a->block > 32) return false;
+    const bool empty = (int64_t)a->batch * a->n_q == 0;
+    if (!empty && (!a->q || !a->w || (a->n_keys > 0 && (!a->k_codes || !a->k_scales)))) return false;
+    if (a->k_codes && !aligned(a->k_codes, 16)) return false;
+    if (a->mode == CSA2_INDEX_POOL) {
+        if (a->n_pool_blocks < 0) return false;
+        if (!empty && a->n_pool_blocks > 0 && !a->pool_blocks) return false;
+        if ((int64_t)a->n_pool_blocks * a->block >= (int64_t(1) << 31)) return false;
+    }
+    return true;
+}
+
+int64_t index_candidates(const csa2_index_args *a)
+{
+    return a->mode == CSA2_INDEX_POOL ? (int64_t)a->n_pool_blocks * a->block : a->n_keys;
+}
+
+bool attn_args_ok(const csa2_attn_args *a)
+{
+    if (!a) return false;
+    if (a->batch < 0 || a->n_q < 0 || a->n_kv < 0) return false;
+    if ((int64_t)a->batch * a->n_q > 65535) return false;
+    if (a->n_heads < 1 || a->n_heads > 128) return false;
+    if (a->d_qk < 32 || a->d_qk > 1024 || a->d_qk % 32) return false;
+    if (a->d_v < 8 || a->d_v > a->d_qk || a->d_v % 8) return false;
+    if (a->topk < 0 || a->topk > 2048 || a->window < 0) return false;
+    const bool empty = (int64_t)a->batch * a->n_q == 0;
+    if (empty) return true;
+    if (!a->q) return false;
+    if (a->topk > 0 && (!a->idx || (a->n_kv > 0 && (!a->kv_codes || !a->kv_scales)))) return false;
+    if (a->swa) {
+        if (a->n_swa < 0 || !a->swa_pos0 || !a->q_pos) return false;
+    }
+    return true;
+}
+
+} // namespace
+
+extern "C" {
+
+const char *csa2_status_string(csa2_status s)
+{
+    switch (s) {
+    case CSA2_OK: return "ok";
+    case CSA2_ERR_INVALID_ARG: return "invalid argument";
+    case CSA2_ERR_UNSUPPORTED: return "unsupported request";
+    case CSA2_ERR_CUDA: return "CUDA launch error";
+    case CSA2_ERR_WORKSPACE: return "workspace too small";
+    }
+    return "unknown status";
+}
+
+int csa2_version(void) { return 100; }
+
+size_t csa2_cache_bytes_per_position(csa2_fp4_format main_fmt, int32_t d_main, int32_t d_idx)
+{
+    if (d_main <= 0 || d_idx <= 0 || d_idx % 32) return 0;
+    size_t main_bytes;
+    if (main_fmt == CSA2_FMT_MXFP4) {
+        if (d_main % 32) return 0;
+        main_bytes = (size_t)d_main / 2 + (size_t)d_main / 32;     // E2M1 codes + E8M0 / 32
+    } else if (main_fmt == CSA2_FMT_NVFP4_E4M3_16) {
+        if (d_main % 16) return 0;
+        main_bytes = (size_t)d_main / 2 + (size_t)d_main / 16;     // E2M1 codes + E4M3 / 16
+    } else {
+        return 0;
+    }
+    return main_bytes + (size_t)d_idx / 2 + (size_t)d_idx / 32;    // MXFP4 indexer key
+}
+
+csa2_status csa2_quant_fp4(const void *x, csa2_dtype xt, int64_t rows, int64_t cols, int64_t ldx,
+                           uint8_t *codes, int64_t ldc, uint8_t *scales, int64_t lds,
+                           csa2_fp4_format fmt, uint32_t *d_status, csa2_stream stream)
+{
+    if (fmt == CSA2_FMT_NVFP4_E4M3_16) return CSA2_ERR_UNSUPPORTED;
+    if (fmt != CSA2_FMT_MXFP4 || (xt != CSA2_BF16 && xt != CSA2_F32)) return CSA2_ERR_INVALID_ARG;
+    if (rows < 0 || cols < 0 || cols % 32) return CSA2_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0) return CSA2_OK;
+    if (!x || !codes || !scales) return CSA2_ERR_INVALID_ARG;
+    if (ldx < cols || ldc < cols / 2 || lds < cols / 32) return CSA2_ERR_INVALID_ARG;
+    return from_cuda(launch_quant_mxfp4(x, xt == CSA2_BF16, rows, cols, ldx, codes, ldc, scales,
+                                        lds, d_status, as_stream(stream)));
+}
+
+csa2_status csa2_dequant_fp4(const uint8_t *codes, int64_t ldc, const uint8_t *scales,
+                             int64_t lds, int64_t rows, int64_t cols, csa2_fp4_format fmt,
+                             void *y, csa2_dtype yt, int64_t ldy, csa2_stream stream)
+{
+    if (fmt == CSA2_FMT_NVFP4_E4M3_16) return CSA2_ERR_UNSUPPORTED;
+    if (fmt != CSA2_FMT_MXFP4 || (yt != CSA2_BF16 && yt != CSA2_F32)) return CSA2_ERR_INVALID_ARG;
+    if (rows < 0 || cols < 0 || cols % 32) return CSA2_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0) return CSA2_OK;
+    if (!y || !codes || !scales) return CSA2_ERR_INVALID_ARG;
+    if (ldy < cols || ldc < cols / 2 || lds < cols / 32) return CSA2_ERR_INVALID_ARG;
+    return from_cuda(launch_dequant_mxfp4(codes, ldc, scales, lds, rows, cols, y, yt == CSA2_BF16,
+                                          ldy, as_stream(stream)));
+}
+
+size_t csa2_index_score_workspace_size(const csa2_index_args *) { return 0; }
+
+csa2_status csa2_index_score(const csa2_index_args *a, float *scores, int32_t *row_len, void *ws,
+                             size_t ws_bytes, uint32_t *d_status, csa2_stream stream)
+{
+    if (!index_args_ok(a)) return CSA2_ERR_INVALID_ARG;
+    if ((int64_t)a->batch * a->n_q == 0) return CSA2_OK;
+    if (!scores && index_candidates(a) > 0) return CSA2_ERR_INVALID_ARG;
+    if (ws_bytes < csa2_index_score_workspace_size(a)) return CSA2_ERR_WORKSPACE;
+    (void)ws;
+    return from_cuda(launch_index_score(*a, scores, row_len, d_status, as_stream(stream)));
+}
+
+size_t csa2_topk_workspace_size(int64_t rows, int64_t n, int32_t k)
+{
+    return topk_ws_bytes(rows, n, k);
+}
+
+csa2_status csa2_topk(const float *scores, int64_t rows, int64_t n, const int32_t *row_len,
+                      const int32_t *pool_blocks, int32_t block, int32_t k, int32_t *idx,
+                      float *out_scores, void *ws, size_t ws_bytes, uint32_t *d_status,
+                      csa2_stream stream)
+{
+    if (rows < 0 || n < 0 || n >= (int64_t(1) << 31) || k < 0 || rows > (int64_t(1) << 31))
+        return CSA2_ERR_INVALID_ARG;
+    if (pool_blocks && (block < 1 || n % block)) return CSA2_ERR_INVALID_ARG;
+    if (rows == 0 || k == 0) return CSA2_OK;
+    if (!idx || (n > 0 && !scores)) return CSA2_ERR_INVALID_ARG;
+    if (ws_bytes < csa2_topk_workspace_size(rows, n, k)) return CSA2_ERR_WORKSPACE;
+    return from_cuda(launch_topk(scores, rows, n, row_len, pool_blocks, block, k, idx, out_scores,
+                                 ws, d_status, as_stream(stream)));
+}
+
+size_t csa2_block_candidates_workspace_size(int64_t rows, int64_t n, int32_t block, int32_t nb)
+{
+    if (rows <= 0 || n < 0 || block < 1 || nb <= 0) return 0;
+    return block_candidates_ws_bytes(rows, n, block, nb);
+}
+
+csa2_status csa2_block_candidates(const float *scores, int64_t rows, int64_t n,
+                                  const int32_t *row_len, int32_t block, int32_t nb,
+                                  int32_t *block_ids, void *ws, size_t ws_bytes,
+                                  uint32_t *d_status, csa2_stream stream)
+{
+    if (rows < 0 || n < 0 || n >= (int64_t(1) << 31) || block < 1 || nb < 0 ||
+        rows > (int64_t(1) << 31))
+        return CSA2_ERR_INVALID_ARG;
+    if (rows == 0 || nb == 0) return CSA2_OK;
+    if (!block_ids || (n > 0 && !scores)) return CSA2_ERR_INVALID_ARG;
+    const size_t need = csa2_block_candidates_workspace_size(rows, n, block, nb);
+    if (ws_bytes < need) return CSA2_ERR_WORKSPACE;
+    if (need && (!ws || !aligned(ws, 16))) return CSA2_ERR_INVALID_ARG;
+    return from_cuda(launch_block_candidates(scores, rows, n, row_len, block, nb, block_ids, ws,
+                                             d_status, as_stream(stream)));
+}
+
+size_t csa2_sparse_attn_workspace_size(const csa2_attn_args *a)
+{
+    return a ? sparse_attn_ws_bytes(*a) : 0;
+}
+
+csa2_status csa2_sparse_attn(const csa2_attn_args *a, uint16_t *out, float *lse, void *ws,
+                             size_t ws_bytes, uint32_t *d_status, csa2_stream stream)
+{
+    if (!attn_args_ok(a)) return CSA2_ERR_INVALID_ARG;
+    if ((int64_t)a->batch * a->n_q == 0) return CSA2_OK;
+    if (!out) return CSA2_ERR_INVALID_ARG;
+    if (ws_bytes < csa2_sparse_attn_workspace_size(a)) return CSA2_ERR_WORKSPACE;
+    return from_cuda(launch_sparse_attn(*a, out, lse, ws, d_status, as_stream(stream)));
+}
+
+} // extern "C"

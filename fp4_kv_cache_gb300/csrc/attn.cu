@@ -1,0 +1,248 @@
+// attn.cu -- CSA2 core sparse latent attention (csa2_sparse_attn), CUDA-core kernel.
+//
+// DeepSeek-V4.1-Flash report (aipaper.jasonlin.tech) §2.3 / §2.3.1: in every mode a query
+// attends the selected main-KV entries together with the layer's SWA KV; §2.4.4: the FP4
+// main-KV entries are dequantised before attention; §3.2.2: a query at token i attends
+// SWA keys in [max(s, i-W+1), i].  Review page (papers.chlience.com, CSA2 section): the
+// main KV is a latent shared by every query head, so V is its leading d_v dims.
+//
+// One CTA = one query row x 8 heads.  Keys stream through shared memory in tiles of 32
+// (gathered FP4 rows dequantised exactly to float, then the SWA slots), with an online
+// softmax per head and fp32 accumulation.
+#include "common.cuh"
+#include "internal.h"
+#include <math.h>
+
+namespace csa2 {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kHG = 8;    // heads per CTA (one warp each for the logits)
+constexpr int kKT = 32;   // keys per tile (one lane each for the logits)
+
+struct AttnParams {
+    int32_t T, H, d_qk, d_v, topk, window, n_swa;
+    float sm_scale;
+    int64_t n_kv;
+    const uint16_t *q;
+    const uint8_t *kvc, *kvs;
+    const int32_t *idx;
+    const uint16_t *swa;
+    const int32_t *swa_pos0, *swa_start, *q_pos;
+    uint16_t *out;
+    float *lse;
+    uint32_t *d_status;
+};
+
+__device__ __forceinline__ float warp_max(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+template <int CPT>
+__global__ void __launch_bounds__(kThreads) sparse_attn_cc_kernel(AttnParams P)
+{
+    extern __shared__ float smem[];
+    const int ldk = P.d_qk + 1;
+    float *s_k = smem;                       // [kKT][ldk]
+    float *s_q = s_k + kKT * ldk;            // [kHG][d_qk]
+    float *s_p = s_q + kHG * P.d_qk;         // [kHG][kKT]
+    __shared__ int64_t s_src[kKT];           // >= 0: main-KV row; <= -2: SWA slot -(src+2); -1: none
+    __shared__ float s_corr[kHG], s_m[kHG], s_l[kHG];
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t row = blockIdx.y;
+    const int64_t b = row / P.T;
+    const int h0 = blockIdx.x * kHG;
+
+    for (int e = tid; e < kHG * P.d_qk; e += kThreads) {
+        const int hh = e / P.d_qk, c = e % P.d_qk;
+        s_q[e] = (h0 + hh < P.H)
+                     ? __uint_as_float((uint32_t)P.q[(row * P.H + h0 + hh) * (int64_t)P.d_qk + c] << 16)
+                     : 0.0f;
+    }
+
+    // SWA slots of this query: tokens [max(s, p - W + 1, 0), p] of a buffer whose slot 0
+    // holds token swa_pos0
+    int64_t j0 = 0, n_sw = 0;
+    if (P.swa) {
+        const int64_t p = P.q_pos[row];
+        const int64_t s0 = P.swa_start ? (int64_t)P.swa_start[b] : 0;
+        int64_t lo = p - P.window + 1;
+        lo = lo < s0 ? s0 : lo;
+        lo = lo < 0 ? 0 : lo;
+        const int64_t pos0 = P.swa_pos0[b];
+        j0 = lo - pos0 < 0 ? 0 : lo - pos0;
+        int64_t j1 = p - pos0;
+        j1 = j1 > P.n_swa - 1 ? P.n_swa - 1 : j1;
+        n_sw = j1 >= j0 ? j1 - j0 + 1 : 0;
+    }
+    const int64_t n_slots = P.topk + n_sw;
+
+    float acc[kHG][CPT];
+#pragma unroll
+    for (int hh = 0; hh < kHG; ++hh)
+#pragma unroll
+        for (int u = 0; u < CPT; ++u) acc[hh][u] = 0.0f;
+    float m_run = -INFINITY, l_run = 0.0f;   // per-head state, held by the head's warp
+    const int my_h = h0 + warp;
+
+    for (int64_t t0 = 0; t0 < n_slots; t0 += kKT) {
+        if (tid < kKT) {
+            const int64_t sl = t0 + tid;
+            int64_t src = -1;
+            if (sl < P.topk) {
+                const int32_t id = P.idx[row * P.topk + sl];
+                if (id >= 0 && id < P.n_kv) src = id;
+                else if (id != -1) dev_flag(P.d_status, CSA2_DEV_BAD_INDEX);
+            } else if (sl < n_slots) {
+                src = -(j0 + (sl - P.topk) + 2);
+            }
+            s_src[tid] = src;
+        }
+        __syncthreads();
+        // gather + dequantise (main KV) or widen (SWA) the tile's keys
+        for (int e = tid; e < kKT * P.d_qk; e += kThreads) {
+            const int j = e / P.d_qk, c = e % P.d_qk;
+            const int64_t src = s_src[j];
+            float v = 0.0f;
+            if (src >= 0) {
+                const int64_t r = b * P.n_kv + src;
+                const uint32_t byte = P.kvc[r * (P.d_qk / 2) + c / 2];
+                const uint32_t code = (c & 1) ? (byte >> 4) : (byte & 15u);
+                v = e2m1_mag(code & 7u) * e8m0_value(P.kvs[r * (P.d_qk / 32) + c / 32]);
+                if (code & 8u) v = -v;
+            } else if (src <= -2) {
+                const int64_t slot = -src - 2;
+                v = __uint_as_float((uint32_t)P.swa[(b * P.n_swa + slot) * (int64_t)P.d_qk + c] << 16);
+            }
+            s_k[j * ldk + c] = v;
+        }
+        __syncthreads();
+        // logits: warp = head, lane = key
+        {
+            float l = -INFINITY;
+            if (my_h < P.H && s_src[lane] != -1) {
+                float dot = 0.0f;
+                const float *qh = s_q + warp * P.d_qk;
+                const float *kj = s_k + lane * ldk;
+                for (int c = 0; c < P.d_qk; ++c) dot = fmaf(qh[c], kj[c], dot);
+                l = dot * P.sm_scale;
+            }
+            const float m_new = fmaxf(m_run, warp_max(l));
+            float p = 0.0f, corr = 1.0f;
+            if (m_new != -INFINITY) {
+                p = (l == -INFINITY) ? 0.0f : expf(l - m_new);
+                corr = (m_run == -INFINITY) ? 0.0f : expf(m_run - m_new);
+            }
+            l_run = l_run * corr + warp_sum(p);
+            m_run = m_new;
+            s_p[warp * kKT + lane] = p;
+            if (lane == 0) s_corr[warp] = corr;
+        }
+        __syncthreads();
+        // P.V over the tile: thread owns columns tid + 256u of every head
+#pragma unroll
+        for (int hh = 0; hh < kHG; ++hh) {
+            const float corr = s_corr[hh];
+#pragma unroll
+            for (int u = 0; u < CPT; ++u) acc[hh][u] *= corr;
+        }
+        for (int j = 0; j < kKT; ++j) {
+            float v[CPT];
+#pragma unroll
+            for (int u = 0; u < CPT; ++u) {
+                const int c = tid + kThreads * u;
+                v[u] = c < P.d_v ? s_k[j * ldk + c] : 0.0f;
+            }
+#pragma unroll
+            for (int hh = 0; hh < kHG; ++hh) {
+                const float p = s_p[hh * kKT + j];
+#pragma unroll
+                for (int u = 0; u < CPT; ++u) acc[hh][u] = fmaf(p, v[u], acc[hh][u]);
+            }
+        }
+        __syncthreads();
+    }
+    if (lane == 0) { s_m[warp] = m_run; s_l[warp] = l_run; }
+    __syncthreads();
+#pragma unroll
+    for (int hh = 0; hh < kHG; ++hh) {
+        const int h = h0 + hh;
+        if (h >= P.H) continue;
+        const float l = s_l[hh];
+        const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+#pragma unroll
+        for (int u = 0; u < CPT; ++u) {
+            const int c = tid + kThreads * u;
+            if (c < P.d_v) {
+                const float o = acc[hh][u] * inv;
+                // round to nearest even bf16
+                uint32_t bits = __float_as_uint(o);
+                bits += 0x7fffu + ((bits >> 16) & 1u);
+                P.out[(row * P.H + h) * (int64_t)P.d_v + c] = (uint16_t)(bits >> 16);
+            }
+        }
+        if (P.lse && tid == 0) P.lse[row * P.H + h] = l > 0.0f ? s_m[hh] + logf(l) : -INFINITY;
+    }
+}
+
+template <int CPT>
+cudaError_t launch_cc(const AttnParams &P, int64_t rows, cudaStream_t s)
+{
+    const size_t smem = sizeof(float) * ((size_t)kKT * (P.d_qk + 1) + (size_t)kHG * P.d_qk + kHG * kKT);
+    cudaError_t e = cudaFuncSetAttribute(sparse_attn_cc_kernel<CPT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid((unsigned)((P.H + kHG - 1) / kHG), (unsigned)rows);
+    sparse_attn_cc_kernel<CPT><<<grid, kThreads, smem, s>>>(P);
+    return cudaGetLastError();
+}
+
+} // namespace
+
+size_t sparse_attn_ws_bytes(const csa2_attn_args &) { return 0; }
+
+cudaError_t launch_sparse_attn(const csa2_attn_args &a, uint16_t *out, float *lse, void *,
+                               uint32_t *d_status, cudaStream_t s)
+{
+    AttnParams P;
+    P.T = a.n_q;
+    P.H = a.n_heads;
+    P.d_qk = a.d_qk;
+    P.d_v = a.d_v;
+    P.topk = a.topk;
+    P.window = a.window;
+    P.n_swa = a.swa ? a.n_swa : 0;
+    P.sm_scale = a.sm_scale;
+    P.n_kv = a.n_kv;
+    P.q = a.q;
+    P.kvc = a.kv_codes;
+    P.kvs = a.kv_scales;
+    P.idx = a.idx;
+    P.swa = a.swa;
+    P.swa_pos0 = a.swa_pos0;
+    P.swa_start = a.swa_start;
+    P.q_pos = a.q_pos;
+    P.out = out;
+    P.lse = lse;
+    P.d_status = d_status;
+    const int64_t rows = (int64_t)a.batch * a.n_q;
+    if (rows == 0 || a.n_heads == 0) return cudaSuccess;
+    const int cpt = (a.d_v + kThreads - 1) / kThreads;
+    switch (cpt <= 1 ? 1 : cpt <= 2 ? 2 : 4) {
+    case 1: return launch_cc<1>(P, rows, s);
+    case 2: return launch_cc<2>(P, rows, s);
+    default: return launch_cc<4>(P, rows, s);
+    }
+}
+
+} // namespace csa2

@@ -1,0 +1,108 @@
+// quant.cu -- MXFP4 cache codec kernels (csa2_quant_fp4 / csa2_dequant_fp4).
+//
+// DeepSeek-V4.1-Flash report (aipaper.jasonlin.tech) §2.4.4: indexer queries and keys use
+// OCP MXFP4 -- E2M1 values with one power-of-two (E8M0) scale per 32 -- and cached values
+// are dequantised before attention.  One warp quantises one 32-value block per step:
+// lane i holds element i, the block maximum is a warp max over the magnitude bits, and
+// lane pairs merge their nibbles (element 2i in the low nibble).
+#include "common.cuh"
+#include "internal.h"
+#include <cuda_bf16.h>
+
+namespace csa2 {
+namespace {
+
+template <bool BF16>
+__global__ void __launch_bounds__(256) quant_mxfp4_kernel(const void *__restrict__ x, int64_t rows,
+                                                          int64_t cols, int64_t ldx,
+                                                          uint8_t *__restrict__ codes, int64_t ldc,
+                                                          uint8_t *__restrict__ scales, int64_t lds,
+                                                          uint32_t *d_status)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t nblk_row = cols / 32;
+    const int64_t total = rows * nblk_row;
+    const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t blk = warp0; blk < total; blk += nwarps) {
+        const int64_t r = blk / nblk_row, kb = blk % nblk_row;
+        const int64_t col = kb * 32 + lane;
+        float v;
+        if (BF16) {
+            uint16_t bits = static_cast<const uint16_t *>(x)[r * ldx + col];
+            v = __uint_as_float((uint32_t)bits << 16);
+        } else {
+            v = static_cast<const float *>(x)[r * ldx + col];
+        }
+        const uint32_t mag_bits = __float_as_uint(v) & 0x7fffffffu;
+        const uint32_t amax_bits = __reduce_max_sync(0xffffffffu, mag_bits);
+        if (amax_bits >= 0x7f800000u && lane == 0) dev_flag(d_status, CSA2_DEV_NONFINITE);
+        const int X = mx_block_exponent(__uint_as_float(amax_bits >= 0x7f800000u ? 0u : amax_bits));
+        const uint32_t c = e2m1_encode(v, pow2_neg(X));
+        const uint32_t c_hi = __shfl_down_sync(0xffffffffu, c, 1);
+        if ((lane & 1) == 0) codes[r * ldc + kb * 16 + (lane >> 1)] = (uint8_t)(c | (c_hi << 4));
+        if (lane == 0) scales[r * lds + kb] = (uint8_t)(X + 127);
+    }
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(256) dequant_mxfp4_kernel(const uint8_t *__restrict__ codes,
+                                                            int64_t ldc,
+                                                            const uint8_t *__restrict__ scales,
+                                                            int64_t lds, int64_t rows, int64_t cols,
+                                                            void *__restrict__ y, int64_t ldy)
+{
+    const int64_t total = rows * cols;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = i / cols, c = i % cols;
+        const uint32_t byte = codes[r * ldc + c / 2];
+        const uint32_t code = (c & 1) ? (byte >> 4) : (byte & 15u);
+        float v = e2m1_mag(code & 7u) * e8m0_value(scales[r * lds + c / 32]);
+        if (code & 8u) v = -v;
+        if (BF16)
+            static_cast<uint16_t *>(y)[r * ldy + c] = (uint16_t)(__float_as_uint(v) >> 16);
+        else
+            static_cast<float *>(y)[r * ldy + c] = v;
+    }
+}
+
+int grid_for(int64_t work_items, int per_block)
+{
+    int64_t g = (work_items + per_block - 1) / per_block;
+    if (g < 1) g = 1;
+    if (g > 152 * 16) g = 152 * 16;
+    return (int)g;
+}
+
+} // namespace
+
+cudaError_t launch_quant_mxfp4(const void *x, bool x_bf16, int64_t rows, int64_t cols, int64_t ldx,
+                               uint8_t *codes, int64_t ldc, uint8_t *scales, int64_t lds,
+                               uint32_t *d_status, cudaStream_t s)
+{
+    if (rows == 0 || cols == 0) return cudaSuccess;
+    const int grid = grid_for(rows * (cols / 32), 8);
+    if (x_bf16)
+        quant_mxfp4_kernel<true><<<grid, 256, 0, s>>>(x, rows, cols, ldx, codes, ldc, scales, lds,
+                                                      d_status);
+    else
+        quant_mxfp4_kernel<false><<<grid, 256, 0, s>>>(x, rows, cols, ldx, codes, ldc, scales, lds,
+                                                       d_status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dequant_mxfp4(const uint8_t *codes, int64_t ldc, const uint8_t *scales,
+                                 int64_t lds, int64_t rows, int64_t cols, void *y, bool y_bf16,
+                                 int64_t ldy, cudaStream_t s)
+{
+    if (rows == 0 || cols == 0) return cudaSuccess;
+    const int grid = grid_for(rows * cols, 256);
+    if (y_bf16)
+        dequant_mxfp4_kernel<true><<<grid, 256, 0, s>>>(codes, ldc, scales, lds, rows, cols, y, ldy);
+    else
+        dequant_mxfp4_kernel<false><<<grid, 256, 0, s>>>(codes, ldc, scales, lds, rows, cols, y, ldy);
+    return cudaGetLastError();
+}
+
+} // namespace csa2

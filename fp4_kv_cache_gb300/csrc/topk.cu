@@ -1,0 +1,202 @@
+// topk.cu -- Top-K selection (csa2_topk) and the block pool (csa2_block_candidates).
+//
+// DeepSeek-V4.1-Flash report (aipaper.jasonlin.tech) §2.3: the indexer keeps the Top-K
+// entries per query (K = 512, §4.2.1); §2.3.2 and Figure 5: the decoder's first Full
+// layer gives each block of 8 positions the maximum index score among its positions and
+// keeps the best blocks (at most 2,048).  Ties go to the lower index; output ascending.
+//
+// Selection is an exact radix select on an order-preserving 32-bit key of each score:
+// four 8-bit digit passes (most significant first) find the K-th key tau and how many
+// entries equal to tau must be taken; a final pass in index order emits every entry
+// above tau and the first `need` entries equal to tau, which yields ascending output.
+#include "common.cuh"
+#include "internal.h"
+
+namespace csa2 {
+namespace {
+
+constexpr int kTopkThreads = 1024;
+
+__device__ __forceinline__ int64_t cand_pos(const int32_t *pool_row, int32_t block, int64_t i)
+{
+    if (!pool_row) return i;
+    return (int64_t)pool_row[i / block] * block + i % block;
+}
+
+// Block-wide exclusive prefix count of a 1-bit flag (all threads must call).
+__device__ __forceinline__ uint32_t block_excl_count(bool f, uint32_t *s_warp, uint32_t &total)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t bal = __ballot_sync(0xffffffffu, f);
+    const uint32_t in_warp = __popc(bal & ((1u << lane) - 1u));
+    if (lane == 0) s_warp[warp] = __popc(bal);
+    __syncthreads();
+    if (warp == 0) {
+        uint32_t v = lane < (int)(blockDim.x >> 5) ? s_warp[lane] : 0u;
+        uint32_t incl = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += t;
+        }
+        s_warp[lane] = incl - v;             // exclusive
+        if (lane == 31) s_warp[32] = incl;   // total
+    }
+    __syncthreads();
+    const uint32_t r = s_warp[warp] + in_warp;
+    total = s_warp[32];
+    __syncthreads();
+    return r;
+}
+
+__global__ void __launch_bounds__(kTopkThreads)
+topk_radix_kernel(const float *__restrict__ scores, int64_t n, const int32_t *__restrict__ row_len,
+                  const int32_t *__restrict__ pool, int32_t block, int32_t k,
+                  int32_t *__restrict__ idx, float *__restrict__ out_scores)
+{
+    __shared__ uint32_t s_hist[256];
+    __shared__ uint32_t s_warp[33];
+    __shared__ uint32_t s_prefix, s_mask, s_remaining;
+
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int64_t row = blockIdx.x;
+    int64_t len = row_len ? (int64_t)row_len[row] : n;
+    len = len < 0 ? 0 : (len > n ? n : len);
+    const float *s = scores + row * n;
+    const int32_t *pool_row = pool ? pool + row * (n / block) : nullptr;
+    int32_t *out = idx + row * (int64_t)k;
+    float *out_s = out_scores ? out_scores + row * (int64_t)k : nullptr;
+
+    if (len <= k) {                          // everything competes and wins
+        for (int64_t i = tid; i < k; i += kTopkThreads) {
+            out[i] = i < len ? (int32_t)cand_pos(pool_row, block, i) : -1;
+            if (out_s) out_s[i] = i < len ? s[i] : 0.0f;
+        }
+        return;
+    }
+
+    if (tid == 0) { s_prefix = 0; s_mask = 0; s_remaining = (uint32_t)k; }
+    for (int pass = 0; pass < 4; ++pass) {
+        const int shift = 24 - 8 * pass;
+        for (int i = tid; i < 256; i += kTopkThreads) s_hist[i] = 0;
+        __syncthreads();
+        const uint32_t prefix = s_prefix, mask = s_mask;
+        for (int64_t base = 0; base < len; base += kTopkThreads) {
+            const int64_t i = base + tid;
+            uint32_t key = 0;
+            bool act = false;
+            if (i < len) {
+                key = score_key(s[i]);
+                act = (key & mask) == prefix;
+            }
+            const uint32_t am = __ballot_sync(0xffffffffu, act);
+            if (act) {
+                const uint32_t digit = (key >> shift) & 255u;
+                const uint32_t peers = __match_any_sync(am, digit);
+                if (lane == __ffs(peers) - 1) atomicAdd(&s_hist[digit], (uint32_t)__popc(peers));
+            }
+        }
+        __syncthreads();
+        if (tid == 0) {
+            uint32_t cum = 0, rem = s_remaining;
+            for (int d = 255; d >= 0; --d) {
+                const uint32_t h = s_hist[d];
+                if (cum + h >= rem) {
+                    s_prefix = prefix | ((uint32_t)d << shift);
+                    s_mask = mask | (255u << shift);
+                    s_remaining = rem - cum;
+                    break;
+                }
+                cum += h;
+            }
+        }
+        __syncthreads();
+    }
+    const uint32_t tau = s_prefix;
+    const uint32_t need = s_remaining;       // entries equal to tau still to take
+
+    uint32_t base_eq = 0, base_sel = 0;
+    for (int64_t base = 0; base < len && base_sel < (uint32_t)k; base += kTopkThreads) {
+        const int64_t i = base + tid;
+        uint32_t key = 0;
+        float v = 0.0f;
+        if (i < len) { v = s[i]; key = score_key(v); }
+        const bool gt = i < len && key > tau;
+        const bool eq = i < len && key == tau;
+        uint32_t tot_eq, tot_sel;
+        const uint32_t eq_rank = base_eq + block_excl_count(eq, s_warp, tot_eq);
+        const bool sel = gt || (eq && eq_rank < need);
+        const uint32_t sel_rank = base_sel + block_excl_count(sel, s_warp, tot_sel);
+        if (sel && sel_rank < (uint32_t)k) {
+            out[sel_rank] = (int32_t)cand_pos(pool_row, block, i);
+            if (out_s) out_s[sel_rank] = v;
+        }
+        base_eq += tot_eq;
+        base_sel += tot_sel;
+    }
+}
+
+// Block score = max over the block's valid positions (NaN ignored; all-NaN -> NaN).
+__global__ void block_max_kernel(const float *__restrict__ scores, int64_t n,
+                                 const int32_t *__restrict__ row_len, int32_t block, int64_t nbmax,
+                                 float *__restrict__ bscores, int32_t *__restrict__ brow_len)
+{
+    const int64_t row = blockIdx.y;
+    int64_t len = row_len ? (int64_t)row_len[row] : n;
+    len = len < 0 ? 0 : (len > n ? n : len);
+    const int64_t nblk = (len + block - 1) / block;
+    if (blockIdx.x == 0 && threadIdx.x == 0) brow_len[row] = (int32_t)nblk;
+    const float *s = scores + row * n;
+    for (int64_t bi = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; bi < nblk;
+         bi += (int64_t)gridDim.x * blockDim.x) {
+        float m = __uint_as_float(0x7fc00000u);
+        const int64_t p0 = bi * block;
+        for (int j = 0; j < block && p0 + j < len; ++j) m = fmaxf(m, s[p0 + j]);
+        bscores[row * nbmax + bi] = m;
+    }
+}
+
+} // namespace
+
+size_t topk_ws_bytes(int64_t, int64_t, int32_t) { return 0; }
+
+cudaError_t launch_topk(const float *scores, int64_t rows, int64_t n, const int32_t *row_len,
+                        const int32_t *pool, int32_t block, int32_t k, int32_t *idx,
+                        float *out_scores, void *, uint32_t *, cudaStream_t s)
+{
+    if (rows == 0 || k == 0) return cudaSuccess;
+    topk_radix_kernel<<<(unsigned)rows, kTopkThreads, 0, s>>>(scores, n, row_len, pool, block, k,
+                                                             idx, out_scores);
+    return cudaGetLastError();
+}
+
+size_t block_candidates_ws_bytes(int64_t rows, int64_t n, int32_t block, int32_t)
+{
+    const int64_t nbmax = (n + block - 1) / block;
+    size_t a = (size_t)rows * (size_t)nbmax * sizeof(float);
+    a = (a + 255) & ~(size_t)255;
+    return a + (size_t)rows * sizeof(int32_t);
+}
+
+cudaError_t launch_block_candidates(const float *scores, int64_t rows, int64_t n,
+                                    const int32_t *row_len, int32_t block, int32_t nb,
+                                    int32_t *block_ids, void *ws, uint32_t *d_status,
+                                    cudaStream_t s)
+{
+    if (rows == 0 || nb == 0) return cudaSuccess;
+    const int64_t nbmax = (n + block - 1) / block;
+    float *bscores = static_cast<float *>(ws);
+    size_t off = ((size_t)rows * (size_t)nbmax * sizeof(float) + 255) & ~(size_t)255;
+    int32_t *brow_len = reinterpret_cast<int32_t *>(static_cast<char *>(ws) + off);
+    int64_t gx = (nbmax + 255) / 256;
+    if (gx > 64) gx = 64;
+    if (gx < 1) gx = 1;
+    block_max_kernel<<<dim3((unsigned)gx, (unsigned)rows), 256, 0, s>>>(scores, n, row_len, block,
+                                                                        nbmax, bscores, brow_len);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_topk(bscores, rows, nbmax, brow_len, nullptr, 1, nb, block_ids, nullptr, nullptr,
+                       d_status, s);
+}
+
+} // namespace csa2

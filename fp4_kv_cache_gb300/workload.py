@@ -1,0 +1,72 @@
+"""Device-resident inputs of a CSA2 workload, built from the seeded generator.
+
+Float inputs are drawn on the host (``synth``), copied to the device one sequence at a
+time and quantised there by csa2_quant_fp4, so a 1M-position cache never needs a
+full float copy on the host.  Used by the benchmark and the GPU tests.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+from typing import Dict, Optional
+
+import numpy as np
+import torch
+
+from . import csa2, synth
+
+
+def bf16_tensor(bits: np.ndarray, device) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device).view(torch.bfloat16)
+
+
+@dataclass
+class DeviceWorkload:
+    w: synth.Workload
+    rows: list
+    t: Dict[str, torch.Tensor] = field(default_factory=dict)
+    sm_scale: float = 0.0
+
+    def __getitem__(self, k):
+        return self.t[k]
+
+
+def build(w: synth.Workload, rows=None, device="cuda:0", kv: bool = True, kidx: bool = True,
+          d_status: Optional[torch.Tensor] = None) -> DeviceWorkload:
+    rows = list(range(w.batch)) if rows is None else list(rows)
+    B = len(rows)
+    dev = torch.device(device)
+    out = DeviceWorkload(w, rows)
+    qi, ww, qa = synth.gen_queries(w, rows)
+    out.t["q_idx"] = bf16_tensor(qi, dev)
+    out.t["w_idx"] = torch.from_numpy(ww).to(dev)
+    out.t["q_attn"] = bf16_tensor(qa, dev)
+    out.t["q_pos"] = torch.from_numpy(synth.q_positions(w)[: B]).to(dev)
+    n_slots, pos0 = synth.swa_layout(w)
+    out.t["swa_pos0"] = torch.full((B,), pos0, dtype=torch.int32, device=dev)
+    N = w.n_keys
+    if kidx:
+        kc = torch.empty((B, N, w.idx_dim // 2), dtype=torch.uint8, device=dev)
+        ks = torch.empty((B, N, w.idx_dim // 32), dtype=torch.uint8, device=dev)
+        for i, b in enumerate(rows):
+            x = bf16_tensor(synth.gen_index_keys(w, b, qi[i], ww[i]), dev)
+            csa2.csa2_quant_fp4(x, kc[i], ks[i], d_status)
+            del x
+        out.t["k_codes"], out.t["k_scales"] = kc, ks
+    if kv:
+        vc = torch.empty((B, N, w.d_qk // 2), dtype=torch.uint8, device=dev)
+        vs = torch.empty((B, N, w.d_qk // 32), dtype=torch.uint8, device=dev)
+        swa = torch.empty((B, n_slots, w.d_qk), dtype=torch.bfloat16, device=dev)
+        for i, b in enumerate(rows):
+            x = bf16_tensor(synth.gen_main_kv(w, b), dev)
+            csa2.csa2_quant_fp4(x, vc[i], vs[i], d_status)
+            del x
+            swa[i] = bf16_tensor(synth.gen_swa(w, b), dev)
+        out.t["kv_codes"], out.t["kv_scales"], out.t["swa"] = vc, vs, swa
+    if w.pool_blocks:
+        out.t["pool"] = torch.from_numpy(np.stack([synth.gen_pool_blocks(w, b) for b in rows])).to(dev)
+    if w.reuse_idx:
+        out.t["reuse_idx"] = torch.from_numpy(np.stack([synth.gen_reuse_idx(w, b) for b in rows])).to(dev)
+    out.sm_scale = 1.0 / math.sqrt(w.d_qk)
+    torch.cuda.synchronize(dev)
+    return out

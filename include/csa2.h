@@ -1,0 +1,219 @@
+/*
+ * csa2.h -- C ABI of libcsa2.so, the GB300 (sm_103a) CSA2 decode/prefill hot path.
+ *
+ * CSA2 = Compressed Sparse Attention 2 of "DeepSeek-V4.1-Flash: Pushing the Limits of
+ * KV Cache Compression".  Citations name the page and its section:
+ *   [report]  aipaper.jasonlin.tech  (the report's own text, its § numbers)
+ *   [review]  papers.chlience.com    (analytical review; byte ledger, layer schedule)
+ *
+ * The path (report §2.3, §2.3.1, §2.3.2; review, "CSA2" section and Figure 4 reading):
+ *   indexer Q + FP4 indexer K  -> scores -> Top-512 (+ block pool in the decoder's
+ *   first Full layer) -> gather + dequantise the selected FP4 main-KV entries ->
+ *   join with the layer's SWA window -> core latent attention over all query heads.
+ * Modes (report §2.3.1): Full = score all visible entries; Reindex = score only the
+ * block pool with the layer's own indexer query; Reuse = attention over given indices.
+ *
+ * Conventions for every entry point
+ *   - Pointers are DEVICE pointers owned by the caller unless a comment says "host".
+ *     The library never allocates device memory and never frees caller memory.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default stream)
+ *     and is asynchronous: no call synchronises and none copies between host and device.
+ *   - Scratch memory is a caller buffer `ws` of at least *_workspace_size() bytes
+ *     (16-byte aligned); ws may be NULL when that size is 0.
+ *   - Return value: CSA2_OK, or an error found on the host BEFORE anything is launched
+ *     (bad shapes, NULL pointers, misalignment, too-small workspace, launch failure).
+ *   - Errors found on the device are ORed as CSA2_DEV_* bits into *d_status (a caller
+ *     uint32_t in device memory; may be NULL to ignore them).  Read it after the stream
+ *     synchronises.  The affected outputs are then unspecified but every access stays
+ *     in bounds.
+ *   - bf16 tensors are passed as uint16_t bit patterns.  Layouts are dense row-major
+ *     (C order) with the shapes given; "B" = batch, "T" = query tokens per sequence.
+ *   - Calls on different streams with disjoint outputs may run concurrently; the
+ *     library keeps no mutable global state.
+ */
+#ifndef CSA2_H
+#define CSA2_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define CSA2_API __attribute__((visibility("default")))
+#else
+#define CSA2_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef void *csa2_stream; /* a cudaStream_t */
+
+typedef enum {
+    CSA2_OK = 0,
+    CSA2_ERR_INVALID_ARG = 1, /* shape, pointer, alignment or enum out of range */
+    CSA2_ERR_UNSUPPORTED = 2, /* valid request this build does not implement     */
+    CSA2_ERR_CUDA = 3,        /* a CUDA launch or attribute call failed          */
+    CSA2_ERR_WORKSPACE = 4    /* ws_bytes below the *_workspace_size() value     */
+} csa2_status;
+
+/* Device-side status bits (ORed into *d_status). */
+#define CSA2_DEV_BAD_INDEX 0x1u  /* an attention index outside [-1, n_kv) was ignored      */
+#define CSA2_DEV_BAD_POOL 0x2u   /* pool block ids not ascending-unique, -1 padded, in range */
+#define CSA2_DEV_NONFINITE 0x4u  /* a quantiser block held Inf/NaN (its output unspecified) */
+#define CSA2_DEV_TIMEOUT 0x8u    /* a bounded device wait gave up; outputs unspecified      */
+
+typedef enum { CSA2_BF16 = 0, CSA2_F32 = 1 } csa2_dtype;
+
+/* 4-bit cache formats.
+ * MXFP4: E2M1 codes + one E8M0 (power-of-two) scale per 32 values -- the OCP MX format
+ *   the report gives for indexer queries and keys (report §2.4.4), used here for both
+ *   caches.  Codes are packed two per byte, element 2i in the low nibble; scale byte
+ *   e means 2^(e-127).  Quantisation: X = floor(log2(max|x|)) - 2 clamped to
+ *   [-127, 127] (X = 0 for an all-zero block), element code = round-half-even of
+ *   |x|/2^X onto {0, .5, 1, 1.5, 2, 3, 4, 6}, saturating at 6, sign bit = sign bit of x.
+ * NVFP4_E4M3_16: E2M1 + one E4M3 scale per 16, no global scale -- the report's main-KV
+ *   format (report §2.4.4).  Only its byte ledger is implemented in this build. */
+typedef enum { CSA2_FMT_MXFP4 = 0, CSA2_FMT_NVFP4_E4M3_16 = 1 } csa2_fp4_format;
+
+typedef enum {
+    CSA2_INDEX_FULL = 0, /* every causally visible entry is a candidate (Full mode)     */
+    CSA2_INDEX_POOL = 1  /* only the positions of the given block pool (Reindex mode)    */
+} csa2_index_mode;
+
+CSA2_API const char *csa2_status_string(csa2_status s);
+CSA2_API int csa2_version(void); /* major*10000 + minor*100 + patch */
+
+/* Bytes one global position takes in the cache of one source layer: main-KV latent of
+ * d_main channels in `main_fmt` plus an MXFP4 indexer key of d_idx channels.
+ * Review page, "四位缓存：890 字节究竟由什么组成": 512-channel E2M1 + E4M3/16 main KV and
+ * a 128-channel MXFP4 indexer key give 256 + 32 + 64 + 4 = 356 bytes.  Returns 0 for an
+ * invalid request (d not a multiple of the format's block). */
+CSA2_API size_t csa2_cache_bytes_per_position(csa2_fp4_format main_fmt, int32_t d_main, int32_t d_idx);
+
+/* ---------------------------------------------------------------------------------- */
+/* csa2_quant_fp4 / csa2_dequant_fp4 -- the 4-bit cache codec (report §2.4.4).         */
+/* x: rows x cols values of type xt (BF16 or F32), row stride ldx elements.  cols % 32  */
+/* == 0.  codes: rows x cols/2 bytes, row stride ldc bytes; scales: rows x cols/32      */
+/* bytes, row stride lds bytes.  fmt must be CSA2_FMT_MXFP4.  Non-finite input sets     */
+/* CSA2_DEV_NONFINITE.  dequant writes y (BF16 or F32, row stride ldy); every MXFP4     */
+/* value with scale byte <= 252 is exact in both types.                                 */
+/* ---------------------------------------------------------------------------------- */
+CSA2_API csa2_status csa2_quant_fp4(const void *x, csa2_dtype xt, int64_t rows, int64_t cols, int64_t ldx,
+                           uint8_t *codes, int64_t ldc, uint8_t *scales, int64_t lds,
+                           csa2_fp4_format fmt, uint32_t *d_status, csa2_stream stream);
+CSA2_API csa2_status csa2_dequant_fp4(const uint8_t *codes, int64_t ldc, const uint8_t *scales,
+                             int64_t lds, int64_t rows, int64_t cols, csa2_fp4_format fmt,
+                             void *y, csa2_dtype yt, int64_t ldy, csa2_stream stream);
+
+/* ---------------------------------------------------------------------------------- */
+/* csa2_index_score -- indexer scores (report §2.3: the indexer scores main-KV entries  */
+/* with indexer Q and indexer K; §2.3.2: Reindex layers score only the pool).           */
+/*                                                                                    */
+/* Score of a candidate position t for a query with heads h = 0..H-1:                 */
+/*   q_hat = MXFP4(q_h) (quantised inside the call, 32-value blocks, same rule as       */
+/*   csa2_quant_fp4), D_h = float32 round-to-nearest-even of the exact dot             */
+/*   q_hat_h . k_hat_t, and s = float32 fma chain s <- fma(w_h, max(D_h, 0), s) over     */
+/*   h = 0..H-1 from s = +0.  (The pages give no formula; the head-weighted ReLU sum is */
+/*   the workload's definition, and this precision is the one the kernels use.)        */
+/* Visibility: entry j covers tokens [j*m, j*m+m-1] (no overlap, report §2.3) and a     */
+/* query at token position p sees entries with (j+1)*m - 1 <= p:                       */
+/*   n_vis = min(n_keys, (p + 1) / m).                                                  */
+/* ---------------------------------------------------------------------------------- */
+typedef struct {
+    int32_t batch, n_q;        /* B, T                                                    */
+    int32_t n_heads, head_dim; /* H_i (1..64), d_i (32, 64 or 128)                         */
+    int32_t ratio_m;           /* compression ratio m >= 1                                 */
+    int64_t n_keys;            /* N entries per sequence (< 2^31)                          */
+    const uint16_t *q;         /* bf16 [B, T, H_i, d_i]                                    */
+    const float *w;            /* [B, T, H_i] head weights (finite)                        */
+    const uint8_t *k_codes;    /* [B, N, d_i/2]   MXFP4 indexer-K codes                    */
+    const uint8_t *k_scales;   /* [B, N, d_i/32]  MXFP4 indexer-K scales                   */
+    const int32_t *q_pos;      /* [B, T] absolute token positions; NULL: all N visible     */
+    csa2_index_mode mode;
+    const int32_t *pool_blocks; /* POOL: [B, T, n_pool_blocks] block ids, ascending and     */
+    int32_t n_pool_blocks;      /* unique, padded with -1 at the end; block b covers        */
+    int32_t block;              /* positions [b*block, b*block+block-1].  block: 1..32.     */
+} csa2_index_args;
+
+/* Outputs: scores [B, T, n_cand] float32, n_cand = N (FULL) or n_pool_blocks*block (POOL);
+ * candidate i is position i (FULL) or pool_blocks[i/block]*block + i%block (POOL).
+ * row_len [B, T] int32: the candidates 0..row_len-1 of each row are the valid ones
+ * (FULL: n_vis; POOL: the pool positions that exist and are visible -- a prefix because
+ * the pool is ascending).  Entries at or beyond row_len are left unwritten. */
+CSA2_API size_t csa2_index_score_workspace_size(const csa2_index_args *a);
+CSA2_API csa2_status csa2_index_score(const csa2_index_args *a, float *scores, int32_t *row_len,
+                             void *ws, size_t ws_bytes, uint32_t *d_status, csa2_stream stream);
+
+/* ---------------------------------------------------------------------------------- */
+/* csa2_topk -- Top-K selection (report §2.3: Top-K entries per query; §4.2.1: K=512).  */
+/* For each of `rows` rows of n candidates: the k candidates with the largest scores,   */
+/* ties broken by the lower candidate index; float order (-0 == +0), NaN below every    */
+/* number.  Only candidates 0..row_len[r]-1 compete (row_len NULL: all n).             */
+/* idx [rows, k] int32: the selected POSITIONS in ascending order, padded with -1 when  */
+/* fewer than k compete.  Position of candidate i: i, or with pool_blocks != NULL        */
+/* ([rows, n/block]) pool_blocks[i/block]*block + i%block -- ascending candidates map to */
+/* ascending positions, so the tie rule is the lower position.                         */
+/* out_scores (nullable) [rows, k]: the score of each selected entry (0 for padding).   */
+/* ---------------------------------------------------------------------------------- */
+CSA2_API size_t csa2_topk_workspace_size(int64_t rows, int64_t n, int32_t k);
+CSA2_API csa2_status csa2_topk(const float *scores, int64_t rows, int64_t n, const int32_t *row_len,
+                      const int32_t *pool_blocks, int32_t block, int32_t k, int32_t *idx,
+                      float *out_scores, void *ws, size_t ws_bytes, uint32_t *d_status,
+                      csa2_stream stream);
+
+/* ---------------------------------------------------------------------------------- */
+/* csa2_block_candidates -- the hierarchical sparse indexer's block pool (report §2.3.2 */
+/* and Figure 5; review: block selection uses the global position scores directly).     */
+/* For each row of FULL-mode scores (candidate i = position i, valid i < row_len): block */
+/* b covers positions [b*block, b*block+block-1]; its score is the max of its valid     */
+/* positions' scores (NaN ignored; all-NaN -> NaN).  block_ids [rows, nb]: the nb best  */
+/* blocks by (score desc, block id asc), ascending, -1 padded (at most 2,048 blocks of  */
+/* 8 = 16,384 positions in the report's configuration, §4.2.1).                         */
+/* ---------------------------------------------------------------------------------- */
+CSA2_API size_t csa2_block_candidates_workspace_size(int64_t rows, int64_t n, int32_t block, int32_t nb);
+CSA2_API csa2_status csa2_block_candidates(const float *scores, int64_t rows, int64_t n,
+                                  const int32_t *row_len, int32_t block, int32_t nb,
+                                  int32_t *block_ids, void *ws, size_t ws_bytes,
+                                  uint32_t *d_status, csa2_stream stream);
+
+/* ---------------------------------------------------------------------------------- */
+/* csa2_sparse_attn -- core attention (report §2.3 and §2.3.1: every mode attends the   */
+/* selected main-KV entries together with the layer's SWA KV; review: the main KV is a  */
+/* latent shared by all query heads; report §3.2.2: SWA keys of a query at token i are   */
+/* [max(s, i-W+1), i] for a replay starting at s).                                      */
+/* Key set of query (b, t): the main-KV rows idx[b,t,j] for j < topk with idx >= 0      */
+/* (dequantised exactly; duplicates kept; idx >= n_kv or < -1 sets CSA2_DEV_BAD_INDEX   */
+/* and is ignored), then the SWA slots j whose token swa_pos0[b] + j lies in            */
+/* [max(s, p-W+1, 0), p], p = q_pos[b,t], s = swa_start ? swa_start[b] : 0.            */
+/* Per head h: l_j = sm_scale * q_h . k_j over d_qk dims; o_h = sum_j softmax(l)_j *     */
+/* k_j[0:d_v] (V = the latent's leading d_v dims); lse_h = log sum_j exp(l_j) (natural  */
+/* log).  A query with no keys gets o = 0 and lse = -inf.  fp32 accumulation.           */
+/* ---------------------------------------------------------------------------------- */
+typedef struct {
+    int32_t batch, n_q;      /* B, T                                                      */
+    int32_t n_heads;         /* H (1..128)                                                */
+    int32_t d_qk, d_v;       /* d_qk % 32 == 0, d_qk <= 1024; d_v <= d_qk, d_v % 8 == 0     */
+    int32_t topk;            /* entries per idx row (0..2048)                             */
+    int32_t window;          /* SWA window W (>= 0)                                       */
+    float sm_scale;          /* logit scale, e.g. 1/sqrt(d_qk)                            */
+    int64_t n_kv;            /* main-KV entries per sequence                              */
+    const uint16_t *q;       /* bf16 [B, T, H, d_qk]                                      */
+    const uint8_t *kv_codes; /* [B, n_kv, d_qk/2]  MXFP4 main-KV codes                    */
+    const uint8_t *kv_scales;/* [B, n_kv, d_qk/32] MXFP4 main-KV scales                   */
+    const int32_t *idx;      /* [B, T, topk]                                              */
+    const uint16_t *swa;     /* bf16 [B, n_swa, d_qk]; NULL = no SWA keys                 */
+    int32_t n_swa;           /* SWA slots per sequence                                    */
+    const int32_t *swa_pos0; /* [B] token position of slot 0 (required with swa)          */
+    const int32_t *swa_start;/* [B] replay start s, or NULL for s = 0                     */
+    const int32_t *q_pos;    /* [B, T] token position of each query (required with swa)   */
+} csa2_attn_args;
+
+CSA2_API size_t csa2_sparse_attn_workspace_size(const csa2_attn_args *a);
+CSA2_API csa2_status csa2_sparse_attn(const csa2_attn_args *a, uint16_t *out, float *lse, void *ws,
+                             size_t ws_bytes, uint32_t *d_status, csa2_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CSA2_H */

@@ -1,0 +1,130 @@
+"""The C-ABI library on the host: it builds, loads, exports every entry point the header
+declares, computes the cache byte ledger, and rejects bad arguments before launching
+anything (none of these calls reach the GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from fp4_kv_cache_gb300 import build as libbuild
+from fp4_kv_cache_gb300 import csa2
+from fp4_kv_cache_gb300.layers import layer_mode
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+GOLDEN = os.path.join(ROOT, "tests", "golden")
+
+
+def _declared_symbols():
+    src = open(os.path.join(ROOT, "include", "csa2.h")).read()
+    return sorted(set(re.findall(r"CSA2_API[^;(]*?\b(csa2_\w+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    libbuild.build()
+    return csa2.load(build_if_missing=False)
+
+
+def test_exports_every_declared_symbol(lib):
+    syms = _declared_symbols()
+    assert len(syms) == 13
+    for s in syms:
+        assert hasattr(lib, s), s
+    out = os.popen(f"nm -D --defined-only {libbuild.LIB}").read()
+    exported = set(re.findall(r" T (csa2_\w+)", out))
+    assert exported == set(syms)
+
+
+def _ledger():
+    vals = {}
+    for line in open(os.path.join(GOLDEN, "cache_ledger.txt")):
+        line = line.strip()
+        if line and not line.startswith("#"):
+            k, v = line.split()
+            vals[k] = int(v)
+    return vals
+
+
+def test_cache_byte_ledger(lib):
+    g = _ledger()
+    per_pos = csa2.cache_bytes_per_position(csa2.FMT_NVFP4_E4M3_16, 512, 128)
+    assert per_pos == g["per_position_total"] == (g["main_kv_codes_512ch"] + g["main_kv_scales_e4m3_per16"]
+                                                  + g["indexer_k_codes_128ch"]
+                                                  + g["indexer_k_scales_e8m0_per32"])
+    # three encoder source layers at ratio 2 + one decoder source layer at ratio 1
+    assert per_pos * 3 // 2 + per_pos == g["per_token_total"]
+    assert 448 * 6 == g["nvfp4_no_global_scale_max"]
+    assert 2048 * 8 == g["pool_max_positions"]
+    # this build's MXFP4 main KV at 512 + 64 dims: 288 + 18 bytes, plus the 68-byte key
+    assert csa2.cache_bytes_per_position(csa2.FMT_MXFP4, 576, 128) == 288 + 18 + 64 + 4
+    assert csa2.cache_bytes_per_position(csa2.FMT_MXFP4, 500, 128) == 0
+
+
+def test_status_strings(lib):
+    assert csa2.status_string(0) == "ok"
+    assert "invalid" in csa2.status_string(1)
+    assert lib.csa2_version() >= 100
+
+
+FAKE = ctypes.c_void_p(256)   # never dereferenced: every call below fails validation first
+
+
+def test_quant_rejects_bad_shapes(lib):
+    assert lib.csa2_quant_fp4(FAKE, 0, 4, 33, 33, FAKE, 17, FAKE, 2, 0, None, None) == 1
+    assert lib.csa2_quant_fp4(FAKE, 5, 4, 32, 32, FAKE, 16, FAKE, 1, 0, None, None) == 1
+    assert lib.csa2_quant_fp4(FAKE, 0, 4, 32, 16, FAKE, 16, FAKE, 1, 0, None, None) == 1
+    assert lib.csa2_quant_fp4(FAKE, 0, 4, 32, 32, FAKE, 16, FAKE, 1, 1, None, None) == 2
+    assert lib.csa2_quant_fp4(None, 0, 0, 32, 32, None, 16, None, 1, 0, None, None) == 0
+
+
+def test_index_rejects_bad_args(lib):
+    a = csa2.IndexArgs()
+    a.batch, a.n_q, a.n_heads, a.head_dim, a.ratio_m, a.n_keys = 1, 1, 4, 48, 1, 100
+    a.q = a.w = a.k_codes = a.k_scales = FAKE
+    a.mode, a.block = 0, 8
+    f = lib.csa2_index_score
+    assert f(ctypes.byref(a), FAKE, FAKE, None, 0, None, None) == 1        # head_dim 48
+    a.head_dim = 128
+    a.n_heads = 65
+    assert f(ctypes.byref(a), FAKE, FAKE, None, 0, None, None) == 1        # too many heads
+    a.n_heads = 4
+    a.ratio_m = 0
+    assert f(ctypes.byref(a), FAKE, FAKE, None, 0, None, None) == 1
+    a.ratio_m = 1
+    a.k_codes = ctypes.c_void_p(257)                                       # misaligned
+    assert f(ctypes.byref(a), FAKE, FAKE, None, 0, None, None) == 1
+    a.k_codes = FAKE
+    a.mode, a.n_pool_blocks, a.pool_blocks = 1, 16, None                   # pool missing
+    assert f(ctypes.byref(a), FAKE, FAKE, None, 0, None, None) == 1
+    a.batch = 0
+    assert f(ctypes.byref(a), None, None, None, 0, None, None) == 0        # empty: nothing to do
+
+
+def test_select_and_attn_reject_bad_args(lib):
+    assert lib.csa2_topk(FAKE, -1, 10, None, None, 8, 4, FAKE, None, None, 0, None, None) == 1
+    assert lib.csa2_topk(FAKE, 2, 10, None, FAKE, 8, 4, FAKE, None, None, 0, None, None) == 1
+    assert lib.csa2_topk(FAKE, 0, 10, None, None, 8, 4, FAKE, None, None, 0, None, None) == 0
+    need = lib.csa2_block_candidates_workspace_size(4, 1 << 20, 8, 2048)
+    assert need >= 4 * (1 << 17) * 4
+    assert lib.csa2_block_candidates(FAKE, 4, 1 << 20, None, 8, 2048, FAKE, FAKE, need - 1,
+                                     None, None) == 4
+    a = csa2.AttnArgs()
+    a.batch, a.n_q, a.n_heads, a.d_qk, a.d_v, a.topk, a.window = 1, 1, 64, 576, 600, 512, 128
+    a.q = a.idx = a.kv_codes = a.kv_scales = FAKE
+    a.n_kv = 10
+    assert lib.csa2_sparse_attn(ctypes.byref(a), FAKE, None, None, 0, None, None) == 1   # d_v > d_qk
+    a.d_v = 512
+    a.swa, a.n_swa, a.swa_pos0, a.q_pos = FAKE, 128, None, FAKE                          # no pos0
+    assert lib.csa2_sparse_attn(ctypes.byref(a), FAKE, None, None, 0, None, None) == 1
+
+
+def test_layer_schedule_counts():
+    # review page (papers.chlience.com), zero-based schedule table: 4 source layers, 8
+    # indexing layers, 30 Reuse layers, 38 layers with global attention
+    modes = [layer_mode(i) for i in range(40)]
+    assert modes[:2] == ["swa", "swa"]
+    assert [i for i, m in enumerate(modes) if m == "full"] == [2, 8, 14, 20]
+    assert [i for i, m in enumerate(modes) if m == "reindex"] == [24, 28, 32, 36]
+    assert modes.count("reuse") == 30
+    assert sum(m != "swa" for m in modes) == 38

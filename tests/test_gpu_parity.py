@@ -1,0 +1,296 @@
+"""GPU parity of every step of the CSA2 path against the CPU oracle (needs a GB300).
+
+The bar (workload definition): indices, block ids and FP4 codes bit-exact; indexer
+scores bit-exact too (both sides compute them in the same float32 precision); attention
+within 1e-2 relative error per (query, head) row:
+    max_c |o_gpu - o_ref| / max(max_c |o_ref|, 1e-6) <= 1e-2,
+a row-normwise reading of "max relative error" so that near-zero elements do not blow
+the ratio up; lse within 1e-3 absolute.  Every input comes from the seeded generator;
+the oracle quantises, scores, selects and attends with its own code.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp4_kv_cache_gb300 import csa2, synth, workload
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+ATTN_TOL = 1e-2
+LSE_TOL = 1e-3
+
+
+def f32(bits):
+    return synth.bf16_to_f32(bits)
+
+
+def status():
+    return torch.zeros(1, dtype=torch.int32, device=DEV)
+
+
+def same_f32(a, b):
+    """bitwise float32 equality, NaNs compared as NaN."""
+    a = np.asarray(a, np.float32)
+    b = np.asarray(b, np.float32)
+    nan = np.isnan(a) & np.isnan(b)
+    return np.array_equal(a.view(np.uint32)[~nan], b.view(np.uint32)[~nan]) and \
+        np.array_equal(np.isnan(a), np.isnan(b))
+
+
+# ------------------------------------------------------------------ codec
+def _codec_inputs(rows, cols, seed, as_bf16):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((rows, cols)).astype(np.float32)
+    x *= np.exp2(rng.integers(-140, 100, size=(rows, 1))).astype(np.float32)
+    x[0] = 0.0
+    x[1] = -0.0
+    x[2, ::3] = np.float32(1e-45)                       # fp32 subnormals
+    x[3] = np.float32(3.0e38) * np.sign(x[3])
+    ties = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 7.75], np.float32)
+    x[4, :] = 0.0
+    x[4, : cols] = np.resize(ties, cols)
+    if as_bf16:
+        bits = synth.f32_to_bf16_bits(x)
+        return bits, synth.bf16_to_f32(bits)
+    return x, x
+
+
+@pytest.mark.parametrize("cols,as_bf16", [(64, True), (576, True), (128, False), (32, False)])
+def test_quant_dequant_parity(cols, as_bf16):
+    raw, x = _codec_inputs(3001, cols, cols + as_bf16, as_bf16)
+    xt = workload.bf16_tensor(raw, DEV) if as_bf16 else torch.from_numpy(raw).to(DEV)
+    st = status()
+    codes, scales = csa2.quant_fp4(xt, st)
+    c_ref, s_ref = oracle.quant_mxfp4(x)
+    assert np.array_equal(codes.cpu().numpy(), c_ref)
+    assert np.array_equal(scales.cpu().numpy(), s_ref)
+    assert int(st.item()) == 0
+    # dequantisation: exact in float32, and in bf16 (scale bytes here are <= 252)
+    y_ref = oracle.dequant_mxfp4(c_ref, s_ref).astype(np.float32)
+    y32 = csa2.dequant_fp4(codes, scales, torch.float32).cpu().numpy()
+    assert np.array_equal(y32.view(np.uint32), y_ref.view(np.uint32))
+    y16 = csa2.dequant_fp4(codes, scales, torch.bfloat16).view(torch.int16).cpu().numpy()
+    assert np.all(y_ref.view(np.uint32) & 0xFFFF == 0)
+    assert np.array_equal(y16.view(np.uint16), (y_ref.view(np.uint32) >> 16).astype(np.uint16))
+    # FP4 round trip on the GPU: quantising the dequantised values gives the same codes
+    c2, s2 = csa2.quant_fp4(torch.from_numpy(y32).to(DEV))
+    nz = np.any((c_ref & 0x77) != 0, axis=1)
+    assert np.array_equal(c2.cpu().numpy()[nz], c_ref[nz])
+    assert np.array_equal(s2.cpu().numpy()[nz], s_ref[nz])
+
+
+def test_quant_flags_nonfinite():
+    x = torch.zeros((3, 64), dtype=torch.float32, device=DEV)
+    x[1, 40] = float("inf")
+    st = status()
+    codes, scales = csa2.quant_fp4(x, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & csa2.DEV_NONFINITE
+    assert torch.all(codes[0] == 0) and torch.all(codes[2] == 0)
+
+
+# ------------------------------------------------------------------ indexer scores
+W = synth.WORKLOADS
+SCORE_CASES = {
+    "tiny": W["tiny_full_decode"],
+    "ragged_planted": W["full_decode_64k"].scaled(batch=3, n_q=2, n_keys=5003, q_pos0=4000),
+    "ratio2": W["prefill_chunk_m2"].scaled(batch=2, n_q=3, n_keys=3001, q_pos0=5000, seed=9),
+    "d32_h1": W["tiny_full_decode"].scaled(batch=2, n_keys=777, q_pos0=776, idx_heads=1, idx_dim=32),
+    "ties": W["hier_indexer_1m"].scaled(batch=2, n_keys=20000, q_pos0=19999, palette=64),
+}
+
+
+def _oracle_row_scores(w, b, t, qi, ww, kc, ks, pos):
+    qc, qs = oracle.quant_mxfp4(f32(qi[t]))
+    return oracle.index_scores(qc, qs, ww[t], kc, ks, pos)
+
+
+@pytest.mark.parametrize("name", list(SCORE_CASES))
+def test_full_scores_topk_blocks(name):
+    w = SCORE_CASES[name]
+    st = status()
+    dw = workload.build(w, kv=False, device=DEV, d_status=st)
+    scores, row_len = csa2.index_score(dw["q_idx"], dw["w_idx"], dw["k_codes"], dw["k_scales"],
+                                       dw["q_pos"], w.ratio_m, None, w.block, st)
+    idx = csa2.topk(scores, w.topk, row_len, d_status=st)
+    nb = min(w.n_blocks, 300)
+    blocks = csa2.block_candidates(scores, nb, row_len, w.block, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    qi_all, ww_all, _ = synth.gen_queries(w)
+    qpos = synth.q_positions(w)
+    for b in range(w.batch):
+        kc, ks = oracle.quant_mxfp4(f32(synth.gen_index_keys(w, b, qi_all[b], ww_all[b])))
+        assert np.array_equal(dw["k_codes"][b].cpu().numpy(), kc)
+        for t in range(w.n_q):
+            nvis = oracle.n_visible(int(qpos[b, t]), w.ratio_m, w.n_keys)
+            assert int(row_len[b, t]) == nvis
+            pos = np.arange(nvis)
+            s_ref = _oracle_row_scores(w, b, t, qi_all[b], ww_all[b], kc, ks, pos)
+            s_gpu = scores[b, t, :nvis].cpu().numpy()
+            assert same_f32(s_gpu, s_ref), f"{name} b={b} t={t}"
+            assert np.array_equal(idx[b, t].cpu().numpy(), oracle.topk(s_ref, pos, w.topk))
+            assert np.array_equal(blocks[b, t].cpu().numpy(),
+                                  oracle.block_candidates(s_ref, nvis, w.block, nb))
+
+
+def test_scores_wide_exponents():
+    # random FP4 codes with scale bytes over the whole E8M0 range and queries spanning
+    # 2^-60 .. 2^60 per block: the kernels' wide-sum and overflow paths
+    rng = np.random.default_rng(17)
+    B, T, H, d, N = 2, 2, 8, 128, 3000
+    kc = rng.integers(0, 256, size=(B, N, d // 2), dtype=np.uint8)
+    ks = rng.integers(0, 255, size=(B, N, d // 32)).astype(np.uint8)
+    q = rng.standard_normal((B, T, H, d)).astype(np.float32)
+    q *= np.exp2(rng.integers(-60, 60, size=(B, T, H, d // 32, 1))).astype(np.float32).reshape(B, T, H, d // 32, 1).repeat(32, -1).reshape(B, T, H, d)
+    qbits = synth.f32_to_bf16_bits(q)
+    wv = rng.standard_normal((B, T, H)).astype(np.float32)
+    qt = workload.bf16_tensor(qbits, DEV)
+    scores, row_len = csa2.index_score(qt, torch.from_numpy(wv).to(DEV), torch.from_numpy(kc).to(DEV),
+                                       torch.from_numpy(ks).to(DEV))
+    torch.cuda.synchronize()
+    for b in range(B):
+        for t in range(T):
+            qc, qs = oracle.quant_mxfp4(f32(qbits[b, t]))
+            s_ref = oracle.index_scores(qc, qs, wv[b, t], kc[b], ks[b], np.arange(N))
+            assert same_f32(scores[b, t].cpu().numpy(), s_ref)
+
+
+def test_pool_scores_and_topk():
+    w = W["reuse_reindex_decode_128k"].scaled(batch=3, n_q=2, n_keys=40000, q_pos0=30000,
+                                              n_blocks=700)
+    st = status()
+    dw = workload.build(w, kv=False, device=DEV, d_status=st)
+    pool = dw["pool"].clone()
+    pool[1, 0, 650:] = -1                              # -1 padding
+    scores, row_len = csa2.index_score(dw["q_idx"], dw["w_idx"], dw["k_codes"], dw["k_scales"],
+                                       dw["q_pos"], 1, pool, w.block, st)
+    idx = csa2.topk(scores, w.topk, row_len, pool, w.block, d_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    qi_all, ww_all, _ = synth.gen_queries(w)
+    qpos = synth.q_positions(w)
+    pool_np = pool.cpu().numpy()
+    for b in range(w.batch):
+        kc, ks = oracle.quant_mxfp4(f32(synth.gen_index_keys(w, b, qi_all[b], ww_all[b])))
+        for t in range(w.n_q):
+            nvis = oracle.n_visible(int(qpos[b, t]), 1, w.n_keys)
+            pos = oracle.pool_positions(pool_np[b, t], w.block, nvis)
+            assert int(row_len[b, t]) == pos.size
+            s_ref = _oracle_row_scores(w, b, t, qi_all[b], ww_all[b], kc, ks, pos)
+            assert same_f32(scores[b, t, :pos.size].cpu().numpy(), s_ref)
+            idx_ref, _, _ = oracle.reindex_indexer(f32(qi_all[b, t]), ww_all[b, t], kc, ks,
+                                                   int(qpos[b, t]), 1, pool_np[b, t], w.topk, w.block)
+            assert np.array_equal(idx[b, t].cpu().numpy(), idx_ref)
+
+
+def test_pool_flags_bad_order():
+    w = W["reuse_reindex_decode_128k"].scaled(batch=1, n_keys=4096, q_pos0=4095, n_blocks=64)
+    dw = workload.build(w, kv=False, device=DEV)
+    pool = dw["pool"].clone()
+    pool[0, 0, 5], pool[0, 0, 6] = pool[0, 0, 6].item(), pool[0, 0, 5].item()
+    st = status()
+    csa2.index_score(dw["q_idx"], dw["w_idx"], dw["k_codes"], dw["k_scales"], dw["q_pos"], 1,
+                     pool, 8, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & csa2.DEV_BAD_POOL
+
+
+# ------------------------------------------------------------------ selection on given scores
+@pytest.mark.parametrize("rows,n,k,levels", [(3, 300000, 512, 7), (5, 1000, 512, 3), (2, 70000, 2048, 100000),
+                                             (4, 4097, 1, 2), (1, 1 << 20, 512, 1 << 20)])
+def test_topk_on_given_scores(rows, n, k, levels):
+    rng = np.random.default_rng(rows * n + k)
+    s = (rng.integers(0, levels, size=(rows, n)).astype(np.float32) - levels // 2) * np.float32(0.5)
+    s[0, ::97] = np.nan
+    s[0, 1::89] = -0.0
+    s[-1, ::5] = -np.inf
+    row_len = rng.integers(0, n + 1, size=rows).astype(np.int32)
+    row_len[0] = n
+    idx = csa2.topk(torch.from_numpy(s).to(DEV), k, torch.from_numpy(row_len).to(DEV))
+    bl = csa2.block_candidates(torch.from_numpy(s).to(DEV), min(k, 2048),
+                               torch.from_numpy(row_len).to(DEV), 8)
+    torch.cuda.synchronize()
+    for r in range(rows):
+        L = int(row_len[r])
+        assert np.array_equal(idx[r].cpu().numpy(), oracle.topk(s[r, :L], np.arange(L), k))
+        assert np.array_equal(bl[r].cpu().numpy(), oracle.block_candidates(s[r], L, 8, min(k, 2048)))
+
+
+# ------------------------------------------------------------------ attention
+def _attn_check(o_gpu, lse_gpu, o_ref, lse_ref):
+    o_gpu = o_gpu.astype(np.float64)
+    den = np.maximum(np.abs(o_ref).max(axis=-1), 1e-6)
+    err = np.abs(o_gpu - o_ref).max(axis=-1) / den
+    assert err.max() <= ATTN_TOL, f"max row-relative error {err.max():.3e}"
+    fin = np.isfinite(lse_ref)
+    assert np.array_equal(np.isfinite(lse_gpu), fin)
+    assert np.abs(lse_gpu[fin] - lse_ref[fin]).max(initial=0) <= LSE_TOL
+    return err.max()
+
+
+def _oracle_attention(w, dw_rows, idx_np, t_range, swa_start=None):
+    """fp64 oracle attention for rows (b, t) with the given idx."""
+    qpos = synth.q_positions(w)
+    n_slots, pos0 = synth.swa_layout(w)
+    _, _, qa = synth.gen_queries(w)
+    outs, lses = {}, {}
+    for b in dw_rows:
+        kvc, kvs = oracle.quant_mxfp4(f32(synth.gen_main_kv(w, b)))
+        swa = f32(synth.gen_swa(w, b)).astype(np.float64)
+        s0 = 0 if swa_start is None else int(swa_start[b])
+        for t in t_range:
+            keys = oracle.gather_keys(idx_np[b, t], kvc, kvs, swa, int(qpos[b, t]), pos0, w.window, s0)
+            o, l = oracle.attention_rows(f32(qa[b, t])[None].astype(np.float64), [keys],
+                                         1.0 / math.sqrt(w.d_qk), w.d_v)
+            outs[(b, t)], lses[(b, t)] = o[0], l[0]
+    return outs, lses
+
+
+ATTN_CASES = {
+    "tiny": (W["tiny_full_decode"], None),
+    "prod_dims_T3": (W["full_decode_64k"].scaled(batch=2, n_q=3, n_keys=3000, q_pos0=2000), None),
+    "replay_start": (W["full_decode_64k"].scaled(batch=2, n_q=2, n_keys=1500, q_pos0=1400, heads=20), [1350, 0]),
+    "d_v_odd_heads": (W["tiny_full_decode"].scaled(batch=1, n_q=2, heads=5, d_qk=96, d_v=40, n_keys=900, q_pos0=899, topk=100, window=17), None),
+}
+
+
+@pytest.mark.parametrize("name", list(ATTN_CASES))
+def test_attention_parity(name):
+    w, swa_start = ATTN_CASES[name]
+    st = status()
+    dw = workload.build(w, kidx=False, device=DEV, d_status=st)
+    rng = np.random.default_rng(3)
+    idx = np.stack([np.stack([np.sort(rng.choice(w.n_keys, w.topk, replace=False)) for _ in range(w.n_q)])
+                    for _ in range(w.batch)]).astype(np.int32)
+    idx[0, 0, -7:] = -1                                  # padding
+    idx[-1, -1, :3] = idx[-1, -1, 3]                     # duplicates are kept
+    ss = None if swa_start is None else torch.tensor(swa_start, dtype=torch.int32, device=DEV)
+    out, lse = csa2.sparse_attn(dw["q_attn"], dw["kv_codes"], dw["kv_scales"],
+                                torch.from_numpy(idx).to(DEV), dw["swa"], dw["swa_pos0"], dw["q_pos"],
+                                ss, w.window, dw.sm_scale, w.d_v, d_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    o_ref, l_ref = _oracle_attention(w, range(w.batch), idx, range(w.n_q), swa_start)
+    for (b, t), o in o_ref.items():
+        _attn_check(out[b, t].float().cpu().numpy(), lse[b, t].cpu().numpy(), o, l_ref[(b, t)])
+
+
+def test_attention_bad_index_and_empty():
+    w = W["tiny_full_decode"].scaled(batch=2, n_keys=600, q_pos0=599, topk=16)
+    dw = workload.build(w, kidx=False, device=DEV)
+    idx = np.full((2, 1, 16), -1, np.int32)
+    idx[0, 0, :4] = [5, 700, -3, 9]                       # 700 and -3 are out of range
+    st = status()
+    out, lse = csa2.sparse_attn(dw["q_attn"], dw["kv_codes"], dw["kv_scales"],
+                                torch.from_numpy(idx).to(DEV), None, None, None, None, w.window,
+                                dw.sm_scale, w.d_v, d_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & csa2.DEV_BAD_INDEX
+    # row 1 has no keys at all: zeros and -inf
+    assert torch.all(out[1] == 0) and torch.all(torch.isneginf(lse[1]))
+    o_ref, l_ref = _oracle_attention(w.scaled(window=0), [0], np.where(idx >= 600, -1, idx), [0])
+    _attn_check(out[0, 0].float().cpu().numpy(), lse[0, 0].cpu().numpy(), o_ref[(0, 0)], l_ref[(0, 0)])

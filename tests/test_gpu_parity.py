@@ -77,8 +77,10 @@ def test_quant_dequant_parity(cols, as_bf16):
     assert np.array_equal(y16.view(np.uint16), (y_ref.view(np.uint32) >> 16).astype(np.uint16))
     # FP4 round trip on the GPU: quantising the dequantised values gives the same codes
     c2, s2 = csa2.quant_fp4(torch.from_numpy(y32).to(DEV))
-    nz = np.any((c_ref & 0x77) != 0, axis=1)
-    assert np.array_equal(c2.cpu().numpy()[nz], c_ref[nz])
+    # (per 32-value block: a block whose scale clamped at 2^-127 may round to all zeros,
+    # and then takes the zero-block scale)
+    assert np.array_equal(c2.cpu().numpy(), c_ref)
+    nz = np.any((c_ref.reshape(c_ref.shape[0], -1, 16) & 0x77) != 0, axis=2)
     assert np.array_equal(s2.cpu().numpy()[nz], s_ref[nz])
 
 

@@ -125,7 +125,11 @@ csa2_status csa2_dequant_fp4(const uint8_t *codes, int64_t ldc, const uint8_t *s
                                           ldy, as_stream(stream)));
 }
 
-size_t csa2_index_score_workspace_size(const csa2_index_args *) { return 0; }
+size_t csa2_index_score_workspace_size(const csa2_index_args *a)
+{
+    if (!index_args_ok(a)) return 0;
+    return index_score_ws_bytes(*a);
+}
 
 csa2_status csa2_index_score(const csa2_index_args *a, float *scores, int32_t *row_len, void *ws,
                              size_t ws_bytes, uint32_t *d_status, csa2_stream stream)
@@ -133,9 +137,11 @@ csa2_status csa2_index_score(const csa2_index_args *a, float *scores, int32_t *r
     if (!index_args_ok(a)) return CSA2_ERR_INVALID_ARG;
     if ((int64_t)a->batch * a->n_q == 0) return CSA2_OK;
     if (!scores && index_candidates(a) > 0) return CSA2_ERR_INVALID_ARG;
-    if (ws_bytes < csa2_index_score_workspace_size(a)) return CSA2_ERR_WORKSPACE;
-    (void)ws;
-    return from_cuda(launch_index_score(*a, scores, row_len, d_status, as_stream(stream)));
+    const size_t need = csa2_index_score_workspace_size(a);
+    if (ws_bytes < need) return CSA2_ERR_WORKSPACE;
+    if (need && (!ws || !aligned(ws, 16))) return CSA2_ERR_INVALID_ARG;
+    return from_cuda(launch_index_score(*a, scores, row_len, need ? ws : nullptr, d_status,
+                                        as_stream(stream)));
 }
 
 size_t csa2_topk_workspace_size(int64_t rows, int64_t n, int32_t k)

@@ -30,6 +30,7 @@ struct IndexParams {
     bool pool_mode;
     float *scores;
     int32_t *row_len;
+    const uint32_t *seg_flags;   // non-null: only segments flagged here are scored
     uint32_t *d_status;
 };
 
@@ -60,6 +61,7 @@ __global__ void __launch_bounds__(kThreads) index_score_exact_kernel(IndexParams
     const int64_t row = blockIdx.y;
     const int64_t b = row / P.n_q;
     const int H = P.H;
+    if (P.seg_flags && P.seg_flags[row * gridDim.x + blockIdx.x] == 0u) return;
 
     for (int i = tid; i < 256; i += kThreads)
         s_lut[i] = (uint16_t)((e2m1_twice(i & 15u) & 0xff) | ((e2m1_twice(i >> 4) & 0xff) << 8));
@@ -162,8 +164,11 @@ __global__ void __launch_bounds__(kThreads) index_score_exact_kernel(IndexParams
 
 } // namespace
 
-cudaError_t launch_index_score(const csa2_index_args &a, float *scores, int32_t *row_len,
-                               uint32_t *d_status, cudaStream_t s)
+// Exact CUDA-core scoring of every segment of `chunk` candidates (or, with seg_flags, of
+// the flagged segments only).
+cudaError_t launch_index_exact(const csa2_index_args &a, float *scores, int32_t *row_len,
+                               const uint32_t *seg_flags, int64_t chunk, uint32_t *d_status,
+                               cudaStream_t s)
 {
     IndexParams P;
     P.n_q = a.n_q;
@@ -182,15 +187,17 @@ cudaError_t launch_index_score(const csa2_index_args &a, float *scores, int32_t 
     P.pool = a.pool_blocks;
     P.scores = scores;
     P.row_len = row_len;
+    P.seg_flags = seg_flags;
     P.d_status = d_status;
     const int64_t rows = (int64_t)a.batch * a.n_q;
     if (rows == 0) return cudaSuccess;
-    // chunk so that the grid covers the GPU a few times over
-    int64_t chunk = 2048;
-    while (chunk > 256 && rows * ((P.n_cand + chunk - 1) / chunk) < 152 * 8) chunk /= 2;
+    if (chunk <= 0) {   // chunk so that the grid covers the GPU a few times over
+        chunk = 2048;
+        while (chunk > 256 && rows * ((P.n_cand + chunk - 1) / chunk) < 152 * 8) chunk /= 2;
+    }
     P.chunk = chunk;
-    dim3 grid((unsigned)((P.n_cand + chunk - 1) / chunk > 0 ? (P.n_cand + chunk - 1) / chunk : 1),
-              (unsigned)rows);
+    int64_t gx = (P.n_cand + chunk - 1) / chunk;
+    dim3 grid((unsigned)(gx > 0 ? gx : 1), (unsigned)rows);
     switch (a.head_dim) {
     case 32: index_score_exact_kernel<32><<<grid, kThreads, 0, s>>>(P); break;
     case 64: index_score_exact_kernel<64><<<grid, kThreads, 0, s>>>(P); break;
@@ -198,6 +205,31 @@ cudaError_t launch_index_score(const csa2_index_args &a, float *scores, int32_t 
     default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
+}
+
+size_t index_score_ws_bytes(const csa2_index_args &a)
+{
+    if (!index_tc_eligible(a)) return 0;
+    int64_t splits, chunk;
+    index_tc_segments(a, splits, chunk);
+    return (size_t)((int64_t)a.batch * a.n_q * splits) * sizeof(uint32_t);
+}
+
+cudaError_t launch_index_score(const csa2_index_args &a, float *scores, int32_t *row_len, void *ws,
+                               uint32_t *d_status, cudaStream_t s)
+{
+    const int64_t rows = (int64_t)a.batch * a.n_q;
+    if (rows == 0) return cudaSuccess;
+    if (!index_tc_eligible(a) || !ws) return launch_index_exact(a, scores, row_len, nullptr, 0, d_status, s);
+    int64_t splits, chunk;
+    index_tc_segments(a, splits, chunk);
+    uint32_t *flags = static_cast<uint32_t *>(ws);
+    cudaError_t e = cudaMemsetAsync(flags, 0, (size_t)(rows * splits) * sizeof(uint32_t), s);
+    if (e != cudaSuccess) return e;
+    e = launch_index_tc(a, scores, row_len, flags, splits, chunk, d_status, s);
+    if (e != cudaSuccess) return e;
+    // segments holding a position the tensor-core path cannot prove exact: re-score them
+    return launch_index_exact(a, scores, row_len, flags, chunk, d_status, s);
 }
 
 } // namespace csa2

@@ -1,0 +1,432 @@
+// index_tc.cu -- tensor-core CSA2 indexer (csa2_index_score fast path, sm_103a tcgen05).
+//
+// DeepSeek-V4.1-Flash report (aipaper.jasonlin.tech) §2.3 / §2.4.4: the indexer scores
+// main-KV entries with FP4 (MXFP4) indexer queries and keys, which is what FP4 tensor
+// cores accelerate.  Per query row, the positions are a dense contraction
+//     D[t, h] = sum_d k_hat[t, d] * q_hat[h, d]      (t: 128-position tile, h: heads)
+// run as block-scaled MMA (kind::mxf4, E2M1 x E2M1, UE8M0 scale per 32) with M = 128
+// positions, N = 32 heads, K = 128 (two K = 64 steps).  The epilogue reads each
+// position's 32 head dots from tensor memory and forms s = fma32 chain of w_h * ReLU(D_h).
+//
+// Exactness.  The score is defined on D_h = RN32(exact dot).  Each K = 32 block adds an
+// integer (< 2^13) times 2^(Xq + Xk - 2); when every term's exponent lies within 9 of the
+// others and in the normal range, every partial sum is exactly representable, so the MMA's
+// float32 accumulation returns the exact dot whatever its order.  The epilogue checks that
+// condition conservatively per position from the scale bytes; a segment with any position
+// outside it is re-scored by the exact CUDA-core kernel (index_score.cu).
+//
+// Roles (192 threads): warp 0 = producer (TMA for the FP4 codes with the 64-byte swizzle,
+// cp.async for the scale bytes into the 512-byte scale-factor atom), warp 1 = MMA issuer
+// (tcgen05.cp of scale factors to TMEM, tcgen05.mma, tcgen05.commit), warps 2-5 =
+// epilogue (one TMEM lane quadrant each).  8-stage shared-memory ring, double-buffered
+// accumulators in TMEM.  One CTA scores one contiguous segment of one query row.
+#include <cudaTypedefs.h>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+#include "tc_util.cuh"
+
+namespace csa2 {
+namespace {
+
+constexpr int kD = 128;                // indexer head dim of this path
+constexpr int kRowBytes = kD / 2;      // 64 bytes of codes per position
+constexpr int kTile = 128;             // positions per tile (MMA M)
+constexpr int kStages = 8;
+constexpr int kThreads = 192;
+constexpr int kNPad = 32;              // MMA N: heads padded to 32
+constexpr uint32_t kTmemCols = 128;    // acc0 [0,32) acc1 [32,64) sfa0 [64,68) sfa1 [68,72) sfb [72,76)
+constexpr int kCtasPerSm = 3;
+constexpr int kSms = 152;
+
+struct TcParams {
+    int32_t n_q, H, ratio_m, block, n_pool_blocks;
+    int64_t n_keys, n_cand, chunk;
+    const uint16_t *q;
+    const float *w;
+    const uint8_t *ks;
+    const int32_t *q_pos, *pool;
+    int pool_mode;
+    float *scores;
+    int32_t *row_len;
+    uint32_t *seg_flags;
+    uint32_t *d_status;
+};
+
+struct TcSmem {
+    uint8_t a[kStages][kTile * kRowBytes];     // K codes, 64-byte swizzle, 1024-aligned
+    uint8_t b[kNPad * kRowBytes];              // q codes, same layout
+    uint32_t sfa[kStages][kTile];              // scale-factor atoms of the K tiles
+    uint32_t sfb[kTile];                       // scale-factor atom of q
+    uint64_t full[kStages], empty[kStages], accf[2], acce[2];
+    float w[kNPad];
+    int hmin[kNPad], hmax[kNPad];
+    unsigned long long len;
+    uint32_t tmem_base;
+    int abort_flag, unsafe, bad;
+    int q_span, q_min, q_max;
+};
+
+// instruction descriptor, kind::mxf4: A = B = E2M1 (1), UE8M0 scales, K-major A and B,
+// N at bits 17-22 (N/8), M at bits 24-28 (M/16), scale-factor ids at bits 4-5 (B) and
+// 29-30 (A) select the byte pair of the 32-bit scale column used by this K = 64 step.
+__device__ __forceinline__ uint32_t mxf4_idesc(int sf_id)
+{
+    return (1u << 7) | (1u << 10) | ((uint32_t)(kNPad >> 3) << 17) | (1u << 23) |
+           ((uint32_t)(kTile >> 4) << 24) | ((uint32_t)sf_id << 4) | ((uint32_t)sf_id << 29);
+}
+
+__device__ __forceinline__ int64_t n_visible(const TcParams &P, int64_t row)
+{
+    if (!P.q_pos) return P.n_keys;
+    const int64_t p = P.q_pos[row];
+    int64_t v = (p + 1) / P.ratio_m;
+    if (p + 1 < 0) v = 0;
+    return v < 0 ? 0 : (v > P.n_keys ? P.n_keys : v);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P)
+{
+    extern __shared__ uint8_t smem_raw[];
+    TcSmem &S = *reinterpret_cast<TcSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                            ~uintptr_t(1023));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t row = blockIdx.y;
+    const int64_t b = row / P.n_q;
+    const int H = P.H;
+
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            tc::mbar_init(&S.full[s], 1 + 32);
+            tc::mbar_init(&S.empty[s], 1 + 4);
+        }
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(&S.accf[i], 1);
+            tc::mbar_init(&S.acce[i], 4);
+        }
+        S.abort_flag = 0;
+        S.unsafe = 0;
+        S.bad = 0;
+        S.len = 0;
+        tc::fence_mbar_init();
+    }
+    if (tid < kNPad) { S.hmin[tid] = 1 << 20; S.hmax[tid] = -(1 << 20); }
+    if (tid < kTile) S.sfb[tid] = 0x7f7f7f7fu;
+    if (warp == 0 && lane == 0) tc::prefetch_tmap(&tmap);
+    if (warp == 1) {
+        tc::tmem_alloc(&S.tmem_base, kTmemCols);
+        tc::tmem_relinquish();
+    }
+    __syncthreads();
+
+    // ---- the query: MXFP4 codes into the B operand (64-byte swizzle), scale atom, stats
+    if (warp >= 2) {
+        const int kb = warp - 2;                              // this warp's 32-value block
+        const uint16_t *q = P.q + row * (int64_t)H * kD;
+        for (int h = 0; h < kNPad; ++h) {
+            float v = 0.0f;
+            if (h < H) v = __uint_as_float((uint32_t)q[h * kD + kb * 32 + lane] << 16);
+            const uint32_t amax_bits = __reduce_max_sync(0xffffffffu, __float_as_uint(v) & 0x7fffffffu);
+            const bool finite = amax_bits < 0x7f800000u;
+            const int X = mx_block_exponent(__uint_as_float(finite ? amax_bits : 0u));
+            const uint32_t c = e2m1_encode(v, pow2_neg(X));
+            const uint32_t c_hi = __shfl_down_sync(0xffffffffu, c, 1);
+            // row h, 16-byte chunk kb of the 64-byte row, XOR-swizzled by bits 1-2 of h%8
+            const int r8 = h & 7;
+            const int off = (h >> 3) * 512 + r8 * 64 + ((kb ^ ((r8 >> 1) & 3)) << 4);
+            if ((lane & 1) == 0) S.b[off + (lane >> 1)] = (uint8_t)(c | (c_hi << 4));
+            if (lane == 0) {
+                reinterpret_cast<uint8_t *>(S.sfb)[h * 16 + kb] = (uint8_t)(X + 127);
+                if (h < H && amax_bits != 0) {
+                    atomicMin(&S.hmin[h], X);
+                    atomicMax(&S.hmax[h], X);
+                }
+                if (h < H && !finite) dev_flag(P.d_status, CSA2_DEV_NONFINITE);
+            }
+        }
+        if (kb == 0) S.w[lane] = lane < H ? P.w[row * H + lane] : 0.0f;
+        tc::fence_proxy_async_smem();
+    }
+    // ---- valid candidates of this row (and pool checks)
+    const int64_t n_vis = n_visible(P, row);
+    const int32_t *pool = P.pool_mode ? P.pool + row * (int64_t)P.n_pool_blocks : nullptr;
+    const int64_t n_blk_all = (P.n_keys + P.block - 1) / P.block;
+    if (!P.pool_mode) {
+        if (tid == 0) S.len = (unsigned long long)n_vis;
+    } else {
+        unsigned long long part = 0;
+        int bad = 0;
+        for (int i = tid; i < P.n_pool_blocks; i += kThreads) {
+            const int32_t id = pool[i];
+            const int32_t prev = i > 0 ? pool[i - 1] : -1;
+            if (id >= 0) {
+                if (id >= n_blk_all || (i > 0 && (prev < 0 || prev >= id))) bad = 1;
+                const int64_t c = n_vis - (int64_t)id * P.block;
+                part += c <= 0 ? 0 : (c > P.block ? P.block : c);
+            }
+        }
+        if (bad) atomicOr(&S.bad, 1);
+        if (part) atomicAdd(&S.len, part);
+    }
+    __syncthreads();
+    if (tid == 0) {
+        int span = 0, mn = 1 << 20, mx = -(1 << 20);
+        for (int h = 0; h < H; ++h) {
+            if (S.hmin[h] > S.hmax[h]) continue;              // all-zero head
+            span = max(span, S.hmax[h] - S.hmin[h]);
+            mn = min(mn, S.hmin[h]);
+            mx = max(mx, S.hmax[h]);
+        }
+        S.q_span = span;
+        S.q_min = mn;
+        S.q_max = mx;
+    }
+    __syncthreads();
+
+    const int64_t len = (int64_t)S.len;
+    if (blockIdx.x == 0 && tid == 0) {
+        if (P.row_len) P.row_len[row] = (int32_t)len;
+        if (S.bad) dev_flag(P.d_status, CSA2_DEV_BAD_POOL);
+    }
+    const int64_t c0 = (int64_t)blockIdx.x * P.chunk;
+    const int64_t c1 = min(c0 + P.chunk, len);
+    const int ntiles = c1 > c0 ? (int)((c1 - c0 + kTile - 1) / kTile) : 0;
+    const uint32_t tmem = S.tmem_base;
+    const int64_t kbase = b * P.n_keys;
+
+    if (warp == 0) {
+        // ================= producer
+        int issued = 0;
+        for (int i = 0; i < ntiles; ++i) {
+            const int s = i % kStages;
+            const uint32_t ph = (uint32_t)(i / kStages) & 1u;
+            if (!tc::mbar_wait(&S.empty[s], ph ^ 1u, &S.abort_flag)) { S.abort_flag = 1; break; }
+            const int64_t t0 = c0 + (int64_t)i * kTile;
+            if (lane == 0) {
+                if (!P.pool_mode) {
+                    tc::mbar_arrive_expect_tx(&S.full[s], kTile * kRowBytes);
+                    tc::tma_load_2d(S.a[s], &tmap, &S.full[s], 0, (int32_t)(kbase + t0));
+                } else {
+                    uint32_t bytes = 0;
+                    for (int j = 0; j < kTile / 8; ++j)
+                        if (t0 + 8 * j < c1 && pool[(t0 >> 3) + j] >= 0) bytes += 8 * kRowBytes;
+                    tc::mbar_arrive_expect_tx(&S.full[s], bytes);
+                    for (int j = 0; j < kTile / 8; ++j) {
+                        if (t0 + 8 * j >= c1) break;
+                        int64_t id = pool[(t0 >> 3) + j];
+                        if (id < 0) continue;
+                        id = id >= n_blk_all ? n_blk_all - 1 : id;
+                        tc::tma_load_2d(S.a[s] + j * 8 * kRowBytes, &tmap, &S.full[s], 0,
+                                        (int32_t)(kbase + id * 8));
+                    }
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int m = lane + 32 * j;
+                const int64_t cand = t0 + m;
+                uint32_t *dst = &S.sfa[s][lane * 4 + j];
+                if (cand < c1) {
+                    int64_t pos = cand;
+                    if (P.pool_mode) {
+                        int64_t id = pool[cand >> 3];
+                        id = id < 0 ? 0 : (id >= n_blk_all ? n_blk_all - 1 : id);
+                        pos = id * 8 + (cand & 7);
+                        if (pos >= P.n_keys) pos = P.n_keys - 1;
+                    }
+                    tc::cp_async_4(dst, P.ks + (kbase + pos) * 4);
+                } else {
+                    *dst = 0x7f7f7f7fu;
+                }
+            }
+            tc::fence_proxy_async_smem();
+            tc::cp_async_mbar_arrive_noinc(&S.full[s]);
+            ++issued;
+        }
+        if (S.abort_flag) {       // let copies already in flight land before the CTA exits
+            for (int i = issued - 1; i >= 0 && i >= issued - kStages; --i)
+                tc::mbar_wait_bounded(&S.full[i % kStages], (uint32_t)(i / kStages) & 1u);
+        }
+    } else if (warp == 1) {
+        // ================= MMA issuer
+        if (lane == 0 && ntiles > 0) {
+            const uint32_t sfb_t = tmem + 72;
+            tc::tc_fence_after();
+            tc::tc_cp_32x128b_warpx4(sfb_t, tc::smem_desc(tc::smem_u32(S.sfb), 512, 128, tc::kSwizzleNone));
+            for (int i = 0; i < ntiles; ++i) {
+                const int s = i % kStages, acc = i & 1;
+                if (!tc::mbar_wait(&S.acce[acc], ((uint32_t)(i >> 1) & 1u) ^ 1u, &S.abort_flag) ||
+                    !tc::mbar_wait(&S.full[s], (uint32_t)(i / kStages) & 1u, &S.abort_flag)) {
+                    S.abort_flag = 1;
+                    break;
+                }
+                tc::fence_proxy_async_smem();
+                tc::tc_fence_after();
+                const uint32_t sfa_t = tmem + 64 + 4 * acc;
+                tc::tc_cp_32x128b_warpx4(sfa_t, tc::smem_desc(tc::smem_u32(S.sfa[s]), 512, 128,
+                                                              tc::kSwizzleNone));
+                const uint32_t d_t = tmem + acc * kNPad;
+#pragma unroll
+                for (int kk = 0; kk < 2; ++kk) {
+                    const uint64_t ad = tc::smem_desc(tc::smem_u32(S.a[s]) + kk * 32, 16, 512, tc::kSwizzle64B);
+                    const uint64_t bd = tc::smem_desc(tc::smem_u32(S.b) + kk * 32, 16, 512, tc::kSwizzle64B);
+                    tc::tc_mma_mxf4(d_t, ad, bd, mxf4_idesc(2 * kk), sfa_t, sfb_t, kk);
+                }
+                tc::tc_commit(&S.empty[s]);
+                tc::tc_commit(&S.accf[acc]);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ================= epilogue: warp's TMEM lane quadrant
+        const int quad = warp & 3;
+        const int m = quad * 32 + lane;
+        const int q_span = S.q_span, q_min = S.q_min, q_max = S.q_max;
+        for (int i = 0; i < ntiles; ++i) {
+            const int s = i % kStages, acc = i & 1;
+            if (!tc::mbar_wait(&S.accf[acc], (uint32_t)(i >> 1) & 1u, &S.abort_flag) ||
+                !tc::mbar_wait(&S.full[s], (uint32_t)(i / kStages) & 1u, &S.abort_flag)) {
+                S.abort_flag = 1;
+                break;
+            }
+            tc::tc_fence_after();
+            uint32_t r[32];
+            tc::tc_ld_32x32b_x32(tmem + ((uint32_t)(quad * 32) << 16) + acc * kNPad, r);
+            tc::tc_wait_ld();
+            const uint32_t sfw = S.sfa[s][lane * 4 + quad];
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                tc::mbar_arrive(&S.acce[acc]);
+                tc::mbar_arrive(&S.empty[s]);
+            }
+            const int64_t cand = c0 + (int64_t)i * kTile + m;
+            if (cand < c1) {
+                float sc = 0.0f;
+#pragma unroll
+                for (int h = 0; h < kNPad; ++h) {
+                    if (h < H) {
+                        const float D = __uint_as_float(r[h]);
+                        sc = __fmaf_rn(S.w[h], D > 0.0f ? D : 0.0f, sc);
+                    }
+                }
+                const int e0 = (int)(sfw & 255u), e1 = (int)((sfw >> 8) & 255u);
+                const int e2 = (int)((sfw >> 16) & 255u), e3 = (int)(sfw >> 24);
+                const int kmin = min(min(e0, e1), min(e2, e3)) - 127;
+                const int kmax = max(max(e0, e1), max(e2, e3)) - 127;
+                const bool safe = (kmax - kmin) + q_span <= 9 && q_min + kmin - 2 >= -126 &&
+                                  q_max + kmax - 2 <= 100;
+                if (!safe) S.unsafe = 1;
+                P.scores[row * P.n_cand + cand] = sc;
+            }
+        }
+    }
+
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem, kTmemCols);
+    }
+    if (tid == 0) {
+        if (S.unsafe || S.abort_flag) P.seg_flags[row * gridDim.x + blockIdx.x] = 1u;
+        if (S.abort_flag) dev_flag(P.d_status, CSA2_DEV_TIMEOUT);
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+int64_t tc_splits(int64_t rows, int64_t n_cand)
+{
+    const int64_t tiles = (n_cand + kTile - 1) / kTile;
+    int64_t s = (int64_t)kSms * kCtasPerSm / (rows > 0 ? rows : 1);
+    if (s < 1) s = 1;
+    if (s > tiles) s = tiles > 0 ? tiles : 1;
+    return s;
+}
+
+} // namespace
+
+bool index_tc_eligible(const csa2_index_args &a)
+{
+    if (a.head_dim != kD || a.n_heads > kNPad) return false;
+    if (a.mode == CSA2_INDEX_POOL && a.block != 8) return false;
+    if ((int64_t)a.batch * a.n_keys >= (int64_t(1) << 31)) return false;
+    if (((uintptr_t)a.k_codes & 15) != 0) return false;
+    return encode_fn() != nullptr;
+}
+
+// Segment layout shared with the exact kernel: `splits` segments of `chunk` candidates.
+void index_tc_segments(const csa2_index_args &a, int64_t &splits, int64_t &chunk)
+{
+    const int64_t rows = (int64_t)a.batch * a.n_q;
+    const int64_t n_cand = a.mode == CSA2_INDEX_POOL ? (int64_t)a.n_pool_blocks * a.block : a.n_keys;
+    splits = tc_splits(rows, n_cand);
+    const int64_t tiles = (n_cand + kTile - 1) / kTile;
+    chunk = ((tiles + splits - 1) / splits) * kTile;
+    if (chunk < kTile) chunk = kTile;
+    splits = (n_cand + chunk - 1) / chunk;
+    if (splits < 1) splits = 1;
+}
+
+cudaError_t launch_index_tc(const csa2_index_args &a, float *scores, int32_t *row_len,
+                            uint32_t *seg_flags, int64_t splits, int64_t chunk, uint32_t *d_status,
+                            cudaStream_t s)
+{
+    const int64_t rows = (int64_t)a.batch * a.n_q;
+    TcParams P;
+    P.n_q = a.n_q;
+    P.H = a.n_heads;
+    P.ratio_m = a.ratio_m;
+    P.block = a.block;
+    P.n_pool_blocks = a.n_pool_blocks;
+    P.n_keys = a.n_keys;
+    P.pool_mode = a.mode == CSA2_INDEX_POOL;
+    P.n_cand = P.pool_mode ? (int64_t)a.n_pool_blocks * a.block : a.n_keys;
+    P.chunk = chunk;
+    P.q = a.q;
+    P.w = a.w;
+    P.ks = a.k_scales;
+    P.q_pos = a.q_pos;
+    P.pool = a.pool_blocks;
+    P.scores = scores;
+    P.row_len = row_len;
+    P.seg_flags = seg_flags;
+    P.d_status = d_status;
+
+    CUtensorMap map;
+    cuuint64_t dims[2] = {(cuuint64_t)kRowBytes, (cuuint64_t)((int64_t)a.batch * a.n_keys)};
+    cuuint64_t strides[1] = {(cuuint64_t)kRowBytes};
+    cuuint32_t box[2] = {(cuuint32_t)kRowBytes, (cuuint32_t)(P.pool_mode ? 8 : kTile)};
+    cuuint32_t estr[2] = {1, 1};
+    if (dims[1] == 0) dims[1] = 1;
+    CUresult r = encode_fn()(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(a.k_codes),
+                             dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                             CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    const size_t smem = sizeof(TcSmem) + 1024;
+    cudaError_t e = cudaFuncSetAttribute(index_score_tc_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid((unsigned)splits, (unsigned)rows);
+    index_score_tc_kernel<<<grid, kThreads, smem, s>>>(map, P);
+    return cudaGetLastError();
+}
+
+} // namespace csa2

@@ -9,8 +9,12 @@
 // four 8-bit digit passes (most significant first) find the K-th key tau and how many
 // entries equal to tau must be taken; a final pass in index order emits every entry
 // above tau and the first `need` entries equal to tau, which yields ascending output.
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "internal.h"
+
+namespace cg = cooperative_groups;
 
 namespace csa2 {
 namespace {
@@ -136,6 +140,227 @@ topk_radix_kernel(const float *__restrict__ scores, int64_t n, const int32_t *__
     }
 }
 
+// ------------------------------------------------------------------ cluster radix select
+// One thread-block cluster per row.  CTA r of the cluster owns the contiguous slice r of
+// the row (kept as keys in shared memory when it fits).  Three digit passes of 11, 11 and
+// 10 bits: each CTA histograms its slice, the cluster sums the histograms through
+// distributed shared memory, and every CTA derives the same digit.  The final pass emits
+// the selected entries in position order: CTA r starts after everything earlier CTAs
+// selected, and takes ties in order until the cluster-wide quota is used up.
+constexpr int kClThreads = 512;
+constexpr int kClBins = 2048;
+constexpr int kClKeyCap = 24576;            // keys per CTA kept in shared memory (96 KB)
+
+struct ClusterTopkArgs {
+    const float *scores;
+    int64_t n;
+    const int32_t *row_len;
+    const int32_t *pool;
+    int32_t block, k;
+    int32_t *idx;
+    float *out_scores;
+    int64_t key_cap;     // keys of a slice that fit the launch's dynamic shared memory
+};
+
+// Block-wide exclusive prefix sum of one value per thread (kClThreads threads).
+__device__ __forceinline__ uint32_t cl_block_excl_sum(uint32_t v, uint32_t *s_warp, uint32_t &total)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const uint32_t w = lane < kClThreads / 32 ? s_warp[lane] : 0u;
+        uint32_t wi = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t t = __shfl_up_sync(0xffffffffu, wi, o);
+            if (lane >= o) wi += t;
+        }
+        s_warp[lane] = wi - w;
+        if (lane == 31) s_warp[32] = wi;
+    }
+    __syncthreads();
+    const uint32_t r = s_warp[warp] + incl - v;
+    total = s_warp[32];
+    __syncthreads();
+    return r;
+}
+
+__global__ void __launch_bounds__(kClThreads) topk_cluster_kernel(const ClusterTopkArgs A)
+{
+    extern __shared__ uint32_t s_keys[];
+    __shared__ uint32_t s_hist[kClBins];
+    __shared__ uint32_t s_warp[33];
+    __shared__ uint32_t s_cnt[2];
+    __shared__ uint32_t s_pick[2];
+    cg::cluster_group cl = cg::this_cluster();
+    const int rank = (int)cl.block_rank(), CS = (int)cl.num_blocks();
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int64_t row = blockIdx.y;
+    int64_t len = A.row_len ? (int64_t)A.row_len[row] : A.n;
+    len = len < 0 ? 0 : (len > A.n ? A.n : len);
+    const float *s = A.scores + row * A.n;
+    const int32_t *pool_row = A.pool ? A.pool + row * (A.n / A.block) : nullptr;
+    int32_t *out = A.idx + row * (int64_t)A.k;
+    float *out_s = A.out_scores ? A.out_scores + row * (int64_t)A.k : nullptr;
+    const int64_t per = (len + CS - 1) / CS;
+    const int64_t lo = min((int64_t)rank * per, len), hi = min(lo + per, len);
+    const int m = (int)(hi - lo);
+
+    if (len <= A.k) {                          // everything competes and wins
+        for (int i = tid; i < m; i += kClThreads) {
+            out[lo + i] = (int32_t)cand_pos(pool_row, A.block, lo + i);
+            if (out_s) out_s[lo + i] = s[lo + i];
+        }
+        if (rank == CS - 1)
+            for (int64_t i = len + tid; i < A.k; i += kClThreads) {
+                out[i] = -1;
+                if (out_s) out_s[i] = 0.0f;
+            }
+        return;
+    }
+    const bool in_smem = per <= A.key_cap;
+    if (in_smem)
+        for (int i = tid; i < m; i += kClThreads) s_keys[i] = score_key(s[lo + i]);
+
+    uint32_t prefix = 0, mask = 0, remaining = (uint32_t)A.k;
+    const int shifts[3] = {21, 10, 0}, widths[3] = {11, 11, 10};
+    for (int pass = 0; pass < 3; ++pass) {
+        const int shift = shifts[pass], nb = 1 << widths[pass];
+        for (int i = tid; i < kClBins; i += kClThreads) s_hist[i] = 0;
+        __syncthreads();
+        for (int base = 0; base < m; base += kClThreads) {
+            const int i = base + tid;
+            uint32_t key = 0;
+            bool act = false;
+            if (i < m) {
+                key = in_smem ? s_keys[i] : score_key(s[lo + i]);
+                act = (key & mask) == prefix;
+            }
+            const uint32_t am = __ballot_sync(0xffffffffu, act);
+            if (act) {
+                const uint32_t digit = (key >> shift) & (uint32_t)(nb - 1);
+                const uint32_t peers = __match_any_sync(am, digit);
+                if (lane == __ffs(peers) - 1) atomicAdd(&s_hist[digit], (uint32_t)__popc(peers));
+            }
+        }
+        cl.sync();
+        // thread t owns bins nb-1-4t .. nb-4-4t (descending); cluster-wide totals
+        uint32_t tot[4], sum = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int bin = nb - 1 - (4 * tid + j);
+            uint32_t v = 0;
+            if (bin >= 0)
+                for (int r = 0; r < CS; ++r) v += cl.map_shared_rank(s_hist, r)[bin];
+            tot[j] = v;
+            sum += v;
+        }
+        uint32_t all;
+        uint32_t c = cl_block_excl_sum(sum, s_warp, all);   // elements with a larger digit
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int bin = nb - 1 - (4 * tid + j);
+            if (bin >= 0 && c < remaining && c + tot[j] >= remaining) {
+                s_pick[0] = (uint32_t)bin;
+                s_pick[1] = remaining - c;
+            }
+            c += tot[j];
+        }
+        cl.sync();                             // histograms read everywhere before reuse
+        prefix |= s_pick[0] << shift;
+        mask |= (uint32_t)(nb - 1) << shift;
+        remaining = s_pick[1];
+    }
+    const uint32_t tau = prefix, need = remaining;   // take `need` entries equal to tau
+
+    // counts of this slice, then what earlier CTAs of the cluster select
+    uint32_t n_gt = 0, n_eq = 0;
+    for (int i = tid; i < m; i += kClThreads) {
+        const uint32_t key = in_smem ? s_keys[i] : score_key(s[lo + i]);
+        n_gt += key > tau;
+        n_eq += key == tau;
+    }
+    uint32_t t_gt, t_eq;
+    cl_block_excl_sum(n_gt, s_warp, t_gt);
+    cl_block_excl_sum(n_eq, s_warp, t_eq);
+    if (tid == 0) { s_cnt[0] = t_gt; s_cnt[1] = t_eq; }
+    cl.sync();
+    uint32_t gt_before = 0, eq_before = 0;
+    for (int r = 0; r < rank; ++r) {
+        const uint32_t *rc = cl.map_shared_rank(s_cnt, r);
+        gt_before += rc[0];
+        eq_before += rc[1];
+    }
+    cl.sync();                                 // remote counts read: CTAs may now finish alone
+    uint32_t out_base = gt_before + min(eq_before, need);
+    uint32_t ties = eq_before;
+    for (int base = 0; base < m; base += kClThreads) {
+        const int i = base + tid;
+        uint32_t key = 0;
+        if (i < m) key = in_smem ? s_keys[i] : score_key(s[lo + i]);
+        const bool gt = i < m && key > tau;
+        const bool eq = i < m && key == tau;
+        uint32_t tot_eq, tot_sel;
+        const uint32_t eq_rank = ties + cl_block_excl_sum(eq ? 1u : 0u, s_warp, tot_eq);
+        const bool sel = gt || (eq && eq_rank < need);
+        const uint32_t sel_rank = out_base + cl_block_excl_sum(sel ? 1u : 0u, s_warp, tot_sel);
+        if (sel && sel_rank < (uint32_t)A.k) {
+            out[sel_rank] = (int32_t)cand_pos(pool_row, A.block, lo + i);
+            if (out_s) out_s[sel_rank] = s[lo + i];
+        }
+        ties += tot_eq;
+        out_base += tot_sel;
+    }
+}
+
+int cluster_size_for(int64_t rows, int64_t n)
+{
+    int64_t want = (2 * 152 + rows - 1) / (rows > 0 ? rows : 1);      // fill the GPU
+    int64_t need = (n + kClKeyCap - 1) / kClKeyCap;                   // keep keys on chip
+    int64_t c = want > need ? want : need;
+    int64_t per_min = 2048;                                           // no tiny slices
+    int64_t cap = (n + per_min - 1) / per_min;
+    if (c > cap) c = cap;
+    int cs = 1;
+    while (cs < c && cs < 16) cs <<= 1;
+    return cs;
+}
+
+cudaError_t launch_topk_cluster(ClusterTopkArgs A, int64_t rows, cudaStream_t s)
+{
+    const int cs = cluster_size_for(rows, A.n);
+    const int64_t per = (A.n + cs - 1) / cs;          // slice of the longest possible row
+    const size_t smem = per <= kClKeyCap ? (size_t)(per > 0 ? per : 1) * sizeof(uint32_t) : 0;
+    A.key_cap = (int64_t)(smem / sizeof(uint32_t));
+    cudaError_t e = cudaFuncSetAttribute(topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)(kClKeyCap * sizeof(uint32_t)));
+    if (e != cudaSuccess) return e;
+    if (cs > 8) {
+        e = cudaFuncSetAttribute(topk_cluster_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)cs, (unsigned)rows, 1);
+    cfg.blockDim = dim3(kClThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, topk_cluster_kernel, A);
+}
+
 // Block score = max over the block's valid positions (NaN ignored; all-NaN -> NaN).
 __global__ void block_max_kernel(const float *__restrict__ scores, int64_t n,
                                  const int32_t *__restrict__ row_len, int32_t block, int64_t nbmax,
@@ -165,9 +390,13 @@ cudaError_t launch_topk(const float *scores, int64_t rows, int64_t n, const int3
                         float *out_scores, void *, uint32_t *, cudaStream_t s)
 {
     if (rows == 0 || k == 0) return cudaSuccess;
-    topk_radix_kernel<<<(unsigned)rows, kTopkThreads, 0, s>>>(scores, n, row_len, pool, block, k,
-                                                             idx, out_scores);
-    return cudaGetLastError();
+    if (rows > 65535) {
+        topk_radix_kernel<<<(unsigned)rows, kTopkThreads, 0, s>>>(scores, n, row_len, pool, block, k,
+                                                                 idx, out_scores);
+        return cudaGetLastError();
+    }
+    ClusterTopkArgs A{scores, n, row_len, pool, block, k, idx, out_scores, 0};
+    return launch_topk_cluster(A, rows, s);
 }
 
 size_t block_candidates_ws_bytes(int64_t rows, int64_t n, int32_t block, int32_t)

@@ -216,21 +216,37 @@ def run_gpu(args):
                                  dw["q_pos"], w.ratio_m)
     aargs = csa2.make_attn_args(dw["q_attn"], dw["kv_codes"], dw["kv_scales"], idx, dw["swa"],
                                 dw["swa_pos0"], dw["q_pos"], None, w.window, dw.sm_scale, w.d_v)
+    lib = csa2.load()
+    import ctypes
+    ws_index = torch.empty(max(1, lib.csa2_index_score_workspace_size(ctypes.byref(iargs))),
+                           dtype=torch.uint8, device=dev)
+    ws_attn = torch.empty(max(1, lib.csa2_sparse_attn_workspace_size(ctypes.byref(aargs))),
+                          dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
-    launches_per_step = 5
+    # our kernels per step: 2 cache-write quantisers, indexer (tensor-core + exact re-score
+    # of flagged segments), Top-K, attention (+ split combine)
+    launches_per_step = 7
 
     def step(k_ev=None):
+        # k_ev: events bracketing each call of the step (cache write, indexer, Top-K, attention)
+        stream = torch.cuda.current_stream(dev)       # the capture stream while capturing
+        if k_ev:
+            k_ev[0].record(stream)
         # cache write: the new token's main-KV and indexer-K rows, quantised in place
         csa2.csa2_quant_fp4(new_kv, new_kvc, new_kvs, st)
         csa2.csa2_quant_fp4(new_k, new_kc, new_ks, st)
         if k_ev:
-            k_ev[0].record(stream)
-        csa2.csa2_index_score(iargs, scores, row_len, st)
-        if k_ev:
             k_ev[1].record(stream)
+        csa2.csa2_index_score(iargs, scores, row_len, st, workspace=ws_index)
+        if k_ev:
+            k_ev[2].record(stream)
         csa2.csa2_topk(scores, w.topk, idx, row_len, d_status=st)
-        csa2.csa2_sparse_attn(aargs, out, lse, st)
+        if k_ev:
+            k_ev[3].record(stream)
+        csa2.csa2_sparse_attn(aargs, out, lse, st, workspace=ws_attn)
+        if k_ev:
+            k_ev[4].record(stream)
 
     for _ in range(args.warmup):
         step()
@@ -238,25 +254,50 @@ def run_gpu(args):
     if int(st.item()) != 0:
         raise RuntimeError(f"device status {int(st.item())}")
 
+    # ---- the step as a CUDA graph (no host launch gaps), with timing events between calls
+    names = ["cache_write_quant", "index_score", "topk", "sparse_attn"]
+    graph, g_ev = None, None
+    try:
+        g_ev = tuple(torch.cuda.Event(enable_timing=True, external=True) for _ in range(5))
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step(g_ev)
+        for _ in range(args.warmup):
+            graph.replay()
+        torch.cuda.synchronize(dev)
+    except (TypeError, RuntimeError) as exc:          # no external events / capture: eager
+        graph, g_ev = None, None
+        torch.cuda.synchronize(dev)
+        print(f"# CUDA graph capture unavailable ({exc}); timing eager launches", file=sys.stderr)
+    stream = torch.cuda.current_stream(dev)
+
+    def run_step(k_ev=None):
+        if graph is not None:
+            graph.replay()
+        else:
+            step(k_ev)
+
     # ---- device-timed steps: inputs resident in HBM, L2 flushed between steps (untimed)
-    t_steps, t_kern = [], []
+    ms_steps, per_k = [], {n: [] for n in names}
     if dist:
         dist.barrier()
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clocks:
         for _ in range(args.steps):
             flush.fill_(1)
-            e0, e1, k_ev = ev(), ev(), (ev(), ev())
+            e0, e1 = ev(), ev()
+            k_ev = g_ev if graph is not None else tuple(ev() for _ in range(5))
             e0.record(stream)
-            step(k_ev)
+            run_step(k_ev)
             e1.record(stream)
-            t_steps.append((e0, e1))
-            t_kern.append(k_ev)
+            e1.synchronize()
+            ms_steps.append(e0.elapsed_time(e1))
+            for i, n in enumerate(names):
+                per_k[n].append(k_ev[i].elapsed_time(k_ev[i + 1]))
         torch.cuda.synchronize(dev)
-    ms_steps = [a.elapsed_time(b) for a, b in t_steps]
-    ms_kern = [a.elapsed_time(b) for a, b in t_kern]
+    per_kernel = {n: sum(v) / len(v) for n, v in per_k.items()}
     ms_step = sum(ms_steps) / len(ms_steps)
-    ms_k = sum(ms_kern) / len(ms_kern)
+    ms_k = per_kernel["index_score"]
 
     # ---- end to end through the public API from pinned host buffers
     h_qi = dw["q_idx"].cpu().pin_memory()
@@ -265,23 +306,20 @@ def run_gpu(args):
     h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     h2d = h_qi.numel() * 2 + h_w.numel() * 4 + h_qa.numel() * 2
     d2h = h_out.numel() * 2
-    for _ in range(2):
-        dw["q_idx"].copy_(h_qi, non_blocking=True)
-        step()
-    torch.cuda.synchronize(dev)
     e2e_ms = []
-    for _ in range(args.steps):
+    for it in range(args.steps + 2):
         flush.fill_(1)
         e0, e1 = ev(), ev()
         e0.record(stream)
         dw["q_idx"].copy_(h_qi, non_blocking=True)
         dw["w_idx"].copy_(h_w, non_blocking=True)
         dw["q_attn"].copy_(h_qa, non_blocking=True)
-        step()
+        run_step(g_ev if graph is not None else None)
         h_out.copy_(out, non_blocking=True)
         e1.record(stream)
         e1.synchronize()
-        e2e_ms.append(e0.elapsed_time(e1))
+        if it >= 2:
+            e2e_ms.append(e0.elapsed_time(e1))
     e2e_step = sum(e2e_ms) / len(e2e_ms)
     if int(st.item()) != 0:
         raise RuntimeError(f"device status {int(st.item())}")
@@ -309,7 +347,8 @@ def run_gpu(args):
                    "parallelism": f"replicas{world}", "topk": w.topk, "window": w.window,
                    "indexer": f"{w.idx_heads}x{w.idx_dim}", "heads": w.heads,
                    "d_qk": w.d_qk, "d_v": w.d_v,
-                   "l2": "flushed between timed steps (256 MiB write, untimed)"},
+                   "l2": "flushed between timed steps (256 MiB write, untimed)",
+                   "launch": "CUDA graph of the step" if graph is not None else "eager"},
         "achieved_gbs_step": _step_bytes(w) / (ms_step * 1e-3) / 1e9,
         "roofline": {"bound": "hbm", "kernel": "csa2_index_score", "achieved": achieved,
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
@@ -317,6 +356,7 @@ def run_gpu(args):
                      "algorithmic_bytes": kb, "ms": ms_k},
         "e2e": {"value": tokens / (e2e_step * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_step},
+        "kernels_ms": per_kernel,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks.summary(),
     }

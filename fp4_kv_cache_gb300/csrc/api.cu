@@ -198,7 +198,9 @@ csa2_status csa2_sparse_attn(const csa2_attn_args *a, uint16_t *out, float *lse,
     if (!attn_args_ok(a)) return CSA2_ERR_INVALID_ARG;
     if ((int64_t)a->batch * a->n_q == 0) return CSA2_OK;
     if (!out) return CSA2_ERR_INVALID_ARG;
-    if (ws_bytes < csa2_sparse_attn_workspace_size(a)) return CSA2_ERR_WORKSPACE;
+    const size_t need = csa2_sparse_attn_workspace_size(a);
+    if (ws_bytes < need) return CSA2_ERR_WORKSPACE;
+    if (need && (!ws || !aligned(ws, 16))) return CSA2_ERR_INVALID_ARG;
     return from_cuda(launch_sparse_attn(*a, out, lse, ws, d_status, as_stream(stream)));
 }
 

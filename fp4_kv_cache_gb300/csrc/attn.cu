@@ -209,9 +209,12 @@ cudaError_t launch_cc(const AttnParams &P, int64_t rows, cudaStream_t s)
 
 } // namespace
 
-size_t sparse_attn_ws_bytes(const csa2_attn_args &) { return 0; }
+size_t sparse_attn_ws_bytes(const csa2_attn_args &a)
+{
+    return attn_tc_eligible(a) ? attn_tc_ws_bytes(a) : 0;
+}
 
-cudaError_t launch_sparse_attn(const csa2_attn_args &a, uint16_t *out, float *lse, void *,
+cudaError_t launch_sparse_attn(const csa2_attn_args &a, uint16_t *out, float *lse, void *ws,
                                uint32_t *d_status, cudaStream_t s)
 {
     AttnParams P;
@@ -237,6 +240,7 @@ cudaError_t launch_sparse_attn(const csa2_attn_args &a, uint16_t *out, float *ls
     P.d_status = d_status;
     const int64_t rows = (int64_t)a.batch * a.n_q;
     if (rows == 0 || a.n_heads == 0) return cudaSuccess;
+    if (attn_tc_eligible(a)) return launch_attn_tc(a, out, lse, ws, d_status, s);
     const int cpt = (a.d_v + kThreads - 1) / kThreads;
     switch (cpt <= 1 ? 1 : cpt <= 2 ? 2 : 4) {
     case 1: return launch_cc<1>(P, rows, s);

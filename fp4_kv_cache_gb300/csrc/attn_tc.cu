@@ -1,0 +1,523 @@
+// attn_tc.cu -- tensor-core CSA2 core attention (csa2_sparse_attn fast path, sm_103a).
+//
+// DeepSeek-V4.1-Flash report (aipaper.jasonlin.tech) §2.3 / §2.3.1: each query attends its
+// selected main-KV entries (dequantised from FP4, §2.4.4) together with the layer's SWA
+// window; review page (papers.chlience.com, CSA2 section): the latent is shared by all
+// query heads, so K = the whole latent and V = its leading d_v dims.
+//
+// Orientation: keys are the MMA M dimension.  For a tile of 128 key slots:
+//   S^T [128 keys x 64 heads]  = K [keys x 576] . Q^T          (kind::f16, bf16 in, f32 acc)
+//   O^T [512 dims x 64 heads] += V^T [dims x keys] . P^T        (P = softmax numerators)
+// The dequantised key tile lives in shared memory as nine K-major 128-byte-swizzled chunks
+// of 64 dims; the first eight serve as the K-major A operand of S^T and, read MN-major, as
+// V^T for O^T, so the latent is never transposed.  S^T (64 columns) and O^T (4 x 64
+// columns) accumulate in tensor memory.  Softmax runs with one thread per key: per-head
+// maxima and sums are reduced across the 128 threads with a halving shuffle reduction.
+// A CTA covers a contiguous span of tiles of one query row with an online softmax; when
+// a row is split over several CTAs, each writes (O, m, l) partials and a combine kernel
+// merges them.
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "common.cuh"
+#include "internal.h"
+#include "tc_util.cuh"
+
+namespace csa2 {
+namespace {
+
+constexpr int kThreads = 128;
+constexpr int kKeys = 128;            // key slots per tile (MMA M)
+constexpr int kH = 64;                // heads (MMA N; fewer heads are zero-padded)
+constexpr int kDqk = 576, kDv = 512;
+constexpr int kChunks = kDqk / 64;    // 9 chunks of 64 dims
+constexpr int kChunkBytes = kKeys * 128;          // 16 KB: 128 keys x 64 bf16
+constexpr int kQChunkBytes = kH * 128;            // 8 KB: 64 heads x 64 bf16
+constexpr uint32_t kTmemCols = 512;   // S^T [0,64), O^T block m at [64 + 64m, 128 + 64m)
+
+struct AttnTcParams {
+    int32_t T, H, topk, window, n_swa, splits, tiles_per_split;
+    float sm_scale;
+    int64_t n_kv;
+    const uint16_t *q;
+    const uint8_t *kvc, *kvs;
+    const int32_t *idx;
+    const uint16_t *swa;
+    const int32_t *swa_pos0, *swa_start, *q_pos;
+    uint16_t *out;
+    float *lse;
+    float *part_o;    // [rows, splits, H, d_v] (splits > 1)
+    float *part_ml;   // [rows, splits, H, 2]
+    uint32_t *d_status;
+};
+
+// smem layout (dynamic, 1024-aligned): K chunks 0..7 | rope chunk / P^T | Q chunks 0..8
+constexpr int kOffK = 0;
+constexpr int kOffR = 8 * kChunkBytes;                    // 131072
+constexpr int kOffQ = kOffR + kChunkBytes;                // 147456
+constexpr int kSmemBytes = kOffQ + kChunks * kQChunkBytes; // 221184
+
+__device__ __forceinline__ int sw128(int row, int piece)   // byte offset of 16-byte piece
+{
+    return (row >> 3) * 1024 + (row & 7) * 128 + ((piece ^ (row & 7)) << 4);
+}
+
+__device__ __forceinline__ uint32_t f16_idesc(int a_mn)
+{
+    // c = f32, a = b = bf16, A major (0 K, 1 MN), B K-major, N = 64, M = 128
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)(kH >> 3) << 17) |
+           ((uint32_t)(kKeys >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc)
+{
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+                 ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0],"
+                 " {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16,"
+                 " %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};"
+                 ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]),
+                   "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]),
+                   "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+                   "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+                   "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_16(void *dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all()
+{
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// Reduce 64 per-thread values over the 32 lanes of a warp by halving: afterwards lane L
+// holds the reductions for heads 2L and 2L+1 in v[0], v[1].
+template <bool MAX>
+__device__ __forceinline__ void warp_halving_reduce(float (&v)[64], int lane)
+{
+#pragma unroll
+    for (int o = 16, n = 64; o >= 1; o >>= 1, n >>= 1) {
+        const bool upper = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < n / 2; ++i) {
+            const float send = upper ? v[i] : v[i + n / 2];
+            const float keep = upper ? v[i + n / 2] : v[i];
+            const float recv = __shfl_xor_sync(0xffffffffu, send, o);
+            v[i] = MAX ? fmaxf(keep, recv) : keep + recv;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnTcParams P)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ int64_t s_src[kKeys];
+    __shared__ float s_red[4][kH];
+    __shared__ float s_m[kH], s_l[kH], s_corr[kH];
+    __shared__ uint64_t s_bar;
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_abort;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t row = blockIdx.y;
+    const int split = blockIdx.x;
+    const int64_t b = row / P.T;
+    const int H = P.H;
+
+    if (tid == 0) {
+        tc::mbar_init(&s_bar, 1);
+        tc::fence_mbar_init();
+        s_abort = 0;
+    }
+    if (tid < kH) { s_m[tid] = -INFINITY; s_l[tid] = 0.0f; }
+    if (warp == 0) {
+        tc::tmem_alloc(&s_tmem, kTmemCols);
+        tc::tmem_relinquish();
+    }
+    // Q -> nine K-major chunks (rows = heads), zero rows for heads >= H
+    for (int e = tid; e < kH * kChunks * 8; e += kThreads) {
+        const int h = e / (kChunks * 8), rem = e % (kChunks * 8), c = rem >> 3, p = rem & 7;
+        uint8_t *dst = sm + kOffQ + c * kQChunkBytes + sw128(h, p);
+        if (h < H) cp_async_16(dst, P.q + ((row * H + h) * (int64_t)kDqk + c * 64 + p * 8));
+        else *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
+    }
+
+    // this query's key slots: idx entries, then its SWA window [max(s, p-W+1, 0), p]
+    int64_t j0 = 0, n_sw = 0;
+    if (P.swa) {
+        const int64_t p = P.q_pos[row];
+        const int64_t s0 = P.swa_start ? (int64_t)P.swa_start[b] : 0;
+        int64_t lo = p - P.window + 1;
+        lo = lo < s0 ? s0 : lo;
+        lo = lo < 0 ? 0 : lo;
+        const int64_t pos0 = P.swa_pos0[b];
+        j0 = lo - pos0 < 0 ? 0 : lo - pos0;
+        int64_t j1 = p - pos0;
+        j1 = j1 > P.n_swa - 1 ? P.n_swa - 1 : j1;
+        n_sw = j1 >= j0 ? j1 - j0 + 1 : 0;
+    }
+    const int64_t n_slots = P.topk + n_sw;
+    const int n_tiles = (int)((n_slots + kKeys - 1) / kKeys);
+    const int t_begin = split * P.tiles_per_split;
+    const int t_end = min(t_begin + P.tiles_per_split, n_tiles);
+    __syncthreads();
+    const uint32_t tmem = s_tmem;
+    uint32_t phase = 0;
+    bool any_o = false;
+
+    for (int tile = t_begin; tile < t_end; ++tile) {
+        // ---- slot -> source
+        {
+            const int64_t sl = (int64_t)tile * kKeys + tid;
+            int64_t src = -1;
+            if (sl < P.topk) {
+                const int32_t id = P.idx[row * P.topk + sl];
+                if (id >= 0 && id < P.n_kv) src = id;
+                else if (id != -1) dev_flag(P.d_status, CSA2_DEV_BAD_INDEX);
+            } else if (sl < n_slots) {
+                src = -(j0 + (sl - P.topk) + 2);
+            }
+            s_src[tid] = src;
+        }
+        // ---- gather + dequantise key tid into the nine chunks (row tid)
+        {
+            const int64_t src = s_src[tid];
+            const int r = tid;
+            if (src >= 0) {
+                const uint8_t *codes = P.kvc + (b * P.n_kv + src) * (kDqk / 2);
+                const uint8_t *scl = P.kvs + (b * P.n_kv + src) * (kDqk / 32);
+#pragma unroll 3
+                for (int blk = 0; blk < kDqk / 32; ++blk) {      // 18 blocks of 32 values
+                    const uint4 raw = *reinterpret_cast<const uint4 *>(codes + blk * 16);
+                    const float sc = e8m0_value(scl[blk]);
+                    const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+                    const int c = blk >> 1;
+                    uint8_t *base = sm + (c < 8 ? kOffK + c * kChunkBytes : kOffR);
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {             // 8 values -> one 16-byte piece
+                        uint32_t packed[4];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const uint32_t byte = (w4[q4] >> (8 * k)) & 0xffu;
+                            float lo = e2m1_mag(byte & 7u) * sc, hi = e2m1_mag((byte >> 4) & 7u) * sc;
+                            if (byte & 8u) lo = -lo;
+                            if (byte & 0x80u) hi = -hi;
+                            const __nv_bfloat162 bb = __floats2bfloat162_rn(lo, hi);
+                            packed[k] = *reinterpret_cast<const uint32_t *>(&bb);
+                        }
+                        const int piece = (blk & 1) * 4 + q4;
+                        *reinterpret_cast<uint4 *>(base + sw128(r, piece)) =
+                            make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                    }
+                }
+            } else if (src <= -2) {
+                const uint16_t *srow = P.swa + (b * P.n_swa + (-src - 2)) * (int64_t)kDqk;
+                for (int pc = 0; pc < kDqk / 8; ++pc) {
+                    const int c = pc >> 3;
+                    uint8_t *base = sm + (c < 8 ? kOffK + c * kChunkBytes : kOffR);
+                    cp_async_16(base + sw128(r, pc & 7), srow + pc * 8);
+                }
+            } else {
+                for (int pc = 0; pc < kDqk / 8; ++pc) {
+                    const int c = pc >> 3;
+                    uint8_t *base = sm + (c < 8 ? kOffK + c * kChunkBytes : kOffR);
+                    *reinterpret_cast<uint4 *>(base + sw128(r, pc & 7)) = make_uint4(0, 0, 0, 0);
+                }
+            }
+        }
+        cp_async_wait_all();
+        tc::fence_proxy_async_smem();
+        __syncthreads();
+        // ---- S^T = K . Q^T
+        if (tid == 0) {
+            tc::tc_fence_after();
+#pragma unroll 1
+            for (int c = 0; c < kChunks; ++c) {
+                const uint32_t a0 = tc::smem_u32(sm + (c < 8 ? kOffK + c * kChunkBytes : kOffR));
+                const uint32_t b0 = tc::smem_u32(sm + kOffQ + c * kQChunkBytes);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_f16(tmem, tc::smem_desc(a0 + kk * 32, 16, 1024, tc::kSwizzle128B),
+                            tc::smem_desc(b0 + kk * 32, 16, 1024, tc::kSwizzle128B), f16_idesc(0),
+                            (c | kk) != 0);
+            }
+            tc::tc_commit(&s_bar);
+        }
+        __syncwarp();
+        if (__syncthreads_or(!tc::mbar_wait(&s_bar, phase, &s_abort))) { s_abort = 1; break; }
+        phase ^= 1u;
+        tc::tc_fence_after();
+        // ---- softmax numerators for this tile (thread = key slot = TMEM lane)
+        float l[64];
+        {
+            uint32_t r[32];
+            tc::tc_ld_32x32b_x32(tmem + ((uint32_t)(warp * 32) << 16), r);
+            tc::tc_wait_ld();
+#pragma unroll
+            for (int h = 0; h < 32; ++h) l[h] = __uint_as_float(r[h]);
+            tc::tc_ld_32x32b_x32(tmem + ((uint32_t)(warp * 32) << 16) + 32, r);
+            tc::tc_wait_ld();
+#pragma unroll
+            for (int h = 0; h < 32; ++h) l[32 + h] = __uint_as_float(r[h]);
+        }
+        const bool valid = s_src[tid] != -1;
+#pragma unroll
+        for (int h = 0; h < 64; ++h) l[h] = (valid && h < H) ? l[h] * P.sm_scale : -INFINITY;
+        {
+            float v[64];
+#pragma unroll
+            for (int h = 0; h < 64; ++h) v[h] = l[h];
+            warp_halving_reduce<true>(v, lane);
+            s_red[warp][2 * lane] = v[0];
+            s_red[warp][2 * lane + 1] = v[1];
+        }
+        __syncthreads();
+        if (tid < kH) {
+            const float tmax = fmaxf(fmaxf(s_red[0][tid], s_red[1][tid]), fmaxf(s_red[2][tid], s_red[3][tid]));
+            const float m_old = s_m[tid];
+            const float m_new = fmaxf(m_old, tmax);
+            s_corr[tid] = (m_old == -INFINITY) ? 0.0f : expf(m_old - m_new);
+            s_m[tid] = m_new;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int h = 0; h < 64; ++h) {
+            const float m = s_m[h];
+            l[h] = (l[h] == -INFINITY) ? 0.0f : expf(l[h] - m);
+        }
+        {
+            float v[64];
+#pragma unroll
+            for (int h = 0; h < 64; ++h) v[h] = l[h];
+            warp_halving_reduce<false>(v, lane);
+            s_red[warp][2 * lane] = v[0];
+            s_red[warp][2 * lane + 1] = v[1];
+        }
+        // ---- P^T (bf16) into the rope-chunk buffer: [64 heads x 128 keys], two 64-key halves
+        {
+            uint8_t *pbase = sm + kOffR + (tid >> 6) * (kQChunkBytes);
+            const int col = tid & 63;
+            const bool odd = (lane & 1) != 0;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                // even lanes store heads 0..31 for keys (tid, tid+1); odd lanes heads 32..63 for (tid-1, tid)
+                const float mine = odd ? l[32 + i] : l[i];
+                const float send = odd ? l[i] : l[32 + i];
+                const float other = __shfl_xor_sync(0xffffffffu, send, 1);
+                const int h = odd ? 32 + i : i;
+                const int c0 = odd ? col - 1 : col;
+                const __nv_bfloat162 pr = odd ? __floats2bfloat162_rn(other, mine)
+                                              : __floats2bfloat162_rn(mine, other);
+                *reinterpret_cast<__nv_bfloat162 *>(pbase + sw128(h, c0 >> 3) + (c0 & 7) * 2) = pr;
+            }
+        }
+        __syncthreads();
+        if (tid < kH) {
+            const float tsum = s_red[0][tid] + s_red[1][tid] + s_red[2][tid] + s_red[3][tid];
+            s_l[tid] = s_l[tid] * s_corr[tid] + tsum;
+        }
+        // ---- rescale the running O^T by the per-head correction (thread = dim row)
+        if (any_o) {
+#pragma unroll 1
+            for (int m = 0; m < 4; ++m)
+#pragma unroll 1
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t r[32];
+                    const uint32_t ta = tmem + ((uint32_t)(warp * 32) << 16) + 64 + 64 * m + 32 * half;
+                    tc::tc_ld_32x32b_x32(ta, r);
+                    tc::tc_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        r[j] = __float_as_uint(__uint_as_float(r[j]) * s_corr[32 * half + j]);
+                    tmem_st_32x32b_x32(ta, r);
+                }
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        }
+        tc::fence_proxy_async_smem();
+        tc::tc_fence_before();
+        __syncthreads();
+        // ---- O^T += V^T . P^T  (A = key chunks read MN-major, B = P^T K-major)
+        if (tid == 0) {
+            tc::tc_fence_after();
+#pragma unroll 1
+            for (int m = 0; m < 4; ++m) {
+                const uint32_t a0 = tc::smem_u32(sm + kOffK + (2 * m) * kChunkBytes);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t b0 = tc::smem_u32(sm + kOffR + (kk >> 2) * kQChunkBytes) + (kk & 3) * 32;
+                    mma_f16(tmem + 64 + 64 * m,
+                            tc::smem_desc(a0 + kk * 2048, kChunkBytes, 1024, tc::kSwizzle128B),
+                            tc::smem_desc(b0, 16, 1024, tc::kSwizzle128B), f16_idesc(1),
+                            (any_o || kk > 0) ? 1u : 0u);
+                }
+            }
+            tc::tc_commit(&s_bar);
+        }
+        __syncwarp();
+        if (__syncthreads_or(!tc::mbar_wait(&s_bar, phase, &s_abort))) { s_abort = 1; break; }
+        phase ^= 1u;
+        tc::tc_fence_after();
+        any_o = true;
+        __syncthreads();
+    }
+
+    // ---- epilogue: thread = dim row of each O^T block
+    const bool single = P.splits == 1;
+    const int64_t ps = row * P.splits + split;
+#pragma unroll 1
+    for (int m = 0; m < 4; ++m) {
+        const int d = 128 * m + warp * 32 + lane;
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {
+            uint32_t r[32];
+            if (any_o) {
+                tc::tc_ld_32x32b_x32(tmem + ((uint32_t)(warp * 32) << 16) + 64 + 64 * m + 32 * half, r);
+                tc::tc_wait_ld();
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) r[j] = 0u;
+            }
+#pragma unroll 4
+            for (int j = 0; j < 32; ++j) {
+                const int h = 32 * half + j;
+                if (h >= H) break;
+                const float o = __uint_as_float(r[j]);
+                if (single) {
+                    const float L = s_l[h];
+                    const float v = L > 0.0f ? o / L : 0.0f;
+                    uint32_t bits = __float_as_uint(v);
+                    bits += 0x7fffu + ((bits >> 16) & 1u);
+                    P.out[(row * H + h) * (int64_t)kDv + d] = (uint16_t)(bits >> 16);
+                } else {
+                    P.part_o[(ps * H + h) * (int64_t)kDv + d] = o;
+                }
+            }
+        }
+    }
+    if (tid < H) {
+        if (single) {
+            if (P.lse) P.lse[row * H + tid] = s_l[tid] > 0.0f ? s_m[tid] + logf(s_l[tid]) : -INFINITY;
+        } else {
+            P.part_ml[(ps * H + tid) * 2 + 0] = s_m[tid];
+            P.part_ml[(ps * H + tid) * 2 + 1] = s_l[tid];
+        }
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem, kTmemCols);
+    }
+    if (tid == 0 && s_abort) dev_flag(P.d_status, CSA2_DEV_TIMEOUT);
+}
+
+// Merge split partials: o = sum_s e^(m_s - M) O_s / sum_s e^(m_s - M) l_s, lse = M + log(...)
+__global__ void __launch_bounds__(256) attn_combine_kernel(const AttnTcParams P)
+{
+    const int64_t row = blockIdx.y;
+    const int h = blockIdx.x;
+    const int S = P.splits;
+    float M = -INFINITY;
+    for (int s = 0; s < S; ++s) M = fmaxf(M, P.part_ml[((row * S + s) * P.H + h) * 2]);
+    float L = 0.0f;
+    for (int s = 0; s < S; ++s) {
+        const float m = P.part_ml[((row * S + s) * P.H + h) * 2];
+        if (m != -INFINITY) L += expf(m - M) * P.part_ml[((row * S + s) * P.H + h) * 2 + 1];
+    }
+    for (int d = threadIdx.x; d < kDv; d += blockDim.x) {
+        float o = 0.0f;
+        for (int s = 0; s < S; ++s) {
+            const float m = P.part_ml[((row * S + s) * P.H + h) * 2];
+            if (m != -INFINITY) o += expf(m - M) * P.part_o[((row * S + s) * P.H + h) * (int64_t)kDv + d];
+        }
+        const float v = L > 0.0f ? o / L : 0.0f;
+        uint32_t bits = __float_as_uint(v);
+        bits += 0x7fffu + ((bits >> 16) & 1u);
+        P.out[(row * P.H + h) * (int64_t)kDv + d] = (uint16_t)(bits >> 16);
+    }
+    if (threadIdx.x == 0 && P.lse) P.lse[row * P.H + h] = L > 0.0f ? M + logf(L) : -INFINITY;
+}
+
+void attn_tc_split(const csa2_attn_args &a, int &splits, int &tiles_per_split)
+{
+    const int64_t rows = (int64_t)a.batch * a.n_q;
+    const int64_t max_slots = (int64_t)a.topk + (a.swa ? (int64_t)(a.window < a.n_swa ? a.window : a.n_swa) : 0);
+    const int tiles = (int)((max_slots + kKeys - 1) / kKeys);
+    int64_t per = (tiles * rows + 151) / 152;          // tiles per CTA to fill one wave
+    if (per < 1) per = 1;
+    if (per > tiles) per = tiles > 0 ? tiles : 1;
+    tiles_per_split = (int)per;
+    splits = tiles > 0 ? (int)((tiles + per - 1) / per) : 1;
+}
+
+} // namespace
+
+bool attn_tc_eligible(const csa2_attn_args &a)
+{
+    return a.d_qk == kDqk && a.d_v == kDv && a.n_heads <= kH && ((uintptr_t)a.q & 15) == 0 &&
+           (!a.swa || ((uintptr_t)a.swa & 15) == 0) && ((uintptr_t)a.kv_codes & 15) == 0;
+}
+
+size_t attn_tc_ws_bytes(const csa2_attn_args &a)
+{
+    int splits, per;
+    attn_tc_split(a, splits, per);
+    if (splits <= 1) return 0;
+    const size_t rows = (size_t)a.batch * a.n_q;
+    size_t o = rows * splits * a.n_heads * (size_t)kDv * sizeof(float);
+    o = (o + 255) & ~(size_t)255;
+    return o + rows * splits * a.n_heads * 2 * sizeof(float);
+}
+
+cudaError_t launch_attn_tc(const csa2_attn_args &a, uint16_t *out, float *lse, void *ws,
+                           uint32_t *d_status, cudaStream_t s)
+{
+    AttnTcParams P;
+    P.T = a.n_q;
+    P.H = a.n_heads;
+    P.topk = a.topk;
+    P.window = a.window;
+    P.n_swa = a.swa ? a.n_swa : 0;
+    P.sm_scale = a.sm_scale;
+    P.n_kv = a.n_kv;
+    P.q = a.q;
+    P.kvc = a.kv_codes;
+    P.kvs = a.kv_scales;
+    P.idx = a.idx;
+    P.swa = a.swa;
+    P.swa_pos0 = a.swa_pos0;
+    P.swa_start = a.swa_start;
+    P.q_pos = a.q_pos;
+    P.out = out;
+    P.lse = lse;
+    P.d_status = d_status;
+    attn_tc_split(a, P.splits, P.tiles_per_split);
+    const int64_t rows = (int64_t)a.batch * a.n_q;
+    if (P.splits > 1) {
+        const size_t o = ((size_t)rows * P.splits * a.n_heads * (size_t)kDv * sizeof(float) + 255) & ~(size_t)255;
+        P.part_o = static_cast<float *>(ws);
+        P.part_ml = reinterpret_cast<float *>(static_cast<char *>(ws) + o);
+    } else {
+        P.part_o = nullptr;
+        P.part_ml = nullptr;
+    }
+    const int smem = kSmemBytes + 1024;
+    cudaError_t e = cudaFuncSetAttribute(sparse_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    sparse_attn_tc_kernel<<<dim3((unsigned)P.splits, (unsigned)rows), kThreads, smem, s>>>(P);
+    e = cudaGetLastError();
+    if (e != cudaSuccess || P.splits == 1) return e;
+    attn_combine_kernel<<<dim3((unsigned)a.n_heads, (unsigned)rows), 256, 0, s>>>(P);
+    return cudaGetLastError();
+}
+
+} // namespace csa2

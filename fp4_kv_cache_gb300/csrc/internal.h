@@ -39,6 +39,10 @@ cudaError_t launch_block_candidates(const float *scores, int64_t rows, int64_t n
                                     cudaStream_t s);
 
 size_t sparse_attn_ws_bytes(const csa2_attn_args &a);
+bool attn_tc_eligible(const csa2_attn_args &a);
+size_t attn_tc_ws_bytes(const csa2_attn_args &a);
+cudaError_t launch_attn_tc(const csa2_attn_args &a, uint16_t *out, float *lse, void *ws,
+                           uint32_t *d_status, cudaStream_t s);
 cudaError_t launch_sparse_attn(const csa2_attn_args &a, uint16_t *out, float *lse, void *ws,
                                uint32_t *d_status, cudaStream_t s);
 

@@ -322,7 +322,7 @@ __global__ void __launch_bounds__(kClThreads) topk_cluster_kernel(const ClusterT
 
 int cluster_size_for(int64_t rows, int64_t n)
 {
-    int64_t want = (2 * 152 + rows - 1) / (rows > 0 ? rows : 1);      // fill the GPU
+    int64_t want = (152 + rows - 1) / (rows > 0 ? rows : 1);          // about one CTA per SM
     int64_t need = (n + kClKeyCap - 1) / kClKeyCap;                   // keep keys on chip
     int64_t c = want > need ? want : need;
     int64_t per_min = 2048;                                           // no tiny slices

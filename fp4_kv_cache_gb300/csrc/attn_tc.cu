@@ -26,7 +26,7 @@
 namespace csa2 {
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;          // two warps per TMEM lane quadrant
 constexpr int kKeys = 128;            // key slots per tile (MMA M)
 constexpr int kH = 64;                // heads (MMA N; fewer heads are zero-padded)
 constexpr int kDqk = 576, kDv = 512;
@@ -98,13 +98,13 @@ __device__ __forceinline__ void cp_async_wait_all()
     asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
-// Reduce 64 per-thread values over the 32 lanes of a warp by halving: afterwards lane L
-// holds the reductions for heads 2L and 2L+1 in v[0], v[1].
+// Reduce 32 per-thread values over the 32 lanes of a warp by halving: afterwards lane L
+// holds the reduction of value index L in v[0] (31 shuffles instead of 32 x 5).
 template <bool MAX>
-__device__ __forceinline__ void warp_halving_reduce(float (&v)[64], int lane)
+__device__ __forceinline__ float warp_halving_reduce32(float (&v)[32], int lane)
 {
 #pragma unroll
-    for (int o = 16, n = 64; o >= 1; o >>= 1, n >>= 1) {
+    for (int o = 16, n = 32; o >= 1; o >>= 1, n >>= 1) {
         const bool upper = (lane & o) != 0;
 #pragma unroll
         for (int i = 0; i < n / 2; ++i) {
@@ -114,6 +114,7 @@ __device__ __forceinline__ void warp_halving_reduce(float (&v)[64], int lane)
             v[i] = MAX ? fmaxf(keep, recv) : keep + recv;
         }
     }
+    return v[0];
 }
 
 __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnTcParams P)
@@ -174,9 +175,11 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
     uint32_t phase = 0;
     bool any_o = false;
 
+    const int quad = warp & 3, hh0 = 32 * (warp >> 2);   // TMEM lane quadrant, first head
+    const int key_row = 32 * quad + lane;                 // this thread's key / dim row
     for (int tile = t_begin; tile < t_end; ++tile) {
         // ---- slot -> source
-        {
+        if (tid < kKeys) {
             const int64_t sl = (int64_t)tile * kKeys + tid;
             int64_t src = -1;
             if (sl < P.topk) {
@@ -188,18 +191,25 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
             }
             s_src[tid] = src;
         }
-        // ---- gather + dequantise key tid into the nine chunks (row tid)
+        __syncthreads();
+        // ---- gather + dequantise: threads r and r+128 take the two halves of key row r
         {
-            const int64_t src = s_src[tid];
-            const int r = tid;
+            const int r = tid & (kKeys - 1), part = tid >> 7;
+            const int64_t src = s_src[r];
             if (src >= 0) {
-                const uint8_t *codes = P.kvc + (b * P.n_kv + src) * (kDqk / 2);
-                const uint8_t *scl = P.kvs + (b * P.n_kv + src) * (kDqk / 32);
-#pragma unroll 3
-                for (int blk = 0; blk < kDqk / 32; ++blk) {      // 18 blocks of 32 values
-                    const uint4 raw = *reinterpret_cast<const uint4 *>(codes + blk * 16);
-                    const float sc = e8m0_value(scl[blk]);
-                    const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+                const uint8_t *codes = P.kvc + (b * P.n_kv + src) * (kDqk / 2) + part * 9 * 16;
+                const uint8_t *scl = P.kvs + (b * P.n_kv + src) * (kDqk / 32) + part * 9;
+                uint4 raw[9];
+                uint32_t sb[9];
+#pragma unroll
+                for (int i = 0; i < 9; ++i) raw[i] = *reinterpret_cast<const uint4 *>(codes + i * 16);
+#pragma unroll
+                for (int i = 0; i < 9; ++i) sb[i] = scl[i];
+#pragma unroll
+                for (int i = 0; i < 9; ++i) {
+                    const int blk = part * 9 + i;                 // 32-value block of the row
+                    const float sc = e8m0_value(sb[i]);
+                    const uint32_t w4[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
                     const int c = blk >> 1;
                     uint8_t *base = sm + (c < 8 ? kOffK + c * kChunkBytes : kOffR);
 #pragma unroll
@@ -214,20 +224,19 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
                             const __nv_bfloat162 bb = __floats2bfloat162_rn(lo, hi);
                             packed[k] = *reinterpret_cast<const uint32_t *>(&bb);
                         }
-                        const int piece = (blk & 1) * 4 + q4;
-                        *reinterpret_cast<uint4 *>(base + sw128(r, piece)) =
+                        *reinterpret_cast<uint4 *>(base + sw128(r, (blk & 1) * 4 + q4)) =
                             make_uint4(packed[0], packed[1], packed[2], packed[3]);
                     }
                 }
             } else if (src <= -2) {
                 const uint16_t *srow = P.swa + (b * P.n_swa + (-src - 2)) * (int64_t)kDqk;
-                for (int pc = 0; pc < kDqk / 8; ++pc) {
+                for (int pc = part * 36; pc < part * 36 + 36; ++pc) {
                     const int c = pc >> 3;
                     uint8_t *base = sm + (c < 8 ? kOffK + c * kChunkBytes : kOffR);
                     cp_async_16(base + sw128(r, pc & 7), srow + pc * 8);
                 }
             } else {
-                for (int pc = 0; pc < kDqk / 8; ++pc) {
+                for (int pc = part * 36; pc < part * 36 + 36; ++pc) {
                     const int c = pc >> 3;
                     uint8_t *base = sm + (c < 8 ? kOffK + c * kChunkBytes : kOffR);
                     *reinterpret_cast<uint4 *>(base + sw128(r, pc & 7)) = make_uint4(0, 0, 0, 0);
@@ -256,29 +265,22 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
         if (__syncthreads_or(!tc::mbar_wait(&s_bar, phase, &s_abort))) { s_abort = 1; break; }
         phase ^= 1u;
         tc::tc_fence_after();
-        // ---- softmax numerators for this tile (thread = key slot = TMEM lane)
-        float l[64];
+        // ---- softmax numerators: thread = (key row, 32 heads)
+        float l[32];
         {
             uint32_t r[32];
-            tc::tc_ld_32x32b_x32(tmem + ((uint32_t)(warp * 32) << 16), r);
+            tc::tc_ld_32x32b_x32(tmem + ((uint32_t)(quad * 32) << 16) + hh0, r);
             tc::tc_wait_ld();
+            const bool valid = s_src[key_row] != -1;
 #pragma unroll
-            for (int h = 0; h < 32; ++h) l[h] = __uint_as_float(r[h]);
-            tc::tc_ld_32x32b_x32(tmem + ((uint32_t)(warp * 32) << 16) + 32, r);
-            tc::tc_wait_ld();
-#pragma unroll
-            for (int h = 0; h < 32; ++h) l[32 + h] = __uint_as_float(r[h]);
+            for (int j = 0; j < 32; ++j)
+                l[j] = (valid && hh0 + j < H) ? __uint_as_float(r[j]) * P.sm_scale : -INFINITY;
         }
-        const bool valid = s_src[tid] != -1;
-#pragma unroll
-        for (int h = 0; h < 64; ++h) l[h] = (valid && h < H) ? l[h] * P.sm_scale : -INFINITY;
         {
-            float v[64];
+            float v[32];
 #pragma unroll
-            for (int h = 0; h < 64; ++h) v[h] = l[h];
-            warp_halving_reduce<true>(v, lane);
-            s_red[warp][2 * lane] = v[0];
-            s_red[warp][2 * lane + 1] = v[1];
+            for (int j = 0; j < 32; ++j) v[j] = l[j];
+            s_red[quad][hh0 + lane] = warp_halving_reduce32<true>(v, lane);
         }
         __syncthreads();
         if (tid < kH) {
@@ -290,30 +292,26 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
         }
         __syncthreads();
 #pragma unroll
-        for (int h = 0; h < 64; ++h) {
-            const float m = s_m[h];
-            l[h] = (l[h] == -INFINITY) ? 0.0f : expf(l[h] - m);
-        }
+        for (int j = 0; j < 32; ++j) l[j] = (l[j] == -INFINITY) ? 0.0f : expf(l[j] - s_m[hh0 + j]);
         {
-            float v[64];
+            float v[32];
 #pragma unroll
-            for (int h = 0; h < 64; ++h) v[h] = l[h];
-            warp_halving_reduce<false>(v, lane);
-            s_red[warp][2 * lane] = v[0];
-            s_red[warp][2 * lane + 1] = v[1];
+            for (int j = 0; j < 32; ++j) v[j] = l[j];
+            s_red[quad][hh0 + lane] = warp_halving_reduce32<false>(v, lane);
         }
         // ---- P^T (bf16) into the rope-chunk buffer: [64 heads x 128 keys], two 64-key halves
         {
-            uint8_t *pbase = sm + kOffR + (tid >> 6) * (kQChunkBytes);
-            const int col = tid & 63;
+            uint8_t *pbase = sm + kOffR + (key_row >> 6) * kQChunkBytes;
+            const int col = key_row & 63;
             const bool odd = (lane & 1) != 0;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                // even lanes store heads 0..31 for keys (tid, tid+1); odd lanes heads 32..63 for (tid-1, tid)
-                const float mine = odd ? l[32 + i] : l[i];
-                const float send = odd ? l[i] : l[32 + i];
+            for (int i = 0; i < 16; ++i) {
+                // even lanes store heads hh0..hh0+15 for keys (row, row+1); odd lanes heads
+                // hh0+16..hh0+31 for keys (row-1, row)
+                const float mine = odd ? l[16 + i] : l[i];
+                const float send = odd ? l[i] : l[16 + i];
                 const float other = __shfl_xor_sync(0xffffffffu, send, 1);
-                const int h = odd ? 32 + i : i;
+                const int h = hh0 + (odd ? 16 + i : i);
                 const int c0 = odd ? col - 1 : col;
                 const __nv_bfloat162 pr = odd ? __floats2bfloat162_rn(other, mine)
                                               : __floats2bfloat162_rn(mine, other);
@@ -325,21 +323,19 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
             const float tsum = s_red[0][tid] + s_red[1][tid] + s_red[2][tid] + s_red[3][tid];
             s_l[tid] = s_l[tid] * s_corr[tid] + tsum;
         }
-        // ---- rescale the running O^T by the per-head correction (thread = dim row)
+        // ---- rescale the running O^T by the per-head correction (thread = dim row, 32 heads)
         if (any_o) {
 #pragma unroll 1
-            for (int m = 0; m < 4; ++m)
-#pragma unroll 1
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t r[32];
-                    const uint32_t ta = tmem + ((uint32_t)(warp * 32) << 16) + 64 + 64 * m + 32 * half;
-                    tc::tc_ld_32x32b_x32(ta, r);
-                    tc::tc_wait_ld();
+            for (int m = 0; m < 4; ++m) {
+                uint32_t r[32];
+                const uint32_t ta = tmem + ((uint32_t)(quad * 32) << 16) + 64 + 64 * m + hh0;
+                tc::tc_ld_32x32b_x32(ta, r);
+                tc::tc_wait_ld();
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        r[j] = __float_as_uint(__uint_as_float(r[j]) * s_corr[32 * half + j]);
-                    tmem_st_32x32b_x32(ta, r);
-                }
+                for (int j = 0; j < 32; ++j)
+                    r[j] = __float_as_uint(__uint_as_float(r[j]) * s_corr[hh0 + j]);
+                tmem_st_32x32b_x32(ta, r);
+            }
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         }
         tc::fence_proxy_async_smem();
@@ -370,36 +366,33 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
         __syncthreads();
     }
 
-    // ---- epilogue: thread = dim row of each O^T block
+    // ---- epilogue: thread = (dim row of each O^T block, 32 heads)
     const bool single = P.splits == 1;
     const int64_t ps = row * P.splits + split;
 #pragma unroll 1
     for (int m = 0; m < 4; ++m) {
-        const int d = 128 * m + warp * 32 + lane;
-#pragma unroll 1
-        for (int half = 0; half < 2; ++half) {
-            uint32_t r[32];
-            if (any_o) {
-                tc::tc_ld_32x32b_x32(tmem + ((uint32_t)(warp * 32) << 16) + 64 + 64 * m + 32 * half, r);
-                tc::tc_wait_ld();
-            } else {
+        const int d = 128 * m + key_row;
+        uint32_t r[32];
+        if (any_o) {
+            tc::tc_ld_32x32b_x32(tmem + ((uint32_t)(quad * 32) << 16) + 64 + 64 * m + hh0, r);
+            tc::tc_wait_ld();
+        } else {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) r[j] = 0u;
-            }
+            for (int j = 0; j < 32; ++j) r[j] = 0u;
+        }
 #pragma unroll 4
-            for (int j = 0; j < 32; ++j) {
-                const int h = 32 * half + j;
-                if (h >= H) break;
-                const float o = __uint_as_float(r[j]);
-                if (single) {
-                    const float L = s_l[h];
-                    const float v = L > 0.0f ? o / L : 0.0f;
-                    uint32_t bits = __float_as_uint(v);
-                    bits += 0x7fffu + ((bits >> 16) & 1u);
-                    P.out[(row * H + h) * (int64_t)kDv + d] = (uint16_t)(bits >> 16);
-                } else {
-                    P.part_o[(ps * H + h) * (int64_t)kDv + d] = o;
-                }
+        for (int j = 0; j < 32; ++j) {
+            const int h = hh0 + j;
+            if (h >= H) break;
+            const float o = __uint_as_float(r[j]);
+            if (single) {
+                const float L = s_l[h];
+                const float v = L > 0.0f ? o / L : 0.0f;
+                uint32_t bits = __float_as_uint(v);
+                bits += 0x7fffu + ((bits >> 16) & 1u);
+                P.out[(row * H + h) * (int64_t)kDv + d] = (uint16_t)(bits >> 16);
+            } else {
+                P.part_o[(ps * H + h) * (int64_t)kDv + d] = o;
             }
         }
     }

@@ -36,7 +36,9 @@ constexpr int kTile = 128;             // positions per tile (MMA M)
 constexpr int kStages = 8;
 constexpr int kThreads = 192;
 constexpr int kNPad = 32;              // MMA N: heads padded to 32
-constexpr uint32_t kTmemCols = 128;    // acc0 [0,32) acc1 [32,64) sfa0 [64,68) sfa1 [68,72) sfb [72,76)
+constexpr int kAcc = 3;                // accumulator stages in TMEM
+constexpr uint32_t kTmemCols = 128;    // acc k at [32k, 32k+32), sfa k at [96+4k, 100+4k), sfb at [108,112)
+constexpr uint32_t kColSfa = 96, kColSfb = 108;
 constexpr int kCtasPerSm = 3;
 constexpr int kSms = 152;
 
@@ -59,7 +61,7 @@ struct TcSmem {
     uint8_t b[kNPad * kRowBytes];              // q codes, same layout
     uint32_t sfa[kStages][kTile];              // scale-factor atoms of the K tiles
     uint32_t sfb[kTile];                       // scale-factor atom of q
-    uint64_t full[kStages], empty[kStages], accf[2], acce[2];
+    uint64_t full[kStages], empty[kStages], accf[kAcc], acce[kAcc], qready;
     float w[kNPad];
     int hmin[kNPad], hmax[kNPad];
     unsigned long long len;
@@ -102,10 +104,11 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
             tc::mbar_init(&S.full[s], 1 + 32);
             tc::mbar_init(&S.empty[s], 1 + 4);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kAcc; ++i) {
             tc::mbar_init(&S.accf[i], 1);
             tc::mbar_init(&S.acce[i], 4);
         }
+        tc::mbar_init(&S.qready, 1);
         S.abort_flag = 0;
         S.unsafe = 0;
         S.bad = 0;
@@ -119,40 +122,11 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
         tc::tmem_alloc(&S.tmem_base, kTmemCols);
         tc::tmem_relinquish();
     }
-    __syncthreads();
-
-    // ---- the query: MXFP4 codes into the B operand (64-byte swizzle), scale atom, stats
-    if (warp >= 2) {
-        const int kb = warp - 2;                              // this warp's 32-value block
-        const uint16_t *q = P.q + row * (int64_t)H * kD;
-        for (int h = 0; h < kNPad; ++h) {
-            float v = 0.0f;
-            if (h < H) v = __uint_as_float((uint32_t)q[h * kD + kb * 32 + lane] << 16);
-            const uint32_t amax_bits = __reduce_max_sync(0xffffffffu, __float_as_uint(v) & 0x7fffffffu);
-            const bool finite = amax_bits < 0x7f800000u;
-            const int X = mx_block_exponent(__uint_as_float(finite ? amax_bits : 0u));
-            const uint32_t c = e2m1_encode(v, pow2_neg(X));
-            const uint32_t c_hi = __shfl_down_sync(0xffffffffu, c, 1);
-            // row h, 16-byte chunk kb of the 64-byte row, XOR-swizzled by bits 1-2 of h%8
-            const int r8 = h & 7;
-            const int off = (h >> 3) * 512 + r8 * 64 + ((kb ^ ((r8 >> 1) & 3)) << 4);
-            if ((lane & 1) == 0) S.b[off + (lane >> 1)] = (uint8_t)(c | (c_hi << 4));
-            if (lane == 0) {
-                reinterpret_cast<uint8_t *>(S.sfb)[h * 16 + kb] = (uint8_t)(X + 127);
-                if (h < H && amax_bits != 0) {
-                    atomicMin(&S.hmin[h], X);
-                    atomicMax(&S.hmax[h], X);
-                }
-                if (h < H && !finite) dev_flag(P.d_status, CSA2_DEV_NONFINITE);
-            }
-        }
-        if (kb == 0) S.w[lane] = lane < H ? P.w[row * H + lane] : 0.0f;
-        tc::fence_proxy_async_smem();
-    }
-    // ---- valid candidates of this row (and pool checks)
+    // ---- valid candidates of this row (and pool checks): needed before streaming starts
     const int64_t n_vis = n_visible(P, row);
     const int32_t *pool = P.pool_mode ? P.pool + row * (int64_t)P.n_pool_blocks : nullptr;
     const int64_t n_blk_all = (P.n_keys + P.block - 1) / P.block;
+    __syncthreads();                                       // barrier init / len zero visible
     if (!P.pool_mode) {
         if (tid == 0) S.len = (unsigned long long)n_vis;
     } else {
@@ -171,20 +145,6 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
         if (part) atomicAdd(&S.len, part);
     }
     __syncthreads();
-    if (tid == 0) {
-        int span = 0, mn = 1 << 20, mx = -(1 << 20);
-        for (int h = 0; h < H; ++h) {
-            if (S.hmin[h] > S.hmax[h]) continue;              // all-zero head
-            span = max(span, S.hmax[h] - S.hmin[h]);
-            mn = min(mn, S.hmin[h]);
-            mx = max(mx, S.hmax[h]);
-        }
-        S.q_span = span;
-        S.q_min = mn;
-        S.q_max = mx;
-    }
-    __syncthreads();
-
     const int64_t len = (int64_t)S.len;
     if (blockIdx.x == 0 && tid == 0) {
         if (P.row_len) P.row_len[row] = (int32_t)len;
@@ -252,19 +212,22 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
     } else if (warp == 1) {
         // ================= MMA issuer
         if (lane == 0 && ntiles > 0) {
-            const uint32_t sfb_t = tmem + 72;
+            const uint32_t sfb_t = tmem + kColSfb;
+            if (!tc::mbar_wait(&S.qready, 0, &S.abort_flag)) S.abort_flag = 1;
+            tc::fence_proxy_async_smem();
             tc::tc_fence_after();
-            tc::tc_cp_32x128b_warpx4(sfb_t, tc::smem_desc(tc::smem_u32(S.sfb), 512, 128, tc::kSwizzleNone));
-            for (int i = 0; i < ntiles; ++i) {
-                const int s = i % kStages, acc = i & 1;
-                if (!tc::mbar_wait(&S.acce[acc], ((uint32_t)(i >> 1) & 1u) ^ 1u, &S.abort_flag) ||
+            if (!S.abort_flag)
+                tc::tc_cp_32x128b_warpx4(sfb_t, tc::smem_desc(tc::smem_u32(S.sfb), 512, 128, tc::kSwizzleNone));
+            for (int i = 0; i < ntiles && !S.abort_flag; ++i) {
+                const int s = i % kStages, acc = i % kAcc;
+                if (!tc::mbar_wait(&S.acce[acc], ((uint32_t)(i / kAcc) & 1u) ^ 1u, &S.abort_flag) ||
                     !tc::mbar_wait(&S.full[s], (uint32_t)(i / kStages) & 1u, &S.abort_flag)) {
                     S.abort_flag = 1;
                     break;
                 }
                 tc::fence_proxy_async_smem();
                 tc::tc_fence_after();
-                const uint32_t sfa_t = tmem + 64 + 4 * acc;
+                const uint32_t sfa_t = tmem + kColSfa + 4 * acc;
                 tc::tc_cp_32x128b_warpx4(sfa_t, tc::smem_desc(tc::smem_u32(S.sfa[s]), 512, 128,
                                                               tc::kSwizzleNone));
                 const uint32_t d_t = tmem + acc * kNPad;
@@ -280,13 +243,55 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
         }
         __syncwarp();
     } else {
-        // ================= epilogue: warp's TMEM lane quadrant
+        // ================= epilogue warps: first the query (B operand), then the scores
+        {
+            const int kb = warp - 2;                          // this warp's 32-value block
+            const uint16_t *q = P.q + row * (int64_t)H * kD;
+            for (int h = 0; h < kNPad; ++h) {
+                float v = 0.0f;
+                if (h < H) v = __uint_as_float((uint32_t)q[h * kD + kb * 32 + lane] << 16);
+                const uint32_t amax_bits = __reduce_max_sync(0xffffffffu, __float_as_uint(v) & 0x7fffffffu);
+                const bool finite = amax_bits < 0x7f800000u;
+                const int X = mx_block_exponent(__uint_as_float(finite ? amax_bits : 0u));
+                const uint32_t c = e2m1_encode(v, pow2_neg(X));
+                const uint32_t c_hi = __shfl_down_sync(0xffffffffu, c, 1);
+                // row h, 16-byte chunk kb of the 64-byte row, XOR-swizzled by bits 1-2 of h%8
+                const int r8 = h & 7;
+                const int off = (h >> 3) * 512 + r8 * 64 + ((kb ^ ((r8 >> 1) & 3)) << 4);
+                if ((lane & 1) == 0) S.b[off + (lane >> 1)] = (uint8_t)(c | (c_hi << 4));
+                if (lane == 0) {
+                    reinterpret_cast<uint8_t *>(S.sfb)[h * 16 + kb] = (uint8_t)(X + 127);
+                    if (h < H && amax_bits != 0) {
+                        atomicMin(&S.hmin[h], X);
+                        atomicMax(&S.hmax[h], X);
+                    }
+                    if (h < H && !finite) dev_flag(P.d_status, CSA2_DEV_NONFINITE);
+                }
+            }
+            if (kb == 0) S.w[lane] = lane < H ? P.w[row * H + lane] : 0.0f;
+            tc::fence_proxy_async_smem();
+            asm volatile("bar.sync 1, 128;" ::: "memory");   // the four epilogue warps
+            if (warp == 2 && lane == 0) {
+                int span = 0, mn = 1 << 20, mx = -(1 << 20);
+                for (int h = 0; h < H; ++h) {
+                    if (S.hmin[h] > S.hmax[h]) continue;      // all-zero head
+                    span = max(span, S.hmax[h] - S.hmin[h]);
+                    mn = min(mn, S.hmin[h]);
+                    mx = max(mx, S.hmax[h]);
+                }
+                S.q_span = span;
+                S.q_min = mn;
+                S.q_max = mx;
+                tc::mbar_arrive(&S.qready);
+            }
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+        }
         const int quad = warp & 3;
         const int m = quad * 32 + lane;
         const int q_span = S.q_span, q_min = S.q_min, q_max = S.q_max;
         for (int i = 0; i < ntiles; ++i) {
-            const int s = i % kStages, acc = i & 1;
-            if (!tc::mbar_wait(&S.accf[acc], (uint32_t)(i >> 1) & 1u, &S.abort_flag) ||
+            const int s = i % kStages, acc = i % kAcc;
+            if (!tc::mbar_wait(&S.accf[acc], (uint32_t)(i / kAcc) & 1u, &S.abort_flag) ||
                 !tc::mbar_wait(&S.full[s], (uint32_t)(i / kStages) & 1u, &S.abort_flag)) {
                 S.abort_flag = 1;
                 break;

@@ -45,6 +45,65 @@ __global__ void __launch_bounds__(256) quant_mxfp4_kernel(const void *__restrict
     }
 }
 
+// Vectorised variant: four lanes share a 32-value block, each lane converts 8 values
+// (one 16-byte bf16 load or two 16-byte f32 loads) and stores their 8 nibbles as one
+// 32-bit word.  Needs 16-byte aligned rows of x and 4-byte aligned rows of codes.
+template <bool BF16>
+__global__ void __launch_bounds__(256) quant_mxfp4_vec_kernel(const void *__restrict__ x, int64_t rows,
+                                                              int64_t cols, int64_t ldx,
+                                                              uint8_t *__restrict__ codes, int64_t ldc,
+                                                              uint8_t *__restrict__ scales, int64_t lds,
+                                                              uint32_t *d_status)
+{
+    const int64_t nblk_row = cols / 32;
+    const int64_t total = rows * nblk_row * 4;                 // lanes of work
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t total32 = (total + 31) & ~int64_t(31);
+    for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total32; t += stride) {
+        const bool act = t < total;
+        const int64_t grp = t >> 2;
+        const int sub = (int)(t & 3);
+        const int64_t r = act ? grp / nblk_row : 0, kb = act ? grp % nblk_row : 0;
+        float v[8];
+        if (act) {
+            if (BF16) {
+                const uint4 raw = *reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(x) +
+                                                                   r * ldx + kb * 32 + sub * 8);
+                const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    v[2 * i] = __uint_as_float(w[i] << 16);
+                    v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+                }
+            } else {
+                const float4 *src = reinterpret_cast<const float4 *>(static_cast<const float *>(x) +
+                                                                     r * ldx + kb * 32 + sub * 8);
+                const float4 a = src[0], b = src[1];
+                v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+                v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = 0.0f;
+        }
+        uint32_t amax = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) amax = max(amax, __float_as_uint(v[i]) & 0x7fffffffu);
+        amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        if (!act) continue;
+        const bool finite = amax < 0x7f800000u;
+        if (!finite && sub == 0) dev_flag(d_status, CSA2_DEV_NONFINITE);
+        const int X = mx_block_exponent(__uint_as_float(finite ? amax : 0u));
+        const float inv = pow2_neg(X);
+        uint32_t word = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) word |= e2m1_encode(v[i], inv) << (4 * i);
+        *reinterpret_cast<uint32_t *>(codes + r * ldc + kb * 16 + sub * 4) = word;
+        if (sub == 0) scales[r * lds + kb] = (uint8_t)(X + 127);
+    }
+}
+
 template <bool BF16>
 __global__ void __launch_bounds__(256) dequant_mxfp4_kernel(const uint8_t *__restrict__ codes,
                                                             int64_t ldc,
@@ -82,6 +141,19 @@ cudaError_t launch_quant_mxfp4(const void *x, bool x_bf16, int64_t rows, int64_t
                                uint32_t *d_status, cudaStream_t s)
 {
     if (rows == 0 || cols == 0) return cudaSuccess;
+    const size_t esz = x_bf16 ? 2 : 4;
+    const bool vec = ((uintptr_t)x % 16 == 0) && ((ldx * (int64_t)esz) % 16 == 0) &&
+                     ((uintptr_t)codes % 4 == 0) && (ldc % 4 == 0);
+    if (vec) {
+        const int grid = grid_for(rows * (cols / 32) * 4, 256);
+        if (x_bf16)
+            quant_mxfp4_vec_kernel<true><<<grid, 256, 0, s>>>(x, rows, cols, ldx, codes, ldc, scales,
+                                                              lds, d_status);
+        else
+            quant_mxfp4_vec_kernel<false><<<grid, 256, 0, s>>>(x, rows, cols, ldx, codes, ldc, scales,
+                                                               lds, d_status);
+        return cudaGetLastError();
+    }
     const int grid = grid_for(rows * (cols / 32), 8);
     if (x_bf16)
         quant_mxfp4_kernel<true><<<grid, 256, 0, s>>>(x, rows, cols, ldx, codes, ldc, scales, lds,

@@ -195,7 +195,7 @@ __device__ __forceinline__ uint32_t cl_block_excl_sum(uint32_t v, uint32_t *s_wa
 __global__ void __launch_bounds__(kClThreads) topk_cluster_kernel(const ClusterTopkArgs A)
 {
     extern __shared__ uint32_t s_keys[];
-    __shared__ uint32_t s_hist[kClBins];
+    __shared__ __align__(16) uint32_t s_hist[kClBins];
     __shared__ uint32_t s_warp[33];
     __shared__ uint32_t s_cnt[2];
     __shared__ uint32_t s_pick[2];
@@ -253,14 +253,23 @@ __global__ void __launch_bounds__(kClThreads) topk_cluster_kernel(const ClusterT
         cl.sync();
         // thread t owns bins nb-1-4t .. nb-4-4t (descending); cluster-wide totals
         uint32_t tot[4], sum = 0;
+        {
+            // all remote loads of this thread's four bins issued before any is consumed
+            const int bin0 = nb - 4 - 4 * tid;               // bins bin0 .. bin0+3
+            uint4 part[16];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int bin = nb - 1 - (4 * tid + j);
-            uint32_t v = 0;
-            if (bin >= 0)
-                for (int r = 0; r < CS; ++r) v += cl.map_shared_rank(s_hist, r)[bin];
-            tot[j] = v;
-            sum += v;
+            for (int r = 0; r < 16; ++r) {
+                part[r] = make_uint4(0, 0, 0, 0);
+                if (r < CS && bin0 >= 0)
+                    part[r] = *reinterpret_cast<const uint4 *>(cl.map_shared_rank(s_hist, r) + bin0);
+            }
+            uint4 t4 = make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+                t4.x += part[r].x; t4.y += part[r].y; t4.z += part[r].z; t4.w += part[r].w;
+            }
+            tot[0] = t4.w; tot[1] = t4.z; tot[2] = t4.y; tot[3] = t4.x;  // descending bins
+            sum = t4.x + t4.y + t4.z + t4.w;
         }
         uint32_t all;
         uint32_t c = cl_block_excl_sum(sum, s_warp, all);   // elements with a larger digit
@@ -280,16 +289,19 @@ __global__ void __launch_bounds__(kClThreads) topk_cluster_kernel(const ClusterT
     }
     const uint32_t tau = prefix, need = remaining;   // take `need` entries equal to tau
 
-    // counts of this slice, then what earlier CTAs of the cluster select
+    // counts of this slice, then what earlier CTAs of the cluster select.  Thread t owns the
+    // contiguous run [t*run, (t+1)*run) of the slice, so two block scans order everything.
+    const int run = (m + kClThreads - 1) / kClThreads;
+    const int r0 = min(tid * run, m), r1 = min(r0 + run, m);
     uint32_t n_gt = 0, n_eq = 0;
-    for (int i = tid; i < m; i += kClThreads) {
+    for (int i = r0; i < r1; ++i) {
         const uint32_t key = in_smem ? s_keys[i] : score_key(s[lo + i]);
         n_gt += key > tau;
         n_eq += key == tau;
     }
     uint32_t t_gt, t_eq;
-    cl_block_excl_sum(n_gt, s_warp, t_gt);
-    cl_block_excl_sum(n_eq, s_warp, t_eq);
+    const uint32_t gt_mine_before = cl_block_excl_sum(n_gt, s_warp, t_gt);
+    const uint32_t eq_mine_before = cl_block_excl_sum(n_eq, s_warp, t_eq);
     if (tid == 0) { s_cnt[0] = t_gt; s_cnt[1] = t_eq; }
     cl.sync();
     uint32_t gt_before = 0, eq_before = 0;
@@ -299,25 +311,26 @@ __global__ void __launch_bounds__(kClThreads) topk_cluster_kernel(const ClusterT
         eq_before += rc[1];
     }
     cl.sync();                                 // remote counts read: CTAs may now finish alone
-    uint32_t out_base = gt_before + min(eq_before, need);
-    uint32_t ties = eq_before;
-    for (int base = 0; base < m; base += kClThreads) {
-        const int i = base + tid;
-        uint32_t key = 0;
-        if (i < m) key = in_smem ? s_keys[i] : score_key(s[lo + i]);
-        const bool gt = i < m && key > tau;
-        const bool eq = i < m && key == tau;
-        uint32_t tot_eq, tot_sel;
-        const uint32_t eq_rank = ties + cl_block_excl_sum(eq ? 1u : 0u, s_warp, tot_eq);
-        const bool sel = gt || (eq && eq_rank < need);
-        const uint32_t sel_rank = out_base + cl_block_excl_sum(sel ? 1u : 0u, s_warp, tot_sel);
-        if (sel && sel_rank < (uint32_t)A.k) {
-            out[sel_rank] = (int32_t)cand_pos(pool_row, A.block, lo + i);
-            if (out_s) out_s[sel_rank] = s[lo + i];
+    // ties taken by this thread: the ones whose cluster-wide tie rank is below `need`
+    const uint32_t tie0 = eq_before + eq_mine_before;
+    const uint32_t take_eq = tie0 >= need ? 0u : min(n_eq, need - tie0);
+    uint32_t t_sel;
+    const uint32_t sel_before = cl_block_excl_sum(n_gt + take_eq, s_warp, t_sel);
+    uint32_t out_pos = gt_before + min(eq_before, need) + sel_before;
+    uint32_t ties = 0;
+    for (int i = r0; i < r1; ++i) {
+        const uint32_t key = in_smem ? s_keys[i] : score_key(s[lo + i]);
+        bool sel = key > tau;
+        if (key == tau) sel = ties++ < take_eq;
+        if (sel) {
+            if (out_pos < (uint32_t)A.k) {
+                out[out_pos] = (int32_t)cand_pos(pool_row, A.block, lo + i);
+                if (out_s) out_s[out_pos] = s[lo + i];
+            }
+            ++out_pos;
         }
-        ties += tot_eq;
-        out_base += tot_sel;
     }
+    (void)gt_mine_before;
 }
 
 int cluster_size_for(int64_t rows, int64_t n)

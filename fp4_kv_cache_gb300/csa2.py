@@ -97,6 +97,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
             lib.csa2_sparse_attn_workspace_size.argtypes = [ctypes.POINTER(AttnArgs)]
             lib.csa2_sparse_attn.restype = S
             lib.csa2_sparse_attn.argtypes = [ctypes.POINTER(AttnArgs), _P, _P, _P, sz, _P, _P]
+            lib.csa2_index_score_noalloc.restype = S
+            lib.csa2_index_score_noalloc.argtypes = [ctypes.POINTER(IndexArgs), _P, _P, _P, _P]
             _lib = lib
     return _lib
 
@@ -212,6 +214,14 @@ def csa2_index_score(args: IndexArgs, scores: torch.Tensor, row_len: torch.Tenso
     _check("csa2_index_score", lib.csa2_index_score(ctypes.byref(args), _ptr(scores),
                                                     _ptr(row_len), ws, wsb, _ptr(d_status),
                                                     _stream(stream)))
+
+
+def csa2_index_score_noalloc(args: IndexArgs, scores: torch.Tensor, row_len: torch.Tensor,
+                             d_status=None, stream=None):
+    """csa2_index_score without a workspace: scratch comes from the library's own static
+    device array (for callers that cannot allocate; see include/csa2.h)."""
+    _check("csa2_index_score_noalloc", load().csa2_index_score_noalloc(
+        ctypes.byref(args), _ptr(scores), _ptr(row_len), _ptr(d_status), _stream(stream)))
 
 
 def csa2_topk(scores: torch.Tensor, k: int, idx: torch.Tensor, row_len=None, pool_blocks=None,

@@ -213,6 +213,34 @@ CSA2_API size_t csa2_sparse_attn_workspace_size(const csa2_attn_args *a);
 CSA2_API csa2_status csa2_sparse_attn(const csa2_attn_args *a, uint16_t *out, float *lse, void *ws,
                              size_t ws_bytes, uint32_t *d_status, csa2_stream stream);
 
+/* ---------------------------------------------------------------------------------- */
+/* csa2_index_score_noalloc -- csa2_index_score for callers that cannot allocate device */
+/* memory.  The paper has no counterpart; this is a deployment convenience.             */
+/*                                                                                    */
+/* Who needs it: an inference server that splits all device memory into fixed pools at */
+/* start-up and forbids later allocations, a plug-in inside a framework that owns the    */
+/* allocator, or a decode loop that must not block on the allocator or risk running out */
+/* of memory mid-step.  Such callers cannot provide the workspace csa2_index_score asks  */
+/* for.  This call takes the same arguments minus the workspace and computes exactly    */
+/* what csa2_index_score computes.                                                      */
+/*                                                                                    */
+/* Scratch: a file-scope __device__ array of 65,536 32-bit words (256 KB), which every  */
+/* GPU that loads the library holds until the process exits.  A request whose workspace */
+/* (csa2_index_score_workspace_size) exceeds 256 KB is rejected with CSA2_ERR_WORKSPACE */
+/* before anything is launched; every valid request of this build fits.  The call makes */
+/* no cudaMalloc, cudaFree or other allocating call; it clears the scratch it needs with */
+/* cudaMemsetAsync on `stream`.                                                         */
+/*                                                                                    */
+/* The first call on a device (with that device current) looks up the array's device   */
+/* address with cudaGetSymbolAddress and caches it; make that first call before any     */
+/* stream capture on that device.  All calls on a device share the one array and it    */
+/* keeps the last call's contents: calls whose GPU work overlaps (concurrent streams)   */
+/* race on it, so serialise them.                                                       */
+/* ---------------------------------------------------------------------------------- */
+CSA2_API csa2_status csa2_index_score_noalloc(const csa2_index_args *a, float *scores,
+                                              int32_t *row_len, uint32_t *d_status,
+                                              csa2_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -201,7 +201,8 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
                     *dst = 0x7f7f7f7fu;
                 }
             }
-            tc::fence_proxy_async_smem();
+            // no proxy fence here: it would wait for this lane's copies in flight; the MMA
+            // thread fences after it has seen the stage complete
             tc::cp_async_mbar_arrive_noinc(&S.full[s]);
             ++issued;
         }
@@ -289,6 +290,9 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
         const int quad = warp & 3;
         const int m = quad * 32 + lane;
         const int q_span = S.q_span, q_min = S.q_min, q_max = S.q_max;
+        float wv[kNPad];
+#pragma unroll
+        for (int h = 0; h < kNPad; ++h) wv[h] = S.w[h];
         for (int i = 0; i < ntiles; ++i) {
             const int s = i % kStages, acc = i % kAcc;
             if (!tc::mbar_wait(&S.accf[acc], (uint32_t)(i / kAcc) & 1u, &S.abort_flag) ||
@@ -314,7 +318,7 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
                 for (int h = 0; h < kNPad; ++h) {
                     if (h < H) {
                         const float D = __uint_as_float(r[h]);
-                        sc = __fmaf_rn(S.w[h], D > 0.0f ? D : 0.0f, sc);
+                        sc = __fmaf_rn(wv[h], D > 0.0f ? D : 0.0f, sc);
                     }
                 }
                 const int e0 = (int)(sfw & 255u), e1 = (int)((sfw >> 8) & 255u);

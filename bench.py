@@ -35,6 +35,10 @@ from fp4_kv_cache_gb300 import synth  # noqa: E402
 METRIC = "CSA2 decode tokens/s per layer (Full mode, 64K ctx)"
 WORKLOAD = "full_decode_64k"
 L2_FLUSH_BYTES = 256 << 20
+# DRAM bytes (read + write) of one csa2_index_score tensor-core launch on this workload, from
+# the ncu capture summarised in profiles/index_score_tc_kernel_full_decode_64k.md; None
+# whenever the kernel has changed since that capture.
+INDEX_TRAFFIC_BYTES = 142_928_640 + 5_904_640
 
 
 def _peaks():
@@ -352,7 +356,7 @@ def run_gpu(args):
         "achieved_gbs_step": _step_bytes(w) / (ms_step * 1e-3) / 1e9,
         "roofline": {"bound": "hbm", "kernel": "csa2_index_score", "achieved": achieved,
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None,
+                     "frac": achieved / peak, "traffic": INDEX_TRAFFIC_BYTES,
                      "algorithmic_bytes": kb, "ms": ms_k},
         "e2e": {"value": tokens / (e2e_step * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_step},

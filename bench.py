@@ -38,7 +38,7 @@ L2_FLUSH_BYTES = 256 << 20
 # DRAM bytes (read + write) of one csa2_index_score tensor-core launch on this workload, from
 # the ncu capture summarised in profiles/index_score_tc_kernel_full_decode_64k.md; None
 # whenever the kernel has changed since that capture.
-INDEX_TRAFFIC_BYTES = 142_928_640 + 5_904_640
+INDEX_TRAFFIC_BYTES = None
 
 
 def _peaks():
@@ -226,6 +226,8 @@ def run_gpu(args):
                            dtype=torch.uint8, device=dev)
     ws_attn = torch.empty(max(1, lib.csa2_sparse_attn_workspace_size(ctypes.byref(aargs))),
                           dtype=torch.uint8, device=dev)
+    ws_topk = torch.empty(max(1, lib.csa2_topk_workspace_size(B * T, w.n_keys, w.topk)),
+                          dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
     # our kernels per step: 2 cache-write quantisers, indexer (tensor-core + exact re-score
@@ -245,7 +247,7 @@ def run_gpu(args):
         csa2.csa2_index_score(iargs, scores, row_len, st, workspace=ws_index)
         if k_ev:
             k_ev[2].record(stream)
-        csa2.csa2_topk(scores, w.topk, idx, row_len, d_status=st)
+        csa2.csa2_topk(scores, w.topk, idx, row_len, d_status=st, workspace=ws_topk)
         if k_ev:
             k_ev[3].record(stream)
         csa2.csa2_sparse_attn(aargs, out, lse, st, workspace=ws_attn)

@@ -127,6 +127,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
     __shared__ uint64_t s_bar;
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
+    __shared__ uint32_t s_lut[256];     // code byte -> bf16x2 of its two E2M1 values (scale 1)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t row = blockIdx.y;
@@ -140,6 +141,15 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
         s_abort = 0;
     }
     if (tid < kH) { s_m[tid] = -INFINITY; s_l[tid] = 0.0f; }
+    {
+        // bf16 of the E2M1 values: sign bit 15, and the magnitude exactly (all fit in bf16)
+        const uint32_t byte = (uint32_t)tid;
+        float lo = e2m1_mag(byte & 7u), hi = e2m1_mag((byte >> 4) & 7u);
+        if (byte & 8u) lo = -lo;
+        if (byte & 0x80u) hi = -hi;
+        const __nv_bfloat162 bb = __floats2bfloat162_rn(lo, hi);
+        s_lut[tid] = *reinterpret_cast<const uint32_t *>(&bb);
+    }
     if (warp == 0) {
         tc::tmem_alloc(&s_tmem, kTmemCols);
         tc::tmem_relinquish();
@@ -208,24 +218,43 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
 #pragma unroll
                 for (int i = 0; i < 9; ++i) {
                     const int blk = part * 9 + i;                 // 32-value block of the row
-                    const float sc = e8m0_value(sb[i]);
                     const uint32_t w4[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
                     const int c = blk >> 1;
                     uint8_t *base = sm + (c < 8 ? kOffK + c * kChunkBytes : kOffR);
+                    if (sb[i] >= 8u && sb[i] <= 250u) {
+                        // table value x 2^(e-127) in bf16: exact, every product stays normal
+                        const __nv_bfloat162 sc2 = __halves2bfloat162(
+                            __ushort_as_bfloat16((unsigned short)(sb[i] << 7)),
+                            __ushort_as_bfloat16((unsigned short)(sb[i] << 7)));
 #pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {             // 8 values -> one 16-byte piece
-                        uint32_t packed[4];
+                        for (int q4 = 0; q4 < 4; ++q4) {         // 8 values -> one 16-byte piece
+                            uint32_t packed[4];
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const uint32_t byte = (w4[q4] >> (8 * k)) & 0xffu;
-                            float lo = e2m1_mag(byte & 7u) * sc, hi = e2m1_mag((byte >> 4) & 7u) * sc;
-                            if (byte & 8u) lo = -lo;
-                            if (byte & 0x80u) hi = -hi;
-                            const __nv_bfloat162 bb = __floats2bfloat162_rn(lo, hi);
-                            packed[k] = *reinterpret_cast<const uint32_t *>(&bb);
+                            for (int k = 0; k < 4; ++k) {
+                                const uint32_t t = s_lut[(w4[q4] >> (8 * k)) & 0xffu];
+                                const __nv_bfloat162 v = __hmul2(*reinterpret_cast<const __nv_bfloat162 *>(&t), sc2);
+                                packed[k] = *reinterpret_cast<const uint32_t *>(&v);
+                            }
+                            *reinterpret_cast<uint4 *>(base + sw128(r, (blk & 1) * 4 + q4)) =
+                                make_uint4(packed[0], packed[1], packed[2], packed[3]);
                         }
-                        *reinterpret_cast<uint4 *>(base + sw128(r, (blk & 1) * 4 + q4)) =
-                            make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                    } else {
+                        const float sc = e8m0_value(sb[i]);
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            uint32_t packed[4];
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                const uint32_t byte = (w4[q4] >> (8 * k)) & 0xffu;
+                                float lo = e2m1_mag(byte & 7u) * sc, hi = e2m1_mag((byte >> 4) & 7u) * sc;
+                                if (byte & 8u) lo = -lo;
+                                if (byte & 0x80u) hi = -hi;
+                                const __nv_bfloat162 bb = __floats2bfloat162_rn(lo, hi);
+                                packed[k] = *reinterpret_cast<const uint32_t *>(&bb);
+                            }
+                            *reinterpret_cast<uint4 *>(base + sw128(r, (blk & 1) * 4 + q4)) =
+                                make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                        }
                     }
                 }
             } else if (src <= -2) {

@@ -248,9 +248,12 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
         {
             const int kb = warp - 2;                          // this warp's 32-value block
             const uint16_t *q = P.q + row * (int64_t)H * kD;
+            uint16_t qv[kNPad];                               // all loads in flight at once
+#pragma unroll
+            for (int h = 0; h < kNPad; ++h) qv[h] = h < H ? q[h * kD + kb * 32 + lane] : (uint16_t)0;
+#pragma unroll 4
             for (int h = 0; h < kNPad; ++h) {
-                float v = 0.0f;
-                if (h < H) v = __uint_as_float((uint32_t)q[h * kD + kb * 32 + lane] << 16);
+                const float v = __uint_as_float((uint32_t)qv[h] << 16);
                 const uint32_t amax_bits = __reduce_max_sync(0xffffffffu, __float_as_uint(v) & 0x7fffffffu);
                 const bool finite = amax_bits < 0x7f800000u;
                 const int X = mx_block_exponent(__uint_as_float(finite ? amax_bits : 0u));

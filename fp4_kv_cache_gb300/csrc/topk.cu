@@ -9,12 +9,9 @@
 // four 8-bit digit passes (most significant first) find the K-th key tau and how many
 // entries equal to tau must be taken; a final pass in index order emits every entry
 // above tau and the first `need` entries equal to tau, which yields ascending output.
-#include <cooperative_groups.h>
-
 #include "common.cuh"
 #include "internal.h"
 
-namespace cg = cooperative_groups;
 
 namespace csa2 {
 namespace {
@@ -53,17 +50,48 @@ __device__ __forceinline__ uint32_t block_excl_count(bool f, uint32_t *s_warp, u
     return r;
 }
 
-__global__ void __launch_bounds__(kTopkThreads)
-topk_radix_kernel(const float *__restrict__ scores, int64_t n, const int32_t *__restrict__ row_len,
-                  const int32_t *__restrict__ pool, int32_t block, int32_t k,
-                  int32_t *__restrict__ idx, float *__restrict__ out_scores)
+// Whole-row radix select by one CTA of kTopkThreads threads, reading the row from global
+// memory in four 8-bit digit passes.  The fallback of the group-max path for rows whose
+// candidates do not fit on chip (heavy ties), and the path for more than 2^31 rows.
+// Block-wide exclusive prefix sum of one value per thread (all threads must call).
+__device__ __forceinline__ uint32_t block_excl_count_sum(uint32_t v, uint32_t *s_warp, uint32_t &total)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const uint32_t w = lane < (int)(blockDim.x >> 5) ? s_warp[lane] : 0u;
+        uint32_t wi = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t t = __shfl_up_sync(0xffffffffu, wi, o);
+            if (lane >= o) wi += t;
+        }
+        s_warp[lane] = wi - w;
+        if (lane == 31) s_warp[32] = wi;
+    }
+    __syncthreads();
+    const uint32_t r = s_warp[warp] + incl - v;
+    total = s_warp[32];
+    __syncthreads();
+    return r;
+}
+
+__device__ void radix_select_row(const float *__restrict__ scores, int64_t n, const int32_t *__restrict__ row_len,
+                                 const int32_t *__restrict__ pool, int32_t block, int32_t k,
+                                 int32_t *__restrict__ idx, float *__restrict__ out_scores, int64_t row)
 {
     __shared__ uint32_t s_hist[256];
     __shared__ uint32_t s_warp[33];
     __shared__ uint32_t s_prefix, s_mask, s_remaining;
 
     const int tid = threadIdx.x, lane = tid & 31;
-    const int64_t row = blockIdx.x;
     int64_t len = row_len ? (int64_t)row_len[row] : n;
     len = len < 0 ? 0 : (len > n ? n : len);
     const float *s = scores + row * n;
@@ -140,238 +168,239 @@ topk_radix_kernel(const float *__restrict__ scores, int64_t n, const int32_t *__
     }
 }
 
-// ------------------------------------------------------------------ cluster radix select
-// One thread-block cluster per row.  CTA r of the cluster owns the contiguous slice r of
-// the row (kept as keys in shared memory when it fits).  Three digit passes of 11, 11 and
-// 10 bits: each CTA histograms its slice, the cluster sums the histograms through
-// distributed shared memory, and every CTA derives the same digit.  The final pass emits
-// the selected entries in position order: CTA r starts after everything earlier CTAs
-// selected, and takes ties in order until the cluster-wide quota is used up.
-constexpr int kClThreads = 512;
-constexpr int kClBins = 2048;
-constexpr int kClKeyCap = 24576;            // keys per CTA kept in shared memory (96 KB)
-
-struct ClusterTopkArgs {
-    const float *scores;
-    int64_t n;
-    const int32_t *row_len;
-    const int32_t *pool;
-    int32_t block, k;
-    int32_t *idx;
-    float *out_scores;
-    int64_t key_cap;     // keys of a slice that fit the launch's dynamic shared memory
-};
-
-// Block-wide exclusive prefix sum of one value per thread (kClThreads threads).
-__device__ __forceinline__ uint32_t cl_block_excl_sum(uint32_t v, uint32_t *s_warp, uint32_t &total)
+__global__ void __launch_bounds__(kTopkThreads)
+topk_radix_kernel(const float *__restrict__ scores, int64_t n, const int32_t *__restrict__ row_len,
+                  const int32_t *__restrict__ pool, int32_t block, int32_t k,
+                  int32_t *__restrict__ idx, float *__restrict__ out_scores)
 {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    uint32_t incl = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += t;
-    }
-    if (lane == 31) s_warp[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-        const uint32_t w = lane < kClThreads / 32 ? s_warp[lane] : 0u;
-        uint32_t wi = w;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t t = __shfl_up_sync(0xffffffffu, wi, o);
-            if (lane >= o) wi += t;
-        }
-        s_warp[lane] = wi - w;
-        if (lane == 31) s_warp[32] = wi;
-    }
-    __syncthreads();
-    const uint32_t r = s_warp[warp] + incl - v;
-    total = s_warp[32];
-    __syncthreads();
-    return r;
+    radix_select_row(scores, n, row_len, pool, block, k, idx, out_scores, blockIdx.x);
 }
 
-__global__ void __launch_bounds__(kClThreads) topk_cluster_kernel(const ClusterTopkArgs A)
+// ------------------------------------------------------------------ group-max select
+// Pass 1 (group_max_kernel): the largest key of every group of gs consecutive candidates.
+// Pass 2 (topk_gmax_kernel, one CTA per row): tau0 = the k-th largest group key.  Each of
+// those k groups holds an element >= tau0, so at least k elements are >= tau0 and every
+// element of the top-k is >= tau0; only groups whose key is >= tau0 can hold one.  Those
+// groups' elements >= tau0 are gathered on chip in position order, and an exact radix
+// select among them (key desc, position asc) gives the top-k, emitted in order.
+constexpr int kGThreads = 1024;
+constexpr int kGBins = 2048;
+constexpr int kGroupCap = 32768;        // group keys per row kept on chip
+constexpr int kCandCap = 8192;          // candidates per row kept on chip
+
+struct GSmem {
+    uint32_t hist[kGBins];
+    uint32_t warp[33];
+    uint32_t pick[2];
+    uint32_t total;
+    int overflow;
+};
+
+__global__ void __launch_bounds__(256) group_max_kernel(const float *__restrict__ scores, int64_t n,
+                                                        const int32_t *__restrict__ row_len, int64_t rows,
+                                                        int32_t gs, int64_t G, uint32_t *__restrict__ gkeys)
 {
-    extern __shared__ uint32_t s_keys[];
-    __shared__ __align__(16) uint32_t s_hist[kClBins];
-    __shared__ uint32_t s_warp[33];
-    __shared__ uint32_t s_cnt[2];
-    __shared__ uint32_t s_pick[2];
-    cg::cluster_group cl = cg::this_cluster();
-    const int rank = (int)cl.block_rank(), CS = (int)cl.num_blocks();
-    const int tid = threadIdx.x, lane = tid & 31;
-    const int64_t row = blockIdx.y;
-    int64_t len = A.row_len ? (int64_t)A.row_len[row] : A.n;
-    len = len < 0 ? 0 : (len > A.n ? A.n : len);
-    const float *s = A.scores + row * A.n;
-    const int32_t *pool_row = A.pool ? A.pool + row * (A.n / A.block) : nullptr;
-    int32_t *out = A.idx + row * (int64_t)A.k;
-    float *out_s = A.out_scores ? A.out_scores + row * (int64_t)A.k : nullptr;
-    const int64_t per = (len + CS - 1) / CS;
-    const int64_t lo = min((int64_t)rank * per, len), hi = min(lo + per, len);
-    const int m = (int)(hi - lo);
-
-    if (len <= A.k) {                          // everything competes and wins
-        for (int i = tid; i < m; i += kClThreads) {
-            out[lo + i] = (int32_t)cand_pos(pool_row, A.block, lo + i);
-            if (out_s) out_s[lo + i] = s[lo + i];
-        }
-        if (rank == CS - 1)
-            for (int64_t i = len + tid; i < A.k; i += kClThreads) {
-                out[i] = -1;
-                if (out_s) out_s[i] = 0.0f;
-            }
-        return;
+    const int lane = threadIdx.x & 31;
+    const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t w = warp0; w < rows * G; w += nwarps) {
+        const int64_t row = w / G, g = w % G;
+        int64_t len = row_len ? (int64_t)row_len[row] : n;
+        len = len < 0 ? 0 : (len > n ? n : len);
+        const float *s = scores + row * n;
+        uint32_t m = 0;
+        for (int64_t p = g * gs + lane; p < (g + 1) * gs && p < len; p += 32) m = max(m, score_key(s[p]));
+        m = __reduce_max_sync(0xffffffffu, m);
+        if (lane == 0) gkeys[row * G + g] = m;
     }
-    const bool in_smem = per <= A.key_cap;
-    if (in_smem)
-        for (int i = tid; i < m; i += kClThreads) s_keys[i] = score_key(s[lo + i]);
+}
 
-    uint32_t prefix = 0, mask = 0, remaining = (uint32_t)A.k;
+// Exact k-th largest key of n keys in shared memory (3 digit passes: 11, 11, 10 bits);
+// returns tau, and in need how many keys equal to tau belong to the top k.
+__device__ uint32_t g_threshold(const uint32_t *keys, int n, uint32_t k, GSmem &S, uint32_t &need)
+{
+    const int tid = threadIdx.x, lane = tid & 31;
+    uint32_t prefix = 0, mask = 0, remaining = k;
     const int shifts[3] = {21, 10, 0}, widths[3] = {11, 11, 10};
     for (int pass = 0; pass < 3; ++pass) {
         const int shift = shifts[pass], nb = 1 << widths[pass];
-        for (int i = tid; i < kClBins; i += kClThreads) s_hist[i] = 0;
+        for (int i = tid; i < kGBins; i += kGThreads) S.hist[i] = 0;
         __syncthreads();
-        for (int base = 0; base < m; base += kClThreads) {
+        for (int base = 0; base < n; base += kGThreads) {
             const int i = base + tid;
             uint32_t key = 0;
             bool act = false;
-            if (i < m) {
-                key = in_smem ? s_keys[i] : score_key(s[lo + i]);
+            if (i < n) {
+                key = keys[i];
                 act = (key & mask) == prefix;
             }
             const uint32_t am = __ballot_sync(0xffffffffu, act);
             if (act) {
                 const uint32_t digit = (key >> shift) & (uint32_t)(nb - 1);
                 const uint32_t peers = __match_any_sync(am, digit);
-                if (lane == __ffs(peers) - 1) atomicAdd(&s_hist[digit], (uint32_t)__popc(peers));
+                if (lane == __ffs(peers) - 1) atomicAdd(&S.hist[digit], (uint32_t)__popc(peers));
             }
         }
-        cl.sync();
-        // thread t owns bins nb-1-4t .. nb-4-4t (descending); cluster-wide totals
-        uint32_t tot[4], sum = 0;
-        {
-            // all remote loads of this thread's four bins issued before any is consumed
-            const int bin0 = nb - 4 - 4 * tid;               // bins bin0 .. bin0+3
-            uint4 part[16];
-#pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                part[r] = make_uint4(0, 0, 0, 0);
-                if (r < CS && bin0 >= 0)
-                    part[r] = *reinterpret_cast<const uint4 *>(cl.map_shared_rank(s_hist, r) + bin0);
-            }
-            uint4 t4 = make_uint4(0, 0, 0, 0);
-#pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                t4.x += part[r].x; t4.y += part[r].y; t4.z += part[r].z; t4.w += part[r].w;
-            }
-            tot[0] = t4.w; tot[1] = t4.z; tot[2] = t4.y; tot[3] = t4.x;  // descending bins
-            sum = t4.x + t4.y + t4.z + t4.w;
-        }
+        __syncthreads();
+        // thread t owns bins nb-1-2t and nb-2-2t (descending)
+        uint32_t t0 = 0, t1 = 0;
+        const int b0 = nb - 1 - 2 * tid;
+        if (b0 >= 0) t0 = S.hist[b0];
+        if (b0 - 1 >= 0) t1 = S.hist[b0 - 1];
         uint32_t all;
-        uint32_t c = cl_block_excl_sum(sum, s_warp, all);   // elements with a larger digit
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int bin = nb - 1 - (4 * tid + j);
-            if (bin >= 0 && c < remaining && c + tot[j] >= remaining) {
-                s_pick[0] = (uint32_t)bin;
-                s_pick[1] = remaining - c;
-            }
-            c += tot[j];
-        }
-        cl.sync();                             // histograms read everywhere before reuse
-        prefix |= s_pick[0] << shift;
+        uint32_t c = block_excl_count_sum(t0 + t1, S.warp, all);
+        if (b0 >= 0 && c < remaining && c + t0 >= remaining) { S.pick[0] = (uint32_t)b0; S.pick[1] = remaining - c; }
+        c += t0;
+        if (b0 - 1 >= 0 && c < remaining && c + t1 >= remaining) { S.pick[0] = (uint32_t)(b0 - 1); S.pick[1] = remaining - c; }
+        __syncthreads();
+        prefix |= S.pick[0] << shift;
         mask |= (uint32_t)(nb - 1) << shift;
-        remaining = s_pick[1];
+        remaining = S.pick[1];
+        __syncthreads();
     }
-    const uint32_t tau = prefix, need = remaining;   // take `need` entries equal to tau
+    need = remaining;
+    return prefix;
+}
 
-    // counts of this slice, then what earlier CTAs of the cluster select.  Thread t owns the
-    // contiguous run [t*run, (t+1)*run) of the slice, so two block scans order everything.
-    const int run = (m + kClThreads - 1) / kClThreads;
-    const int r0 = min(tid * run, m), r1 = min(r0 + run, m);
-    uint32_t n_gt = 0, n_eq = 0;
-    for (int i = r0; i < r1; ++i) {
-        const uint32_t key = in_smem ? s_keys[i] : score_key(s[lo + i]);
-        n_gt += key > tau;
-        n_eq += key == tau;
+__global__ void __launch_bounds__(kGThreads, 1)
+topk_gmax_kernel(const float *__restrict__ scores, int64_t n, const int32_t *__restrict__ row_len,
+                 const int32_t *__restrict__ pool, int32_t block, int32_t k, int32_t *__restrict__ idx,
+                 float *__restrict__ out_scores, const uint32_t *__restrict__ gkeys, int32_t gs, int64_t G)
+{
+    extern __shared__ uint32_t g_sm[];
+    uint32_t *s_g = g_sm;                                  // group keys, then candidate-group list
+    uint32_t *s_ck = g_sm + kGroupCap;                     // candidate keys
+    int32_t *s_cp = reinterpret_cast<int32_t *>(s_ck + kCandCap);   // candidate positions (index)
+    __shared__ GSmem S;
+    const int tid = threadIdx.x;
+    const int64_t row = blockIdx.x;
+    int64_t len = row_len ? (int64_t)row_len[row] : n;
+    len = len < 0 ? 0 : (len > n ? n : len);
+    const float *s = scores + row * n;
+    const int32_t *pool_row = pool ? pool + row * (n / block) : nullptr;
+    int32_t *out = idx + row * (int64_t)k;
+    float *out_s = out_scores ? out_scores + row * (int64_t)k : nullptr;
+
+    if (len <= k) {                                        // everything competes and wins
+        for (int64_t i = tid; i < k; i += kGThreads) {
+            out[i] = i < len ? (int32_t)cand_pos(pool_row, block, i) : -1;
+            if (out_s) out_s[i] = i < len ? s[i] : 0.0f;
+        }
+        return;
     }
-    uint32_t t_gt, t_eq;
-    const uint32_t gt_mine_before = cl_block_excl_sum(n_gt, s_warp, t_gt);
-    const uint32_t eq_mine_before = cl_block_excl_sum(n_eq, s_warp, t_eq);
-    if (tid == 0) { s_cnt[0] = t_gt; s_cnt[1] = t_eq; }
-    cl.sync();
-    uint32_t gt_before = 0, eq_before = 0;
-    for (int r = 0; r < rank; ++r) {
-        const uint32_t *rc = cl.map_shared_rank(s_cnt, r);
-        gt_before += rc[0];
-        eq_before += rc[1];
+    const int ng = (int)((len + gs - 1) / gs);
+    if (ng > kGroupCap) {                                  // too long for the on-chip path
+        radix_select_row(scores, n, row_len, pool, block, k, idx, out_scores, row);
+        return;
     }
-    cl.sync();                                 // remote counts read: CTAs may now finish alone
-    // ties taken by this thread: the ones whose cluster-wide tie rank is below `need`
-    const uint32_t tie0 = eq_before + eq_mine_before;
-    const uint32_t take_eq = tie0 >= need ? 0u : min(n_eq, need - tie0);
-    uint32_t t_sel;
-    const uint32_t sel_before = cl_block_excl_sum(n_gt + take_eq, s_warp, t_sel);
-    uint32_t out_pos = gt_before + min(eq_before, need) + sel_before;
-    uint32_t ties = 0;
-    for (int i = r0; i < r1; ++i) {
-        const uint32_t key = in_smem ? s_keys[i] : score_key(s[lo + i]);
-        bool sel = key > tau;
-        if (key == tau) sel = ties++ < take_eq;
-        if (sel) {
-            if (out_pos < (uint32_t)A.k) {
-                out[out_pos] = (int32_t)cand_pos(pool_row, A.block, lo + i);
-                if (out_s) out_s[out_pos] = s[lo + i];
+    for (int g = tid; g < ng; g += kGThreads) s_g[g] = gkeys[row * G + g];
+    if (tid == 0) S.overflow = 0;
+    __syncthreads();
+    uint32_t need0;
+    const uint32_t tau0 = ng > k ? g_threshold(s_g, ng, (uint32_t)k, S, need0) : 0u;
+
+    // candidate groups (key >= tau0), compacted in place in ascending order: thread t owns
+    // the run [t*run, (t+1)*run) and writes only below its own run after everyone has read
+    const int run = (ng + kGThreads - 1) / kGThreads;        // <= 32
+    const int r0 = min(tid * run, ng), r1 = min(r0 + run, ng);
+    uint32_t mine = 0;                                      // bit j: group r0+j is a candidate
+    for (int i = r0; i < r1; ++i) mine |= (s_g[i] >= tau0 ? 1u : 0u) << (i - r0);
+    uint32_t n_cg;
+    const uint32_t at = block_excl_count_sum((uint32_t)__popc(mine), S.warp, n_cg);
+    {
+        uint32_t o = at;
+        for (int i = r0; i < r1; ++i)
+            if ((mine >> (i - r0)) & 1u) s_g[o++] = (uint32_t)i;
+    }
+    __syncthreads();
+
+    // gather candidates: one thread per candidate group, its elements >= tau0, in order
+    uint32_t n_c = 0;
+    for (uint32_t base = 0; base < n_cg; base += kGThreads) {
+        const uint32_t j = base + tid;
+        // groups of 32 whose 32 scores lie inside the row buffer are read with eight 16-byte
+        // loads issued together; other groups element by element
+        uint32_t cnt = 0, sel = 0;
+        uint32_t kk[32];
+        int64_t g0 = 0;
+        const bool fast = gs == 32 && ((reinterpret_cast<uintptr_t>(s) & 15u) == 0);   // 16-byte rows
+        if (j < n_cg) {
+            g0 = (int64_t)s_g[j] * gs;
+            if (fast && g0 + 32 <= n) {
+                float4 f[8];
+                const float4 *src = reinterpret_cast<const float4 *>(s + g0);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) f[e] = src[e];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    kk[4 * e + 0] = score_key(f[e].x); kk[4 * e + 1] = score_key(f[e].y);
+                    kk[4 * e + 2] = score_key(f[e].z); kk[4 * e + 3] = score_key(f[e].w);
+                }
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    sel |= (kk[e] >= tau0 && g0 + e < len ? 1u : 0u) << e;
+                cnt = __popc(sel);
+            } else {
+                for (int e = 0; e < gs && g0 + e < len; ++e) cnt += score_key(s[g0 + e]) >= tau0;
             }
-            ++out_pos;
+        }
+        uint32_t tot;
+        uint32_t o = n_c + block_excl_count_sum(cnt, S.warp, tot);
+        if (n_c + tot > kCandCap) {                         // does not fit: fall back
+            if (tid == 0) S.overflow = 1;
+            break;
+        }
+        if (j < n_cg) {
+            if (fast && g0 + 32 <= n) {
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    if ((sel >> e) & 1u) { s_ck[o] = kk[e]; s_cp[o] = (int32_t)(g0 + e); ++o; }
+            } else {
+                for (int e = 0; e < gs && g0 + e < len; ++e) {
+                    const uint32_t key = score_key(s[g0 + e]);
+                    if (key >= tau0) { s_ck[o] = key; s_cp[o] = (int32_t)(g0 + e); ++o; }
+                }
+            }
+        }
+        n_c += tot;
+    }
+    __syncthreads();
+    if (S.overflow) {
+        radix_select_row(scores, n, row_len, pool, block, k, idx, out_scores, row);
+        return;
+    }
+    // exact selection among the candidates (n_c >= k), emitted in position order
+    uint32_t need;
+    const uint32_t tau = g_threshold(s_ck, (int)n_c, (uint32_t)k, S, need);
+    const int crun = ((int)n_c + kGThreads - 1) / kGThreads;
+    const int c0 = min(tid * crun, (int)n_c), c1 = min(c0 + crun, (int)n_c);
+    uint32_t n_gt = 0, n_eq = 0;
+    for (int i = c0; i < c1; ++i) {
+        n_gt += s_ck[i] > tau;
+        n_eq += s_ck[i] == tau;
+    }
+    uint32_t t_eq, t_sel;
+    const uint32_t eq_before = block_excl_count_sum(n_eq, S.warp, t_eq);
+    const uint32_t take = eq_before >= need ? 0u : min(n_eq, need - eq_before);
+    uint32_t o = block_excl_count_sum(n_gt + take, S.warp, t_sel);
+    uint32_t ties = 0;
+    for (int i = c0; i < c1; ++i) {
+        const uint32_t key = s_ck[i];
+        bool sel = key > tau;
+        if (key == tau) sel = ties++ < take;
+        if (sel && o < (uint32_t)k) {
+            out[o] = (int32_t)cand_pos(pool_row, block, s_cp[i]);
+            if (out_s) out_s[o] = s[s_cp[i]];
+            ++o;
         }
     }
-    (void)gt_mine_before;
 }
 
-int cluster_size_for(int64_t rows, int64_t n)
+int32_t group_size_for(int64_t n)
 {
-    int64_t want = (152 + rows - 1) / (rows > 0 ? rows : 1);          // about one CTA per SM
-    int64_t need = (n + kClKeyCap - 1) / kClKeyCap;                   // keep keys on chip
-    int64_t c = want > need ? want : need;
-    int64_t per_min = 2048;                                           // no tiny slices
-    int64_t cap = (n + per_min - 1) / per_min;
-    if (c > cap) c = cap;
-    int cs = 1;
-    while (cs < c && cs < 16) cs <<= 1;
-    return cs;
-}
-
-cudaError_t launch_topk_cluster(ClusterTopkArgs A, int64_t rows, cudaStream_t s)
-{
-    const int cs = cluster_size_for(rows, A.n);
-    const int64_t per = (A.n + cs - 1) / cs;          // slice of the longest possible row
-    const size_t smem = per <= kClKeyCap ? (size_t)(per > 0 ? per : 1) * sizeof(uint32_t) : 0;
-    A.key_cap = (int64_t)(smem / sizeof(uint32_t));
-    cudaError_t e = cudaFuncSetAttribute(topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)(kClKeyCap * sizeof(uint32_t)));
-    if (e != cudaSuccess) return e;
-    if (cs > 8) {
-        e = cudaFuncSetAttribute(topk_cluster_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        if (e != cudaSuccess) return e;
-    }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)cs, (unsigned)rows, 1);
-    cfg.blockDim = dim3(kClThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)cs;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, topk_cluster_kernel, A);
+    int32_t gs = 32;
+    while ((n + gs - 1) / gs > kGroupCap && gs < (1 << 20)) gs *= 2;
+    return gs;
 }
 
 // Block score = max over the block's valid positions (NaN ignored; all-NaN -> NaN).
@@ -396,28 +425,48 @@ __global__ void block_max_kernel(const float *__restrict__ scores, int64_t n,
 
 } // namespace
 
-size_t topk_ws_bytes(int64_t, int64_t, int32_t) { return 0; }
+size_t topk_ws_bytes(int64_t rows, int64_t n, int32_t)
+{
+    const int64_t G = (n + group_size_for(n) - 1) / group_size_for(n);
+    return (size_t)rows * (size_t)(G > 0 ? G : 1) * sizeof(uint32_t);
+}
 
 cudaError_t launch_topk(const float *scores, int64_t rows, int64_t n, const int32_t *row_len,
                         const int32_t *pool, int32_t block, int32_t k, int32_t *idx,
-                        float *out_scores, void *, uint32_t *, cudaStream_t s)
+                        float *out_scores, void *ws, uint32_t *, cudaStream_t s)
 {
     if (rows == 0 || k == 0) return cudaSuccess;
-    if (rows > 65535) {
+    if (rows > 0x7fffffffLL || !ws) {
         topk_radix_kernel<<<(unsigned)rows, kTopkThreads, 0, s>>>(scores, n, row_len, pool, block, k,
                                                                  idx, out_scores);
         return cudaGetLastError();
     }
-    ClusterTopkArgs A{scores, n, row_len, pool, block, k, idx, out_scores, 0};
-    return launch_topk_cluster(A, rows, s);
+    const int32_t gs = group_size_for(n);
+    const int64_t G = (n + gs - 1) / gs;
+    uint32_t *gkeys = static_cast<uint32_t *>(ws);
+    if (G > 0) {
+        int64_t blocks = (rows * G * 32 + 255) / 256;
+        if (blocks > 152 * 16) blocks = 152 * 16;
+        group_max_kernel<<<(unsigned)blocks, 256, 0, s>>>(scores, n, row_len, rows, gs, G, gkeys);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    const size_t smem = (size_t)(kGroupCap + 2 * kCandCap) * sizeof(uint32_t);
+    cudaError_t e = cudaFuncSetAttribute(topk_gmax_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    topk_gmax_kernel<<<(unsigned)rows, kGThreads, smem, s>>>(scores, n, row_len, pool, block, k, idx,
+                                                             out_scores, gkeys, gs, G);
+    return cudaGetLastError();
 }
 
-size_t block_candidates_ws_bytes(int64_t rows, int64_t n, int32_t block, int32_t)
+size_t block_candidates_ws_bytes(int64_t rows, int64_t n, int32_t block, int32_t nb)
 {
     const int64_t nbmax = (n + block - 1) / block;
     size_t a = (size_t)rows * (size_t)nbmax * sizeof(float);
     a = (a + 255) & ~(size_t)255;
-    return a + (size_t)rows * sizeof(int32_t);
+    a += (size_t)rows * sizeof(int32_t);
+    a = (a + 255) & ~(size_t)255;
+    return a + topk_ws_bytes(rows, nbmax, nb);
 }
 
 cudaError_t launch_block_candidates(const float *scores, int64_t rows, int64_t n,
@@ -437,8 +486,9 @@ cudaError_t launch_block_candidates(const float *scores, int64_t rows, int64_t n
                                                                         nbmax, bscores, brow_len);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    return launch_topk(bscores, rows, nbmax, brow_len, nullptr, 1, nb, block_ids, nullptr, nullptr,
-                       d_status, s);
+    const size_t off2 = (off + (size_t)rows * sizeof(int32_t) + 255) & ~(size_t)255;
+    return launch_topk(bscores, rows, nbmax, brow_len, nullptr, 1, nb, block_ids, nullptr,
+                       static_cast<char *>(ws) + off2, d_status, s);
 }
 
 } // namespace csa2

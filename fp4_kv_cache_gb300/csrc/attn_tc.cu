@@ -409,10 +409,10 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
 #pragma unroll
             for (int j = 0; j < 32; ++j) r[j] = 0u;
         }
-#pragma unroll 4
-        for (int j = 0; j < 32; ++j) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {              // fully unrolled: r stays in registers
             const int h = hh0 + j;
-            if (h >= H) break;
+            if (h >= H) continue;
             const float o = __uint_as_float(r[j]);
             if (single) {
                 const float L = s_l[h];

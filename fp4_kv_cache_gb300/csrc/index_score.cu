@@ -30,7 +30,8 @@ struct IndexParams {
     bool pool_mode;
     float *scores;
     int32_t *row_len;
-    const uint32_t *seg_flags;   // non-null: only segments flagged here are scored
+    const uint32_t *seg_flags;   // non-null: [rows, n_seg]; only flagged segments are scored
+    int64_t n_seg;
     uint32_t *d_status;
 };
 
@@ -61,7 +62,14 @@ __global__ void __launch_bounds__(kThreads) index_score_exact_kernel(IndexParams
     const int64_t row = blockIdx.y;
     const int64_t b = row / P.n_q;
     const int H = P.H;
-    if (P.seg_flags && P.seg_flags[row * gridDim.x + blockIdx.x] == 0u) return;
+    // segments this CTA scores: its own (blockIdx.x), or with seg_flags every flagged
+    // segment of the row (one CTA per row; it returns at once when none is flagged)
+    const int64_t n_seg = P.seg_flags ? P.n_seg : 1;
+    if (P.seg_flags) {
+        int any = 0;
+        for (int64_t i = tid; i < n_seg; i += kThreads) any |= P.seg_flags[row * n_seg + i] != 0u;
+        if (!__syncthreads_or(any)) return;
+    }
 
     for (int i = tid; i < 256; i += kThreads)
         s_lut[i] = (uint16_t)((e2m1_twice(i & 15u) & 0xff) | ((e2m1_twice(i >> 4) & 0xff) << 8));
@@ -114,9 +122,12 @@ __global__ void __launch_bounds__(kThreads) index_score_exact_kernel(IndexParams
         if (s_bad) dev_flag(P.d_status, CSA2_DEV_BAD_POOL);
     }
 
-    const int64_t c0 = (int64_t)blockIdx.x * P.chunk;
-    const int64_t c1 = min(c0 + P.chunk, len);
     const int64_t kbase = b * P.n_keys;
+    for (int64_t seg = 0; seg < n_seg; ++seg) {
+    const int64_t seg_id = P.seg_flags ? seg : (int64_t)blockIdx.x;
+    if (P.seg_flags && P.seg_flags[row * n_seg + seg] == 0u) continue;
+    const int64_t c0 = seg_id * P.chunk;
+    const int64_t c1 = min(c0 + P.chunk, len);
     for (int64_t cand = c0 + tid; cand < c1; cand += kThreads) {
         int64_t pos = cand;
         if (P.pool_mode) {
@@ -160,6 +171,7 @@ __global__ void __launch_bounds__(kThreads) index_score_exact_kernel(IndexParams
         }
         P.scores[row * P.n_cand + cand] = s;
     }
+    }
 }
 
 } // namespace
@@ -197,7 +209,8 @@ cudaError_t launch_index_exact(const csa2_index_args &a, float *scores, int32_t 
     }
     P.chunk = chunk;
     int64_t gx = (P.n_cand + chunk - 1) / chunk;
-    dim3 grid((unsigned)(gx > 0 ? gx : 1), (unsigned)rows);
+    P.n_seg = gx > 0 ? gx : 1;
+    dim3 grid(seg_flags ? 1u : (unsigned)(gx > 0 ? gx : 1), (unsigned)rows);
     switch (a.head_dim) {
     case 32: index_score_exact_kernel<32><<<grid, kThreads, 0, s>>>(P); break;
     case 64: index_score_exact_kernel<64><<<grid, kThreads, 0, s>>>(P); break;

@@ -251,8 +251,8 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
             uint16_t qv[kNPad];                               // all loads in flight at once
 #pragma unroll
             for (int h = 0; h < kNPad; ++h) qv[h] = h < H ? q[h * kD + kb * 32 + lane] : (uint16_t)0;
-#pragma unroll 4
-            for (int h = 0; h < kNPad; ++h) {
+#pragma unroll
+            for (int h = 0; h < kNPad; ++h) {       // fully unrolled: qv stays in registers
                 const float v = __uint_as_float((uint32_t)qv[h] << 16);
                 const uint32_t amax_bits = __reduce_max_sync(0xffffffffu, __float_as_uint(v) & 0x7fffffffu);
                 const bool finite = amax_bits < 0x7f800000u;

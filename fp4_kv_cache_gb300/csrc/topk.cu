@@ -196,6 +196,33 @@ struct GSmem {
     int overflow;
 };
 
+// One thread per group of 32 whose row starts 16-byte aligned: eight 16-byte loads in
+// flight at once, no cross-lane work.
+__global__ void __launch_bounds__(256) group_max32_kernel(const float *__restrict__ scores, int64_t n,
+                                                          const int32_t *__restrict__ row_len, int64_t rows,
+                                                          int64_t G, uint32_t *__restrict__ gkeys)
+{
+    const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= rows * G) return;
+    const int64_t row = t / G, g = t % G;
+    int64_t len = row_len ? (int64_t)row_len[row] : n;
+    len = len < 0 ? 0 : (len > n ? n : len);
+    const int64_t p0 = g * 32;
+    uint32_t m = 0;
+    if (p0 + 32 <= len) {
+        const float4 *src = reinterpret_cast<const float4 *>(scores + row * n + p0);
+        float4 f[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[e] = src[e];
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            m = max(max(max(m, score_key(f[e].x)), score_key(f[e].y)), max(score_key(f[e].z), score_key(f[e].w)));
+    } else {
+        for (int64_t p = p0; p < p0 + 32 && p < len; ++p) m = max(m, score_key(scores[row * n + p]));
+    }
+    gkeys[t] = m;
+}
+
 __global__ void __launch_bounds__(256) group_max_kernel(const float *__restrict__ scores, int64_t n,
                                                         const int32_t *__restrict__ row_len, int64_t rows,
                                                         int32_t gs, int64_t G, uint32_t *__restrict__ gkeys)
@@ -445,9 +472,14 @@ cudaError_t launch_topk(const float *scores, int64_t rows, int64_t n, const int3
     const int64_t G = (n + gs - 1) / gs;
     uint32_t *gkeys = static_cast<uint32_t *>(ws);
     if (G > 0) {
-        int64_t blocks = (rows * G * 32 + 255) / 256;
-        if (blocks > 152 * 16) blocks = 152 * 16;
-        group_max_kernel<<<(unsigned)blocks, 256, 0, s>>>(scores, n, row_len, rows, gs, G, gkeys);
+        if (gs == 32 && ((uintptr_t)scores % 16) == 0 && n % 4 == 0) {
+            const int64_t blocks = (rows * G + 255) / 256;
+            group_max32_kernel<<<(unsigned)blocks, 256, 0, s>>>(scores, n, row_len, rows, G, gkeys);
+        } else {
+            int64_t blocks = (rows * G * 32 + 255) / 256;
+            if (blocks > 152 * 16) blocks = 152 * 16;
+            group_max_kernel<<<(unsigned)blocks, 256, 0, s>>>(scores, n, row_len, rows, gs, G, gkeys);
+        }
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

@@ -231,16 +231,26 @@ def run_gpu(args):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
     # our kernels per step: 2 cache-write quantisers, indexer (tensor-core + exact re-score
-    # of flagged segments), Top-K, attention (+ split combine)
+    # of flagged segments), Top-K (group maxima + select), attention
     launches_per_step = 7
 
+    side = torch.cuda.Stream(dev)
+
     def step(k_ev=None):
-        # k_ev: events bracketing each call of the step (cache write, indexer, Top-K, attention)
+        # k_ev: events bracketing each call of the step (indexer-K write, indexer, Top-K,
+        # attention).  The main-KV row write only feeds attention, so it runs on a side
+        # stream, overlapped with the indexer and Top-K.
         stream = torch.cuda.current_stream(dev)       # the capture stream while capturing
+        fork = torch.cuda.Event()
+        fork.record(stream)
+        side.wait_event(fork)
+        with torch.cuda.stream(side):
+            csa2.csa2_quant_fp4(new_kv, new_kvc, new_kvs, st, stream=side)
+        kv_done = torch.cuda.Event()
+        kv_done.record(side)
         if k_ev:
             k_ev[0].record(stream)
-        # cache write: the new token's main-KV and indexer-K rows, quantised in place
-        csa2.csa2_quant_fp4(new_kv, new_kvc, new_kvs, st)
+        # cache write: the new token's indexer-K row, quantised in place
         csa2.csa2_quant_fp4(new_k, new_kc, new_ks, st)
         if k_ev:
             k_ev[1].record(stream)
@@ -250,6 +260,7 @@ def run_gpu(args):
         csa2.csa2_topk(scores, w.topk, idx, row_len, d_status=st, workspace=ws_topk)
         if k_ev:
             k_ev[3].record(stream)
+        stream.wait_event(kv_done)
         csa2.csa2_sparse_attn(aargs, out, lse, st, workspace=ws_attn)
         if k_ev:
             k_ev[4].record(stream)

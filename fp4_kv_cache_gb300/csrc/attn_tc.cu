@@ -13,9 +13,12 @@
 // V^T for O^T, so the latent is never transposed.  S^T (64 columns) and O^T (4 x 64
 // columns) accumulate in tensor memory.  Softmax runs with one thread per key: per-head
 // maxima and sums are reduced across the 128 threads with a halving shuffle reduction.
+// The softmax runs in base 2: logits are scaled by sm_scale * log2(e), so every exponential
+// is one exp2f, and lse = m * ln 2 + log(l).
 // A CTA covers a contiguous span of tiles of one query row with an online softmax; when
-// a row is split over several CTAs, each writes (O, m, l) partials and a combine kernel
-// merges them.
+// a row is split over several CTAs, they form one thread-block cluster and merge their
+// (O, m, l) partials through distributed shared memory.  Each thread holds the next tile's FP4 half-row in
+// registers while the current tile is multiplied, so the gather latency overlaps the MMAs.
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -34,10 +37,14 @@ constexpr int kChunks = kDqk / 64;    // 9 chunks of 64 dims
 constexpr int kChunkBytes = kKeys * 128;          // 16 KB: 128 keys x 64 bf16
 constexpr int kQChunkBytes = kH * 128;            // 8 KB: 64 heads x 64 bf16
 constexpr uint32_t kTmemCols = 512;   // S^T [0,64), O^T block m at [64 + 64m, 128 + 64m)
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr int kMaxSplits = 7;          // CTAs (one cluster) per split row
+constexpr int kRecvRow = kH + 4;       // floats per received O^T row (padding against bank conflicts)
+constexpr int kRecvBytes = kKeys * kRecvRow * 4;   // one received 128-dim O^T block
 
 struct AttnTcParams {
     int32_t T, H, topk, window, n_swa, splits, tiles_per_split;
-    float sm_scale;
+    float log2_scale;       // logit scale x log2(e): the softmax runs in base 2
     int64_t n_kv;
     const uint16_t *q;
     const uint8_t *kvc, *kvs;
@@ -46,8 +53,6 @@ struct AttnTcParams {
     const int32_t *swa_pos0, *swa_start, *q_pos;
     uint16_t *out;
     float *lse;
-    float *part_o;    // [rows, splits, H, d_v] (splits > 1)
-    float *part_ml;   // [rows, splits, H, 2]
     uint32_t *d_status;
 };
 
@@ -60,6 +65,34 @@ constexpr int kSmemBytes = kOffQ + kChunks * kQChunkBytes; // 221184
 __device__ __forceinline__ int sw128(int row, int piece)   // byte offset of 16-byte piece
 {
     return (row >> 3) * 1024 + (row & 7) * 128 + ((piece ^ (row & 7)) << 4);
+}
+
+__device__ __forceinline__ uint16_t bf16_bits(float v)    // round to nearest even
+{
+    uint32_t bits = __float_as_uint(v);
+    bits += 0x7fffu + ((bits >> 16) & 1u);
+    return (uint16_t)(bits >> 16);
+}
+
+// distributed shared memory: the same shared-memory offset in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t map_peer(uint32_t local, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v)
+{
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+{
+    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ uint32_t f16_idesc(int a_mn)
@@ -121,12 +154,13 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    __shared__ int64_t s_src[kKeys];
     __shared__ float s_red[4][kH];
     __shared__ float s_m[kH], s_l[kH], s_corr[kH];
     __shared__ uint64_t s_bar;
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
+    __shared__ float s_mlx[kMaxSplits][2][kH];   // split row: every rank's (m, l) per head
+    __shared__ float s_fac[kMaxSplits][kH];      // split row: e^(m_s - M)
     __shared__ uint32_t s_lut[256];     // code byte -> bf16x2 of its two E2M1 values (scale 1)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -134,6 +168,19 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
     const int split = blockIdx.x;
     const int64_t b = row / P.T;
     const int H = P.H;
+    const int quad = warp & 3, hh0 = 32 * (warp >> 2);   // TMEM lane quadrant, first head
+    const int key_row = 32 * quad + lane;                 // this thread's key / dim row
+    const int part = tid >> 7;                            // which half of the key row it gathers
+    const int t_begin = split * P.tiles_per_split;
+    // index entry of slot `key_row` of a tile (idx slots come first; 0 past them)
+    auto slot_id = [&](int tile) -> int32_t {
+        const int64_t sl = (int64_t)tile * kKeys + key_row;
+        return sl < P.topk ? P.idx[row * P.topk + sl] : 0;
+    };
+    // the first two tiles' index entries are read before anything else, so their latency
+    // overlaps the set-up below
+    const int32_t id_first = slot_id(t_begin);
+    int32_t id_next = slot_id(t_begin + 1);
 
     if (tid == 0) {
         tc::mbar_init(&s_bar, 1);
@@ -178,51 +225,65 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
     }
     const int64_t n_slots = P.topk + n_sw;
     const int n_tiles = (int)((n_slots + kKeys - 1) / kKeys);
-    const int t_begin = split * P.tiles_per_split;
     const int t_end = min(t_begin + P.tiles_per_split, n_tiles);
     __syncthreads();
     const uint32_t tmem = s_tmem;
     uint32_t phase = 0;
     bool any_o = false;
 
-    const int quad = warp & 3, hh0 = 32 * (warp >> 2);   // TMEM lane quadrant, first head
-    const int key_row = 32 * quad + lane;                 // this thread's key / dim row
-    for (int tile = t_begin; tile < t_end; ++tile) {
-        // ---- slot -> source
-        if (tid < kKeys) {
-            const int64_t sl = (int64_t)tile * kKeys + tid;
-            int64_t src = -1;
-            if (sl < P.topk) {
-                const int32_t id = P.idx[row * P.topk + sl];
-                if (id >= 0 && id < P.n_kv) src = id;
-                else if (id != -1) dev_flag(P.d_status, CSA2_DEV_BAD_INDEX);
-            } else if (sl < n_slots) {
-                src = -(j0 + (sl - P.topk) + 2);
-            }
-            s_src[tid] = src;
+    // Key slot `key_row` of a tile: idx entries first, then the SWA window.  Returns the
+    // main-KV row (>= 0), -(SWA slot + 2), or -1 for an empty slot.
+    auto slot_src = [&](int tile, int32_t id) -> int64_t {
+        const int64_t sl = (int64_t)tile * kKeys + key_row;
+        if (sl < P.topk) {
+            if (id >= 0 && id < P.n_kv) return id;
+            if (id != -1) dev_flag(P.d_status, CSA2_DEV_BAD_INDEX);
+            return -1;
         }
-        __syncthreads();
-        // ---- gather + dequantise: threads r and r+128 take the two halves of key row r
+        return sl < n_slots ? -(j0 + (sl - P.topk) + 2) : -1;
+    };
+    // Registers carry the next tile's FP4 half-row while the current tile computes; SWA rows
+    // (bf16, 4x the bytes) are pulled into L2 a tile ahead and copied with cp.async.
+    uint4 raw[9];
+    uint32_t sb[9];
+    auto issue = [&](int64_t src) {
+        if (src >= 0) {
+            const uint8_t *codes = P.kvc + (b * P.n_kv + src) * (kDqk / 2) + part * 9 * 16;
+            const uint8_t *scl = P.kvs + (b * P.n_kv + src) * (kDqk / 32) + part * 9;
+#pragma unroll
+            for (int i = 0; i < 9; ++i) raw[i] = *reinterpret_cast<const uint4 *>(codes + i * 16);
+#pragma unroll
+            for (int i = 0; i < 9; ++i) sb[i] = scl[i];
+        } else if (src <= -2) {
+            const char *srow = reinterpret_cast<const char *>(P.swa + (b * P.n_swa + (-src - 2)) * (int64_t)kDqk);
+#pragma unroll
+            for (int i = 0; i < 5; ++i)
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(srow + part * 576 + i * 128));
+        }
+    };
+    int64_t src_cur = -1;
+    if (t_begin < t_end) {
+        src_cur = slot_src(t_begin, id_first);
+        issue(src_cur);
+    }
+    for (int tile = t_begin; tile < t_end; ++tile) {
+        // ---- dequantise the staged half-row into the key chunks (threads r and r+128 take
+        //      the two halves of key row r)
         {
-            const int r = tid & (kKeys - 1), part = tid >> 7;
-            const int64_t src = s_src[r];
+            const int r = key_row;
+            const int64_t src = src_cur;
             if (src >= 0) {
-                const uint8_t *codes = P.kvc + (b * P.n_kv + src) * (kDqk / 2) + part * 9 * 16;
-                const uint8_t *scl = P.kvs + (b * P.n_kv + src) * (kDqk / 32) + part * 9;
-                uint4 raw[9];
-                uint32_t sb[9];
+                bool fast = true;
 #pragma unroll
-                for (int i = 0; i < 9; ++i) raw[i] = *reinterpret_cast<const uint4 *>(codes + i * 16);
+                for (int i = 0; i < 9; ++i) fast = fast && sb[i] >= 8u && sb[i] <= 250u;
+                if (fast) {
+                    // table value x 2^(e-127) in bf16: exact, every product stays normal
 #pragma unroll
-                for (int i = 0; i < 9; ++i) sb[i] = scl[i];
-#pragma unroll
-                for (int i = 0; i < 9; ++i) {
-                    const int blk = part * 9 + i;                 // 32-value block of the row
-                    const uint32_t w4[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
-                    const int c = blk >> 1;
-                    uint8_t *base = sm + (c < 8 ? kOffK + c * kChunkBytes : kOffR);
-                    if (sb[i] >= 8u && sb[i] <= 250u) {
-                        // table value x 2^(e-127) in bf16: exact, every product stays normal
+                    for (int i = 0; i < 9; ++i) {
+                        const int blk = part * 9 + i;             // 32-value block of the row
+                        const uint32_t w4[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+                        const int c = blk >> 1;
+                        uint8_t *base = sm + (c < 8 ? kOffK + c * kChunkBytes : kOffR);
                         const __nv_bfloat162 sc2 = __halves2bfloat162(
                             __ushort_as_bfloat16((unsigned short)(sb[i] << 7)),
                             __ushort_as_bfloat16((unsigned short)(sb[i] << 7)));
@@ -238,8 +299,20 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
                             *reinterpret_cast<uint4 *>(base + sw128(r, (blk & 1) * 4 + q4)) =
                                 make_uint4(packed[0], packed[1], packed[2], packed[3]);
                         }
-                    } else {
-                        const float sc = e8m0_value(sb[i]);
+                    }
+                } else {
+                    // a scale outside [2^-119, 2^123] (rare): exact float products, one block
+                    // at a time with the codes read again, so this path stays small
+                    const uint8_t *codes = P.kvc + (b * P.n_kv + src) * (kDqk / 2) + part * 9 * 16;
+                    const uint8_t *scl = P.kvs + (b * P.n_kv + src) * (kDqk / 32) + part * 9;
+#pragma unroll 1
+                    for (int i = 0; i < 9; ++i) {
+                        const int blk = part * 9 + i;
+                        const uint4 rw = *reinterpret_cast<const uint4 *>(codes + i * 16);
+                        const uint32_t w4[4] = {rw.x, rw.y, rw.z, rw.w};
+                        const int c = blk >> 1;
+                        uint8_t *base = sm + (c < 8 ? kOffK + c * kChunkBytes : kOffR);
+                        const float sc = e8m0_value(scl[i]);
 #pragma unroll
                         for (int q4 = 0; q4 < 4; ++q4) {
                             uint32_t packed[4];
@@ -272,6 +345,13 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
                 }
             }
         }
+        const bool valid = src_cur != -1;
+        // ---- stage the next tile (its index was read one tile earlier)
+        if (tile + 1 < t_end) {
+            src_cur = slot_src(tile + 1, id_next);
+            issue(src_cur);
+            id_next = tile + 2 < t_end ? slot_id(tile + 2) : 0;
+        }
         cp_async_wait_all();
         tc::fence_proxy_async_smem();
         __syncthreads();
@@ -300,10 +380,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
             uint32_t r[32];
             tc::tc_ld_32x32b_x32(tmem + ((uint32_t)(quad * 32) << 16) + hh0, r);
             tc::tc_wait_ld();
-            const bool valid = s_src[key_row] != -1;
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-                l[j] = (valid && hh0 + j < H) ? __uint_as_float(r[j]) * P.sm_scale : -INFINITY;
+                l[j] = (valid && hh0 + j < H) ? __uint_as_float(r[j]) * P.log2_scale : -INFINITY;
         }
         {
             float v[32];
@@ -316,12 +395,12 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
             const float tmax = fmaxf(fmaxf(s_red[0][tid], s_red[1][tid]), fmaxf(s_red[2][tid], s_red[3][tid]));
             const float m_old = s_m[tid];
             const float m_new = fmaxf(m_old, tmax);
-            s_corr[tid] = (m_old == -INFINITY) ? 0.0f : expf(m_old - m_new);
+            s_corr[tid] = (m_old == -INFINITY) ? 0.0f : exp2f(m_old - m_new);
             s_m[tid] = m_new;
         }
         __syncthreads();
 #pragma unroll
-        for (int j = 0; j < 32; ++j) l[j] = (l[j] == -INFINITY) ? 0.0f : expf(l[j] - s_m[hh0 + j]);
+        for (int j = 0; j < 32; ++j) l[j] = (l[j] == -INFINITY) ? 0.0f : exp2f(l[j] - s_m[hh0 + j]);
         {
             float v[32];
 #pragma unroll
@@ -396,41 +475,120 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
     }
 
     // ---- epilogue: thread = (dim row of each O^T block, 32 heads)
-    const bool single = P.splits == 1;
-    const int64_t ps = row * P.splits + split;
+    if (P.splits == 1) {
+        if (tid < kH) s_corr[tid] = s_l[tid] > 0.0f ? 1.0f / s_l[tid] : 0.0f;   // 1/l per head
+        __syncthreads();
 #pragma unroll 1
-    for (int m = 0; m < 4; ++m) {
-        const int d = 128 * m + key_row;
-        uint32_t r[32];
-        if (any_o) {
-            tc::tc_ld_32x32b_x32(tmem + ((uint32_t)(quad * 32) << 16) + 64 + 64 * m + hh0, r);
-            tc::tc_wait_ld();
-        } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) r[j] = 0u;
-        }
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {              // fully unrolled: r stays in registers
-            const int h = hh0 + j;
-            if (h >= H) continue;
-            const float o = __uint_as_float(r[j]);
-            if (single) {
-                const float L = s_l[h];
-                const float v = L > 0.0f ? o / L : 0.0f;
-                uint32_t bits = __float_as_uint(v);
-                bits += 0x7fffu + ((bits >> 16) & 1u);
-                P.out[(row * H + h) * (int64_t)kDv + d] = (uint16_t)(bits >> 16);
+        for (int m = 0; m < 4; ++m) {
+            const int d = 128 * m + key_row;
+            uint32_t r[32];
+            if (any_o) {
+                tc::tc_ld_32x32b_x32(tmem + ((uint32_t)(quad * 32) << 16) + 64 + 64 * m + hh0, r);
+                tc::tc_wait_ld();
             } else {
-                P.part_o[(ps * H + h) * (int64_t)kDv + d] = o;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) r[j] = 0u;
+            }
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {          // fully unrolled: r stays in registers
+                const int h = hh0 + j;
+                if (h >= H) continue;
+                P.out[(row * H + h) * (int64_t)kDv + d] = bf16_bits(__uint_as_float(r[j]) * s_corr[h]);
             }
         }
-    }
-    if (tid < H) {
-        if (single) {
-            if (P.lse) P.lse[row * H + tid] = s_l[tid] > 0.0f ? s_m[tid] + logf(s_l[tid]) : -INFINITY;
-        } else {
-            P.part_ml[(ps * H + tid) * 2 + 0] = s_m[tid];
-            P.part_ml[(ps * H + tid) * 2 + 1] = s_l[tid];
+        if (tid < H && P.lse) P.lse[row * H + tid] = s_l[tid] > 0.0f ? s_m[tid] * kLn2 + logf(s_l[tid]) : -INFINITY;
+    } else {
+        // Split row: the row's CTAs form one cluster (rank = split).  They exchange (m, l)
+        // through distributed shared memory, then each O^T block m (128 dims) is merged by
+        // CTA m % S from the peers' raw partials:
+        //   o = sum_s e^(m_s - M) O_s / sum_s e^(m_s - M) l_s,  lse = M + log(...)
+        const int S = P.splits;
+        if (tid < kH) {
+            const uint32_t lm = tc::smem_u32(&s_mlx[split][0][tid]), ll = tc::smem_u32(&s_mlx[split][1][tid]);
+            for (int c = 0; c < S; ++c) {
+                st_cluster_f32(map_peer(lm, (uint32_t)c), s_m[tid]);
+                st_cluster_f32(map_peer(ll, (uint32_t)c), s_l[tid]);
+            }
+        }
+        tc::tc_fence_before();
+        cluster_sync();                   // every loop done: peers' key buffers are free
+        tc::tc_fence_after();
+        if (tid < kH) {
+            float M = -INFINITY;
+            for (int sp = 0; sp < S; ++sp) M = fmaxf(M, s_mlx[sp][0][tid]);
+            float L = 0.0f;
+            for (int sp = 0; sp < S; ++sp) {
+                const float ms = s_mlx[sp][0][tid];
+                const float e = ms == -INFINITY ? 0.0f : exp2f(ms - M);
+                s_fac[sp][tid] = e;
+                if (ms != -INFINITY) L += e * s_mlx[sp][1][tid];
+            }
+            s_corr[tid] = L > 0.0f ? 1.0f / L : 0.0f;                 // 1/l per head
+            if (split == 0 && tid < H && P.lse) P.lse[row * H + tid] = L > 0.0f ? M * kLn2 + logf(L) : -INFINITY;
+        }
+        // send every O^T block this CTA does not merge to its owner: slot (block index
+        // among the owner's, source rank) of rows padded to kRecvRow floats
+#pragma unroll 1
+        for (int m = 0; m < 4; ++m) {
+            const int owner = m % S;
+            if (owner == split) continue;
+            uint32_t r[32];
+            if (any_o) {
+                tc::tc_ld_32x32b_x32(tmem + ((uint32_t)(quad * 32) << 16) + 64 + 64 * m + hh0, r);
+                tc::tc_wait_ld();
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) r[j] = 0u;
+            }
+            const int slot = (m / S) * (S - 1) + (split < owner ? split : split - 1);
+            const uint32_t dst = map_peer(tc::smem_u32(sm + (size_t)slot * kRecvBytes + key_row * kRecvRow * 4 + hh0 * 4),
+                                          (uint32_t)owner);
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+                st_cluster_v4(dst + j * 4, r[j], r[j + 1], r[j + 2], r[j + 3]);
+        }
+        tc::tc_fence_before();
+        cluster_sync();                   // partials delivered; no remote access after this
+        tc::tc_fence_after();
+#pragma unroll 1
+        for (int m = split; m < 4; m += S) {
+            const int d = 128 * m + key_row;
+            uint32_t own[32];
+            if (any_o) {
+                tc::tc_ld_32x32b_x32(tmem + ((uint32_t)(quad * 32) << 16) + 64 + 64 * m + hh0, own);
+                tc::tc_wait_ld();
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) own[j] = 0u;
+            }
+            float acc[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) acc[j] = 0.0f;
+#pragma unroll 1
+            for (int sp = 0; sp < S; ++sp) {
+                if (sp == split) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) acc[j] += s_fac[sp][hh0 + j] * __uint_as_float(own[j]);
+                } else {
+                    const int slot = (m / S) * (S - 1) + (sp < split ? sp : sp - 1);
+                    const float *src = reinterpret_cast<const float *>(sm + (size_t)slot * kRecvBytes) +
+                                       key_row * kRecvRow + hh0;
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4) {
+                        const float4 v = *reinterpret_cast<const float4 *>(src + j);
+                        acc[j + 0] += s_fac[sp][hh0 + j + 0] * v.x;
+                        acc[j + 1] += s_fac[sp][hh0 + j + 1] * v.y;
+                        acc[j + 2] += s_fac[sp][hh0 + j + 2] * v.z;
+                        acc[j + 3] += s_fac[sp][hh0 + j + 3] * v.w;
+                    }
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const int h = hh0 + j;
+                if (h >= H) continue;
+                P.out[(row * H + h) * (int64_t)kDv + d] = bf16_bits(acc[j] * s_corr[h]);
+            }
         }
     }
     tc::tc_fence_before();
@@ -442,33 +600,6 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
     if (tid == 0 && s_abort) dev_flag(P.d_status, CSA2_DEV_TIMEOUT);
 }
 
-// Merge split partials: o = sum_s e^(m_s - M) O_s / sum_s e^(m_s - M) l_s, lse = M + log(...)
-__global__ void __launch_bounds__(256) attn_combine_kernel(const AttnTcParams P)
-{
-    const int64_t row = blockIdx.y;
-    const int h = blockIdx.x;
-    const int S = P.splits;
-    float M = -INFINITY;
-    for (int s = 0; s < S; ++s) M = fmaxf(M, P.part_ml[((row * S + s) * P.H + h) * 2]);
-    float L = 0.0f;
-    for (int s = 0; s < S; ++s) {
-        const float m = P.part_ml[((row * S + s) * P.H + h) * 2];
-        if (m != -INFINITY) L += expf(m - M) * P.part_ml[((row * S + s) * P.H + h) * 2 + 1];
-    }
-    for (int d = threadIdx.x; d < kDv; d += blockDim.x) {
-        float o = 0.0f;
-        for (int s = 0; s < S; ++s) {
-            const float m = P.part_ml[((row * S + s) * P.H + h) * 2];
-            if (m != -INFINITY) o += expf(m - M) * P.part_o[((row * S + s) * P.H + h) * (int64_t)kDv + d];
-        }
-        const float v = L > 0.0f ? o / L : 0.0f;
-        uint32_t bits = __float_as_uint(v);
-        bits += 0x7fffu + ((bits >> 16) & 1u);
-        P.out[(row * P.H + h) * (int64_t)kDv + d] = (uint16_t)(bits >> 16);
-    }
-    if (threadIdx.x == 0 && P.lse) P.lse[row * P.H + h] = L > 0.0f ? M + logf(L) : -INFINITY;
-}
-
 void attn_tc_split(const csa2_attn_args &a, int &splits, int &tiles_per_split)
 {
     const int64_t rows = (int64_t)a.batch * a.n_q;
@@ -476,6 +607,7 @@ void attn_tc_split(const csa2_attn_args &a, int &splits, int &tiles_per_split)
     const int tiles = (int)((max_slots + kKeys - 1) / kKeys);
     int64_t per = (tiles * rows + 151) / 152;          // tiles per CTA to fill one wave
     if (per < 1) per = 1;
+    if (per * kMaxSplits < tiles) per = (tiles + kMaxSplits - 1) / kMaxSplits;   // one cluster per row
     if (per > tiles) per = tiles > 0 ? tiles : 1;
     tiles_per_split = (int)per;
     splits = tiles > 0 ? (int)((tiles + per - 1) / per) : 1;
@@ -489,15 +621,9 @@ bool attn_tc_eligible(const csa2_attn_args &a)
            (!a.swa || ((uintptr_t)a.swa & 15) == 0) && ((uintptr_t)a.kv_codes & 15) == 0;
 }
 
-size_t attn_tc_ws_bytes(const csa2_attn_args &a)
+size_t attn_tc_ws_bytes(const csa2_attn_args &)
 {
-    int splits, per;
-    attn_tc_split(a, splits, per);
-    if (splits <= 1) return 0;
-    const size_t rows = (size_t)a.batch * a.n_q;
-    size_t o = rows * splits * a.n_heads * (size_t)kDv * sizeof(float);
-    o = (o + 255) & ~(size_t)255;
-    return o + rows * splits * a.n_heads * 2 * sizeof(float);
+    return 0;     // split rows merge through distributed shared memory
 }
 
 cudaError_t launch_attn_tc(const csa2_attn_args &a, uint16_t *out, float *lse, void *ws,
@@ -509,7 +635,7 @@ cudaError_t launch_attn_tc(const csa2_attn_args &a, uint16_t *out, float *lse, v
     P.topk = a.topk;
     P.window = a.window;
     P.n_swa = a.swa ? a.n_swa : 0;
-    P.sm_scale = a.sm_scale;
+    P.log2_scale = a.sm_scale * 1.4426950408889634f;
     P.n_kv = a.n_kv;
     P.q = a.q;
     P.kvc = a.kv_codes;
@@ -524,21 +650,23 @@ cudaError_t launch_attn_tc(const csa2_attn_args &a, uint16_t *out, float *lse, v
     P.d_status = d_status;
     attn_tc_split(a, P.splits, P.tiles_per_split);
     const int64_t rows = (int64_t)a.batch * a.n_q;
-    if (P.splits > 1) {
-        const size_t o = ((size_t)rows * P.splits * a.n_heads * (size_t)kDv * sizeof(float) + 255) & ~(size_t)255;
-        P.part_o = static_cast<float *>(ws);
-        P.part_ml = reinterpret_cast<float *>(static_cast<char *>(ws) + o);
-    } else {
-        P.part_o = nullptr;
-        P.part_ml = nullptr;
-    }
     const int smem = kSmemBytes + 1024;
     cudaError_t e = cudaFuncSetAttribute(sparse_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    sparse_attn_tc_kernel<<<dim3((unsigned)P.splits, (unsigned)rows), kThreads, smem, s>>>(P);
-    e = cudaGetLastError();
-    if (e != cudaSuccess || P.splits == 1) return e;
-    attn_combine_kernel<<<dim3((unsigned)a.n_heads, (unsigned)rows), 256, 0, s>>>(P);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)P.splits, (unsigned)rows);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)P.splits;     // a row's CTAs: one cluster
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, sparse_attn_tc_kernel, P);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

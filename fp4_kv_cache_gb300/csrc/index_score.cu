@@ -236,10 +236,8 @@ cudaError_t launch_index_score(const csa2_index_args &a, float *scores, int32_t 
     if (!index_tc_eligible(a) || !ws) return launch_index_exact(a, scores, row_len, nullptr, 0, d_status, s);
     int64_t splits, chunk;
     index_tc_segments(a, splits, chunk);
-    uint32_t *flags = static_cast<uint32_t *>(ws);
-    cudaError_t e = cudaMemsetAsync(flags, 0, (size_t)(rows * splits) * sizeof(uint32_t), s);
-    if (e != cudaSuccess) return e;
-    e = launch_index_tc(a, scores, row_len, flags, splits, chunk, d_status, s);
+    uint32_t *flags = static_cast<uint32_t *>(ws);   // [rows, splits], written by every tensor-core CTA
+    cudaError_t e = launch_index_tc(a, scores, row_len, flags, splits, chunk, d_status, s);
     if (e != cudaSuccess) return e;
     // segments holding a position the tensor-core path cannot prove exact: re-score them
     return launch_index_exact(a, scores, row_len, flags, chunk, d_status, s);

@@ -246,33 +246,55 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
     } else {
         // ================= epilogue warps: first the query (B operand), then the scores
         {
-            const int kb = warp - 2;                          // this warp's 32-value block
-            const uint16_t *q = P.q + row * (int64_t)H * kD;
-            uint16_t qv[kNPad];                               // all loads in flight at once
+            // thread (h, kb) quantises block kb of head h on its own: 4 x 16-byte loads,
+            // a local maximum, 32 codes packed into one 16-byte store of the B operand
+            const int et = tid - 64, h = et >> 2, kb = et & 3;
+            uint4 raw[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
+                            make_uint4(0, 0, 0, 0)};
+            if (h < H) {
+                const uint4 *src = reinterpret_cast<const uint4 *>(P.q + row * (int64_t)H * kD + h * kD + kb * 32);
 #pragma unroll
-            for (int h = 0; h < kNPad; ++h) qv[h] = h < H ? q[h * kD + kb * 32 + lane] : (uint16_t)0;
+                for (int j = 0; j < 4; ++j) raw[j] = src[j];
+            }
+            float v[32];
 #pragma unroll
-            for (int h = 0; h < kNPad; ++h) {       // fully unrolled: qv stays in registers
-                const float v = __uint_as_float((uint32_t)qv[h] << 16);
-                const uint32_t amax_bits = __reduce_max_sync(0xffffffffu, __float_as_uint(v) & 0x7fffffffu);
-                const bool finite = amax_bits < 0x7f800000u;
-                const int X = mx_block_exponent(__uint_as_float(finite ? amax_bits : 0u));
-                const uint32_t c = e2m1_encode(v, pow2_neg(X));
-                const uint32_t c_hi = __shfl_down_sync(0xffffffffu, c, 1);
-                // row h, 16-byte chunk kb of the 64-byte row, XOR-swizzled by bits 1-2 of h%8
-                const int r8 = h & 7;
-                const int off = (h >> 3) * 512 + r8 * 64 + ((kb ^ ((r8 >> 1) & 3)) << 4);
-                if ((lane & 1) == 0) S.b[off + (lane >> 1)] = (uint8_t)(c | (c_hi << 4));
-                if (lane == 0) {
-                    reinterpret_cast<uint8_t *>(S.sfb)[h * 16 + kb] = (uint8_t)(X + 127);
-                    if (h < H && amax_bits != 0) {
-                        atomicMin(&S.hmin[h], X);
-                        atomicMax(&S.hmax[h], X);
-                    }
-                    if (h < H && !finite) dev_flag(P.d_status, CSA2_DEV_NONFINITE);
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t w4[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    v[8 * j + 2 * k] = __uint_as_float(w4[k] << 16);
+                    v[8 * j + 2 * k + 1] = __uint_as_float(w4[k] & 0xffff0000u);
                 }
             }
-            if (kb == 0) S.w[lane] = lane < H ? P.w[row * H + lane] : 0.0f;
+            uint32_t amax_bits = 0;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) amax_bits = max(amax_bits, __float_as_uint(v[e]) & 0x7fffffffu);
+            const bool finite = amax_bits < 0x7f800000u;
+            const int X = mx_block_exponent(__uint_as_float(finite ? amax_bits : 0u));
+            const float inv = pow2_neg(X);
+            uint32_t packed[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                uint32_t word = 0;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) word |= e2m1_encode(v[8 * j + e], inv) << (4 * e);
+                packed[j] = word;
+            }
+            // row h, 16-byte chunk kb of the 64-byte row, XOR-swizzled by bits 1-2 of h%8
+            const int r8 = h & 7;
+            *reinterpret_cast<uint4 *>(S.b + (h >> 3) * 512 + r8 * 64 + ((kb ^ ((r8 >> 1) & 3)) << 4)) =
+                make_uint4(packed[0], packed[1], packed[2], packed[3]);
+            reinterpret_cast<uint8_t *>(S.sfb)[h * 16 + kb] = (uint8_t)(X + 127);
+            // per-head exponent range over its non-zero blocks (the 4 blocks sit in 4 lanes)
+            int mn = (h < H && amax_bits != 0) ? X : (1 << 20);
+            int mx = (h < H && amax_bits != 0) ? X : -(1 << 20);
+            mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, 1));
+            mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, 2));
+            mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            if (kb == 0) { S.hmin[h] = mn; S.hmax[h] = mx; }
+            if (h < H && !finite) dev_flag(P.d_status, CSA2_DEV_NONFINITE);
+            if (et < kNPad) S.w[et] = et < H ? P.w[row * H + et] : 0.0f;
             tc::fence_proxy_async_smem();
             asm volatile("bar.sync 1, 128;" ::: "memory");   // the four epilogue warps
             if (warp == 2 && lane == 0) {
@@ -343,7 +365,8 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
         tc::tmem_dealloc(tmem, kTmemCols);
     }
     if (tid == 0) {
-        if (S.unsafe || S.abort_flag) P.seg_flags[row * gridDim.x + blockIdx.x] = 1u;
+        // every CTA writes its segment's flag, so the flags need no clearing beforehand
+        P.seg_flags[row * gridDim.x + blockIdx.x] = (S.unsafe || S.abort_flag) ? 1u : 0u;
         if (S.abort_flag) dev_flag(P.d_status, CSA2_DEV_TIMEOUT);
     }
 }
@@ -377,6 +400,7 @@ int64_t tc_splits(int64_t rows, int64_t n_cand)
 bool index_tc_eligible(const csa2_index_args &a)
 {
     if (a.head_dim != kD || a.n_heads > kNPad) return false;
+    if (((uintptr_t)a.q & 15) != 0) return false;           // 16-byte query loads
     if (a.mode == CSA2_INDEX_POOL && a.block != 8) return false;
     if ((int64_t)a.batch * a.n_keys >= (int64_t(1) << 31)) return false;
     if (((uintptr_t)a.k_codes & 15) != 0) return false;
@@ -435,6 +459,10 @@ cudaError_t launch_index_tc(const csa2_index_args &a, float *scores, int32_t *ro
     const size_t smem = sizeof(TcSmem) + 1024;
     cudaError_t e = cudaFuncSetAttribute(index_score_tc_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    // the whole unified L1 as shared memory, so kCtasPerSm CTAs are resident on every SM
+    e = cudaFuncSetAttribute(index_score_tc_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)splits, (unsigned)rows);
     index_score_tc_kernel<<<grid, kThreads, smem, s>>>(map, P);

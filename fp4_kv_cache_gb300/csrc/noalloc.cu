@@ -8,8 +8,9 @@
 // allocator's locks or risk an out-of-memory error mid-step.  This entry point needs no
 // workspace argument: its scratch (the indexer's per-segment re-score flags) lives in a
 // file-scope __device__ array that every GPU loading the library holds until the process
-// exits.  It calls no cudaMalloc, cudaFree or allocating library routine; the flags are
-// cleared with cudaMemsetAsync on the caller's stream inside each call.
+// exits.  It calls no cudaMalloc, cudaFree or allocating library routine; every call's
+// tensor-core kernel writes all the flags it covers before the re-score pass reads them,
+// so nothing is carried over from an earlier call.
 #include <cuda_runtime.h>
 #include <mutex>
 #include <stdint.h>

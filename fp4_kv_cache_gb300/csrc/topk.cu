@@ -177,12 +177,14 @@ topk_radix_kernel(const float *__restrict__ scores, int64_t n, const int32_t *__
 }
 
 // ------------------------------------------------------------------ group-max select
-// Pass 1 (group_max_kernel): the largest key of every group of gs consecutive candidates.
-// Pass 2 (topk_gmax_kernel, one CTA per row): tau0 = the k-th largest group key.  Each of
-// those k groups holds an element >= tau0, so at least k elements are >= tau0 and every
-// element of the top-k is >= tau0; only groups whose key is >= tau0 can hold one.  Those
-// groups' elements >= tau0 are gathered on chip in position order, and an exact radix
-// select among them (key desc, position asc) gives the top-k, emitted in order.
+// Pass 1 (group_max32_kernel / group_max_kernel): the largest key of every group of gs
+// consecutive candidates, spread over the whole GPU.  Pass 2 (topk_gmax_kernel, one CTA
+// per row): tau0 = the k-th largest group key.  Each of those k groups holds an element
+// >= tau0, so at least k elements are >= tau0 and every element of the top-k is >= tau0;
+// only groups whose key is >= tau0 can hold one.  Any lower bound of tau0 keeps that
+// property, so tau0 is taken to 22 of its 32 bits.  Those groups' elements >= the bound
+// are gathered on chip in position order, and an exact radix select among them (key
+// desc, position asc) gives the top-k, emitted in order.
 constexpr int kGThreads = 1024;
 constexpr int kGBins = 2048;
 constexpr int kGroupCap = 32768;        // group keys per row kept on chip
@@ -242,14 +244,17 @@ __global__ void __launch_bounds__(256) group_max_kernel(const float *__restrict_
     }
 }
 
-// Exact k-th largest key of n keys in shared memory (3 digit passes: 11, 11, 10 bits);
-// returns tau, and in need how many keys equal to tau belong to the top k.
-__device__ uint32_t g_threshold(const uint32_t *keys, int n, uint32_t k, GSmem &S, uint32_t &need)
+// k-th largest key of n keys in shared memory by digit passes of 11, 11 and 10 bits.
+// With all three passes: the exact key tau, and in need how many keys equal to tau belong
+// to the top k.  With the first `passes` only: tau with its unresolved low bits zero, a
+// lower bound of the exact key (need is then meaningless).
+__device__ uint32_t g_threshold(const uint32_t *keys, int n, uint32_t k, GSmem &S, uint32_t &need,
+                                int passes = 3)
 {
     const int tid = threadIdx.x, lane = tid & 31;
     uint32_t prefix = 0, mask = 0, remaining = k;
     const int shifts[3] = {21, 10, 0}, widths[3] = {11, 11, 10};
-    for (int pass = 0; pass < 3; ++pass) {
+    for (int pass = 0; pass < passes; ++pass) {
         const int shift = shifts[pass], nb = 1 << widths[pass];
         for (int i = tid; i < kGBins; i += kGThreads) S.hist[i] = 0;
         __syncthreads();
@@ -323,8 +328,10 @@ topk_gmax_kernel(const float *__restrict__ scores, int64_t n, const int32_t *__r
     for (int g = tid; g < ng; g += kGThreads) s_g[g] = gkeys[row * G + g];
     if (tid == 0) S.overflow = 0;
     __syncthreads();
+    // a lower bound of the k-th largest group key is enough to keep every top-k element
+    // (the groups above the bound are a superset of those above the exact key)
     uint32_t need0;
-    const uint32_t tau0 = ng > k ? g_threshold(s_g, ng, (uint32_t)k, S, need0) : 0u;
+    const uint32_t tau0 = ng > k ? g_threshold(s_g, ng, (uint32_t)k, S, need0, 2) : 0u;
 
     // candidate groups (key >= tau0), compacted in place in ascending order: thread t owns
     // the run [t*run, (t+1)*run) and writes only below its own run after everyone has read

@@ -216,8 +216,9 @@ def run_gpu(args):
     idx = torch.empty((B, T, w.topk), dtype=torch.int32, device=dev)
     out = torch.empty((B, T, w.heads, w.d_v), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((B, T, w.heads), dtype=torch.float32, device=dev)
+    gmax = csa2.group_max_buffer(scores)     # per-32 group maxima: indexer -> Top-K
     iargs = csa2.make_index_args(dw["q_idx"], dw["w_idx"], dw["k_codes"], dw["k_scales"],
-                                 dw["q_pos"], w.ratio_m)
+                                 dw["q_pos"], w.ratio_m, group_max=gmax)
     aargs = csa2.make_attn_args(dw["q_attn"], dw["kv_codes"], dw["kv_scales"], idx, dw["swa"],
                                 dw["swa_pos0"], dw["q_pos"], None, w.window, dw.sm_scale, w.d_v)
     lib = csa2.load()
@@ -231,8 +232,8 @@ def run_gpu(args):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
     # our kernels per step: 2 cache-write quantisers, indexer (tensor-core + exact re-score
-    # of flagged segments), Top-K (group maxima + select), attention
-    launches_per_step = 7
+    # of flagged segments, which also writes the per-32 group maxima), Top-K select, attention
+    launches_per_step = 6
 
     side = torch.cuda.Stream(dev)
 
@@ -257,7 +258,7 @@ def run_gpu(args):
         csa2.csa2_index_score(iargs, scores, row_len, st, workspace=ws_index)
         if k_ev:
             k_ev[2].record(stream)
-        csa2.csa2_topk(scores, w.topk, idx, row_len, d_status=st, workspace=ws_topk)
+        csa2.csa2_topk(scores, w.topk, idx, row_len, d_status=st, workspace=ws_topk, group_max=gmax)
         if k_ev:
             k_ev[3].record(stream)
         stream.wait_event(kv_done)

@@ -38,7 +38,7 @@ class IndexArgs(ctypes.Structure):
     _fields_ = [("batch", _I32), ("n_q", _I32), ("n_heads", _I32), ("head_dim", _I32),
                 ("ratio_m", _I32), ("n_keys", _I64), ("q", _P), ("w", _P), ("k_codes", _P),
                 ("k_scales", _P), ("q_pos", _P), ("mode", ctypes.c_int), ("pool_blocks", _P),
-                ("n_pool_blocks", _I32), ("block", _I32)]
+                ("n_pool_blocks", _I32), ("block", _I32), ("group_max", _P)]
 
 
 class AttnArgs(ctypes.Structure):
@@ -88,7 +88,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
             lib.csa2_topk_workspace_size.restype = sz
             lib.csa2_topk_workspace_size.argtypes = [_I64, _I64, _I32]
             lib.csa2_topk.restype = S
-            lib.csa2_topk.argtypes = [_P, _I64, _I64, _P, _P, _I32, _I32, _P, _P, _P, sz, _P, _P]
+            lib.csa2_topk.argtypes = [_P, _I64, _I64, _P, _P, _P, _I32, _I32, _P, _P, _P, sz, _P, _P]
             lib.csa2_block_candidates_workspace_size.restype = sz
             lib.csa2_block_candidates_workspace_size.argtypes = [_I64, _I64, _I32, _I32]
             lib.csa2_block_candidates.restype = S
@@ -190,7 +190,8 @@ def csa2_dequant_fp4(codes: torch.Tensor, scales: torch.Tensor, y: torch.Tensor,
         _stream(stream)))
 
 
-def make_index_args(q, w, k_codes, k_scales, q_pos=None, ratio_m=1, pool_blocks=None, block=8):
+def make_index_args(q, w, k_codes, k_scales, q_pos=None, ratio_m=1, pool_blocks=None, block=8,
+                    group_max=None):
     B, T, H, d = q.shape
     a = IndexArgs()
     a.batch, a.n_q, a.n_heads, a.head_dim, a.ratio_m = B, T, H, d, ratio_m
@@ -203,6 +204,7 @@ def make_index_args(q, w, k_codes, k_scales, q_pos=None, ratio_m=1, pool_blocks=
     else:
         a.mode, a.pool_blocks, a.n_pool_blocks = INDEX_POOL, _ptr(pool_blocks), pool_blocks.shape[-1]
     a.block = block
+    a.group_max = _ptr(group_max)
     return a
 
 
@@ -225,15 +227,16 @@ def csa2_index_score_noalloc(args: IndexArgs, scores: torch.Tensor, row_len: tor
 
 
 def csa2_topk(scores: torch.Tensor, k: int, idx: torch.Tensor, row_len=None, pool_blocks=None,
-              block: int = 8, out_scores=None, d_status=None, stream=None, workspace=None):
+              block: int = 8, out_scores=None, d_status=None, stream=None, workspace=None,
+              group_max=None):
     lib = load()
     n = scores.shape[-1]
     rows = scores.numel() // n if n else idx.numel() // max(k, 1)
     need = lib.csa2_topk_workspace_size(rows, n, k)
     ws, wsb = _ws(need, idx.device, workspace, stream)
-    _check("csa2_topk", lib.csa2_topk(_ptr(scores), rows, n, _ptr(row_len), _ptr(pool_blocks),
-                                      block, k, _ptr(idx), _ptr(out_scores), ws, wsb,
-                                      _ptr(d_status), _stream(stream)))
+    _check("csa2_topk", lib.csa2_topk(_ptr(scores), rows, n, _ptr(row_len), _ptr(group_max),
+                                      _ptr(pool_blocks), block, k, _ptr(idx), _ptr(out_scores),
+                                      ws, wsb, _ptr(d_status), _stream(stream)))
 
 
 def csa2_block_candidates(scores: torch.Tensor, nb: int, block_ids: torch.Tensor, row_len=None,
@@ -291,24 +294,32 @@ def dequant_fp4(codes, scales, dtype=torch.float32, stream=None):
     return y
 
 
+def group_max_buffer(scores: torch.Tensor) -> torch.Tensor:
+    """Buffer for the indexer's per-32-candidate group maxima of `scores` (32-bit keys)."""
+    return torch.empty(scores.shape[:-1] + ((scores.shape[-1] + 31) // 32,), dtype=torch.int32,
+                       device=scores.device)
+
+
 def index_score(q, w, k_codes, k_scales, q_pos=None, ratio_m=1, pool_blocks=None, block=8,
-                d_status=None, stream=None):
-    """-> (scores f32 [B, T, n_cand], row_len int32 [B, T])."""
+                d_status=None, stream=None, group_max=None):
+    """-> (scores f32 [B, T, n_cand], row_len int32 [B, T]); group_max: optional buffer
+    from group_max_buffer(scores) that receives the group maxima for csa2_topk."""
     B, T = q.shape[:2]
     n_cand = k_codes.shape[1] if pool_blocks is None else pool_blocks.shape[-1] * block
     scores = torch.empty((B, T, n_cand), dtype=torch.float32, device=q.device)
     row_len = torch.empty((B, T), dtype=torch.int32, device=q.device)
-    args = make_index_args(q, w, k_codes, k_scales, q_pos, ratio_m, pool_blocks, block)
+    args = make_index_args(q, w, k_codes, k_scales, q_pos, ratio_m, pool_blocks, block, group_max)
     csa2_index_score(args, scores, row_len, d_status, stream)
     return scores, row_len
 
 
 def topk(scores, k=512, row_len=None, pool_blocks=None, block=8, want_scores=False,
-         d_status=None, stream=None):
+         d_status=None, stream=None, group_max=None):
     shape = scores.shape[:-1]
     idx = torch.empty(shape + (k,), dtype=torch.int32, device=scores.device)
     out_s = torch.empty(shape + (k,), dtype=torch.float32, device=scores.device) if want_scores else None
-    csa2_topk(scores, k, idx, row_len, pool_blocks, block, out_s, d_status, stream)
+    csa2_topk(scores, k, idx, row_len, pool_blocks, block, out_s, d_status, stream,
+              group_max=group_max)
     return (idx, out_s) if want_scores else idx
 
 

@@ -150,9 +150,9 @@ size_t csa2_topk_workspace_size(int64_t rows, int64_t n, int32_t k)
 }
 
 csa2_status csa2_topk(const float *scores, int64_t rows, int64_t n, const int32_t *row_len,
-                      const int32_t *pool_blocks, int32_t block, int32_t k, int32_t *idx,
-                      float *out_scores, void *ws, size_t ws_bytes, uint32_t *d_status,
-                      csa2_stream stream)
+                      const uint32_t *group_max, const int32_t *pool_blocks, int32_t block,
+                      int32_t k, int32_t *idx, float *out_scores, void *ws, size_t ws_bytes,
+                      uint32_t *d_status, csa2_stream stream)
 {
     if (rows < 0 || n < 0 || n >= (int64_t(1) << 31) || k < 0 || rows > (int64_t(1) << 31))
         return CSA2_ERR_INVALID_ARG;
@@ -160,8 +160,9 @@ csa2_status csa2_topk(const float *scores, int64_t rows, int64_t n, const int32_
     if (rows == 0 || k == 0) return CSA2_OK;
     if (!idx || (n > 0 && !scores)) return CSA2_ERR_INVALID_ARG;
     if (ws_bytes < csa2_topk_workspace_size(rows, n, k)) return CSA2_ERR_WORKSPACE;
-    return from_cuda(launch_topk(scores, rows, n, row_len, pool_blocks, block, k, idx, out_scores,
-                                 ws, d_status, as_stream(stream)));
+    if (group_max && !aligned(group_max, 4)) return CSA2_ERR_INVALID_ARG;
+    return from_cuda(launch_topk(scores, rows, n, row_len, group_max, pool_blocks, block, k, idx,
+                                 out_scores, ws, d_status, as_stream(stream)));
 }
 
 size_t csa2_block_candidates_workspace_size(int64_t rows, int64_t n, int32_t block, int32_t nb)

@@ -30,6 +30,8 @@ struct IndexParams {
     bool pool_mode;
     float *scores;
     int32_t *row_len;
+    uint32_t *gmax;              // optional [rows, G]: largest selection key of each 32-group
+    int64_t G;
     const uint32_t *seg_flags;   // non-null: [rows, n_seg]; only flagged segments are scored
     int64_t n_seg;
     uint32_t *d_status;
@@ -44,6 +46,57 @@ __device__ __forceinline__ int64_t visible_entries(const IndexParams &P, int64_t
     int64_t v = (p + 1) / P.ratio_m;
     if (p + 1 < 0) v = 0;
     return v < 0 ? 0 : (v > P.n_keys ? P.n_keys : v);
+}
+
+// Exact score of one candidate: the key row's codes as int8x4 words of twice the E2M1
+// values, per-block integer dots with dp4a against the quantised query, each head's
+// dyadic sum rounded once to float32, then the fma chain over heads.
+template <int D>
+__device__ __forceinline__ float score_candidate(const IndexParams &P, const int32_t *pool, int64_t kbase,
+                                                 int64_t cand, const int32_t *s_qw, const int32_t *s_qx,
+                                                 const float *s_w, const uint16_t *s_lut)
+{
+    constexpr int NB = D / 32, NW = D / 4;
+    int64_t pos = cand;
+    if (P.pool_mode) {
+        const int32_t id = pool[cand / P.block];
+        pos = (int64_t)(id < 0 ? 0 : id) * P.block + cand % P.block;
+        if (pos >= P.n_keys) pos = P.n_keys - 1;           // only for a flagged bad pool
+    }
+    int32_t kw[NW];
+    const uint8_t *kc = P.kc + (kbase + pos) * (D / 2);
+#pragma unroll
+    for (int v = 0; v < D / 32; ++v) {
+        const uint4 raw = *reinterpret_cast<const uint4 *>(kc + 16 * v);
+        const uint32_t r4[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            kw[v * 8 + 2 * j] = (int32_t)((uint32_t)s_lut[r4[j] & 0xff] |
+                                          ((uint32_t)s_lut[(r4[j] >> 8) & 0xff] << 16));
+            kw[v * 8 + 2 * j + 1] = (int32_t)((uint32_t)s_lut[(r4[j] >> 16) & 0xff] |
+                                              ((uint32_t)s_lut[r4[j] >> 24] << 16));
+        }
+    }
+    int kx[NB];
+    const uint8_t *ks = P.ks + (kbase + pos) * NB;
+#pragma unroll
+    for (int k = 0; k < NB; ++k) kx[k] = (int)ks[k] - 127;
+
+    float s = 0.0f;
+    for (int h = 0; h < P.H; ++h) {
+        int I[NB], E[NB];
+#pragma unroll
+        for (int k = 0; k < NB; ++k) {
+            int acc = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc = __dp4a(s_qw[h * NW + k * 8 + j], kw[k * 8 + j], acc);
+            I[k] = acc;
+            E[k] = s_qx[h * NB + k] + kx[k] - 2;
+        }
+        const float Dh = dyadic_sum_f32<NB>(I, E);
+        s = __fmaf_rn(s_w[h], Dh > 0.0f ? Dh : 0.0f, s);
+    }
+    return s;
 }
 
 template <int D>
@@ -124,53 +177,26 @@ __global__ void __launch_bounds__(kThreads) index_score_exact_kernel(IndexParams
 
     const int64_t kbase = b * P.n_keys;
     for (int64_t seg = 0; seg < n_seg; ++seg) {
-    const int64_t seg_id = P.seg_flags ? seg : (int64_t)blockIdx.x;
-    if (P.seg_flags && P.seg_flags[row * n_seg + seg] == 0u) continue;
-    const int64_t c0 = seg_id * P.chunk;
-    const int64_t c1 = min(c0 + P.chunk, len);
-    for (int64_t cand = c0 + tid; cand < c1; cand += kThreads) {
-        int64_t pos = cand;
-        if (P.pool_mode) {
-            int32_t id = pool[cand / P.block];
-            pos = (int64_t)(id < 0 ? 0 : id) * P.block + cand % P.block;
-            if (pos >= P.n_keys) pos = P.n_keys - 1;        // only for a flagged bad pool
-        }
-        // codes of the key row -> int8x4 words of twice the E2M1 values
-        int32_t kw[NW];
-        const uint8_t *kc = P.kc + (kbase + pos) * (D / 2);
-#pragma unroll
-        for (int v = 0; v < D / 32; ++v) {
-            const uint4 raw = *reinterpret_cast<const uint4 *>(kc + 16 * v);
-            const uint32_t r4[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                kw[v * 8 + 2 * j] = (int32_t)((uint32_t)s_lut[r4[j] & 0xff] |
-                                              ((uint32_t)s_lut[(r4[j] >> 8) & 0xff] << 16));
-                kw[v * 8 + 2 * j + 1] = (int32_t)((uint32_t)s_lut[(r4[j] >> 16) & 0xff] |
-                                                  ((uint32_t)s_lut[r4[j] >> 24] << 16));
+        const int64_t seg_id = P.seg_flags ? seg : (int64_t)blockIdx.x;
+        if (P.seg_flags && P.seg_flags[row * n_seg + seg] == 0u) continue;
+        const int64_t c0 = seg_id * P.chunk;
+        const int64_t c1 = min(c0 + P.chunk, len);
+        // uniform trip count: every warp meets the group reduction below; c0 is a multiple
+        // of 32, so each warp's 32 candidates form one group
+        for (int64_t base = c0; base < c1; base += kThreads) {
+            const int64_t cand = base + tid;
+            uint32_t gkey = 0;
+            if (cand < c1) {
+                const float s = score_candidate<D>(P, pool, kbase, cand, s_qw, s_qx, s_w, s_lut);
+                P.scores[row * P.n_cand + cand] = s;
+                gkey = score_key(s);
+            }
+            if (P.gmax) {
+                const uint32_t gk = __reduce_max_sync(0xffffffffu, gkey);
+                const int64_t g0 = base + (tid & ~31);
+                if (lane == 0 && g0 < c1) P.gmax[row * P.G + (g0 >> 5)] = gk;
             }
         }
-        int kx[NB];
-        const uint8_t *ks = P.ks + (kbase + pos) * NB;
-#pragma unroll
-        for (int k = 0; k < NB; ++k) kx[k] = (int)ks[k] - 127;
-
-        float s = 0.0f;
-        for (int h = 0; h < H; ++h) {
-            int I[NB], E[NB];
-#pragma unroll
-            for (int k = 0; k < NB; ++k) {
-                int acc = 0;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) acc = __dp4a(s_qw[h * NW + k * 8 + j], kw[k * 8 + j], acc);
-                I[k] = acc;
-                E[k] = s_qx[h * NB + k] + kx[k] - 2;
-            }
-            const float Dh = dyadic_sum_f32<NB>(I, E);
-            s = __fmaf_rn(s_w[h], Dh > 0.0f ? Dh : 0.0f, s);
-        }
-        P.scores[row * P.n_cand + cand] = s;
-    }
     }
 }
 
@@ -199,6 +225,8 @@ cudaError_t launch_index_exact(const csa2_index_args &a, float *scores, int32_t 
     P.pool = a.pool_blocks;
     P.scores = scores;
     P.row_len = row_len;
+    P.gmax = a.group_max;
+    P.G = (P.n_cand + 31) / 32;
     P.seg_flags = seg_flags;
     P.d_status = d_status;
     const int64_t rows = (int64_t)a.batch * a.n_q;

@@ -52,6 +52,8 @@ struct TcParams {
     int pool_mode;
     float *scores;
     int32_t *row_len;
+    uint32_t *gmax;          // optional [rows, G]: largest selection key of each 32-group
+    int64_t G;
     uint32_t *seg_flags;
     uint32_t *d_status;
 };
@@ -88,7 +90,10 @@ __device__ __forceinline__ int64_t n_visible(const TcParams &P, int64_t row)
     return v < 0 ? 0 : (v > P.n_keys ? P.n_keys : v);
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+// kCtasPerSm resident CTAs need every warp within its sub-partition's share of the register
+// file (18 warps over 4 sub-partitions: at most 96 registers a thread); the bound makes
+// the compiler keep to it.
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
 index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -162,7 +167,10 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
         for (int i = 0; i < ntiles; ++i) {
             const int s = i % kStages;
             const uint32_t ph = (uint32_t)(i / kStages) & 1u;
-            if (!tc::mbar_wait(&S.empty[s], ph ^ 1u, &S.abort_flag)) { S.abort_flag = 1; break; }
+            if (!__all_sync(0xffffffffu, tc::mbar_wait(&S.empty[s], ph ^ 1u, &S.abort_flag))) {
+                S.abort_flag = 1;
+                break;
+            }
             const int64_t t0 = c0 + (int64_t)i * kTile;
             if (lane == 0) {
                 if (!P.pool_mode) {
@@ -320,8 +328,9 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
         for (int h = 0; h < kNPad; ++h) wv[h] = S.w[h];
         for (int i = 0; i < ntiles; ++i) {
             const int s = i % kStages, acc = i % kAcc;
-            if (!tc::mbar_wait(&S.accf[acc], (uint32_t)(i / kAcc) & 1u, &S.abort_flag) ||
-                !tc::mbar_wait(&S.full[s], (uint32_t)(i / kStages) & 1u, &S.abort_flag)) {
+            const bool ok = tc::mbar_wait(&S.accf[acc], (uint32_t)(i / kAcc) & 1u, &S.abort_flag) &&
+                            tc::mbar_wait(&S.full[s], (uint32_t)(i / kStages) & 1u, &S.abort_flag);
+            if (!__all_sync(0xffffffffu, ok)) {   // the warp leaves together (aligned ops follow)
                 S.abort_flag = 1;
                 break;
             }
@@ -337,6 +346,7 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
                 tc::mbar_arrive(&S.empty[s]);
             }
             const int64_t cand = c0 + (int64_t)i * kTile + m;
+            uint32_t key = 0;
             if (cand < c1) {
                 float sc = 0.0f;
 #pragma unroll
@@ -354,6 +364,12 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
                                   q_max + kmax - 2 <= 100;
                 if (!safe) S.unsafe = 1;
                 P.scores[row * P.n_cand + cand] = sc;
+                key = score_key(sc);
+            }
+            if (P.gmax) {            // this warp's 32 candidates are one aligned group
+                const uint32_t gk = __reduce_max_sync(0xffffffffu, key);
+                const int64_t g0 = c0 + (int64_t)i * kTile + quad * 32;
+                if (lane == 0 && g0 < c1) P.gmax[row * P.G + (g0 >> 5)] = gk;
             }
         }
     }
@@ -442,6 +458,8 @@ cudaError_t launch_index_tc(const csa2_index_args &a, float *scores, int32_t *ro
     P.pool = a.pool_blocks;
     P.scores = scores;
     P.row_len = row_len;
+    P.gmax = a.group_max;
+    P.G = (P.n_cand + 31) / 32;
     P.seg_flags = seg_flags;
     P.d_status = d_status;
 

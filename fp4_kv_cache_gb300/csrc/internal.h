@@ -30,8 +30,9 @@ cudaError_t launch_index_tc(const csa2_index_args &a, float *scores, int32_t *ro
 // Top-K over rows of float scores (see csa2_topk).  ws: topk_ws_bytes(rows, n, k).
 size_t topk_ws_bytes(int64_t rows, int64_t n, int32_t k);
 cudaError_t launch_topk(const float *scores, int64_t rows, int64_t n, const int32_t *row_len,
-                        const int32_t *pool, int32_t block, int32_t k, int32_t *idx,
-                        float *out_scores, void *ws, uint32_t *d_status, cudaStream_t s);
+                        const uint32_t *group_max, const int32_t *pool, int32_t block, int32_t k,
+                        int32_t *idx, float *out_scores, void *ws, uint32_t *d_status,
+                        cudaStream_t s);
 size_t block_candidates_ws_bytes(int64_t rows, int64_t n, int32_t block, int32_t nb);
 cudaError_t launch_block_candidates(const float *scores, int64_t rows, int64_t n,
                                     const int32_t *row_len, int32_t block, int32_t nb,

@@ -466,8 +466,8 @@ size_t topk_ws_bytes(int64_t rows, int64_t n, int32_t)
 }
 
 cudaError_t launch_topk(const float *scores, int64_t rows, int64_t n, const int32_t *row_len,
-                        const int32_t *pool, int32_t block, int32_t k, int32_t *idx,
-                        float *out_scores, void *ws, uint32_t *, cudaStream_t s)
+                        const uint32_t *group_max, const int32_t *pool, int32_t block, int32_t k,
+                        int32_t *idx, float *out_scores, void *ws, uint32_t *, cudaStream_t s)
 {
     if (rows == 0 || k == 0) return cudaSuccess;
     if (rows > 0x7fffffffLL || !ws) {
@@ -477,15 +477,18 @@ cudaError_t launch_topk(const float *scores, int64_t rows, int64_t n, const int3
     }
     const int32_t gs = group_size_for(n);
     const int64_t G = (n + gs - 1) / gs;
-    uint32_t *gkeys = static_cast<uint32_t *>(ws);
-    if (G > 0) {
+    const uint32_t *gkeys = static_cast<const uint32_t *>(ws);
+    if (group_max && gs == 32) {
+        gkeys = group_max;                                 // written by the indexer
+    } else if (G > 0) {
+        uint32_t *gk = static_cast<uint32_t *>(ws);
         if (gs == 32 && ((uintptr_t)scores % 16) == 0 && n % 4 == 0) {
             const int64_t blocks = (rows * G + 255) / 256;
-            group_max32_kernel<<<(unsigned)blocks, 256, 0, s>>>(scores, n, row_len, rows, G, gkeys);
+            group_max32_kernel<<<(unsigned)blocks, 256, 0, s>>>(scores, n, row_len, rows, G, gk);
         } else {
             int64_t blocks = (rows * G * 32 + 255) / 256;
             if (blocks > 152 * 16) blocks = 152 * 16;
-            group_max_kernel<<<(unsigned)blocks, 256, 0, s>>>(scores, n, row_len, rows, gs, G, gkeys);
+            group_max_kernel<<<(unsigned)blocks, 256, 0, s>>>(scores, n, row_len, rows, gs, G, gk);
         }
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
@@ -526,7 +529,7 @@ cudaError_t launch_block_candidates(const float *scores, int64_t rows, int64_t n
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const size_t off2 = (off + (size_t)rows * sizeof(int32_t) + 255) & ~(size_t)255;
-    return launch_topk(bscores, rows, nbmax, brow_len, nullptr, 1, nb, block_ids, nullptr,
+    return launch_topk(bscores, rows, nbmax, brow_len, nullptr, nullptr, 1, nb, block_ids, nullptr,
                        static_cast<char *>(ws) + off2, d_status, s);
 }
 

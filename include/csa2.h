@@ -134,6 +134,15 @@ typedef struct {
     const int32_t *pool_blocks; /* POOL: [B, T, n_pool_blocks] block ids, ascending and     */
     int32_t n_pool_blocks;      /* unique, padded with -1 at the end; block b covers        */
     int32_t block;              /* positions [b*block, b*block+block-1].  block: 1..32.     */
+    uint32_t *group_max;        /* optional output (NULL: none), [B, T, ceil(n_cand/32)]:   */
+                                /* per row, for every group of 32 consecutive candidates   */
+                                /* that holds a valid one, the largest selection key of    */
+                                /* its valid candidates; entries past the valid groups are */
+                                /* left unwritten.  Handing it to csa2_topk spares that    */
+                                /* call its first pass.  Selection key of a score s (the   */
+                                /* order csa2_topk uses): 0 for NaN; with u = the bits of  */
+                                /* s and -0 read as +0, u | 0x80000000 for s >= 0 and ~u   */
+                                /* for s < 0 (so keys rise with the score).                */
 } csa2_index_args;
 
 /* Outputs: scores [B, T, n_cand] float32, n_cand = N (FULL) or n_pool_blocks*block (POOL);
@@ -155,12 +164,15 @@ CSA2_API csa2_status csa2_index_score(const csa2_index_args *a, float *scores, i
 /* ([rows, n/block]) pool_blocks[i/block]*block + i%block -- ascending candidates map to */
 /* ascending positions, so the tie rule is the lower position.                         */
 /* out_scores (nullable) [rows, k]: the score of each selected entry (0 for padding).   */
+/* group_max (nullable) [rows, ceil(n/32)]: the group_max output of the csa2_index_score */
+/* call that wrote these scores and row_len; when given, the call skips computing it.  */
+/* (Used only while n <= 2^20; longer rows use wider groups and compute their own.)     */
 /* ---------------------------------------------------------------------------------- */
 CSA2_API size_t csa2_topk_workspace_size(int64_t rows, int64_t n, int32_t k);
 CSA2_API csa2_status csa2_topk(const float *scores, int64_t rows, int64_t n, const int32_t *row_len,
-                      const int32_t *pool_blocks, int32_t block, int32_t k, int32_t *idx,
-                      float *out_scores, void *ws, size_t ws_bytes, uint32_t *d_status,
-                      csa2_stream stream);
+                      const uint32_t *group_max, const int32_t *pool_blocks, int32_t block,
+                      int32_t k, int32_t *idx, float *out_scores, void *ws, size_t ws_bytes,
+                      uint32_t *d_status, csa2_stream stream);
 
 /* ---------------------------------------------------------------------------------- */
 /* csa2_block_candidates -- the hierarchical sparse indexer's block pool (report §2.3.2 */

@@ -102,9 +102,12 @@ def test_index_rejects_bad_args(lib):
 
 
 def test_select_and_attn_reject_bad_args(lib):
-    assert lib.csa2_topk(FAKE, -1, 10, None, None, 8, 4, FAKE, None, None, 0, None, None) == 1
-    assert lib.csa2_topk(FAKE, 2, 10, None, FAKE, 8, 4, FAKE, None, None, 0, None, None) == 1
-    assert lib.csa2_topk(FAKE, 0, 10, None, None, 8, 4, FAKE, None, None, 0, None, None) == 0
+    assert lib.csa2_topk(FAKE, -1, 10, None, None, None, 8, 4, FAKE, None, None, 0, None, None) == 1
+    assert lib.csa2_topk(FAKE, 2, 10, None, None, FAKE, 8, 4, FAKE, None, None, 0, None, None) == 1
+    assert lib.csa2_topk(FAKE, 0, 10, None, None, None, 8, 4, FAKE, None, None, 0, None, None) == 0
+    need = lib.csa2_topk_workspace_size(2, 64, 4)
+    assert lib.csa2_topk(FAKE, 2, 64, None, ctypes.c_void_p(258), None, 8, 4, FAKE, None, FAKE,
+                         need, None, None) == 1                                 # misaligned
     need = lib.csa2_block_candidates_workspace_size(4, 1 << 20, 8, 2048)
     assert need >= 4 * (1 << 17) * 4
     assert lib.csa2_block_candidates(FAKE, 4, 1 << 20, None, 8, 2048, FAKE, FAKE, need - 1,

@@ -105,6 +105,35 @@ SCORE_CASES = {
 }
 
 
+def sel_key(s):
+    """Selection key of float32 scores as include/csa2.h defines it (NaN 0, -0 as +0)."""
+    s = np.asarray(s, np.float32)
+    u = s.view(np.uint32).copy()
+    u[u == 0x80000000] = 0
+    key = np.where(u & np.uint32(0x80000000), ~u, u | np.uint32(0x80000000)).astype(np.uint32)
+    key[np.isnan(s)] = 0
+    return key
+
+
+def group_keys(s_valid):
+    """Largest selection key of each group of 32 consecutive valid candidates."""
+    k = sel_key(s_valid)
+    ng = (k.size + 31) // 32
+    pad = np.zeros(ng * 32, np.uint32)
+    pad[:k.size] = k
+    return pad.reshape(ng, 32).max(axis=1)
+
+
+def _with_group_max(dw, w, pool=None, st=None):
+    """The indexer again with its group-maximum output, then Top-K fed from it."""
+    n_cand = w.n_keys if pool is None else pool.shape[-1] * w.block
+    gm = torch.full((w.batch, w.n_q, (n_cand + 31) // 32), -1, dtype=torch.int32, device=DEV)
+    scores, row_len = csa2.index_score(dw["q_idx"], dw["w_idx"], dw["k_codes"], dw["k_scales"],
+                                       dw["q_pos"], w.ratio_m, pool, w.block, st, group_max=gm)
+    idx = csa2.topk(scores, w.topk, row_len, pool, w.block, d_status=st, group_max=gm)
+    return scores, gm, idx
+
+
 def _oracle_row_scores(w, b, t, qi, ww, kc, ks, pos):
     qc, qs = oracle.quant_mxfp4(f32(qi[t]))
     return oracle.index_scores(qc, qs, ww[t], kc, ks, pos)
@@ -120,6 +149,7 @@ def test_full_scores_topk_blocks(name):
     idx = csa2.topk(scores, w.topk, row_len, d_status=st)
     nb = min(w.n_blocks, 300)
     blocks = csa2.block_candidates(scores, nb, row_len, w.block, st)
+    scores_g, gm, idx_g = _with_group_max(dw, w, None, st)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     qi_all, ww_all, _ = synth.gen_queries(w)
@@ -137,6 +167,11 @@ def test_full_scores_topk_blocks(name):
             assert np.array_equal(idx[b, t].cpu().numpy(), oracle.topk(s_ref, pos, w.topk))
             assert np.array_equal(blocks[b, t].cpu().numpy(),
                                   oracle.block_candidates(s_ref, nvis, w.block, nb))
+            # group-maximum output and Top-K fed from it
+            assert same_f32(scores_g[b, t, :nvis].cpu().numpy(), s_ref)
+            ng = (nvis + 31) // 32
+            assert np.array_equal(gm[b, t, :ng].cpu().numpy().view(np.uint32), group_keys(s_ref))
+            assert np.array_equal(idx_g[b, t].cpu().numpy(), idx[b, t].cpu().numpy())
 
 
 def test_scores_wide_exponents():
@@ -151,14 +186,17 @@ def test_scores_wide_exponents():
     qbits = synth.f32_to_bf16_bits(q)
     wv = rng.standard_normal((B, T, H)).astype(np.float32)
     qt = workload.bf16_tensor(qbits, DEV)
+    gm = torch.full((B, T, (N + 31) // 32), -1, dtype=torch.int32, device=DEV)
     scores, row_len = csa2.index_score(qt, torch.from_numpy(wv).to(DEV), torch.from_numpy(kc).to(DEV),
-                                       torch.from_numpy(ks).to(DEV))
+                                       torch.from_numpy(ks).to(DEV), group_max=gm)
     torch.cuda.synchronize()
     for b in range(B):
         for t in range(T):
             qc, qs = oracle.quant_mxfp4(f32(qbits[b, t]))
             s_ref = oracle.index_scores(qc, qs, wv[b, t], kc[b], ks[b], np.arange(N))
             assert same_f32(scores[b, t].cpu().numpy(), s_ref)
+            # groups re-scored by the exact pass carry the exact scores' maxima
+            assert np.array_equal(gm[b, t].cpu().numpy().view(np.uint32), group_keys(s_ref))
 
 
 def test_pool_scores_and_topk():
@@ -171,6 +209,7 @@ def test_pool_scores_and_topk():
     scores, row_len = csa2.index_score(dw["q_idx"], dw["w_idx"], dw["k_codes"], dw["k_scales"],
                                        dw["q_pos"], 1, pool, w.block, st)
     idx = csa2.topk(scores, w.topk, row_len, pool, w.block, d_status=st)
+    _, gm, idx_g = _with_group_max(dw, w, pool, st)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     qi_all, ww_all, _ = synth.gen_queries(w)
@@ -184,6 +223,9 @@ def test_pool_scores_and_topk():
             assert int(row_len[b, t]) == pos.size
             s_ref = _oracle_row_scores(w, b, t, qi_all[b], ww_all[b], kc, ks, pos)
             assert same_f32(scores[b, t, :pos.size].cpu().numpy(), s_ref)
+            ng = (pos.size + 31) // 32
+            assert np.array_equal(gm[b, t, :ng].cpu().numpy().view(np.uint32), group_keys(s_ref))
+            assert np.array_equal(idx_g[b, t].cpu().numpy(), idx[b, t].cpu().numpy())
             idx_ref, _, _ = oracle.reindex_indexer(f32(qi_all[b, t]), ww_all[b, t], kc, ks,
                                                    int(qpos[b, t]), 1, pool_np[b, t], w.topk, w.block)
             assert np.array_equal(idx[b, t].cpu().numpy(), idx_ref)

@@ -16,8 +16,9 @@
 // The softmax runs in base 2: logits are scaled by sm_scale * log2(e), so every exponential
 // is one exp2f, and lse = m * ln 2 + log(l).
 // A CTA covers a contiguous span of tiles of one query row with an online softmax; when
-// a row is split over several CTAs, they form one thread-block cluster and merge their
-// (O, m, l) partials through distributed shared memory.  Each thread holds the next tile's FP4 half-row in
+// a row is split over several CTAs, they form one thread-block cluster: (m, l) go
+// through distributed shared memory, O partials through L2, and each CTA merges a
+// quarter-slice of the output dims.  Each thread holds the next tile's FP4 half-row in
 // registers while the current tile is multiplied, so the gather latency overlaps the MMAs.
 #include <cuda_bf16.h>
 #include <math.h>
@@ -39,12 +40,11 @@ constexpr int kQChunkBytes = kH * 128;            // 8 KB: 64 heads x 64 bf16
 constexpr uint32_t kTmemCols = 512;   // S^T [0,64), O^T block m at [64 + 64m, 128 + 64m)
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kMaxSplits = 7;          // CTAs (one cluster) per split row
-constexpr int kRecvRow = kH + 4;       // floats per received O^T row (padding against bank conflicts)
-constexpr int kRecvBytes = kKeys * kRecvRow * 4;   // one received 128-dim O^T block
 
 struct AttnTcParams {
     int32_t T, H, topk, window, n_swa, splits, tiles_per_split;
     float log2_scale;       // logit scale x log2(e): the softmax runs in base 2
+    float *part_o;          // split rows: [rows, splits, H, d_v] raw O partials (workspace)
     int64_t n_kv;
     const uint16_t *q;
     const uint8_t *kvc, *kvs;
@@ -84,11 +84,6 @@ __device__ __forceinline__ uint32_t map_peer(uint32_t local, uint32_t rank)
 __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v)
 {
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
-{
-    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
-                 : "memory");
 }
 __device__ __forceinline__ void cluster_sync()
 {
@@ -498,10 +493,11 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
         }
         if (tid < H && P.lse) P.lse[row * H + tid] = s_l[tid] > 0.0f ? s_m[tid] * kLn2 + logf(s_l[tid]) : -INFINITY;
     } else {
-        // Split row: the row's CTAs form one cluster (rank = split).  They exchange (m, l)
-        // through distributed shared memory, then each O^T block m (128 dims) is merged by
-        // CTA m % S from the peers' raw partials:
-        //   o = sum_s e^(m_s - M) O_s / sum_s e^(m_s - M) l_s,  lse = M + log(...)
+        // Split row: the row's CTAs form one cluster (rank = split).  Each publishes (m, l)
+        // to every rank through distributed shared memory and its raw O^T blocks to the
+        // workspace (they stay in L2); after one cluster barrier, O^T block m (128 dims)
+        // is merged by rank m % S from its own tensor memory and the others' partials:
+        //   o = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s,  lse = (M + log2 l) ln 2
         const int S = P.splits;
         if (tid < kH) {
             const uint32_t lm = tc::smem_u32(&s_mlx[split][0][tid]), ll = tc::smem_u32(&s_mlx[split][1][tid]);
@@ -510,8 +506,25 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
                 st_cluster_f32(map_peer(ll, (uint32_t)c), s_l[tid]);
             }
         }
+        float *mine = P.part_o + (row * S + split) * (int64_t)H * kDv;   // [H][d_v]
+#pragma unroll 1
+        for (int m = 0; m < 4; ++m) {
+            if (m % S == split) continue;
+            uint32_t r[32];
+            if (any_o) {
+                tc::tc_ld_32x32b_x32(tmem + ((uint32_t)(quad * 32) << 16) + 64 + 64 * m + hh0, r);
+                tc::tc_wait_ld();
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) r[j] = 0u;
+            }
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (hh0 + j < H) mine[(hh0 + j) * kDv + 128 * m + key_row] = __uint_as_float(r[j]);
+        }
+        __threadfence();
         tc::tc_fence_before();
-        cluster_sync();                   // every loop done: peers' key buffers are free
+        cluster_sync();                   // (m, l) and partials visible to the whole cluster
         tc::tc_fence_after();
         if (tid < kH) {
             float M = -INFINITY;
@@ -526,30 +539,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
             s_corr[tid] = L > 0.0f ? 1.0f / L : 0.0f;                 // 1/l per head
             if (split == 0 && tid < H && P.lse) P.lse[row * H + tid] = L > 0.0f ? M * kLn2 + logf(L) : -INFINITY;
         }
-        // send every O^T block this CTA does not merge to its owner: slot (block index
-        // among the owner's, source rank) of rows padded to kRecvRow floats
-#pragma unroll 1
-        for (int m = 0; m < 4; ++m) {
-            const int owner = m % S;
-            if (owner == split) continue;
-            uint32_t r[32];
-            if (any_o) {
-                tc::tc_ld_32x32b_x32(tmem + ((uint32_t)(quad * 32) << 16) + 64 + 64 * m + hh0, r);
-                tc::tc_wait_ld();
-            } else {
-#pragma unroll
-                for (int j = 0; j < 32; ++j) r[j] = 0u;
-            }
-            const int slot = (m / S) * (S - 1) + (split < owner ? split : split - 1);
-            const uint32_t dst = map_peer(tc::smem_u32(sm + (size_t)slot * kRecvBytes + key_row * kRecvRow * 4 + hh0 * 4),
-                                          (uint32_t)owner);
-#pragma unroll
-            for (int j = 0; j < 32; j += 4)
-                st_cluster_v4(dst + j * 4, r[j], r[j + 1], r[j + 2], r[j + 3]);
-        }
-        tc::tc_fence_before();
-        cluster_sync();                   // partials delivered; no remote access after this
-        tc::tc_fence_after();
+        __syncthreads();
 #pragma unroll 1
         for (int m = split; m < 4; m += S) {
             const int d = 128 * m + key_row;
@@ -570,17 +560,12 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
 #pragma unroll
                     for (int j = 0; j < 32; ++j) acc[j] += s_fac[sp][hh0 + j] * __uint_as_float(own[j]);
                 } else {
-                    const int slot = (m / S) * (S - 1) + (sp < split ? sp : sp - 1);
-                    const float *src = reinterpret_cast<const float *>(sm + (size_t)slot * kRecvBytes) +
-                                       key_row * kRecvRow + hh0;
+                    const float *src = P.part_o + (row * S + sp) * (int64_t)H * kDv + d;
+                    float v[32];
 #pragma unroll
-                    for (int j = 0; j < 32; j += 4) {
-                        const float4 v = *reinterpret_cast<const float4 *>(src + j);
-                        acc[j + 0] += s_fac[sp][hh0 + j + 0] * v.x;
-                        acc[j + 1] += s_fac[sp][hh0 + j + 1] * v.y;
-                        acc[j + 2] += s_fac[sp][hh0 + j + 2] * v.z;
-                        acc[j + 3] += s_fac[sp][hh0 + j + 3] * v.w;
-                    }
+                    for (int j = 0; j < 32; ++j) v[j] = hh0 + j < H ? __ldcg(src + (hh0 + j) * kDv) : 0.0f;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) acc[j] += s_fac[sp][hh0 + j] * v[j];
                 }
             }
 #pragma unroll
@@ -621,9 +606,12 @@ bool attn_tc_eligible(const csa2_attn_args &a)
            (!a.swa || ((uintptr_t)a.swa & 15) == 0) && ((uintptr_t)a.kv_codes & 15) == 0;
 }
 
-size_t attn_tc_ws_bytes(const csa2_attn_args &)
+size_t attn_tc_ws_bytes(const csa2_attn_args &a)
 {
-    return 0;     // split rows merge through distributed shared memory
+    int splits, per;
+    attn_tc_split(a, splits, per);
+    if (splits <= 1) return 0;
+    return (size_t)a.batch * a.n_q * splits * a.n_heads * (size_t)kDv * sizeof(float);
 }
 
 cudaError_t launch_attn_tc(const csa2_attn_args &a, uint16_t *out, float *lse, void *ws,
@@ -649,6 +637,7 @@ cudaError_t launch_attn_tc(const csa2_attn_args &a, uint16_t *out, float *lse, v
     P.lse = lse;
     P.d_status = d_status;
     attn_tc_split(a, P.splits, P.tiles_per_split);
+    P.part_o = static_cast<float *>(ws);
     const int64_t rows = (int64_t)a.batch * a.n_q;
     const int smem = kSmemBytes + 1024;
     cudaError_t e = cudaFuncSetAttribute(sparse_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);

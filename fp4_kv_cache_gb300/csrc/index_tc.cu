@@ -107,7 +107,7 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             tc::mbar_init(&S.full[s], 1 + 32);
-            tc::mbar_init(&S.empty[s], 1 + 4);
+            tc::mbar_init(&S.empty[s], 1);       // the MMA's commit
         }
         for (int i = 0; i < kAcc; ++i) {
             tc::mbar_init(&S.accf[i], 1);
@@ -327,24 +327,28 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
 #pragma unroll
         for (int h = 0; h < kNPad; ++h) wv[h] = S.w[h];
         for (int i = 0; i < ntiles; ++i) {
-            const int s = i % kStages, acc = i % kAcc;
-            const bool ok = tc::mbar_wait(&S.accf[acc], (uint32_t)(i / kAcc) & 1u, &S.abort_flag) &&
-                            tc::mbar_wait(&S.full[s], (uint32_t)(i / kStages) & 1u, &S.abort_flag);
+            const int acc = i % kAcc;
+            // the stage itself is not touched here: the MMA's completion frees it, and this
+            // position's scale bytes are read back from the tensor-memory copy the MMA used
+            const bool ok = tc::mbar_wait(&S.accf[acc], (uint32_t)(i / kAcc) & 1u, &S.abort_flag);
             if (!__all_sync(0xffffffffu, ok)) {   // the warp leaves together (aligned ops follow)
                 S.abort_flag = 1;
                 break;
             }
             tc::tc_fence_after();
-            uint32_t r[32];
-            tc::tc_ld_32x32b_x32(tmem + ((uint32_t)(quad * 32) << 16) + acc * kNPad, r);
+            uint32_t r[32], sf4[4];
+            const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+            tc::tc_ld_32x32b_x32(lane_base + acc * kNPad, r);
+            // the scale atom holds in lane L the words of rows L, L+32, L+64, L+96 (copied to
+            // every lane quadrant), so row quad*32+lane is word `quad` of this lane
+            asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(sf4[0]), "=r"(sf4[1]), "=r"(sf4[2]), "=r"(sf4[3])
+                         : "r"(lane_base + kColSfa + 4 * acc));
             tc::tc_wait_ld();
-            const uint32_t sfw = S.sfa[s][lane * 4 + quad];
+            const uint32_t sfw = quad == 0 ? sf4[0] : quad == 1 ? sf4[1] : quad == 2 ? sf4[2] : sf4[3];
             tc::tc_fence_before();
             __syncwarp();
-            if (lane == 0) {
-                tc::mbar_arrive(&S.acce[acc]);
-                tc::mbar_arrive(&S.empty[s]);
-            }
+            if (lane == 0) tc::mbar_arrive(&S.acce[acc]);
             const int64_t cand = c0 + (int64_t)i * kTile + m;
             uint32_t key = 0;
             if (cand < c1) {

@@ -21,7 +21,8 @@ constexpr int kTopkThreads = 1024;
 __device__ __forceinline__ int64_t cand_pos(const int32_t *pool_row, int32_t block, int64_t i)
 {
     if (!pool_row) return i;
-    return (int64_t)pool_row[i / block] * block + i % block;
+    const uint32_t u = (uint32_t)i, b = (uint32_t)block;    // candidates < 2^31: 32-bit division
+    return (int64_t)pool_row[u / b] * block + (int64_t)(u % b);
 }
 
 // Block-wide exclusive prefix count of a 1-bit flag (all threads must call).
@@ -83,7 +84,8 @@ __device__ __forceinline__ uint32_t block_excl_count_sum(uint32_t v, uint32_t *s
     return r;
 }
 
-__device__ void radix_select_row(const float *__restrict__ scores, int64_t n, const int32_t *__restrict__ row_len,
+__device__ __noinline__ void radix_select_row(const float *__restrict__ scores, int64_t n,
+                                              const int32_t *__restrict__ row_len,
                                  const int32_t *__restrict__ pool, int32_t block, int32_t k,
                                  int32_t *__restrict__ idx, float *__restrict__ out_scores, int64_t row)
 {
@@ -187,15 +189,13 @@ topk_radix_kernel(const float *__restrict__ scores, int64_t n, const int32_t *__
 // desc, position asc) gives the top-k, emitted in order.
 constexpr int kGThreads = 1024;
 constexpr int kGBins = 2048;
-constexpr int kGroupCap = 32768;        // group keys per row kept on chip
+constexpr int kGroupCap = 8192;         // group keys per row kept on chip (longer rows: wider groups)
 constexpr int kCandCap = 8192;          // candidates per row kept on chip
 
 struct GSmem {
-    uint32_t hist[kGBins];
-    uint32_t warp[33];
+    uint32_t hist[2][kGBins];    // double buffer: the next digit pass clears one while
+    uint32_t warp[33];           // the current one counts into the other
     uint32_t pick[2];
-    uint32_t total;
-    int overflow;
 };
 
 // One thread per group of 32 whose row starts 16-byte aligned: eight 16-byte loads in
@@ -248,16 +248,25 @@ __global__ void __launch_bounds__(256) group_max_kernel(const float *__restrict_
 // With all three passes: the exact key tau, and in need how many keys equal to tau belong
 // to the top k.  With the first `passes` only: tau with its unresolved low bits zero, a
 // lower bound of the exact key (need is then meaningless).
-__device__ uint32_t g_threshold(const uint32_t *keys, int n, uint32_t k, GSmem &S, uint32_t &need,
-                                int passes = 3)
+// Each pass: one histogram of the keys that match the digits found so far (the other
+// buffer is cleared meanwhile for the next pass), then warp 0 alone finds the digit: each
+// lane sums a chunk of bins (descending), a shuffle scan locates the chunk where the
+// count from the top reaches `remaining`, and the lanes split that chunk to find the bin.
+// Two barriers a pass.
+__device__ __forceinline__ uint32_t g_threshold(const uint32_t *keys, int n, uint32_t k, GSmem &S,
+                                             uint32_t &need, int passes)
 {
-    const int tid = threadIdx.x, lane = tid & 31;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     uint32_t prefix = 0, mask = 0, remaining = k;
     const int shifts[3] = {21, 10, 0}, widths[3] = {11, 11, 10};
+    for (int i = tid; i < kGBins; i += kGThreads) S.hist[0][i] = 0;
+    __syncthreads();
+#pragma unroll 1
     for (int pass = 0; pass < passes; ++pass) {
         const int shift = shifts[pass], nb = 1 << widths[pass];
-        for (int i = tid; i < kGBins; i += kGThreads) S.hist[i] = 0;
-        __syncthreads();
+        uint32_t *h = S.hist[pass & 1];
+        if (pass + 1 < passes)
+            for (int i = tid; i < kGBins; i += kGThreads) S.hist[(pass + 1) & 1][i] = 0;
         for (int base = 0; base < n; base += kGThreads) {
             const int i = base + tid;
             uint32_t key = 0;
@@ -270,25 +279,50 @@ __device__ uint32_t g_threshold(const uint32_t *keys, int n, uint32_t k, GSmem &
             if (act) {
                 const uint32_t digit = (key >> shift) & (uint32_t)(nb - 1);
                 const uint32_t peers = __match_any_sync(am, digit);
-                if (lane == __ffs(peers) - 1) atomicAdd(&S.hist[digit], (uint32_t)__popc(peers));
+                if (lane == __ffs(peers) - 1) atomicAdd(&h[digit], (uint32_t)__popc(peers));
             }
         }
         __syncthreads();
-        // thread t owns bins nb-1-2t and nb-2-2t (descending)
-        uint32_t t0 = 0, t1 = 0;
-        const int b0 = nb - 1 - 2 * tid;
-        if (b0 >= 0) t0 = S.hist[b0];
-        if (b0 - 1 >= 0) t1 = S.hist[b0 - 1];
-        uint32_t all;
-        uint32_t c = block_excl_count_sum(t0 + t1, S.warp, all);
-        if (b0 >= 0 && c < remaining && c + t0 >= remaining) { S.pick[0] = (uint32_t)b0; S.pick[1] = remaining - c; }
-        c += t0;
-        if (b0 - 1 >= 0 && c < remaining && c + t1 >= remaining) { S.pick[0] = (uint32_t)(b0 - 1); S.pick[1] = remaining - c; }
+        if (warp == 0) {
+            // chunk L = bins [nb - (L+1)*cw, nb - L*cw); the rotated read order keeps the
+            // 32 lanes on 32 different banks
+            const int cw = nb >> 5;
+            const int lo = nb - (lane + 1) * cw;
+            uint32_t sum = 0;                 // cw is 32 or 64: loads eight at a time
+#pragma unroll 8
+            for (int i = 0; i < cw; ++i) sum += h[lo + ((i + lane) & (cw - 1))];
+            uint32_t incl = sum;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += t;
+            }
+            const uint32_t excl = incl - sum;
+            int L = __ffs(__ballot_sync(0xffffffffu, excl < remaining && incl >= remaining)) - 1;
+            if (L < 0) L = 31;            // cannot happen (the matching keys number >= remaining)
+            const uint32_t above = __shfl_sync(0xffffffffu, excl, L);   // count in higher chunks
+            // chunk L split over the lanes: lane j takes q = cw / 32 bins, descending
+            const int q = cw >> 5, top = nb - 1 - L * cw - lane * q;
+            uint32_t t0 = h[top], t1 = q > 1 ? h[top - 1] : 0u;
+            uint32_t s2 = t0 + t1, inc2 = s2;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t t = __shfl_up_sync(0xffffffffu, inc2, o);
+                if (lane >= o) inc2 += t;
+            }
+            const uint32_t c = above + inc2 - s2;                      // count above my bins
+            if (c < remaining && c + t0 >= remaining) {
+                S.pick[0] = (uint32_t)top;
+                S.pick[1] = remaining - c;
+            } else if (q > 1 && c + t0 < remaining && c + t0 + t1 >= remaining) {
+                S.pick[0] = (uint32_t)(top - 1);
+                S.pick[1] = remaining - c - t0;
+            }
+        }
         __syncthreads();
         prefix |= S.pick[0] << shift;
         mask |= (uint32_t)(nb - 1) << shift;
         remaining = S.pick[1];
-        __syncthreads();
     }
     need = remaining;
     return prefix;
@@ -326,7 +360,6 @@ topk_gmax_kernel(const float *__restrict__ scores, int64_t n, const int32_t *__r
         return;
     }
     for (int g = tid; g < ng; g += kGThreads) s_g[g] = gkeys[row * G + g];
-    if (tid == 0) S.overflow = 0;
     __syncthreads();
     // a lower bound of the k-th largest group key is enough to keep every top-k element
     // (the groups above the bound are a superset of those above the exact key)
@@ -348,48 +381,58 @@ topk_gmax_kernel(const float *__restrict__ scores, int64_t n, const int32_t *__r
     }
     __syncthreads();
 
-    // gather candidates: one thread per candidate group, its elements >= tau0, in order
+    // gather candidates, in position order: one thread per candidate group reads its
+    // scores (groups of 32 as eight 16-byte loads, all in flight at once) and keeps a bit
+    // mask of its elements >= tau0; after a scan of the counts it walks the mask in a
+    // rolled loop, reading each selected score again (the lines are in L1 by then).  This
+    // code runs once per row, so it is kept small.
+    const bool vec = gs == 32 && ((reinterpret_cast<uintptr_t>(s) & 15u) == 0);   // 16-byte rows
     uint32_t n_c = 0;
+#pragma unroll 1
     for (uint32_t base = 0; base < n_cg; base += kGThreads) {
         const uint32_t j = base + tid;
-        // groups of 32 whose 32 scores lie inside the row buffer are read with eight 16-byte
-        // loads issued together; other groups element by element
-        uint32_t cnt = 0, sel = 0;
-        uint32_t kk[32];
+        uint32_t sel = 0;                                  // groups of 32: bit e = element e
+        uint32_t cnt = 0;
         int64_t g0 = 0;
-        const bool fast = gs == 32 && ((reinterpret_cast<uintptr_t>(s) & 15u) == 0);   // 16-byte rows
         if (j < n_cg) {
             g0 = (int64_t)s_g[j] * gs;
-            if (fast && g0 + 32 <= n) {
+            if (vec && g0 + 32 <= n) {
                 float4 f[8];
                 const float4 *src = reinterpret_cast<const float4 *>(s + g0);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) f[e] = src[e];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    kk[4 * e + 0] = score_key(f[e].x); kk[4 * e + 1] = score_key(f[e].y);
-                    kk[4 * e + 2] = score_key(f[e].z); kk[4 * e + 3] = score_key(f[e].w);
+                    sel |= (uint32_t)(score_key(f[e].x) >= tau0) << (4 * e);
+                    sel |= (uint32_t)(score_key(f[e].y) >= tau0) << (4 * e + 1);
+                    sel |= (uint32_t)(score_key(f[e].z) >= tau0) << (4 * e + 2);
+                    sel |= (uint32_t)(score_key(f[e].w) >= tau0) << (4 * e + 3);
                 }
-#pragma unroll
-                for (int e = 0; e < 32; ++e)
-                    sel |= (kk[e] >= tau0 && g0 + e < len ? 1u : 0u) << e;
+                if (g0 + 32 > len) sel &= len > g0 ? (1u << (len - g0)) - 1u : 0u;
                 cnt = __popc(sel);
             } else {
+#pragma unroll 1
                 for (int e = 0; e < gs && g0 + e < len; ++e) cnt += score_key(s[g0 + e]) >= tau0;
             }
         }
         uint32_t tot;
         uint32_t o = n_c + block_excl_count_sum(cnt, S.warp, tot);
-        if (n_c + tot > kCandCap) {                         // does not fit: fall back
-            if (tid == 0) S.overflow = 1;
-            break;
+        if (n_c + tot > kCandCap) {                        // does not fit on chip: fall back
+            radix_select_row(scores, n, row_len, pool, block, k, idx, out_scores, row);
+            return;
         }
         if (j < n_cg) {
-            if (fast && g0 + 32 <= n) {
-#pragma unroll
-                for (int e = 0; e < 32; ++e)
-                    if ((sel >> e) & 1u) { s_ck[o] = kk[e]; s_cp[o] = (int32_t)(g0 + e); ++o; }
+            if (vec && g0 + 32 <= n) {
+#pragma unroll 1
+                while (sel) {
+                    const int e = __ffs(sel) - 1;
+                    sel &= sel - 1u;
+                    s_ck[o] = score_key(s[g0 + e]);
+                    s_cp[o] = (int32_t)(g0 + e);
+                    ++o;
+                }
             } else {
+#pragma unroll 1
                 for (int e = 0; e < gs && g0 + e < len; ++e) {
                     const uint32_t key = score_key(s[g0 + e]);
                     if (key >= tau0) { s_ck[o] = key; s_cp[o] = (int32_t)(g0 + e); ++o; }
@@ -399,13 +442,9 @@ topk_gmax_kernel(const float *__restrict__ scores, int64_t n, const int32_t *__r
         n_c += tot;
     }
     __syncthreads();
-    if (S.overflow) {
-        radix_select_row(scores, n, row_len, pool, block, k, idx, out_scores, row);
-        return;
-    }
     // exact selection among the candidates (n_c >= k), emitted in position order
     uint32_t need;
-    const uint32_t tau = g_threshold(s_ck, (int)n_c, (uint32_t)k, S, need);
+    const uint32_t tau = g_threshold(s_ck, (int)n_c, (uint32_t)k, S, need, 3);
     const int crun = ((int)n_c + kGThreads - 1) / kGThreads;
     const int c0 = min(tid * crun, (int)n_c), c1 = min(c0 + crun, (int)n_c);
     uint32_t n_gt = 0, n_eq = 0;
@@ -413,15 +452,17 @@ topk_gmax_kernel(const float *__restrict__ scores, int64_t n, const int32_t *__r
         n_gt += s_ck[i] > tau;
         n_eq += s_ck[i] == tau;
     }
-    uint32_t t_eq, t_sel;
-    const uint32_t eq_before = block_excl_count_sum(n_eq, S.warp, t_eq);
-    const uint32_t take = eq_before >= need ? 0u : min(n_eq, need - eq_before);
-    uint32_t o = block_excl_count_sum(n_gt + take, S.warp, t_sel);
-    uint32_t ties = 0;
+    // one scan of (above, equal) counts packed in 16-bit halves (n_c <= kCandCap < 2^16):
+    // the candidates equal to tau taken are the first `need` in position order
+    uint32_t t_both;
+    const uint32_t before = block_excl_count_sum((n_gt << 16) | n_eq, S.warp, t_both);
+    const uint32_t eq_before = before & 0xffffu;
+    uint32_t o = (before >> 16) + min(eq_before, need);
+    uint32_t ties = eq_before;
     for (int i = c0; i < c1; ++i) {
         const uint32_t key = s_ck[i];
         bool sel = key > tau;
-        if (key == tau) sel = ties++ < take;
+        if (key == tau) sel = ties++ < need;
         if (sel && o < (uint32_t)k) {
             out[o] = (int32_t)cand_pos(pool_row, block, s_cp[i]);
             if (out_s) out_s[o] = s[s_cp[i]];

@@ -156,7 +156,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
     __shared__ int s_abort;
     __shared__ float s_mlx[kMaxSplits][2][kH];   // split row: every rank's (m, l) per head
     __shared__ float s_fac[kMaxSplits][kH];      // split row: e^(m_s - M)
-    __shared__ uint32_t s_lut[256];     // code byte -> bf16x2 of its two E2M1 values (scale 1)
+    __shared__ uint32_t s_lut[2][256];  // code byte -> bf16x2 of its two E2M1 values (scale 1);
+                                        // two copies, one per lane parity, halve bank conflicts
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t row = blockIdx.y;
@@ -190,7 +191,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
         if (byte & 8u) lo = -lo;
         if (byte & 0x80u) hi = -hi;
         const __nv_bfloat162 bb = __floats2bfloat162_rn(lo, hi);
-        s_lut[tid] = *reinterpret_cast<const uint32_t *>(&bb);
+        s_lut[0][tid] = *reinterpret_cast<const uint32_t *>(&bb);
+        s_lut[1][tid] = *reinterpret_cast<const uint32_t *>(&bb);
     }
     if (warp == 0) {
         tc::tmem_alloc(&s_tmem, kTmemCols);
@@ -272,22 +274,28 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
 #pragma unroll
                 for (int i = 0; i < 9; ++i) fast = fast && sb[i] >= 8u && sb[i] <= 250u;
                 if (fast) {
-                    // table value x 2^(e-127) in bf16: exact, every product stays normal
-#pragma unroll
+                    // table value x 2^(e-127) in bf16: exact, every product stays normal.  A
+                    // rolled loop over the 9 blocks keeps this code small (it is fetched
+                    // cold); the staged registers shift down one block per iteration.
+                    const uint32_t *lut = s_lut[lane & 1];
+#pragma unroll 1
                     for (int i = 0; i < 9; ++i) {
                         const int blk = part * 9 + i;             // 32-value block of the row
-                        const uint32_t w4[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+                        const uint32_t w4[4] = {raw[0].x, raw[0].y, raw[0].z, raw[0].w};
+                        const uint32_t sbi = sb[0];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) { raw[j] = raw[j + 1]; sb[j] = sb[j + 1]; }
                         const int c = blk >> 1;
                         uint8_t *base = sm + (c < 8 ? kOffK + c * kChunkBytes : kOffR);
                         const __nv_bfloat162 sc2 = __halves2bfloat162(
-                            __ushort_as_bfloat16((unsigned short)(sb[i] << 7)),
-                            __ushort_as_bfloat16((unsigned short)(sb[i] << 7)));
+                            __ushort_as_bfloat16((unsigned short)(sbi << 7)),
+                            __ushort_as_bfloat16((unsigned short)(sbi << 7)));
 #pragma unroll
                         for (int q4 = 0; q4 < 4; ++q4) {         // 8 values -> one 16-byte piece
                             uint32_t packed[4];
 #pragma unroll
                             for (int k = 0; k < 4; ++k) {
-                                const uint32_t t = s_lut[(w4[q4] >> (8 * k)) & 0xffu];
+                                const uint32_t t = lut[(w4[q4] >> (8 * k)) & 0xffu];
                                 const __nv_bfloat162 v = __hmul2(*reinterpret_cast<const __nv_bfloat162 *>(&t), sc2);
                                 packed[k] = *reinterpret_cast<const uint32_t *>(&v);
                             }

@@ -32,8 +32,6 @@ struct IndexParams {
     int32_t *row_len;
     uint32_t *gmax;              // optional [rows, G]: largest selection key of each 32-group
     int64_t G;
-    const uint32_t *seg_flags;   // non-null: [rows, n_seg]; only flagged segments are scored
-    int64_t n_seg;
     uint32_t *d_status;
 };
 
@@ -115,15 +113,6 @@ __global__ void __launch_bounds__(kThreads) index_score_exact_kernel(IndexParams
     const int64_t row = blockIdx.y;
     const int64_t b = row / P.n_q;
     const int H = P.H;
-    // segments this CTA scores: its own (blockIdx.x), or with seg_flags every flagged
-    // segment of the row (one CTA per row; it returns at once when none is flagged)
-    const int64_t n_seg = P.seg_flags ? P.n_seg : 1;
-    if (P.seg_flags) {
-        int any = 0;
-        for (int64_t i = tid; i < n_seg; i += kThreads) any |= P.seg_flags[row * n_seg + i] != 0u;
-        if (!__syncthreads_or(any)) return;
-    }
-
     for (int i = tid; i < 256; i += kThreads)
         s_lut[i] = (uint16_t)((e2m1_twice(i & 15u) & 0xff) | ((e2m1_twice(i >> 4) & 0xff) << 8));
     if (tid == 0) { s_len = 0; s_bad = 0; }
@@ -176,10 +165,8 @@ __global__ void __launch_bounds__(kThreads) index_score_exact_kernel(IndexParams
     }
 
     const int64_t kbase = b * P.n_keys;
-    for (int64_t seg = 0; seg < n_seg; ++seg) {
-        const int64_t seg_id = P.seg_flags ? seg : (int64_t)blockIdx.x;
-        if (P.seg_flags && P.seg_flags[row * n_seg + seg] == 0u) continue;
-        const int64_t c0 = seg_id * P.chunk;
+    {
+        const int64_t c0 = (int64_t)blockIdx.x * P.chunk;
         const int64_t c1 = min(c0 + P.chunk, len);
         // uniform trip count: every warp meets the group reduction below; c0 is a multiple
         // of 32, so each warp's 32 candidates form one group
@@ -202,11 +189,9 @@ __global__ void __launch_bounds__(kThreads) index_score_exact_kernel(IndexParams
 
 } // namespace
 
-// Exact CUDA-core scoring of every segment of `chunk` candidates (or, with seg_flags, of
-// the flagged segments only).
+// Exact CUDA-core scoring: one CTA per (segment of `chunk` candidates, query row).
 cudaError_t launch_index_exact(const csa2_index_args &a, float *scores, int32_t *row_len,
-                               const uint32_t *seg_flags, int64_t chunk, uint32_t *d_status,
-                               cudaStream_t s)
+                               uint32_t *d_status, cudaStream_t s)
 {
     IndexParams P;
     P.n_q = a.n_q;
@@ -227,18 +212,14 @@ cudaError_t launch_index_exact(const csa2_index_args &a, float *scores, int32_t 
     P.row_len = row_len;
     P.gmax = a.group_max;
     P.G = (P.n_cand + 31) / 32;
-    P.seg_flags = seg_flags;
     P.d_status = d_status;
     const int64_t rows = (int64_t)a.batch * a.n_q;
     if (rows == 0) return cudaSuccess;
-    if (chunk <= 0) {   // chunk so that the grid covers the GPU a few times over
-        chunk = 2048;
-        while (chunk > 256 && rows * ((P.n_cand + chunk - 1) / chunk) < 152 * 8) chunk /= 2;
-    }
+    int64_t chunk = 2048;          // so that the grid covers the GPU a few times over
+    while (chunk > 256 && rows * ((P.n_cand + chunk - 1) / chunk) < 152 * 8) chunk /= 2;
     P.chunk = chunk;
-    int64_t gx = (P.n_cand + chunk - 1) / chunk;
-    P.n_seg = gx > 0 ? gx : 1;
-    dim3 grid(seg_flags ? 1u : (unsigned)(gx > 0 ? gx : 1), (unsigned)rows);
+    const int64_t gx = (P.n_cand + chunk - 1) / chunk;
+    dim3 grid((unsigned)(gx > 0 ? gx : 1), (unsigned)rows);
     switch (a.head_dim) {
     case 32: index_score_exact_kernel<32><<<grid, kThreads, 0, s>>>(P); break;
     case 64: index_score_exact_kernel<64><<<grid, kThreads, 0, s>>>(P); break;
@@ -248,12 +229,12 @@ cudaError_t launch_index_exact(const csa2_index_args &a, float *scores, int32_t 
     return cudaGetLastError();
 }
 
+// Workspace of the tensor-core path: one tile counter per query row.
 size_t index_score_ws_bytes(const csa2_index_args &a)
 {
     if (!index_tc_eligible(a)) return 0;
-    int64_t splits, chunk;
-    index_tc_segments(a, splits, chunk);
-    return (size_t)((int64_t)a.batch * a.n_q * splits) * sizeof(uint32_t);
+    const size_t rows = (size_t)a.batch * a.n_q;
+    return (rows * sizeof(uint32_t) + 15) & ~(size_t)15;
 }
 
 cudaError_t launch_index_score(const csa2_index_args &a, float *scores, int32_t *row_len, void *ws,
@@ -261,14 +242,11 @@ cudaError_t launch_index_score(const csa2_index_args &a, float *scores, int32_t 
 {
     const int64_t rows = (int64_t)a.batch * a.n_q;
     if (rows == 0) return cudaSuccess;
-    if (!index_tc_eligible(a) || !ws) return launch_index_exact(a, scores, row_len, nullptr, 0, d_status, s);
-    int64_t splits, chunk;
-    index_tc_segments(a, splits, chunk);
-    uint32_t *flags = static_cast<uint32_t *>(ws);   // [rows, splits], written by every tensor-core CTA
-    cudaError_t e = launch_index_tc(a, scores, row_len, flags, splits, chunk, d_status, s);
+    if (!index_tc_eligible(a) || !ws) return launch_index_exact(a, scores, row_len, d_status, s);
+    uint32_t *tile_ctr = static_cast<uint32_t *>(ws);
+    cudaError_t e = cudaMemsetAsync(tile_ctr, 0, (size_t)rows * sizeof(uint32_t), s);
     if (e != cudaSuccess) return e;
-    // segments holding a position the tensor-core path cannot prove exact: re-score them
-    return launch_index_exact(a, scores, row_len, flags, chunk, d_status, s);
+    return launch_index_tc(a, scores, row_len, tile_ctr, d_status, s);
 }
 
 } // namespace csa2

@@ -44,17 +44,17 @@ constexpr int kSms = 152;
 
 struct TcParams {
     int32_t n_q, H, ratio_m, block, n_pool_blocks;
-    int64_t n_keys, n_cand, chunk;
+    int64_t n_keys, n_cand;
     const uint16_t *q;
     const float *w;
-    const uint8_t *ks;
+    const uint8_t *kc, *ks;
     const int32_t *q_pos, *pool;
     int pool_mode;
     float *scores;
     int32_t *row_len;
     uint32_t *gmax;          // optional [rows, G]: largest selection key of each 32-group
     int64_t G;
-    uint32_t *seg_flags;
+    uint32_t *tile_ctr;      // [rows]: next unclaimed tile of each row (zero at launch)
     uint32_t *d_status;
 };
 
@@ -64,11 +64,13 @@ struct TcSmem {
     uint32_t sfa[kStages][kTile];              // scale-factor atoms of the K tiles
     uint32_t sfb[kTile];                       // scale-factor atom of q
     uint64_t full[kStages], empty[kStages], accf[kAcc], acce[kAcc], qready;
+    int32_t tile[kStages];                     // tile held by each stage (-1: no more)
+    int32_t acc_tile[kAcc];                    // tile held by each accumulator
     float w[kNPad];
     int hmin[kNPad], hmax[kNPad];
     unsigned long long len;
     uint32_t tmem_base;
-    int abort_flag, unsafe, bad;
+    int abort_flag, bad;
     int q_span, q_min, q_max;
 };
 
@@ -88,6 +90,77 @@ __device__ __forceinline__ int64_t n_visible(const TcParams &P, int64_t row)
     int64_t v = (p + 1) / P.ratio_m;
     if (p + 1 < 0) v = 0;
     return v < 0 ? 0 : (v > P.n_keys ? P.n_keys : v);
+}
+
+// Four E2M1 codes (the low 16 bits, element 0 in the lowest nibble) as four int8 lanes of
+// twice their values.
+__device__ __forceinline__ int32_t twice4(uint32_t x)
+{
+    uint32_t r = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) r |= ((uint32_t)e2m1_twice((x >> (4 * i)) & 15u) & 0xffu) << (8 * i);
+    return (int32_t)r;
+}
+
+// Exact D_h of one position for head h = this lane (the rare positions the tensor-core
+// result cannot be proven exact for): per 32-value block the integer dot of twice the
+// E2M1 values (dp4a) and its dyadic sum rounded once to float32.  The key row is read by
+// all lanes at once; the query's codes and scales come from the B-operand copy in shared
+// memory (64-byte rows, 16-byte chunks XOR-swizzled by bits 1-2 of the row within its
+// group of 8).
+__device__ __forceinline__ float exact_head_dot(const uint8_t *kc, uint32_t sfw, const uint8_t *qb,
+                                                const uint8_t *qsf, int h)
+{
+    const int r8 = h & 7;
+    const uint8_t *qrow = qb + (h >> 3) * 512 + r8 * 64;
+    int I[4], E[4];
+#pragma unroll
+    for (int kb = 0; kb < 4; ++kb) {
+        const uint4 k = *reinterpret_cast<const uint4 *>(kc + 16 * kb);
+        const uint4 q = *reinterpret_cast<const uint4 *>(qrow + ((kb ^ ((r8 >> 1) & 3)) << 4));
+        const uint32_t k4[4] = {k.x, k.y, k.z, k.w}, q4[4] = {q.x, q.y, q.z, q.w};
+        int acc = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            acc = __dp4a(twice4(q4[j] & 0xffffu), twice4(k4[j] & 0xffffu), acc);
+            acc = __dp4a(twice4(q4[j] >> 16), twice4(k4[j] >> 16), acc);
+        }
+        I[kb] = acc;
+        E[kb] = ((int)qsf[h * 16 + kb] - 127) + ((int)((sfw >> (8 * kb)) & 255u) - 127) - 2;
+    }
+    return dyadic_sum_f32<4>(I, E);
+}
+
+// The warp re-scores its lanes flagged in `todo` exactly, one head per lane, chaining the
+// heads' terms in head order as the tensor-core path does; returns this lane's new score
+// (or `score` when the lane was not flagged).  Out of line: the hot loop keeps only the
+// call.
+__device__ __noinline__ float rescore_flagged(uint32_t todo, float score, uint32_t sfw, int64_t cand0,
+                                              const uint8_t *kc_row0, const int32_t *pool, int pool_mode,
+                                              int64_t n_keys, const uint8_t *qb, const uint8_t *qsf,
+                                              const float *w, int H)
+{
+    const int lane = threadIdx.x & 31;
+    while (todo) {
+        const int src = __ffs(todo) - 1;
+        todo &= todo - 1u;
+        const int64_t pc = cand0 + src;
+        int64_t pos = pc;
+        if (pool_mode) {
+            const int32_t id = pool[pc >> 3];
+            pos = (int64_t)(id < 0 ? 0 : id) * 8 + (pc & 7);
+            if (pos >= n_keys) pos = n_keys - 1;
+        }
+        const uint32_t psfw = __shfl_sync(0xffffffffu, sfw, src);
+        const float Dh = lane < H ? exact_head_dot(kc_row0 + pos * kRowBytes, psfw, qb, qsf, lane) : 0.0f;
+        float e = 0.0f;
+        for (int h = 0; h < H; ++h) {
+            const float d = __shfl_sync(0xffffffffu, Dh, h);
+            e = __fmaf_rn(w[h], d > 0.0f ? d : 0.0f, e);
+        }
+        if (lane == src) score = e;
+    }
+    return score;
 }
 
 // kCtasPerSm resident CTAs need every warp within its sub-partition's share of the register
@@ -110,12 +183,11 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
             tc::mbar_init(&S.empty[s], 1);       // the MMA's commit
         }
         for (int i = 0; i < kAcc; ++i) {
-            tc::mbar_init(&S.accf[i], 1);
+            tc::mbar_init(&S.accf[i], 2);        // the MMA's commit + the issuer's own arrive
             tc::mbar_init(&S.acce[i], 4);
         }
         tc::mbar_init(&S.qready, 1);
         S.abort_flag = 0;
-        S.unsafe = 0;
         S.bad = 0;
         S.len = 0;
         tc::fence_mbar_init();
@@ -155,24 +227,55 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
         if (P.row_len) P.row_len[row] = (int32_t)len;
         if (S.bad) dev_flag(P.d_status, CSA2_DEV_BAD_POOL);
     }
-    const int64_t c0 = (int64_t)blockIdx.x * P.chunk;
-    const int64_t c1 = min(c0 + P.chunk, len);
-    const int ntiles = c1 > c0 ? (int)((c1 - c0 + kTile - 1) / kTile) : 0;
+    // Tiles of the row: CTA c first takes the R consecutive tiles [cR, cR + R) (C CTAs in
+    // the row, R two tiles short of an even share; consecutive tiles keep the reads
+    // sequential); the rest are handed out one at a time from the row's counter, so the
+    // CTAs of a row finish together.  Each claim is
+    // made one tile ahead of its use, which hides the atomic's latency.  A stage carries
+    // its tile number from the producer to the MMA issuer (-1: no more tiles), an
+    // accumulator carries it on to the epilogue.
+    const int ntr = len > 0 ? (int)((len + kTile - 1) / kTile) : 0;
+    const int C = (int)gridDim.x;
+    const int R = ntr / C > 2 ? ntr / C - 2 : 0;
+    const int64_t c1 = len;
     const uint32_t tmem = S.tmem_base;
     const int64_t kbase = b * P.n_keys;
 
     if (warp == 0) {
         // ================= producer
         int issued = 0;
-        for (int i = 0; i < ntiles; ++i) {
+        uint32_t claim = 0;                       // lane 0: the next claim from the counter
+        if (lane == 0 && R == 0) claim = atomicAdd(&P.tile_ctr[row], 1u);
+        for (int i = 0;; ++i) {
             const int s = i % kStages;
             const uint32_t ph = (uint32_t)(i / kStages) & 1u;
             if (!__all_sync(0xffffffffu, tc::mbar_wait(&S.empty[s], ph ^ 1u, &S.abort_flag))) {
                 S.abort_flag = 1;
                 break;
             }
-            const int64_t t0 = c0 + (int64_t)i * kTile;
+            int t = 0;
+            if (i < R) {
+                t = (int)blockIdx.x * R + i;
+                if (lane == 0 && i == R - 1) claim = atomicAdd(&P.tile_ctr[row], 1u);
+            } else {
+                if (lane == 0) {
+                    t = R * C + (int)claim;
+                    if (t < ntr) claim = atomicAdd(&P.tile_ctr[row], 1u);
+                }
+                t = __shfl_sync(0xffffffffu, t, 0);
+            }
+            if (t >= ntr) {                       // end marker: 1 + 32 plain arrivals, no bytes
+                if (lane == 0) {
+                    S.tile[s] = -1;
+                    tc::mbar_arrive(&S.full[s]);
+                }
+                __syncwarp();
+                tc::mbar_arrive(&S.full[s]);
+                break;
+            }
+            const int64_t t0 = (int64_t)t * kTile;
             if (lane == 0) {
+                S.tile[s] = t;
                 if (!P.pool_mode) {
                     tc::mbar_arrive_expect_tx(&S.full[s], kTile * kRowBytes);
                     tc::tma_load_2d(S.a[s], &tmap, &S.full[s], 0, (int32_t)(kbase + t0));
@@ -220,18 +323,25 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
         }
     } else if (warp == 1) {
         // ================= MMA issuer
-        if (lane == 0 && ntiles > 0) {
+        if (lane == 0) {
             const uint32_t sfb_t = tmem + kColSfb;
             if (!tc::mbar_wait(&S.qready, 0, &S.abort_flag)) S.abort_flag = 1;
             tc::fence_proxy_async_smem();
             tc::tc_fence_after();
             if (!S.abort_flag)
                 tc::tc_cp_32x128b_warpx4(sfb_t, tc::smem_desc(tc::smem_u32(S.sfb), 512, 128, tc::kSwizzleNone));
-            for (int i = 0; i < ntiles && !S.abort_flag; ++i) {
+            for (int i = 0; !S.abort_flag; ++i) {
                 const int s = i % kStages, acc = i % kAcc;
                 if (!tc::mbar_wait(&S.acce[acc], ((uint32_t)(i / kAcc) & 1u) ^ 1u, &S.abort_flag) ||
                     !tc::mbar_wait(&S.full[s], (uint32_t)(i / kStages) & 1u, &S.abort_flag)) {
                     S.abort_flag = 1;
+                    break;
+                }
+                const int t = S.tile[s];
+                S.acc_tile[acc] = t;
+                if (t < 0) {                      // pass the end marker to the epilogue
+                    tc::mbar_arrive(&S.accf[acc]);
+                    tc::mbar_arrive(&S.accf[acc]);
                     break;
                 }
                 tc::fence_proxy_async_smem();
@@ -248,6 +358,7 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
                 }
                 tc::tc_commit(&S.empty[s]);
                 tc::tc_commit(&S.accf[acc]);
+                tc::mbar_arrive(&S.accf[acc]);    // releases acc_tile to the epilogue
             }
         }
         __syncwarp();
@@ -326,7 +437,7 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
         float wv[kNPad];
 #pragma unroll
         for (int h = 0; h < kNPad; ++h) wv[h] = S.w[h];
-        for (int i = 0; i < ntiles; ++i) {
+        for (int i = 0;; ++i) {
             const int acc = i % kAcc;
             // the stage itself is not touched here: the MMA's completion frees it, and this
             // position's scale bytes are read back from the tensor-memory copy the MMA used
@@ -335,6 +446,8 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
                 S.abort_flag = 1;
                 break;
             }
+            const int t = S.acc_tile[acc];
+            if (t < 0) break;                     // end marker (the same for the whole warp)
             tc::tc_fence_after();
             uint32_t r[32], sf4[4];
             const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
@@ -349,10 +462,11 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
             tc::tc_fence_before();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&S.acce[acc]);
-            const int64_t cand = c0 + (int64_t)i * kTile + m;
+            const int64_t cand = (int64_t)t * kTile + m;
             uint32_t key = 0;
+            bool unsafe = false;
+            float sc = 0.0f;
             if (cand < c1) {
-                float sc = 0.0f;
 #pragma unroll
                 for (int h = 0; h < kNPad; ++h) {
                     if (h < H) {
@@ -364,15 +478,21 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
                 const int e2 = (int)((sfw >> 16) & 255u), e3 = (int)(sfw >> 24);
                 const int kmin = min(min(e0, e1), min(e2, e3)) - 127;
                 const int kmax = max(max(e0, e1), max(e2, e3)) - 127;
-                const bool safe = (kmax - kmin) + q_span <= 9 && q_min + kmin - 2 >= -126 &&
-                                  q_max + kmax - 2 <= 100;
-                if (!safe) S.unsafe = 1;
+                unsafe = (kmax - kmin) + q_span > 9 || q_min + kmin - 2 < -126 || q_max + kmax - 2 > 100;
+            }
+            // rare: positions whose tensor-core result cannot be proven exact
+            const uint32_t todo = __ballot_sync(0xffffffffu, unsafe);
+            if (todo)
+                sc = rescore_flagged(todo, sc, sfw, (int64_t)t * kTile + quad * 32, P.kc + kbase * kRowBytes,
+                                     pool, P.pool_mode, P.n_keys, S.b,
+                                     reinterpret_cast<const uint8_t *>(S.sfb), S.w, H);
+            if (cand < c1) {
                 P.scores[row * P.n_cand + cand] = sc;
                 key = score_key(sc);
             }
             if (P.gmax) {            // this warp's 32 candidates are one aligned group
                 const uint32_t gk = __reduce_max_sync(0xffffffffu, key);
-                const int64_t g0 = c0 + (int64_t)i * kTile + quad * 32;
+                const int64_t g0 = (int64_t)t * kTile + quad * 32;
                 if (lane == 0 && g0 < c1) P.gmax[row * P.G + (g0 >> 5)] = gk;
             }
         }
@@ -384,11 +504,7 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
         tc::tc_fence_after();
         tc::tmem_dealloc(tmem, kTmemCols);
     }
-    if (tid == 0) {
-        // every CTA writes its segment's flag, so the flags need no clearing beforehand
-        P.seg_flags[row * gridDim.x + blockIdx.x] = (S.unsafe || S.abort_flag) ? 1u : 0u;
-        if (S.abort_flag) dev_flag(P.d_status, CSA2_DEV_TIMEOUT);
-    }
+    if (tid == 0 && S.abort_flag) dev_flag(P.d_status, CSA2_DEV_TIMEOUT);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
@@ -427,23 +543,19 @@ bool index_tc_eligible(const csa2_index_args &a)
     return encode_fn() != nullptr;
 }
 
-// Segment layout shared with the exact kernel: `splits` segments of `chunk` candidates.
-void index_tc_segments(const csa2_index_args &a, int64_t &splits, int64_t &chunk)
+// CTAs per query row: enough rows x CTAs to fill kCtasPerSm CTAs on every SM, at most one
+// per tile of the row.
+int64_t index_tc_ctas_per_row(const csa2_index_args &a)
 {
     const int64_t rows = (int64_t)a.batch * a.n_q;
     const int64_t n_cand = a.mode == CSA2_INDEX_POOL ? (int64_t)a.n_pool_blocks * a.block : a.n_keys;
-    splits = tc_splits(rows, n_cand);
-    const int64_t tiles = (n_cand + kTile - 1) / kTile;
-    chunk = ((tiles + splits - 1) / splits) * kTile;
-    if (chunk < kTile) chunk = kTile;
-    splits = (n_cand + chunk - 1) / chunk;
-    if (splits < 1) splits = 1;
+    return tc_splits(rows, n_cand);
 }
 
 cudaError_t launch_index_tc(const csa2_index_args &a, float *scores, int32_t *row_len,
-                            uint32_t *seg_flags, int64_t splits, int64_t chunk, uint32_t *d_status,
-                            cudaStream_t s)
+                            uint32_t *tile_ctr, uint32_t *d_status, cudaStream_t s)
 {
+    const int64_t splits = index_tc_ctas_per_row(a);
     const int64_t rows = (int64_t)a.batch * a.n_q;
     TcParams P;
     P.n_q = a.n_q;
@@ -454,9 +566,9 @@ cudaError_t launch_index_tc(const csa2_index_args &a, float *scores, int32_t *ro
     P.n_keys = a.n_keys;
     P.pool_mode = a.mode == CSA2_INDEX_POOL;
     P.n_cand = P.pool_mode ? (int64_t)a.n_pool_blocks * a.block : a.n_keys;
-    P.chunk = chunk;
     P.q = a.q;
     P.w = a.w;
+    P.kc = a.k_codes;
     P.ks = a.k_scales;
     P.q_pos = a.q_pos;
     P.pool = a.pool_blocks;
@@ -464,7 +576,7 @@ cudaError_t launch_index_tc(const csa2_index_args &a, float *scores, int32_t *ro
     P.row_len = row_len;
     P.gmax = a.group_max;
     P.G = (P.n_cand + 31) / 32;
-    P.seg_flags = seg_flags;
+    P.tile_ctr = tile_ctr;
     P.d_status = d_status;
 
     CUtensorMap map;

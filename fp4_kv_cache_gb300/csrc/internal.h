@@ -13,19 +13,18 @@ cudaError_t launch_dequant_mxfp4(const uint8_t *codes, int64_t ldc, const uint8_
                                  int64_t lds, int64_t rows, int64_t cols, void *y, bool y_bf16,
                                  int64_t ldy, cudaStream_t s);
 
-// Indexer scoring: tensor-core path where it applies (index_tc.cu) with an exact
-// re-score of flagged segments, else the exact CUDA-core kernel (index_score.cu).
+// Indexer scoring: tensor-core path where it applies (index_tc.cu; it re-scores the rare
+// positions it cannot prove exact on CUDA cores), else the exact CUDA-core kernel
+// (index_score.cu).
 size_t index_score_ws_bytes(const csa2_index_args &a);
 cudaError_t launch_index_score(const csa2_index_args &a, float *scores, int32_t *row_len, void *ws,
                                uint32_t *d_status, cudaStream_t s);
 cudaError_t launch_index_exact(const csa2_index_args &a, float *scores, int32_t *row_len,
-                               const uint32_t *seg_flags, int64_t chunk, uint32_t *d_status,
-                               cudaStream_t s);
+                               uint32_t *d_status, cudaStream_t s);
 bool index_tc_eligible(const csa2_index_args &a);
-void index_tc_segments(const csa2_index_args &a, int64_t &splits, int64_t &chunk);
+int64_t index_tc_ctas_per_row(const csa2_index_args &a);
 cudaError_t launch_index_tc(const csa2_index_args &a, float *scores, int32_t *row_len,
-                            uint32_t *seg_flags, int64_t splits, int64_t chunk, uint32_t *d_status,
-                            cudaStream_t s);
+                            uint32_t *tile_ctr, uint32_t *d_status, cudaStream_t s);
 
 // Top-K over rows of float scores (see csa2_topk).  ws: topk_ws_bytes(rows, n, k).
 size_t topk_ws_bytes(int64_t rows, int64_t n, int32_t k);

@@ -6,11 +6,10 @@
 // pools at start-up and forbids later allocations, a plug-in running inside a framework
 // that owns the device allocator, or a real-time decode loop that must not take the
 // allocator's locks or risk an out-of-memory error mid-step.  This entry point needs no
-// workspace argument: its scratch (the indexer's per-segment re-score flags) lives in a
+// workspace argument: its scratch (the indexer's per-row tile counters) lives in a
 // file-scope __device__ array that every GPU loading the library holds until the process
-// exits.  It calls no cudaMalloc, cudaFree or allocating library routine; every call's
-// tensor-core kernel writes all the flags it covers before the re-score pass reads them,
-// so nothing is carried over from an earlier call.
+// exits.  It calls no cudaMalloc, cudaFree or allocating library routine; the counters
+// are cleared with cudaMemsetAsync on the caller's stream inside each call.
 #include <cuda_runtime.h>
 #include <mutex>
 #include <stdint.h>
@@ -19,8 +18,8 @@
 
 namespace {
 
-// 65,536 flags (256 KB): one per (query row, segment) of the tensor-core indexer.  A
-// valid request needs at most max(B*T, 456) of them, so every valid request fits.
+// 65,536 words (256 KB): one tile counter per query row of the tensor-core indexer, so
+// requests of up to 65,536 query rows fit.
 constexpr size_t kScratchWords = 65536;
 static __device__ __align__(256) uint32_t g_index_scratch[kScratchWords];
 

@@ -258,12 +258,11 @@ __device__ __forceinline__ uint32_t g_threshold(const uint32_t *keys, int n, uin
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     uint32_t prefix = 0, mask = 0, remaining = k;
-    const int shifts[3] = {21, 10, 0}, widths[3] = {11, 11, 10};
     for (int i = tid; i < kGBins; i += kGThreads) S.hist[0][i] = 0;
     __syncthreads();
 #pragma unroll 1
     for (int pass = 0; pass < passes; ++pass) {
-        const int shift = shifts[pass], nb = 1 << widths[pass];
+        const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0), nb = pass < 2 ? 2048 : 1024;
         uint32_t *h = S.hist[pass & 1];
         if (pass + 1 < passes)
             for (int i = tid; i < kGBins; i += kGThreads) S.hist[(pass + 1) & 1][i] = 0;

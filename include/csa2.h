@@ -239,9 +239,9 @@ CSA2_API csa2_status csa2_sparse_attn(const csa2_attn_args *a, uint16_t *out, fl
 /* Scratch: a file-scope __device__ array of 65,536 32-bit words (256 KB), which every  */
 /* GPU that loads the library holds until the process exits.  A request whose workspace */
 /* (csa2_index_score_workspace_size) exceeds 256 KB is rejected with CSA2_ERR_WORKSPACE */
-/* before anything is launched; every valid request of this build fits.  The call makes */
-/* no cudaMalloc, cudaFree or other allocating call; its kernels on `stream` write every */
-/* scratch word they read before reading it.                                           */
+/* before anything is launched (it needs one word per query row, so up to 65,536 rows   */
+/* fit).  The call makes no cudaMalloc, cudaFree or other allocating call; it clears    */
+/* the scratch it uses with cudaMemsetAsync on `stream`.                                */
 /*                                                                                    */
 /* The first call on a device (with that device current) looks up the array's device   */
 /* address with cudaGetSymbolAddress and caches it; make that first call before any     */

@@ -14,7 +14,7 @@
 // columns) accumulate in tensor memory.  Softmax runs with one thread per key: per-head
 // maxima and sums are reduced across the 128 threads with a halving shuffle reduction.
 // The softmax runs in base 2: logits are scaled by sm_scale * log2(e), so every exponential
-// is one exp2f, and lse = m * ln 2 + log(l).
+// is one exp2f, and lse = (m + log2 l) ln 2.
 // A CTA covers a contiguous span of tiles of one query row with an online softmax; when
 // a row is split over several CTAs, they form one thread-block cluster: (m, l) go
 // through distributed shared memory, O partials through L2, and each CTA merges a
@@ -44,7 +44,7 @@ constexpr int kMaxSplits = 7;          // CTAs (one cluster) per split row
 struct AttnTcParams {
     int32_t T, H, topk, window, n_swa, splits, tiles_per_split;
     float log2_scale;       // logit scale x log2(e): the softmax runs in base 2
-    float *part_o;          // split rows: [rows, splits, H, d_v] raw O partials (workspace)
+    float *part_o;          // split rows: [rows, splits, 4 blocks, H, 128] raw O^T partials
     int64_t n_kv;
     const uint16_t *q;
     const uint8_t *kvc, *kvs;
@@ -85,6 +85,54 @@ __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v)
 {
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
+{
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+// Eight E2M1 codes (element 2i in the low nibble of byte i) -> four bf16x2 words of their
+// values times sc2, on the ALUs (no table in shared memory).  The bf16 bits of a magnitude
+// code c in 0..7 are looked up with byte permutes: high bytes {00,3F,3F,3F,40,40,40,40},
+// low bytes {00,00,80,C0,00,40,80,C0} (0, 0.5, 1, 1.5, 2, 3, 4, 6); the code's sign bit
+// is copied to bit 15 of its half with a sign-replicating permute.  The product with a
+// power of two sc2 is exact while it stays normal.
+__device__ __forceinline__ void e2m1x8_to_bf16(uint32_t w, __nv_bfloat162 sc2, uint32_t (&o)[4])
+{
+    const uint32_t mags = w & 0x77777777u, mhi = mags >> 16, w4 = w << 4;
+    const uint32_t h03 = prmt(0x3F3F3F00u, 0x40404040u, mags), l03 = prmt(0xC0800000u, 0xC0804000u, mags);
+    const uint32_t h47 = prmt(0x3F3F3F00u, 0x40404040u, mhi), l47 = prmt(0xC0800000u, 0xC0804000u, mhi);
+    uint32_t v[4] = {prmt(l03, h03, 0x5140u), prmt(l03, h03, 0x7362u), prmt(l47, h47, 0x5140u),
+                     prmt(l47, h47, 0x7362u)};
+    const uint32_t sel[4] = {0xC080u, 0xD191u, 0xE2A2u, 0xF3B3u};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        v[k] ^= prmt(w4, w, sel[k]) & 0x80008000u;
+        const __nv_bfloat162 x = __hmul2(*reinterpret_cast<const __nv_bfloat162 *>(&v[k]), sc2);
+        o[k] = *reinterpret_cast<const uint32_t *>(&x);
+    }
+}
+
+// 8 consecutive 32-bit TMEM columns of this warp's lane quadrant
+__device__ __forceinline__ void tmem_ld_x8(uint32_t taddr, uint32_t (&r)[8])
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                   "=r"(r[7])
+                 : "r"(taddr));
+}
+// bulk copy global -> this CTA's shared memory, completion counted on `bar`
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(tc::smem_u32(dst)), "l"(src), "r"(bytes), "r"(tc::smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_global()
+{
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 __device__ __forceinline__ void cluster_sync()
 {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -151,13 +199,11 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ float s_red[4][kH];
     __shared__ float s_m[kH], s_l[kH], s_corr[kH];
-    __shared__ uint64_t s_bar;
+    __shared__ uint64_t s_bar, s_bar_merge;
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
     __shared__ float s_mlx[kMaxSplits][2][kH];   // split row: every rank's (m, l) per head
     __shared__ float s_fac[kMaxSplits][kH];      // split row: e^(m_s - M)
-    __shared__ uint32_t s_lut[2][256];  // code byte -> bf16x2 of its two E2M1 values (scale 1);
-                                        // two copies, one per lane parity, halve bank conflicts
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t row = blockIdx.y;
@@ -180,20 +226,11 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
 
     if (tid == 0) {
         tc::mbar_init(&s_bar, 1);
+        tc::mbar_init(&s_bar_merge, 1);
         tc::fence_mbar_init();
         s_abort = 0;
     }
     if (tid < kH) { s_m[tid] = -INFINITY; s_l[tid] = 0.0f; }
-    {
-        // bf16 of the E2M1 values: sign bit 15, and the magnitude exactly (all fit in bf16)
-        const uint32_t byte = (uint32_t)tid;
-        float lo = e2m1_mag(byte & 7u), hi = e2m1_mag((byte >> 4) & 7u);
-        if (byte & 8u) lo = -lo;
-        if (byte & 0x80u) hi = -hi;
-        const __nv_bfloat162 bb = __floats2bfloat162_rn(lo, hi);
-        s_lut[0][tid] = *reinterpret_cast<const uint32_t *>(&bb);
-        s_lut[1][tid] = *reinterpret_cast<const uint32_t *>(&bb);
-    }
     if (warp == 0) {
         tc::tmem_alloc(&s_tmem, kTmemCols);
         tc::tmem_relinquish();
@@ -274,31 +311,20 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
 #pragma unroll
                 for (int i = 0; i < 9; ++i) fast = fast && sb[i] >= 8u && sb[i] <= 250u;
                 if (fast) {
-                    // table value x 2^(e-127) in bf16: exact, every product stays normal.  A
-                    // rolled loop over the 9 blocks keeps this code small (it is fetched
-                    // cold); the staged registers shift down one block per iteration.
-                    const uint32_t *lut = s_lut[lane & 1];
-#pragma unroll 1
+                    // code value x 2^(e-127) in bf16: exact, every product stays normal
+#pragma unroll
                     for (int i = 0; i < 9; ++i) {
                         const int blk = part * 9 + i;             // 32-value block of the row
-                        const uint32_t w4[4] = {raw[0].x, raw[0].y, raw[0].z, raw[0].w};
-                        const uint32_t sbi = sb[0];
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) { raw[j] = raw[j + 1]; sb[j] = sb[j + 1]; }
+                        const uint32_t w4[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
                         const int c = blk >> 1;
                         uint8_t *base = sm + (c < 8 ? kOffK + c * kChunkBytes : kOffR);
                         const __nv_bfloat162 sc2 = __halves2bfloat162(
-                            __ushort_as_bfloat16((unsigned short)(sbi << 7)),
-                            __ushort_as_bfloat16((unsigned short)(sbi << 7)));
+                            __ushort_as_bfloat16((unsigned short)(sb[i] << 7)),
+                            __ushort_as_bfloat16((unsigned short)(sb[i] << 7)));
 #pragma unroll
                         for (int q4 = 0; q4 < 4; ++q4) {         // 8 values -> one 16-byte piece
                             uint32_t packed[4];
-#pragma unroll
-                            for (int k = 0; k < 4; ++k) {
-                                const uint32_t t = lut[(w4[q4] >> (8 * k)) & 0xffu];
-                                const __nv_bfloat162 v = __hmul2(*reinterpret_cast<const __nv_bfloat162 *>(&t), sc2);
-                                packed[k] = *reinterpret_cast<const uint32_t *>(&v);
-                            }
+                            e2m1x8_to_bf16(w4[q4], sc2, packed);
                             *reinterpret_cast<uint4 *>(base + sw128(r, (blk & 1) * 4 + q4)) =
                                 make_uint4(packed[0], packed[1], packed[2], packed[3]);
                         }
@@ -335,12 +361,14 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
                 }
             } else if (src <= -2) {
                 const uint16_t *srow = P.swa + (b * P.n_swa + (-src - 2)) * (int64_t)kDqk;
+#pragma unroll 4
                 for (int pc = part * 36; pc < part * 36 + 36; ++pc) {
                     const int c = pc >> 3;
                     uint8_t *base = sm + (c < 8 ? kOffK + c * kChunkBytes : kOffR);
                     cp_async_16(base + sw128(r, pc & 7), srow + pc * 8);
                 }
             } else {
+#pragma unroll 4
                 for (int pc = part * 36; pc < part * 36 + 36; ++pc) {
                     const int c = pc >> 3;
                     uint8_t *base = sm + (c < 8 ? kOffK + c * kChunkBytes : kOffR);
@@ -477,67 +505,92 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
         __syncthreads();
     }
 
-    // ---- epilogue: thread = (dim row of each O^T block, 32 heads)
+    // ---- epilogue: thread = (dim row of each O^T block, its 32 heads in chunks of 8); the
+    //      loops stay rolled, since this code runs once per CTA and is fetched cold
+    const uint32_t lane_t = tmem + ((uint32_t)(quad * 32) << 16);
     if (P.splits == 1) {
         if (tid < kH) s_corr[tid] = s_l[tid] > 0.0f ? 1.0f / s_l[tid] : 0.0f;   // 1/l per head
         __syncthreads();
 #pragma unroll 1
         for (int m = 0; m < 4; ++m) {
             const int d = 128 * m + key_row;
-            uint32_t r[32];
-            if (any_o) {
-                tc::tc_ld_32x32b_x32(tmem + ((uint32_t)(quad * 32) << 16) + 64 + 64 * m + hh0, r);
-                tc::tc_wait_ld();
-            } else {
+#pragma unroll 1
+            for (int h0 = hh0; h0 < hh0 + 32 && h0 < H; h0 += 8) {
+                uint32_t r[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+                if (any_o) {
+                    tmem_ld_x8(lane_t + 64 + 64 * m + h0, r);
+                    tc::tc_wait_ld();
+                }
 #pragma unroll
-                for (int j = 0; j < 32; ++j) r[j] = 0u;
-            }
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {          // fully unrolled: r stays in registers
-                const int h = hh0 + j;
-                if (h >= H) continue;
-                P.out[(row * H + h) * (int64_t)kDv + d] = bf16_bits(__uint_as_float(r[j]) * s_corr[h]);
+                for (int u = 0; u < 8; ++u)
+                    if (h0 + u < H)
+                        P.out[(row * H + h0 + u) * (int64_t)kDv + d] = bf16_bits(__uint_as_float(r[u]) * s_corr[h0 + u]);
             }
         }
-        if (tid < H && P.lse) P.lse[row * H + tid] = s_l[tid] > 0.0f ? s_m[tid] * kLn2 + logf(s_l[tid]) : -INFINITY;
+        if (tid < H && P.lse) P.lse[row * H + tid] = s_l[tid] > 0.0f ? (s_m[tid] + log2f(s_l[tid])) * kLn2 : -INFINITY;
     } else {
         // Split row: the row's CTAs form one cluster (rank = split).  Each publishes (m, l)
         // to every rank through distributed shared memory and its raw O^T blocks to the
-        // workspace (they stay in L2); after one cluster barrier, O^T block m (128 dims)
-        // is merged by rank m % S from its own tensor memory and the others' partials:
+        // workspace, laid out [row][split][block][head][128 dims] so that a block is one
+        // contiguous run; after one cluster barrier, O^T block m is merged by rank m % S:
+        // it pulls the other ranks' copies of the block into shared memory with bulk
+        // copies and adds them to its own (still in tensor memory):
         //   o = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s,  lse = (M + log2 l) ln 2
         const int S = P.splits;
+        const int64_t blk_floats = (int64_t)H * kKeys;                 // one block of a rank
         if (tid < kH) {
             const uint32_t lm = tc::smem_u32(&s_mlx[split][0][tid]), ll = tc::smem_u32(&s_mlx[split][1][tid]);
+#pragma unroll 1
             for (int c = 0; c < S; ++c) {
                 st_cluster_f32(map_peer(lm, (uint32_t)c), s_m[tid]);
                 st_cluster_f32(map_peer(ll, (uint32_t)c), s_l[tid]);
             }
         }
-        float *mine = P.part_o + (row * S + split) * (int64_t)H * kDv;   // [H][d_v]
 #pragma unroll 1
         for (int m = 0; m < 4; ++m) {
             if (m % S == split) continue;
-            uint32_t r[32];
-            if (any_o) {
-                tc::tc_ld_32x32b_x32(tmem + ((uint32_t)(quad * 32) << 16) + 64 + 64 * m + hh0, r);
-                tc::tc_wait_ld();
-            } else {
+            float *dst = P.part_o + ((row * S + split) * 4 + m) * blk_floats + key_row;
+#pragma unroll 1
+            for (int h0 = hh0; h0 < hh0 + 32 && h0 < H; h0 += 8) {
+                uint32_t r[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+                if (any_o) {
+                    tmem_ld_x8(lane_t + 64 + 64 * m + h0, r);
+                    tc::tc_wait_ld();
+                }
 #pragma unroll
-                for (int j = 0; j < 32; ++j) r[j] = 0u;
+                for (int u = 0; u < 8; ++u)
+                    if (h0 + u < H) dst[(h0 + u) * kKeys] = __uint_as_float(r[u]);
             }
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-                if (hh0 + j < H) mine[(hh0 + j) * kDv + 128 * m + key_row] = __uint_as_float(r[j]);
         }
+        fence_proxy_async_global();       // the bulk copies below read these stores
         __threadfence();
         tc::tc_fence_before();
         cluster_sync();                   // (m, l) and partials visible to the whole cluster
         tc::tc_fence_after();
+        // pull the other ranks' copies of the blocks this rank merges: slot (owned block k,
+        // rank sp != split) holds H x 128 floats; every CTA of the cluster is done with its
+        // key chunks by now, so they hold the slots
+        const int n_own = (4 - split + S - 1) / S;                       // blocks m = split + kS
+        if (tid == 0) {
+            fence_proxy_async_global();
+            tc::mbar_arrive_expect_tx(&s_bar_merge, (uint32_t)(n_own * (S - 1) * blk_floats * 4));
+#pragma unroll 1
+            for (int k = 0; k < n_own; ++k)
+#pragma unroll 1
+                for (int sp = 0; sp < S; ++sp) {
+                    if (sp == split) continue;
+                    const int slot = k * (S - 1) + (sp < split ? sp : sp - 1);
+                    bulk_g2s(sm + (size_t)slot * blk_floats * 4,
+                             P.part_o + ((row * S + sp) * 4 + split + k * S) * blk_floats,
+                             (uint32_t)(blk_floats * 4), &s_bar_merge);
+                }
+        }
         if (tid < kH) {
             float M = -INFINITY;
+#pragma unroll 1
             for (int sp = 0; sp < S; ++sp) M = fmaxf(M, s_mlx[sp][0][tid]);
             float L = 0.0f;
+#pragma unroll 1
             for (int sp = 0; sp < S; ++sp) {
                 const float ms = s_mlx[sp][0][tid];
                 const float e = ms == -INFINITY ? 0.0f : exp2f(ms - M);
@@ -545,42 +598,37 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
                 if (ms != -INFINITY) L += e * s_mlx[sp][1][tid];
             }
             s_corr[tid] = L > 0.0f ? 1.0f / L : 0.0f;                 // 1/l per head
-            if (split == 0 && tid < H && P.lse) P.lse[row * H + tid] = L > 0.0f ? M * kLn2 + logf(L) : -INFINITY;
+            if (split == 0 && tid < H && P.lse) P.lse[row * H + tid] = L > 0.0f ? (M + log2f(L)) * kLn2 : -INFINITY;
         }
+        if (n_own > 0 && !tc::mbar_wait(&s_bar_merge, 0, &s_abort)) s_abort = 1;
         __syncthreads();
 #pragma unroll 1
-        for (int m = split; m < 4; m += S) {
-            const int d = 128 * m + key_row;
-            uint32_t own[32];
-            if (any_o) {
-                tc::tc_ld_32x32b_x32(tmem + ((uint32_t)(quad * 32) << 16) + 64 + 64 * m + hh0, own);
-                tc::tc_wait_ld();
-            } else {
-#pragma unroll
-                for (int j = 0; j < 32; ++j) own[j] = 0u;
-            }
-            float acc[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) acc[j] = 0.0f;
+        for (int k = 0; k < n_own; ++k) {
+            const int m = split + k * S, d = 128 * m + key_row;
 #pragma unroll 1
-            for (int sp = 0; sp < S; ++sp) {
-                if (sp == split) {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) acc[j] += s_fac[sp][hh0 + j] * __uint_as_float(own[j]);
-                } else {
-                    const float *src = P.part_o + (row * S + sp) * (int64_t)H * kDv + d;
-                    float v[32];
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] = hh0 + j < H ? __ldcg(src + (hh0 + j) * kDv) : 0.0f;
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) acc[j] += s_fac[sp][hh0 + j] * v[j];
+            for (int h0 = hh0; h0 < hh0 + 32 && h0 < H; h0 += 8) {
+                uint32_t own[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+                if (any_o) {
+                    tmem_ld_x8(lane_t + 64 + 64 * m + h0, own);
+                    tc::tc_wait_ld();
                 }
-            }
+                float acc[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll 1
+                for (int sp = 0; sp < S; ++sp) {
+                    if (sp == split) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int h = hh0 + j;
-                if (h >= H) continue;
-                P.out[(row * H + h) * (int64_t)kDv + d] = bf16_bits(acc[j] * s_corr[h]);
+                        for (int u = 0; u < 8; ++u) acc[u] += s_fac[sp][h0 + u] * __uint_as_float(own[u]);
+                    } else {
+                        const int slot = k * (S - 1) + (sp < split ? sp : sp - 1);
+                        const float *src = reinterpret_cast<const float *>(sm) + slot * blk_floats + key_row;
+#pragma unroll
+                        for (int u = 0; u < 8; ++u)
+                            if (h0 + u < H) acc[u] += s_fac[sp][h0 + u] * src[(h0 + u) * kKeys];
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    if (h0 + u < H) P.out[(row * H + h0 + u) * (int64_t)kDv + d] = bf16_bits(acc[u] * s_corr[h0 + u]);
             }
         }
     }

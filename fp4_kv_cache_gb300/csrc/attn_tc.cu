@@ -114,25 +114,6 @@ __device__ __forceinline__ void e2m1x8_to_bf16(uint32_t w, __nv_bfloat162 sc2, u
     }
 }
 
-// 8 consecutive 32-bit TMEM columns of this warp's lane quadrant
-__device__ __forceinline__ void tmem_ld_x8(uint32_t taddr, uint32_t (&r)[8])
-{
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-                   "=r"(r[7])
-                 : "r"(taddr));
-}
-// bulk copy global -> this CTA's shared memory, completion counted on `bar`
-__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
-{
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                 ::"r"(tc::smem_u32(dst)), "l"(src), "r"(bytes), "r"(tc::smem_u32(bar)) : "memory");
-}
-__device__ __forceinline__ void fence_proxy_async_global()
-{
-    asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-
 __device__ __forceinline__ void cluster_sync()
 {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -199,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ float s_red[4][kH];
     __shared__ float s_m[kH], s_l[kH], s_corr[kH];
-    __shared__ uint64_t s_bar, s_bar_merge;
+    __shared__ uint64_t s_bar;
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
     __shared__ float s_mlx[kMaxSplits][2][kH];   // split row: every rank's (m, l) per head
@@ -219,14 +200,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
         const int64_t sl = (int64_t)tile * kKeys + key_row;
         return sl < P.topk ? P.idx[row * P.topk + sl] : 0;
     };
-    // the first two tiles' index entries are read before anything else, so their latency
-    // overlaps the set-up below
-    const int32_t id_first = slot_id(t_begin);
-    int32_t id_next = slot_id(t_begin + 1);
-
     if (tid == 0) {
         tc::mbar_init(&s_bar, 1);
-        tc::mbar_init(&s_bar_merge, 1);
         tc::fence_mbar_init();
         s_abort = 0;
     }
@@ -235,6 +210,13 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
         tc::tmem_alloc(&s_tmem, kTmemCols);
         tc::tmem_relinquish();
     }
+    // everything above touched no input: it overlaps the previous kernel's tail
+    pdl_wait();
+    pdl_allow_dependents();
+    // the first two tiles' index entries are read first, so their latency overlaps the
+    // set-up below
+    const int32_t id_first = slot_id(t_begin);
+    int32_t id_next = slot_id(t_begin + 1);
     // Q -> nine K-major chunks (rows = heads), zero rows for heads >= H
     for (int e = tid; e < kH * kChunks * 8; e += kThreads) {
         const int h = e / (kChunks * 8), rem = e % (kChunks * 8), c = rem >> 3, p = rem & 7;
@@ -505,8 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
         __syncthreads();
     }
 
-    // ---- epilogue: thread = (dim row of each O^T block, its 32 heads in chunks of 8); the
-    //      loops stay rolled, since this code runs once per CTA and is fetched cold
+    // ---- epilogue: thread = (dim row of each O^T block, its 32 heads)
     const uint32_t lane_t = tmem + ((uint32_t)(quad * 32) << 16);
     if (P.splits == 1) {
         if (tid < kH) s_corr[tid] = s_l[tid] > 0.0f ? 1.0f / s_l[tid] : 0.0f;   // 1/l per head
@@ -514,27 +495,26 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
 #pragma unroll 1
         for (int m = 0; m < 4; ++m) {
             const int d = 128 * m + key_row;
-#pragma unroll 1
-            for (int h0 = hh0; h0 < hh0 + 32 && h0 < H; h0 += 8) {
-                uint32_t r[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-                if (any_o) {
-                    tmem_ld_x8(lane_t + 64 + 64 * m + h0, r);
-                    tc::tc_wait_ld();
-                }
+            uint32_t r[32];
+            if (any_o) {
+                tc::tc_ld_32x32b_x32(lane_t + 64 + 64 * m + hh0, r);
+                tc::tc_wait_ld();
+            } else {
 #pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    if (h0 + u < H)
-                        P.out[(row * H + h0 + u) * (int64_t)kDv + d] = bf16_bits(__uint_as_float(r[u]) * s_corr[h0 + u]);
+                for (int j = 0; j < 32; ++j) r[j] = 0u;
             }
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (hh0 + j < H)
+                    P.out[(row * H + hh0 + j) * (int64_t)kDv + d] = bf16_bits(__uint_as_float(r[j]) * s_corr[hh0 + j]);
         }
         if (tid < H && P.lse) P.lse[row * H + tid] = s_l[tid] > 0.0f ? (s_m[tid] + log2f(s_l[tid])) * kLn2 : -INFINITY;
     } else {
         // Split row: the row's CTAs form one cluster (rank = split).  Each publishes (m, l)
         // to every rank through distributed shared memory and its raw O^T blocks to the
-        // workspace, laid out [row][split][block][head][128 dims] so that a block is one
-        // contiguous run; after one cluster barrier, O^T block m is merged by rank m % S:
-        // it pulls the other ranks' copies of the block into shared memory with bulk
-        // copies and adds them to its own (still in tensor memory):
+        // workspace ([row][split][block][head][128 dims]); after one cluster barrier, O^T
+        // block m is merged by rank m % S from its own copy (still in tensor memory) and
+        // the other ranks' copies, read through L2:
         //   o = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s,  lse = (M + log2 l) ln 2
         const int S = P.splits;
         const int64_t blk_floats = (int64_t)H * kKeys;                 // one block of a rank
@@ -550,41 +530,23 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
         for (int m = 0; m < 4; ++m) {
             if (m % S == split) continue;
             float *dst = P.part_o + ((row * S + split) * 4 + m) * blk_floats + key_row;
-#pragma unroll 1
-            for (int h0 = hh0; h0 < hh0 + 32 && h0 < H; h0 += 8) {
-                uint32_t r[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-                if (any_o) {
-                    tmem_ld_x8(lane_t + 64 + 64 * m + h0, r);
-                    tc::tc_wait_ld();
-                }
+            uint32_t r[32];
+            if (any_o) {                  // one load of the 32 columns, one wait
+                tc::tc_ld_32x32b_x32(lane_t + 64 + 64 * m + hh0, r);
+                tc::tc_wait_ld();
+            } else {
 #pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    if (h0 + u < H) dst[(h0 + u) * kKeys] = __uint_as_float(r[u]);
+                for (int j = 0; j < 32; ++j) r[j] = 0u;
             }
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (hh0 + j < H) dst[(hh0 + j) * kKeys] = __uint_as_float(r[j]);
         }
-        fence_proxy_async_global();       // the bulk copies below read these stores
         __threadfence();
         tc::tc_fence_before();
         cluster_sync();                   // (m, l) and partials visible to the whole cluster
         tc::tc_fence_after();
-        // pull the other ranks' copies of the blocks this rank merges: slot (owned block k,
-        // rank sp != split) holds H x 128 floats; every CTA of the cluster is done with its
-        // key chunks by now, so they hold the slots
         const int n_own = (4 - split + S - 1) / S;                       // blocks m = split + kS
-        if (tid == 0) {
-            fence_proxy_async_global();
-            tc::mbar_arrive_expect_tx(&s_bar_merge, (uint32_t)(n_own * (S - 1) * blk_floats * 4));
-#pragma unroll 1
-            for (int k = 0; k < n_own; ++k)
-#pragma unroll 1
-                for (int sp = 0; sp < S; ++sp) {
-                    if (sp == split) continue;
-                    const int slot = k * (S - 1) + (sp < split ? sp : sp - 1);
-                    bulk_g2s(sm + (size_t)slot * blk_floats * 4,
-                             P.part_o + ((row * S + sp) * 4 + split + k * S) * blk_floats,
-                             (uint32_t)(blk_floats * 4), &s_bar_merge);
-                }
-        }
         if (tid < kH) {
             float M = -INFINITY;
 #pragma unroll 1
@@ -600,36 +562,38 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
             s_corr[tid] = L > 0.0f ? 1.0f / L : 0.0f;                 // 1/l per head
             if (split == 0 && tid < H && P.lse) P.lse[row * H + tid] = L > 0.0f ? (M + log2f(L)) * kLn2 : -INFINITY;
         }
-        if (n_own > 0 && !tc::mbar_wait(&s_bar_merge, 0, &s_abort)) s_abort = 1;
         __syncthreads();
 #pragma unroll 1
         for (int k = 0; k < n_own; ++k) {
             const int m = split + k * S, d = 128 * m + key_row;
-#pragma unroll 1
-            for (int h0 = hh0; h0 < hh0 + 32 && h0 < H; h0 += 8) {
-                uint32_t own[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-                if (any_o) {
-                    tmem_ld_x8(lane_t + 64 + 64 * m + h0, own);
-                    tc::tc_wait_ld();
-                }
-                float acc[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll 1
-                for (int sp = 0; sp < S; ++sp) {
-                    if (sp == split) {
+            uint32_t own[32];
+            if (any_o) {
+                tc::tc_ld_32x32b_x32(lane_t + 64 + 64 * m + hh0, own);
+                tc::tc_wait_ld();
+            } else {
 #pragma unroll
-                        for (int u = 0; u < 8; ++u) acc[u] += s_fac[sp][h0 + u] * __uint_as_float(own[u]);
-                    } else {
-                        const int slot = k * (S - 1) + (sp < split ? sp : sp - 1);
-                        const float *src = reinterpret_cast<const float *>(sm) + slot * blk_floats + key_row;
-#pragma unroll
-                        for (int u = 0; u < 8; ++u)
-                            if (h0 + u < H) acc[u] += s_fac[sp][h0 + u] * src[(h0 + u) * kKeys];
-                    }
-                }
-#pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    if (h0 + u < H) P.out[(row * H + h0 + u) * (int64_t)kDv + d] = bf16_bits(acc[u] * s_corr[h0 + u]);
+                for (int j = 0; j < 32; ++j) own[j] = 0u;
             }
+            float acc[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) acc[j] = 0.0f;
+#pragma unroll 1
+            for (int sp = 0; sp < S; ++sp) {
+                if (sp == split) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) acc[j] += s_fac[sp][hh0 + j] * __uint_as_float(own[j]);
+                } else {                  // the peer's copy of block m, read through L2
+                    const float *src = P.part_o + ((row * S + sp) * 4 + m) * blk_floats + key_row;
+                    float v[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = hh0 + j < H ? __ldcg(src + (hh0 + j) * kKeys) : 0.0f;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) acc[j] += s_fac[sp][hh0 + j] * v[j];
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (hh0 + j < H) P.out[(row * H + hh0 + j) * (int64_t)kDv + d] = bf16_bits(acc[j] * s_corr[hh0 + j]);
         }
     }
     tc::tc_fence_before();
@@ -698,21 +662,9 @@ cudaError_t launch_attn_tc(const csa2_attn_args &a, uint16_t *out, float *lse, v
     const int smem = kSmemBytes + 1024;
     cudaError_t e = cudaFuncSetAttribute(sparse_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)P.splits, (unsigned)rows);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = (size_t)smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)P.splits;     // a row's CTAs: one cluster
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, sparse_attn_tc_kernel, P);
-    if (e != cudaSuccess) return e;
-    return cudaGetLastError();
+    // a row's CTAs form one cluster
+    return launch_pdl(sparse_attn_tc_kernel, dim3((unsigned)P.splits, (unsigned)rows), dim3(kThreads),
+                      (size_t)smem, s, (unsigned)P.splits, P);
 }
 
 } // namespace csa2

@@ -202,4 +202,12 @@ __device__ __forceinline__ float dyadic_sum_f32(const int (&I)[NB], const int (&
     return wide_sum_round_f32(NB, I, E);
 }
 
+// ------------------------------------------------------------------ dependent launch
+// A kernel launched with programmatic dependent launch waits here until the previous
+// kernel in the stream has completed and its writes are visible (immediately, when there
+// is no such kernel); pdl_allow_dependents lets the next kernel in the stream start its
+// own set-up early.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 } // namespace csa2

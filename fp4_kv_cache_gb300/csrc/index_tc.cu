@@ -199,6 +199,9 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
         tc::tmem_alloc(&S.tmem_base, kTmemCols);
         tc::tmem_relinquish();
     }
+    // everything above touched no input: it overlaps the previous kernel's tail
+    pdl_wait();
+    pdl_allow_dependents();
     // ---- valid candidates of this row (and pool checks): needed before streaming starts
     const int64_t n_vis = n_visible(P, row);
     const int32_t *pool = P.pool_mode ? P.pool + row * (int64_t)P.n_pool_blocks : nullptr;
@@ -598,9 +601,8 @@ cudaError_t launch_index_tc(const csa2_index_args &a, float *scores, int32_t *ro
     e = cudaFuncSetAttribute(index_score_tc_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                              (int)cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)splits, (unsigned)rows);
-    index_score_tc_kernel<<<grid, kThreads, smem, s>>>(map, P);
-    return cudaGetLastError();
+    return launch_pdl(index_score_tc_kernel, dim3((unsigned)splits, (unsigned)rows), dim3(kThreads), smem, s, 1,
+                      map, P);
 }
 
 } // namespace csa2

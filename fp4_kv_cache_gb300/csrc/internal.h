@@ -2,6 +2,7 @@
 #pragma once
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <utility>
 #include "../../include/csa2.h"
 
 namespace csa2 {
@@ -45,5 +46,36 @@ cudaError_t launch_attn_tc(const csa2_attn_args &a, uint16_t *out, float *lse, v
                            uint32_t *d_status, cudaStream_t s);
 cudaError_t launch_sparse_attn(const csa2_attn_args &a, uint16_t *out, float *lse, void *ws,
                                uint32_t *d_status, cudaStream_t s);
+
+// Launch with programmatic dependent launch: the kernel may start while the previous kernel
+// in the stream is still running, and must execute griddepcontrol.wait (pdl_wait) before it
+// reads anything that kernel writes.  cluster_x > 1 also groups consecutive CTAs along x
+// into clusters of that size.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t s, unsigned cluster_x, Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    unsigned n = 0;
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+    if (cluster_x > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = cluster_x;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
 
 } // namespace csa2

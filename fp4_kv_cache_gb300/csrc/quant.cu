@@ -55,6 +55,8 @@ __global__ void __launch_bounds__(256) quant_mxfp4_vec_kernel(const void *__rest
                                                               uint8_t *__restrict__ scales, int64_t lds,
                                                               uint32_t *d_status)
 {
+    pdl_wait();                                   // x may come from the kernel before
+    pdl_allow_dependents();
     const int64_t nblk_row = cols / 32;
     const int64_t total = rows * nblk_row * 4;                 // lanes of work
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -147,12 +149,10 @@ cudaError_t launch_quant_mxfp4(const void *x, bool x_bf16, int64_t rows, int64_t
     if (vec) {
         const int grid = grid_for(rows * (cols / 32) * 4, 256);
         if (x_bf16)
-            quant_mxfp4_vec_kernel<true><<<grid, 256, 0, s>>>(x, rows, cols, ldx, codes, ldc, scales,
-                                                              lds, d_status);
-        else
-            quant_mxfp4_vec_kernel<false><<<grid, 256, 0, s>>>(x, rows, cols, ldx, codes, ldc, scales,
-                                                               lds, d_status);
-        return cudaGetLastError();
+            return launch_pdl(quant_mxfp4_vec_kernel<true>, dim3(grid), dim3(256), 0, s, 1, x, rows, cols, ldx,
+                              codes, ldc, scales, lds, d_status);
+        return launch_pdl(quant_mxfp4_vec_kernel<false>, dim3(grid), dim3(256), 0, s, 1, x, rows, cols, ldx,
+                          codes, ldc, scales, lds, d_status);
     }
     const int grid = grid_for(rows * (cols / 32), 8);
     if (x_bf16)

@@ -339,6 +339,8 @@ topk_gmax_kernel(const float *__restrict__ scores, int64_t n, const int32_t *__r
     __shared__ GSmem S;
     const int tid = threadIdx.x;
     const int64_t row = blockIdx.x;
+    pdl_wait();                                            // scores come from the kernel before
+    pdl_allow_dependents();
     int64_t len = row_len ? (int64_t)row_len[row] : n;
     len = len < 0 ? 0 : (len > n ? n : len);
     const float *s = scores + row * n;
@@ -536,9 +538,8 @@ cudaError_t launch_topk(const float *scores, int64_t rows, int64_t n, const int3
     const size_t smem = (size_t)(kGroupCap + 2 * kCandCap) * sizeof(uint32_t);
     cudaError_t e = cudaFuncSetAttribute(topk_gmax_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    topk_gmax_kernel<<<(unsigned)rows, kGThreads, smem, s>>>(scores, n, row_len, pool, block, k, idx,
-                                                             out_scores, gkeys, gs, G);
-    return cudaGetLastError();
+    return launch_pdl(topk_gmax_kernel, dim3((unsigned)rows), dim3(kGThreads), smem, s, 1, scores, n, row_len,
+                      pool, block, k, idx, out_scores, gkeys, gs, G);
 }
 
 size_t block_candidates_ws_bytes(int64_t rows, int64_t n, int32_t block, int32_t nb)

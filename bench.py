@@ -223,8 +223,8 @@ def run_gpu(args):
                                 dw["swa_pos0"], dw["q_pos"], None, w.window, dw.sm_scale, w.d_v)
     lib = csa2.load()
     import ctypes
-    ws_index = torch.empty(max(1, lib.csa2_index_score_workspace_size(ctypes.byref(iargs))),
-                           dtype=torch.uint8, device=dev)
+    ws_index = torch.zeros(max(1, lib.csa2_index_score_workspace_size(ctypes.byref(iargs))),
+                           dtype=torch.uint8, device=dev)     # zero before first use
     ws_attn = torch.empty(max(1, lib.csa2_sparse_attn_workspace_size(ctypes.byref(aargs))),
                           dtype=torch.uint8, device=dev)
     ws_topk = torch.empty(max(1, lib.csa2_topk_workspace_size(B * T, w.n_keys, w.topk)),
@@ -272,26 +272,33 @@ def run_gpu(args):
     if int(st.item()) != 0:
         raise RuntimeError(f"device status {int(st.item())}")
 
-    # ---- the step as a CUDA graph (no host launch gaps), with timing events between calls
+    # ---- the step as CUDA graphs (no host launch gaps): one plain, timed as the step (its
+    #      kernels follow one another directly, so each may start its set-up while the
+    #      previous one finishes), and one with timing events between the calls, replayed
+    #      separately for the per-call breakdown
     names = ["cache_write_quant", "index_score", "topk", "sparse_attn"]
-    graph, g_ev = None, None
+    graph, graph_ev, g_ev = None, None, None
     try:
         g_ev = tuple(torch.cuda.Event(enable_timing=True, external=True) for _ in range(5))
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
+            step()
+        graph_ev = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_ev):
             step(g_ev)
         for _ in range(args.warmup):
             graph.replay()
+            graph_ev.replay()
         torch.cuda.synchronize(dev)
     except (TypeError, RuntimeError) as exc:          # no external events / capture: eager
-        graph, g_ev = None, None
+        graph, graph_ev, g_ev = None, None, None
         torch.cuda.synchronize(dev)
         print(f"# CUDA graph capture unavailable ({exc}); timing eager launches", file=sys.stderr)
     stream = torch.cuda.current_stream(dev)
 
     def run_step(k_ev=None):
         if graph is not None:
-            graph.replay()
+            (graph_ev if k_ev is not None else graph).replay()
         else:
             step(k_ev)
 
@@ -304,15 +311,20 @@ def run_gpu(args):
         for _ in range(args.steps):
             flush.fill_(1)
             e0, e1 = ev(), ev()
-            k_ev = g_ev if graph is not None else tuple(ev() for _ in range(5))
             e0.record(stream)
-            run_step(k_ev)
+            run_step()
             e1.record(stream)
             e1.synchronize()
             ms_steps.append(e0.elapsed_time(e1))
-            for i, n in enumerate(names):
-                per_k[n].append(k_ev[i].elapsed_time(k_ev[i + 1]))
         torch.cuda.synchronize(dev)
+    for _ in range(args.steps):                       # per-call breakdown (not the step time)
+        flush.fill_(1)
+        k_ev = g_ev if graph is not None else tuple(ev() for _ in range(5))
+        run_step(k_ev)
+        k_ev[4].synchronize()
+        for i, n in enumerate(names):
+            per_k[n].append(k_ev[i].elapsed_time(k_ev[i + 1]))
+    torch.cuda.synchronize(dev)
     per_kernel = {n: sum(v) / len(v) for n, v in per_k.items()}
     ms_step = sum(ms_steps) / len(ms_steps)
     ms_k = per_kernel["index_score"]
@@ -332,7 +344,7 @@ def run_gpu(args):
         dw["q_idx"].copy_(h_qi, non_blocking=True)
         dw["w_idx"].copy_(h_w, non_blocking=True)
         dw["q_attn"].copy_(h_qa, non_blocking=True)
-        run_step(g_ev if graph is not None else None)
+        run_step()
         h_out.copy_(out, non_blocking=True)
         e1.record(stream)
         e1.synchronize()

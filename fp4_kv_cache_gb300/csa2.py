@@ -136,7 +136,7 @@ def _ws(nbytes: int, device, workspace: Optional[torch.Tensor], stream=None):
         if workspace.numel() * workspace.element_size() < nbytes:
             raise ValueError("workspace too small")
         return _ptr(workspace), workspace.numel() * workspace.element_size()
-    w = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    w = torch.zeros(nbytes, dtype=torch.uint8, device=device)     # workspaces start zeroed
     if stream is not None:
         w.record_stream(stream)
     return _ptr(w), nbytes

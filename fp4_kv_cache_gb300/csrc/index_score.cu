@@ -229,12 +229,13 @@ cudaError_t launch_index_exact(const csa2_index_args &a, float *scores, int32_t 
     return cudaGetLastError();
 }
 
-// Workspace of the tensor-core path: one tile counter per query row.
+// Workspace of the tensor-core path: two counters per query row (tiles claimed, CTAs done),
+// zero between calls: the row's last CTA clears them.
 size_t index_score_ws_bytes(const csa2_index_args &a)
 {
     if (!index_tc_eligible(a)) return 0;
     const size_t rows = (size_t)a.batch * a.n_q;
-    return (rows * sizeof(uint32_t) + 15) & ~(size_t)15;
+    return (2 * rows * sizeof(uint32_t) + 15) & ~(size_t)15;
 }
 
 cudaError_t launch_index_score(const csa2_index_args &a, float *scores, int32_t *row_len, void *ws,
@@ -243,10 +244,7 @@ cudaError_t launch_index_score(const csa2_index_args &a, float *scores, int32_t 
     const int64_t rows = (int64_t)a.batch * a.n_q;
     if (rows == 0) return cudaSuccess;
     if (!index_tc_eligible(a) || !ws) return launch_index_exact(a, scores, row_len, d_status, s);
-    uint32_t *tile_ctr = static_cast<uint32_t *>(ws);
-    cudaError_t e = cudaMemsetAsync(tile_ctr, 0, (size_t)rows * sizeof(uint32_t), s);
-    if (e != cudaSuccess) return e;
-    return launch_index_tc(a, scores, row_len, tile_ctr, d_status, s);
+    return launch_index_tc(a, scores, row_len, static_cast<uint32_t *>(ws), d_status, s);
 }
 
 } // namespace csa2

@@ -54,7 +54,8 @@ struct TcParams {
     int32_t *row_len;
     uint32_t *gmax;          // optional [rows, G]: largest selection key of each 32-group
     int64_t G;
-    uint32_t *tile_ctr;      // [rows]: next unclaimed tile of each row (zero at launch)
+    uint32_t *tile_ctr;      // [rows]: claims from each row's shared tiles (zero at launch)
+    uint32_t *tile_done;     // [rows]: CTAs of the row done claiming (zero at launch)
     uint32_t *d_status;
 };
 
@@ -507,7 +508,15 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
         tc::tc_fence_after();
         tc::tmem_dealloc(tmem, kTmemCols);
     }
-    if (tid == 0 && S.abort_flag) dev_flag(P.d_status, CSA2_DEV_TIMEOUT);
+    if (tid == 0) {
+        if (S.abort_flag) dev_flag(P.d_status, CSA2_DEV_TIMEOUT);
+        // the row's last CTA to finish sets both counters back to zero for the next call
+        __threadfence();
+        if (atomicAdd(&P.tile_done[row], 1u) == gridDim.x - 1u) {
+            P.tile_ctr[row] = 0u;
+            P.tile_done[row] = 0u;
+        }
+    }
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
@@ -580,6 +589,7 @@ cudaError_t launch_index_tc(const csa2_index_args &a, float *scores, int32_t *ro
     P.gmax = a.group_max;
     P.G = (P.n_cand + 31) / 32;
     P.tile_ctr = tile_ctr;
+    P.tile_done = tile_ctr + rows;
     P.d_status = d_status;
 
     CUtensorMap map;

@@ -8,8 +8,9 @@
 // allocator's locks or risk an out-of-memory error mid-step.  This entry point needs no
 // workspace argument: its scratch (the indexer's per-row tile counters) lives in a
 // file-scope __device__ array that every GPU loading the library holds until the process
-// exits.  It calls no cudaMalloc, cudaFree or allocating library routine; the counters
-// are cleared with cudaMemsetAsync on the caller's stream inside each call.
+// exits.  It calls no cudaMalloc, cudaFree or allocating library routine; it clears the
+// counters it uses with cudaMemsetAsync on the caller's stream in each call, so a call
+// that timed out cannot leave stale counts behind.
 #include <cuda_runtime.h>
 #include <mutex>
 #include <stdint.h>
@@ -18,8 +19,8 @@
 
 namespace {
 
-// 65,536 words (256 KB): one tile counter per query row of the tensor-core indexer, so
-// requests of up to 65,536 query rows fit.
+// 65,536 words (256 KB): two counters per query row of the tensor-core indexer, so
+// requests of up to 32,768 query rows fit.
 constexpr size_t kScratchWords = 65536;
 static __device__ __align__(256) uint32_t g_index_scratch[kScratchWords];
 
@@ -62,6 +63,8 @@ csa2_status csa2_index_score_noalloc(const csa2_index_args *a, float *scores, in
         const csa2_status st = scratch_for_current_device(&ws);
         if (st != CSA2_OK) return st;
     }
+    if (need && cudaMemsetAsync(ws, 0, need, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return CSA2_ERR_CUDA;        // counters start from zero whatever an earlier call left
     return csa2_index_score(a, scores, row_len, ws, need, d_status, stream);
 }
 

@@ -150,6 +150,9 @@ typedef struct {
  * row_len [B, T] int32: the candidates 0..row_len-1 of each row are the valid ones
  * (FULL: n_vis; POOL: the pool positions that exist and are visible -- a prefix because
  * the pool is ascending).  Entries at or beyond row_len are left unwritten. */
+/* Workspace: per-row tile counters.  Zero-fill it before its first use; every call     */
+/* leaves it zero-filled again (a call that raised CSA2_DEV_TIMEOUT may not: zero it     */
+/* again before reusing it).                                                            */
 CSA2_API size_t csa2_index_score_workspace_size(const csa2_index_args *a);
 CSA2_API csa2_status csa2_index_score(const csa2_index_args *a, float *scores, int32_t *row_len,
                              void *ws, size_t ws_bytes, uint32_t *d_status, csa2_stream stream);
@@ -239,7 +242,7 @@ CSA2_API csa2_status csa2_sparse_attn(const csa2_attn_args *a, uint16_t *out, fl
 /* Scratch: a file-scope __device__ array of 65,536 32-bit words (256 KB), which every  */
 /* GPU that loads the library holds until the process exits.  A request whose workspace */
 /* (csa2_index_score_workspace_size) exceeds 256 KB is rejected with CSA2_ERR_WORKSPACE */
-/* before anything is launched (it needs one word per query row, so up to 65,536 rows   */
+/* before anything is launched (it needs two words per query row, so up to 32,768 rows  */
 /* fit).  The call makes no cudaMalloc, cudaFree or other allocating call; it clears    */
 /* the scratch it uses with cudaMemsetAsync on `stream`.                                */
 /*                                                                                    */

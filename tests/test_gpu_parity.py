@@ -8,6 +8,7 @@ a row-normwise reading of "max relative error" so that near-zero elements do not
 the ratio up; lse within 1e-3 absolute.  Every input comes from the seeded generator;
 the oracle quantises, scores, selects and attends with its own code.
 """
+import ctypes
 import math
 
 import numpy as np
@@ -229,6 +230,34 @@ def test_pool_scores_and_topk():
             idx_ref, _, _ = oracle.reindex_indexer(f32(qi_all[b, t]), ww_all[b, t], kc, ks,
                                                    int(qpos[b, t]), 1, pool_np[b, t], w.topk, w.block)
             assert np.array_equal(idx[b, t].cpu().numpy(), idx_ref)
+
+
+def test_index_workspace_left_zeroed():
+    """The indexer's workspace (per-row tile counters) must be zero-filled before its first
+    use and is left zero-filled by every call: three calls on one workspace agree bit for
+    bit, and the workspace reads all zero after each."""
+    w = SCORE_CASES["ragged_planted"]
+    dw = workload.build(w, kv=False, device=DEV)
+    args = csa2.make_index_args(dw["q_idx"], dw["w_idx"], dw["k_codes"], dw["k_scales"], dw["q_pos"],
+                                w.ratio_m)
+    need = csa2.load().csa2_index_score_workspace_size(ctypes.byref(args))
+    assert need > 0
+    ws = torch.zeros(need, dtype=torch.uint8, device=DEV)
+    outs = []
+    for _ in range(3):
+        sc = torch.empty((w.batch, w.n_q, w.n_keys), dtype=torch.float32, device=DEV)
+        rl = torch.empty((w.batch, w.n_q), dtype=torch.int32, device=DEV)
+        csa2.csa2_index_score(args, sc, rl, workspace=ws)
+        torch.cuda.synchronize()
+        assert int(ws.count_nonzero()) == 0
+        outs.append((sc, rl))
+    for sc, rl in outs[1:]:
+        assert torch.equal(rl, outs[0][1])
+        for b in range(w.batch):
+            for t in range(w.n_q):
+                L = int(rl[b, t])
+                assert np.array_equal(sc[b, t, :L].cpu().numpy().view(np.uint32),
+                                      outs[0][0][b, t, :L].cpu().numpy().view(np.uint32))
 
 
 def test_pool_flags_bad_order():

@@ -63,6 +63,17 @@ __device__ __forceinline__ uint32_t e2m1_encode(float x, float inv)
     return c | ((__float_as_uint(x) >> 28) & 8u);
 }
 
+// The E2M1 codes of two already scaled values (a to the low nibble, b to the high one) by
+// the hardware conversion: round to nearest, ties to even, saturating at 6, sign kept --
+// the rule of e2m1_encode, checked against it on the GPU over every rounding boundary.
+__device__ __forceinline__ uint32_t e2m1x2_cvt(float a_scaled, float b_scaled)
+{
+    uint16_t d;
+    asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u16.u8 %0, t;\n\t}"
+        : "=h"(d) : "f"(b_scaled), "f"(a_scaled));
+    return d;
+}
+
 // Magnitude of an E2M1 code's low 3 bits, as float.
 __device__ __forceinline__ float e2m1_mag(uint32_t c3)
 {

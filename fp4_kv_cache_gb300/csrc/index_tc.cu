@@ -400,7 +400,8 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
             for (int j = 0; j < 4; ++j) {
                 uint32_t word = 0;
 #pragma unroll
-                for (int e = 0; e < 8; ++e) word |= e2m1_encode(v[8 * j + e], inv) << (4 * e);
+                for (int e = 0; e < 8; e += 2)
+                    word |= e2m1x2_cvt(v[8 * j + e] * inv, v[8 * j + e + 1] * inv) << (4 * e);
                 packed[j] = word;
             }
             // row h, 16-byte chunk kb of the 64-byte row, XOR-swizzled by bits 1-2 of h%8
@@ -420,18 +421,18 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
             if (et < kNPad) S.w[et] = et < H ? P.w[row * H + et] : 0.0f;
             tc::fence_proxy_async_smem();
             asm volatile("bar.sync 1, 128;" ::: "memory");   // the four epilogue warps
-            if (warp == 2 && lane == 0) {
-                int span = 0, mn = 1 << 20, mx = -(1 << 20);
-                for (int h = 0; h < H; ++h) {
-                    if (S.hmin[h] > S.hmax[h]) continue;      // all-zero head
-                    span = max(span, S.hmax[h] - S.hmin[h]);
-                    mn = min(mn, S.hmin[h]);
-                    mx = max(mx, S.hmax[h]);
+            if (warp == 2) {                      // lane h: head h (kNPad = 32 lanes)
+                const int hmn = S.hmin[lane], hmx = S.hmax[lane];
+                const bool live = lane < H && hmn <= hmx;     // not an all-zero head
+                const int span = __reduce_max_sync(0xffffffffu, live ? hmx - hmn : 0);
+                const int mn = __reduce_min_sync(0xffffffffu, live ? hmn : (1 << 20));
+                const int mx = __reduce_max_sync(0xffffffffu, live ? hmx : -(1 << 20));
+                if (lane == 0) {
+                    S.q_span = span;
+                    S.q_min = mn;
+                    S.q_max = mx;
+                    tc::mbar_arrive(&S.qready);
                 }
-                S.q_span = span;
-                S.q_min = mn;
-                S.q_max = mx;
-                tc::mbar_arrive(&S.qready);
             }
             asm volatile("bar.sync 1, 128;" ::: "memory");
         }

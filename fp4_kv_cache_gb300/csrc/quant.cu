@@ -100,7 +100,7 @@ __global__ void __launch_bounds__(256) quant_mxfp4_vec_kernel(const void *__rest
         const float inv = pow2_neg(X);
         uint32_t word = 0;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) word |= e2m1_encode(v[i], inv) << (4 * i);
+        for (int i = 0; i < 8; i += 2) word |= e2m1x2_cvt(v[i] * inv, v[i + 1] * inv) << (4 * i);
         *reinterpret_cast<uint32_t *>(codes + r * ldc + kb * 16 + sub * 4) = word;
         if (sub == 0) scales[r * lds + kb] = (uint8_t)(X + 127);
     }

@@ -5,7 +5,7 @@
 // cores accelerate.  Per query row, the positions are a dense contraction
 //     D[t, h] = sum_d k_hat[t, d] * q_hat[h, d]      (t: 128-position tile, h: heads)
 // run as block-scaled MMA (kind::mxf4, E2M1 x E2M1, UE8M0 scale per 32) with M = 128
-// positions, N = 32 heads, K = 128 (two K = 64 steps).  The epilogue reads each
+// positions, N = 32 heads per query, K = 128 (two K = 64 steps).  The epilogue reads each
 // position's 32 head dots from tensor memory and forms s = fma32 chain of w_h * ReLU(D_h).
 //
 // Exactness.  The score is defined on D_h = RN32(exact dot).  Each K = 32 block adds an
@@ -15,11 +15,13 @@
 // condition conservatively per position from the scale bytes; a segment with any position
 // outside it is re-scored by the exact CUDA-core kernel (index_score.cu).
 //
-// Roles (192 threads): warp 0 = producer (TMA for the FP4 codes with the 64-byte swizzle,
-// cp.async for the scale bytes into the 512-byte scale-factor atom), warp 1 = MMA issuer
-// (tcgen05.cp of scale factors to TMEM, tcgen05.mma, tcgen05.commit), warps 2-5 =
-// epilogue (one TMEM lane quadrant each).  8-stage shared-memory ring, double-buffered
-// accumulators in TMEM.  One CTA scores one contiguous segment of one query row.
+// Roles: warp 0 = producer (TMA for the FP4 codes with the 64-byte swizzle, cp.async for
+// the scale bytes into the 512-byte scale-factor atom), warp 1 = MMA issuer (tcgen05.cp of
+// scale factors to TMEM, tcgen05.mma, tcgen05.commit), then the epilogue warps (each reads
+// its own TMEM lane quadrant).  A shared-memory ring of K tiles, accumulators rotating in
+// TMEM.  A CTA scores QG queries of one sequence (N = QG x 32): QG = 1 in decode, where
+// the CTAs of one query row share its tiles; QG = 4 in prefill chunks, where one K tile
+// feeds four queries' dots.
 #include <cudaTypedefs.h>
 #include <mutex>
 
@@ -33,14 +35,23 @@ namespace {
 constexpr int kD = 128;                // indexer head dim of this path
 constexpr int kRowBytes = kD / 2;      // 64 bytes of codes per position
 constexpr int kTile = 128;             // positions per tile (MMA M)
-constexpr int kStages = 8;
-constexpr int kThreads = 192;
-constexpr int kNPad = 32;              // MMA N: heads padded to 32
-constexpr int kAcc = 3;                // accumulator stages in TMEM
-constexpr uint32_t kTmemCols = 128;    // acc k at [32k, 32k+32), sfa k at [96+4k, 100+4k), sfb at [108,112)
-constexpr uint32_t kColSfa = 96, kColSfb = 108;
-constexpr int kCtasPerSm = 3;
+constexpr int kNPad = 32;              // heads per query, padded to 32
 constexpr int kSms = 152;
+
+// A CTA scores QG queries of one sequence against the same key tiles: MMA N = QG x 32
+// (queries x heads).  QG = 1 for decode (many CTAs per query row, 3 per SM); QG = 4 for
+// prefill chunks, where every query of a group sees nearly the same positions, so one
+// K tile feeds four queries' dots (one CTA per SM: its accumulators fill tensor memory).
+template <int QG> struct Cfg;
+template <> struct Cfg<1> {
+    static constexpr int kStages = 8, kAcc = 3, kEpiPerQuad = 1, kCtasPerSm = 3;
+    static constexpr uint32_t kTmemCols = 128, kColSfa = 96, kColSfb = 108;  // acc k at 32k
+};
+template <> struct Cfg<4> {
+    static constexpr int kStages = 12, kAcc = 2, kEpiPerQuad = 2, kCtasPerSm = 1;
+    static constexpr uint32_t kTmemCols = 512, kColSfa = 256, kColSfb = 264; // acc k at 128k
+};
+template <int QG> constexpr int kThreadsOf = 64 + 128 * Cfg<QG>::kEpiPerQuad;
 
 struct TcParams {
     int32_t n_q, H, ratio_m, block, n_pool_blocks;
@@ -54,33 +65,37 @@ struct TcParams {
     int32_t *row_len;
     uint32_t *gmax;          // optional [rows, G]: largest selection key of each 32-group
     int64_t G;
-    uint32_t *tile_ctr;      // [rows]: claims from each row's shared tiles (zero at launch)
-    uint32_t *tile_done;     // [rows]: CTAs of the row done claiming (zero at launch)
+    uint32_t *tile_ctr;      // [units]: claims from each unit's shared tiles (zero at launch)
+    uint32_t *tile_done;     // [units]: CTAs of the unit done (zero at launch)
     uint32_t *d_status;
 };
 
+template <int QG>
 struct TcSmem {
+    static constexpr int kStages = Cfg<QG>::kStages, kAcc = Cfg<QG>::kAcc;
     uint8_t a[kStages][kTile * kRowBytes];     // K codes, 64-byte swizzle, 1024-aligned
-    uint8_t b[kNPad * kRowBytes];              // q codes, same layout
+    uint8_t b[QG * kNPad * kRowBytes];         // q codes (row = query x 32 + head), same layout
     uint32_t sfa[kStages][kTile];              // scale-factor atoms of the K tiles
-    uint32_t sfb[kTile];                       // scale-factor atom of q
+    uint32_t sfb[kTile];                       // scale-factor atom of q (rows 0..QG*32-1)
     uint64_t full[kStages], empty[kStages], accf[kAcc], acce[kAcc], qready;
     int32_t tile[kStages];                     // tile held by each stage (-1: no more)
     int32_t acc_tile[kAcc];                    // tile held by each accumulator
-    float w[kNPad];
-    int hmin[kNPad], hmax[kNPad];
-    unsigned long long len;
+    alignas(16) float w[QG][kNPad];            // head weights, 0 for padded heads
+    int hmin[QG][kNPad], hmax[QG][kNPad];
+    unsigned long long len;                    // candidates of the group (its longest row)
+    int64_t qlen[QG];                          // candidates of each query (0: no query)
     uint32_t tmem_base;
     int abort_flag, bad;
-    int q_span, q_min, q_max;
+    int q_span[QG], q_min[QG], q_max[QG];
 };
 
 // instruction descriptor, kind::mxf4: A = B = E2M1 (1), UE8M0 scales, K-major A and B,
 // N at bits 17-22 (N/8), M at bits 24-28 (M/16), scale-factor ids at bits 4-5 (B) and
 // 29-30 (A) select the byte pair of the 32-bit scale column used by this K = 64 step.
+template <int QG>
 __device__ __forceinline__ uint32_t mxf4_idesc(int sf_id)
 {
-    return (1u << 7) | (1u << 10) | ((uint32_t)(kNPad >> 3) << 17) | (1u << 23) |
+    return (1u << 7) | (1u << 10) | ((uint32_t)((QG * kNPad) >> 3) << 17) | (1u << 23) |
            ((uint32_t)(kTile >> 4) << 24) | ((uint32_t)sf_id << 4) | ((uint32_t)sf_id << 29);
 }
 
@@ -110,10 +125,10 @@ __device__ __forceinline__ int32_t twice4(uint32_t x)
 // memory (64-byte rows, 16-byte chunks XOR-swizzled by bits 1-2 of the row within its
 // group of 8).
 __device__ __forceinline__ float exact_head_dot(const uint8_t *kc, uint32_t sfw, const uint8_t *qb,
-                                                const uint8_t *qsf, int h)
+                                                const uint8_t *qsf, int qi, int h)
 {
-    const int r8 = h & 7;
-    const uint8_t *qrow = qb + (h >> 3) * 512 + r8 * 64;
+    const int n = qi * kNPad + h, r8 = n & 7;               // B-operand row of (query, head)
+    const uint8_t *qrow = qb + (n >> 3) * 512 + r8 * 64;
     int I[4], E[4];
 #pragma unroll
     for (int kb = 0; kb < 4; ++kb) {
@@ -127,7 +142,7 @@ __device__ __forceinline__ float exact_head_dot(const uint8_t *kc, uint32_t sfw,
             acc = __dp4a(twice4(q4[j] >> 16), twice4(k4[j] >> 16), acc);
         }
         I[kb] = acc;
-        E[kb] = ((int)qsf[h * 16 + kb] - 127) + ((int)((sfw >> (8 * kb)) & 255u) - 127) - 2;
+        E[kb] = ((int)qsf[h * 16 + qi * 4 + kb] - 127) + ((int)((sfw >> (8 * kb)) & 255u) - 127) - 2;
     }
     return dyadic_sum_f32<4>(I, E);
 }
@@ -139,7 +154,7 @@ __device__ __forceinline__ float exact_head_dot(const uint8_t *kc, uint32_t sfw,
 __device__ __noinline__ float rescore_flagged(uint32_t todo, float score, uint32_t sfw, int64_t cand0,
                                               const uint8_t *kc_row0, const int32_t *pool, int pool_mode,
                                               int64_t n_keys, const uint8_t *qb, const uint8_t *qsf,
-                                              const float *w, int H)
+                                              const float *w, int qi, int H)
 {
     const int lane = threadIdx.x & 31;
     while (todo) {
@@ -153,7 +168,7 @@ __device__ __noinline__ float rescore_flagged(uint32_t todo, float score, uint32
             if (pos >= n_keys) pos = n_keys - 1;
         }
         const uint32_t psfw = __shfl_sync(0xffffffffu, sfw, src);
-        const float Dh = lane < H ? exact_head_dot(kc_row0 + pos * kRowBytes, psfw, qb, qsf, lane) : 0.0f;
+        const float Dh = lane < H ? exact_head_dot(kc_row0 + pos * kRowBytes, psfw, qb, qsf, qi, lane) : 0.0f;
         float e = 0.0f;
         for (int h = 0; h < H; ++h) {
             const float d = __shfl_sync(0xffffffffu, Dh, h);
@@ -164,18 +179,26 @@ __device__ __noinline__ float rescore_flagged(uint32_t todo, float score, uint32
     return score;
 }
 
-// kCtasPerSm resident CTAs need every warp within its sub-partition's share of the register
-// file (18 warps over 4 sub-partitions: at most 96 registers a thread); the bound makes
-// the compiler keep to it.
-__global__ void __launch_bounds__(kThreads, kCtasPerSm)
+// Registers: with QG = 1, three resident CTAs need every warp within its sub-partition's
+// share of the register file (18 warps over 4 sub-partitions: at most 96 registers a
+// thread); the launch bound makes the compiler keep to it.
+template <int QG>
+__global__ void __launch_bounds__(kThreadsOf<QG>, Cfg<QG>::kCtasPerSm)
 index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P)
 {
+    using C = Cfg<QG>;
+    constexpr int kStages = C::kStages, kAcc = C::kAcc, kN = QG * kNPad;
+    constexpr int kEpiWarps = 4 * C::kEpiPerQuad, kQPerWarp = QG / C::kEpiPerQuad;
     extern __shared__ uint8_t smem_raw[];
-    TcSmem &S = *reinterpret_cast<TcSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                            ~uintptr_t(1023));
+    TcSmem<QG> &S = *reinterpret_cast<TcSmem<QG> *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                    ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int64_t row = blockIdx.y;
-    const int64_t b = row / P.n_q;
+    // unit = the QG consecutive queries of one sequence this CTA scores (rows row0 ..)
+    const int64_t unit = blockIdx.y;
+    const int64_t groups = (P.n_q + QG - 1) / QG;
+    const int64_t b = unit / groups;
+    const int t0q = (int)(unit % groups) * QG;                 // first query of the group
+    const int64_t row0 = b * P.n_q + t0q;
     const int H = P.H;
 
     if (tid == 0) {
@@ -185,7 +208,7 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
         }
         for (int i = 0; i < kAcc; ++i) {
             tc::mbar_init(&S.accf[i], 2);        // the MMA's commit + the issuer's own arrive
-            tc::mbar_init(&S.acce[i], 4);
+            tc::mbar_init(&S.acce[i], kEpiWarps);
         }
         tc::mbar_init(&S.qready, 1);
         S.abort_flag = 0;
@@ -193,27 +216,32 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
         S.len = 0;
         tc::fence_mbar_init();
     }
-    if (tid < kNPad) { S.hmin[tid] = 1 << 20; S.hmax[tid] = -(1 << 20); }
+    if (tid < QG * kNPad) { S.hmin[tid >> 5][tid & 31] = 1 << 20; S.hmax[tid >> 5][tid & 31] = -(1 << 20); }
     if (tid < kTile) S.sfb[tid] = 0x7f7f7f7fu;
     if (warp == 0 && lane == 0) tc::prefetch_tmap(&tmap);
     if (warp == 1) {
-        tc::tmem_alloc(&S.tmem_base, kTmemCols);
+        tc::tmem_alloc(&S.tmem_base, C::kTmemCols);
         tc::tmem_relinquish();
     }
     // everything above touched no input: it overlaps the previous kernel's tail
     pdl_wait();
     pdl_allow_dependents();
-    // ---- valid candidates of this row (and pool checks): needed before streaming starts
-    const int64_t n_vis = n_visible(P, row);
-    const int32_t *pool = P.pool_mode ? P.pool + row * (int64_t)P.n_pool_blocks : nullptr;
+    // ---- valid candidates of the group's rows (and pool checks): needed before streaming
+    const int32_t *pool = P.pool_mode ? P.pool + row0 * (int64_t)P.n_pool_blocks : nullptr;
     const int64_t n_blk_all = (P.n_keys + P.block - 1) / P.block;
     __syncthreads();                                       // barrier init / len zero visible
     if (!P.pool_mode) {
-        if (tid == 0) S.len = (unsigned long long)n_vis;
-    } else {
+        if (tid < QG) {
+            const bool live = t0q + tid < P.n_q;
+            const int64_t nv = live ? n_visible(P, row0 + tid) : 0;
+            S.qlen[tid] = nv;
+            atomicMax(&S.len, (unsigned long long)nv);
+        }
+    } else {                                               // QG == 1 here
+        const int64_t n_vis = n_visible(P, row0);
         unsigned long long part = 0;
         int bad = 0;
-        for (int i = tid; i < P.n_pool_blocks; i += kThreads) {
+        for (int i = tid; i < P.n_pool_blocks; i += kThreadsOf<QG>) {
             const int32_t id = pool[i];
             const int32_t prev = i > 0 ? pool[i - 1] : -1;
             if (id >= 0) {
@@ -227,20 +255,21 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
     }
     __syncthreads();
     const int64_t len = (int64_t)S.len;
-    if (blockIdx.x == 0 && tid == 0) {
-        if (P.row_len) P.row_len[row] = (int32_t)len;
-        if (S.bad) dev_flag(P.d_status, CSA2_DEV_BAD_POOL);
+    if (P.pool_mode && tid == 0) S.qlen[0] = len;
+    __syncthreads();
+    if (blockIdx.x == 0 && tid < QG && t0q + tid < P.n_q) {
+        if (P.row_len) P.row_len[row0 + tid] = (int32_t)S.qlen[tid];
+        if (tid == 0 && S.bad) dev_flag(P.d_status, CSA2_DEV_BAD_POOL);
     }
-    // Tiles of the row: CTA c first takes the R consecutive tiles [cR, cR + R) (C CTAs in
-    // the row, R two tiles short of an even share; consecutive tiles keep the reads
-    // sequential); the rest are handed out one at a time from the row's counter, so the
-    // CTAs of a row finish together.  Each claim is
-    // made one tile ahead of its use, which hides the atomic's latency.  A stage carries
-    // its tile number from the producer to the MMA issuer (-1: no more tiles), an
-    // accumulator carries it on to the epilogue.
+    // Tiles of the group: CTA c first takes the R consecutive tiles [cR, cR + R) (C CTAs per
+    // group, R two tiles short of an even share; consecutive tiles keep the reads
+    // sequential); the rest are handed out one at a time from the group's counter, so its
+    // CTAs finish together.  Each claim is made one tile ahead of its use, which hides the
+    // atomic's latency.  A stage carries its tile number from the producer to the MMA
+    // issuer (-1: no more tiles), an accumulator carries it on to the epilogue.
     const int ntr = len > 0 ? (int)((len + kTile - 1) / kTile) : 0;
-    const int C = (int)gridDim.x;
-    const int R = ntr / C > 2 ? ntr / C - 2 : 0;
+    const int CT = (int)gridDim.x;
+    const int R = ntr / CT > 2 ? ntr / CT - 2 : 0;
     const int64_t c1 = len;
     const uint32_t tmem = S.tmem_base;
     const int64_t kbase = b * P.n_keys;
@@ -249,7 +278,7 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
         // ================= producer
         int issued = 0;
         uint32_t claim = 0;                       // lane 0: the next claim from the counter
-        if (lane == 0 && R == 0) claim = atomicAdd(&P.tile_ctr[row], 1u);
+        if (lane == 0 && R == 0) claim = atomicAdd(&P.tile_ctr[unit], 1u);
         for (int i = 0;; ++i) {
             const int s = i % kStages;
             const uint32_t ph = (uint32_t)(i / kStages) & 1u;
@@ -260,11 +289,11 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
             int t = 0;
             if (i < R) {
                 t = (int)blockIdx.x * R + i;
-                if (lane == 0 && i == R - 1) claim = atomicAdd(&P.tile_ctr[row], 1u);
+                if (lane == 0 && i == R - 1) claim = atomicAdd(&P.tile_ctr[unit], 1u);
             } else {
                 if (lane == 0) {
-                    t = R * C + (int)claim;
-                    if (t < ntr) claim = atomicAdd(&P.tile_ctr[row], 1u);
+                    t = R * CT + (int)claim;
+                    if (t < ntr) claim = atomicAdd(&P.tile_ctr[unit], 1u);
                 }
                 t = __shfl_sync(0xffffffffu, t, 0);
             }
@@ -328,7 +357,7 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
     } else if (warp == 1) {
         // ================= MMA issuer
         if (lane == 0) {
-            const uint32_t sfb_t = tmem + kColSfb;
+            const uint32_t sfb_t = tmem + C::kColSfb;
             if (!tc::mbar_wait(&S.qready, 0, &S.abort_flag)) S.abort_flag = 1;
             tc::fence_proxy_async_smem();
             tc::tc_fence_after();
@@ -350,15 +379,15 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
                 }
                 tc::fence_proxy_async_smem();
                 tc::tc_fence_after();
-                const uint32_t sfa_t = tmem + kColSfa + 4 * acc;
+                const uint32_t sfa_t = tmem + C::kColSfa + 4 * acc;
                 tc::tc_cp_32x128b_warpx4(sfa_t, tc::smem_desc(tc::smem_u32(S.sfa[s]), 512, 128,
                                                               tc::kSwizzleNone));
-                const uint32_t d_t = tmem + acc * kNPad;
+                const uint32_t d_t = tmem + acc * kN;
 #pragma unroll
                 for (int kk = 0; kk < 2; ++kk) {
                     const uint64_t ad = tc::smem_desc(tc::smem_u32(S.a[s]) + kk * 32, 16, 512, tc::kSwizzle64B);
                     const uint64_t bd = tc::smem_desc(tc::smem_u32(S.b) + kk * 32, 16, 512, tc::kSwizzle64B);
-                    tc::tc_mma_mxf4(d_t, ad, bd, mxf4_idesc(2 * kk), sfa_t, sfb_t, kk);
+                    tc::tc_mma_mxf4(d_t, ad, bd, mxf4_idesc<QG>(2 * kk), sfa_t, sfb_t, kk);
                 }
                 tc::tc_commit(&S.empty[s]);
                 tc::tc_commit(&S.accf[acc]);
@@ -367,81 +396,92 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
         }
         __syncwarp();
     } else {
-        // ================= epilogue warps: first the query (B operand), then the scores
-        {
-            // thread (h, kb) quantises block kb of head h on its own: 4 x 16-byte loads,
-            // a local maximum, 32 codes packed into one 16-byte store of the B operand
-            const int et = tid - 64, h = et >> 2, kb = et & 3;
-            uint4 raw[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
-                            make_uint4(0, 0, 0, 0)};
-            if (h < H) {
-                const uint4 *src = reinterpret_cast<const uint4 *>(P.q + row * (int64_t)H * kD + h * kD + kb * 32);
+        // ================= epilogue warps: first the queries (B operand), then the scores
+        const int et = tid - 64;
+        if (et < 128) {
+            // thread (h, kb) quantises block kb of head h of each query on its own: 4 x
+            // 16-byte loads, a local maximum, 32 codes packed into one 16-byte store
+            const int h = et >> 2, kb = et & 3;
+#pragma unroll 1
+            for (int qi = 0; qi < QG; ++qi) {
+                const bool live = h < H && t0q + qi < P.n_q;
+                uint4 raw[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
+                                make_uint4(0, 0, 0, 0)};
+                if (live) {
+                    const uint4 *src = reinterpret_cast<const uint4 *>(P.q + (row0 + qi) * (int64_t)H * kD +
+                                                                       h * kD + kb * 32);
 #pragma unroll
-                for (int j = 0; j < 4; ++j) raw[j] = src[j];
-            }
-            float v[32];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint32_t w4[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    v[8 * j + 2 * k] = __uint_as_float(w4[k] << 16);
-                    v[8 * j + 2 * k + 1] = __uint_as_float(w4[k] & 0xffff0000u);
+                    for (int j = 0; j < 4; ++j) raw[j] = src[j];
                 }
+                float v[32];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t w4[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        v[8 * j + 2 * k] = __uint_as_float(w4[k] << 16);
+                        v[8 * j + 2 * k + 1] = __uint_as_float(w4[k] & 0xffff0000u);
+                    }
+                }
+                uint32_t amax_bits = 0;
+#pragma unroll
+                for (int e = 0; e < 32; ++e) amax_bits = max(amax_bits, __float_as_uint(v[e]) & 0x7fffffffu);
+                const bool finite = amax_bits < 0x7f800000u;
+                const int X = mx_block_exponent(__uint_as_float(finite ? amax_bits : 0u));
+                const float inv = pow2_neg(X);
+                uint32_t packed[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    uint32_t word = 0;
+#pragma unroll
+                    for (int e = 0; e < 8; e += 2)
+                        word |= e2m1x2_cvt(v[8 * j + e] * inv, v[8 * j + e + 1] * inv) << (4 * e);
+                    packed[j] = word;
+                }
+                // B row n = query x 32 + head, 16-byte chunk kb of the 64-byte row,
+                // XOR-swizzled by bits 1-2 of n % 8; its scale byte (n%32)*16 + (n/32)*4 + kb
+                const int n = qi * kNPad + h, r8 = n & 7;
+                *reinterpret_cast<uint4 *>(S.b + (n >> 3) * 512 + r8 * 64 + ((kb ^ ((r8 >> 1) & 3)) << 4)) =
+                    make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                reinterpret_cast<uint8_t *>(S.sfb)[h * 16 + qi * 4 + kb] = (uint8_t)(X + 127);
+                // per-head exponent range over its non-zero blocks (the 4 blocks sit in 4 lanes)
+                int mn = (live && amax_bits != 0) ? X : (1 << 20);
+                int mx = (live && amax_bits != 0) ? X : -(1 << 20);
+                mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, 1));
+                mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, 2));
+                mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                if (kb == 0) { S.hmin[qi][h] = mn; S.hmax[qi][h] = mx; }
+                if (live && !finite) dev_flag(P.d_status, CSA2_DEV_NONFINITE);
+                if (et < kNPad)
+                    S.w[qi][et] = et < H && t0q + qi < P.n_q ? P.w[(row0 + qi) * H + et] : 0.0f;
             }
-            uint32_t amax_bits = 0;
-#pragma unroll
-            for (int e = 0; e < 32; ++e) amax_bits = max(amax_bits, __float_as_uint(v[e]) & 0x7fffffffu);
-            const bool finite = amax_bits < 0x7f800000u;
-            const int X = mx_block_exponent(__uint_as_float(finite ? amax_bits : 0u));
-            const float inv = pow2_neg(X);
-            uint32_t packed[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                uint32_t word = 0;
-#pragma unroll
-                for (int e = 0; e < 8; e += 2)
-                    word |= e2m1x2_cvt(v[8 * j + e] * inv, v[8 * j + e + 1] * inv) << (4 * e);
-                packed[j] = word;
-            }
-            // row h, 16-byte chunk kb of the 64-byte row, XOR-swizzled by bits 1-2 of h%8
-            const int r8 = h & 7;
-            *reinterpret_cast<uint4 *>(S.b + (h >> 3) * 512 + r8 * 64 + ((kb ^ ((r8 >> 1) & 3)) << 4)) =
-                make_uint4(packed[0], packed[1], packed[2], packed[3]);
-            reinterpret_cast<uint8_t *>(S.sfb)[h * 16 + kb] = (uint8_t)(X + 127);
-            // per-head exponent range over its non-zero blocks (the 4 blocks sit in 4 lanes)
-            int mn = (h < H && amax_bits != 0) ? X : (1 << 20);
-            int mx = (h < H && amax_bits != 0) ? X : -(1 << 20);
-            mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, 1));
-            mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-            mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, 2));
-            mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-            if (kb == 0) { S.hmin[h] = mn; S.hmax[h] = mx; }
-            if (h < H && !finite) dev_flag(P.d_status, CSA2_DEV_NONFINITE);
-            if (et < kNPad) S.w[et] = et < H ? P.w[row * H + et] : 0.0f;
             tc::fence_proxy_async_smem();
-            asm volatile("bar.sync 1, 128;" ::: "memory");   // the four epilogue warps
-            if (warp == 2) {                      // lane h: head h (kNPad = 32 lanes)
-                const int hmn = S.hmin[lane], hmx = S.hmax[lane];
+            asm volatile("bar.sync 1, 128;" ::: "memory");   // the first four epilogue warps
+            if (warp - 2 < QG) {                  // warp 2 + qi: query qi; lane h: head h
+                const int qi = warp - 2;
+                const int hmn = S.hmin[qi][lane], hmx = S.hmax[qi][lane];
                 const bool live = lane < H && hmn <= hmx;     // not an all-zero head
                 const int span = __reduce_max_sync(0xffffffffu, live ? hmx - hmn : 0);
                 const int mn = __reduce_min_sync(0xffffffffu, live ? hmn : (1 << 20));
                 const int mx = __reduce_max_sync(0xffffffffu, live ? hmx : -(1 << 20));
                 if (lane == 0) {
-                    S.q_span = span;
-                    S.q_min = mn;
-                    S.q_max = mx;
-                    tc::mbar_arrive(&S.qready);
+                    S.q_span[qi] = span;
+                    S.q_min[qi] = mn;
+                    S.q_max[qi] = mx;
                 }
             }
             asm volatile("bar.sync 1, 128;" ::: "memory");
+            if (et == 0) tc::mbar_arrive(&S.qready);
         }
-        const int quad = warp & 3;
+        // epilogue warp: TMEM lane quadrant `quad`, queries [q_lo, q_lo + kQPerWarp)
+        const int ew = warp - 2, quad = warp & 3, q_lo = (ew >> 2) * kQPerWarp;
         const int m = quad * 32 + lane;
-        const int q_span = S.q_span, q_min = S.q_min, q_max = S.q_max;
-        float wv[kNPad];
-#pragma unroll
-        for (int h = 0; h < kNPad; ++h) wv[h] = S.w[h];
+        const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+        // this warp's queries: candidates and exponent ranges (read once the first
+        // accumulator is full, which is after the queries were quantised)
+        int64_t qlen[kQPerWarp];
+        int qspan[kQPerWarp], qmin[kQPerWarp], qmax[kQPerWarp];
         for (int i = 0;; ++i) {
             const int acc = i % kAcc;
             // the stage itself is not touched here: the MMA's completion frees it, and this
@@ -453,52 +493,71 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
             }
             const int t = S.acc_tile[acc];
             if (t < 0) break;                     // end marker (the same for the whole warp)
+            if (i == 0) {
+#pragma unroll
+                for (int u = 0; u < kQPerWarp; ++u) {
+                    qlen[u] = S.qlen[q_lo + u];
+                    qspan[u] = S.q_span[q_lo + u];
+                    qmin[u] = S.q_min[q_lo + u];
+                    qmax[u] = S.q_max[q_lo + u];
+                }
+            }
             tc::tc_fence_after();
-            uint32_t r[32], sf4[4];
-            const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
-            tc::tc_ld_32x32b_x32(lane_base + acc * kNPad, r);
+            uint32_t sf4[4];
             // the scale atom holds in lane L the words of rows L, L+32, L+64, L+96 (copied to
             // every lane quadrant), so row quad*32+lane is word `quad` of this lane
             asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
                          : "=r"(sf4[0]), "=r"(sf4[1]), "=r"(sf4[2]), "=r"(sf4[3])
-                         : "r"(lane_base + kColSfa + 4 * acc));
+                         : "r"(lane_base + C::kColSfa + 4 * acc));
+            uint32_t r[kQPerWarp][32];
+#pragma unroll
+            for (int u = 0; u < kQPerWarp; ++u) tc::tc_ld_32x32b_x32(lane_base + acc * kN + (q_lo + u) * kNPad, r[u]);
             tc::tc_wait_ld();
             const uint32_t sfw = quad == 0 ? sf4[0] : quad == 1 ? sf4[1] : quad == 2 ? sf4[2] : sf4[3];
             tc::tc_fence_before();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&S.acce[acc]);
             const int64_t cand = (int64_t)t * kTile + m;
-            uint32_t key = 0;
-            bool unsafe = false;
-            float sc = 0.0f;
-            if (cand < c1) {
+            const int e0 = (int)(sfw & 255u), e1 = (int)((sfw >> 8) & 255u);
+            const int e2 = (int)((sfw >> 16) & 255u), e3 = (int)(sfw >> 24);
+            const int kmin = min(min(e0, e1), min(e2, e3)) - 127;
+            const int kmax = max(max(e0, e1), max(e2, e3)) - 127;
 #pragma unroll
-                for (int h = 0; h < kNPad; ++h) {
-                    if (h < H) {
-                        const float D = __uint_as_float(r[h]);
-                        sc = __fmaf_rn(wv[h], D > 0.0f ? D : 0.0f, sc);
+            for (int u = 0; u < kQPerWarp; ++u) {
+                const int qi = q_lo + u;
+                const bool valid = cand < qlen[u];
+                uint32_t key = 0;
+                // straight-line chain over all 32 head slots: a padded head has weight 0 and
+                // D = 0 (zero query codes), so its step adds +0 to a sum that is never -0
+                const float4 *w4 = reinterpret_cast<const float4 *>(S.w[qi]);
+                float sc = 0.0f;
+#pragma unroll
+                for (int h4 = 0; h4 < kNPad / 4; ++h4) {
+                    const float4 wv = w4[h4];
+                    const float wh[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const float D = __uint_as_float(r[u][4 * h4 + j]);
+                        sc = __fmaf_rn(wh[j], D > 0.0f ? D : 0.0f, sc);
                     }
                 }
-                const int e0 = (int)(sfw & 255u), e1 = (int)((sfw >> 8) & 255u);
-                const int e2 = (int)((sfw >> 16) & 255u), e3 = (int)(sfw >> 24);
-                const int kmin = min(min(e0, e1), min(e2, e3)) - 127;
-                const int kmax = max(max(e0, e1), max(e2, e3)) - 127;
-                unsafe = (kmax - kmin) + q_span > 9 || q_min + kmin - 2 < -126 || q_max + kmax - 2 > 100;
-            }
-            // rare: positions whose tensor-core result cannot be proven exact
-            const uint32_t todo = __ballot_sync(0xffffffffu, unsafe);
-            if (todo)
-                sc = rescore_flagged(todo, sc, sfw, (int64_t)t * kTile + quad * 32, P.kc + kbase * kRowBytes,
-                                     pool, P.pool_mode, P.n_keys, S.b,
-                                     reinterpret_cast<const uint8_t *>(S.sfb), S.w, H);
-            if (cand < c1) {
-                P.scores[row * P.n_cand + cand] = sc;
-                key = score_key(sc);
-            }
-            if (P.gmax) {            // this warp's 32 candidates are one aligned group
-                const uint32_t gk = __reduce_max_sync(0xffffffffu, key);
-                const int64_t g0 = (int64_t)t * kTile + quad * 32;
-                if (lane == 0 && g0 < c1) P.gmax[row * P.G + (g0 >> 5)] = gk;
+                const bool unsafe = valid && ((kmax - kmin) + qspan[u] > 9 || qmin[u] + kmin - 2 < -126 ||
+                                              qmax[u] + kmax - 2 > 100);
+                // rare: positions whose tensor-core result cannot be proven exact
+                const uint32_t todo = __ballot_sync(0xffffffffu, unsafe);
+                if (todo)
+                    sc = rescore_flagged(todo, sc, sfw, (int64_t)t * kTile + quad * 32, P.kc + kbase * kRowBytes,
+                                         pool, P.pool_mode, P.n_keys, S.b,
+                                         reinterpret_cast<const uint8_t *>(S.sfb), S.w[qi], qi, H);
+                if (valid) {
+                    P.scores[(row0 + qi) * P.n_cand + cand] = sc;
+                    key = score_key(sc);
+                }
+                if (P.gmax) {            // this warp's 32 candidates are one aligned group
+                    const uint32_t gk = __reduce_max_sync(0xffffffffu, key);
+                    const int64_t g0 = (int64_t)t * kTile + quad * 32;
+                    if (lane == 0 && g0 < qlen[u]) P.gmax[(row0 + qi) * P.G + (g0 >> 5)] = gk;
+                }
             }
         }
     }
@@ -507,15 +566,15 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
     __syncthreads();
     if (warp == 1) {
         tc::tc_fence_after();
-        tc::tmem_dealloc(tmem, kTmemCols);
+        tc::tmem_dealloc(tmem, C::kTmemCols);
     }
     if (tid == 0) {
         if (S.abort_flag) dev_flag(P.d_status, CSA2_DEV_TIMEOUT);
-        // the row's last CTA to finish sets both counters back to zero for the next call
+        // the group's last CTA to finish sets both counters back to zero for the next call
         __threadfence();
-        if (atomicAdd(&P.tile_done[row], 1u) == gridDim.x - 1u) {
-            P.tile_ctr[row] = 0u;
-            P.tile_done[row] = 0u;
+        if (atomicAdd(&P.tile_done[unit], 1u) == gridDim.x - 1u) {
+            P.tile_ctr[unit] = 0u;
+            P.tile_done[unit] = 0u;
         }
     }
 }
@@ -535,13 +594,38 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
     return fn;
 }
 
-int64_t tc_splits(int64_t rows, int64_t n_cand)
+// Queries per CTA: 4 for a chunk of queries scored against a shared cache (Full mode,
+// at least 8 queries a sequence), else 1.
+int tc_query_group(const csa2_index_args &a)
+{
+    return a.mode != CSA2_INDEX_POOL && a.n_q >= 8 ? 4 : 1;
+}
+
+// CTAs per unit (QG queries): enough units x CTAs to fill the resident CTAs of every SM,
+// at most one per tile of the unit.
+int64_t tc_splits(int64_t units, int64_t n_cand, int ctas_per_sm)
 {
     const int64_t tiles = (n_cand + kTile - 1) / kTile;
-    int64_t s = (int64_t)kSms * kCtasPerSm / (rows > 0 ? rows : 1);
+    int64_t s = (int64_t)kSms * ctas_per_sm / (units > 0 ? units : 1);
     if (s < 1) s = 1;
     if (s > tiles) s = tiles > 0 ? tiles : 1;
     return s;
+}
+
+template <int QG>
+cudaError_t launch_tc(const CUtensorMap &map, const TcParams &P, int64_t units, int64_t splits,
+                      cudaStream_t s)
+{
+    const size_t smem = sizeof(TcSmem<QG>) + 1024;
+    cudaError_t e = cudaFuncSetAttribute(index_score_tc_kernel<QG>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    // the whole unified L1 as shared memory, so the resident CTAs fit on every SM
+    e = cudaFuncSetAttribute(index_score_tc_kernel<QG>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(index_score_tc_kernel<QG>, dim3((unsigned)splits, (unsigned)units),
+                      dim3(kThreadsOf<QG>), smem, s, 1, map, P);
 }
 
 } // namespace
@@ -556,20 +640,22 @@ bool index_tc_eligible(const csa2_index_args &a)
     return encode_fn() != nullptr;
 }
 
-// CTAs per query row: enough rows x CTAs to fill kCtasPerSm CTAs on every SM, at most one
-// per tile of the row.
+// CTAs per unit of QG queries (see tc_query_group).
 int64_t index_tc_ctas_per_row(const csa2_index_args &a)
 {
-    const int64_t rows = (int64_t)a.batch * a.n_q;
+    const int qg = tc_query_group(a);
+    const int64_t units = (int64_t)a.batch * ((a.n_q + qg - 1) / qg);
     const int64_t n_cand = a.mode == CSA2_INDEX_POOL ? (int64_t)a.n_pool_blocks * a.block : a.n_keys;
-    return tc_splits(rows, n_cand);
+    return tc_splits(units, n_cand, qg == 4 ? Cfg<4>::kCtasPerSm : Cfg<1>::kCtasPerSm);
 }
 
 cudaError_t launch_index_tc(const csa2_index_args &a, float *scores, int32_t *row_len,
                             uint32_t *tile_ctr, uint32_t *d_status, cudaStream_t s)
 {
+    const int qg = tc_query_group(a);
     const int64_t splits = index_tc_ctas_per_row(a);
     const int64_t rows = (int64_t)a.batch * a.n_q;
+    const int64_t units = (int64_t)a.batch * ((a.n_q + qg - 1) / qg);
     TcParams P;
     P.n_q = a.n_q;
     P.H = a.n_heads;
@@ -604,16 +690,7 @@ cudaError_t launch_index_tc(const csa2_index_args &a, float *scores, int32_t *ro
                              CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    const size_t smem = sizeof(TcSmem) + 1024;
-    cudaError_t e = cudaFuncSetAttribute(index_score_tc_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    // the whole unified L1 as shared memory, so kCtasPerSm CTAs are resident on every SM
-    e = cudaFuncSetAttribute(index_score_tc_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             (int)cudaSharedmemCarveoutMaxShared);
-    if (e != cudaSuccess) return e;
-    return launch_pdl(index_score_tc_kernel, dim3((unsigned)splits, (unsigned)rows), dim3(kThreads), smem, s, 1,
-                      map, P);
+    return qg == 4 ? launch_tc<4>(map, P, units, splits, s) : launch_tc<1>(map, P, units, splits, s);
 }
 
 } // namespace csa2

@@ -101,6 +101,9 @@ SCORE_CASES = {
     "tiny": W["tiny_full_decode"],
     "ragged_planted": W["full_decode_64k"].scaled(batch=3, n_q=2, n_keys=5003, q_pos0=4000),
     "ratio2": W["prefill_chunk_m2"].scaled(batch=2, n_q=3, n_keys=3001, q_pos0=5000, seed=9),
+    # a chunk of 11 queries (groups of 4 queries, the last one ragged) whose visible
+    # lengths cross a tile boundary (2,048) inside a group
+    "chunk_groups": W["prefill_chunk_m2"].scaled(batch=2, n_q=11, n_keys=2100, q_pos0=4090, seed=11),
     "d32_h1": W["tiny_full_decode"].scaled(batch=2, n_keys=777, q_pos0=776, idx_heads=1, idx_dim=32),
     "ties": W["hier_indexer_1m"].scaled(batch=2, n_keys=20000, q_pos0=19999, palette=64),
 }

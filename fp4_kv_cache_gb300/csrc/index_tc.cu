@@ -522,14 +522,13 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
             const int e2 = (int)((sfw >> 16) & 255u), e3 = (int)(sfw >> 24);
             const int kmin = min(min(e0, e1), min(e2, e3)) - 127;
             const int kmax = max(max(e0, e1), max(e2, e3)) - 127;
+            // the score chains of this warp's queries: straight-line over all 32 head slots
+            // (a padded head has weight 0 and D = 0 from zero query codes, so its step adds +0
+            // to a sum that is never -0)
+            float scs[kQPerWarp];
 #pragma unroll
             for (int u = 0; u < kQPerWarp; ++u) {
-                const int qi = q_lo + u;
-                const bool valid = cand < qlen[u];
-                uint32_t key = 0;
-                // straight-line chain over all 32 head slots: a padded head has weight 0 and
-                // D = 0 (zero query codes), so its step adds +0 to a sum that is never -0
-                const float4 *w4 = reinterpret_cast<const float4 *>(S.w[qi]);
+                const float4 *w4 = reinterpret_cast<const float4 *>(S.w[q_lo + u]);
                 float sc = 0.0f;
 #pragma unroll
                 for (int h4 = 0; h4 < kNPad / 4; ++h4) {
@@ -541,6 +540,14 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
                         sc = __fmaf_rn(wh[j], D > 0.0f ? D : 0.0f, sc);
                     }
                 }
+                scs[u] = sc;
+            }
+#pragma unroll
+            for (int u = 0; u < kQPerWarp; ++u) {
+                const int qi = q_lo + u;
+                const bool valid = cand < qlen[u];
+                uint32_t key = 0;
+                float sc = scs[u];
                 const bool unsafe = valid && ((kmax - kmin) + qspan[u] > 9 || qmin[u] + kmin - 2 < -126 ||
                                               qmax[u] + kmax - 2 > 100);
                 // rare: positions whose tensor-core result cannot be proven exact

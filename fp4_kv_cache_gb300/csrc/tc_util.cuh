@@ -48,8 +48,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 // Bounded wait for the phase with the given parity; false on timeout or abort.
+// The poll loops stay rolled: unrolled, each inlined wait would grow into hundreds of
+// polls of straight-line code and crowd the instruction cache of the loops around it.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const volatile int *abort)
 {
+#pragma unroll 1
     for (uint32_t i = 0; i < kSpinLimit; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 255u) == 255u && *abort) return false;
@@ -60,6 +63,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const 
 // Bounded wait without an abort flag (used while draining after an abort).
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity)
 {
+#pragma unroll 1
     for (uint32_t i = 0; i < kSpinLimit; ++i)
         if (mbar_try_wait(bar, parity)) return true;
     return false;

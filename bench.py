@@ -10,8 +10,10 @@ SWA 128 (bf16).  One step = the whole path for one new token per sequence:
 metric: decode tokens/s per layer (batch / step time); roofline of the dominant kernel
 (the indexer scan) in achieved HBM GB/s.
 
-  python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--extra]
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--no-prefill]
 Under torchrun each rank runs its own replica (the path has no exchange step).
+Rank 0 also times the prefill indexer on an encoder chunk (4,096 queries after 65,536
+entries at ratio 2) and reports it beside the decode line as "prefill_indexer".
 """
 from __future__ import annotations
 
@@ -38,7 +40,7 @@ L2_FLUSH_BYTES = 256 << 20
 # DRAM bytes (read + write) of one csa2_index_score tensor-core launch on this workload, from
 # the ncu capture summarised in profiles/index_score_tc_kernel_full_decode_64k.md; None
 # whenever the kernel has changed since that capture.
-INDEX_TRAFFIC_BYTES = None      # kernel changed since the last capture
+INDEX_TRAFFIC_BYTES = 150924288      # ncu: dram__bytes_read.sum + dram__bytes_write.sum, one launch
 
 
 def _peaks():
@@ -390,6 +392,8 @@ def run_gpu(args):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks.summary(),
     }
+    if not args.no_prefill:
+        line["prefill_indexer"] = prefill_indexer(dev, line["clocks"].get("sm_mhz"))
     if not args.no_cpu_baseline:
         import oracle
         dt, tok = oracle_sample(w, [0, 1])
@@ -403,6 +407,51 @@ def run_gpu(args):
     return 0
 
 
+PREFILL_WORKLOAD = "prefill_chunk_m2"
+
+
+def prefill_indexer(dev, sm_mhz):
+    """Tensor-core indexer over one prefill chunk: FP4 dot TFLOP/s (2 x heads x d_i per
+    visible (query, position) pair) against the FP4 tensor peak (the measured bf16 GEMM
+    peak x 6, the nominal fp4/bf16 ratio) and against the CUDA-core bound of its epilogue
+    (one max and one fma in fp32 per pair and head)."""
+    import torch
+    from fp4_kv_cache_gb300 import csa2, workload
+    w = synth.WORKLOADS[PREFILL_WORKLOAD]
+    dw = workload.build(w, device=dev, kv=False)
+    B, T = w.batch, w.n_q
+    scores = torch.empty((B, T, w.n_keys), dtype=torch.float32, device=dev)
+    gmax = csa2.group_max_buffer(scores)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    ms = []
+    for it in range(8):
+        flush.fill_(1)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        _, row_len = csa2.index_score(dw["q_idx"], dw["w_idx"], dw["k_codes"], dw["k_scales"],
+                                      dw["q_pos"], w.ratio_m, group_max=gmax)
+        e1.record()
+        e1.synchronize()
+        if it >= 3:
+            ms.append(e0.elapsed_time(e1))
+    t = statistics.median(ms)
+    pairs = int(row_len.sum().item())
+    flop = 2.0 * pairs * w.idx_heads * w.idx_dim
+    tf = flop / (t * 1e-3) / 1e12
+    d = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
+        os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+    bf16 = float(d.get("bf16_tflops", 1900.0))
+    fp4_peak = 6.0 * bf16
+    mhz = sm_mhz or 2070.0
+    alu_tf = 152 * 128 * mhz * 1e6 / 2 * (2 * w.idx_dim) / 1e12
+    return {"workload": PREFILL_WORKLOAD, "queries": B * T, "positions": w.n_keys,
+            "visible_pairs": pairs, "ms": t, "achieved": tf, "unit": "TFLOP/s",
+            "fp4_peak": fp4_peak,
+            "fp4_peak_kind": ("measured bf16 x 6" if "bf16_tflops" in d else "fallback bf16 x 6"),
+            "frac_fp4": tf / fp4_peak, "alu_peak": alu_tf, "frac_alu": tf / alu_tf,
+            "l2": "flushed between timed launches"}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -410,6 +459,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -210,20 +210,21 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
         tc::tmem_alloc(&s_tmem, kTmemCols);
         tc::tmem_relinquish();
     }
-    // everything above touched no input: it overlaps the previous kernel's tail
-    pdl_wait();
-    pdl_allow_dependents();
-    // the first two tiles' index entries are read first, so their latency overlaps the
-    // set-up below
-    const int32_t id_first = slot_id(t_begin);
-    int32_t id_next = slot_id(t_begin + 1);
-    // Q -> nine K-major chunks (rows = heads), zero rows for heads >= H
+    // Q -> nine K-major chunks (rows = heads), zero rows for heads >= H.  Issued before the
+    // wait for the previous kernel: only the index entries come from it (the Top-K of this
+    // step); the query is complete before that kernel starts (see csa2_sparse_attn).
     for (int e = tid; e < kH * kChunks * 8; e += kThreads) {
         const int h = e / (kChunks * 8), rem = e % (kChunks * 8), c = rem >> 3, p = rem & 7;
         uint8_t *dst = sm + kOffQ + c * kQChunkBytes + sw128(h, p);
         if (h < H) cp_async_16(dst, P.q + ((row * H + h) * (int64_t)kDqk + c * 64 + p * 8));
         else *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
     }
+    pdl_wait();
+    pdl_allow_dependents();
+    // the first two tiles' index entries are read first, so their latency overlaps the
+    // set-up below
+    const int32_t id_first = slot_id(t_begin);
+    int32_t id_next = slot_id(t_begin + 1);
 
     // this query's key slots: idx entries, then its SWA window [max(s, p-W+1, 0), p]
     int64_t j0 = 0, n_sw = 0;

@@ -39,19 +39,26 @@ constexpr int kNPad = 32;              // heads per query, padded to 32
 constexpr int kSms = 152;
 
 // A CTA scores QG queries of one sequence against the same key tiles: MMA N = QG x 32
-// (queries x heads).  QG = 1 for decode (many CTAs per query row, 3 per SM); QG = 4 for
-// prefill chunks, where every query of a group sees nearly the same positions, so one
-// K tile feeds four queries' dots (one CTA per SM: its accumulators fill tensor memory).
+// (queries x heads).  A stage holds kMB tiles of 128 positions (one MMA M block each).
+//   QG = 1 (decode): two CTAs per SM, stages of two tiles, so the producer's and the MMA
+//     issuer's per-stage costs cover 256 positions and each SM has four tiles in its
+//     epilogues at once (two warps per TMEM lane quadrant, one per M block).
+//   QG = 4 (prefill chunks): every query of a group sees nearly the same positions, so
+//     one K tile feeds four queries' dots; one CTA per SM (its accumulators fill tensor
+//     memory), two epilogue warps per lane quadrant, two queries each.
+// Tensor-memory columns: accumulator (a, mb) at (a * kMB + mb) * N, then the scale-factor
+// columns of A (4 per accumulator block) and of B (4).
 template <int QG> struct Cfg;
 template <> struct Cfg<1> {
-    static constexpr int kStages = 8, kAcc = 3, kEpiPerQuad = 1, kCtasPerSm = 3;
-    static constexpr uint32_t kTmemCols = 128, kColSfa = 96, kColSfb = 108;  // acc k at 32k
+    static constexpr int kStages = 6, kAcc = 3, kMB = 2, kEpiPerQuad = 2, kCtasPerSm = 2;
+    static constexpr uint32_t kTmemCols = 256, kColSfa = 192, kColSfb = 216;
 };
 template <> struct Cfg<4> {
-    static constexpr int kStages = 12, kAcc = 2, kEpiPerQuad = 2, kCtasPerSm = 1;
-    static constexpr uint32_t kTmemCols = 512, kColSfa = 256, kColSfb = 264; // acc k at 128k
+    static constexpr int kStages = 12, kAcc = 2, kMB = 1, kEpiPerQuad = 2, kCtasPerSm = 1;
+    static constexpr uint32_t kTmemCols = 512, kColSfa = 256, kColSfb = 264;
 };
 template <int QG> constexpr int kThreadsOf = 64 + 128 * Cfg<QG>::kEpiPerQuad;
+template <int QG> constexpr int kSpanOf = Cfg<QG>::kMB * 128;   // positions per stage
 
 struct TcParams {
     int32_t n_q, H, ratio_m, block, n_pool_blocks;
@@ -72,13 +79,14 @@ struct TcParams {
 
 template <int QG>
 struct TcSmem {
-    static constexpr int kStages = Cfg<QG>::kStages, kAcc = Cfg<QG>::kAcc;
-    uint8_t a[kStages][kTile * kRowBytes];     // K codes, 64-byte swizzle, 1024-aligned
+    static constexpr int kStages = Cfg<QG>::kStages, kAcc = Cfg<QG>::kAcc, kSpan = kSpanOf<QG>;
+    uint8_t a[kStages][kSpan * kRowBytes];     // K codes, 64-byte swizzle, 1024-aligned
     uint8_t b[QG * kNPad * kRowBytes];         // q codes (row = query x 32 + head), same layout
-    uint32_t sfa[kStages][kTile];              // scale-factor atoms of the K tiles
+    uint32_t sfa[kStages][kSpan];              // scale-factor atoms of the K tiles (one per block)
     uint32_t sfb[kTile];                       // scale-factor atom of q (rows 0..QG*32-1)
     uint64_t full[kStages], empty[kStages], accf[kAcc], acce[kAcc], qready;
-    int32_t tile[kStages];                     // tile held by each stage (-1: no more)
+    int32_t tile[kStages];                     // stage number held by each stage (-1: no more)
+    int32_t sf_raw[kStages];                   // 1: sfa holds the scales in position order
     int32_t acc_tile[kAcc];                    // tile held by each accumulator
     alignas(16) float w[QG][kNPad];            // head weights, 0 for padded heads
     int hmin[QG][kNPad], hmax[QG][kNPad];
@@ -179,16 +187,17 @@ __device__ __noinline__ float rescore_flagged(uint32_t todo, float score, uint32
     return score;
 }
 
-// Registers: with QG = 1, three resident CTAs need every warp within its sub-partition's
-// share of the register file (18 warps over 4 sub-partitions: at most 96 registers a
-// thread); the launch bound makes the compiler keep to it.
+// Registers: with QG = 1, two resident CTAs of 320 threads need every warp within its
+// sub-partition's share of the register file (20 warps over 4 sub-partitions: at most 102
+// registers a thread, 96 after rounding); the launch bound makes the compiler keep to it.
 template <int QG>
 __global__ void __launch_bounds__(kThreadsOf<QG>, Cfg<QG>::kCtasPerSm)
 index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P)
 {
     using C = Cfg<QG>;
-    constexpr int kStages = C::kStages, kAcc = C::kAcc, kN = QG * kNPad;
-    constexpr int kEpiWarps = 4 * C::kEpiPerQuad, kQPerWarp = QG / C::kEpiPerQuad;
+    constexpr int kStages = C::kStages, kAcc = C::kAcc, kN = QG * kNPad, kMB = C::kMB;
+    constexpr int kSpan = kSpanOf<QG>;
+    constexpr int kEpiWarps = 4 * C::kEpiPerQuad, kQPerWarp = QG * kMB / C::kEpiPerQuad;
     extern __shared__ uint8_t smem_raw[];
     TcSmem<QG> &S = *reinterpret_cast<TcSmem<QG> *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                     ~uintptr_t(1023));
@@ -261,13 +270,14 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
         if (P.row_len) P.row_len[row0 + tid] = (int32_t)S.qlen[tid];
         if (tid == 0 && S.bad) dev_flag(P.d_status, CSA2_DEV_BAD_POOL);
     }
-    // Tiles of the group: CTA c first takes the R consecutive tiles [cR, cR + R) (C CTAs per
-    // group, R two tiles short of an even share; consecutive tiles keep the reads
-    // sequential); the rest are handed out one at a time from the group's counter, so its
-    // CTAs finish together.  Each claim is made one tile ahead of its use, which hides the
-    // atomic's latency.  A stage carries its tile number from the producer to the MMA
-    // issuer (-1: no more tiles), an accumulator carries it on to the epilogue.
-    const int ntr = len > 0 ? (int)((len + kTile - 1) / kTile) : 0;
+    // Stages of the group (kSpan positions each): CTA c first takes the R consecutive
+    // stages [cR, cR + R) (C CTAs per group, R two short of an even share; consecutive
+    // stages keep the reads sequential); the rest are handed out one at a time from the
+    // group's counter, so its CTAs finish together.  Each claim is made one stage ahead of
+    // its use, which hides the atomic's latency.  A stage carries its number from the
+    // producer to the MMA issuer (-1: no more), an accumulator carries it on to the
+    // epilogue.
+    const int ntr = len > 0 ? (int)((len + kSpan - 1) / kSpan) : 0;
     const int CT = (int)gridDim.x;
     const int R = ntr / CT > 2 ? ntr / CT - 2 : 0;
     const int64_t c1 = len;
@@ -276,6 +286,9 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
 
     if (warp == 0) {
         // ================= producer
+        // first the quantising warps' query reads enter the memory system (named barrier
+        // 2), so they are not queued behind every CTA's first tile loads
+        asm volatile("bar.sync 2, 160;" ::: "memory");
         int issued = 0;
         uint32_t claim = 0;                       // lane 0: the next claim from the counter
         if (lane == 0 && R == 0) claim = atomicAdd(&P.tile_ctr[unit], 1u);
@@ -306,18 +319,25 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
                 tc::mbar_arrive(&S.full[s]);
                 break;
             }
-            const int64_t t0 = (int64_t)t * kTile;
+            const int64_t t0 = (int64_t)t * kSpan;
+            // a whole stage of consecutive positions: its scale bytes are one contiguous run,
+            // copied in position order by one bulk copy (the MMA warp rearranges them into
+            // the scale-factor atoms); otherwise each lane copies its atom words
+            const uint8_t *ks_run = P.ks + (kbase + t0) * 4;
+            const bool sf_bulk = !P.pool_mode && t0 + kSpan <= c1 && ((uintptr_t)ks_run & 15u) == 0;
             if (lane == 0) {
                 S.tile[s] = t;
+                S.sf_raw[s] = sf_bulk ? 1 : 0;
                 if (!P.pool_mode) {
-                    tc::mbar_arrive_expect_tx(&S.full[s], kTile * kRowBytes);
+                    tc::mbar_arrive_expect_tx(&S.full[s], kSpan * kRowBytes + (sf_bulk ? kSpan * 4 : 0));
                     tc::tma_load_2d(S.a[s], &tmap, &S.full[s], 0, (int32_t)(kbase + t0));
+                    if (sf_bulk) tc::bulk_load(S.sfa[s], ks_run, kSpan * 4, &S.full[s]);
                 } else {
                     uint32_t bytes = 0;
-                    for (int j = 0; j < kTile / 8; ++j)
+                    for (int j = 0; j < kSpan / 8; ++j)
                         if (t0 + 8 * j < c1 && pool[(t0 >> 3) + j] >= 0) bytes += 8 * kRowBytes;
                     tc::mbar_arrive_expect_tx(&S.full[s], bytes);
-                    for (int j = 0; j < kTile / 8; ++j) {
+                    for (int j = 0; j < kSpan / 8; ++j) {
                         if (t0 + 8 * j >= c1) break;
                         int64_t id = pool[(t0 >> 3) + j];
                         if (id < 0) continue;
@@ -327,11 +347,13 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
                     }
                 }
             }
+            // scale atom of block mb: word lane * 4 + j holds position mb * 128 + lane + 32 j
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < 4 * kMB; ++j) {
+                if (sf_bulk) break;
                 const int m = lane + 32 * j;
                 const int64_t cand = t0 + m;
-                uint32_t *dst = &S.sfa[s][lane * 4 + j];
+                uint32_t *dst = &S.sfa[s][(j >> 2) * kTile + lane * 4 + (j & 3)];
                 if (cand < c1) {
                     int64_t pos = cand;
                     if (P.pool_mode) {
@@ -355,46 +377,73 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
                 tc::mbar_wait_bounded(&S.full[i % kStages], (uint32_t)(i / kStages) & 1u);
         }
     } else if (warp == 1) {
-        // ================= MMA issuer
+        // ================= MMA issuer (lane 0; the warp rearranges bulk-copied scales)
+        const uint32_t sfb_t = tmem + C::kColSfb;
+        bool ok = tc::mbar_wait(&S.qready, 0, &S.abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) S.abort_flag = 1;
         if (lane == 0) {
-            const uint32_t sfb_t = tmem + C::kColSfb;
-            if (!tc::mbar_wait(&S.qready, 0, &S.abort_flag)) S.abort_flag = 1;
             tc::fence_proxy_async_smem();
             tc::tc_fence_after();
             if (!S.abort_flag)
                 tc::tc_cp_32x128b_warpx4(sfb_t, tc::smem_desc(tc::smem_u32(S.sfb), 512, 128, tc::kSwizzleNone));
-            for (int i = 0; !S.abort_flag; ++i) {
-                const int s = i % kStages, acc = i % kAcc;
-                if (!tc::mbar_wait(&S.acce[acc], ((uint32_t)(i / kAcc) & 1u) ^ 1u, &S.abort_flag) ||
-                    !tc::mbar_wait(&S.full[s], (uint32_t)(i / kStages) & 1u, &S.abort_flag)) {
-                    S.abort_flag = 1;
-                    break;
+        }
+        __syncwarp();
+        for (int i = 0;; ++i) {
+            if (__any_sync(0xffffffffu, S.abort_flag != 0)) break;    // the warp leaves together
+            const int s = i % kStages, acc = i % kAcc;
+            ok = tc::mbar_wait(&S.acce[acc], ((uint32_t)(i / kAcc) & 1u) ^ 1u, &S.abort_flag) &&
+                 tc::mbar_wait(&S.full[s], (uint32_t)(i / kStages) & 1u, &S.abort_flag);
+            if (!__all_sync(0xffffffffu, ok)) {
+                S.abort_flag = 1;
+                break;
+            }
+            const int t = S.tile[s];
+            if (t < 0) {                          // pass the end marker to the epilogue
+                if (lane == 0) {
+                    S.acc_tile[acc] = t;
+                    tc::mbar_arrive(&S.accf[acc]);
+                    tc::mbar_arrive(&S.accf[acc]);
                 }
-                const int t = S.tile[s];
+                break;
+            }
+            if (S.sf_raw[s]) {
+                // position-ordered scale words -> atoms (word lane * 4 + j of block mb holds
+                // position mb * 128 + lane + 32 j): all reads, then all writes
+                uint32_t v[4 * kMB];
+#pragma unroll
+                for (int j = 0; j < 4 * kMB; ++j) v[j] = S.sfa[s][(j >> 2) * kTile + lane + 32 * (j & 3)];
+                __syncwarp();
+#pragma unroll
+                for (int mb = 0; mb < kMB; ++mb)
+                    *reinterpret_cast<uint4 *>(&S.sfa[s][mb * kTile + lane * 4]) =
+                        make_uint4(v[4 * mb], v[4 * mb + 1], v[4 * mb + 2], v[4 * mb + 3]);
+                tc::fence_proxy_async_smem();
+                __syncwarp();
+            }
+            if (lane == 0) {
                 S.acc_tile[acc] = t;
-                if (t < 0) {                      // pass the end marker to the epilogue
-                    tc::mbar_arrive(&S.accf[acc]);
-                    tc::mbar_arrive(&S.accf[acc]);
-                    break;
-                }
                 tc::fence_proxy_async_smem();
                 tc::tc_fence_after();
-                const uint32_t sfa_t = tmem + C::kColSfa + 4 * acc;
-                tc::tc_cp_32x128b_warpx4(sfa_t, tc::smem_desc(tc::smem_u32(S.sfa[s]), 512, 128,
-                                                              tc::kSwizzleNone));
-                const uint32_t d_t = tmem + acc * kN;
 #pragma unroll
-                for (int kk = 0; kk < 2; ++kk) {
-                    const uint64_t ad = tc::smem_desc(tc::smem_u32(S.a[s]) + kk * 32, 16, 512, tc::kSwizzle64B);
-                    const uint64_t bd = tc::smem_desc(tc::smem_u32(S.b) + kk * 32, 16, 512, tc::kSwizzle64B);
-                    tc::tc_mma_mxf4(d_t, ad, bd, mxf4_idesc<QG>(2 * kk), sfa_t, sfb_t, kk);
+                for (int mb = 0; mb < kMB; ++mb) {
+                    const uint32_t sfa_t = tmem + C::kColSfa + 4 * (acc * kMB + mb);
+                    tc::tc_cp_32x128b_warpx4(sfa_t, tc::smem_desc(tc::smem_u32(S.sfa[s] + mb * kTile), 512, 128,
+                                                                  tc::kSwizzleNone));
+                    const uint32_t d_t = tmem + (acc * kMB + mb) * kN;
+                    const uint32_t a0 = tc::smem_u32(S.a[s]) + mb * kTile * kRowBytes;
+#pragma unroll
+                    for (int kk = 0; kk < 2; ++kk) {
+                        const uint64_t ad = tc::smem_desc(a0 + kk * 32, 16, 512, tc::kSwizzle64B);
+                        const uint64_t bd = tc::smem_desc(tc::smem_u32(S.b) + kk * 32, 16, 512, tc::kSwizzle64B);
+                        tc::tc_mma_mxf4(d_t, ad, bd, mxf4_idesc<QG>(2 * kk), sfa_t, sfb_t, kk);
+                    }
                 }
                 tc::tc_commit(&S.empty[s]);
                 tc::tc_commit(&S.accf[acc]);
                 tc::mbar_arrive(&S.accf[acc]);    // releases acc_tile to the epilogue
             }
+            __syncwarp();
         }
-        __syncwarp();
     } else {
         // ================= epilogue warps: first the queries (B operand), then the scores
         const int et = tid - 64;
@@ -402,6 +451,11 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
             // thread (h, kb) quantises block kb of head h of each query on its own: 4 x
             // 16-byte loads, a local maximum, 32 codes packed into one 16-byte store
             const int h = et >> 2, kb = et & 3;
+#pragma unroll 1
+            for (int qi = 0; qi < QG; ++qi)
+                if (h < H && t0q + qi < P.n_q)
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(P.q + (row0 + qi) * (int64_t)H * kD + h * kD + kb * 32));
+            asm volatile("bar.arrive 2, 160;" ::: "memory");     // releases the producer
 #pragma unroll 1
             for (int qi = 0; qi < QG; ++qi) {
                 const bool live = h < H && t0q + qi < P.n_q;
@@ -474,9 +528,10 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
             asm volatile("bar.sync 1, 128;" ::: "memory");
             if (et == 0) tc::mbar_arrive(&S.qready);
         }
-        // epilogue warp: TMEM lane quadrant `quad`, queries [q_lo, q_lo + kQPerWarp)
-        const int ew = warp - 2, quad = warp & 3, q_lo = (ew >> 2) * kQPerWarp;
-        const int m = quad * 32 + lane;
+        // epilogue warp ew: lane quadrant `quad`, M block mb of each stage, queries
+        // [q_lo, q_lo + kQPerWarp)
+        const int ew = warp - 2, quad = warp & 3, mb = (ew >> 2) % kMB, q_lo = (ew >> 2) / kMB * kQPerWarp;
+        const int m = mb * kTile + quad * 32 + lane;           // position within the stage
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
         // this warp's queries: candidates and exponent ranges (read once the first
         // accumulator is full, which is after the queries were quantised)
@@ -508,16 +563,18 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
             // every lane quadrant), so row quad*32+lane is word `quad` of this lane
             asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
                          : "=r"(sf4[0]), "=r"(sf4[1]), "=r"(sf4[2]), "=r"(sf4[3])
-                         : "r"(lane_base + C::kColSfa + 4 * acc));
+                         : "r"(lane_base + C::kColSfa + 4 * (acc * kMB + mb)));
             uint32_t r[kQPerWarp][32];
 #pragma unroll
-            for (int u = 0; u < kQPerWarp; ++u) tc::tc_ld_32x32b_x32(lane_base + acc * kN + (q_lo + u) * kNPad, r[u]);
+            for (int u = 0; u < kQPerWarp; ++u)
+                tc::tc_ld_32x32b_x32(lane_base + (acc * kMB + mb) * kN + (q_lo + u) * kNPad, r[u]);
             tc::tc_wait_ld();
             const uint32_t sfw = quad == 0 ? sf4[0] : quad == 1 ? sf4[1] : quad == 2 ? sf4[2] : sf4[3];
             tc::tc_fence_before();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&S.acce[acc]);
-            const int64_t cand = (int64_t)t * kTile + m;
+            const int64_t cand = (int64_t)t * kSpan + m;
+            const int64_t g0 = (int64_t)t * kSpan + mb * kTile + quad * 32;   // this warp's 32
             const int e0 = (int)(sfw & 255u), e1 = (int)((sfw >> 8) & 255u);
             const int e2 = (int)((sfw >> 16) & 255u), e3 = (int)(sfw >> 24);
             const int kmin = min(min(e0, e1), min(e2, e3)) - 127;
@@ -553,7 +610,7 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
                 // rare: positions whose tensor-core result cannot be proven exact
                 const uint32_t todo = __ballot_sync(0xffffffffu, unsafe);
                 if (todo)
-                    sc = rescore_flagged(todo, sc, sfw, (int64_t)t * kTile + quad * 32, P.kc + kbase * kRowBytes,
+                    sc = rescore_flagged(todo, sc, sfw, g0, P.kc + kbase * kRowBytes,
                                          pool, P.pool_mode, P.n_keys, S.b,
                                          reinterpret_cast<const uint8_t *>(S.sfb), S.w[qi], qi, H);
                 if (valid) {
@@ -562,7 +619,6 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
                 }
                 if (P.gmax) {            // this warp's 32 candidates are one aligned group
                     const uint32_t gk = __reduce_max_sync(0xffffffffu, key);
-                    const int64_t g0 = (int64_t)t * kTile + quad * 32;
                     if (lane == 0 && g0 < qlen[u]) P.gmax[(row0 + qi) * P.G + (g0 >> 5)] = gk;
                 }
             }
@@ -609,10 +665,10 @@ int tc_query_group(const csa2_index_args &a)
 }
 
 // CTAs per unit (QG queries): enough units x CTAs to fill the resident CTAs of every SM,
-// at most one per tile of the unit.
-int64_t tc_splits(int64_t units, int64_t n_cand, int ctas_per_sm)
+// at most one per stage (span positions) of the unit.
+int64_t tc_splits(int64_t units, int64_t n_cand, int ctas_per_sm, int span)
 {
-    const int64_t tiles = (n_cand + kTile - 1) / kTile;
+    const int64_t tiles = (n_cand + span - 1) / span;
     int64_t s = (int64_t)kSms * ctas_per_sm / (units > 0 ? units : 1);
     if (s < 1) s = 1;
     if (s > tiles) s = tiles > 0 ? tiles : 1;
@@ -653,7 +709,8 @@ int64_t index_tc_ctas_per_row(const csa2_index_args &a)
     const int qg = tc_query_group(a);
     const int64_t units = (int64_t)a.batch * ((a.n_q + qg - 1) / qg);
     const int64_t n_cand = a.mode == CSA2_INDEX_POOL ? (int64_t)a.n_pool_blocks * a.block : a.n_keys;
-    return tc_splits(units, n_cand, qg == 4 ? Cfg<4>::kCtasPerSm : Cfg<1>::kCtasPerSm);
+    return qg == 4 ? tc_splits(units, n_cand, Cfg<4>::kCtasPerSm, kSpanOf<4>)
+                   : tc_splits(units, n_cand, Cfg<1>::kCtasPerSm, kSpanOf<1>);
 }
 
 cudaError_t launch_index_tc(const csa2_index_args &a, float *scores, int32_t *row_len,
@@ -689,7 +746,8 @@ cudaError_t launch_index_tc(const csa2_index_args &a, float *scores, int32_t *ro
     CUtensorMap map;
     cuuint64_t dims[2] = {(cuuint64_t)kRowBytes, (cuuint64_t)((int64_t)a.batch * a.n_keys)};
     cuuint64_t strides[1] = {(cuuint64_t)kRowBytes};
-    cuuint32_t box[2] = {(cuuint32_t)kRowBytes, (cuuint32_t)(P.pool_mode ? 8 : kTile)};
+    cuuint32_t box[2] = {(cuuint32_t)kRowBytes,
+                         (cuuint32_t)(P.pool_mode ? 8 : (qg == 4 ? kSpanOf<4> : kSpanOf<1>))};
     cuuint32_t estr[2] = {1, 1};
     if (dims[1] == 0) dims[1] = 1;
     CUresult r = encode_fn()(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(a.k_codes),

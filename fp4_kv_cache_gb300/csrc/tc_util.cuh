@@ -84,6 +84,13 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, u
                    "r"(x), "r"(y)
                  : "memory");
 }
+// Untiled bulk copy global -> shared, completion counted on `bar` (both addresses 16-byte
+// aligned, `bytes` a multiple of 16).
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
+}
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

@@ -37,6 +37,21 @@ from fp4_kv_cache_gb300 import synth  # noqa: E402
 METRIC = "CSA2 decode tokens/s per layer (Full mode, 64K ctx)"
 WORKLOAD = "full_decode_64k"
 L2_FLUSH_BYTES = 256 << 20
+
+
+class L2Flush:
+    """Evicts L2 between timed runs: writes one buffer larger than L2, then reads a second
+    one, so the dirty lines the write leaves are written back before the timed region
+    instead of competing with its reads.  Untimed."""
+
+    def __init__(self, dev):
+        import torch
+        self.a = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        self.b = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+
+    def __call__(self):
+        self.a.fill_(1)
+        self.b.max()
 # DRAM bytes (read + write) of one csa2_index_score tensor-core launch on this workload, from
 # the ncu capture summarised in profiles/index_score_tc_kernel_full_decode_64k.md; None
 # whenever the kernel has changed since that capture.
@@ -231,29 +246,22 @@ def run_gpu(args):
                           dtype=torch.uint8, device=dev)
     ws_topk = torch.empty(max(1, lib.csa2_topk_workspace_size(B * T, w.n_keys, w.topk)),
                           dtype=torch.uint8, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
     # our kernels per step: 2 cache-write quantisers, the indexer (it also writes the per-32
     # group maxima), Top-K select, attention
     launches_per_step = 5
 
-    side = torch.cuda.Stream(dev)
-
     def step(k_ev=None):
-        # k_ev: events bracketing each call of the step (indexer-K write, indexer, Top-K,
-        # attention).  The main-KV row write only feeds attention, so it runs on a side
-        # stream, overlapped with the indexer and Top-K.
+        # k_ev: events bracketing each call of the step.  The calls form one chain on one
+        # stream, so each kernel can start its set-up while the one before it drains (a
+        # side stream for the main-KV write would join the chain with an event and cut the
+        # programmatic overlap of attention with Top-K).
         stream = torch.cuda.current_stream(dev)       # the capture stream while capturing
-        fork = torch.cuda.Event()
-        fork.record(stream)
-        side.wait_event(fork)
-        with torch.cuda.stream(side):
-            csa2.csa2_quant_fp4(new_kv, new_kvc, new_kvs, st, stream=side)
-        kv_done = torch.cuda.Event()
-        kv_done.record(side)
         if k_ev:
             k_ev[0].record(stream)
-        # cache write: the new token's indexer-K row, quantised in place
+        # cache write: the new token's main-KV and indexer-K rows, quantised in place
+        csa2.csa2_quant_fp4(new_kv, new_kvc, new_kvs, st)
         csa2.csa2_quant_fp4(new_k, new_kc, new_ks, st)
         if k_ev:
             k_ev[1].record(stream)
@@ -263,7 +271,6 @@ def run_gpu(args):
         csa2.csa2_topk(scores, w.topk, idx, row_len, d_status=st, workspace=ws_topk, group_max=gmax)
         if k_ev:
             k_ev[3].record(stream)
-        stream.wait_event(kv_done)
         csa2.csa2_sparse_attn(aargs, out, lse, st, workspace=ws_attn)
         if k_ev:
             k_ev[4].record(stream)
@@ -311,7 +318,7 @@ def run_gpu(args):
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clocks:
         for _ in range(args.steps):
-            flush.fill_(1)
+            flush()
             e0, e1 = ev(), ev()
             e0.record(stream)
             run_step()
@@ -320,7 +327,7 @@ def run_gpu(args):
             ms_steps.append(e0.elapsed_time(e1))
         torch.cuda.synchronize(dev)
     for _ in range(args.steps):                       # per-call breakdown (not the step time)
-        flush.fill_(1)
+        flush()
         k_ev = g_ev if graph is not None else tuple(ev() for _ in range(5))
         run_step(k_ev)
         k_ev[4].synchronize()
@@ -340,7 +347,7 @@ def run_gpu(args):
     d2h = h_out.numel() * 2
     e2e_ms = []
     for it in range(args.steps + 2):
-        flush.fill_(1)
+        flush()
         e0, e1 = ev(), ev()
         e0.record(stream)
         dw["q_idx"].copy_(h_qi, non_blocking=True)
@@ -379,7 +386,8 @@ def run_gpu(args):
                    "parallelism": f"replicas{world}", "topk": w.topk, "window": w.window,
                    "indexer": f"{w.idx_heads}x{w.idx_dim}", "heads": w.heads,
                    "d_qk": w.d_qk, "d_v": w.d_v,
-                   "l2": "flushed between timed steps (256 MiB write, untimed)",
+                   "l2": "flushed between timed steps (256 MiB written, then 256 MiB read so the "
+                         "write-back drains; untimed)",
                    "launch": "CUDA graph of the step" if graph is not None else "eager"},
         "achieved_gbs_step": _step_bytes(w) / (ms_step * 1e-3) / 1e9,
         "roofline": {"bound": "hbm", "kernel": "csa2_index_score", "achieved": achieved,
@@ -422,10 +430,10 @@ def prefill_indexer(dev, sm_mhz):
     B, T = w.batch, w.n_q
     scores = torch.empty((B, T, w.n_keys), dtype=torch.float32, device=dev)
     gmax = csa2.group_max_buffer(scores)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     ms = []
     for it in range(8):
-        flush.fill_(1)
+        flush()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         _, row_len = csa2.index_score(dw["q_idx"], dw["w_idx"], dw["k_codes"], dw["k_scales"],
@@ -449,7 +457,7 @@ def prefill_indexer(dev, sm_mhz):
             "fp4_peak": fp4_peak,
             "fp4_peak_kind": ("measured bf16 x 6" if "bf16_tflops" in d else "fallback bf16 x 6"),
             "frac_fp4": tf / fp4_peak, "alu_peak": alu_tf, "frac_alu": tf / alu_tf,
-            "l2": "flushed between timed launches"}
+            "l2": "flushed between timed launches (write + read of 256 MiB)"}
 
 
 def main():

@@ -210,21 +210,16 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
         tc::tmem_alloc(&s_tmem, kTmemCols);
         tc::tmem_relinquish();
     }
-    // Q -> nine K-major chunks (rows = heads), zero rows for heads >= H.  Issued before the
-    // wait for the previous kernel: only the index entries come from it (the Top-K of this
-    // step); the query is complete before that kernel starts (see csa2_sparse_attn).
+    // Q -> nine K-major chunks (rows = heads), zero rows for heads >= H, and the SWA window
+    // bounds: both before the wait for the previous kernel, since only the index entries
+    // come from it (the Top-K of this step); the query, its position and the SWA rows are
+    // complete before that kernel starts (see csa2_sparse_attn).
     for (int e = tid; e < kH * kChunks * 8; e += kThreads) {
         const int h = e / (kChunks * 8), rem = e % (kChunks * 8), c = rem >> 3, p = rem & 7;
         uint8_t *dst = sm + kOffQ + c * kQChunkBytes + sw128(h, p);
         if (h < H) cp_async_16(dst, P.q + ((row * H + h) * (int64_t)kDqk + c * 64 + p * 8));
         else *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
     }
-    pdl_wait();
-    pdl_allow_dependents();
-    // the first two tiles' index entries are read first, so their latency overlaps the
-    // set-up below
-    const int32_t id_first = slot_id(t_begin);
-    int32_t id_next = slot_id(t_begin + 1);
 
     // this query's key slots: idx entries, then its SWA window [max(s, p-W+1, 0), p]
     int64_t j0 = 0, n_sw = 0;
@@ -243,6 +238,12 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
     const int64_t n_slots = P.topk + n_sw;
     const int n_tiles = (int)((n_slots + kKeys - 1) / kKeys);
     const int t_end = min(t_begin + P.tiles_per_split, n_tiles);
+    pdl_wait();
+    pdl_allow_dependents();
+    // the first two tiles' index entries are read first, so their latency overlaps the
+    // set-up below
+    const int32_t id_first = slot_id(t_begin);
+    int32_t id_next = slot_id(t_begin + 1);
     __syncthreads();
     const uint32_t tmem = s_tmem;
     uint32_t phase = 0;

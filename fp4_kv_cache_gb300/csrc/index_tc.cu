@@ -582,22 +582,27 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
             // the score chains of this warp's queries: straight-line over all 32 head slots
             // (a padded head has weight 0 and D = 0 from zero query codes, so its step adds +0
             // to a sum that is never -0)
+            // (the chains of a warp's queries advance together: independent FMAs between
+            // the dependent steps of each chain)
             float scs[kQPerWarp];
 #pragma unroll
-            for (int u = 0; u < kQPerWarp; ++u) {
-                const float4 *w4 = reinterpret_cast<const float4 *>(S.w[q_lo + u]);
-                float sc = 0.0f;
+            for (int u = 0; u < kQPerWarp; ++u) scs[u] = 0.0f;
 #pragma unroll
-                for (int h4 = 0; h4 < kNPad / 4; ++h4) {
-                    const float4 wv = w4[h4];
-                    const float wh[4] = {wv.x, wv.y, wv.z, wv.w};
+            for (int h4 = 0; h4 < kNPad / 4; ++h4) {
+                float wh[kQPerWarp][4];
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
+                for (int u = 0; u < kQPerWarp; ++u) {
+                    const float4 wv = reinterpret_cast<const float4 *>(S.w[q_lo + u])[h4];
+                    wh[u][0] = wv.x; wh[u][1] = wv.y; wh[u][2] = wv.z; wh[u][3] = wv.w;
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+#pragma unroll
+                    for (int u = 0; u < kQPerWarp; ++u) {
                         const float D = __uint_as_float(r[u][4 * h4 + j]);
-                        sc = __fmaf_rn(wh[j], D > 0.0f ? D : 0.0f, sc);
+                        scs[u] = __fmaf_rn(wh[u][j], D > 0.0f ? D : 0.0f, scs[u]);
                     }
                 }
-                scs[u] = sc;
             }
 #pragma unroll
             for (int u = 0; u < kQPerWarp; ++u) {

@@ -34,9 +34,10 @@
  *     set-up while the kernel before it on the stream drains, and waits for that kernel
  *     to complete before it reads what that kernel may write.  Every kernel of the
  *     library lets its dependents start only after that wait.  One exception:
- *     csa2_sparse_attn reads q before its wait (only idx may come from the kernel just
- *     before it), so q must not be written by a kernel that lets its dependents start
- *     early (a plain kernel, or any call of this library, is fine).
+ *     csa2_sparse_attn reads q, q_pos, swa_pos0 and swa_start before its wait (only idx
+ *     may come from the kernel just before it), so those must not be written by a kernel
+ *     that lets its dependents start early (a plain kernel, or any call of this library,
+ *     is fine).
  */
 #ifndef CSA2_H
 #define CSA2_H

@@ -49,16 +49,22 @@ constexpr int kSms = 152;
 // Tensor-memory columns: accumulator (a, mb) at (a * kMB + mb) * N, then the scale-factor
 // columns of A (4 per accumulator block) and of B (4).
 template <int QG> struct Cfg;
+// kDeferred: positions the MMA may round are found per stage by the producer and re-scored
+// after the main loop (prefill: it keeps the re-scoring code out of the epilogue's loop);
+// otherwise the epilogue checks each position's bounds and re-scores in place (decode).
 template <> struct Cfg<1> {
+    static constexpr bool kDeferred = false;
     static constexpr int kStages = 6, kAcc = 3, kMB = 2, kEpiPerQuad = 2, kCtasPerSm = 2;
     static constexpr uint32_t kTmemCols = 256, kColSfa = 192, kColSfb = 216;
 };
 template <> struct Cfg<4> {
+    static constexpr bool kDeferred = true;
     static constexpr int kStages = 12, kAcc = 2, kMB = 1, kEpiPerQuad = 2, kCtasPerSm = 1;
     static constexpr uint32_t kTmemCols = 512, kColSfa = 256, kColSfb = 264;
 };
 template <int QG> constexpr int kThreadsOf = 64 + 128 * Cfg<QG>::kEpiPerQuad;
 template <int QG> constexpr int kSpanOf = Cfg<QG>::kMB * 128;   // positions per stage
+constexpr int kFlagWords = 512;        // stage flags: at most 16,384 stages per query group
 
 struct TcParams {
     int32_t n_q, H, ratio_m, block, n_pool_blocks;
@@ -87,6 +93,8 @@ struct TcSmem {
     uint64_t full[kStages], empty[kStages], accf[kAcc], acce[kAcc], qready;
     int32_t tile[kStages];                     // stage number held by each stage (-1: no more)
     int32_t sf_raw[kStages];                   // 1: sfa holds the scales in position order
+    uint32_t flag_bits[kFlagWords];            // stages with positions to re-check exactly
+    int thr_span, thr_lo, thr_hi;              // key-exponent bounds safe for every query
     int32_t acc_tile[kAcc];                    // tile held by each accumulator
     alignas(16) float w[QG][kNPad];            // head weights, 0 for padded heads
     int hmin[QG][kNPad], hmax[QG][kNPad];
@@ -187,6 +195,52 @@ __device__ __noinline__ float rescore_flagged(uint32_t todo, float score, uint32
     return score;
 }
 
+// Exact re-check of one flagged stage by one warp: per 32 positions and query, the
+// positions whose key exponents break that query's exactness bounds are re-scored on CUDA
+// cores (rescore_flagged) and their score and group maximum rewritten.  Runs after the main
+// loop, so the loop itself carries no re-scoring code.
+template <int QG>
+__device__ __noinline__ void recheck_stage(const TcParams &P, const TcSmem<QG> &S, int t, int span, int64_t row0,
+                                           int t0q, int64_t kbase, const int32_t *pool, int64_t n_blk_all)
+{
+    const int lane = threadIdx.x & 31;
+#pragma unroll 1
+    for (int c = 0; c < span / 32; ++c) {
+        const int64_t g0 = (int64_t)t * span + c * 32, p = g0 + lane;
+        int64_t pos = p;
+        if (P.pool_mode) {
+            const int64_t plen = (int64_t)P.n_pool_blocks * P.block;
+            int64_t id = p < plen ? pool[p >> 3] : 0;
+            id = id < 0 ? 0 : (id >= n_blk_all ? n_blk_all - 1 : id);
+            pos = id * 8 + (p & 7);
+        }
+        if (pos >= P.n_keys) pos = P.n_keys - 1;
+        const uint32_t kw = *reinterpret_cast<const uint32_t *>(P.ks + (kbase + pos) * 4);
+        const int e0 = (int)(kw & 255u), e1 = (int)((kw >> 8) & 255u);
+        const int e2 = (int)((kw >> 16) & 255u), e3 = (int)(kw >> 24);
+        const int kmin = min(min(e0, e1), min(e2, e3)) - 127, kmax = max(max(e0, e1), max(e2, e3)) - 127;
+#pragma unroll 1
+        for (int qi = 0; qi < QG; ++qi) {
+            if (t0q + qi >= P.n_q) break;
+            const int64_t qlen = S.qlen[qi];
+            const bool valid = p < qlen;
+            const bool unsafe = valid && ((kmax - kmin) + S.q_span[qi] > 9 || S.q_min[qi] + kmin - 2 < -126 ||
+                                          S.q_max[qi] + kmax - 2 > 100);
+            const uint32_t todo = __ballot_sync(0xffffffffu, unsafe);
+            if (!todo) continue;
+            float *srow = P.scores + (row0 + qi) * P.n_cand;
+            float sc = valid ? srow[p] : 0.0f;
+            sc = rescore_flagged(todo, sc, kw, g0, P.kc + kbase * kRowBytes, pool, P.pool_mode, P.n_keys, S.b,
+                                 reinterpret_cast<const uint8_t *>(S.sfb), S.w[qi], qi, P.H);
+            if ((todo >> lane) & 1u) srow[p] = sc;
+            if (P.gmax) {
+                const uint32_t gk = __reduce_max_sync(0xffffffffu, valid ? score_key(sc) : 0u);
+                if (lane == 0 && g0 < qlen) P.gmax[(row0 + qi) * P.G + (g0 >> 5)] = gk;
+            }
+        }
+    }
+}
+
 // Registers: with QG = 1, two resident CTAs of 320 threads need every warp within its
 // sub-partition's share of the register file (20 warps over 4 sub-partitions: at most 102
 // registers a thread, 96 after rounding); the launch bound makes the compiler keep to it.
@@ -227,6 +281,7 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
     }
     if (tid < QG * kNPad) { S.hmin[tid >> 5][tid & 31] = 1 << 20; S.hmax[tid >> 5][tid & 31] = -(1 << 20); }
     if (tid < kTile) S.sfb[tid] = 0x7f7f7f7fu;
+    for (int i = tid; i < kFlagWords; i += kThreadsOf<QG>) S.flag_bits[i] = 0u;
     if (warp == 0 && lane == 0) tc::prefetch_tmap(&tmap);
     if (warp == 1) {
         tc::tmem_alloc(&S.tmem_base, C::kTmemCols);
@@ -289,6 +344,37 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
         // first the quantising warps' query reads enter the memory system (named barrier
         // 2), so they are not queued behind every CTA's first tile loads
         asm volatile("bar.sync 2, 160;" ::: "memory");
+        // Exactness (see the file header): a position's MMA dot is exact for query q when its
+        // key block exponents kmin..kmax satisfy kmax - kmin <= 9 - span_q, kmin >= -124 -
+        // min_q and kmax <= 102 - max_q.  When the MMA has released a stage, the producer
+        // reads its scale words back and flags the stage if any position breaks the bounds
+        // of some query of this CTA; flagged stages are re-checked per query and re-scored
+        // after the main loop, so neither the MMA issuer nor the epilogue carries that work.
+        int thr_span = 0, thr_lo = 0, thr_hi = 0;
+        bool have_thr = false;
+        auto check_stage = [&](int st, int tp) {
+            if (!have_thr) {
+                if (!__all_sync(0xffffffffu, tc::mbar_wait(&S.qready, 0, &S.abort_flag))) return;
+                thr_span = 1 << 20; thr_lo = -(1 << 20); thr_hi = 1 << 20;
+#pragma unroll 1
+                for (int qi = 0; qi < QG; ++qi) {
+                    thr_span = min(thr_span, 9 - S.q_span[qi]);
+                    thr_lo = max(thr_lo, -124 - S.q_min[qi]);
+                    thr_hi = min(thr_hi, 102 - S.q_max[qi]);
+                }
+                have_thr = true;
+            }
+            bool uns = false;
+#pragma unroll
+            for (int j = 0; j < 4 * kMB; ++j) {
+                const uint32_t x = S.sfa[st][j * 32 + lane];       // every word once, any order
+                const int e0 = (int)(x & 255u), e1 = (int)((x >> 8) & 255u);
+                const int e2 = (int)((x >> 16) & 255u), e3 = (int)(x >> 24);
+                const int kmn = min(min(e0, e1), min(e2, e3)) - 127, kmx = max(max(e0, e1), max(e2, e3)) - 127;
+                uns |= kmx - kmn > thr_span || kmn < thr_lo || kmx > thr_hi;
+            }
+            if (__any_sync(0xffffffffu, uns) && lane == 0) S.flag_bits[tp >> 5] |= 1u << (tp & 31);
+        };
         int issued = 0;
         uint32_t claim = 0;                       // lane 0: the next claim from the counter
         if (lane == 0 && R == 0) claim = atomicAdd(&P.tile_ctr[unit], 1u);
@@ -299,6 +385,7 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
                 S.abort_flag = 1;
                 break;
             }
+            if (C::kDeferred && i >= kStages && !S.abort_flag) check_stage(s, S.tile[s]);   // its previous tile
             int t = 0;
             if (i < R) {
                 t = (int)blockIdx.x * R + i;
@@ -375,7 +462,21 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
         if (S.abort_flag) {       // let copies already in flight land before the CTA exits
             for (int i = issued - 1; i >= 0 && i >= issued - kStages; --i)
                 tc::mbar_wait_bounded(&S.full[i % kStages], (uint32_t)(i / kStages) & 1u);
+        } else if (C::kDeferred) {
+            // the tiles still in stages: checked once the MMA has released them
+#pragma unroll 1
+            for (int j = issued - kStages + 1 > 0 ? issued - kStages + 1 : 0; j < issued; ++j) {
+                const int st = j % kStages;
+                if (!__all_sync(0xffffffffu, tc::mbar_wait(&S.empty[st], (uint32_t)(j / kStages) & 1u,
+                                                           &S.abort_flag))) {
+                    S.abort_flag = 1;
+                    break;
+                }
+                check_stage(st, S.tile[st]);
+            }
         }
+        // joins the epilogue warps before their re-check of the flagged stages
+        if (C::kDeferred) asm volatile("bar.sync 3, %0;" ::"r"((kEpiWarps + 1) * 32) : "memory");
     } else if (warp == 1) {
         // ================= MMA issuer (lane 0; the warp rearranges bulk-copied scales)
         const uint32_t sfb_t = tmem + C::kColSfb;
@@ -533,14 +634,13 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
         const int ew = warp - 2, quad = warp & 3, mb = (ew >> 2) % kMB, q_lo = (ew >> 2) / kMB * kQPerWarp;
         const int m = mb * kTile + quad * 32 + lane;           // position within the stage
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
-        // this warp's queries: candidates and exponent ranges (read once the first
+        // this warp's queries' candidates and exponent ranges (read once the first
         // accumulator is full, which is after the queries were quantised)
         int64_t qlen[kQPerWarp];
         int qspan[kQPerWarp], qmin[kQPerWarp], qmax[kQPerWarp];
         for (int i = 0;; ++i) {
             const int acc = i % kAcc;
-            // the stage itself is not touched here: the MMA's completion frees it, and this
-            // position's scale bytes are read back from the tensor-memory copy the MMA used
+            // the stage itself is not touched here: the MMA's completion frees it
             const bool ok = tc::mbar_wait(&S.accf[acc], (uint32_t)(i / kAcc) & 1u, &S.abort_flag);
             if (!__all_sync(0xffffffffu, ok)) {   // the warp leaves together (aligned ops follow)
                 S.abort_flag = 1;
@@ -558,12 +658,14 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
                 }
             }
             tc::tc_fence_after();
-            uint32_t sf4[4];
-            // the scale atom holds in lane L the words of rows L, L+32, L+64, L+96 (copied to
-            // every lane quadrant), so row quad*32+lane is word `quad` of this lane
-            asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
-                         : "=r"(sf4[0]), "=r"(sf4[1]), "=r"(sf4[2]), "=r"(sf4[3])
-                         : "r"(lane_base + C::kColSfa + 4 * (acc * kMB + mb)));
+            uint32_t sf4[4] = {0u, 0u, 0u, 0u};
+            if constexpr (!C::kDeferred) {
+                // the scale atom holds in lane L the words of rows L, L+32, L+64, L+96 (copied
+                // to every lane quadrant), so row quad*32+lane is word `quad` of this lane
+                asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(sf4[0]), "=r"(sf4[1]), "=r"(sf4[2]), "=r"(sf4[3])
+                             : "r"(lane_base + C::kColSfa + 4 * (acc * kMB + mb)));
+            }
             uint32_t r[kQPerWarp][32];
 #pragma unroll
             for (int u = 0; u < kQPerWarp; ++u)
@@ -610,14 +712,16 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
                 const bool valid = cand < qlen[u];
                 uint32_t key = 0;
                 float sc = scs[u];
-                const bool unsafe = valid && ((kmax - kmin) + qspan[u] > 9 || qmin[u] + kmin - 2 < -126 ||
-                                              qmax[u] + kmax - 2 > 100);
-                // rare: positions whose tensor-core result cannot be proven exact
-                const uint32_t todo = __ballot_sync(0xffffffffu, unsafe);
-                if (todo)
-                    sc = rescore_flagged(todo, sc, sfw, g0, P.kc + kbase * kRowBytes,
-                                         pool, P.pool_mode, P.n_keys, S.b,
-                                         reinterpret_cast<const uint8_t *>(S.sfb), S.w[qi], qi, H);
+                if constexpr (!C::kDeferred) {
+                    // rare: positions whose tensor-core result cannot be proven exact
+                    const bool unsafe = valid && ((kmax - kmin) + qspan[u] > 9 || qmin[u] + kmin - 2 < -126 ||
+                                                  qmax[u] + kmax - 2 > 100);
+                    const uint32_t todo = __ballot_sync(0xffffffffu, unsafe);
+                    if (todo)
+                        sc = rescore_flagged(todo, sc, sfw, g0, P.kc + kbase * kRowBytes, pool, P.pool_mode,
+                                             P.n_keys, S.b, reinterpret_cast<const uint8_t *>(S.sfb), S.w[qi],
+                                             qi, H);
+                }
                 if (valid) {
                     P.scores[(row0 + qi) * P.n_cand + cand] = sc;
                     key = score_key(sc);
@@ -625,6 +729,27 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
                 if (P.gmax) {            // this warp's 32 candidates are one aligned group
                     const uint32_t gk = __reduce_max_sync(0xffffffffu, key);
                     if (lane == 0 && g0 < qlen[u]) P.gmax[(row0 + qi) * P.G + (g0 >> 5)] = gk;
+                }
+            }
+        }
+        // ---- the flagged stages, after every epilogue warp has written its scores: each
+        //      position is checked per query and re-scored exactly where the MMA result may
+        //      be rounded; the group maxima around re-scored positions are recomputed
+        if constexpr (C::kDeferred) {
+            asm volatile("bar.sync 3, %0;" ::"r"((kEpiWarps + 1) * 32) : "memory");
+            if (!S.abort_flag) {
+                const int nwords = (ntr + 31) >> 5;
+                int seen = 0;
+#pragma unroll 1
+                for (int wi = 0; wi < nwords; ++wi) {
+                    uint32_t bits = S.flag_bits[wi];
+#pragma unroll 1
+                    while (bits) {
+                        const int bit = __ffs(bits) - 1;
+                        bits &= bits - 1u;
+                        if (seen++ % kEpiWarps != ew) continue;
+                        recheck_stage<QG>(P, S, wi * 32 + bit, kSpan, row0, t0q, kbase, pool, n_blk_all);
+                    }
                 }
             }
         }
@@ -663,10 +788,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 }
 
 // Queries per CTA: 4 for a chunk of queries scored against a shared cache (Full mode,
-// at least 8 queries a sequence), else 1.
+// at least 8 queries a sequence, and few enough stages for the stage flags), else 1.
 int tc_query_group(const csa2_index_args &a)
 {
-    return a.mode != CSA2_INDEX_POOL && a.n_q >= 8 ? 4 : 1;
+    const int64_t stages = ((int64_t)a.n_keys + kSpanOf<4> - 1) / kSpanOf<4>;
+    return a.mode != CSA2_INDEX_POOL && a.n_q >= 8 && stages <= (int64_t)kFlagWords * 32 ? 4 : 1;
 }
 
 // CTAs per unit (QG queries): enough units x CTAs to fill the resident CTAs of every SM,

@@ -51,9 +51,6 @@ __device__ __forceinline__ uint32_t block_excl_count(bool f, uint32_t *s_warp, u
     return r;
 }
 
-// Whole-row radix select by one CTA of kTopkThreads threads, reading the row from global
-// memory in four 8-bit digit passes.  The fallback of the group-max path for rows whose
-// candidates do not fit on chip (heavy ties), and the path for more than 2^31 rows.
 // Block-wide exclusive prefix sum of one value per thread (all threads must call).
 __device__ __forceinline__ uint32_t block_excl_count_sum(uint32_t v, uint32_t *s_warp, uint32_t &total)
 {
@@ -84,6 +81,9 @@ __device__ __forceinline__ uint32_t block_excl_count_sum(uint32_t v, uint32_t *s
     return r;
 }
 
+// Whole-row radix select by one CTA of kTopkThreads threads, reading the row from global
+// memory in four 8-bit digit passes.  The fallback of the group-max path for rows whose
+// candidates do not fit on chip (heavy ties), and the path for more than 2^31 rows.
 __device__ __noinline__ void radix_select_row(const float *__restrict__ scores, int64_t n,
                                               const int32_t *__restrict__ row_len,
                                  const int32_t *__restrict__ pool, int32_t block, int32_t k,
@@ -249,14 +249,14 @@ __global__ void __launch_bounds__(256) group_max_kernel(const float *__restrict_
 // to the top k.  With the first `passes` only: tau with its unresolved low bits zero, a
 // lower bound of the exact key (need is then meaningless).
 // Each pass: one histogram of the keys that match the digits found so far (the other
-// buffer is cleared meanwhile for the next pass), then warp 0 alone finds the digit: each
-// lane sums a chunk of bins (descending), a shuffle scan locates the chunk where the
-// count from the top reaches `remaining`, and the lanes split that chunk to find the bin.
-// Two barriers a pass.
+// buffer is cleared meanwhile for the next pass), then a block-wide scan finds the digit:
+// thread t owns nb / kGThreads consecutive bins from the top, an exclusive prefix sum of
+// their counts in thread order is the count above them, and the thread whose bins reach
+// `remaining` names the digit.
 __device__ __forceinline__ uint32_t g_threshold(const uint32_t *keys, int n, uint32_t k, GSmem &S,
                                              uint32_t &need, int passes)
 {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = threadIdx.x, lane = tid & 31;
     uint32_t prefix = 0, mask = 0, remaining = k;
     for (int i = tid; i < kGBins; i += kGThreads) S.hist[0][i] = 0;
     __syncthreads();
@@ -282,41 +282,17 @@ __device__ __forceinline__ uint32_t g_threshold(const uint32_t *keys, int n, uin
             }
         }
         __syncthreads();
-        if (warp == 0) {
-            // chunk L = bins [nb - (L+1)*cw, nb - L*cw); the rotated read order keeps the
-            // 32 lanes on 32 different banks
-            const int cw = nb >> 5;
-            const int lo = nb - (lane + 1) * cw;
-            uint32_t sum = 0;                 // cw is 32 or 64: loads eight at a time
-#pragma unroll 8
-            for (int i = 0; i < cw; ++i) sum += h[lo + ((i + lane) & (cw - 1))];
-            uint32_t incl = sum;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += t;
-            }
-            const uint32_t excl = incl - sum;
-            int L = __ffs(__ballot_sync(0xffffffffu, excl < remaining && incl >= remaining)) - 1;
-            if (L < 0) L = 31;            // cannot happen (the matching keys number >= remaining)
-            const uint32_t above = __shfl_sync(0xffffffffu, excl, L);   // count in higher chunks
-            // chunk L split over the lanes: lane j takes q = cw / 32 bins, descending
-            const int q = cw >> 5, top = nb - 1 - L * cw - lane * q;
-            uint32_t t0 = h[top], t1 = q > 1 ? h[top - 1] : 0u;
-            uint32_t s2 = t0 + t1, inc2 = s2;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const uint32_t t = __shfl_up_sync(0xffffffffu, inc2, o);
-                if (lane >= o) inc2 += t;
-            }
-            const uint32_t c = above + inc2 - s2;                      // count above my bins
-            if (c < remaining && c + t0 >= remaining) {
-                S.pick[0] = (uint32_t)top;
-                S.pick[1] = remaining - c;
-            } else if (q > 1 && c + t0 < remaining && c + t0 + t1 >= remaining) {
-                S.pick[0] = (uint32_t)(top - 1);
-                S.pick[1] = remaining - c - t0;
-            }
+        const int c = nb / kGThreads;                       // 2 or 1 bins per thread
+        const int top = nb - 1 - tid * c;
+        const uint32_t v0 = h[top], v1 = c > 1 ? h[top - 1] : 0u;
+        uint32_t total;
+        const uint32_t above = block_excl_count_sum(v0 + v1, S.warp, total);   // ends with a barrier
+        if (above < remaining && above + v0 >= remaining) {
+            S.pick[0] = (uint32_t)top;
+            S.pick[1] = remaining - above;
+        } else if (c > 1 && above + v0 < remaining && above + v0 + v1 >= remaining) {
+            S.pick[0] = (uint32_t)(top - 1);
+            S.pick[1] = remaining - above - v0;
         }
         __syncthreads();
         prefix |= S.pick[0] << shift;

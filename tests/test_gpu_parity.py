@@ -178,15 +178,23 @@ def test_full_scores_topk_blocks(name):
             assert np.array_equal(idx_g[b, t].cpu().numpy(), idx[b, t].cpu().numpy())
 
 
-def test_scores_wide_exponents():
+@pytest.mark.parametrize("T,sparse", [(2, False), (9, False), (9, True)])
+def test_scores_wide_exponents(T, sparse):
     # random FP4 codes with scale bytes over the whole E8M0 range and queries spanning
-    # 2^-60 .. 2^60 per block: the kernels' wide-sum and overflow paths
-    rng = np.random.default_rng(17)
-    B, T, H, d, N = 2, 2, 8, 128, 3000
+    # 2^-60 .. 2^60 per block: the kernels' wide-sum and overflow paths.  T = 9 takes the
+    # four-queries-per-CTA kernel (stages flagged and re-checked after its main loop);
+    # `sparse` keeps ordinary scales except at 1% of the positions, so only some stages
+    # are flagged and only some positions of those need re-scoring.
+    rng = np.random.default_rng(17 + T + int(sparse))
+    B, H, d, N = 2, 8, 128, 3000
     kc = rng.integers(0, 256, size=(B, N, d // 2), dtype=np.uint8)
     ks = rng.integers(0, 255, size=(B, N, d // 32)).astype(np.uint8)
+    if sparse:
+        wide = rng.random((B, N)) < 0.01
+        ks = np.where(wide[..., None], ks, rng.integers(125, 130, size=ks.shape)).astype(np.uint8)
     q = rng.standard_normal((B, T, H, d)).astype(np.float32)
-    q *= np.exp2(rng.integers(-60, 60, size=(B, T, H, d // 32, 1))).astype(np.float32).reshape(B, T, H, d // 32, 1).repeat(32, -1).reshape(B, T, H, d)
+    qe = rng.integers(-60, 60, size=(B, T, H, d // 32, 1)) if not sparse else rng.integers(-2, 3, size=(B, T, H, d // 32, 1))
+    q *= np.exp2(qe).astype(np.float32).reshape(B, T, H, d // 32, 1).repeat(32, -1).reshape(B, T, H, d)
     qbits = synth.f32_to_bf16_bits(q)
     wv = rng.standard_normal((B, T, H)).astype(np.float32)
     qt = workload.bf16_tensor(qbits, DEV)

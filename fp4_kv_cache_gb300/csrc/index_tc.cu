@@ -507,7 +507,8 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
                 }
                 break;
             }
-            if (S.sf_raw[s]) {
+            const bool raw = S.sf_raw[s] != 0;
+            if (raw) {
                 // position-ordered scale words -> atoms (word lane * 4 + j of block mb holds
                 // position mb * 128 + lane + 32 j): all reads, then all writes
                 uint32_t v[4 * kMB];
@@ -523,7 +524,9 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
             }
             if (lane == 0) {
                 S.acc_tile[acc] = t;
-                tc::fence_proxy_async_smem();
+                // atoms the producer's lanes copied (cp.async) are seen by the tensor core's
+                // copy after this fence; rearranged atoms were fenced by the writing lanes
+                if (!raw) tc::fence_proxy_async_smem();
                 tc::tc_fence_after();
 #pragma unroll
                 for (int mb = 0; mb < kMB; ++mb) {

@@ -3,7 +3,7 @@
 Default workload: Full-mode decode layer, batch 32, 65,536 global positions per sequence,
 indexer 32 heads x 128 (MXFP4 K), main KV 512 + 64 dims (MXFP4), 64 heads, Top-512,
 SWA 128 (bf16).  One step = the whole path for one new token per sequence:
-  csa2_quant_fp4  (write the token's main-KV and indexer-K rows into the caches)
+  csa2_quant_fp4_batch (write the token's main-KV and indexer-K rows into the caches)
   csa2_index_score (indexer query quantised inside; every visible position scored)
   csa2_topk        (Top-512, ascending)
   csa2_sparse_attn (gather + dequantise 512 entries, + 128 SWA keys, 64-head attention)
@@ -248,9 +248,11 @@ def run_gpu(args):
                           dtype=torch.uint8, device=dev)
     flush = L2Flush(dev)
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
-    # our kernels per step: 2 cache-write quantisers, the indexer (it also writes the per-32
-    # group maxima), Top-K select, attention
-    launches_per_step = 5
+    cache_rows = [(new_kv, new_kvc, new_kvs), (new_k, new_kc, new_ks)]
+    cache_jobs = csa2.quant_jobs(cache_rows)
+    # our kernels per step: the cache-write quantiser (both rows), the indexer (it also writes
+    # the per-32 group maxima), Top-K select, attention
+    launches_per_step = 4
 
     def step(k_ev=None):
         # k_ev: events bracketing each call of the step.  The calls form one chain on one
@@ -260,9 +262,9 @@ def run_gpu(args):
         stream = torch.cuda.current_stream(dev)       # the capture stream while capturing
         if k_ev:
             k_ev[0].record(stream)
-        # cache write: the new token's main-KV and indexer-K rows, quantised in place
-        csa2.csa2_quant_fp4(new_kv, new_kvc, new_kvs, st)
-        csa2.csa2_quant_fp4(new_k, new_kc, new_ks, st)
+        # cache write: the new token's main-KV and indexer-K rows, quantised in place (one
+        # launch for both)
+        csa2.csa2_quant_fp4_batch(cache_rows, st, jobs=cache_jobs)
         if k_ev:
             k_ev[1].record(stream)
         csa2.csa2_index_score(iargs, scores, row_len, st, workspace=ws_index)
@@ -468,9 +470,16 @@ def main():
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--prefill-only", action="store_true",
+                    help="time only the prefill indexer (for profiling it) and print its object")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.prefill_only:
+        import torch
+        torch.cuda.set_device(0)
+        print(json.dumps({"prefill_indexer": prefill_indexer(torch.device("cuda", 0), None)}))
+        return 0
     if args.impl == "reference":
         return run_reference(args)
     return run_gpu(args)

@@ -59,6 +59,16 @@ def library_path() -> str:
     return _build.LIB
 
 
+class QuantJob(ctypes.Structure):
+    """csa2_quant_job of include/csa2.h."""
+    _fields_ = [("x", ctypes.c_void_p), ("xt", ctypes.c_int), ("rows", ctypes.c_int64),
+                ("cols", ctypes.c_int64), ("ldx", ctypes.c_int64), ("codes", ctypes.c_void_p),
+                ("ldc", ctypes.c_int64), ("scales", ctypes.c_void_p), ("lds", ctypes.c_int64)]
+
+
+QUANT_MAX_JOBS = 4
+
+
 def load(build_if_missing: bool = True) -> ctypes.CDLL:
     """Load libcsa2.so (building it in-tree first if it is absent or stale)."""
     global _lib
@@ -79,6 +89,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
             lib.csa2_cache_bytes_per_position.argtypes = [S, _I32, _I32]
             lib.csa2_quant_fp4.restype = S
             lib.csa2_quant_fp4.argtypes = [_P, S, _I64, _I64, _I64, _P, _I64, _P, _I64, S, _P, _P]
+            lib.csa2_quant_fp4_batch.restype = S
+            lib.csa2_quant_fp4_batch.argtypes = [ctypes.POINTER(QuantJob), _I32, S, _P, _P]
             lib.csa2_dequant_fp4.restype = S
             lib.csa2_dequant_fp4.argtypes = [_P, _I64, _P, _I64, _I64, _I64, S, _P, S, _I64, _P]
             lib.csa2_index_score_workspace_size.restype = sz
@@ -178,6 +190,31 @@ def csa2_quant_fp4(x: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor,
         raise ValueError("x, codes and scales must have the same number of rows")
     _check("csa2_quant_fp4", load().csa2_quant_fp4(
         px, xt, rows, cols, ldx, pc, ldc, ps, lds, fmt, _ptr(d_status), _stream(stream)))
+
+
+def quant_jobs(triples) -> ctypes.Array:
+    """(x, codes, scales) tensor triples -> a csa2_quant_job array (keep it alive while used)."""
+    jobs = (QuantJob * max(1, len(triples)))()
+    for i, (x, codes, scales) in enumerate(triples):
+        xt = BF16 if x.dtype == torch.bfloat16 else F32 if x.dtype == torch.float32 else None
+        if xt is None:
+            raise ValueError("x must be bf16 or f32")
+        px, rows, ldx = _rows_view(x)
+        pc, rows_c, ldc = _rows_view(codes)
+        ps, rows_s, lds = _rows_view(scales)
+        if rows_c != rows or rows_s != rows:
+            raise ValueError("x, codes and scales must have the same number of rows")
+        jobs[i] = QuantJob(px.value, xt, rows, x.shape[-1], ldx, pc.value, ldc, ps.value, lds)
+    return jobs
+
+
+def csa2_quant_fp4_batch(triples, d_status: Optional[torch.Tensor] = None, stream=None,
+                         fmt: int = FMT_MXFP4, jobs=None):
+    """Quantise several (x, codes, scales) triples in one launch (csa2_quant_fp4_batch)."""
+    if jobs is None:
+        jobs = quant_jobs(triples)
+    _check("csa2_quant_fp4_batch", load().csa2_quant_fp4_batch(
+        jobs, len(triples), fmt, _ptr(d_status), _stream(stream)))
 
 
 def csa2_dequant_fp4(codes: torch.Tensor, scales: torch.Tensor, y: torch.Tensor, stream=None,

@@ -111,6 +111,35 @@ csa2_status csa2_quant_fp4(const void *x, csa2_dtype xt, int64_t rows, int64_t c
                                         lds, d_status, as_stream(stream)));
 }
 
+csa2_status csa2_quant_fp4_batch(const csa2_quant_job *jobs, int32_t n_jobs, csa2_fp4_format fmt,
+                                 uint32_t *d_status, csa2_stream stream)
+{
+    if (fmt == CSA2_FMT_NVFP4_E4M3_16) return CSA2_ERR_UNSUPPORTED;
+    if (fmt != CSA2_FMT_MXFP4 || n_jobs < 0 || n_jobs > CSA2_QUANT_MAX_JOBS) return CSA2_ERR_INVALID_ARG;
+    if (n_jobs == 0) return CSA2_OK;
+    if (!jobs) return CSA2_ERR_INVALID_ARG;
+    QuantJobDesc d[CSA2_QUANT_MAX_JOBS];
+    bool vec = true;
+    for (int k = 0; k < n_jobs; ++k) {
+        const csa2_quant_job &j = jobs[k];
+        if (j.xt != CSA2_BF16 && j.xt != CSA2_F32) return CSA2_ERR_INVALID_ARG;
+        if (j.rows < 0 || j.cols < 0 || j.cols % 32) return CSA2_ERR_INVALID_ARG;
+        if (j.rows && j.cols) {
+            if (!j.x || !j.codes || !j.scales) return CSA2_ERR_INVALID_ARG;
+            if (j.ldx < j.cols || j.ldc < j.cols / 2 || j.lds < j.cols / 32) return CSA2_ERR_INVALID_ARG;
+        }
+        d[k] = {j.x, j.xt == CSA2_BF16, j.rows, j.cols, j.ldx, j.codes, j.ldc, j.scales, j.lds};
+        vec = vec && quant_job_vec_ok(d[k]);
+    }
+    if (vec) return from_cuda(launch_quant_mxfp4_batch(d, n_jobs, d_status, as_stream(stream)));
+    for (int k = 0; k < n_jobs; ++k) {           // some rows misaligned: one launch per job
+        const cudaError_t e = launch_quant_mxfp4(d[k].x, d[k].x_bf16, d[k].rows, d[k].cols, d[k].ldx, d[k].codes,
+                                                 d[k].ldc, d[k].scales, d[k].lds, d_status, as_stream(stream));
+        if (e != cudaSuccess) return from_cuda(e);
+    }
+    return CSA2_OK;
+}
+
 csa2_status csa2_dequant_fp4(const uint8_t *codes, int64_t ldc, const uint8_t *scales,
                              int64_t lds, int64_t rows, int64_t cols, csa2_fp4_format fmt,
                              void *y, csa2_dtype yt, int64_t ldy, csa2_stream stream)

@@ -106,6 +106,74 @@ __global__ void __launch_bounds__(256) quant_mxfp4_vec_kernel(const void *__rest
     }
 }
 
+// Several jobs in one launch: their 4-lane block groups are laid end to end (each job's
+// lane count is a multiple of 4, so no group straddles two jobs) and every lane finds its
+// job from the running lane counts; the per-lane work is the vectorised kernel's.
+struct QuantBatchParams {
+    const void *x[4];
+    uint8_t *codes[4], *scales[4];
+    int64_t nblk[4], ldx[4], ldc[4], lds[4];
+    int64_t lanes_end[4];          // running total of 4 x blocks over jobs 0..j
+    int bf16[4];
+    int n;
+};
+
+__global__ void __launch_bounds__(256) quant_mxfp4_batch_kernel(const __grid_constant__ QuantBatchParams B,
+                                                                uint32_t *d_status)
+{
+    pdl_wait();                                   // x may come from the kernel before
+    pdl_allow_dependents();
+    const int64_t total = B.lanes_end[B.n - 1];
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t total32 = (total + 31) & ~int64_t(31);
+    for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total32; t += stride) {
+        const bool act = t < total;
+        int j = 0;
+#pragma unroll
+        for (int k = 0; k < 3; ++k) j += (k + 1 < B.n && t >= B.lanes_end[k]) ? 1 : 0;
+        const int64_t tl = act ? t - (j > 0 ? B.lanes_end[j - 1] : 0) : 0;
+        const int64_t grp = tl >> 2;
+        const int sub = (int)(tl & 3);
+        const int64_t nblk = B.nblk[j];
+        const int64_t r = grp / nblk, kb = grp % nblk;
+        float v[8];
+        if (act && B.bf16[j]) {
+            const uint4 raw = *reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(B.x[j]) +
+                                                               r * B.ldx[j] + kb * 32 + sub * 8);
+            const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                v[2 * i] = __uint_as_float(w[i] << 16);
+                v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+            }
+        } else if (act) {
+            const float4 *src = reinterpret_cast<const float4 *>(static_cast<const float *>(B.x[j]) +
+                                                                 r * B.ldx[j] + kb * 32 + sub * 8);
+            const float4 a = src[0], b = src[1];
+            v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+            v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = 0.0f;
+        }
+        uint32_t amax = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) amax = max(amax, __float_as_uint(v[i]) & 0x7fffffffu);
+        amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        if (!act) continue;
+        const bool finite = amax < 0x7f800000u;
+        if (!finite && sub == 0) dev_flag(d_status, CSA2_DEV_NONFINITE);
+        const int X = mx_block_exponent(__uint_as_float(finite ? amax : 0u));
+        const float inv = pow2_neg(X);
+        uint32_t word = 0;
+#pragma unroll
+        for (int i = 0; i < 8; i += 2) word |= e2m1x2_cvt(v[i] * inv, v[i + 1] * inv) << (4 * i);
+        *reinterpret_cast<uint32_t *>(B.codes[j] + r * B.ldc[j] + kb * 16 + sub * 4) = word;
+        if (sub == 0) B.scales[j][r * B.lds[j] + kb] = (uint8_t)(X + 127);
+    }
+}
+
 template <bool BF16>
 __global__ void __launch_bounds__(256) dequant_mxfp4_kernel(const uint8_t *__restrict__ codes,
                                                             int64_t ldc,
@@ -162,6 +230,41 @@ cudaError_t launch_quant_mxfp4(const void *x, bool x_bf16, int64_t rows, int64_t
         quant_mxfp4_kernel<false><<<grid, 256, 0, s>>>(x, rows, cols, ldx, codes, ldc, scales, lds,
                                                        d_status);
     return cudaGetLastError();
+}
+
+bool quant_job_vec_ok(const QuantJobDesc &j)
+{
+    const size_t esz = j.x_bf16 ? 2 : 4;
+    return ((uintptr_t)j.x % 16 == 0) && ((j.ldx * (int64_t)esz) % 16 == 0) && ((uintptr_t)j.codes % 4 == 0) &&
+           (j.ldc % 4 == 0);
+}
+
+cudaError_t launch_quant_mxfp4_batch(const QuantJobDesc *jobs, int n_jobs, uint32_t *d_status, cudaStream_t s)
+{
+    if (n_jobs < 1 || n_jobs > 4) return cudaErrorInvalidValue;
+    QuantBatchParams B = {};
+    int64_t acc = 0;
+    int n = 0;
+    for (int k = 0; k < n_jobs; ++k) {
+        const QuantJobDesc &j = jobs[k];
+        if (!quant_job_vec_ok(j)) return cudaErrorInvalidValue;
+        if (j.rows == 0 || j.cols == 0) continue;
+        B.x[n] = j.x;
+        B.codes[n] = j.codes;
+        B.scales[n] = j.scales;
+        B.nblk[n] = j.cols / 32;
+        B.ldx[n] = j.ldx;
+        B.ldc[n] = j.ldc;
+        B.lds[n] = j.lds;
+        B.bf16[n] = j.x_bf16 ? 1 : 0;
+        acc += j.rows * (j.cols / 32) * 4;
+        B.lanes_end[n] = acc;
+        ++n;
+    }
+    if (n == 0) return cudaSuccess;
+    B.n = n;
+    for (int k = n; k < 4; ++k) B.lanes_end[k] = acc;
+    return launch_pdl(quant_mxfp4_batch_kernel, dim3(grid_for(acc, 256)), dim3(256), 0, s, 1, B, d_status);
 }
 
 cudaError_t launch_dequant_mxfp4(const uint8_t *codes, int64_t ldc, const uint8_t *scales,

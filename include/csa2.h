@@ -115,6 +115,28 @@ CSA2_API csa2_status csa2_dequant_fp4(const uint8_t *codes, int64_t ldc, const u
                              void *y, csa2_dtype yt, int64_t ldy, csa2_stream stream);
 
 /* ---------------------------------------------------------------------------------- */
+/* csa2_quant_fp4_batch -- up to CSA2_QUANT_MAX_JOBS independent csa2_quant_fp4 calls  */
+/* in one launch (a decode step writes its token's main-KV row and indexer-K row).      */
+/* jobs: HOST array of n_jobs (0..CSA2_QUANT_MAX_JOBS) descriptions, each with the      */
+/* meaning and rules of the csa2_quant_fp4 arguments of the same names; every job uses  */
+/* format fmt.  The outputs of different jobs must not overlap.  Results are those of   */
+/* n_jobs separate csa2_quant_fp4 calls (one kernel when every job has 16-byte aligned  */
+/* rows of x and 4-byte aligned rows of codes, else one launch per job).                */
+/* ---------------------------------------------------------------------------------- */
+#define CSA2_QUANT_MAX_JOBS 4
+typedef struct {
+    const void *x;        /* rows x cols values of type xt, row stride ldx elements        */
+    csa2_dtype xt;        /* CSA2_BF16 or CSA2_F32                                         */
+    int64_t rows, cols, ldx;
+    uint8_t *codes;       /* rows x cols/2 bytes, row stride ldc                           */
+    int64_t ldc;
+    uint8_t *scales;      /* rows x cols/32 bytes, row stride lds                          */
+    int64_t lds;
+} csa2_quant_job;
+CSA2_API csa2_status csa2_quant_fp4_batch(const csa2_quant_job *jobs, int32_t n_jobs, csa2_fp4_format fmt,
+                                          uint32_t *d_status, csa2_stream stream);
+
+/* ---------------------------------------------------------------------------------- */
 /* csa2_index_score -- indexer scores (report §2.3: the indexer scores main-KV entries  */
 /* with indexer Q and indexer K; §2.3.2: Reindex layers score only the pool).           */
 /*                                                                                    */

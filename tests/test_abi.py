@@ -28,7 +28,7 @@ def lib():
 
 def test_exports_every_declared_symbol(lib):
     syms = _declared_symbols()
-    assert len(syms) == 14
+    assert len(syms) == 15
     for s in syms:
         assert hasattr(lib, s), s
     out = os.popen(f"nm -D --defined-only {libbuild.LIB}").read()
@@ -76,6 +76,26 @@ def test_quant_rejects_bad_shapes(lib):
     assert lib.csa2_quant_fp4(FAKE, 0, 4, 32, 16, FAKE, 16, FAKE, 1, 0, None, None) == 1
     assert lib.csa2_quant_fp4(FAKE, 0, 4, 32, 32, FAKE, 16, FAKE, 1, 1, None, None) == 2
     assert lib.csa2_quant_fp4(None, 0, 0, 32, 32, None, 16, None, 1, 0, None, None) == 0
+
+
+def test_quant_batch_rejects_bad_args(lib):
+    def jobs(*specs):
+        arr = (csa2.QuantJob * max(1, len(specs)))()
+        for i, (xt, rows, cols, ldx, ldc, lds) in enumerate(specs):
+            arr[i] = csa2.QuantJob(FAKE, xt, rows, cols, ldx, FAKE, ldc, FAKE, lds)
+        return arr
+    ok = (0, 4, 32, 32, 16, 1)
+    assert lib.csa2_quant_fp4_batch(jobs(ok), 5, 0, None, None) == 1          # more than 4 jobs
+    assert lib.csa2_quant_fp4_batch(jobs(ok), -1, 0, None, None) == 1
+    assert lib.csa2_quant_fp4_batch(jobs(ok), 1, 1, None, None) == 2          # NVFP4: unsupported
+    assert lib.csa2_quant_fp4_batch(None, 1, 0, None, None) == 1
+    assert lib.csa2_quant_fp4_batch(jobs(ok, (0, 4, 33, 33, 17, 2)), 2, 0, None, None) == 1
+    assert lib.csa2_quant_fp4_batch(jobs(ok, (5, 4, 32, 32, 16, 1)), 2, 0, None, None) == 1
+    assert lib.csa2_quant_fp4_batch(jobs(ok, (0, 4, 32, 16, 16, 1)), 2, 0, None, None) == 1
+    assert lib.csa2_quant_fp4_batch(None, 0, 0, None, None) == 0              # nothing to do
+    empty = (csa2.QuantJob * 1)()
+    empty[0] = csa2.QuantJob(None, 0, 0, 32, 32, None, 16, None, 1)
+    assert lib.csa2_quant_fp4_batch(empty, 1, 0, None, None) == 0             # zero rows: no launch
 
 
 def test_index_rejects_bad_args(lib):

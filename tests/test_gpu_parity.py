@@ -85,6 +85,33 @@ def test_quant_dequant_parity(cols, as_bf16):
     assert np.array_equal(s2.cpu().numpy()[nz], s_ref[nz])
 
 
+@pytest.mark.parametrize("aligned", [True, False])
+def test_quant_batch_parity(aligned):
+    # one launch for several jobs (bf16 and f32, different widths, a row-strided cache view);
+    # aligned=False gives one job rows that are not 16-byte aligned (one launch per job)
+    specs = [(577, 576, True), (33, 128, False), (5, 64, True), (40, 32, False)]
+    st = status()
+    triples, refs = [], []
+    for i, (rows, cols, bf16) in enumerate(specs):
+        raw, x = _codec_inputs(rows, cols, 7000 + i, bf16)
+        xt = workload.bf16_tensor(raw, DEV) if bf16 else torch.from_numpy(raw).to(DEV)
+        if not aligned and i == 1:            # rows of 128 + 1 floats: 4-byte aligned only
+            wide = torch.zeros((rows, cols + 1), dtype=xt.dtype, device=DEV)
+            wide[:, :cols] = xt
+            xt = wide[:, :cols]
+        cache_c = torch.full((rows, cols // 2 + 16), 0xAB, dtype=torch.uint8, device=DEV)   # strided rows
+        cache_s = torch.full((rows, cols // 32 + 4), 0xAB, dtype=torch.uint8, device=DEV)
+        triples.append((xt, cache_c[:, : cols // 2], cache_s[:, : cols // 32]))
+        refs.append((oracle.quant_mxfp4(x), cache_c, cache_s, cols))
+    csa2.csa2_quant_fp4_batch(triples, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    for (c_ref, s_ref), cache_c, cache_s, cols in refs:
+        assert np.array_equal(cache_c[:, : cols // 2].cpu().numpy(), c_ref)
+        assert np.array_equal(cache_s[:, : cols // 32].cpu().numpy(), s_ref)
+        assert torch.all(cache_c[:, cols // 2:] == 0xAB) and torch.all(cache_s[:, cols // 32:] == 0xAB)
+
+
 def test_quant_flags_nonfinite():
     x = torch.zeros((3, 64), dtype=torch.float32, device=DEV)
     x[1, 40] = float("inf")

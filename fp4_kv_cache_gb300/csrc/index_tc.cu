@@ -11,17 +11,20 @@
 // Exactness.  The score is defined on D_h = RN32(exact dot).  Each K = 32 block adds an
 // integer (< 2^13) times 2^(Xq + Xk - 2); when every term's exponent lies within 9 of the
 // others and in the normal range, every partial sum is exactly representable, so the MMA's
-// float32 accumulation returns the exact dot whatever its order.  The epilogue checks that
-// condition conservatively per position from the scale bytes; a segment with any position
-// outside it is re-scored by the exact CUDA-core kernel (index_score.cu).
+// float32 accumulation returns the exact dot whatever its order.  That condition is checked
+// conservatively per position and query from the scale bytes; a position outside it is
+// re-scored on CUDA cores (per head, an integer dot of the E2M1 codes per block and one
+// dyadic sum rounded once): in decode by the epilogue warp in place, in prefill chunks
+// after the main loop for the stages the producer flagged.
 //
-// Roles: warp 0 = producer (TMA for the FP4 codes with the 64-byte swizzle, cp.async for
-// the scale bytes into the 512-byte scale-factor atom), warp 1 = MMA issuer (tcgen05.cp of
-// scale factors to TMEM, tcgen05.mma, tcgen05.commit), then the epilogue warps (each reads
-// its own TMEM lane quadrant).  A shared-memory ring of K tiles, accumulators rotating in
-// TMEM.  A CTA scores QG queries of one sequence (N = QG x 32): QG = 1 in decode, where
-// the CTAs of one query row share its tiles; QG = 4 in prefill chunks, where one K tile
-// feeds four queries' dots.
+// Roles: warp 0 = producer (TMA for the FP4 codes with the 64-byte swizzle; the scale
+// bytes by one bulk copy per stage, or by cp.async straight into the 512-byte
+// scale-factor atoms where a stage is not one contiguous run), warp 1 = MMA issuer (lays
+// bulk-copied scales out as atoms, tcgen05.cp of scale factors to TMEM, tcgen05.mma,
+// tcgen05.commit), then the epilogue warps (each reads its own TMEM lane quadrant).  A
+// shared-memory ring of stages, accumulators rotating in TMEM.  A CTA scores QG queries of
+// one sequence (N = QG x 32): QG = 1 in decode, where the CTAs of one query row share its
+// stages; QG = 4 in prefill chunks, where one K tile feeds four queries' dots.
 #include <cudaTypedefs.h>
 #include <mutex>
 

@@ -13,7 +13,9 @@ metric: decode tokens/s per layer (batch / step time); roofline of the dominant 
   python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--no-prefill]
 Under torchrun each rank runs its own replica (the path has no exchange step).
 Rank 0 also times the prefill indexer on an encoder chunk (4,096 queries after 65,536
-entries at ratio 2) and reports it beside the decode line as "prefill_indexer".
+entries at ratio 2) and reports it beside the decode line as "prefill_indexer", and one
+decoder group (the Full layer's step, then 3 Reuse layers attending its Top-K) as
+"decoder_group".
 """
 from __future__ import annotations
 
@@ -396,6 +398,47 @@ def run_gpu(args):
     if int(st.item()) != 0:
         raise RuntimeError(f"device status {int(st.item())}")
 
+    # ---- a decoder group (report §4.2.1 schedule: a Full layer then 3 Reuse layers that
+    #      attend its Top-K over the same shared cache, each with its own query and SWA KV),
+    #      one CUDA graph, L2 flushed between groups; rank 0 only
+    group = None
+    if rank == 0 and not args.no_group and graph is not None:
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(w.seed * 7919 + 3)
+        r_q = [torch.randn(dw["q_attn"].shape, generator=gen, device=dev).to(torch.bfloat16) for _ in range(3)]
+        r_swa = [torch.randn(dw["swa"].shape, generator=gen, device=dev).to(torch.bfloat16) for _ in range(3)]
+        r_out = [torch.empty_like(out) for _ in range(3)]
+        r_lse = [torch.empty_like(lse) for _ in range(3)]
+        r_args = [csa2.make_attn_args(r_q[l], dw["kv_codes"], dw["kv_scales"], idx, r_swa[l], dw["swa_pos0"],
+                                      dw["q_pos"], None, w.window, dw.sm_scale, w.d_v) for l in range(3)]
+
+        def group_step():
+            step()
+            for l in range(3):
+                csa2.csa2_sparse_attn(r_args[l], r_out[l], r_lse[l], st, workspace=ws_attn)
+
+        for _ in range(args.warmup):
+            group_step()
+        g_group = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_group):
+            group_step()
+        g_ms = []
+        for it in range(args.steps + 2):
+            flush()
+            e0, e1 = ev(), ev()
+            e0.record(stream)
+            g_group.replay()
+            e1.record(stream)
+            e1.synchronize()
+            if it >= 2:
+                g_ms.append(e0.elapsed_time(e1))
+        if int(st.item()) != 0:
+            raise RuntimeError(f"device status {int(st.item())}")
+        gt = sum(g_ms) / len(g_ms)
+        group = {"layers": "Full + 3 Reuse (one decoder group, shared cache, Full layer's Top-K reused)",
+                 "ms": gt, "tokens_per_s": B * T / (gt * 1e-3), "ms_per_layer": gt / 4,
+                 "launches": launches_per_step + 3}
+
     # ---- max over ranks
     if dist:
         t = torch.tensor([ms_step, ms_k, e2e_step], dtype=torch.float64, device=dev)
@@ -435,6 +478,8 @@ def run_gpu(args):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks.summary(),
     }
+    if group is not None:
+        line["decoder_group"] = group
     if not args.no_prefill:
         line["prefill_indexer"] = prefill_indexer(dev, line["clocks"].get("sm_mhz"))
     if not args.no_cpu_baseline:
@@ -503,6 +548,7 @@ def main():
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-group", action="store_true")
     ap.add_argument("--prefill-only", action="store_true",
                     help="time only the prefill indexer (for profiling it) and print its object")
     args = ap.parse_args()

@@ -57,7 +57,7 @@ template <int QG> struct Cfg;
 // otherwise the epilogue checks each position's bounds and re-scores in place (decode).
 template <> struct Cfg<1> {
     static constexpr bool kDeferred = false;
-    static constexpr int kStages = 6, kAcc = 3, kMB = 2, kEpiPerQuad = 2, kCtasPerSm = 2;
+    static constexpr int kStages = 4, kAcc = 3, kMB = 2, kEpiPerQuad = 2, kCtasPerSm = 2;
     static constexpr uint32_t kTmemCols = 256, kColSfa = 192, kColSfb = 216;
 };
 template <> struct Cfg<4> {

@@ -57,7 +57,7 @@ class L2Flush:
 # DRAM bytes (read + write) of one csa2_index_score tensor-core launch on this workload, from
 # the ncu capture summarised in profiles/index_score_tc_kernel_full_decode_64k.md; None
 # whenever the kernel has changed since that capture.
-INDEX_TRAFFIC_BYTES = 150076160      # ncu: dram__bytes_read.sum + dram__bytes_write.sum, one launch
+INDEX_TRAFFIC_BYTES = None      # kernel changed since the last capture
 
 
 def _peaks():

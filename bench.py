@@ -57,7 +57,7 @@ class L2Flush:
 # DRAM bytes (read + write) of one csa2_index_score tensor-core launch on this workload, from
 # the ncu capture summarised in profiles/index_score_tc_kernel_full_decode_64k.md; None
 # whenever the kernel has changed since that capture.
-INDEX_TRAFFIC_BYTES = None      # kernel changed since the last capture
+INDEX_TRAFFIC_BYTES = 143_169_024 + 7_500_288
 
 
 def _peaks():

@@ -6,7 +6,8 @@ with the CUDA sources: the arithmetic lives in ``csa2_oracle.c`` (plain loops,
 exact integers, fp64), selection here uses a library sort.
 
 What it computes, step by step (DeepSeek-V4.1-Flash report, aipaper.jasonlin.tech):
-  1. MXFP4 codec for indexer q/k and the main KV (report §2.4.4; OCP MX v1.0 rule).
+  1. MXFP4 codec for indexer q/k and the main KV (report §2.4.4; OCP MX v1.0 rule);
+     the report's own main-KV format, E2M1 + E4M3 per 16 (report §2.4.4), as an option.
   2. Indexer score of every candidate position, s = sum_h w_h ReLU(q_h . k), with the
      per-head dot rounded once to float32 and the head sum a float32 fma chain
      (the kernel's precision, since these floats decide indices).
@@ -60,6 +61,8 @@ def _L():
             I = ctypes.c_int
             lib.orc_quant_mxfp4.argtypes = [P, I64, I64, P, P]
             lib.orc_dequant_mxfp4.argtypes = [P, P, I64, I64, P]
+            lib.orc_quant_nvfp4.argtypes = [P, I64, I64, P, P]
+            lib.orc_dequant_nvfp4.argtypes = [P, P, I64, I64, P]
             lib.orc_head_dots.argtypes = [I, I, P, P, P, P, P, I64, P]
             lib.orc_index_scores.argtypes = [I, I, P, P, P, P, P, P, I64, P]
             lib.orc_attention.argtypes = [I64, I, I, I, P, P, P, ctypes.c_double, P, P]
@@ -99,6 +102,44 @@ def dequant_mxfp4(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
     y = np.empty(codes.shape[:-1] + (D,), np.float64)
     _L().orc_dequant_mxfp4(_p(codes), _p(scales), rows, D, _p(y))
     return y
+
+
+# ---------------------------------------------------------------- E2M1 + E4M3/16 codec
+def quant_nvfp4(x: np.ndarray):
+    """Main-KV format of the report (§2.4.4): E2M1 codes with one E4M3 scale per 16
+    values, no global scale.  x [..., D] (exact values), D % 16 == 0 ->
+    (codes uint8 [..., D/2], scales uint8 [..., D/16]).  Scale = amax/6 rounded to the
+    nearest E4M3 value (ties to even, clamped to 448); a zero scale zeroes the block."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    D = x.shape[-1]
+    assert D % 16 == 0
+    rows = x.size // D
+    codes = np.empty(x.shape[:-1] + (D // 2,), np.uint8)
+    scales = np.empty(x.shape[:-1] + (D // 16,), np.uint8)
+    _L().orc_quant_nvfp4(_p(x), rows, D, _p(codes), _p(scales))
+    return codes, scales
+
+
+def dequant_nvfp4(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.uint8)
+    D = codes.shape[-1] * 2
+    rows = codes.size // (D // 2)
+    y = np.empty(codes.shape[:-1] + (D,), np.float64)
+    _L().orc_dequant_nvfp4(_p(codes), _p(scales), rows, D, _p(y))
+    return y
+
+
+def quant_main_kv(x: np.ndarray, fmt: str = "mxfp4"):
+    """Main-KV cache rows in format ``fmt`` ("mxfp4" or "nvfp4")."""
+    return quant_nvfp4(x) if fmt == "nvfp4" else quant_mxfp4(x)
+
+
+def dequant_main_kv(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """Dequantise main-KV rows; the format follows from the scale count (D/16 scales:
+    E2M1 + E4M3/16, D/32: MXFP4)."""
+    D = codes.shape[-1] * 2
+    return dequant_nvfp4(codes, scales) if scales.shape[-1] == D // 16 else dequant_mxfp4(codes, scales)
 
 
 # ---------------------------------------------------------------- scoring
@@ -242,12 +283,13 @@ def attention_rows(q_rows, key_lists, sm_scale, d_v):
 
 def gather_keys(idx, kv_codes, kv_scales, swa_f64, q_pos, swa_pos0, window, swa_start):
     """Key list of one query: dequantised main-KV rows for idx >= 0 (in idx order,
-    duplicates kept, out-of-range indices dropped), then its SWA slots in order."""
+    duplicates kept, out-of-range indices dropped), then its SWA slots in order.  The
+    main KV may be MXFP4 or E2M1 + E4M3/16 (told apart by the scale count)."""
     n = kv_codes.shape[0]
     sel = [int(i) for i in np.asarray(idx).reshape(-1) if 0 <= int(i) < n]
     parts = []
     if sel:
-        parts.append(dequant_mxfp4(kv_codes[sel], kv_scales[sel]))
+        parts.append(dequant_main_kv(kv_codes[sel], kv_scales[sel]))
     if swa_f64 is not None:
         j0, j1 = swa_keys_range(q_pos, swa_pos0, swa_f64.shape[0], window, swa_start)
         if j1 >= j0:

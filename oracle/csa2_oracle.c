@@ -119,6 +119,108 @@ void orc_dequant_mxfp4(const uint8_t *codes, const uint8_t *scales, int64_t rows
 }
 
 /* ------------------------------------------------------------------------- */
+/* NVFP4-style main-KV codec: E2M1 elements with one E4M3 scale per block of   */
+/* 16 and no global scale (report §2.4.4; review page, "四位缓存" ledger:       */
+/* 256 B of E2M1 codes + 32 B of E4M3 scales for 512 channels).  The pages do  */
+/* not say how the scale is picked; the reading used here maps the block's    */
+/* largest magnitude onto the largest E2M1 value: scale = amax / 6 rounded to  */
+/* the nearest E4M3 value (ties to the even code), values above 448 clamped to */
+/* 448; elements = x / scale rounded to the nearest E2M1 value (ties to the    */
+/* even code, saturating at 6), sign bit = sign bit of x.  A scale that rounds */
+/* to 0 encodes every element of its block as a signed zero.                  */
+/* Every decision below is an exact comparison in double: the products of a   */
+/* scale (4 significant bits) with a grid value or midpoint (<= 3 bits) and    */
+/* with 6 are exact.                                                          */
+/* ------------------------------------------------------------------------- */
+
+/* E4M3 value of a byte: 1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits;
+ * exponent field 0 is subnormal (m * 2^-9); 0x7F / 0xFF are NaN (no infinities). */
+static double e4m3_value(int byte)
+{
+    int e = (byte >> 3) & 15, m = byte & 7;
+    double mag;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) mag = ldexp((double)m, -9);
+    else mag = ldexp(1.0 + m / 8.0, e - 7);
+    return (byte & 0x80) ? -mag : mag;
+}
+
+/* E4M3 scale byte for a block maximum amax >= 0: the nearest non-negative finite E4M3
+ * value to amax / 6 (codes 0x00..0x7E ascend with their values), ties to the even code,
+ * anything above 448 clamped to 448 (0x7E). */
+static int e4m3_scale_byte(double amax)
+{
+    if (amax > 6.0 * 448.0) return 0x7E;
+    for (int c = 0; c < 0x7E; ++c) {
+        double lo = e4m3_value(c), hi = e4m3_value(c + 1);
+        if (amax <= 6.0 * hi) {
+            double mid6 = 6.0 * (0.5 * (lo + hi));        /* exact */
+            if (amax < mid6) return c;
+            if (amax > mid6) return c + 1;
+            return (c % 2 == 0) ? c : c + 1;
+        }
+    }
+    return 0x7E;
+}
+
+/* Nearest E2M1 magnitude code to a / s (a >= 0, s > 0), ties to the even code, saturating
+ * at 6: a compared with s * (grid midpoint), exact in double. */
+static int e2m1_round_ratio(double a, double s)
+{
+    if (a >= 6.0 * s) return 7;
+    for (int c = 0; c < 7; ++c) {
+        double lo = e2m1_magnitude(c), hi = e2m1_magnitude(c + 1);
+        if (a <= hi * s) {
+            double mid = s * (0.5 * (lo + hi));           /* exact */
+            if (a < mid) return c;
+            if (a > mid) return c + 1;
+            return (c % 2 == 0) ? c : c + 1;
+        }
+    }
+    return 7;
+}
+
+/* Quantise rows of doubles (exact bf16/fp32 values) to E2M1 + E4M3 per 16.
+ * codes: [rows, cols/2], element 2i in the low nibble; scales: [rows, cols/16]. */
+void orc_quant_nvfp4(const double *x, int64_t rows, int64_t cols, uint8_t *codes, uint8_t *scales)
+{
+    int64_t nblk = cols / 16;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t b = 0; b < nblk; ++b) {
+            const double *xb = x + r * cols + b * 16;
+            double amax = 0.0;
+            for (int i = 0; i < 16; ++i) amax = fmax(amax, fabs(xb[i]));
+            int sb = e4m3_scale_byte(amax);
+            double s = e4m3_value(sb);
+            scales[r * nblk + b] = (uint8_t)sb;
+            for (int i = 0; i < 16; ++i) {
+                int mag = s > 0.0 ? e2m1_round_ratio(fabs(xb[i]), s) : 0;
+                int c = mag | (signbit(xb[i]) ? 8 : 0);
+                uint8_t *p = &codes[r * (cols / 2) + b * 8 + i / 2];
+                if (i % 2 == 0) *p = (uint8_t)c;
+                else *p = (uint8_t)(*p | (c << 4));
+            }
+        }
+    }
+}
+
+/* Dequantise E2M1 + E4M3/16 rows to doubles: sign * magnitude(code) * e4m3(scale). */
+void orc_dequant_nvfp4(const uint8_t *codes, const uint8_t *scales, int64_t rows, int64_t cols,
+                       double *y)
+{
+    int64_t nblk = cols / 16;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t i = 0; i < cols; ++i) {
+            int byte = codes[r * (cols / 2) + i / 2];
+            int c = (i % 2 == 0) ? (byte & 15) : (byte >> 4);
+            double m = e2m1_magnitude(c & 7) * e4m3_value(scales[r * nblk + i / 16]);
+            y[r * cols + i] = (c & 8) ? -m : m;
+        }
+}
+
+/* ------------------------------------------------------------------------- */
 /* Exact dot product of two MXFP4 vectors, rounded once to float32.           */
 /* Twice an E2M1 magnitude is an integer, so each block of 32 contributes     */
 /*   I_b * 2^(Xq_b + Xk_b - 2),  I_b = sum (2 q_i)(2 k_i)  (|I_b| <= 4608).     */

@@ -6,8 +6,10 @@ rounding an explicit integer round-half-even.  Slow by design: only for inputs
 of a few dozen positions.
 
 Format facts used (DeepSeek-V4.1-Flash report, aipaper.jasonlin.tech, §2.4.4:
-indexer queries and keys in OCP MXFP4): E2M1 = 1 sign bit, 2 exponent bits with
-bias 1, 1 mantissa bit; E8M0 scale = 2^(byte - 127); blocks of 32.
+indexer queries and keys in OCP MXFP4; main KV in E2M1 with an E4M3 scale per 16):
+E2M1 = 1 sign bit, 2 exponent bits with bias 1, 1 mantissa bit; E8M0 scale =
+2^(byte - 127); blocks of 32.  E4M3 = 1 sign bit, 4 exponent bits with bias 7,
+3 mantissa bits, no infinities, 0x7F/0xFF NaN; blocks of 16.
 """
 from __future__ import annotations
 
@@ -58,6 +60,37 @@ def quant_block(xs: Sequence[Fraction], signs: Sequence[bool]):
             c = best
         codes.append(c | (8 if neg else 0))
     return X + 127, codes
+
+
+def e4m3_value(byte: int):
+    """Value of an E4M3 byte from its bit fields (None for the NaN codes)."""
+    e, m = (byte >> 3) & 15, byte & 7
+    if e == 15 and m == 7:
+        return None
+    mag = Fraction(m, 8) * TWO ** -6 if e == 0 else (1 + Fraction(m, 8)) * TWO ** (e - 7)
+    return -mag if byte & 0x80 else mag
+
+
+def quant_block_nvfp4(xs: Sequence[Fraction], signs: Sequence[bool]):
+    """One block of 16 exact values in E2M1 + E4M3 -> (scale byte, [codes]).
+
+    Scale: the finite non-negative E4M3 value nearest to amax/6 (ties to the even
+    code; beyond 448 the nearest is 448).  Elements: the E2M1 magnitude nearest to
+    |x|/scale (ties to the even code), all zero when the scale is 0."""
+    amax = max(abs(x) for x in xs)
+    t = amax / 6
+    sb = min(range(0x7F), key=lambda c: (abs(t - e4m3_value(c)), c % 2))
+    s = e4m3_value(sb)
+    grid = [abs(e2m1_value(c)) for c in range(8)]
+    codes = []
+    for x, neg in zip(xs, signs):
+        if s == 0:
+            c = 0
+        else:
+            v = abs(x) / s
+            c = min(range(8), key=lambda c: (abs(v - grid[c]), c % 2))
+        codes.append(c | (8 if neg else 0))
+    return sb, codes
 
 
 def rn32(x: Fraction) -> np.float32:

@@ -216,7 +216,8 @@ def run_gpu(args):
 
     w = synth.WORKLOADS[WORKLOAD]
     st = torch.zeros(1, dtype=torch.int32, device=dev)
-    dw = workload.build(w, device=dev, d_status=st)
+    want_nv = rank == 0 and not args.no_nvfp4
+    dw = workload.build(w, device=dev, d_status=st, also_nvfp4=want_nv)
     B, T = w.batch, w.n_q
     stream = torch.cuda.current_stream(dev)
 
@@ -439,6 +440,64 @@ def run_gpu(args):
                  "ms": gt, "tokens_per_s": B * T / (gt * 1e-3), "ms_per_layer": gt / 4,
                  "launches": launches_per_step + 3}
 
+    # ---- the same step over the report's own main-KV format (E2M1 + E4M3 per 16, report
+    #      §2.4.4): cache write (main-KV row in that format, indexer-K row in MXFP4: two
+    #      launches), indexer, Top-K, attention over the E4M3/16 cache; one CUDA graph, L2
+    #      flushed between steps; the attention call alone is timed for both formats
+    nv = None
+    if want_nv and graph is not None:
+        nv_c, nv_s = dw["kv_codes_nv"], dw["kv_scales_nv"]
+        aargs_nv = csa2.make_attn_args(dw["q_attn"], nv_c, nv_s, idx, dw["swa"], dw["swa_pos0"],
+                                       dw["q_pos"], None, w.window, dw.sm_scale, w.d_v)
+        ws_attn_nv = torch.empty(max(1, lib.csa2_sparse_attn_workspace_size(ctypes.byref(aargs_nv))),
+                                 dtype=torch.uint8, device=dev)
+        out_nv, lse_nv = torch.empty_like(out), torch.empty_like(lse)
+        nv_row = [(new_kv, nv_c[:, last], nv_s[:, last])]
+        nv_jobs, k_jobs = csa2.quant_jobs(nv_row), csa2.quant_jobs(cache_rows[1:])
+
+        def step_nv():
+            csa2.csa2_quant_fp4_batch(nv_row, st, jobs=nv_jobs, fmt=csa2.FMT_NVFP4_E4M3_16)
+            csa2.csa2_quant_fp4_batch(cache_rows[1:], st, jobs=k_jobs)
+            csa2.csa2_index_score(iargs, scores, row_len, st, workspace=ws_index)
+            csa2.csa2_topk(scores, w.topk, idx, row_len, d_status=st, workspace=ws_topk, group_max=gmax)
+            csa2.csa2_sparse_attn(aargs_nv, out_nv, lse_nv, st, workspace=ws_attn_nv)
+
+        for _ in range(args.warmup):
+            step_nv()
+        g_nv, g_a_nv, g_a_mx = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_nv):
+            step_nv()
+        with torch.cuda.graph(g_a_nv):
+            csa2.csa2_sparse_attn(aargs_nv, out_nv, lse_nv, st, workspace=ws_attn_nv)
+        with torch.cuda.graph(g_a_mx):
+            csa2.csa2_sparse_attn(aargs, out, lse, st, workspace=ws_attn)
+
+        def timed(g):
+            ts = []
+            for it in range(args.steps + 2):
+                flush()
+                e0, e1 = ev(), ev()
+                e0.record(stream)
+                g.replay()
+                e1.record(stream)
+                e1.synchronize()
+                if it >= 2:
+                    ts.append(e0.elapsed_time(e1))
+            return sum(ts) / len(ts)
+
+        t_nv, t_a_nv, t_a_mx = timed(g_nv), timed(g_a_nv), timed(g_a_mx)
+        if int(st.item()) != 0:
+            raise RuntimeError(f"device status {int(st.item())}")
+        row_nv = w.d_qk // 2 + w.d_qk // 16
+        nv = {"format": "E2M1 + E4M3 per 16, no global scale (report §2.4.4)",
+              "ms_per_step": t_nv, "tokens_per_s": B * T / (t_nv * 1e-3), "launches": launches_per_step + 1,
+              "sparse_attn_ms": t_a_nv, "sparse_attn_ms_mxfp4": t_a_mx,
+              "main_kv_bytes_per_position": row_nv,
+              "cache_bytes_per_position": lib.csa2_cache_bytes_per_position(csa2.FMT_NVFP4_E4M3_16, w.d_qk,
+                                                                            w.idx_dim),
+              "cache_bytes_per_position_512ch": lib.csa2_cache_bytes_per_position(csa2.FMT_NVFP4_E4M3_16,
+                                                                                  512, w.idx_dim)}
+
     # ---- max over ranks
     if dist:
         t = torch.tensor([ms_step, ms_k, e2e_step], dtype=torch.float64, device=dev)
@@ -480,6 +539,8 @@ def run_gpu(args):
     }
     if group is not None:
         line["decoder_group"] = group
+    if nv is not None:
+        line["main_kv_e4m3_16"] = nv
     if not args.no_prefill:
         line["prefill_indexer"] = prefill_indexer(dev, line["clocks"].get("sm_mhz"))
     if not args.no_cpu_baseline:
@@ -549,6 +610,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-group", action="store_true")
+    ap.add_argument("--no-nvfp4", action="store_true",
+                    help="skip the step over the E2M1 + E4M3/16 main-KV cache")
     ap.add_argument("--prefill-only", action="store_true",
                     help="time only the prefill indexer (for profiling it) and print its object")
     args = ap.parse_args()

@@ -26,6 +26,7 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_WORKSPACE = 0, 1, 2, 3, 4
 DEV_BAD_INDEX, DEV_BAD_POOL, DEV_NONFINITE, DEV_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 BF16, F32 = 0, 1
 FMT_MXFP4, FMT_NVFP4_E4M3_16 = 0, 1
+FMT_BLOCK = {FMT_MXFP4: 32, FMT_NVFP4_E4M3_16: 16}     # values per scale byte
 INDEX_FULL, INDEX_POOL = 0, 1
 
 _P = ctypes.c_void_p
@@ -46,7 +47,8 @@ class AttnArgs(ctypes.Structure):
     _fields_ = [("batch", _I32), ("n_q", _I32), ("n_heads", _I32), ("d_qk", _I32), ("d_v", _I32),
                 ("topk", _I32), ("window", _I32), ("sm_scale", ctypes.c_float), ("n_kv", _I64),
                 ("q", _P), ("kv_codes", _P), ("kv_scales", _P), ("idx", _P), ("swa", _P),
-                ("n_swa", _I32), ("swa_pos0", _P), ("swa_start", _P), ("q_pos", _P)]
+                ("n_swa", _I32), ("swa_pos0", _P), ("swa_start", _P), ("q_pos", _P),
+                ("kv_fmt", ctypes.c_int)]
 
 
 class Csa2Error(RuntimeError):
@@ -223,8 +225,14 @@ def csa2_dequant_fp4(codes: torch.Tensor, scales: torch.Tensor, y: torch.Tensor,
     rows = codes.numel() // (cols // 2) if cols else 0
     yt = BF16 if y.dtype == torch.bfloat16 else F32
     _check("csa2_dequant_fp4", load().csa2_dequant_fp4(
-        _ptr(codes), cols // 2, _ptr(scales), cols // 32, rows, cols, fmt, _ptr(y), yt, cols,
-        _stream(stream)))
+        _ptr(codes), cols // 2, _ptr(scales), cols // FMT_BLOCK[fmt], rows, cols, fmt, _ptr(y), yt,
+        cols, _stream(stream)))
+
+
+def scales_format(cols: int, scales: torch.Tensor) -> int:
+    """Format of rows of `cols` values whose scales tensor is `scales` (one scale per 16
+    values: E2M1 + E4M3/16, per 32: MXFP4)."""
+    return FMT_NVFP4_E4M3_16 if scales.shape[-1] * 16 == cols else FMT_MXFP4
 
 
 def make_index_args(q, w, k_codes, k_scales, q_pos=None, ratio_m=1, pool_blocks=None, block=8,
@@ -290,8 +298,10 @@ def csa2_block_candidates(scores: torch.Tensor, nb: int, block_ids: torch.Tensor
 
 def make_attn_args(q, kv_codes, kv_scales, idx, swa=None, swa_pos0=None, q_pos=None,
                    swa_start=None, window=128, sm_scale=None, d_v=None):
+    """csa2_attn_args; the main-KV format follows from the width of kv_scales."""
     B, T, H, dqk = q.shape
     a = AttnArgs()
+    a.kv_fmt = scales_format(dqk, kv_scales)
     a.batch, a.n_q, a.n_heads, a.d_qk = B, T, H, dqk
     a.d_v = d_v if d_v is not None else dqk
     a.topk = idx.shape[-1] if idx is not None else 0
@@ -316,18 +326,21 @@ def csa2_sparse_attn(args: AttnArgs, out: torch.Tensor, lse=None, d_status=None,
 
 
 # ------------------------------------------------------------------ allocating helpers
-def quant_fp4(x: torch.Tensor, d_status=None, stream=None):
-    """x [..., D] bf16/f32 -> (codes uint8 [..., D/2], scales uint8 [..., D/32])."""
+def quant_fp4(x: torch.Tensor, d_status=None, stream=None, fmt: int = FMT_MXFP4):
+    """x [..., D] bf16/f32 -> (codes uint8 [..., D/2], scales uint8 [..., D/G]), G = 32
+    (MXFP4) or 16 (E2M1 + E4M3/16)."""
     D = x.shape[-1]
     codes = torch.empty(x.shape[:-1] + (D // 2,), dtype=torch.uint8, device=x.device)
-    scales = torch.empty(x.shape[:-1] + (D // 32,), dtype=torch.uint8, device=x.device)
-    csa2_quant_fp4(x, codes, scales, d_status, stream)
+    scales = torch.empty(x.shape[:-1] + (D // FMT_BLOCK[fmt],), dtype=torch.uint8, device=x.device)
+    csa2_quant_fp4(x, codes, scales, d_status, stream, fmt=fmt)
     return codes, scales
 
 
 def dequant_fp4(codes, scales, dtype=torch.float32, stream=None):
-    y = torch.empty(codes.shape[:-1] + (codes.shape[-1] * 2,), dtype=dtype, device=codes.device)
-    csa2_dequant_fp4(codes, scales, y, stream)
+    """Dequantise MXFP4 or E2M1 + E4M3/16 rows (told apart by the width of scales)."""
+    cols = codes.shape[-1] * 2
+    y = torch.empty(codes.shape[:-1] + (cols,), dtype=dtype, device=codes.device)
+    csa2_dequant_fp4(codes, scales, y, stream, fmt=scales_format(cols, scales))
     return y
 
 

@@ -18,6 +18,12 @@ inline csa2_status from_cuda(cudaError_t e) { return e == cudaSuccess ? CSA2_OK 
 
 inline cudaStream_t as_stream(csa2_stream s) { return reinterpret_cast<cudaStream_t>(s); }
 
+// values per scale of a 4-bit format (0: not a format)
+inline int fmt_block(csa2_fp4_format f)
+{
+    return f == CSA2_FMT_MXFP4 ? 32 : f == CSA2_FMT_NVFP4_E4M3_16 ? 16 : 0;
+}
+
 bool index_args_ok(const csa2_index_args *a)
 {
     if (!a) return false;
@@ -53,6 +59,7 @@ bool attn_args_ok(const csa2_attn_args *a)
     if (a->d_qk < 32 || a->d_qk > 1024 || a->d_qk % 32) return false;
     if (a->d_v < 8 || a->d_v > a->d_qk || a->d_v % 8) return false;
     if (a->topk < 0 || a->topk > 2048 || a->window < 0) return false;
+    if (a->kv_fmt != CSA2_FMT_MXFP4 && a->kv_fmt != CSA2_FMT_NVFP4_E4M3_16) return false;
     const bool empty = (int64_t)a->batch * a->n_q == 0;
     if (empty) return true;
     if (!a->q) return false;
@@ -101,12 +108,15 @@ csa2_status csa2_quant_fp4(const void *x, csa2_dtype xt, int64_t rows, int64_t c
                            uint8_t *codes, int64_t ldc, uint8_t *scales, int64_t lds,
                            csa2_fp4_format fmt, uint32_t *d_status, csa2_stream stream)
 {
-    if (fmt == CSA2_FMT_NVFP4_E4M3_16) return CSA2_ERR_UNSUPPORTED;
-    if (fmt != CSA2_FMT_MXFP4 || (xt != CSA2_BF16 && xt != CSA2_F32)) return CSA2_ERR_INVALID_ARG;
-    if (rows < 0 || cols < 0 || cols % 32) return CSA2_ERR_INVALID_ARG;
+    const int G = fmt_block(fmt);
+    if (!G || (xt != CSA2_BF16 && xt != CSA2_F32)) return CSA2_ERR_INVALID_ARG;
+    if (rows < 0 || cols < 0 || cols % G) return CSA2_ERR_INVALID_ARG;
     if (rows == 0 || cols == 0) return CSA2_OK;
     if (!x || !codes || !scales) return CSA2_ERR_INVALID_ARG;
-    if (ldx < cols || ldc < cols / 2 || lds < cols / 32) return CSA2_ERR_INVALID_ARG;
+    if (ldx < cols || ldc < cols / 2 || lds < cols / G) return CSA2_ERR_INVALID_ARG;
+    if (fmt == CSA2_FMT_NVFP4_E4M3_16)
+        return from_cuda(launch_quant_nvfp4(x, xt == CSA2_BF16, rows, cols, ldx, codes, ldc, scales,
+                                            lds, d_status, as_stream(stream)));
     return from_cuda(launch_quant_mxfp4(x, xt == CSA2_BF16, rows, cols, ldx, codes, ldc, scales,
                                         lds, d_status, as_stream(stream)));
 }
@@ -114,27 +124,31 @@ csa2_status csa2_quant_fp4(const void *x, csa2_dtype xt, int64_t rows, int64_t c
 csa2_status csa2_quant_fp4_batch(const csa2_quant_job *jobs, int32_t n_jobs, csa2_fp4_format fmt,
                                  uint32_t *d_status, csa2_stream stream)
 {
-    if (fmt == CSA2_FMT_NVFP4_E4M3_16) return CSA2_ERR_UNSUPPORTED;
-    if (fmt != CSA2_FMT_MXFP4 || n_jobs < 0 || n_jobs > CSA2_QUANT_MAX_JOBS) return CSA2_ERR_INVALID_ARG;
+    const int G = fmt_block(fmt);
+    if (!G || n_jobs < 0 || n_jobs > CSA2_QUANT_MAX_JOBS) return CSA2_ERR_INVALID_ARG;
     if (n_jobs == 0) return CSA2_OK;
     if (!jobs) return CSA2_ERR_INVALID_ARG;
     QuantJobDesc d[CSA2_QUANT_MAX_JOBS];
-    bool vec = true;
+    bool vec = fmt == CSA2_FMT_MXFP4;
     for (int k = 0; k < n_jobs; ++k) {
         const csa2_quant_job &j = jobs[k];
         if (j.xt != CSA2_BF16 && j.xt != CSA2_F32) return CSA2_ERR_INVALID_ARG;
-        if (j.rows < 0 || j.cols < 0 || j.cols % 32) return CSA2_ERR_INVALID_ARG;
+        if (j.rows < 0 || j.cols < 0 || j.cols % G) return CSA2_ERR_INVALID_ARG;
         if (j.rows && j.cols) {
             if (!j.x || !j.codes || !j.scales) return CSA2_ERR_INVALID_ARG;
-            if (j.ldx < j.cols || j.ldc < j.cols / 2 || j.lds < j.cols / 32) return CSA2_ERR_INVALID_ARG;
+            if (j.ldx < j.cols || j.ldc < j.cols / 2 || j.lds < j.cols / G) return CSA2_ERR_INVALID_ARG;
         }
         d[k] = {j.x, j.xt == CSA2_BF16, j.rows, j.cols, j.ldx, j.codes, j.ldc, j.scales, j.lds};
         vec = vec && quant_job_vec_ok(d[k]);
     }
     if (vec) return from_cuda(launch_quant_mxfp4_batch(d, n_jobs, d_status, as_stream(stream)));
-    for (int k = 0; k < n_jobs; ++k) {           // some rows misaligned: one launch per job
-        const cudaError_t e = launch_quant_mxfp4(d[k].x, d[k].x_bf16, d[k].rows, d[k].cols, d[k].ldx, d[k].codes,
-                                                 d[k].ldc, d[k].scales, d[k].lds, d_status, as_stream(stream));
+    for (int k = 0; k < n_jobs; ++k) {           // NVFP4 or misaligned rows: one launch per job
+        const cudaError_t e =
+            fmt == CSA2_FMT_NVFP4_E4M3_16
+                ? launch_quant_nvfp4(d[k].x, d[k].x_bf16, d[k].rows, d[k].cols, d[k].ldx, d[k].codes, d[k].ldc,
+                                     d[k].scales, d[k].lds, d_status, as_stream(stream))
+                : launch_quant_mxfp4(d[k].x, d[k].x_bf16, d[k].rows, d[k].cols, d[k].ldx, d[k].codes, d[k].ldc,
+                                     d[k].scales, d[k].lds, d_status, as_stream(stream));
         if (e != cudaSuccess) return from_cuda(e);
     }
     return CSA2_OK;
@@ -144,14 +158,14 @@ csa2_status csa2_dequant_fp4(const uint8_t *codes, int64_t ldc, const uint8_t *s
                              int64_t lds, int64_t rows, int64_t cols, csa2_fp4_format fmt,
                              void *y, csa2_dtype yt, int64_t ldy, csa2_stream stream)
 {
-    if (fmt == CSA2_FMT_NVFP4_E4M3_16) return CSA2_ERR_UNSUPPORTED;
-    if (fmt != CSA2_FMT_MXFP4 || (yt != CSA2_BF16 && yt != CSA2_F32)) return CSA2_ERR_INVALID_ARG;
-    if (rows < 0 || cols < 0 || cols % 32) return CSA2_ERR_INVALID_ARG;
+    const int G = fmt_block(fmt);
+    if (!G || (yt != CSA2_BF16 && yt != CSA2_F32)) return CSA2_ERR_INVALID_ARG;
+    if (rows < 0 || cols < 0 || cols % G) return CSA2_ERR_INVALID_ARG;
     if (rows == 0 || cols == 0) return CSA2_OK;
     if (!y || !codes || !scales) return CSA2_ERR_INVALID_ARG;
-    if (ldy < cols || ldc < cols / 2 || lds < cols / 32) return CSA2_ERR_INVALID_ARG;
-    return from_cuda(launch_dequant_mxfp4(codes, ldc, scales, lds, rows, cols, y, yt == CSA2_BF16,
-                                          ldy, as_stream(stream)));
+    if (ldy < cols || ldc < cols / 2 || lds < cols / G) return CSA2_ERR_INVALID_ARG;
+    return from_cuda(launch_dequant_fp4(codes, ldc, scales, lds, rows, cols, fmt == CSA2_FMT_NVFP4_E4M3_16, y,
+                                        yt == CSA2_BF16, ldy, as_stream(stream)));
 }
 
 size_t csa2_index_score_workspace_size(const csa2_index_args *a)

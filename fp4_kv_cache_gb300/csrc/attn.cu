@@ -7,7 +7,8 @@
 // main KV is a latent shared by every query head, so V is its leading d_v dims.
 //
 // One CTA = one query row x 8 heads.  Keys stream through shared memory in tiles of 32
-// (gathered FP4 rows dequantised exactly to float, then the SWA slots), with an online
+// (gathered FP4 rows -- MXFP4 or E2M1 + E4M3/16 -- dequantised exactly to float, then the
+// SWA slots), with an online
 // softmax per head and fp32 accumulation.
 #include "common.cuh"
 #include "internal.h"
@@ -22,6 +23,7 @@ constexpr int kKT = 32;   // keys per tile (one lane each for the logits)
 
 struct AttnParams {
     int32_t T, H, d_qk, d_v, topk, window, n_swa;
+    int32_t nv;              // main KV: 0 = MXFP4 (E8M0 / 32), 1 = E2M1 + E4M3 / 16
     float sm_scale;
     int64_t n_kv;
     const uint16_t *q;
@@ -118,7 +120,8 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_cc_kernel(AttnParams P)
                 const int64_t r = b * P.n_kv + src;
                 const uint32_t byte = P.kvc[r * (P.d_qk / 2) + c / 2];
                 const uint32_t code = (c & 1) ? (byte >> 4) : (byte & 15u);
-                v = e2m1_mag(code & 7u) * e8m0_value(P.kvs[r * (P.d_qk / 32) + c / 32]);
+                v = e2m1_mag(code & 7u) * (P.nv ? e4m3_value(P.kvs[r * (P.d_qk / 16) + c / 16])
+                                                : e8m0_value(P.kvs[r * (P.d_qk / 32) + c / 32]));
                 if (code & 8u) v = -v;
             } else if (src <= -2) {
                 const int64_t slot = -src - 2;
@@ -225,6 +228,7 @@ cudaError_t launch_sparse_attn(const csa2_attn_args &a, uint16_t *out, float *ls
     P.topk = a.topk;
     P.window = a.window;
     P.n_swa = a.swa ? a.n_swa : 0;
+    P.nv = a.kv_fmt == CSA2_FMT_NVFP4_E4M3_16 ? 1 : 0;
     P.sm_scale = a.sm_scale;
     P.n_kv = a.n_kv;
     P.q = a.q;

@@ -174,6 +174,9 @@ __device__ __forceinline__ float warp_halving_reduce32(float (&v)[32], int lane)
     return v[0];
 }
 
+// NV: the main KV holds E2M1 codes with one E4M3 scale per 16 values (report §2.4.4)
+// instead of one E8M0 scale per 32; only the gather and the dequantisation differ.
+template <bool NV>
 __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnTcParams P)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -263,15 +266,22 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
     // Registers carry the next tile's FP4 half-row while the current tile computes; SWA rows
     // (bf16, 4x the bytes) are pulled into L2 a tile ahead and copied with cp.async.
     uint4 raw[9];
-    uint32_t sb[9];
+    uint32_t sb[9];          // scale byte(s) of each 32 codes: one E8M0, or two E4M3 (NV)
     auto issue = [&](int64_t src) {
         if (src >= 0) {
             const uint8_t *codes = P.kvc + (b * P.n_kv + src) * (kDqk / 2) + part * 9 * 16;
-            const uint8_t *scl = P.kvs + (b * P.n_kv + src) * (kDqk / 32) + part * 9;
 #pragma unroll
             for (int i = 0; i < 9; ++i) raw[i] = *reinterpret_cast<const uint4 *>(codes + i * 16);
+            if constexpr (NV) {
+                const uint16_t *scl = reinterpret_cast<const uint16_t *>(P.kvs + (b * P.n_kv + src) * (kDqk / 16) +
+                                                                         part * 18);
 #pragma unroll
-            for (int i = 0; i < 9; ++i) sb[i] = scl[i];
+                for (int i = 0; i < 9; ++i) sb[i] = scl[i];
+            } else {
+                const uint8_t *scl = P.kvs + (b * P.n_kv + src) * (kDqk / 32) + part * 9;
+#pragma unroll
+                for (int i = 0; i < 9; ++i) sb[i] = scl[i];
+            }
         } else if (src <= -2) {
             const char *srow = reinterpret_cast<const char *>(P.swa + (b * P.n_swa + (-src - 2)) * (int64_t)kDqk);
 #pragma unroll
@@ -290,7 +300,29 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
         {
             const int r = key_row;
             const int64_t src = src_cur;
-            if (src >= 0) {
+            if (NV && src >= 0) {
+                // code value x E4M3 scale in bf16: exact (at most 6 significant bits, every
+                // product in [2^-10, 2688])
+#pragma unroll
+                for (int i = 0; i < 9; ++i) {
+                    const int blk = part * 9 + i;                 // 32-value block of the row
+                    const uint32_t w4[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+                    const int c = blk >> 1;
+                    uint8_t *base = sm + (c < 8 ? kOffK + c * kChunkBytes : kOffR);
+                    const unsigned short s_lo = (unsigned short)(__float_as_uint(e4m3_value(sb[i] & 0xffu)) >> 16);
+                    const unsigned short s_hi = (unsigned short)(__float_as_uint(e4m3_value(sb[i] >> 8)) >> 16);
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {             // 8 values -> one 16-byte piece
+                        const unsigned short sbits = q4 < 2 ? s_lo : s_hi;
+                        const __nv_bfloat162 sc2 =
+                            __halves2bfloat162(__ushort_as_bfloat16(sbits), __ushort_as_bfloat16(sbits));
+                        uint32_t packed[4];
+                        e2m1x8_to_bf16(w4[q4], sc2, packed);
+                        *reinterpret_cast<uint4 *>(base + sw128(r, (blk & 1) * 4 + q4)) =
+                            make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                    }
+                }
+            } else if (src >= 0) {
                 bool fast = true;
 #pragma unroll
                 for (int i = 0; i < 9; ++i) fast = fast && sb[i] >= 8u && sb[i] <= 250u;
@@ -625,7 +657,8 @@ void attn_tc_split(const csa2_attn_args &a, int &splits, int &tiles_per_split)
 bool attn_tc_eligible(const csa2_attn_args &a)
 {
     return a.d_qk == kDqk && a.d_v == kDv && a.n_heads <= kH && ((uintptr_t)a.q & 15) == 0 &&
-           (!a.swa || ((uintptr_t)a.swa & 15) == 0) && ((uintptr_t)a.kv_codes & 15) == 0;
+           (!a.swa || ((uintptr_t)a.swa & 15) == 0) && ((uintptr_t)a.kv_codes & 15) == 0 &&
+           (a.kv_fmt != CSA2_FMT_NVFP4_E4M3_16 || ((uintptr_t)a.kv_scales & 1) == 0);
 }
 
 size_t attn_tc_ws_bytes(const csa2_attn_args &a)
@@ -662,10 +695,12 @@ cudaError_t launch_attn_tc(const csa2_attn_args &a, uint16_t *out, float *lse, v
     P.part_o = static_cast<float *>(ws);
     const int64_t rows = (int64_t)a.batch * a.n_q;
     const int smem = kSmemBytes + 1024;
-    cudaError_t e = cudaFuncSetAttribute(sparse_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    const bool nv = a.kv_fmt == CSA2_FMT_NVFP4_E4M3_16;
+    void (*kern)(AttnTcParams) = nv ? sparse_attn_tc_kernel<true> : sparse_attn_tc_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     // a row's CTAs form one cluster
-    return launch_pdl(sparse_attn_tc_kernel, dim3((unsigned)P.splits, (unsigned)rows), dim3(kThreads),
+    return launch_pdl(kern, dim3((unsigned)P.splits, (unsigned)rows), dim3(kThreads),
                       (size_t)smem, s, (unsigned)P.splits, P);
 }
 

@@ -88,6 +88,30 @@ __device__ __forceinline__ float e8m0_value(uint32_t sb)
     return sb == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(sb << 23);
 }
 
+// ------------------------------------------------------------------ E4M3 block scales
+// (report §2.4.4: the main KV keeps E2M1 values with one E4M3 scale per 16.)
+// Value of an E4M3 byte: sign, 4 exponent bits (bias 7), 3 mantissa bits; exponent field
+// 0 is subnormal (m x 2^-9); 0x7F / 0xFF are NaN.
+__device__ __forceinline__ float e4m3_value(uint32_t byte)
+{
+    const uint32_t e = (byte >> 3) & 15u, m = byte & 7u;
+    float mag = e == 0 ? (float)m * 0.001953125f : __uint_as_float(((e + 120u) << 23) | (m << 20));
+    if ((byte & 0x7fu) == 0x7fu) mag = __uint_as_float(0x7fc00000u);
+    return (byte & 0x80u) ? -mag : mag;
+}
+
+// Scale byte of a 16-value block with maximum magnitude amax (finite, >= 0): amax / 6
+// rounded to the nearest E4M3 value, ties to even, clamped to 448.  The float32 quotient
+// rounds onto an E4M3 midpoint only when the exact quotient is that midpoint (the
+// midpoints have 5 significant bits), so the two roundings give the exact one.
+__device__ __forceinline__ uint32_t e4m3_block_scale(float amax)
+{
+    const float t = __fdiv_rn(amax, 6.0f);
+    uint16_t d;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %1;" : "=h"(d) : "f"(t));
+    return (uint32_t)(d & 0xffu);
+}
+
 // Twice the signed E2M1 value of a code, an integer in [-12, 12].
 __device__ __forceinline__ int e2m1_twice(uint32_t c)
 {

@@ -23,9 +23,12 @@ struct QuantJobDesc {
 };
 bool quant_job_vec_ok(const QuantJobDesc &j);
 cudaError_t launch_quant_mxfp4_batch(const QuantJobDesc *jobs, int n_jobs, uint32_t *d_status, cudaStream_t s);
-cudaError_t launch_dequant_mxfp4(const uint8_t *codes, int64_t ldc, const uint8_t *scales,
-                                 int64_t lds, int64_t rows, int64_t cols, void *y, bool y_bf16,
-                                 int64_t ldy, cudaStream_t s);
+cudaError_t launch_quant_nvfp4(const void *x, bool x_bf16, int64_t rows, int64_t cols, int64_t ldx,
+                               uint8_t *codes, int64_t ldc, uint8_t *scales, int64_t lds,
+                               uint32_t *d_status, cudaStream_t s);
+cudaError_t launch_dequant_fp4(const uint8_t *codes, int64_t ldc, const uint8_t *scales,
+                               int64_t lds, int64_t rows, int64_t cols, bool nvfp4, void *y,
+                               bool y_bf16, int64_t ldy, cudaStream_t s);
 
 // Indexer scoring: tensor-core path where it applies (index_tc.cu; it re-scores the rare
 // positions it cannot prove exact on CUDA cores), else the exact CUDA-core kernel

@@ -1,10 +1,11 @@
-// quant.cu -- MXFP4 cache codec kernels (csa2_quant_fp4 / csa2_dequant_fp4).
+// quant.cu -- 4-bit cache codec kernels (csa2_quant_fp4 / csa2_dequant_fp4).
 //
 // DeepSeek-V4.1-Flash report (aipaper.jasonlin.tech) §2.4.4: indexer queries and keys use
-// OCP MXFP4 -- E2M1 values with one power-of-two (E8M0) scale per 32 -- and cached values
-// are dequantised before attention.  One warp quantises one 32-value block per step:
-// lane i holds element i, the block maximum is a warp max over the magnitude bits, and
-// lane pairs merge their nibbles (element 2i in the low nibble).
+// OCP MXFP4 -- E2M1 values with one power-of-two (E8M0) scale per 32 -- the main KV keeps
+// E2M1 values with one E4M3 scale per 16, and cached values are dequantised before
+// attention.  MXFP4 scalar kernel: one warp quantises one 32-value block per step: lane i
+// holds element i, the block maximum is a warp max over the magnitude bits, and lane
+// pairs merge their nibbles (element 2i in the low nibble).
 #include "common.cuh"
 #include "internal.h"
 #include <cuda_bf16.h>
@@ -174,12 +175,125 @@ __global__ void __launch_bounds__(256) quant_mxfp4_batch_kernel(const __grid_con
     }
 }
 
+// ---------------------------------------------------------------- E2M1 + E4M3 per 16
+// The report's main-KV format (§2.4.4): one E4M3 scale per 16 values, no global scale.
+// Scale = amax/6 rounded to E4M3 (e4m3_block_scale); element code = the E2M1 rounding of
+// x / scale.  The float32 quotient x / scale rounds onto an E2M1 midpoint only when the
+// exact quotient is that midpoint (x has <= 24 significant bits, scale x midpoint <= 7),
+// so the hardware conversion of the quotient gives the exact rounding.  A zero scale
+// leaves only the sign bits.
+
+// Two lanes share a 16-value block; each converts 8 values (one 16-byte bf16 load or two
+// 16-byte f32 loads) and stores their 8 nibbles as one 32-bit word.  Needs 16-byte aligned
+// rows of x and 4-byte aligned rows of codes.
 template <bool BF16>
-__global__ void __launch_bounds__(256) dequant_mxfp4_kernel(const uint8_t *__restrict__ codes,
-                                                            int64_t ldc,
-                                                            const uint8_t *__restrict__ scales,
-                                                            int64_t lds, int64_t rows, int64_t cols,
-                                                            void *__restrict__ y, int64_t ldy)
+__global__ void __launch_bounds__(256) quant_nvfp4_vec_kernel(const void *__restrict__ x, int64_t rows,
+                                                              int64_t cols, int64_t ldx,
+                                                              uint8_t *__restrict__ codes, int64_t ldc,
+                                                              uint8_t *__restrict__ scales, int64_t lds,
+                                                              uint32_t *d_status)
+{
+    pdl_wait();                                   // x may come from the kernel before
+    pdl_allow_dependents();
+    const int64_t nblk_row = cols / 16;
+    const int64_t total = rows * nblk_row * 2;                 // lanes of work
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t total32 = (total + 31) & ~int64_t(31);
+    for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total32; t += stride) {
+        const bool act = t < total;
+        const int64_t grp = t >> 1;
+        const int sub = (int)(t & 1);
+        const int64_t r = act ? grp / nblk_row : 0, kb = act ? grp % nblk_row : 0;
+        float v[8];
+        if (act) {
+            if (BF16) {
+                const uint4 raw = *reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(x) +
+                                                                   r * ldx + kb * 16 + sub * 8);
+                const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    v[2 * i] = __uint_as_float(w[i] << 16);
+                    v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+                }
+            } else {
+                const float4 *src = reinterpret_cast<const float4 *>(static_cast<const float *>(x) +
+                                                                     r * ldx + kb * 16 + sub * 8);
+                const float4 a = src[0], b = src[1];
+                v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+                v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = 0.0f;
+        }
+        uint32_t amax = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) amax = max(amax, __float_as_uint(v[i]) & 0x7fffffffu);
+        amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        if (!act) continue;
+        const bool finite = amax < 0x7f800000u;
+        if (!finite && sub == 0) dev_flag(d_status, CSA2_DEV_NONFINITE);
+        const uint32_t sb = e4m3_block_scale(__uint_as_float(finite ? amax : 0u));
+        const float sc = e4m3_value(sb);
+        uint32_t word = 0;
+        if (sc > 0.0f) {
+#pragma unroll
+            for (int i = 0; i < 8; i += 2)
+                word |= e2m1x2_cvt(__fdiv_rn(v[i], sc), __fdiv_rn(v[i + 1], sc)) << (4 * i);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) word |= (__float_as_uint(v[i]) >> 31) << (4 * i + 3);
+        }
+        *reinterpret_cast<uint32_t *>(codes + r * ldc + kb * 8 + sub * 4) = word;
+        if (sub == 0) scales[r * lds + kb] = (uint8_t)sb;
+    }
+}
+
+// Rows without the vector kernel's alignment: one warp takes two 16-value blocks per step
+// (lane = element), block maximum by shuffles within each half-warp.
+template <bool BF16>
+__global__ void __launch_bounds__(256) quant_nvfp4_kernel(const void *__restrict__ x, int64_t rows,
+                                                          int64_t cols, int64_t ldx,
+                                                          uint8_t *__restrict__ codes, int64_t ldc,
+                                                          uint8_t *__restrict__ scales, int64_t lds,
+                                                          uint32_t *d_status)
+{
+    const int lane = threadIdx.x & 31, e16 = lane & 15;
+    const int64_t nblk_row = cols / 16;
+    const int64_t total = rows * nblk_row;
+    const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t pair = warp0; pair * 2 < total; pair += nwarps) {
+        const int64_t blk = pair * 2 + (lane >> 4);
+        const bool act = blk < total;
+        const int64_t r = act ? blk / nblk_row : 0, kb = act ? blk % nblk_row : 0;
+        const int64_t col = kb * 16 + e16;
+        float v = 0.0f;
+        if (act) {
+            if (BF16) v = __uint_as_float((uint32_t)static_cast<const uint16_t *>(x)[r * ldx + col] << 16);
+            else v = static_cast<const float *>(x)[r * ldx + col];
+        }
+        uint32_t amax = __float_as_uint(v) & 0x7fffffffu;
+#pragma unroll
+        for (int o = 1; o < 16; o <<= 1) amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        const bool finite = amax < 0x7f800000u;
+        if (act && !finite && e16 == 0) dev_flag(d_status, CSA2_DEV_NONFINITE);
+        const uint32_t sb = e4m3_block_scale(__uint_as_float(finite ? amax : 0u));
+        const float sc = e4m3_value(sb);
+        const uint32_t c = sc > 0.0f ? (e2m1x2_cvt(__fdiv_rn(v, sc), 0.0f) & 15u)
+                                     : ((__float_as_uint(v) >> 28) & 8u);
+        const uint32_t c_hi = __shfl_down_sync(0xffffffffu, c, 1);
+        if (act && (lane & 1) == 0) codes[r * ldc + kb * 8 + (e16 >> 1)] = (uint8_t)(c | (c_hi << 4));
+        if (act && e16 == 0) scales[r * lds + kb] = (uint8_t)sb;
+    }
+}
+
+template <bool BF16, bool NV>
+__global__ void __launch_bounds__(256) dequant_fp4_kernel(const uint8_t *__restrict__ codes,
+                                                          int64_t ldc,
+                                                          const uint8_t *__restrict__ scales,
+                                                          int64_t lds, int64_t rows, int64_t cols,
+                                                          void *__restrict__ y, int64_t ldy)
 {
     const int64_t total = rows * cols;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
@@ -187,7 +301,8 @@ __global__ void __launch_bounds__(256) dequant_mxfp4_kernel(const uint8_t *__res
         const int64_t r = i / cols, c = i % cols;
         const uint32_t byte = codes[r * ldc + c / 2];
         const uint32_t code = (c & 1) ? (byte >> 4) : (byte & 15u);
-        float v = e2m1_mag(code & 7u) * e8m0_value(scales[r * lds + c / 32]);
+        float v = e2m1_mag(code & 7u) * (NV ? e4m3_value(scales[r * lds + c / 16])
+                                            : e8m0_value(scales[r * lds + c / 32]));
         if (code & 8u) v = -v;
         if (BF16)
             static_cast<uint16_t *>(y)[r * ldy + c] = (uint16_t)(__float_as_uint(v) >> 16);
@@ -267,16 +382,47 @@ cudaError_t launch_quant_mxfp4_batch(const QuantJobDesc *jobs, int n_jobs, uint3
     return launch_pdl(quant_mxfp4_batch_kernel, dim3(grid_for(acc, 256)), dim3(256), 0, s, 1, B, d_status);
 }
 
-cudaError_t launch_dequant_mxfp4(const uint8_t *codes, int64_t ldc, const uint8_t *scales,
-                                 int64_t lds, int64_t rows, int64_t cols, void *y, bool y_bf16,
-                                 int64_t ldy, cudaStream_t s)
+cudaError_t launch_quant_nvfp4(const void *x, bool x_bf16, int64_t rows, int64_t cols, int64_t ldx,
+                               uint8_t *codes, int64_t ldc, uint8_t *scales, int64_t lds,
+                               uint32_t *d_status, cudaStream_t s)
+{
+    if (rows == 0 || cols == 0) return cudaSuccess;
+    const size_t esz = x_bf16 ? 2 : 4;
+    const bool vec = ((uintptr_t)x % 16 == 0) && ((ldx * (int64_t)esz) % 16 == 0) &&
+                     ((uintptr_t)codes % 4 == 0) && (ldc % 4 == 0);
+    if (vec) {
+        const int grid = grid_for(rows * (cols / 16) * 2, 256);
+        if (x_bf16)
+            return launch_pdl(quant_nvfp4_vec_kernel<true>, dim3(grid), dim3(256), 0, s, 1, x, rows, cols, ldx,
+                              codes, ldc, scales, lds, d_status);
+        return launch_pdl(quant_nvfp4_vec_kernel<false>, dim3(grid), dim3(256), 0, s, 1, x, rows, cols, ldx,
+                          codes, ldc, scales, lds, d_status);
+    }
+    const int grid = grid_for(rows * (cols / 16), 16);
+    if (x_bf16)
+        quant_nvfp4_kernel<true><<<grid, 256, 0, s>>>(x, rows, cols, ldx, codes, ldc, scales, lds, d_status);
+    else
+        quant_nvfp4_kernel<false><<<grid, 256, 0, s>>>(x, rows, cols, ldx, codes, ldc, scales, lds, d_status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dequant_fp4(const uint8_t *codes, int64_t ldc, const uint8_t *scales,
+                               int64_t lds, int64_t rows, int64_t cols, bool nvfp4, void *y,
+                               bool y_bf16, int64_t ldy, cudaStream_t s)
 {
     if (rows == 0 || cols == 0) return cudaSuccess;
     const int grid = grid_for(rows * cols, 256);
-    if (y_bf16)
-        dequant_mxfp4_kernel<true><<<grid, 256, 0, s>>>(codes, ldc, scales, lds, rows, cols, y, ldy);
-    else
-        dequant_mxfp4_kernel<false><<<grid, 256, 0, s>>>(codes, ldc, scales, lds, rows, cols, y, ldy);
+    if (nvfp4) {
+        if (y_bf16)
+            dequant_fp4_kernel<true, true><<<grid, 256, 0, s>>>(codes, ldc, scales, lds, rows, cols, y, ldy);
+        else
+            dequant_fp4_kernel<false, true><<<grid, 256, 0, s>>>(codes, ldc, scales, lds, rows, cols, y, ldy);
+    } else {
+        if (y_bf16)
+            dequant_fp4_kernel<true, false><<<grid, 256, 0, s>>>(codes, ldc, scales, lds, rows, cols, y, ldy);
+        else
+            dequant_fp4_kernel<false, false><<<grid, 256, 0, s>>>(codes, ldc, scales, lds, rows, cols, y, ldy);
+    }
     return cudaGetLastError();
 }
 

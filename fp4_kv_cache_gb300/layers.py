@@ -24,7 +24,7 @@ from . import csa2
 class Cache:
     """One source layer's shared global cache (main KV + indexer K), MXFP4 planes."""
     kv_codes: torch.Tensor      # uint8 [B, N, d_qk/2]
-    kv_scales: torch.Tensor     # uint8 [B, N, d_qk/32]
+    kv_scales: torch.Tensor     # uint8 [B, N, d_qk/32] (MXFP4) or [B, N, d_qk/16] (E2M1 + E4M3/16)
     k_codes: torch.Tensor       # uint8 [B, N, d_i/2]
     k_scales: torch.Tensor      # uint8 [B, N, d_i/32]
     ratio_m: int = 1

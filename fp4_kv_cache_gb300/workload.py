@@ -32,7 +32,11 @@ class DeviceWorkload:
 
 
 def build(w: synth.Workload, rows=None, device="cuda:0", kv: bool = True, kidx: bool = True,
-          d_status: Optional[torch.Tensor] = None) -> DeviceWorkload:
+          d_status: Optional[torch.Tensor] = None, kv_fmt: int = csa2.FMT_MXFP4,
+          also_nvfp4: bool = False) -> DeviceWorkload:
+    """kv_fmt: main-KV cache format (MXFP4, or E2M1 + E4M3/16 as the report stores it);
+    the indexer keys are MXFP4 either way.  also_nvfp4: quantise the same main-KV rows a
+    second time into E2M1 + E4M3/16 ("kv_codes_nv", "kv_scales_nv")."""
     rows = list(range(w.batch)) if rows is None else list(rows)
     B = len(rows)
     dev = torch.device(device)
@@ -55,11 +59,17 @@ def build(w: synth.Workload, rows=None, device="cuda:0", kv: bool = True, kidx: 
         out.t["k_codes"], out.t["k_scales"] = kc, ks
     if kv:
         vc = torch.empty((B, N, w.d_qk // 2), dtype=torch.uint8, device=dev)
-        vs = torch.empty((B, N, w.d_qk // 32), dtype=torch.uint8, device=dev)
+        vs = torch.empty((B, N, w.d_qk // csa2.FMT_BLOCK[kv_fmt]), dtype=torch.uint8, device=dev)
         swa = torch.empty((B, n_slots, w.d_qk), dtype=torch.bfloat16, device=dev)
+        if also_nvfp4:
+            nvc = torch.empty((B, N, w.d_qk // 2), dtype=torch.uint8, device=dev)
+            nvs = torch.empty((B, N, w.d_qk // 16), dtype=torch.uint8, device=dev)
+            out.t["kv_codes_nv"], out.t["kv_scales_nv"] = nvc, nvs
         for i, b in enumerate(rows):
             x = bf16_tensor(synth.gen_main_kv(w, b), dev)
-            csa2.csa2_quant_fp4(x, vc[i], vs[i], d_status)
+            csa2.csa2_quant_fp4(x, vc[i], vs[i], d_status, fmt=kv_fmt)
+            if also_nvfp4:
+                csa2.csa2_quant_fp4(x, nvc[i], nvs[i], d_status, fmt=csa2.FMT_NVFP4_E4M3_16)
             del x
             swa[i] = bf16_tensor(synth.gen_swa(w, b), dev)
         out.t["kv_codes"], out.t["kv_scales"], out.t["swa"] = vc, vs, swa

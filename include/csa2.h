@@ -81,7 +81,16 @@ typedef enum { CSA2_BF16 = 0, CSA2_F32 = 1 } csa2_dtype;
  *   [-127, 127] (X = 0 for an all-zero block), element code = round-half-even of
  *   |x|/2^X onto {0, .5, 1, 1.5, 2, 3, 4, 6}, saturating at 6, sign bit = sign bit of x.
  * NVFP4_E4M3_16: E2M1 + one E4M3 scale per 16, no global scale -- the report's main-KV
- *   format (report §2.4.4).  Only its byte ledger is implemented in this build. */
+ *   format (report §2.4.4; the review's byte ledger counts 256 B of codes and 32 B of
+ *   scales for 512 channels).  Codes are packed as for MXFP4; scale byte = an E4M3 value
+ *   (1 sign, 4 exponent bits with bias 7, 3 mantissa bits; 0x7F/0xFF are NaN).  The pages
+ *   do not say how a scale is chosen; here the block maximum is mapped onto 6: scale =
+ *   amax/6 rounded to the nearest E4M3 value (ties to the even code, values above 448
+ *   clamped to 448), element code = round-half-even of |x|/scale onto the E2M1 grid,
+ *   saturating at 6, sign bit = sign bit of x; a scale that rounds to 0 encodes its block
+ *   as signed zeros.  Every element value (code x scale) is exact in bf16.  Accepted by
+ *   the codec calls and as the main-KV format of csa2_sparse_attn; the indexer keys are
+ *   always MXFP4 (report §2.4.4). */
 typedef enum { CSA2_FMT_MXFP4 = 0, CSA2_FMT_NVFP4_E4M3_16 = 1 } csa2_fp4_format;
 
 typedef enum {
@@ -101,11 +110,12 @@ CSA2_API size_t csa2_cache_bytes_per_position(csa2_fp4_format main_fmt, int32_t 
 
 /* ---------------------------------------------------------------------------------- */
 /* csa2_quant_fp4 / csa2_dequant_fp4 -- the 4-bit cache codec (report §2.4.4).         */
-/* x: rows x cols values of type xt (BF16 or F32), row stride ldx elements.  cols % 32  */
-/* == 0.  codes: rows x cols/2 bytes, row stride ldc bytes; scales: rows x cols/32      */
-/* bytes, row stride lds bytes.  fmt must be CSA2_FMT_MXFP4.  Non-finite input sets     */
-/* CSA2_DEV_NONFINITE.  dequant writes y (BF16 or F32, row stride ldy); every MXFP4     */
-/* value with scale byte <= 252 is exact in both types.                                 */
+/* x: rows x cols values of type xt (BF16 or F32), row stride ldx elements.  cols is a  */
+/* multiple of the format's block G (32 for MXFP4, 16 for NVFP4_E4M3_16).  codes: rows  */
+/* x cols/2 bytes, row stride ldc bytes; scales: rows x cols/G bytes, row stride lds    */
+/* bytes.  Non-finite input sets CSA2_DEV_NONFINITE.  dequant writes y (BF16 or F32,    */
+/* row stride ldy); every MXFP4 value with scale byte <= 252 and every finite           */
+/* NVFP4_E4M3_16 value is exact in both types.                                          */
 /* ---------------------------------------------------------------------------------- */
 CSA2_API csa2_status csa2_quant_fp4(const void *x, csa2_dtype xt, int64_t rows, int64_t cols, int64_t ldx,
                            uint8_t *codes, int64_t ldc, uint8_t *scales, int64_t lds,
@@ -120,8 +130,8 @@ CSA2_API csa2_status csa2_dequant_fp4(const uint8_t *codes, int64_t ldc, const u
 /* jobs: HOST array of n_jobs (0..CSA2_QUANT_MAX_JOBS) descriptions, each with the      */
 /* meaning and rules of the csa2_quant_fp4 arguments of the same names; every job uses  */
 /* format fmt.  The outputs of different jobs must not overlap.  Results are those of   */
-/* n_jobs separate csa2_quant_fp4 calls (one kernel when every job has 16-byte aligned  */
-/* rows of x and 4-byte aligned rows of codes, else one launch per job).                */
+/* n_jobs separate csa2_quant_fp4 calls (one kernel when fmt is MXFP4 and every job has */
+/* 16-byte aligned rows of x and 4-byte aligned rows of codes, else one launch per job).*/
 /* ---------------------------------------------------------------------------------- */
 #define CSA2_QUANT_MAX_JOBS 4
 typedef struct {
@@ -244,14 +254,15 @@ typedef struct {
     float sm_scale;          /* logit scale, e.g. 1/sqrt(d_qk)                            */
     int64_t n_kv;            /* main-KV entries per sequence                              */
     const uint16_t *q;       /* bf16 [B, T, H, d_qk]                                      */
-    const uint8_t *kv_codes; /* [B, n_kv, d_qk/2]  MXFP4 main-KV codes                    */
-    const uint8_t *kv_scales;/* [B, n_kv, d_qk/32] MXFP4 main-KV scales                   */
+    const uint8_t *kv_codes; /* [B, n_kv, d_qk/2]  main-KV codes (format kv_fmt)          */
+    const uint8_t *kv_scales;/* [B, n_kv, d_qk/G]  main-KV scales, G = 32 (MXFP4) or 16   */
     const int32_t *idx;      /* [B, T, topk]                                              */
     const uint16_t *swa;     /* bf16 [B, n_swa, d_qk]; NULL = no SWA keys                 */
     int32_t n_swa;           /* SWA slots per sequence                                    */
     const int32_t *swa_pos0; /* [B] token position of slot 0 (required with swa)          */
     const int32_t *swa_start;/* [B] replay start s, or NULL for s = 0                     */
     const int32_t *q_pos;    /* [B, T] token position of each query (required with swa)   */
+    csa2_fp4_format kv_fmt;  /* main-KV format: CSA2_FMT_MXFP4 (0) or NVFP4_E4M3_16 (1)   */
 } csa2_attn_args;
 
 CSA2_API size_t csa2_sparse_attn_workspace_size(const csa2_attn_args *a);

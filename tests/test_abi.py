@@ -59,6 +59,9 @@ def test_cache_byte_ledger(lib):
     # this build's MXFP4 main KV at 512 + 64 dims: 288 + 18 bytes, plus the 68-byte key
     assert csa2.cache_bytes_per_position(csa2.FMT_MXFP4, 576, 128) == 288 + 18 + 64 + 4
     assert csa2.cache_bytes_per_position(csa2.FMT_MXFP4, 500, 128) == 0
+    # the report's main-KV format at 512 + 64 dims: 288 + 36 bytes, plus the key
+    assert csa2.cache_bytes_per_position(csa2.FMT_NVFP4_E4M3_16, 576, 128) == 288 + 36 + 64 + 4
+    assert csa2.cache_bytes_per_position(csa2.FMT_NVFP4_E4M3_16, 40, 128) == 0
 
 
 def test_status_strings(lib):
@@ -74,7 +77,11 @@ def test_quant_rejects_bad_shapes(lib):
     assert lib.csa2_quant_fp4(FAKE, 0, 4, 33, 33, FAKE, 17, FAKE, 2, 0, None, None) == 1
     assert lib.csa2_quant_fp4(FAKE, 5, 4, 32, 32, FAKE, 16, FAKE, 1, 0, None, None) == 1
     assert lib.csa2_quant_fp4(FAKE, 0, 4, 32, 16, FAKE, 16, FAKE, 1, 0, None, None) == 1
-    assert lib.csa2_quant_fp4(FAKE, 0, 4, 32, 32, FAKE, 16, FAKE, 1, 1, None, None) == 2
+    # E2M1 + E4M3/16: one scale per 16 values, so 32 columns need 2 scale bytes per row
+    assert lib.csa2_quant_fp4(FAKE, 0, 4, 32, 32, FAKE, 16, FAKE, 1, 1, None, None) == 1
+    assert lib.csa2_quant_fp4(FAKE, 0, 4, 40, 40, FAKE, 20, FAKE, 3, 1, None, None) == 1  # 40 % 16
+    assert lib.csa2_quant_fp4(FAKE, 0, 4, 32, 32, FAKE, 16, FAKE, 2, 2, None, None) == 1  # no format 2
+    assert lib.csa2_dequant_fp4(FAKE, 16, FAKE, 1, 4, 32, 1, FAKE, 0, 32, None) == 1
     assert lib.csa2_quant_fp4(None, 0, 0, 32, 32, None, 16, None, 1, 0, None, None) == 0
 
 
@@ -87,7 +94,8 @@ def test_quant_batch_rejects_bad_args(lib):
     ok = (0, 4, 32, 32, 16, 1)
     assert lib.csa2_quant_fp4_batch(jobs(ok), 5, 0, None, None) == 1          # more than 4 jobs
     assert lib.csa2_quant_fp4_batch(jobs(ok), -1, 0, None, None) == 1
-    assert lib.csa2_quant_fp4_batch(jobs(ok), 1, 1, None, None) == 2          # NVFP4: unsupported
+    assert lib.csa2_quant_fp4_batch(jobs(ok), 1, 1, None, None) == 1          # NVFP4: 2 scales per row
+    assert lib.csa2_quant_fp4_batch(jobs(ok), 1, 2, None, None) == 1          # no format 2
     assert lib.csa2_quant_fp4_batch(None, 1, 0, None, None) == 1
     assert lib.csa2_quant_fp4_batch(jobs(ok, (0, 4, 33, 33, 17, 2)), 2, 0, None, None) == 1
     assert lib.csa2_quant_fp4_batch(jobs(ok, (5, 4, 32, 32, 16, 1)), 2, 0, None, None) == 1
@@ -138,6 +146,9 @@ def test_select_and_attn_reject_bad_args(lib):
     a.n_kv = 10
     assert lib.csa2_sparse_attn(ctypes.byref(a), FAKE, None, None, 0, None, None) == 1   # d_v > d_qk
     a.d_v = 512
+    a.kv_fmt = 2                                                                         # no format 2
+    assert lib.csa2_sparse_attn(ctypes.byref(a), FAKE, None, None, 0, None, None) == 1
+    a.kv_fmt = csa2.FMT_NVFP4_E4M3_16
     a.swa, a.n_swa, a.swa_pos0, a.q_pos = FAKE, 128, None, FAKE                          # no pos0
     assert lib.csa2_sparse_attn(ctypes.byref(a), FAKE, None, None, 0, None, None) == 1
 

@@ -85,6 +85,65 @@ def test_quant_dequant_parity(cols, as_bf16):
     assert np.array_equal(s2.cpu().numpy()[nz], s_ref[nz])
 
 
+@pytest.mark.parametrize("cols,as_bf16", [(576, True), (48, False), (16, True)])
+def test_quant_dequant_nvfp4_parity(cols, as_bf16):
+    # E2M1 + E4M3/16 (the report's main-KV format): codes and scale bytes bit-exact, and
+    # every dequantised value exact in float32 and bf16
+    raw, x = _codec_inputs(2001, cols, 100 + cols + as_bf16, as_bf16)
+    rng = np.random.default_rng(cols)
+    x_small = rng.standard_normal((400, cols)).astype(np.float32)
+    x_small *= np.exp2(rng.integers(-16, 14, size=(400, 1))).astype(np.float32)   # E4M3 range
+    if as_bf16:
+        bits_small = synth.f32_to_bf16_bits(x_small)
+        raw, x = np.concatenate([raw, bits_small]), np.concatenate([x, f32(bits_small)])
+    else:
+        raw = x = np.concatenate([x, x_small])
+    xt = workload.bf16_tensor(raw, DEV) if as_bf16 else torch.from_numpy(raw).to(DEV)
+    st = status()
+    codes, scales = csa2.quant_fp4(xt, st, fmt=csa2.FMT_NVFP4_E4M3_16)
+    c_ref, s_ref = oracle.quant_nvfp4(x)
+    assert scales.shape[-1] == cols // 16
+    assert np.array_equal(scales.cpu().numpy(), s_ref)
+    assert np.array_equal(codes.cpu().numpy(), c_ref)
+    assert int(st.item()) == 0
+    y_ref = oracle.dequant_nvfp4(c_ref, s_ref).astype(np.float32)
+    y32 = csa2.dequant_fp4(codes, scales, torch.float32).cpu().numpy()
+    assert np.array_equal(y32.view(np.uint32), y_ref.view(np.uint32))
+    y16 = csa2.dequant_fp4(codes, scales, torch.bfloat16).view(torch.int16).cpu().numpy()
+    assert np.all(y_ref.view(np.uint32) & 0xFFFF == 0)
+    assert np.array_equal(y16.view(np.uint16), (y_ref.view(np.uint32) >> 16).astype(np.uint16))
+    # row-strided, unaligned rows take the scalar kernel: same bytes
+    wide = torch.zeros((xt.shape[0], cols + 1), dtype=xt.dtype, device=DEV)
+    wide[:, :cols] = xt
+    c_u = torch.empty_like(codes)
+    s_u = torch.empty_like(scales)
+    csa2.csa2_quant_fp4(wide[:, :cols], c_u, s_u, st, fmt=csa2.FMT_NVFP4_E4M3_16)
+    assert np.array_equal(c_u.cpu().numpy(), c_ref) and np.array_equal(s_u.cpu().numpy(), s_ref)
+
+
+def test_nvfp4_scale_rounding_boundaries():
+    # block maxima at, and one float32 step either side of, 6 x every E4M3 rounding midpoint,
+    # plus the zero-scale and clamp edges: the GPU's scale bytes and codes match the oracle's
+    vals = oracle.dequant_nvfp4(np.full((0x7F, 8), 0x22, np.uint8),        # code 2 = 1.0
+                                np.arange(0x7F, dtype=np.uint8)[:, None])[:, 0]   # E4M3 values
+    amax = []
+    for lo, hi in zip(vals[:-1], vals[1:]):
+        m = np.float32(3.0 * (lo + hi))
+        amax += [np.nextafter(m, np.float32(0)), m, np.nextafter(m, np.float32(np.inf))]
+    amax += [np.float32(v) for v in (0.0, 1e-30, 6 * 2.0 ** -10, 2688.0, 2785.0, 1e30)]
+    amax = np.asarray(amax, np.float32)
+    x = np.zeros((amax.size, 16), np.float32)
+    x[:, 5] = amax
+    x[:, 6] = -amax * np.float32(0.3)
+    x[:, 7] = amax * np.float32(0.75 / 6.0)
+    st = status()
+    codes, scales = csa2.quant_fp4(torch.from_numpy(x).to(DEV), st, fmt=csa2.FMT_NVFP4_E4M3_16)
+    c_ref, s_ref = oracle.quant_nvfp4(x.astype(np.float64))
+    assert np.array_equal(scales.cpu().numpy(), s_ref)
+    assert np.array_equal(codes.cpu().numpy(), c_ref)
+    assert int(st.item()) == 0
+
+
 @pytest.mark.parametrize("aligned", [True, False])
 def test_quant_batch_parity(aligned):
     # one launch for several jobs (bf16 and f32, different widths, a row-strided cache view);
@@ -343,14 +402,14 @@ def _attn_check(o_gpu, lse_gpu, o_ref, lse_ref):
     return err.max()
 
 
-def _oracle_attention(w, dw_rows, idx_np, t_range, swa_start=None):
+def _oracle_attention(w, dw_rows, idx_np, t_range, swa_start=None, kv_fmt="mxfp4"):
     """fp64 oracle attention for rows (b, t) with the given idx."""
     qpos = synth.q_positions(w)
     n_slots, pos0 = synth.swa_layout(w)
     _, _, qa = synth.gen_queries(w)
     outs, lses = {}, {}
     for b in dw_rows:
-        kvc, kvs = oracle.quant_mxfp4(f32(synth.gen_main_kv(w, b)))
+        kvc, kvs = oracle.quant_main_kv(f32(synth.gen_main_kv(w, b)), kv_fmt)
         swa = f32(synth.gen_swa(w, b)).astype(np.float64)
         s0 = 0 if swa_start is None else int(swa_start[b])
         for t in t_range:
@@ -369,11 +428,16 @@ ATTN_CASES = {
 }
 
 
-@pytest.mark.parametrize("name", list(ATTN_CASES))
-def test_attention_parity(name):
+@pytest.mark.parametrize("name,kv_fmt", [(n, "mxfp4") for n in ATTN_CASES] +
+                         [("prod_dims_T3", "nvfp4"), ("replay_start", "nvfp4"), ("tiny", "nvfp4"),
+                          ("d_v_odd_heads", "nvfp4")])
+def test_attention_parity(name, kv_fmt):
+    # kv_fmt "nvfp4": the main KV in the report's E2M1 + E4M3/16 format (tensor-core kernel
+    # for the production dims, CUDA-core kernel for the others)
     w, swa_start = ATTN_CASES[name]
     st = status()
-    dw = workload.build(w, kidx=False, device=DEV, d_status=st)
+    fmt = csa2.FMT_NVFP4_E4M3_16 if kv_fmt == "nvfp4" else csa2.FMT_MXFP4
+    dw = workload.build(w, kidx=False, device=DEV, d_status=st, kv_fmt=fmt)
     rng = np.random.default_rng(3)
     idx = np.stack([np.stack([np.sort(rng.choice(w.n_keys, w.topk, replace=False)) for _ in range(w.n_q)])
                     for _ in range(w.batch)]).astype(np.int32)
@@ -385,7 +449,7 @@ def test_attention_parity(name):
                                 ss, w.window, dw.sm_scale, w.d_v, d_status=st)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
-    o_ref, l_ref = _oracle_attention(w, range(w.batch), idx, range(w.n_q), swa_start)
+    o_ref, l_ref = _oracle_attention(w, range(w.batch), idx, range(w.n_q), swa_start, kv_fmt)
     for (b, t), o in o_ref.items():
         _attn_check(out[b, t].float().cpu().numpy(), lse[b, t].cpu().numpy(), o, l_ref[(b, t)])
 

@@ -82,7 +82,9 @@ def _step_bytes(w):
     idx_bytes = _kernel_bytes(w)
     attn = w.batch * w.n_q * (w.topk * (kv_row + 4) + w.window * w.d_qk * 2
                               + w.heads * w.d_qk * 2 + w.heads * w.d_v * 2)
-    write = w.batch * (w.d_qk * 2 + kv_row + w.idx_dim * 2 + w.idx_dim // 2 + w.idx_dim // 32)
+    # cache write: both bf16 rows in, their codes and scales out, and the RoPE table row
+    # (64 cosines and sines) of the new token
+    write = w.batch * (w.d_qk * 2 + kv_row + w.idx_dim * 2 + w.idx_dim // 2 + w.idx_dim // 32 + 64 * 4)
     return idx_bytes + attn + write
 
 
@@ -251,10 +253,19 @@ def run_gpu(args):
                           dtype=torch.uint8, device=dev)
     flush = L2Flush(dev)
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
-    cache_rows = [(new_kv, new_kvc, new_kvs), (new_k, new_kc, new_ks)]
-    cache_jobs = csa2.quant_jobs(cache_rows)
-    # our kernels per step: the cache-write quantiser (both rows), the indexer (it also writes
-    # the per-32 group maxima), Top-K select, attention
+    # cache write (report §2.4.4: quantised after RoPE): the new main-KV row's 64 trailing
+    # (RoPE) channels are rotated with a synthetic table (base 10,000) at the token's position,
+    # then both rows are quantised -- one launch
+    R = 64
+    ang = np.arange(w.n_keys, dtype=np.float64)[:, None] * \
+        10000.0 ** (-2.0 * np.arange(R // 2, dtype=np.float64) / R)[None, :]
+    rope_tab = torch.from_numpy(np.concatenate([np.cos(ang), np.sin(ang)], 1).astype(np.float32)).to(dev)
+    new_pos = torch.full((B,), last, dtype=torch.int32, device=dev)
+    cache_rows = [(new_kv, new_kvc, new_kvs, R, new_pos, rope_tab, csa2.FMT_MXFP4),
+                  (new_k, new_kc, new_ks, 0, None, None, csa2.FMT_MXFP4)]
+    cache_jobs = csa2.rope_quant_jobs(cache_rows)
+    # our kernels per step: the cache write (RoPE + quantisation of both rows), the indexer (it
+    # also writes the per-32 group maxima), Top-K select, attention
     launches_per_step = 4
 
     def step(k_ev=None):
@@ -265,9 +276,9 @@ def run_gpu(args):
         stream = torch.cuda.current_stream(dev)       # the capture stream while capturing
         if k_ev:
             k_ev[0].record(stream)
-        # cache write: the new token's main-KV and indexer-K rows, quantised in place (one
-        # launch for both)
-        csa2.csa2_quant_fp4_batch(cache_rows, st, jobs=cache_jobs)
+        # cache write: the new token's main-KV row (after RoPE) and indexer-K row, quantised
+        # in place (one launch for both)
+        csa2.csa2_rope_quant_fp4(cache_rows, st, jobs=cache_jobs)
         if k_ev:
             k_ev[1].record(stream)
         csa2.csa2_index_score(iargs, scores, row_len, st, workspace=ws_index)
@@ -290,7 +301,7 @@ def run_gpu(args):
     #      kernels follow one another directly, so each may start its set-up while the
     #      previous one finishes), and one with timing events between the calls, replayed
     #      separately for the per-call breakdown
-    names = ["cache_write_quant", "index_score", "topk", "sparse_attn"]
+    names = ["cache_write", "index_score", "topk", "sparse_attn"]
     graph, graph_ev, g_ev = None, None, None
     try:
         g_ev = tuple(torch.cuda.Event(enable_timing=True, external=True) for _ in range(5))
@@ -348,7 +359,7 @@ def run_gpu(args):
     #      cache write, the indexer and Top-K run (as a serving loop would pipeline it): the
     #      step is replayed as two graphs, the attention one after the copy's event.
     def step_front():
-        csa2.csa2_quant_fp4_batch(cache_rows, st, jobs=cache_jobs)
+        csa2.csa2_rope_quant_fp4(cache_rows, st, jobs=cache_jobs)
         csa2.csa2_index_score(iargs, scores, row_len, st, workspace=ws_index)
         csa2.csa2_topk(scores, w.topk, idx, row_len, d_status=st, workspace=ws_topk, group_max=gmax)
 
@@ -441,9 +452,9 @@ def run_gpu(args):
                  "launches": launches_per_step + 3}
 
     # ---- the same step over the report's own main-KV format (E2M1 + E4M3 per 16, report
-    #      §2.4.4): cache write (main-KV row in that format, indexer-K row in MXFP4: two
-    #      launches), indexer, Top-K, attention over the E4M3/16 cache; one CUDA graph, L2
-    #      flushed between steps; the attention call alone is timed for both formats
+    #      §2.4.4): cache write (main-KV row after RoPE in that format, indexer-K row in
+    #      MXFP4: one launch), indexer, Top-K, attention over the E4M3/16 cache; one CUDA
+    #      graph, L2 flushed between steps; the attention call alone is timed for both formats
     nv = None
     if want_nv and graph is not None:
         nv_c, nv_s = dw["kv_codes_nv"], dw["kv_scales_nv"]
@@ -452,12 +463,12 @@ def run_gpu(args):
         ws_attn_nv = torch.empty(max(1, lib.csa2_sparse_attn_workspace_size(ctypes.byref(aargs_nv))),
                                  dtype=torch.uint8, device=dev)
         out_nv, lse_nv = torch.empty_like(out), torch.empty_like(lse)
-        nv_row = [(new_kv, nv_c[:, last], nv_s[:, last])]
-        nv_jobs, k_jobs = csa2.quant_jobs(nv_row), csa2.quant_jobs(cache_rows[1:])
+        nv_rows = [(new_kv, nv_c[:, last], nv_s[:, last], R, new_pos, rope_tab, csa2.FMT_NVFP4_E4M3_16),
+                   cache_rows[1]]
+        nv_jobs = csa2.rope_quant_jobs(nv_rows)
 
         def step_nv():
-            csa2.csa2_quant_fp4_batch(nv_row, st, jobs=nv_jobs, fmt=csa2.FMT_NVFP4_E4M3_16)
-            csa2.csa2_quant_fp4_batch(cache_rows[1:], st, jobs=k_jobs)
+            csa2.csa2_rope_quant_fp4(nv_rows, st, jobs=nv_jobs)
             csa2.csa2_index_score(iargs, scores, row_len, st, workspace=ws_index)
             csa2.csa2_topk(scores, w.topk, idx, row_len, d_status=st, workspace=ws_topk, group_max=gmax)
             csa2.csa2_sparse_attn(aargs_nv, out_nv, lse_nv, st, workspace=ws_attn_nv)
@@ -490,7 +501,7 @@ def run_gpu(args):
             raise RuntimeError(f"device status {int(st.item())}")
         row_nv = w.d_qk // 2 + w.d_qk // 16
         nv = {"format": "E2M1 + E4M3 per 16, no global scale (report §2.4.4)",
-              "ms_per_step": t_nv, "tokens_per_s": B * T / (t_nv * 1e-3), "launches": launches_per_step + 1,
+              "ms_per_step": t_nv, "tokens_per_s": B * T / (t_nv * 1e-3), "launches": launches_per_step,
               "sparse_attn_ms": t_a_nv, "sparse_attn_ms_mxfp4": t_a_mx,
               "main_kv_bytes_per_position": row_nv,
               "cache_bytes_per_position": lib.csa2_cache_bytes_per_position(csa2.FMT_NVFP4_E4M3_16, w.d_qk,

@@ -71,6 +71,15 @@ class QuantJob(ctypes.Structure):
 QUANT_MAX_JOBS = 4
 
 
+class RopeQuantJob(ctypes.Structure):
+    """csa2_rope_quant_job of include/csa2.h."""
+    _fields_ = [("x", ctypes.c_void_p), ("rows", ctypes.c_int64), ("cols", ctypes.c_int64),
+                ("ldx", ctypes.c_int64), ("rope_dim", ctypes.c_int32), ("pos", ctypes.c_void_p),
+                ("cos_sin", ctypes.c_void_p), ("n_pos", ctypes.c_int64), ("codes", ctypes.c_void_p),
+                ("ldc", ctypes.c_int64), ("scales", ctypes.c_void_p), ("lds", ctypes.c_int64),
+                ("fmt", ctypes.c_int)]
+
+
 def load(build_if_missing: bool = True) -> ctypes.CDLL:
     """Load libcsa2.so (building it in-tree first if it is absent or stale)."""
     global _lib
@@ -93,6 +102,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
             lib.csa2_quant_fp4.argtypes = [_P, S, _I64, _I64, _I64, _P, _I64, _P, _I64, S, _P, _P]
             lib.csa2_quant_fp4_batch.restype = S
             lib.csa2_quant_fp4_batch.argtypes = [ctypes.POINTER(QuantJob), _I32, S, _P, _P]
+            lib.csa2_rope_quant_fp4.restype = S
+            lib.csa2_rope_quant_fp4.argtypes = [ctypes.POINTER(RopeQuantJob), _I32, _P, _P]
             lib.csa2_dequant_fp4.restype = S
             lib.csa2_dequant_fp4.argtypes = [_P, _I64, _P, _I64, _I64, _I64, S, _P, S, _I64, _P]
             lib.csa2_index_score_workspace_size.restype = sz
@@ -217,6 +228,35 @@ def csa2_quant_fp4_batch(triples, d_status: Optional[torch.Tensor] = None, strea
         jobs = quant_jobs(triples)
     _check("csa2_quant_fp4_batch", load().csa2_quant_fp4_batch(
         jobs, len(triples), fmt, _ptr(d_status), _stream(stream)))
+
+
+def rope_quant_jobs(specs) -> ctypes.Array:
+    """(x bf16 [rows, cols], codes, scales, rope_dim, pos int32 [rows] or None, cos_sin f32
+    [n_pos, rope_dim] or None, fmt) tuples -> a csa2_rope_quant_job array (keep it alive)."""
+    jobs = (RopeQuantJob * max(1, len(specs)))()
+    for i, (x, codes, scales, rope_dim, pos, cos_sin, fmt) in enumerate(specs):
+        if x.dtype != torch.bfloat16:
+            raise ValueError("x must be bf16")
+        px, rows, ldx = _rows_view(x)
+        pc, rows_c, ldc = _rows_view(codes)
+        ps, rows_s, lds = _rows_view(scales)
+        if rows_c != rows or rows_s != rows:
+            raise ValueError("x, codes and scales must have the same number of rows")
+        jobs[i] = RopeQuantJob(px.value, rows, x.shape[-1], ldx, rope_dim,
+                               pos.data_ptr() if pos is not None else None,
+                               cos_sin.data_ptr() if cos_sin is not None else None,
+                               cos_sin.shape[0] if cos_sin is not None else 0,
+                               pc.value, ldc, ps.value, lds, fmt)
+    return jobs
+
+
+def csa2_rope_quant_fp4(specs, d_status: Optional[torch.Tensor] = None, stream=None, jobs=None):
+    """RoPE on the trailing rope_dim channels, then the 4-bit codec, for up to four jobs
+    in one launch (csa2_rope_quant_fp4); specs as for rope_quant_jobs."""
+    if jobs is None:
+        jobs = rope_quant_jobs(specs)
+    _check("csa2_rope_quant_fp4", load().csa2_rope_quant_fp4(jobs, len(specs), _ptr(d_status),
+                                                             _stream(stream)))
 
 
 def csa2_dequant_fp4(codes: torch.Tensor, scales: torch.Tensor, y: torch.Tensor, stream=None,

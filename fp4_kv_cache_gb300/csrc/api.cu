@@ -154,6 +154,31 @@ csa2_status csa2_quant_fp4_batch(const csa2_quant_job *jobs, int32_t n_jobs, csa
     return CSA2_OK;
 }
 
+csa2_status csa2_rope_quant_fp4(const csa2_rope_quant_job *jobs, int32_t n_jobs, uint32_t *d_status,
+                                csa2_stream stream)
+{
+    if (n_jobs < 0 || n_jobs > CSA2_QUANT_MAX_JOBS) return CSA2_ERR_INVALID_ARG;
+    if (n_jobs == 0) return CSA2_OK;
+    if (!jobs) return CSA2_ERR_INVALID_ARG;
+    RopeQuantJobDesc d[CSA2_QUANT_MAX_JOBS];
+    for (int k = 0; k < n_jobs; ++k) {
+        const csa2_rope_quant_job &j = jobs[k];
+        const int G = fmt_block(j.fmt);
+        if (!G || j.rows < 0 || j.cols < 0 || j.cols % G) return CSA2_ERR_INVALID_ARG;
+        if (j.rope_dim < 0 || j.rope_dim % 2 || j.rope_dim > j.cols) return CSA2_ERR_INVALID_ARG;
+        if (j.rows && j.cols) {
+            if (!j.x || !j.codes || !j.scales) return CSA2_ERR_INVALID_ARG;
+            if (j.ldx < j.cols || j.ldc < j.cols / 2 || j.lds < j.cols / G) return CSA2_ERR_INVALID_ARG;
+            if (!aligned(j.x, 16) || j.ldx % 8 || !aligned(j.codes, 4) || j.ldc % 4) return CSA2_ERR_INVALID_ARG;
+            if (j.rope_dim > 0 && (!j.pos || !j.cos_sin || j.n_pos < 1 || !aligned(j.cos_sin, 4)))
+                return CSA2_ERR_INVALID_ARG;
+        }
+        d[k] = {j.x, j.rows, j.cols, j.ldx, j.rope_dim, j.pos, j.cos_sin, j.n_pos, j.codes, j.ldc, j.scales, j.lds,
+                j.fmt == CSA2_FMT_NVFP4_E4M3_16};
+    }
+    return from_cuda(launch_rope_quant(d, n_jobs, d_status, as_stream(stream)));
+}
+
 csa2_status csa2_dequant_fp4(const uint8_t *codes, int64_t ldc, const uint8_t *scales,
                              int64_t lds, int64_t rows, int64_t cols, csa2_fp4_format fmt,
                              void *y, csa2_dtype yt, int64_t ldy, csa2_stream stream)

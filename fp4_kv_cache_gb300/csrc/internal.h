@@ -26,6 +26,22 @@ cudaError_t launch_quant_mxfp4_batch(const QuantJobDesc *jobs, int n_jobs, uint3
 cudaError_t launch_quant_nvfp4(const void *x, bool x_bf16, int64_t rows, int64_t cols, int64_t ldx,
                                uint8_t *codes, int64_t ldc, uint8_t *scales, int64_t lds,
                                uint32_t *d_status, cudaStream_t s);
+// The cache write with the rotary embedding fused in (csa2_rope_quant_fp4): up to four jobs,
+// rows already validated (16-byte aligned bf16 x, 4-byte aligned codes).
+struct RopeQuantJobDesc {
+    const uint16_t *x;
+    int64_t rows, cols, ldx;
+    int32_t rope_dim;
+    const int32_t *pos;
+    const float *cos_sin;
+    int64_t n_pos;
+    uint8_t *codes;
+    int64_t ldc;
+    uint8_t *scales;
+    int64_t lds;
+    bool nvfp4;
+};
+cudaError_t launch_rope_quant(const RopeQuantJobDesc *jobs, int n_jobs, uint32_t *d_status, cudaStream_t s);
 cudaError_t launch_dequant_fp4(const uint8_t *codes, int64_t ldc, const uint8_t *scales,
                                int64_t lds, int64_t rows, int64_t cols, bool nvfp4, void *y,
                                bool y_bf16, int64_t ldy, cudaStream_t s);

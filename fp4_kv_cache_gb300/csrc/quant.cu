@@ -311,6 +311,111 @@ __global__ void __launch_bounds__(256) dequant_fp4_kernel(const uint8_t *__restr
     }
 }
 
+// ---------------------------------------------------------------- RoPE + quantise
+// The cache write of report §2.4.4 (quantise after RoPE, one format for both parts): every
+// lane takes 8 values of one block (one 16-byte bf16 load), rotates the pairs that fall in
+// the trailing rope_dim channels with the caller's cos/sin row, and quantises like the
+// vector kernels above.  Jobs are laid end to end; each job's lane run starts on a multiple
+// of 4 so that a block's lanes (4 for MXFP4, 2 for E2M1 + E4M3/16) share an aligned group.
+struct RopeQuantParams {
+    const uint16_t *x[4];
+    const int32_t *pos[4];
+    const float *cs[4];
+    uint8_t *codes[4], *scales[4];
+    int64_t cols[4], nblk[4], blocks[4], ldx[4], ldc[4], lds[4], n_pos[4];
+    int64_t lanes_end[4];          // running total of each job's lanes, rounded up to 4
+    int32_t rope[4], nv[4];
+    int n;
+};
+
+__global__ void __launch_bounds__(256) rope_quant_kernel(const __grid_constant__ RopeQuantParams B,
+                                                         uint32_t *d_status)
+{
+    pdl_wait();                                   // x and pos may come from the kernel before
+    pdl_allow_dependents();
+    const int64_t total = B.lanes_end[B.n - 1];
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t total32 = (total + 31) & ~int64_t(31);
+    for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total32; t += stride) {
+        int j = 0;
+#pragma unroll
+        for (int k = 0; k < 3; ++k) j += (k + 1 < B.n && t >= B.lanes_end[k]) ? 1 : 0;
+        const int64_t tl = t < total ? t - (j > 0 ? B.lanes_end[j - 1] : 0) : 0;
+        const bool nv = B.nv[j] != 0;
+        const int64_t grp = nv ? tl >> 1 : tl >> 2;
+        const int sub = (int)(tl & (nv ? 1 : 3));
+        const bool act = t < total && grp < B.blocks[j];
+        const int64_t nblk = B.nblk[j];
+        const int64_t r = act ? grp / nblk : 0, kb = act ? grp % nblk : 0;
+        const int G = nv ? 16 : 32;
+        const int64_t col = kb * G + sub * 8;
+        float v[8];
+        if (act) {
+            const uint4 raw = *reinterpret_cast<const uint4 *>(B.x[j] + r * B.ldx[j] + col);
+            const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                v[2 * i] = __uint_as_float(w[i] << 16);
+                v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+            }
+            const int rope = B.rope[j];
+            const int64_t c0 = B.cols[j] - rope;
+            if (rope > 0 && col + 8 > c0) {
+                const int64_t p = B.pos[j][r];
+                if (p < 0 || p >= B.n_pos[j]) {
+                    dev_flag(d_status, CSA2_DEV_BAD_INDEX);
+                } else {
+                    const float *cs = B.cs[j] + p * rope;
+                    const int half = rope >> 1;
+#pragma unroll
+                    for (int e = 0; e < 8; e += 2) {
+                        if (col + e >= c0) {          // c0 and col + e are even: a whole pair
+                            const int i = (int)((col + e - c0) >> 1);
+                            const float c = cs[i], sn = cs[half + i], a = v[e], b = v[e + 1];
+                            v[e] = __fsub_rn(__fmul_rn(a, c), __fmul_rn(b, sn));
+                            v[e + 1] = __fadd_rn(__fmul_rn(a, sn), __fmul_rn(b, c));
+                        }
+                    }
+                }
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = 0.0f;
+        }
+        uint32_t amax = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) amax = max(amax, __float_as_uint(v[i]) & 0x7fffffffu);
+        amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        const uint32_t amax4 = max(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        if (!nv) amax = amax4;
+        if (!act) continue;
+        const bool finite = amax < 0x7f800000u;
+        if (!finite && sub == 0) dev_flag(d_status, CSA2_DEV_NONFINITE);
+        const float amax_f = __uint_as_float(finite ? amax : 0u);
+        uint32_t word = 0, sbyte;
+        if (nv) {
+            sbyte = e4m3_block_scale(amax_f);
+            const float sc = e4m3_value(sbyte);
+            if (sc > 0.0f) {
+#pragma unroll
+                for (int i = 0; i < 8; i += 2)
+                    word |= e2m1x2_cvt(__fdiv_rn(v[i], sc), __fdiv_rn(v[i + 1], sc)) << (4 * i);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) word |= (__float_as_uint(v[i]) >> 31) << (4 * i + 3);
+            }
+        } else {
+            const int X = mx_block_exponent(amax_f);
+            const float inv = pow2_neg(X);
+#pragma unroll
+            for (int i = 0; i < 8; i += 2) word |= e2m1x2_cvt(v[i] * inv, v[i + 1] * inv) << (4 * i);
+            sbyte = (uint32_t)(X + 127);
+        }
+        *reinterpret_cast<uint32_t *>(B.codes[j] + r * B.ldc[j] + kb * (G / 2) + sub * 4) = word;
+        if (sub == 0) B.scales[j][r * B.lds[j] + kb] = (uint8_t)sbyte;
+    }
+}
+
 int grid_for(int64_t work_items, int per_block)
 {
     int64_t g = (work_items + per_block - 1) / per_block;
@@ -404,6 +509,40 @@ cudaError_t launch_quant_nvfp4(const void *x, bool x_bf16, int64_t rows, int64_t
     else
         quant_nvfp4_kernel<false><<<grid, 256, 0, s>>>(x, rows, cols, ldx, codes, ldc, scales, lds, d_status);
     return cudaGetLastError();
+}
+
+cudaError_t launch_rope_quant(const RopeQuantJobDesc *jobs, int n_jobs, uint32_t *d_status, cudaStream_t s)
+{
+    if (n_jobs < 1 || n_jobs > 4) return cudaErrorInvalidValue;
+    RopeQuantParams B = {};
+    int64_t acc = 0;
+    int n = 0;
+    for (int k = 0; k < n_jobs; ++k) {
+        const RopeQuantJobDesc &j = jobs[k];
+        if (j.rows == 0 || j.cols == 0) continue;
+        const int G = j.nvfp4 ? 16 : 32;
+        B.x[n] = j.x;
+        B.pos[n] = j.pos;
+        B.cs[n] = j.cos_sin;
+        B.codes[n] = j.codes;
+        B.scales[n] = j.scales;
+        B.cols[n] = j.cols;
+        B.nblk[n] = j.cols / G;
+        B.blocks[n] = j.rows * (j.cols / G);
+        B.ldx[n] = j.ldx;
+        B.ldc[n] = j.ldc;
+        B.lds[n] = j.lds;
+        B.n_pos[n] = j.n_pos;
+        B.rope[n] = j.rope_dim;
+        B.nv[n] = j.nvfp4 ? 1 : 0;
+        acc += (B.blocks[n] * (G / 8) + 3) & ~int64_t(3);
+        B.lanes_end[n] = acc;
+        ++n;
+    }
+    if (n == 0) return cudaSuccess;
+    B.n = n;
+    for (int k = n; k < 4; ++k) B.lanes_end[k] = acc;
+    return launch_pdl(rope_quant_kernel, dim3(grid_for(acc, 256)), dim3(256), 0, s, 1, B, d_status);
 }
 
 cudaError_t launch_dequant_fp4(const uint8_t *codes, int64_t ldc, const uint8_t *scales,

@@ -147,6 +147,43 @@ CSA2_API csa2_status csa2_quant_fp4_batch(const csa2_quant_job *jobs, int32_t n_
                                           uint32_t *d_status, csa2_stream stream);
 
 /* ---------------------------------------------------------------------------------- */
+/* csa2_rope_quant_fp4 -- the decode step's cache write with the rotary embedding fused */
+/* in: report §2.4.4 quantises the main-KV cache AFTER RoPE, with the RoPE and non-RoPE */
+/* channels in the same 4-bit format.  Up to CSA2_QUANT_MAX_JOBS jobs in one launch,    */
+/* each with its own format and rotated width.  For job j, row r of x (bf16):           */
+/*   the last rope_dim channels c0 = cols - rope_dim ... cols-1 are rotated in pairs     */
+/*   (c0 + 2i, c0 + 2i + 1), i < rope_dim/2, by the caller's table row p = pos[r]:       */
+/*     c = cos_sin[p * rope_dim + i], s = cos_sin[p * rope_dim + rope_dim/2 + i]         */
+/*     y[c0+2i]   = RN32(RN32(a*c) - RN32(b*s)),  y[c0+2i+1] = RN32(RN32(a*s) + RN32(b*c)) */
+/*   (a, b = the pair's input values; float32, one rounding per product and per sum,  */
+/*   no fused multiply-add), the other channels y = x; then y (float32, not rounded to  */
+/*   bf16) is quantised in format fmt exactly as csa2_quant_fp4 quantises its input.    */
+/* The pages give no RoPE formula; the pairing, the table and its frequencies are the   */
+/* caller's (rope_dim = 0: no rotation, pos and cos_sin unused).                        */
+/* Requirements per job: x rows 16-byte aligned (x and ldx*2), codes rows 4-byte        */
+/* aligned (codes and ldc), cols % G == 0 (G = 32 MXFP4, 16 NVFP4_E4M3_16), rope_dim    */
+/* even and <= cols; with rope_dim > 0: pos [rows] (device) and cos_sin [n_pos,        */
+/* rope_dim] float32 (device), n_pos >= 1.  A row whose pos is outside [0, n_pos) sets  */
+/* CSA2_DEV_BAD_INDEX and is quantised unrotated.  Outputs of different jobs must not   */
+/* overlap.                                                                            */
+/* ---------------------------------------------------------------------------------- */
+typedef struct {
+    const uint16_t *x;       /* bf16 rows x cols, row stride ldx elements                 */
+    int64_t rows, cols, ldx;
+    int32_t rope_dim;        /* rotated trailing channels (0: none)                       */
+    const int32_t *pos;      /* [rows] token position of each row (rope_dim > 0)          */
+    const float *cos_sin;    /* [n_pos, rope_dim]: rope_dim/2 cosines, then the sines      */
+    int64_t n_pos;
+    uint8_t *codes;          /* rows x cols/2 bytes, row stride ldc                        */
+    int64_t ldc;
+    uint8_t *scales;         /* rows x cols/G bytes, row stride lds                        */
+    int64_t lds;
+    csa2_fp4_format fmt;
+} csa2_rope_quant_job;
+CSA2_API csa2_status csa2_rope_quant_fp4(const csa2_rope_quant_job *jobs, int32_t n_jobs,
+                                         uint32_t *d_status, csa2_stream stream);
+
+/* ---------------------------------------------------------------------------------- */
 /* csa2_index_score -- indexer scores (report §2.3: the indexer scores main-KV entries  */
 /* with indexer Q and indexer K; §2.3.2: Reindex layers score only the pool).           */
 /*                                                                                    */

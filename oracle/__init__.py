@@ -142,6 +142,34 @@ def dequant_main_kv(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
     return dequant_nvfp4(codes, scales) if scales.shape[-1] == D // 16 else dequant_mxfp4(codes, scales)
 
 
+# ---------------------------------------------------------------- RoPE before the cache write
+def rope_rotate(x: np.ndarray, pos: np.ndarray, cos_sin: np.ndarray, rope_dim: int) -> np.ndarray:
+    """Rotary embedding of the trailing ``rope_dim`` channels of each row, the step the
+    report (§2.4.4) places before the main-KV cache is quantised.
+
+    The pages give no formula; the reading used: channel pairs (c0 + 2i, c0 + 2i + 1),
+    c0 = cols - rope_dim, rotated by the caller's table row p = pos[r] (rope_dim/2 cosines
+    then rope_dim/2 sines):  (a, b) -> (a c - b s, a s + b c).  The rotated values decide
+    the integer codes, so they are computed in the kernel's float32 precision: one rounding
+    per product and per sum, no fused multiply-add.  x [rows, cols] (float32 values) ->
+    float32 [rows, cols]."""
+    y = np.array(x, dtype=np.float32, copy=True)
+    if rope_dim == 0 or y.shape[0] == 0:
+        return y
+    c0, h = y.shape[1] - rope_dim, rope_dim // 2
+    tab = np.asarray(cos_sin, np.float32)[np.asarray(pos, np.int64)]
+    c, s = tab[:, :h], tab[:, h:]
+    a, b = y[:, c0::2].copy(), y[:, c0 + 1::2].copy()
+    y[:, c0::2] = np.subtract(np.multiply(a, c), np.multiply(b, s))
+    y[:, c0 + 1::2] = np.add(np.multiply(a, s), np.multiply(b, c))
+    return y
+
+
+def rope_quant(x: np.ndarray, pos, cos_sin, rope_dim: int, fmt: str = "mxfp4"):
+    """Cache write of one main-KV (or key) row block: RoPE, then the 4-bit codec."""
+    return quant_main_kv(rope_rotate(x, pos, cos_sin, rope_dim).astype(np.float64), fmt)
+
+
 # ---------------------------------------------------------------- scoring
 def head_dots(qc, qs, kc, ks, pos) -> np.ndarray:
     """Per-head float32 dots D [npos, H] of one quantised query ([H, d/2], [H, d/32])

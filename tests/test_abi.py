@@ -28,7 +28,7 @@ def lib():
 
 def test_exports_every_declared_symbol(lib):
     syms = _declared_symbols()
-    assert len(syms) == 15
+    assert len(syms) == 16
     for s in syms:
         assert hasattr(lib, s), s
     out = os.popen(f"nm -D --defined-only {libbuild.LIB}").read()
@@ -104,6 +104,31 @@ def test_quant_batch_rejects_bad_args(lib):
     empty = (csa2.QuantJob * 1)()
     empty[0] = csa2.QuantJob(None, 0, 0, 32, 32, None, 16, None, 1)
     assert lib.csa2_quant_fp4_batch(empty, 1, 0, None, None) == 0             # zero rows: no launch
+
+
+def test_rope_quant_rejects_bad_args(lib):
+    def job(rows=4, cols=64, ldx=64, rope=32, pos=FAKE, cs=FAKE, n_pos=10, ldc=32, lds=2, fmt=0,
+            x=FAKE, codes=FAKE):
+        j = (csa2.RopeQuantJob * 1)()
+        j[0] = csa2.RopeQuantJob(x.value if x else None, rows, cols, ldx, rope, pos.value if pos else None,
+                                 cs.value if cs else None, n_pos, codes.value if codes else None, ldc,
+                                 FAKE.value, lds, fmt)
+        return j
+    f = lib.csa2_rope_quant_fp4
+    assert f(job(rope=31), 1, None, None) == 1                     # odd rotated width
+    assert f(job(rope=66), 1, None, None) == 1                     # wider than the row
+    assert f(job(pos=None), 1, None, None) == 1                    # rotation without positions
+    assert f(job(n_pos=0), 1, None, None) == 1
+    assert f(job(ldx=68), 1, None, None) == 1                      # rows not 16-byte aligned
+    assert f(job(x=ctypes.c_void_p(264)), 1, None, None) == 1
+    assert f(job(ldc=34), 1, None, None) == 1                      # code rows not 4-byte aligned
+    assert f(job(cols=48, ldx=48, ldc=24, lds=1), 1, None, None) == 1    # 48 % 32
+    assert f(job(fmt=1, lds=2), 1, None, None) == 1                # E4M3/16: 4 scales per row
+    assert f(job(fmt=2), 1, None, None) == 1
+    assert f(job(), 5, None, None) == 1                            # more than 4 jobs
+    assert f(None, 1, None, None) == 1
+    assert f(None, 0, None, None) == 0                             # nothing to do
+    assert f(job(rows=0), 1, None, None) == 0                      # zero rows: no launch
 
 
 def test_index_rejects_bad_args(lib):

@@ -144,6 +144,60 @@ def test_nvfp4_scale_rounding_boundaries():
     assert int(st.item()) == 0
 
 
+def _rope_table(n_pos, rope_dim, base=10000.0):
+    """Synthetic RoPE table [n_pos, rope_dim]: cosines then sines of p * base^(-2i/R)."""
+    i = np.arange(rope_dim // 2, dtype=np.float64)
+    ang = np.arange(n_pos, dtype=np.float64)[:, None] * base ** (-2.0 * i / rope_dim)[None, :]
+    return np.concatenate([np.cos(ang), np.sin(ang)], axis=1).astype(np.float32)
+
+
+def test_rope_quant_parity():
+    # report §2.4.4: the cache is quantised after RoPE.  One launch, four jobs: main-KV rows
+    # (512 + 64 rotated channels) in both formats, a 128-channel key block with 64 rotated
+    # channels, and a block with no rotation; codes and scales bit-exact against the oracle;
+    # one row's position lies outside the table (flagged, quantised unrotated)
+    rng = np.random.default_rng(77)
+    n_pos = 4096
+    tab = _rope_table(n_pos, 64)
+    tab_d = torch.from_numpy(tab).to(DEV)
+    specs = [(333, 576, 64, csa2.FMT_MXFP4), (129, 576, 64, csa2.FMT_NVFP4_E4M3_16),
+             (70, 128, 64, csa2.FMT_MXFP4), (17, 512, 0, csa2.FMT_NVFP4_E4M3_16)]
+    st = status()
+    call, refs = [], []
+    for rows, cols, R, fmt in specs:
+        g = csa2.FMT_BLOCK[fmt]
+        x = rng.standard_normal((rows, cols)).astype(np.float32)
+        x *= np.exp2(rng.integers(-12, 8, size=(rows, 1))).astype(np.float32)
+        bits = synth.f32_to_bf16_bits(x)
+        pos = rng.integers(0, n_pos, rows).astype(np.int32)
+        pos[0], pos[-1] = 0, n_pos - 1
+        codes = torch.full((rows, cols // 2 + 8), 0xAB, dtype=torch.uint8, device=DEV)   # strided rows
+        scales = torch.full((rows, cols // g + 4), 0xAB, dtype=torch.uint8, device=DEV)
+        xt = workload.bf16_tensor(bits, DEV)
+        pos_d = torch.from_numpy(pos).to(DEV)
+        call.append((xt, codes[:, : cols // 2], scales[:, : cols // g], R, pos_d if R else None,
+                     tab_d if R else None, fmt))
+        refs.append((oracle.rope_quant(f32(bits), pos, tab, R, "nvfp4" if g == 16 else "mxfp4"),
+                     codes, scales, cols, g))
+    csa2.csa2_rope_quant_fp4(call, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    for (c_ref, s_ref), codes, scales, cols, g in refs:
+        assert np.array_equal(codes[:, : cols // 2].cpu().numpy(), c_ref)
+        assert np.array_equal(scales[:, : cols // g].cpu().numpy(), s_ref)
+        assert torch.all(codes[:, cols // 2:] == 0xAB) and torch.all(scales[:, cols // g:] == 0xAB)
+    # a position past the table: flagged, and that row is quantised without rotation
+    xt, codes, scales, R, pos_d, _, fmt = call[0]
+    pos_bad = pos_d.clone()
+    pos_bad[5] = n_pos
+    st2 = status()
+    csa2.csa2_rope_quant_fp4([(xt, codes, scales, R, pos_bad, tab_d, fmt)], st2)
+    torch.cuda.synchronize()
+    assert int(st2.item()) & csa2.DEV_BAD_INDEX
+    c_plain, s_plain = oracle.quant_mxfp4(f32(xt[5:6].view(torch.int16).cpu().numpy().view(np.uint16)))
+    assert np.array_equal(codes[5:6].cpu().numpy(), c_plain) and np.array_equal(scales[5:6].cpu().numpy(), s_plain)
+
+
 @pytest.mark.parametrize("aligned", [True, False])
 def test_quant_batch_parity(aligned):
     # one launch for several jobs (bf16 and f32, different widths, a row-strided cache view);

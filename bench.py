@@ -570,7 +570,7 @@ def run_gpu(args):
 PREFILL_WORKLOAD = "prefill_chunk_m2"
 
 
-def prefill_indexer(dev, sm_mhz):
+def prefill_indexer(dev, sm_mhz, with_chunk=True):
     """Tensor-core indexer over one prefill chunk: FP4 dot TFLOP/s (2 x heads x d_i per
     visible (query, position) pair) against the FP4 tensor peak (the measured bf16 GEMM
     peak x 6, the nominal fp4/bf16 ratio) and against the CUDA-core bound of its epilogue
@@ -578,23 +578,69 @@ def prefill_indexer(dev, sm_mhz):
     import torch
     from fp4_kv_cache_gb300 import csa2, workload
     w = synth.WORKLOADS[PREFILL_WORKLOAD]
-    dw = workload.build(w, device=dev, kv=False)
+    dw = workload.build(w, device=dev, kv=with_chunk)
     B, T = w.batch, w.n_q
     scores = torch.empty((B, T, w.n_keys), dtype=torch.float32, device=dev)
+    row_len = torch.empty((B, T), dtype=torch.int32, device=dev)
     gmax = csa2.group_max_buffer(scores)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    iargs = csa2.make_index_args(dw["q_idx"], dw["w_idx"], dw["k_codes"], dw["k_scales"], dw["q_pos"],
+                                 w.ratio_m, group_max=gmax)
+    import ctypes
+    lib = csa2.load()
+    ws_index = torch.zeros(max(1, lib.csa2_index_score_workspace_size(ctypes.byref(iargs))),
+                           dtype=torch.uint8, device=dev)     # zero before first use; calls keep it so
     flush = L2Flush(dev)
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
     ms = []
     for it in range(8):
         flush()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0, e1 = ev(), ev()
         e0.record()
-        _, row_len = csa2.index_score(dw["q_idx"], dw["w_idx"], dw["k_codes"], dw["k_scales"],
-                                      dw["q_pos"], w.ratio_m, group_max=gmax)
+        csa2.csa2_index_score(iargs, scores, row_len, st, workspace=ws_index)
         e1.record()
         e1.synchronize()
         if it >= 3:
             ms.append(e0.elapsed_time(e1))
     t = statistics.median(ms)
+    chunk = None
+    if with_chunk:
+        # the whole chunk (encoder Full layer): indexer, per-query Top-512 (fed the indexer's
+        # group maxima), then attention over the 512 selected entries + the SWA window
+        idx = torch.empty((B, T, w.topk), dtype=torch.int32, device=dev)
+        out = torch.empty((B, T, w.heads, w.d_v), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((B, T, w.heads), dtype=torch.float32, device=dev)
+        aargs = csa2.make_attn_args(dw["q_attn"], dw["kv_codes"], dw["kv_scales"], idx, dw["swa"],
+                                    dw["swa_pos0"], dw["q_pos"], None, w.window, dw.sm_scale, w.d_v)
+        ws_topk = torch.empty(max(1, lib.csa2_topk_workspace_size(B * T, w.n_keys, w.topk)),
+                              dtype=torch.uint8, device=dev)
+        ws_attn = torch.empty(max(1, lib.csa2_sparse_attn_workspace_size(ctypes.byref(aargs))),
+                              dtype=torch.uint8, device=dev)
+        per = {"index_score": [], "topk": [], "sparse_attn": [], "chunk": []}
+        for it in range(7):
+            flush()
+            e = [ev() for _ in range(4)]
+            e[0].record()
+            csa2.csa2_index_score(iargs, scores, row_len, st, workspace=ws_index)
+            e[1].record()
+            csa2.csa2_topk(scores, w.topk, idx, row_len, d_status=st, workspace=ws_topk, group_max=gmax)
+            e[2].record()
+            csa2.csa2_sparse_attn(aargs, out, lse, st, workspace=ws_attn)
+            e[3].record()
+            e[3].synchronize()
+            if it >= 2:
+                for k, (a, b) in zip(["index_score", "topk", "sparse_attn", "chunk"],
+                                     [(0, 1), (1, 2), (2, 3), (0, 3)]):
+                    per[k].append(e[a].elapsed_time(e[b]))
+        if int(st.item()) != 0:
+            raise RuntimeError(f"device status {int(st.item())}")
+        med = {k: statistics.median(v) for k, v in per.items()}
+        attn_flop = 2.0 * B * T * w.heads * (w.topk + w.window) * (w.d_qk + w.d_v)
+        chunk = {"layer": "encoder Full layer at ratio 2: indexer, Top-512, attention (512 + SWA 128)",
+                 "ms": med["chunk"], "tokens_per_s": B * T / (med["chunk"] * 1e-3),
+                 "ms_per_call": {k: med[k] for k in ("index_score", "topk", "sparse_attn")},
+                 "attn_tflops": attn_flop / (med["sparse_attn"] * 1e-3) / 1e12,
+                 "launches": 3}
     pairs = int(row_len.sum().item())
     flop = 2.0 * pairs * w.idx_heads * w.idx_dim
     tf = flop / (t * 1e-3) / 1e12
@@ -604,12 +650,15 @@ def prefill_indexer(dev, sm_mhz):
     fp4_peak = 6.0 * bf16
     mhz = sm_mhz or 2070.0
     alu_tf = 152 * 128 * mhz * 1e6 / 2 * (2 * w.idx_dim) / 1e12
-    return {"workload": PREFILL_WORKLOAD, "queries": B * T, "positions": w.n_keys,
-            "visible_pairs": pairs, "ms": t, "achieved": tf, "unit": "TFLOP/s",
+    res = {"workload": PREFILL_WORKLOAD, "queries": B * T, "positions": w.n_keys,
+           "visible_pairs": pairs, "ms": t, "achieved": tf, "unit": "TFLOP/s",
             "fp4_peak": fp4_peak,
             "fp4_peak_kind": ("measured bf16 x 6" if "bf16_tflops" in d else "fallback bf16 x 6"),
-            "frac_fp4": tf / fp4_peak, "alu_peak": alu_tf, "frac_alu": tf / alu_tf,
-            "l2": "flushed between timed launches (write + read of 256 MiB)"}
+           "frac_fp4": tf / fp4_peak, "alu_peak": alu_tf, "frac_alu": tf / alu_tf,
+           "l2": "flushed between timed launches (write + read of 256 MiB)"}
+    if chunk is not None:
+        res["chunk"] = chunk
+    return res
 
 
 def main():
@@ -631,7 +680,7 @@ def main():
     if args.prefill_only:
         import torch
         torch.cuda.set_device(0)
-        print(json.dumps({"prefill_indexer": prefill_indexer(torch.device("cuda", 0), None)}))
+        print(json.dumps({"prefill_indexer": prefill_indexer(torch.device("cuda", 0), None, with_chunk=False)}))
         return 0
     if args.impl == "reference":
         return run_reference(args)

@@ -354,54 +354,66 @@ def run_gpu(args):
     ms_step = sum(ms_steps) / len(ms_steps)
     ms_k = per_kernel["index_score"]
 
-    # ---- end to end through the public API from pinned host buffers.  The attention query
-    #      is only needed by the last call, so its copy runs on a second stream while the
-    #      cache write, the indexer and Top-K run (as a serving loop would pipeline it): the
-    #      step is replayed as two graphs, the attention one after the copy's event.
-    def step_front():
-        csa2.csa2_rope_quant_fp4(cache_rows, st, jobs=cache_jobs)
-        csa2.csa2_index_score(iargs, scores, row_len, st, workspace=ws_index)
-        csa2.csa2_topk(scores, w.topk, idx, row_len, d_status=st, workspace=ws_topk, group_max=gmax)
-
-    def step_attn():
-        csa2.csa2_sparse_attn(aargs, out, lse, st, workspace=ws_attn)
-
-    g_front, g_attn = None, None
-    if graph is not None:
-        g_front, g_attn = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g_front):
-            step_front()
-        with torch.cuda.graph(g_attn):
-            step_attn()
-    copy_stream = torch.cuda.Stream(dev)
-    h_qi = dw["q_idx"].cpu().pin_memory()
-    h_w = dw["w_idx"].cpu().pin_memory()
+    # ---- end to end through the public API from pinned host buffers: every step uploads
+    #      its inputs (the indexer query and head weights as one packed copy, the attention
+    #      query on a second branch, since only the last call needs it), runs the four calls
+    #      and downloads the attention output.  The whole sequence is one CUDA graph (copy
+    #      nodes and kernels), so host launch gaps stay out of it; eager calls otherwise.
+    n_qi = dw["q_idx"].numel() * 2
+    n_w = dw["w_idx"].numel() * 4
+    d_in = torch.empty(n_qi + n_w, dtype=torch.uint8, device=dev)      # packed inputs
+    e_qi = d_in[:n_qi].view(torch.bfloat16).view(dw["q_idx"].shape)
+    e_w = d_in[n_qi:].view(torch.float32).view(dw["w_idx"].shape)
+    h_in = torch.empty(n_qi + n_w, dtype=torch.uint8).pin_memory()
+    h_in[:n_qi].copy_(dw["q_idx"].cpu().view(torch.uint8).reshape(-1))
+    h_in[n_qi:].copy_(dw["w_idx"].cpu().view(torch.uint8).reshape(-1))
+    iargs_e2e = csa2.make_index_args(e_qi, e_w, dw["k_codes"], dw["k_scales"], dw["q_pos"], w.ratio_m,
+                                     group_max=gmax)
     h_qa = dw["q_attn"].cpu().pin_memory()
     h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h2d = h_qi.numel() * 2 + h_w.numel() * 4 + h_qa.numel() * 2
+    h2d = h_in.numel() + h_qa.numel() * 2
     d2h = h_out.numel() * 2
+    copy_stream = torch.cuda.Stream(dev)
+
+    def e2e_step_calls():
+        cs = torch.cuda.current_stream(dev)
+        fork = torch.cuda.Event()
+        fork.record(cs)
+        copy_stream.wait_event(fork)
+        with torch.cuda.stream(copy_stream):
+            dw["q_attn"].copy_(h_qa, non_blocking=True)
+        qa_done = torch.cuda.Event()
+        qa_done.record(copy_stream)
+        d_in.copy_(h_in, non_blocking=True)
+        csa2.csa2_rope_quant_fp4(cache_rows, st, jobs=cache_jobs)
+        csa2.csa2_index_score(iargs_e2e, scores, row_len, st, workspace=ws_index)
+        csa2.csa2_topk(scores, w.topk, idx, row_len, d_status=st, workspace=ws_topk, group_max=gmax)
+        cs.wait_event(qa_done)
+        csa2.csa2_sparse_attn(aargs, out, lse, st, workspace=ws_attn)
+        h_out.copy_(out, non_blocking=True)
+
+    g_e2e = None
+    if graph is not None:
+        try:
+            for _ in range(2):
+                e2e_step_calls()
+            torch.cuda.synchronize(dev)
+            g_e2e = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_e2e):
+                e2e_step_calls()
+        except (TypeError, RuntimeError) as exc:
+            g_e2e = None
+            torch.cuda.synchronize(dev)
+            print(f"# end-to-end graph capture unavailable ({exc}); eager calls", file=sys.stderr)
     e2e_ms = []
     for it in range(args.steps + 2):
         flush()
         e0, e1 = ev(), ev()
         e0.record(stream)
-        copy_stream.wait_event(e0)
-        with torch.cuda.stream(copy_stream):
-            dw["q_attn"].copy_(h_qa, non_blocking=True)
-        qa_done = torch.cuda.Event()
-        qa_done.record(copy_stream)
-        dw["q_idx"].copy_(h_qi, non_blocking=True)
-        dw["w_idx"].copy_(h_w, non_blocking=True)
-        if g_front is not None:
-            g_front.replay()
+        if g_e2e is not None:
+            g_e2e.replay()
         else:
-            step_front()
-        stream.wait_event(qa_done)
-        if g_attn is not None:
-            g_attn.replay()
-        else:
-            step_attn()
-        h_out.copy_(out, non_blocking=True)
+            e2e_step_calls()
         e1.record(stream)
         e1.synchronize()
         if it >= 2:
@@ -542,8 +554,10 @@ def run_gpu(args):
                      "algorithmic_bytes": kb, "ms": ms_k},
         "e2e": {"value": tokens / (e2e_step * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_step,
-                "copies": "pinned host buffers; the attention query uploads on a second stream "
-                          "while the cache write, indexer and Top-K run"},
+                "copies": "pinned host buffers; indexer query + head weights in one upload, the "
+                          "attention query uploads on a second branch while the cache write, "
+                          "indexer and Top-K run; output downloaded; "
+                          + ("one CUDA graph per step" if g_e2e is not None else "eager calls")},
         "kernels_ms": per_kernel,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks.summary(),

@@ -3,7 +3,8 @@
 Default workload: Full-mode decode layer, batch 32, 65,536 global positions per sequence,
 indexer 32 heads x 128 (MXFP4 K), main KV 512 + 64 dims (MXFP4), 64 heads, Top-512,
 SWA 128 (bf16).  One step = the whole path for one new token per sequence:
-  csa2_quant_fp4_batch (write the token's main-KV and indexer-K rows into the caches)
+  csa2_rope_quant_fp4 (write the token's main-KV row, after RoPE on its 64 trailing channels,
+                       and its indexer-K row into the caches: one launch)
   csa2_index_score (indexer query quantised inside; every visible position scored)
   csa2_topk        (Top-512, ascending)
   csa2_sparse_attn (gather + dequantise 512 entries, + 128 SWA keys, 64-head attention)
@@ -13,9 +14,10 @@ metric: decode tokens/s per layer (batch / step time); roofline of the dominant 
   python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--no-prefill]
 Under torchrun each rank runs its own replica (the path has no exchange step).
 Rank 0 also times the prefill indexer on an encoder chunk (4,096 queries after 65,536
-entries at ratio 2) and reports it beside the decode line as "prefill_indexer", and one
-decoder group (the Full layer's step, then 3 Reuse layers attending its Top-K) as
-"decoder_group".
+entries at ratio 2) and the whole chunk (indexer, Top-512, attention), reported beside the
+decode line as "prefill_indexer"; one decoder group (the Full layer's step, then 3 Reuse
+layers attending its Top-K) as "decoder_group"; and the step over the report's E2M1 +
+E4M3/16 main-KV cache as "main_kv_e4m3_16".
 """
 from __future__ import annotations
 
@@ -199,6 +201,23 @@ def run_reference(args):
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
     return 0
+
+
+# ------------------------------------------------------------------ ranks
+def max_over_ranks(dist, values, device):
+    """Each timing's maximum over the ranks (every rank runs its own replica of the step
+    between barriers, so the job is as fast as its slowest rank); no reduction alone."""
+    if dist is None:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_throughput(units_per_rank, world, ms):
+    """Whole-job units per second: `world` ranks each process units_per_rank in ms."""
+    return units_per_rank * world / (ms * 1e-3)
 
 
 # ------------------------------------------------------------------ GPU arm
@@ -522,10 +541,7 @@ def run_gpu(args):
                                                                                   512, w.idx_dim)}
 
     # ---- max over ranks
-    if dist:
-        t = torch.tensor([ms_step, ms_k, e2e_step], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step, ms_k, e2e_step = t.tolist()
+    ms_step, ms_k, e2e_step = max_over_ranks(dist, [ms_step, ms_k, e2e_step], dev)
     if rank != 0:
         if dist:
             dist.destroy_process_group()
@@ -534,9 +550,8 @@ def run_gpu(args):
     peak, peak_kind = _peaks()
     kb = _kernel_bytes(w)
     achieved = kb / (ms_k * 1e-3) / 1e9
-    tokens = B * T * world
     line = {
-        "metric": METRIC, "value": tokens / (ms_step * 1e-3), "unit": "tokens/s",
+        "metric": METRIC, "value": job_throughput(B * T, world, ms_step), "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp4-e2m1/f32",
         "data": "synthetic (seeded N(0,1) caches quantised to MXFP4, U(0,1) head weights, 1% planted)",
@@ -552,7 +567,7 @@ def run_gpu(args):
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": INDEX_TRAFFIC_BYTES,
                      "algorithmic_bytes": kb, "ms": ms_k},
-        "e2e": {"value": tokens / (e2e_step * 1e-3), "unit": "tokens/s",
+        "e2e": {"value": job_throughput(B * T, world, e2e_step), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_step,
                 "copies": "pinned host buffers; indexer query + head weights in one upload, the "
                           "attention query uploads on a second branch while the cache write, "

@@ -122,6 +122,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
             lib.csa2_sparse_attn_workspace_size.argtypes = [ctypes.POINTER(AttnArgs)]
             lib.csa2_sparse_attn.restype = S
             lib.csa2_sparse_attn.argtypes = [ctypes.POINTER(AttnArgs), _P, _P, _P, sz, _P, _P]
+            lib.csa2_selftest_bounded_wait.restype = S
+            lib.csa2_selftest_bounded_wait.argtypes = [ctypes.c_uint32, _P, _P]
             lib.csa2_index_score_noalloc.restype = S
             lib.csa2_index_score_noalloc.argtypes = [ctypes.POINTER(IndexArgs), _P, _P, _P, _P]
             _lib = lib
@@ -309,6 +311,13 @@ def csa2_index_score_noalloc(args: IndexArgs, scores: torch.Tensor, row_len: tor
     device array (for callers that cannot allocate; see include/csa2.h)."""
     _check("csa2_index_score_noalloc", load().csa2_index_score_noalloc(
         ctypes.byref(args), _ptr(scores), _ptr(row_len), _ptr(d_status), _stream(stream)))
+
+
+def csa2_selftest_bounded_wait(polls: int, d_status: torch.Tensor, stream=None):
+    """One CTA waits `polls` polls on an mbarrier nothing completes; *d_status must then
+    hold DEV_TIMEOUT (the bounded-wait check of include/csa2.h)."""
+    _check("csa2_selftest_bounded_wait", load().csa2_selftest_bounded_wait(polls, _ptr(d_status),
+                                                                           _stream(stream)))
 
 
 def csa2_topk(scores: torch.Tensor, k: int, idx: torch.Tensor, row_len=None, pool_blocks=None,

@@ -273,4 +273,10 @@ csa2_status csa2_sparse_attn(const csa2_attn_args *a, uint16_t *out, float *lse,
     return from_cuda(launch_sparse_attn(*a, out, lse, ws, d_status, as_stream(stream)));
 }
 
+csa2_status csa2_selftest_bounded_wait(uint32_t polls, uint32_t *d_status, csa2_stream stream)
+{
+    if (polls < 1 || polls > (1u << 20) || !d_status) return CSA2_ERR_INVALID_ARG;
+    return from_cuda(launch_bounded_wait_selftest(polls, d_status, as_stream(stream)));
+}
+
 } // extern "C"

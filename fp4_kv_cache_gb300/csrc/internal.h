@@ -79,6 +79,9 @@ cudaError_t launch_attn_tc(const csa2_attn_args &a, uint16_t *out, float *lse, v
 cudaError_t launch_sparse_attn(const csa2_attn_args &a, uint16_t *out, float *lse, void *ws,
                                uint32_t *d_status, cudaStream_t s);
 
+// Self-test of the bounded device waits (csa2_selftest_bounded_wait).
+cudaError_t launch_bounded_wait_selftest(uint32_t polls, uint32_t *d_status, cudaStream_t s);
+
 // Launch with programmatic dependent launch: the kernel may start while the previous kernel
 // in the stream is still running, and must execute griddepcontrol.wait (pdl_wait) before it
 // reads anything that kernel writes.  cluster_x > 1 also groups consecutive CTAs along x

@@ -50,14 +50,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
 // Bounded wait for the phase with the given parity; false on timeout or abort.
 // The poll loops stay rolled: unrolled, each inlined wait would grow into hundreds of
 // polls of straight-line code and crowd the instruction cache of the loops around it.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const volatile int *abort)
+__device__ __forceinline__ bool mbar_wait_limit(uint64_t *bar, uint32_t parity, const volatile int *abort,
+                                                uint32_t polls)
 {
 #pragma unroll 1
-    for (uint32_t i = 0; i < kSpinLimit; ++i) {
+    for (uint32_t i = 0; i < polls; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 255u) == 255u && *abort) return false;
     }
     return false;
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const volatile int *abort)
+{
+    return mbar_wait_limit(bar, parity, abort, kSpinLimit);
 }
 
 // Bounded wait without an abort flag (used while draining after an abort).

@@ -334,6 +334,21 @@ CSA2_API csa2_status csa2_index_score_noalloc(const csa2_index_args *a, float *s
                                               int32_t *row_len, uint32_t *d_status,
                                               csa2_stream stream);
 
+/* ---------------------------------------------------------------------------------- */
+/* csa2_selftest_bounded_wait -- failure-detection self-test.  The pages have no        */
+/* counterpart; it checks a property of this library.                                 */
+/*                                                                                    */
+/* Every device wait of the library's kernels (an mbarrier phase completed by a copy, */
+/* an MMA commit or another warp) is bounded: after its poll limit it gives up, the     */
+/* kernel ORs CSA2_DEV_TIMEOUT into *d_status and returns, so a lost arrival ends the   */
+/* kernel instead of hanging the GPU, and the context stays usable.  This call launches */
+/* one CTA whose threads wait, through the same routine with a limit of `polls` polls   */
+/* (1 .. 2^20; each poll may suspend the thread for a short, hardware-defined time),    */
+/* on an mbarrier that nothing ever arrives on; it must leave CSA2_DEV_TIMEOUT in       */
+/* *d_status (device memory, required).  Nothing else is read or written.              */
+/* ---------------------------------------------------------------------------------- */
+CSA2_API csa2_status csa2_selftest_bounded_wait(uint32_t polls, uint32_t *d_status, csa2_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -28,7 +28,7 @@ def lib():
 
 def test_exports_every_declared_symbol(lib):
     syms = _declared_symbols()
-    assert len(syms) == 16
+    assert len(syms) == 17
     for s in syms:
         assert hasattr(lib, s), s
     out = os.popen(f"nm -D --defined-only {libbuild.LIB}").read()
@@ -129,6 +129,12 @@ def test_rope_quant_rejects_bad_args(lib):
     assert f(None, 1, None, None) == 1
     assert f(None, 0, None, None) == 0                             # nothing to do
     assert f(job(rows=0), 1, None, None) == 0                      # zero rows: no launch
+
+
+def test_selftest_rejects_bad_args(lib):
+    assert lib.csa2_selftest_bounded_wait(0, FAKE, None) == 1                  # no polls
+    assert lib.csa2_selftest_bounded_wait((1 << 20) + 1, FAKE, None) == 1      # too many
+    assert lib.csa2_selftest_bounded_wait(16, None, None) == 1                 # status required
 
 
 def test_index_rejects_bad_args(lib):

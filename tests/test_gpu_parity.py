@@ -523,3 +523,27 @@ def test_attention_bad_index_and_empty():
     assert torch.all(out[1] == 0) and torch.all(torch.isneginf(lse[1]))
     o_ref, l_ref = _oracle_attention(w.scaled(window=0), [0], np.where(idx >= 600, -1, idx), [0])
     _attn_check(out[0, 0].float().cpu().numpy(), lse[0, 0].cpu().numpy(), o_ref[(0, 0)], l_ref[(0, 0)])
+
+
+# ------------------------------------------------------------------ failure detection
+def test_bounded_wait_gives_up_and_context_survives():
+    # no fault involved: one CTA waits, through the kernels' own bounded-wait routine, on an
+    # mbarrier that nothing completes; the wait must end after its poll limit with
+    # CSA2_DEV_TIMEOUT, and the next call on the stream must run normally
+    st = status()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    csa2.csa2_selftest_bounded_wait(1024, st)
+    e1.record()
+    torch.cuda.synchronize()
+    assert int(st.item()) & csa2.DEV_TIMEOUT
+    ms = e0.elapsed_time(e1)
+    print(f"1,024 polls of an mbarrier that never completes: {ms:.3f} ms")
+    assert ms < 5000.0
+    raw, x = _codec_inputs(64, 64, 5, True)
+    st2 = status()
+    codes, scales = csa2.quant_fp4(workload.bf16_tensor(raw, DEV), st2)
+    c_ref, s_ref = oracle.quant_mxfp4(x)
+    torch.cuda.synchronize()
+    assert int(st2.item()) == 0
+    assert np.array_equal(codes.cpu().numpy(), c_ref) and np.array_equal(scales.cpu().numpy(), s_ref)

@@ -1,9 +1,11 @@
 // tc_util.cuh -- inline-PTX wrappers for sm_103a: mbarriers, TMA, cp.async and tcgen05
 // (tensor memory allocation, tcgen05.cp / tcgen05.mma / tcgen05.commit / tcgen05.ld).
 //
-// Every wait here is bounded: mbar_wait gives up after kSpinLimit polls (about a second or
-// more of wall time) and reports failure, so a kernel can raise CSA2_DEV_TIMEOUT and
-// return instead of hanging.
+// Every wait here is bounded: mbar_wait gives up after kSpinLimit polls and reports
+// failure, so a kernel can raise CSA2_DEV_TIMEOUT and return instead of hanging.  A poll
+// of a phase that does not complete suspends the thread for about 5 us on GB300 (1,024
+// polls took 5.3 ms in csa2_selftest_bounded_wait), so 2^18 polls give up after about
+// 1.4 s -- far beyond any wait of these kernels, which complete in microseconds.
 #pragma once
 
 #include <cuda.h>
@@ -13,7 +15,7 @@
 namespace csa2 {
 namespace tc {
 
-constexpr uint32_t kSpinLimit = 1u << 26;
+constexpr uint32_t kSpinLimit = 1u << 18;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
 {

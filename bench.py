@@ -90,6 +90,43 @@ def _step_bytes(w):
     return idx_bytes + attn + write
 
 
+def _bf16_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        return float(json.load(open(p)).get("bf16_tflops", 1900.0))
+    return 1900.0
+
+
+def kernel_rooflines(w, per_kernel_ms, peak_gbs, bf16_tflops):
+    """Per-call roofline of each kernel of the step: its algorithmic bytes per call (and,
+    for attention, its MMA flops) over its event-timed duration.  Cache write: both bf16 rows
+    in, codes and scales out, the RoPE table row; indexer: _kernel_bytes; Top-K: the group
+    keys in and the indices out (the few surviving groups' scores it also reads depend on
+    the data and are left out); attention: as in _step_bytes."""
+    kv_row = w.d_qk // 2 + w.d_qk // 32
+    rows = w.batch * w.n_q
+    algo = {
+        "cache_write": w.batch * (w.d_qk * 2 + kv_row + w.idx_dim * 2 + w.idx_dim // 2
+                                  + w.idx_dim // 32 + 64 * 4),
+        "index_score": _kernel_bytes(w),
+        "topk": rows * (((w.n_keys + 31) // 32) * 4 + w.topk * 4),
+        "sparse_attn": rows * (w.topk * (kv_row + 4) + w.window * w.d_qk * 2
+                               + w.heads * w.d_qk * 2 + w.heads * w.d_v * 2),
+    }
+    out = {}
+    for name, ms in per_kernel_ms.items():
+        if name not in algo or not ms:
+            continue
+        gbs = algo[name] / (ms * 1e-3) / 1e9
+        out[name] = {"bytes": algo[name], "ms": ms, "gbs": gbs, "frac_hbm": gbs / peak_gbs}
+    if "sparse_attn" in out:
+        flop = 2.0 * rows * w.heads * (w.topk + w.window) * (w.d_qk + w.d_v)
+        tf = flop / (per_kernel_ms["sparse_attn"] * 1e-3) / 1e12
+        out["sparse_attn"]["tflops"] = tf
+        out["sparse_attn"]["frac_bf16"] = tf / bf16_tflops
+    return out
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
 
@@ -574,6 +611,7 @@ def run_gpu(args):
                           "indexer and Top-K run; output downloaded; "
                           + ("one CUDA graph per step" if g_e2e is not None else "eager calls")},
         "kernels_ms": per_kernel,
+        "kernels_roofline": kernel_rooflines(w, per_kernel, peak, _bf16_peak()),
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks.summary(),
     }

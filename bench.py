@@ -230,8 +230,10 @@ def run_reference(args):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1000 * sum(times) / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "global_batch": 1, "seq_len": w.n_keys,
-                       "parallelism": "cpu-oracle"},
+            "config": {"workload": WORKLOAD, "global_batch": w.batch, "seq_len": w.n_keys,
+                       "parallelism": "cpu-oracle (one sampled sequence per step)",
+                       "topk": w.topk, "window": w.window, "indexer": f"{w.idx_heads}x{w.idx_dim}",
+                       "heads": w.heads, "d_qk": w.d_qk, "d_v": w.d_v},
             "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0,

@@ -22,7 +22,8 @@ from . import csa2
 
 @dataclass
 class Cache:
-    """One source layer's shared global cache (main KV + indexer K), MXFP4 planes."""
+    """One source layer's shared global cache: the main KV (MXFP4, or the report's E2M1 +
+    E4M3/16 -- told apart by the width of kv_scales) and the MXFP4 indexer K."""
     kv_codes: torch.Tensor      # uint8 [B, N, d_qk/2]
     kv_scales: torch.Tensor     # uint8 [B, N, d_qk/32] (MXFP4) or [B, N, d_qk/16] (E2M1 + E4M3/16)
     k_codes: torch.Tensor       # uint8 [B, N, d_i/2]

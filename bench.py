@@ -623,6 +623,11 @@ def run_gpu(args):
         line["main_kv_e4m3_16"] = nv
     if not args.no_prefill:
         line["prefill_indexer"] = prefill_indexer(dev, line["clocks"].get("sm_mhz"))
+    if not args.no_indexer_rows:
+        try:
+            line["indexer_rows"] = indexer_rows(dev)
+        except Exception as exc:          # reported, not fatal: the decode line stands
+            line["indexer_rows"] = {"error": f"{type(exc).__name__}: {exc}"}
     if not args.no_cpu_baseline:
         import oracle
         dt, tok = oracle_sample(w, [0, 1])
@@ -634,6 +639,124 @@ def run_gpu(args):
     if dist:
         dist.destroy_process_group()
     return 0
+
+
+def indexer_rows(dev):
+    """The indexer steps the decode line does not time, on their own workloads: the Reindex
+    layer's scoring of its block pool (2,048 blocks of 8 per sequence, batch 64, 128K context)
+    with its Top-512 inside the pool, and the decoder's hierarchical indexer at 1M context
+    (batch 4: every causal position scored, Top-512, Top-2,048 blocks of 8).  Each call is
+    timed alone after an L2 flush (median of 7); the indexer against the HBM copy rate with
+    68 B per scored position plus the pool ids, query and head weights."""
+    import ctypes
+    import torch
+    from fp4_kv_cache_gb300 import csa2, workload
+    lib = csa2.load()
+    peak, _ = _peaks()
+    flush = L2Flush(dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def timed(fn):
+        ts = []
+        for it in range(10):
+            flush()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            e1.synchronize()
+            if it >= 3:
+                ts.append(e0.elapsed_time(e1))
+        return statistics.median(ts)
+
+    res = {}
+    # ---- Reindex: pool scoring + Top-512 within the pool
+    w = synth.WORKLOADS["reuse_reindex_decode_128k"]
+    dw = workload.build(w, device=dev, kv=False, d_status=st)
+    B, T = w.batch, w.n_q
+    pool = dw["pool"]
+    n_cand = pool.shape[-1] * w.block
+    scores = torch.empty((B, T, n_cand), dtype=torch.float32, device=dev)
+    row_len = torch.empty((B, T), dtype=torch.int32, device=dev)
+    gmax = csa2.group_max_buffer(scores)
+    idx = torch.empty((B, T, w.topk), dtype=torch.int32, device=dev)
+    iargs = csa2.make_index_args(dw["q_idx"], dw["w_idx"], dw["k_codes"], dw["k_scales"], dw["q_pos"],
+                                 w.ratio_m, pool, w.block, gmax)
+    ws_i = torch.zeros(max(1, lib.csa2_index_score_workspace_size(ctypes.byref(iargs))),
+                       dtype=torch.uint8, device=dev)
+    ws_t = torch.empty(max(1, lib.csa2_topk_workspace_size(B * T, n_cand, w.topk)), dtype=torch.uint8,
+                       device=dev)
+
+    def score():
+        csa2.csa2_index_score(iargs, scores, row_len, st, workspace=ws_i)
+
+    def select():
+        csa2.csa2_topk(scores, w.topk, idx, row_len, pool, w.block, d_status=st, workspace=ws_t,
+                       group_max=gmax)
+
+    def chain():
+        score()
+        select()
+
+    chain()
+    t_score, t_select, t_chain = timed(score), timed(select), timed(chain)
+    torch.cuda.synchronize(dev)
+    if int(st.item()) != 0:
+        raise RuntimeError(f"device status {int(st.item())}")
+    scored = int(row_len.sum().item())
+    ib = scored * 68 + B * T * (pool.shape[-1] * 4 + w.idx_heads * (w.idx_dim * 2 + 4))
+    res["reindex_pool_128k"] = {
+        "workload": w.name, "batch": B, "context": w.n_keys, "pool_positions": n_cand,
+        "positions_scored": scored, "index_score_ms": t_score, "index_bytes": ib,
+        "index_gbs": ib / (t_score * 1e-3) / 1e9, "index_frac_hbm": ib / (t_score * 1e-3) / 1e9 / peak,
+        "topk_ms": t_select, "ms": t_chain, "tokens_per_s": B * T / (t_chain * 1e-3)}
+    del dw, scores, row_len, gmax, idx, ws_i, ws_t, iargs
+    torch.cuda.empty_cache()
+
+    # ---- decoder's hierarchical indexer at 1M: scores, Top-512, Top-2,048 blocks
+    w = synth.WORKLOADS["hier_indexer_1m"]
+    dw = workload.build(w, device=dev, kv=False, d_status=st)
+    B, T = w.batch, w.n_q
+    scores = torch.empty((B, T, w.n_keys), dtype=torch.float32, device=dev)
+    row_len = torch.empty((B, T), dtype=torch.int32, device=dev)
+    gmax = csa2.group_max_buffer(scores)
+    idx = torch.empty((B, T, w.topk), dtype=torch.int32, device=dev)
+    blocks = torch.empty((B, T, w.n_blocks), dtype=torch.int32, device=dev)
+    iargs = csa2.make_index_args(dw["q_idx"], dw["w_idx"], dw["k_codes"], dw["k_scales"], dw["q_pos"],
+                                 w.ratio_m, None, w.block, gmax)
+    ws_i = torch.zeros(max(1, lib.csa2_index_score_workspace_size(ctypes.byref(iargs))),
+                       dtype=torch.uint8, device=dev)
+    ws_t = torch.empty(max(1, lib.csa2_topk_workspace_size(B * T, w.n_keys, w.topk)), dtype=torch.uint8,
+                       device=dev)
+    ws_b = torch.empty(max(1, lib.csa2_block_candidates_workspace_size(B * T, w.n_keys, w.block, w.n_blocks)),
+                       dtype=torch.uint8, device=dev)
+
+    def score1m():
+        csa2.csa2_index_score(iargs, scores, row_len, st, workspace=ws_i)
+
+    def select1m():
+        csa2.csa2_topk(scores, w.topk, idx, row_len, d_status=st, workspace=ws_t, group_max=gmax)
+
+    def blocks1m():
+        csa2.csa2_block_candidates(scores, w.n_blocks, blocks, row_len, w.block, st, workspace=ws_b)
+
+    def chain1m():
+        score1m()
+        select1m()
+        blocks1m()
+
+    chain1m()
+    t_score, t_select, t_blocks, t_chain = timed(score1m), timed(select1m), timed(blocks1m), timed(chain1m)
+    torch.cuda.synchronize(dev)
+    if int(st.item()) != 0:
+        raise RuntimeError(f"device status {int(st.item())}")
+    ib = _kernel_bytes(w)
+    res["hier_indexer_1m"] = {
+        "workload": w.name, "batch": B, "context": w.n_keys, "index_score_ms": t_score,
+        "index_bytes": ib, "index_gbs": ib / (t_score * 1e-3) / 1e9,
+        "index_frac_hbm": ib / (t_score * 1e-3) / 1e9 / peak, "topk_ms": t_select,
+        "block_candidates_ms": t_blocks, "ms": t_chain, "tokens_per_s": B * T / (t_chain * 1e-3)}
+    return res
 
 
 PREFILL_WORKLOAD = "prefill_chunk_m2"
@@ -739,6 +862,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-group", action="store_true")
+    ap.add_argument("--no-indexer-rows", action="store_true",
+                    help="skip timing the Reindex pool scoring (128K) and the 1M hierarchical indexer")
+    ap.add_argument("--indexer-rows-only", action="store_true",
+                    help="time only those and print their object")
     ap.add_argument("--no-nvfp4", action="store_true",
                     help="skip the step over the E2M1 + E4M3/16 main-KV cache")
     ap.add_argument("--prefill-only", action="store_true",
@@ -750,6 +877,11 @@ def main():
         import torch
         torch.cuda.set_device(0)
         print(json.dumps({"prefill_indexer": prefill_indexer(torch.device("cuda", 0), None, with_chunk=False)}))
+        return 0
+    if args.indexer_rows_only:
+        import torch
+        torch.cuda.set_device(0)
+        print(json.dumps({"indexer_rows": indexer_rows(torch.device("cuda", 0))}))
         return 0
     if args.impl == "reference":
         return run_reference(args)

@@ -16,8 +16,11 @@ Under torchrun each rank runs its own replica (the path has no exchange step).
 Rank 0 also times the prefill indexer on an encoder chunk (4,096 queries after 65,536
 entries at ratio 2) and the whole chunk (indexer, Top-512, attention), reported beside the
 decode line as "prefill_indexer"; one decoder group (the Full layer's step, then 3 Reuse
-layers attending its Top-K) as "decoder_group"; and the step over the report's E2M1 +
-E4M3/16 main-KV cache as "main_kv_e4m3_16".
+layers attending its Top-K) as "decoder_group"; the step over the report's E2M1 +
+E4M3/16 main-KV cache as "main_kv_e4m3_16"; and the indexer steps the decode step does not
+exercise -- the Reindex layer's pool scoring at 128K and the decoder's hierarchical indexer
+at 1M (scores, Top-512, Top-2,048 blocks) -- as "indexer_rows".  Every kernel's own roofline
+is in "kernels_roofline".
 """
 from __future__ import annotations
 

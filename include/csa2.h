@@ -60,7 +60,7 @@ typedef void *csa2_stream; /* a cudaStream_t */
 typedef enum {
     CSA2_OK = 0,
     CSA2_ERR_INVALID_ARG = 1, /* shape, pointer, alignment or enum out of range */
-    CSA2_ERR_UNSUPPORTED = 2, /* valid request this build does not implement     */
+    CSA2_ERR_UNSUPPORTED = 2, /* valid request the library does not implement    */
     CSA2_ERR_CUDA = 3,        /* a CUDA launch or attribute call failed          */
     CSA2_ERR_WORKSPACE = 4    /* ws_bytes below the *_workspace_size() value     */
 } csa2_status;

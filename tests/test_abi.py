@@ -56,7 +56,7 @@ def test_cache_byte_ledger(lib):
     assert per_pos * 3 // 2 + per_pos == g["per_token_total"]
     assert 448 * 6 == g["nvfp4_no_global_scale_max"]
     assert 2048 * 8 == g["pool_max_positions"]
-    # this build's MXFP4 main KV at 512 + 64 dims: 288 + 18 bytes, plus the 68-byte key
+    # the default MXFP4 main KV at 512 + 64 dims: 288 + 18 bytes, plus the 68-byte key
     assert csa2.cache_bytes_per_position(csa2.FMT_MXFP4, 576, 128) == 288 + 18 + 64 + 4
     assert csa2.cache_bytes_per_position(csa2.FMT_MXFP4, 500, 128) == 0
     # the report's main-KV format at 512 + 64 dims: 288 + 36 bytes, plus the key

@@ -109,3 +109,25 @@ def test_rope_quant_is_quant_of_rotated(fmt):
     c3, s3 = oracle.quant_main_kv(x.astype(np.float64), fmt)
     nb = (576 - 64) // g
     assert np.array_equal(s[:, :nb], s3[:, :nb]) and np.array_equal(c[:, : nb * g // 2], c3[:, : nb * g // 2])
+
+
+def test_rounding_rule_against_exact_rationals():
+    # every rotated value is RN32(RN32(a c) -/+ RN32(b s)), evaluated here with exact
+    # rationals and the brute-force float32 rounding of oracle/tiny.py
+    from fractions import Fraction
+    from oracle import tiny
+    rng = np.random.default_rng(9)
+    R, cols, n = 8, 24, 40
+    x = _rows(rng, n, cols) * np.float32(2.0) ** rng.integers(-30, 30, (n, 1)).astype(np.float32)
+    tab = _table(64, R)
+    pos = rng.integers(0, 64, n)
+    y = oracle.rope_rotate(x, pos, tab, R)
+    c0 = cols - R
+    for r in range(n):
+        for i in range(R // 2):
+            a, b = Fraction(float(x[r, c0 + 2 * i])), Fraction(float(x[r, c0 + 2 * i + 1]))
+            c, s = Fraction(float(tab[pos[r], i])), Fraction(float(tab[pos[r], R // 2 + i]))
+            ac, bs = tiny.rn32(a * c), tiny.rn32(b * s)
+            as_, bc = tiny.rn32(a * s), tiny.rn32(b * c)
+            assert y[r, c0 + 2 * i] == tiny.rn32(Fraction(float(ac)) - Fraction(float(bs)))
+            assert y[r, c0 + 2 * i + 1] == tiny.rn32(Fraction(float(as_)) + Fraction(float(bc)))

@@ -4,6 +4,7 @@ anything (none of these calls reach the GPU)."""
 import ctypes
 import os
 import re
+import subprocess
 
 import pytest
 
@@ -193,3 +194,20 @@ def test_layer_schedule_counts():
     assert [i for i, m in enumerate(modes) if m == "reindex"] == [24, 28, 32, 36]
     assert modes.count("reuse") == 30
     assert sum(m != "swa" for m in modes) == 38
+
+
+def test_header_is_plain_c(tmp_path):
+    # the boundary is a C ABI: the header compiles as strict C11 (no C++ or CUDA types), and
+    # its argument structs can be zero-initialised and sized from C
+    src = tmp_path / "use_header.c"
+    src.write_text('#include "csa2.h"\n'
+                   'int main(void) {\n'
+                   '    csa2_index_args i = {0}; csa2_attn_args a = {0};\n'
+                   '    csa2_quant_job q = {0}; csa2_rope_quant_job r = {0};\n'
+                   '    return (int)(sizeof i + sizeof a + sizeof q + sizeof r == 0);\n'
+                   '}\n')
+    out = tmp_path / "use_header.o"
+    r = subprocess.run(["gcc", "-std=c11", "-Wall", "-Wextra", "-pedantic", "-Werror",
+                        "-I", os.path.join(ROOT, "include"), "-c", str(src), "-o", str(out)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr

@@ -1,7 +1,9 @@
 // api.cu -- extern "C" entry points of libcsa2.so (declared in include/csa2.h).
 //
-// Host-side validation happens here, before any launch; the kernels live in quant.cu,
-// index_score.cu, topk.cu and attn.cu.
+// Host-side validation happens here, before any launch; the kernels live in quant.cu (cache
+// codec, RoPE + quantise), index_tc.cu and index_score.cu (indexer), topk.cu (Top-K, block
+// pool), attn_tc.cu and attn.cu (attention) and selftest.cu (bounded-wait check);
+// noalloc.cu holds the indexer entry point that needs no workspace.
 #include <cuda_runtime.h>
 #include <stdint.h>
 

@@ -8,13 +8,16 @@ exact integers, fp64), selection here uses a library sort.
 What it computes, step by step (DeepSeek-V4.1-Flash report, aipaper.jasonlin.tech):
   1. MXFP4 codec for indexer q/k and the main KV (report §2.4.4; OCP MX v1.0 rule);
      the report's own main-KV format, E2M1 + E4M3 per 16 (report §2.4.4), as an option.
-  2. Indexer score of every candidate position, s = sum_h w_h ReLU(q_h . k), with the
-     per-head dot rounded once to float32 and the head sum a float32 fma chain
-     (the kernel's precision, since these floats decide indices).
-  3. Top-K (K = 512, report §4.2.1): full sort by (-score, position); emitted in
+  2. Indexer score of every candidate position, s = sum_h w_h ReLU(q_h . k), exact:
+     the dots of the MXFP4 vectors and the weighted head sum are carried out in wide
+     integers with nothing rounded (``index_scores_exact``).  The float32 scores the
+     library writes out beside its selection (each head dot rounded once to float32,
+     the head sum a float32 fma chain) are reproduced by ``index_scores``.
+  3. Top-K (K = 512, report §4.2.1): full sort by (-exact score, position); emitted in
      ascending position order, padded with -1.
-  4. Hierarchical pool (report §2.3.2): block score = max score of the block's visible
-     positions (8 per block); top 2,048 blocks by (-score, block id); ascending, -1 pad.
+  4. Hierarchical pool (report §2.3.2): block score = max exact score of the block's
+     visible positions (8 per block); top 2,048 blocks by (-score, block id);
+     ascending, -1 pad.
   5. Reindex (report §2.3.2; review page, notes on the official code: scores over the
      full range, then a candidate mask): only pool positions compete.
   6. Core attention in fp64 over the selected main-KV entries (dequantised) followed by
@@ -65,6 +68,9 @@ def _L():
             lib.orc_dequant_nvfp4.argtypes = [P, P, I64, I64, P]
             lib.orc_head_dots.argtypes = [I, I, P, P, P, P, P, I64, P]
             lib.orc_index_scores.argtypes = [I, I, P, P, P, P, P, P, I64, P]
+            lib.orc_index_scores_exact.argtypes = [I, I, P, P, P, P, P, P, I64, P]
+            lib.orc_exact_limbs.restype = I
+            lib.orc_exact_e0.restype = I
             lib.orc_attention.argtypes = [I64, I, I, I, P, P, P, ctypes.c_double, P, P]
             lib.orc_num_threads.restype = I
             _lib = lib
@@ -196,6 +202,103 @@ def index_scores(qc, qs, w, kc, ks, pos) -> np.ndarray:
     return out
 
 
+def exact_format():
+    """(limbs, e0): an exact score is a two's-complement integer of ``limbs`` 32-bit
+    limbs (least significant first) in units of 2^e0."""
+    lib = _L()
+    return int(lib.orc_exact_limbs()), int(lib.orc_exact_e0())
+
+
+def index_scores_exact(qc, qs, w, kc, ks, pos) -> np.ndarray:
+    """Exact indexer scores of one quantised query at key rows ``pos``:
+    s = sum_h w_h * max(0, q_hat_h . k_hat), nothing rounded.  Returns uint32 limbs
+    [npos, limbs] (see ``exact_format``)."""
+    qc = np.ascontiguousarray(qc, np.uint8); qs = np.ascontiguousarray(qs, np.uint8)
+    kc = np.ascontiguousarray(kc, np.uint8); ks = np.ascontiguousarray(ks, np.uint8)
+    w = np.ascontiguousarray(w, np.float32)
+    pos = np.ascontiguousarray(pos, np.int64)
+    H, d = qc.shape[0], qc.shape[1] * 2
+    L, _ = exact_format()
+    out = np.empty((pos.size, L), np.uint32)
+    _L().orc_index_scores_exact(H, d, _p(qc), _p(qs), _p(w), _p(kc), _p(ks), _p(pos), pos.size,
+                                _p(out))
+    return out
+
+
+def exact_int(limbs_row) -> int:
+    """The integer S of one exact score (value = S * 2^e0)."""
+    v = int.from_bytes(np.ascontiguousarray(limbs_row, np.uint32).astype("<u4").tobytes(), "little",
+                       signed=True)
+    return v
+
+
+def exact_fraction(limbs_row):
+    """One exact score as a fractions.Fraction."""
+    from fractions import Fraction
+    _, e0 = exact_format()
+    return Fraction(exact_int(limbs_row)) * Fraction(2) ** e0
+
+
+def _exact_desc_keys(limbs: np.ndarray):
+    """numpy.lexsort keys (least significant first) that sort exact scores in
+    descending order: limbs complemented, the top limb's sign bit flipped first so
+    that unsigned limb order is numeric order.  Limbs equal in every row are left out
+    (they cannot change the order)."""
+    lim = np.array(limbs, dtype=np.uint32, copy=True)
+    if lim.shape[0] == 0:
+        return []
+    lim[:, -1] ^= np.uint32(0x80000000)
+    keys = []
+    for j in range(lim.shape[1]):
+        col = lim[:, j]
+        if np.all(col == col[0]):
+            continue
+        keys.append(~col)
+    return keys
+
+
+def order_exact_desc(limbs: np.ndarray, ids: np.ndarray) -> np.ndarray:
+    """Permutation sorting by (exact score descending, id ascending)."""
+    return np.lexsort(tuple([np.asarray(ids)] + _exact_desc_keys(limbs)))
+
+
+def topk_exact(limbs: np.ndarray, pos: np.ndarray, k: int) -> np.ndarray:
+    """The k best positions by (exact score descending, position ascending); returned
+    ascending, -1 padded."""
+    out = np.full(k, -1, np.int32)
+    if pos.size:
+        sel = np.sort(np.asarray(pos)[order_exact_desc(limbs, pos)[:k]])
+        out[: sel.size] = sel
+    return out
+
+
+def block_max_exact(limbs: np.ndarray, n_vis: int, block: int) -> np.ndarray:
+    """Exact block scores: for block b the largest exact score among its visible
+    positions 8b .. (positions 0..n_vis-1, limbs [n_vis, L]).  Returns limbs [nblk, L]."""
+    nblk = (n_vis + block - 1) // block
+    if nblk == 0:
+        return np.zeros((0, limbs.shape[1]), np.uint32)
+    p = np.arange(n_vis)
+    blk = p // block
+    # within each block, its best position first: sort by (block, exact desc)
+    order = np.lexsort(tuple([p] + _exact_desc_keys(limbs[:n_vis]) + [blk]))
+    first = np.ones(n_vis, bool)
+    first[1:] = blk[order][1:] != blk[order][:-1]
+    return limbs[order[first]]
+
+
+def block_candidates_exact(limbs: np.ndarray, n_vis: int, block: int, nb: int) -> np.ndarray:
+    """Top-nb blocks by (exact block score descending, block id ascending); returned
+    ascending, -1 padded."""
+    out = np.full(nb, -1, np.int32)
+    bl = block_max_exact(limbs, n_vis, block)
+    if bl.shape[0]:
+        ids = np.arange(bl.shape[0])
+        sel = np.sort(ids[order_exact_desc(bl, ids)[:nb]])
+        out[: sel.size] = sel
+    return out
+
+
 def n_visible(q_pos: int, ratio_m: int, n_keys: int) -> int:
     """Entries a query at token position q_pos can see: entry j covers tokens
     [j*m, j*m + m - 1] with no overlap (report §2.3), and only complete entries are
@@ -261,25 +364,30 @@ def quant_query(q_f32: np.ndarray):
 
 
 def full_indexer(q_f32, w, kc, ks, q_pos, ratio_m, k=512, block=8, nb=2048,
-                 want_blocks=False):
-    """Full-mode indexer for one query: scores every visible position, Top-K, and
-    (for the decoder's first Full layer) the block pool."""
+                 want_blocks=False, want_f32=True):
+    """Full-mode indexer for one query: exact score of every visible position, Top-K,
+    and (for the decoder's first Full layer) the block pool.  Returns (idx, blocks,
+    float32 scores or None)."""
     qc, qs = quant_query(q_f32)
     nvis = n_visible(q_pos, ratio_m, kc.shape[0])
     pos = np.arange(nvis, dtype=np.int64)
-    s = index_scores(qc, qs, w, kc, ks, pos)
-    idx = topk(s, pos, k)
-    blocks = block_candidates(s, nvis, block, nb) if want_blocks else None
+    ex = index_scores_exact(qc, qs, w, kc, ks, pos)
+    idx = topk_exact(ex, pos, k)
+    blocks = block_candidates_exact(ex, nvis, block, nb) if want_blocks else None
+    s = index_scores(qc, qs, w, kc, ks, pos) if want_f32 else None
     return idx, blocks, s
 
 
-def reindex_indexer(q_f32, w, kc, ks, q_pos, ratio_m, pool_blocks, k=512, block=8):
-    """Reindex-mode indexer for one query: only positions of the pool compete."""
+def reindex_indexer(q_f32, w, kc, ks, q_pos, ratio_m, pool_blocks, k=512, block=8,
+                    want_f32=True):
+    """Reindex-mode indexer for one query: only positions of the pool compete, ranked
+    by their exact scores.  Returns (idx, float32 scores or None, positions)."""
     qc, qs = quant_query(q_f32)
     nvis = n_visible(q_pos, ratio_m, kc.shape[0])
     pos = pool_positions(np.asarray(pool_blocks), block, nvis)
-    s = index_scores(qc, qs, w, kc, ks, pos)
-    return topk(s, pos, k), s, pos
+    ex = index_scores_exact(qc, qs, w, kc, ks, pos)
+    s = index_scores(qc, qs, w, kc, ks, pos) if want_f32 else None
+    return topk_exact(ex, pos, k), s, pos
 
 
 def swa_keys_range(q_pos: int, swa_pos0: int, n_slots: int, window: int, swa_start: int):

@@ -18,9 +18,11 @@
  * The score formula  s = sum_h w_h * ReLU(q_h . k)  is the one the workload
  * definition states; the pages print none.
  *
- * Precision: everything here is exact or fp64 except where a float32 value decides
- * an index (the indexer score), which is computed in the float32 precision the GPU
- * kernel uses:
+ * Precision: everything here is exact or fp64.  The indexer score that decides the
+ * selection is exact: s = sum_h w_h * max(0, d_h) with d_h the exact dot of the MXFP4
+ * vectors and w_h the exact value of the float32 weight, held as a wide integer
+ * (orc_index_scores_exact).  The float32 scores the library also writes out are
+ * reproduced bit for bit by orc_index_scores:
  *   D_h = RN32(exact q_h . k)          one rounding of the exact dyadic dot
  *   s   = fma32(w_{H-1}, R_{H-1}, ... fma32(w_0, R_0, +0))     R_h = max(D_h, 0)
  * Build: gcc -O2 -std=c11 -fopenmp -ffp-contract=off -shared -fPIC.
@@ -377,6 +379,108 @@ void orc_index_scores(int H, int d, const uint8_t *qc, const uint8_t *qs, const 
             s = fmaf(w[h], R, s);
         }
         out[i] = s;
+    }
+}
+
+/* ------------------------------------------------------------------------- */
+/* Exact indexer score (the selection order):                                 */
+/*   s = sum_h w_h * max(0, d_h),  d_h = q_hat_h . k_hat  (exact dyadic dot)  */
+/* with w_h the exact value of the given float32.  Nothing is rounded: s is   */
+/* returned as a wide two's-complement integer S with s = S * 2^EXACT_E0.     */
+/*                                                                           */
+/* Range.  w_h = m_w * 2^e_w with m_w < 2^24 and e_w in [-149, 104]; a block  */
+/* of the dot is I_b * 2^(Xq + Xk - 2) with |I_b| < 2^13 and Xq, Xk in        */
+/* [-127, 128] (scale bytes 0..255).  Every product term m_w * I_b sits at an */
+/* exponent >= -149 - 254 - 2 = -405 and is below 2^(104 + 255 - 2 + 37) =    */
+/* 2^394; 64 heads x 32 blocks of them stay below 2^405.  26 limbs from      */
+/* 2^-416 hold every such sum together with its sign bit (bit 831).           */
+/* ------------------------------------------------------------------------- */
+#define EXACT_LIMBS 26
+#define EXACT_E0 (-416)
+
+int orc_exact_limbs(void) { return EXACT_LIMBS; }
+int orc_exact_e0(void) { return EXACT_E0; }
+
+/* acc (n limbs, bit 0 of weight 2^e0) += m * 2^e, |m| < 2^63, e >= e0. */
+static void wide_add(uint32_t *acc, int n, int e0, int64_t m, int e)
+{
+    if (m == 0) return;
+    int sh = e - e0;
+    int limb = sh / 32, bit = sh % 32;
+    unsigned __int128 mag = (unsigned __int128)(uint64_t)(m < 0 ? -m : m) << bit;
+    uint32_t part[4] = {(uint32_t)mag, (uint32_t)(mag >> 32), (uint32_t)(mag >> 64), 0u};
+    if (m > 0) {
+        uint64_t carry = 0;
+        for (int i = limb; i < n; ++i) {
+            uint64_t v = (uint64_t)acc[i] + (i - limb < 4 ? part[i - limb] : 0u) + carry;
+            acc[i] = (uint32_t)v;
+            carry = v >> 32;
+        }
+    } else {
+        uint64_t borrow = 0;
+        for (int i = limb; i < n; ++i) {
+            uint64_t sub = (uint64_t)(i - limb < 4 ? part[i - limb] : 0u) + borrow;
+            borrow = (uint64_t)acc[i] < sub;
+            acc[i] = (uint32_t)((uint64_t)acc[i] - sub);
+        }
+    }
+}
+
+/* Sign of a two's-complement wide integer: -1, 0 or +1. */
+static int wide_sign(const uint32_t *a, int n)
+{
+    if (a[n - 1] >> 31) return -1;
+    for (int i = 0; i < n; ++i)
+        if (a[i]) return 1;
+    return 0;
+}
+
+/* w = m * 2^e exactly (finite float32). */
+static void f32_parts(float w, int64_t *m, int *e)
+{
+    if (w == 0.0f) { *m = 0; *e = 0; return; }
+    int ex;
+    double f = frexp((double)w, &ex);               /* w = f * 2^ex, 0.5 <= |f| < 1 */
+    *m = (int64_t)ldexp(f, 24);                     /* exact: 24 significant bits at most */
+    *e = ex - 24;
+}
+
+/* Exact score of one query against listed key rows: out [npos, EXACT_LIMBS]. */
+void orc_index_scores_exact(int H, int d, const uint8_t *qc, const uint8_t *qs, const float *w,
+                            const uint8_t *kc, const uint8_t *ks, const int64_t *pos, int64_t npos,
+                            uint32_t *out)
+{
+    int nb = d / 32;
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < npos; ++i) {
+        uint32_t *S = out + i * EXACT_LIMBS;
+        memset(S, 0, EXACT_LIMBS * sizeof(uint32_t));
+        const uint8_t *kr = kc + pos[i] * (d / 2), *kx = ks + pos[i] * (d / 32);
+        for (int h = 0; h < H; ++h) {
+            const uint8_t *qr = qc + (int64_t)h * (d / 2), *qx = qs + (int64_t)h * (d / 32);
+            int64_t I[64];
+            int eb[64];
+            uint32_t dh[BIG_LIMBS];
+            memset(dh, 0, sizeof dh);
+            for (int b = 0; b < nb; ++b) {
+                int64_t acc = 0;
+                for (int t = 0; t < 32; ++t) {
+                    int j = b * 32 + t;
+                    int cq = (j % 2 == 0) ? (qr[j / 2] & 15) : (qr[j / 2] >> 4);
+                    int ck = (j % 2 == 0) ? (kr[j / 2] & 15) : (kr[j / 2] >> 4);
+                    acc += (int64_t)e2m1_twice_signed(cq) * e2m1_twice_signed(ck);
+                }
+                I[b] = acc;
+                eb[b] = ((int)qx[b] - 127) + ((int)kx[b] - 127) - 2;
+                wide_add(dh, BIG_LIMBS, BIG_E0, I[b], eb[b]);
+            }
+            if (wide_sign(dh, BIG_LIMBS) <= 0) continue;            /* ReLU */
+            int64_t mw;
+            int ew;
+            f32_parts(w[h], &mw, &ew);
+            for (int b = 0; b < nb; ++b)
+                wide_add(S, EXACT_LIMBS, EXACT_E0, mw * I[b], ew + eb[b]);
+        }
     }
 }
 

@@ -163,3 +163,23 @@ def topk_positions(scores: Sequence[float], positions: Sequence[int], k: int) ->
     order = sorted(range(len(positions)), key=lambda i: (-float(scores[i]), positions[i]))
     sel = sorted(positions[i] for i in order[:k])
     return sel + [-1] * (k - len(sel))
+
+
+def score_exact(qc, qs, w, kc, ks) -> Fraction:
+    """The exact score sum_h w_h * max(0, q_h . k) as a Fraction (w_h the exact value of
+    each float32 weight; nothing rounded)."""
+    kv = exact_vector(kc, ks)
+    s = Fraction(0)
+    for h in range(qc.shape[0]):
+        qv = exact_vector(qc[h], qs[h])
+        d = sum((a * b for a, b in zip(qv, kv)), Fraction(0))
+        if d > 0:
+            s += Fraction(float(np.float32(w[h]))) * d
+    return s
+
+
+def topk_exact_positions(values: Sequence[Fraction], positions: Sequence[int], k: int) -> List[int]:
+    """k best by (exact value descending, position ascending); ascending, -1 padded."""
+    order = sorted(range(len(positions)), key=lambda i: (-values[i], positions[i]))
+    sel = sorted(positions[i] for i in order[:k])
+    return sel + [-1] * (k - len(sel))

@@ -59,10 +59,6 @@ class L2Flush:
     def __call__(self):
         self.a.fill_(1)
         self.b.max()
-# DRAM bytes (read + write) of one csa2_index_score tensor-core launch on this workload, from
-# the ncu capture summarised in profiles/index_score_tc_kernel_full_decode_64k.md; None
-# whenever the kernel has changed since that capture.
-INDEX_TRAFFIC_BYTES = 143_169_024 + 7_500_288
 
 
 def _peaks():
@@ -237,8 +233,8 @@ def run_reference(args):
                        "parallelism": "cpu-oracle (one sampled sequence per step)",
                        "topk": w.topk, "window": w.window, "indexer": f"{w.idx_heads}x{w.idx_dim}",
                        "heads": w.heads, "d_qk": w.d_qk, "d_v": w.d_v},
-            "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                             "sample": sample},
+            "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": cores, "cpu_model": cpu_model(),
+                             "kind": "oracle", "sample": sample},
             "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
@@ -310,7 +306,7 @@ def run_gpu(args):
                            dtype=torch.uint8, device=dev)     # zero before first use
     ws_attn = torch.empty(max(1, lib.csa2_sparse_attn_workspace_size(ctypes.byref(aargs))),
                           dtype=torch.uint8, device=dev)
-    ws_topk = torch.empty(max(1, lib.csa2_topk_workspace_size(B * T, w.n_keys, w.topk)),
+    ws_topk = torch.empty(max(1, lib.csa2_topk_workspace_size(B * T, w.n_keys, w.topk, ctypes.byref(iargs))),
                           dtype=torch.uint8, device=dev)
     flush = L2Flush(dev)
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
@@ -345,7 +341,8 @@ def run_gpu(args):
         csa2.csa2_index_score(iargs, scores, row_len, st, workspace=ws_index)
         if k_ev:
             k_ev[2].record(stream)
-        csa2.csa2_topk(scores, w.topk, idx, row_len, d_status=st, workspace=ws_topk, group_max=gmax)
+        csa2.csa2_topk(scores, w.topk, idx, row_len, d_status=st, workspace=ws_topk, group_max=gmax,
+                       exact=iargs)
         if k_ev:
             k_ev[3].record(stream)
         csa2.csa2_sparse_attn(aargs, out, lse, st, workspace=ws_attn)
@@ -448,7 +445,8 @@ def run_gpu(args):
         d_in.copy_(h_in, non_blocking=True)
         csa2.csa2_rope_quant_fp4(cache_rows, st, jobs=cache_jobs)
         csa2.csa2_index_score(iargs_e2e, scores, row_len, st, workspace=ws_index)
-        csa2.csa2_topk(scores, w.topk, idx, row_len, d_status=st, workspace=ws_topk, group_max=gmax)
+        csa2.csa2_topk(scores, w.topk, idx, row_len, d_status=st, workspace=ws_topk, group_max=gmax,
+                       exact=iargs_e2e)
         cs.wait_event(qa_done)
         csa2.csa2_sparse_attn(aargs, out, lse, st, workspace=ws_attn)
         h_out.copy_(out, non_blocking=True)
@@ -543,7 +541,8 @@ def run_gpu(args):
         def step_nv():
             csa2.csa2_rope_quant_fp4(nv_rows, st, jobs=nv_jobs)
             csa2.csa2_index_score(iargs, scores, row_len, st, workspace=ws_index)
-            csa2.csa2_topk(scores, w.topk, idx, row_len, d_status=st, workspace=ws_topk, group_max=gmax)
+            csa2.csa2_topk(scores, w.topk, idx, row_len, d_status=st, workspace=ws_topk, group_max=gmax,
+                       exact=iargs)
             csa2.csa2_sparse_attn(aargs_nv, out_nv, lse_nv, st, workspace=ws_attn_nv)
 
         for _ in range(args.warmup):
@@ -590,8 +589,11 @@ def run_gpu(args):
         return 0
 
     peak, peak_kind = _peaks()
-    kb = _kernel_bytes(w)
-    achieved = kb / (ms_k * 1e-3) / 1e9
+    krl = kernel_rooflines(w, per_kernel, peak, _bf16_peak())
+    # the roofline object: the kernel with the longest per-call CUDA-event time in the step
+    dom = max(krl, key=lambda n: krl[n]["ms"])
+    api_name = {"cache_write": "csa2_rope_quant_fp4", "index_score": "csa2_index_score",
+                "topk": "csa2_topk", "sparse_attn": "csa2_sparse_attn"}[dom]
     line = {
         "metric": METRIC, "value": job_throughput(B * T, world, ms_step), "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
@@ -605,10 +607,12 @@ def run_gpu(args):
                          "write-back drains; untimed)",
                    "launch": "CUDA graph of the step" if graph is not None else "eager"},
         "achieved_gbs_step": _step_bytes(w) / (ms_step * 1e-3) / 1e9,
-        "roofline": {"bound": "hbm", "kernel": "csa2_index_score", "achieved": achieved,
+        "frac_step": _step_bytes(w) / (ms_step * 1e-3) / 1e9 / peak,
+        "roofline": {"bound": "hbm", "kernel": api_name, "achieved": krl[dom]["gbs"],
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": INDEX_TRAFFIC_BYTES,
-                     "algorithmic_bytes": kb, "ms": ms_k},
+                     "frac": krl[dom]["frac_hbm"], "traffic": None,
+                     "algorithmic_bytes": krl[dom]["bytes"], "ms": krl[dom]["ms"],
+                     "chosen_as": "longest per-call CUDA-event time of the step's calls"},
         "e2e": {"value": job_throughput(B * T, world, e2e_step), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_step,
                 "copies": "pinned host buffers; indexer query + head weights in one upload, the "
@@ -616,7 +620,7 @@ def run_gpu(args):
                           "indexer and Top-K run; output downloaded; "
                           + ("one CUDA graph per step" if g_e2e is not None else "eager calls")},
         "kernels_ms": per_kernel,
-        "kernels_roofline": kernel_rooflines(w, per_kernel, peak, _bf16_peak()),
+        "kernels_roofline": krl,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks.summary(),
     }
@@ -631,11 +635,15 @@ def run_gpu(args):
             line["indexer_rows"] = indexer_rows(dev)
         except Exception as exc:          # reported, not fatal: the decode line stands
             line["indexer_rows"] = {"error": f"{type(exc).__name__}: {exc}"}
+        try:
+            line["decode_workloads"] = decode_workloads(dev)
+        except Exception as exc:          # reported, not fatal
+            line["decode_workloads"] = {"error": f"{type(exc).__name__}: {exc}"}
     if not args.no_cpu_baseline:
         import oracle
         dt, tok = oracle_sample(w, [0, 1])
         line["cpu_baseline"] = {"value": tok / dt, "unit": "tokens/s", "cores": oracle.num_threads(),
-                                "kind": "oracle",
+                                "cpu_model": cpu_model(), "kind": "oracle",
                                 "sample": "2 of 32 sequences: oracle indexer over 65,536 positions, "
                                           "Top-512, fp64 attention"}
     print(json.dumps(line))
@@ -687,15 +695,15 @@ def indexer_rows(dev):
                                  w.ratio_m, pool, w.block, gmax)
     ws_i = torch.zeros(max(1, lib.csa2_index_score_workspace_size(ctypes.byref(iargs))),
                        dtype=torch.uint8, device=dev)
-    ws_t = torch.empty(max(1, lib.csa2_topk_workspace_size(B * T, n_cand, w.topk)), dtype=torch.uint8,
-                       device=dev)
+    ws_t = torch.empty(max(1, lib.csa2_topk_workspace_size(B * T, n_cand, w.topk, ctypes.byref(iargs))),
+                       dtype=torch.uint8, device=dev)
 
     def score():
         csa2.csa2_index_score(iargs, scores, row_len, st, workspace=ws_i)
 
     def select():
         csa2.csa2_topk(scores, w.topk, idx, row_len, pool, w.block, d_status=st, workspace=ws_t,
-                       group_max=gmax)
+                       group_max=gmax, exact=iargs)
 
     def chain():
         score()
@@ -729,19 +737,22 @@ def indexer_rows(dev):
                                  w.ratio_m, None, w.block, gmax)
     ws_i = torch.zeros(max(1, lib.csa2_index_score_workspace_size(ctypes.byref(iargs))),
                        dtype=torch.uint8, device=dev)
-    ws_t = torch.empty(max(1, lib.csa2_topk_workspace_size(B * T, w.n_keys, w.topk)), dtype=torch.uint8,
+    ws_t = torch.empty(max(1, lib.csa2_topk_workspace_size(B * T, w.n_keys, w.topk, ctypes.byref(iargs))), dtype=torch.uint8,
                        device=dev)
-    ws_b = torch.empty(max(1, lib.csa2_block_candidates_workspace_size(B * T, w.n_keys, w.block, w.n_blocks)),
+    ws_b = torch.empty(max(1, lib.csa2_block_candidates_workspace_size(B * T, w.n_keys, w.block, w.n_blocks,
+                                                                        ctypes.byref(iargs))),
                        dtype=torch.uint8, device=dev)
 
     def score1m():
         csa2.csa2_index_score(iargs, scores, row_len, st, workspace=ws_i)
 
     def select1m():
-        csa2.csa2_topk(scores, w.topk, idx, row_len, d_status=st, workspace=ws_t, group_max=gmax)
+        csa2.csa2_topk(scores, w.topk, idx, row_len, d_status=st, workspace=ws_t, group_max=gmax,
+                       exact=iargs)
 
     def blocks1m():
-        csa2.csa2_block_candidates(scores, w.n_blocks, blocks, row_len, w.block, st, workspace=ws_b)
+        csa2.csa2_block_candidates(scores, w.n_blocks, blocks, row_len, w.block, st, workspace=ws_b,
+                                   exact=iargs)
 
     def chain1m():
         score1m()
@@ -760,6 +771,119 @@ def indexer_rows(dev):
         "index_frac_hbm": ib / (t_score * 1e-3) / 1e9 / peak, "topk_ms": t_select,
         "block_candidates_ms": t_blocks, "ms": t_chain, "tokens_per_s": B * T / (t_chain * 1e-3)}
     return res
+
+
+def decode_workloads(dev):
+    """The two decode workloads the default line does not time, each on its own sizes:
+    the tiny Full decode layer (batch 1, 4,096 positions, indexer 4 x 64, 16 heads over a
+    128-dim latent; index score, exact Top-512, attention) as a latency, and the Reuse layer
+    at batch 64 x 131,072 (attention over the given Top-512 + SWA 128; no indexer work)
+    against the HBM copy rate with its algorithmic bytes (gathered main-KV rows, indices,
+    SWA, query, output).  Each is one CUDA graph, replayed after an L2 flush; median of 20."""
+    import ctypes
+    import torch
+    from fp4_kv_cache_gb300 import csa2, workload
+    lib = csa2.load()
+    peak, _ = _peaks()
+    flush = L2Flush(dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def graph_ms(fn, reps=20):
+        fn()
+        torch.cuda.synchronize(dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        ts = []
+        for it in range(reps + 3):
+            flush()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            g.replay()
+            e1.record()
+            e1.synchronize()
+            if it >= 3:
+                ts.append(e0.elapsed_time(e1))
+        return statistics.median(ts)
+
+    res = {}
+    # ---- tiny Full decode layer (latency)
+    w = synth.WORKLOADS["tiny_full_decode"]
+    dw = workload.build(w, device=dev, d_status=st)
+    B, T = w.batch, w.n_q
+    scores = torch.empty((B, T, w.n_keys), dtype=torch.float32, device=dev)
+    row_len = torch.empty((B, T), dtype=torch.int32, device=dev)
+    idx = torch.empty((B, T, w.topk), dtype=torch.int32, device=dev)
+    out = torch.empty((B, T, w.heads, w.d_v), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, T, w.heads), dtype=torch.float32, device=dev)
+    iargs = csa2.make_index_args(dw["q_idx"], dw["w_idx"], dw["k_codes"], dw["k_scales"], dw["q_pos"],
+                                 w.ratio_m)
+    aargs = csa2.make_attn_args(dw["q_attn"], dw["kv_codes"], dw["kv_scales"], idx, dw["swa"],
+                                dw["swa_pos0"], dw["q_pos"], None, w.window, dw.sm_scale, w.d_v)
+    ws_i = torch.zeros(max(1, lib.csa2_index_score_workspace_size(ctypes.byref(iargs))), dtype=torch.uint8,
+                       device=dev)
+    ws_t = torch.empty(max(1, lib.csa2_topk_workspace_size(B * T, w.n_keys, w.topk, ctypes.byref(iargs))),
+                       dtype=torch.uint8, device=dev)
+    ws_a = torch.empty(max(1, lib.csa2_sparse_attn_workspace_size(ctypes.byref(aargs))), dtype=torch.uint8,
+                       device=dev)
+
+    def tiny_layer():
+        csa2.csa2_index_score(iargs, scores, row_len, st, workspace=ws_i)
+        csa2.csa2_topk(scores, w.topk, idx, row_len, d_status=st, workspace=ws_t, exact=iargs)
+        csa2.csa2_sparse_attn(aargs, out, lse, st, workspace=ws_a)
+
+    t = graph_ms(tiny_layer)
+    if int(st.item()) != 0:
+        raise RuntimeError(f"device status {int(st.item())}")
+    res["tiny_full_decode"] = {"workload": w.name, "batch": B, "context": w.n_keys, "latency_ms": t,
+                               "launches": 3, "calls": "index score, exact Top-512, attention"}
+    del dw, scores, row_len, idx, out, lse, ws_i, ws_t, ws_a
+    torch.cuda.empty_cache()
+
+    # ---- Reuse layer at batch 64 x 131,072 (given Top-512)
+    w = synth.WORKLOADS["reuse_reindex_decode_128k"]
+    dw = workload.build(w, device=dev, kidx=False, d_status=st)
+    B, T = w.batch, w.n_q
+    out = torch.empty((B, T, w.heads, w.d_v), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, T, w.heads), dtype=torch.float32, device=dev)
+    aargs = csa2.make_attn_args(dw["q_attn"], dw["kv_codes"], dw["kv_scales"], dw["reuse_idx"], dw["swa"],
+                                dw["swa_pos0"], dw["q_pos"], None, w.window, dw.sm_scale, w.d_v)
+    ws_a = torch.empty(max(1, lib.csa2_sparse_attn_workspace_size(ctypes.byref(aargs))), dtype=torch.uint8,
+                       device=dev)
+
+    def reuse():
+        csa2.csa2_sparse_attn(aargs, out, lse, st, workspace=ws_a)
+
+    t = graph_ms(reuse)
+    if int(st.item()) != 0:
+        raise RuntimeError(f"device status {int(st.item())}")
+    kv_row = w.d_qk // 2 + w.d_qk // 32
+    ab = B * T * (w.topk * (kv_row + 4) + w.window * w.d_qk * 2 + w.heads * w.d_qk * 2 + w.heads * w.d_v * 2)
+    flop = 2.0 * B * T * w.heads * (w.topk + w.window) * (w.d_qk + w.d_v)
+    res["reuse_decode_128k"] = {
+        "workload": w.name, "batch": B, "context": w.n_keys, "sparse_attn_ms": t,
+        "tokens_per_s": B * T / (t * 1e-3), "bytes": ab, "gbs": ab / (t * 1e-3) / 1e9,
+        "frac_hbm": ab / (t * 1e-3) / 1e9 / peak, "tflops": flop / (t * 1e-3) / 1e12,
+        "frac_bf16": flop / (t * 1e-3) / 1e12 / _bf16_peak()}
+    return res
+
+
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), or None."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for ln in open("/proc/cpuinfo"):
+            if ln.lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return None
 
 
 PREFILL_WORKLOAD = "prefill_chunk_m2"
@@ -807,7 +931,7 @@ def prefill_indexer(dev, sm_mhz, with_chunk=True):
         lse = torch.empty((B, T, w.heads), dtype=torch.float32, device=dev)
         aargs = csa2.make_attn_args(dw["q_attn"], dw["kv_codes"], dw["kv_scales"], idx, dw["swa"],
                                     dw["swa_pos0"], dw["q_pos"], None, w.window, dw.sm_scale, w.d_v)
-        ws_topk = torch.empty(max(1, lib.csa2_topk_workspace_size(B * T, w.n_keys, w.topk)),
+        ws_topk = torch.empty(max(1, lib.csa2_topk_workspace_size(B * T, w.n_keys, w.topk, ctypes.byref(iargs))),
                               dtype=torch.uint8, device=dev)
         ws_attn = torch.empty(max(1, lib.csa2_sparse_attn_workspace_size(ctypes.byref(aargs))),
                               dtype=torch.uint8, device=dev)
@@ -818,7 +942,8 @@ def prefill_indexer(dev, sm_mhz, with_chunk=True):
             e[0].record()
             csa2.csa2_index_score(iargs, scores, row_len, st, workspace=ws_index)
             e[1].record()
-            csa2.csa2_topk(scores, w.topk, idx, row_len, d_status=st, workspace=ws_topk, group_max=gmax)
+            csa2.csa2_topk(scores, w.topk, idx, row_len, d_status=st, workspace=ws_topk, group_max=gmax,
+                       exact=iargs)
             e[2].record()
             csa2.csa2_sparse_attn(aargs, out, lse, st, workspace=ws_attn)
             e[3].record()

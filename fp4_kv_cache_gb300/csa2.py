@@ -24,6 +24,8 @@ _lock = threading.Lock()
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_WORKSPACE = 0, 1, 2, 3, 4
 DEV_BAD_INDEX, DEV_BAD_POOL, DEV_NONFINITE, DEV_TIMEOUT = 0x1, 0x2, 0x4, 0x8
+DEV_SCORE_RANGE, DEV_BAND_LIMIT = 0x10, 0x20
+EXACT_BAND_CAP = 2048
 BF16, F32 = 0, 1
 FMT_MXFP4, FMT_NVFP4_E4M3_16 = 0, 1
 FMT_BLOCK = {FMT_MXFP4: 32, FMT_NVFP4_E4M3_16: 16}     # values per scale byte
@@ -110,14 +112,15 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
             lib.csa2_index_score_workspace_size.argtypes = [ctypes.POINTER(IndexArgs)]
             lib.csa2_index_score.restype = S
             lib.csa2_index_score.argtypes = [ctypes.POINTER(IndexArgs), _P, _P, _P, sz, _P, _P]
+            IA = ctypes.POINTER(IndexArgs)
             lib.csa2_topk_workspace_size.restype = sz
-            lib.csa2_topk_workspace_size.argtypes = [_I64, _I64, _I32]
+            lib.csa2_topk_workspace_size.argtypes = [_I64, _I64, _I32, IA]
             lib.csa2_topk.restype = S
-            lib.csa2_topk.argtypes = [_P, _I64, _I64, _P, _P, _P, _I32, _I32, _P, _P, _P, sz, _P, _P]
+            lib.csa2_topk.argtypes = [_P, _I64, _I64, _P, _P, _P, _I32, IA, _I32, _P, _P, _P, sz, _P, _P]
             lib.csa2_block_candidates_workspace_size.restype = sz
-            lib.csa2_block_candidates_workspace_size.argtypes = [_I64, _I64, _I32, _I32]
+            lib.csa2_block_candidates_workspace_size.argtypes = [_I64, _I64, _I32, _I32, IA]
             lib.csa2_block_candidates.restype = S
-            lib.csa2_block_candidates.argtypes = [_P, _I64, _I64, _P, _I32, _I32, _P, _P, sz, _P, _P]
+            lib.csa2_block_candidates.argtypes = [_P, _I64, _I64, _P, _I32, _I32, IA, _P, _P, sz, _P, _P]
             lib.csa2_sparse_attn_workspace_size.restype = sz
             lib.csa2_sparse_attn_workspace_size.argtypes = [ctypes.POINTER(AttnArgs)]
             lib.csa2_sparse_attn.restype = S
@@ -320,28 +323,35 @@ def csa2_selftest_bounded_wait(polls: int, d_status: torch.Tensor, stream=None):
                                                                            _stream(stream)))
 
 
+def _exact_ref(exact: Optional[IndexArgs]):
+    return ctypes.byref(exact) if exact is not None else None
+
+
 def csa2_topk(scores: torch.Tensor, k: int, idx: torch.Tensor, row_len=None, pool_blocks=None,
               block: int = 8, out_scores=None, d_status=None, stream=None, workspace=None,
-              group_max=None):
+              group_max=None, exact: Optional[IndexArgs] = None):
+    """exact: the IndexArgs of the csa2_index_score call that wrote `scores` (rank by the
+    exact score) or None (rank the given floats)."""
     lib = load()
     n = scores.shape[-1]
     rows = scores.numel() // n if n else idx.numel() // max(k, 1)
-    need = lib.csa2_topk_workspace_size(rows, n, k)
+    need = lib.csa2_topk_workspace_size(rows, n, k, _exact_ref(exact))
     ws, wsb = _ws(need, idx.device, workspace, stream)
     _check("csa2_topk", lib.csa2_topk(_ptr(scores), rows, n, _ptr(row_len), _ptr(group_max),
-                                      _ptr(pool_blocks), block, k, _ptr(idx), _ptr(out_scores),
-                                      ws, wsb, _ptr(d_status), _stream(stream)))
+                                      _ptr(pool_blocks), block, _exact_ref(exact), k, _ptr(idx),
+                                      _ptr(out_scores), ws, wsb, _ptr(d_status), _stream(stream)))
 
 
 def csa2_block_candidates(scores: torch.Tensor, nb: int, block_ids: torch.Tensor, row_len=None,
-                          block: int = 8, d_status=None, stream=None, workspace=None):
+                          block: int = 8, d_status=None, stream=None, workspace=None,
+                          exact: Optional[IndexArgs] = None):
     lib = load()
     n = scores.shape[-1]
     rows = scores.numel() // n if n else block_ids.numel() // max(nb, 1)
-    need = lib.csa2_block_candidates_workspace_size(rows, n, block, nb)
+    need = lib.csa2_block_candidates_workspace_size(rows, n, block, nb, _exact_ref(exact))
     ws, wsb = _ws(need, block_ids.device, workspace, stream)
     _check("csa2_block_candidates", lib.csa2_block_candidates(
-        _ptr(scores), rows, n, _ptr(row_len), block, nb, _ptr(block_ids), ws, wsb,
+        _ptr(scores), rows, n, _ptr(row_len), block, nb, _exact_ref(exact), _ptr(block_ids), ws, wsb,
         _ptr(d_status), _stream(stream)))
 
 
@@ -400,31 +410,33 @@ def group_max_buffer(scores: torch.Tensor) -> torch.Tensor:
 
 
 def index_score(q, w, k_codes, k_scales, q_pos=None, ratio_m=1, pool_blocks=None, block=8,
-                d_status=None, stream=None, group_max=None):
-    """-> (scores f32 [B, T, n_cand], row_len int32 [B, T]); group_max: optional buffer
-    from group_max_buffer(scores) that receives the group maxima for csa2_topk."""
+                d_status=None, stream=None, group_max=None, want_args=False):
+    """-> (scores f32 [B, T, n_cand], row_len int32 [B, T]) and, with want_args, the
+    IndexArgs used (pass them as `exact` to topk / block_candidates to rank by the exact
+    score; they point into q, w and the caches, which must stay alive).  group_max:
+    optional buffer from group_max_buffer(scores) that receives the group maxima."""
     B, T = q.shape[:2]
     n_cand = k_codes.shape[1] if pool_blocks is None else pool_blocks.shape[-1] * block
     scores = torch.empty((B, T, n_cand), dtype=torch.float32, device=q.device)
     row_len = torch.empty((B, T), dtype=torch.int32, device=q.device)
     args = make_index_args(q, w, k_codes, k_scales, q_pos, ratio_m, pool_blocks, block, group_max)
     csa2_index_score(args, scores, row_len, d_status, stream)
-    return scores, row_len
+    return (scores, row_len, args) if want_args else (scores, row_len)
 
 
 def topk(scores, k=512, row_len=None, pool_blocks=None, block=8, want_scores=False,
-         d_status=None, stream=None, group_max=None):
+         d_status=None, stream=None, group_max=None, exact=None):
     shape = scores.shape[:-1]
     idx = torch.empty(shape + (k,), dtype=torch.int32, device=scores.device)
     out_s = torch.empty(shape + (k,), dtype=torch.float32, device=scores.device) if want_scores else None
     csa2_topk(scores, k, idx, row_len, pool_blocks, block, out_s, d_status, stream,
-              group_max=group_max)
+              group_max=group_max, exact=exact)
     return (idx, out_s) if want_scores else idx
 
 
-def block_candidates(scores, nb=2048, row_len=None, block=8, d_status=None, stream=None):
+def block_candidates(scores, nb=2048, row_len=None, block=8, d_status=None, stream=None, exact=None):
     ids = torch.empty(scores.shape[:-1] + (nb,), dtype=torch.int32, device=scores.device)
-    csa2_block_candidates(scores, nb, ids, row_len, block, d_status, stream)
+    csa2_block_candidates(scores, nb, ids, row_len, block, d_status, stream, exact=exact)
     return ids
 
 

@@ -7,10 +7,34 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/csa2.h"
 #include "internal.h"
 
 using namespace csa2;
+
+namespace csa2 {
+
+// Streaming multiprocessors of the current device, queried once per device ordinal (grid
+// sizes are multiples of it); 1 if the query fails.
+int device_sm_count()
+{
+    constexpr int kMaxDevices = 64;
+    static std::atomic<int> cached[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 1;
+    if (dev < kMaxDevices) {
+        const int c = cached[dev].load(std::memory_order_relaxed);
+        if (c > 0) return c;
+    }
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 1;
+    if (dev < kMaxDevices) cached[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
+
+} // namespace csa2
 
 namespace {
 
@@ -214,48 +238,68 @@ csa2_status csa2_index_score(const csa2_index_args *a, float *scores, int32_t *r
                                         as_stream(stream)));
 }
 
-size_t csa2_topk_workspace_size(int64_t rows, int64_t n, int32_t k)
+// An exact context fits scores of `rows` rows of n candidates: rows = batch * n_q and n its
+// candidate count; in POOL mode the pool is given again and matches, in FULL mode none is.
+bool exact_ctx_ok(const csa2_index_args *ex, int64_t rows, int64_t n, const int32_t *pool_blocks,
+                  int32_t block, const int32_t *row_len, bool blocks)
 {
-    return topk_ws_bytes(rows, n, k);
+    if (!index_args_ok(ex)) return false;
+    if ((int64_t)ex->batch * ex->n_q != rows || index_candidates(ex) != n || !row_len) return false;
+    if (ex->mode == CSA2_INDEX_POOL) {
+        if (blocks || pool_blocks != ex->pool_blocks || block != ex->block) return false;
+    } else if (pool_blocks) {
+        return false;
+    }
+    return true;
+}
+
+size_t csa2_topk_workspace_size(int64_t rows, int64_t n, int32_t k, const csa2_index_args *exact)
+{
+    return topk_ws_bytes(rows, n, k, exact != nullptr);
 }
 
 csa2_status csa2_topk(const float *scores, int64_t rows, int64_t n, const int32_t *row_len,
                       const uint32_t *group_max, const int32_t *pool_blocks, int32_t block,
-                      int32_t k, int32_t *idx, float *out_scores, void *ws, size_t ws_bytes,
-                      uint32_t *d_status, csa2_stream stream)
+                      const csa2_index_args *exact, int32_t k, int32_t *idx, float *out_scores, void *ws,
+                      size_t ws_bytes, uint32_t *d_status, csa2_stream stream)
 {
     if (rows < 0 || n < 0 || n >= (int64_t(1) << 31) || k < 0 || rows > (int64_t(1) << 31))
         return CSA2_ERR_INVALID_ARG;
     if (pool_blocks && (block < 1 || n % block)) return CSA2_ERR_INVALID_ARG;
+    if (exact && !exact_ctx_ok(exact, rows, n, pool_blocks, block, row_len, false)) return CSA2_ERR_INVALID_ARG;
     if (rows == 0 || k == 0) return CSA2_OK;
     if (!idx || (n > 0 && !scores)) return CSA2_ERR_INVALID_ARG;
-    if (ws_bytes < csa2_topk_workspace_size(rows, n, k)) return CSA2_ERR_WORKSPACE;
+    const size_t need = csa2_topk_workspace_size(rows, n, k, exact);
+    if (ws_bytes < need) return CSA2_ERR_WORKSPACE;
+    if (exact && (!ws || !aligned(ws, 16))) return CSA2_ERR_INVALID_ARG;
     if (group_max && !aligned(group_max, 4)) return CSA2_ERR_INVALID_ARG;
     return from_cuda(launch_topk(scores, rows, n, row_len, group_max, pool_blocks, block, k, idx,
-                                 out_scores, ws, d_status, as_stream(stream)));
+                                 out_scores, ws, d_status, as_stream(stream), exact));
 }
 
-size_t csa2_block_candidates_workspace_size(int64_t rows, int64_t n, int32_t block, int32_t nb)
+size_t csa2_block_candidates_workspace_size(int64_t rows, int64_t n, int32_t block, int32_t nb,
+                                            const csa2_index_args *exact)
 {
     if (rows <= 0 || n < 0 || block < 1 || nb <= 0) return 0;
-    return block_candidates_ws_bytes(rows, n, block, nb);
+    return block_candidates_ws_bytes(rows, n, block, nb, exact != nullptr);
 }
 
 csa2_status csa2_block_candidates(const float *scores, int64_t rows, int64_t n,
                                   const int32_t *row_len, int32_t block, int32_t nb,
-                                  int32_t *block_ids, void *ws, size_t ws_bytes,
-                                  uint32_t *d_status, csa2_stream stream)
+                                  const csa2_index_args *exact, int32_t *block_ids, void *ws,
+                                  size_t ws_bytes, uint32_t *d_status, csa2_stream stream)
 {
     if (rows < 0 || n < 0 || n >= (int64_t(1) << 31) || block < 1 || nb < 0 ||
         rows > (int64_t(1) << 31))
         return CSA2_ERR_INVALID_ARG;
+    if (exact && !exact_ctx_ok(exact, rows, n, nullptr, block, row_len, true)) return CSA2_ERR_INVALID_ARG;
     if (rows == 0 || nb == 0) return CSA2_OK;
     if (!block_ids || (n > 0 && !scores)) return CSA2_ERR_INVALID_ARG;
-    const size_t need = csa2_block_candidates_workspace_size(rows, n, block, nb);
+    const size_t need = csa2_block_candidates_workspace_size(rows, n, block, nb, exact);
     if (ws_bytes < need) return CSA2_ERR_WORKSPACE;
     if (need && (!ws || !aligned(ws, 16))) return CSA2_ERR_INVALID_ARG;
     return from_cuda(launch_block_candidates(scores, rows, n, row_len, block, nb, block_ids, ws,
-                                             d_status, as_stream(stream)));
+                                             d_status, as_stream(stream), exact));
 }
 
 size_t csa2_sparse_attn_workspace_size(const csa2_attn_args *a)

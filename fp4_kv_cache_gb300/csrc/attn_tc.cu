@@ -644,7 +644,8 @@ void attn_tc_split(const csa2_attn_args &a, int &splits, int &tiles_per_split)
     const int64_t rows = (int64_t)a.batch * a.n_q;
     const int64_t max_slots = (int64_t)a.topk + (a.swa ? (int64_t)(a.window < a.n_swa ? a.window : a.n_swa) : 0);
     const int tiles = (int)((max_slots + kKeys - 1) / kKeys);
-    int64_t per = (tiles * rows + 151) / 152;          // tiles per CTA to fill one wave
+    const int64_t sms = device_sm_count();
+    int64_t per = (tiles * rows + sms - 1) / sms;       // tiles per CTA to fill one wave
     if (per < 1) per = 1;
     if (per * kMaxSplits < tiles) per = (tiles + kMaxSplits - 1) / kMaxSplits;   // one cluster per row
     if (per > tiles) per = tiles > 0 ? tiles : 1;

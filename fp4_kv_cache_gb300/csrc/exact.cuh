@@ -1,0 +1,202 @@
+// exact.cuh -- exact indexer scores for the selection kernels (topk.cu).
+//
+// DeepSeek-V4.1-Flash report (aipaper.jasonlin.tech) §2.3 / §2.4.4: the indexer ranks
+// main-KV entries by scores of MXFP4 indexer queries and keys.  The score is
+//     s = sum_h w_h * max(0, d_h),   d_h = q_hat_h . k_hat  (the exact dot),
+// with w_h the exact value of the float32 weight.  The selection kernels rank by s
+// exactly: float32 scores (within a proven error bound of s) decide every candidate far
+// from the K-th score, and the few candidates within the bound are re-scored here with
+// nothing rounded.
+//
+// Representation: a two's-complement integer S of kLimbs 32-bit limbs with s = S * 2^kE0.
+// A product term m_w * I_b (m_w < 2^24 the weight's significand, |I_b| < 2^13 the integer
+// block dot) sits at exponent e_w + Xq + Xk - 2 >= -149 - 127 - 127 - 2 = -405 and is below
+// 2^(104 + 255 - 2 + 37) = 2^394, so 26 limbs from 2^-416 hold any sum of up to 256 of
+// them with its sign.  A warp computes one score: lane h handles head h (and h + 32), and
+// lane j < 26 owns limb j of the result, accumulating each term's 32-bit slice as a signed
+// 64-bit digit; one carry pass at the end gives the limbs.
+#pragma once
+
+#include "common.cuh"
+
+namespace csa2 {
+namespace exact {
+
+constexpr int kLimbs = 26;
+constexpr int kE0 = -416;
+constexpr int kMaxH = 64;
+constexpr int kMaxWords = 32;          // int8x4 words of one head (head dim <= 128)
+
+// One query row quantised to MXFP4 by the indexer's rule, as the exact pass needs it.
+struct QuantQuery {
+    int32_t qw[kMaxH * kMaxWords];     // twice the E2M1 values as int8x4 words, head-major
+    int32_t qx[kMaxH * 4];             // block exponents X (scale byte - 127)
+    int32_t q1[kMaxH * 4];             // sum of |twice value| over each block
+    int32_t m_w[kMaxH];                // w_h = m_w * 2^e_w exactly
+    int32_t e_w[kMaxH];
+    float w[kMaxH];
+};
+
+// Quantise query row `q` ([H, d] bf16 bits) into Q: one warp per 32-value block, the same
+// block exponent and rounding as csa2_quant_fp4 and the indexer kernels.  All threads of
+// the block call; ends with a barrier.
+__device__ __forceinline__ void quantise_query(QuantQuery &Q, const uint16_t *q, const float *w, int H, int d)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    const int nb = d / 32, nw = d / 4;
+    for (int blk = warp; blk < H * nb; blk += nwarps) {
+        const int h = blk / nb, b = blk % nb;
+        const float v = __uint_as_float((uint32_t)q[(int64_t)h * d + b * 32 + lane] << 16);
+        const uint32_t amax_bits = __reduce_max_sync(0xffffffffu, __float_as_uint(v) & 0x7fffffffu);
+        const int X = mx_block_exponent(__uint_as_float(amax_bits >= 0x7f800000u ? 0u : amax_bits));
+        const int t = e2m1_twice(e2m1_encode(v, pow2_neg(X)));
+        const uint32_t tb = (uint32_t)t & 0xffu;
+        uint32_t word = tb;
+        word |= __shfl_down_sync(0xffffffffu, tb, 1) << 8;
+        word |= __shfl_down_sync(0xffffffffu, tb, 2) << 16;
+        word |= __shfl_down_sync(0xffffffffu, tb, 3) << 24;
+        const int q1 = __reduce_add_sync(0xffffffffu, t < 0 ? -t : t);
+        if ((lane & 3) == 0) Q.qw[h * nw + b * 8 + (lane >> 2)] = (int32_t)word;
+        if (lane == 0) {
+            Q.qx[h * 4 + b] = X;
+            Q.q1[h * 4 + b] = q1;
+        }
+    }
+    for (int h = threadIdx.x; h < H; h += blockDim.x) {
+        const float x = w[h];
+        const uint32_t u = __float_as_uint(x);
+        const int ef = (int)((u >> 23) & 0xffu);
+        int m = (int)(u & 0x7fffffu), e = -149;
+        if (ef != 0) { m |= 0x800000; e = ef - 150; }
+        Q.m_w[h] = (u >> 31) ? -m : m;
+        Q.e_w[h] = e;
+        Q.w[h] = x;
+    }
+    __syncthreads();
+}
+
+// Sign of sum_b I[b] * 2^E[b] (|I[b]| < 2^13), exactly: terms from the largest exponent
+// down; once the partial sum is at least 2^15 times the next term's unit (a gap of >= 15
+// bits, or a partial sum >= 2^40 of its own unit), the remaining terms (fewer than three,
+// each below 2^13 of that unit) cannot change its sign.
+template <int NB>
+__device__ __forceinline__ int dyadic_sign(const int (&I)[NB], const int (&E)[NB])
+{
+    int ii[NB], ee[NB];
+#pragma unroll
+    for (int b = 0; b < NB; ++b) { ii[b] = I[b]; ee[b] = I[b] ? E[b] : -(1 << 20); }
+#pragma unroll
+    for (int i = 0; i < NB; ++i)
+#pragma unroll
+        for (int j = 0; j + 1 < NB - i; ++j)
+            if (ee[j] < ee[j + 1]) {
+                const int te = ee[j], ti = ii[j];
+                ee[j] = ee[j + 1]; ii[j] = ii[j + 1];
+                ee[j + 1] = te; ii[j + 1] = ti;
+            }
+    long long acc = 0;
+    int base = 0;
+#pragma unroll
+    for (int t = 0; t < NB; ++t) {
+        if (ii[t] == 0) continue;
+        if (acc == 0) { acc = ii[t]; base = ee[t]; continue; }
+        const int g = base - ee[t];
+        if (g >= 15 || acc >= (1LL << 40) || acc <= -(1LL << 40)) break;
+        acc = acc * (1LL << g) + ii[t];
+        base = ee[t];
+    }
+    return acc > 0 ? 1 : (acc < 0 ? -1 : 0);
+}
+
+// Signed 32-bit slice of m * 2^(e - kE0) falling on limb `lane` (|m| < 2^63, e >= kE0).
+__device__ __forceinline__ long long limb_slice(long long m, int e, int lane)
+{
+    const int lo = 32 * lane - (e - kE0);
+    const unsigned long long a = (unsigned long long)(m < 0 ? -m : m);
+    uint32_t s = 0;
+    if (lo >= 0 && lo < 64) s = (uint32_t)(a >> lo);
+    else if (lo < 0 && lo > -32) s = (uint32_t)(a << (-lo));
+    return m < 0 ? -(long long)s : (long long)s;
+}
+
+// Four E2M1 codes (the low 16 bits, element 0 in the lowest nibble) as int8x4 of twice
+// their values.
+__device__ __forceinline__ int32_t twice_codes4(uint32_t x)
+{
+    uint32_t r = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) r |= ((uint32_t)e2m1_twice((x >> (4 * i)) & 15u) & 0xffu) << (8 * i);
+    return (int32_t)r;
+}
+
+// Exact score of key row (kc: d/2 code bytes, ks: d/32 scale bytes) against Q, computed by
+// the whole warp.  Returns limb `lane` of S (lanes >= kLimbs return 0), with the top limb's
+// sign bit flipped, so that comparing limbs as unsigned from the top gives numeric order.
+template <int D>
+__device__ __noinline__ uint32_t score_key_limb(const QuantQuery &Q, int H, const uint8_t *kc, const uint8_t *ks)
+{
+    constexpr int NB = D / 32, NW = D / 4;
+    const int lane = threadIdx.x & 31;
+    const int32_t kw = lane < NW ? twice_codes4(*reinterpret_cast<const uint16_t *>(kc + 2 * lane)) : 0;
+    int E_k[NB];
+#pragma unroll
+    for (int b = 0; b < NB; ++b) E_k[b] = (int)ks[b] - 127;
+    long long acc = 0;
+#pragma unroll 1
+    for (int slot = 0; slot < 2; ++slot) {
+        const int h = lane + 32 * slot;
+        if (__all_sync(0xffffffffu, h >= H)) break;
+        const bool live = h < H;
+        const int hq = live ? h : 0;
+        int I[NB], E[NB];
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            int a = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) a = __dp4a(Q.qw[hq * NW + b * 8 + j], __shfl_sync(0xffffffffu, kw, b * 8 + j), a);
+            I[b] = a;
+            E[b] = Q.qx[hq * 4 + b] + E_k[b] - 2;
+        }
+        const bool pos = live && Q.m_w[hq] != 0 && dyadic_sign<NB>(I, E) > 0;
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            const bool has = pos && I[b] != 0;
+            const long long mant = has ? (long long)Q.m_w[hq] * I[b] : 0;
+            const int e = Q.e_w[hq] + E[b];
+            uint32_t mask = __ballot_sync(0xffffffffu, has);
+#pragma unroll 1
+            while (mask) {
+                const int src = __ffs(mask) - 1;
+                mask &= mask - 1u;
+                const long long m = __shfl_sync(0xffffffffu, mant, src);
+                const int ee = __shfl_sync(0xffffffffu, e, src);
+                if (lane < kLimbs) acc += limb_slice(m, ee, lane);
+            }
+        }
+    }
+    // carries: limb j = (acc_j + carry_j) mod 2^32, carry_{j+1} = floor(./2^32)
+    long long carry = 0;
+    uint32_t limb = 0;
+#pragma unroll 1
+    for (int j = 0; j < kLimbs; ++j) {
+        const long long v = acc + carry;
+        if (lane == j) limb = (uint32_t)v;
+        carry = __shfl_sync(0xffffffffu, v >> 32, j);
+    }
+    if (lane == kLimbs - 1) limb ^= 0x80000000u;
+    return lane < kLimbs ? limb : 0u;
+}
+
+// Compares two keys held one limb per lane (as returned by score_key_limb): > 0 when a is
+// the larger score, 0 when equal.  Warp-collective.
+__device__ __forceinline__ int compare_keys(uint32_t a, uint32_t b)
+{
+    const uint32_t diff = __ballot_sync(0xffffffffu, a != b);
+    if (!diff) return 0;
+    const int top = 31 - __clz((int)diff);
+    const uint32_t xa = __shfl_sync(0xffffffffu, a, top), xb = __shfl_sync(0xffffffffu, b, top);
+    return xa > xb ? 1 : -1;
+}
+
+} // namespace exact
+} // namespace csa2

@@ -5,7 +5,11 @@
 // its Top-K; §2.3.2: the first Full layer scores every causally visible position, later
 // Reindex layers score only the positions of the block pool.
 //
-// Score of position t:  D_h = RN32(q_hat_h . k_hat_t),  s = fma32 chain of w_h * max(D_h, 0).
+// Score of position t: s_t = sum_h w_h * max(0, q_hat_h . k_hat_t), written out as its float32
+// approximation D_h = RN32(q_hat_h . k_hat_t), s = fma32 chain of w_h * max(D_h, 0), within a
+// proven bound of the exact value (csa2_topk ranks by the exact value, re-scoring the
+// candidates the bound leaves undecided); a score that is not finite sets
+// CSA2_DEV_SCORE_RANGE.
 //
 // This file holds the exact CUDA-core kernel: each thread owns one candidate position,
 // expands its FP4 codes to int8 (twice the E2M1 value), takes exact per-block integer
@@ -177,6 +181,7 @@ __global__ void __launch_bounds__(kThreads) index_score_exact_kernel(IndexParams
                 const float s = score_candidate<D>(P, pool, kbase, cand, s_qw, s_qx, s_w, s_lut);
                 P.scores[row * P.n_cand + cand] = s;
                 gkey = score_key(s);
+                if (!(fabsf(s) <= 3.4028234663852886e38f)) dev_flag(P.d_status, CSA2_DEV_SCORE_RANGE);
             }
             if (P.gmax) {
                 const uint32_t gk = __reduce_max_sync(0xffffffffu, gkey);
@@ -216,7 +221,7 @@ cudaError_t launch_index_exact(const csa2_index_args &a, float *scores, int32_t 
     const int64_t rows = (int64_t)a.batch * a.n_q;
     if (rows == 0) return cudaSuccess;
     int64_t chunk = 2048;          // so that the grid covers the GPU a few times over
-    while (chunk > 256 && rows * ((P.n_cand + chunk - 1) / chunk) < 152 * 8) chunk /= 2;
+    while (chunk > 256 && rows * ((P.n_cand + chunk - 1) / chunk) < (int64_t)device_sm_count() * 8) chunk /= 2;
     P.chunk = chunk;
     const int64_t gx = (P.n_cand + chunk - 1) / chunk;
     dim3 grid((unsigned)(gx > 0 ? gx : 1), (unsigned)rows);

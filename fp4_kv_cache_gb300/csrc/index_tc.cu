@@ -8,7 +8,10 @@
 // positions, N = 32 heads per query, K = 128 (two K = 64 steps).  The epilogue reads each
 // position's 32 head dots from tensor memory and forms s = fma32 chain of w_h * ReLU(D_h).
 //
-// Exactness.  The score is defined on D_h = RN32(exact dot).  Each K = 32 block adds an
+// Precision.  The float32 score written out is the fma chain over heads of w_h * max(D_h, 0)
+// with D_h = RN32(exact dot); the selection kernels rank by the exact score and use this
+// one through its error bound, which needs each D_h correctly rounded.  Non-finite scores
+// set CSA2_DEV_SCORE_RANGE.  The per-head dot D_h = RN32(exact dot).  Each K = 32 block adds an
 // integer (< 2^13) times 2^(Xq + Xk - 2); when every term's exponent lies within 9 of the
 // others and in the normal range, every partial sum is exactly representable, so the MMA's
 // float32 accumulation returns the exact dot whatever its order.  That condition is checked
@@ -39,7 +42,6 @@ constexpr int kD = 128;                // indexer head dim of this path
 constexpr int kRowBytes = kD / 2;      // 64 bytes of codes per position
 constexpr int kTile = 128;             // positions per tile (MMA M)
 constexpr int kNPad = 32;              // heads per query, padded to 32
-constexpr int kSms = 152;
 
 // A CTA scores QG queries of one sequence against the same key tiles: MMA N = QG x 32
 // (queries x heads).  A stage holds kMB tiles of 128 positions (one MMA M block each).
@@ -236,6 +238,9 @@ __device__ __noinline__ void recheck_stage(const TcParams &P, const TcSmem<QG> &
             sc = rescore_flagged(todo, sc, kw, g0, P.kc + kbase * kRowBytes, pool, P.pool_mode, P.n_keys, S.b,
                                  reinterpret_cast<const uint8_t *>(S.sfb), S.w[qi], qi, P.H);
             if ((todo >> lane) & 1u) srow[p] = sc;
+            if (__any_sync(0xffffffffu, ((todo >> lane) & 1u) && !(fabsf(sc) <= 3.4028234663852886e38f)) &&
+                lane == 0)
+                dev_flag(P.d_status, CSA2_DEV_SCORE_RANGE);
             if (P.gmax) {
                 const uint32_t gk = __reduce_max_sync(0xffffffffu, valid ? score_key(sc) : 0u);
                 if (lane == 0 && g0 < qlen) P.gmax[(row0 + qi) * P.G + (g0 >> 5)] = gk;
@@ -644,6 +649,7 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
         // accumulator is full, which is after the queries were quantised)
         int64_t qlen[kQPerWarp];
         int qspan[kQPerWarp], qmin[kQPerWarp], qmax[kQPerWarp];
+        bool out_of_range = false;            // a score this warp wrote is not finite
         for (int i = 0;; ++i) {
             const int acc = i % kAcc;
             // the stage itself is not touched here: the MMA's completion frees it
@@ -731,6 +737,7 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
                 if (valid) {
                     P.scores[(row0 + qi) * P.n_cand + cand] = sc;
                     key = score_key(sc);
+                    out_of_range |= !(fabsf(sc) <= 3.4028234663852886e38f);
                 }
                 if (P.gmax) {            // this warp's 32 candidates are one aligned group
                     const uint32_t gk = __reduce_max_sync(0xffffffffu, key);
@@ -759,6 +766,7 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
                 }
             }
         }
+        if (__any_sync(0xffffffffu, out_of_range) && lane == 0) dev_flag(P.d_status, CSA2_DEV_SCORE_RANGE);
     }
 
     tc::tc_fence_before();
@@ -806,7 +814,7 @@ int tc_query_group(const csa2_index_args &a)
 int64_t tc_splits(int64_t units, int64_t n_cand, int ctas_per_sm, int span)
 {
     const int64_t tiles = (n_cand + span - 1) / span;
-    int64_t s = (int64_t)kSms * ctas_per_sm / (units > 0 ? units : 1);
+    int64_t s = (int64_t)device_sm_count() * ctas_per_sm / (units > 0 ? units : 1);
     if (s < 1) s = 1;
     if (s > tiles) s = tiles > 0 ? tiles : 1;
     return s;

@@ -59,17 +59,25 @@ int64_t index_tc_ctas_per_row(const csa2_index_args &a);
 cudaError_t launch_index_tc(const csa2_index_args &a, float *scores, int32_t *row_len,
                             uint32_t *tile_ctr, uint32_t *d_status, cudaStream_t s);
 
-// Top-K over rows of float scores (see csa2_topk).  ws: topk_ws_bytes(rows, n, k).
-size_t topk_ws_bytes(int64_t rows, int64_t n, int32_t k);
+// Top-K over rows of float scores (see csa2_topk).  ws: topk_ws_bytes(rows, n, k, ex != 0).
+// ex != NULL: exact order for the scores of csa2_index_score(*ex); candidates are positions
+// (unit 1) or blocks of `unit` positions whose position scores are pos_scores [rows, pos_n]
+// with valid lengths pos_len.
+size_t topk_ws_bytes(int64_t rows, int64_t n, int32_t k, bool exact);
 cudaError_t launch_topk(const float *scores, int64_t rows, int64_t n, const int32_t *row_len,
                         const uint32_t *group_max, const int32_t *pool, int32_t block, int32_t k,
                         int32_t *idx, float *out_scores, void *ws, uint32_t *d_status,
-                        cudaStream_t s);
-size_t block_candidates_ws_bytes(int64_t rows, int64_t n, int32_t block, int32_t nb);
+                        cudaStream_t s, const csa2_index_args *ex = nullptr, int32_t unit = 1,
+                        const float *pos_scores = nullptr, int64_t pos_n = 0,
+                        const int32_t *pos_len = nullptr);
+size_t block_candidates_ws_bytes(int64_t rows, int64_t n, int32_t block, int32_t nb, bool exact);
 cudaError_t launch_block_candidates(const float *scores, int64_t rows, int64_t n,
                                     const int32_t *row_len, int32_t block, int32_t nb,
                                     int32_t *block_ids, void *ws, uint32_t *d_status,
-                                    cudaStream_t s);
+                                    cudaStream_t s, const csa2_index_args *ex);
+
+// Streaming multiprocessors of the current device (queried once per device).
+int device_sm_count();
 
 size_t sparse_attn_ws_bytes(const csa2_attn_args &a);
 bool attn_tc_eligible(const csa2_attn_args &a);

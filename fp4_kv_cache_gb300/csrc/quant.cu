@@ -420,7 +420,8 @@ int grid_for(int64_t work_items, int per_block)
 {
     int64_t g = (work_items + per_block - 1) / per_block;
     if (g < 1) g = 1;
-    if (g > 152 * 16) g = 152 * 16;
+    const int64_t gmax = (int64_t)device_sm_count() * 16;
+    if (g > gmax) g = gmax;
     return (int)g;
 }
 

@@ -10,6 +10,7 @@
 // entries equal to tau must be taken; a final pass in index order emits every entry
 // above tau and the first `need` entries equal to tau, which yields ascending output.
 #include "common.cuh"
+#include "exact.cuh"
 #include "internal.h"
 
 
@@ -190,7 +191,8 @@ topk_radix_kernel(const float *__restrict__ scores, int64_t n, const int32_t *__
 constexpr int kGThreads = 1024;
 constexpr int kGBins = 2048;
 constexpr int kGroupCap = 8192;         // group keys per row kept on chip (longer rows: wider groups)
-constexpr int kCandCap = 8192;          // candidates per row kept on chip
+constexpr int kCandCap = 16384;         // candidates per row kept on chip (a whole
+                                        // 2,048-block pool of 8 positions fits)
 
 struct GSmem {
     uint32_t hist[2][kGBins];    // double buffer: the next digit pass clears one while
@@ -303,20 +305,214 @@ __device__ __forceinline__ uint32_t g_threshold(const uint32_t *keys, int n, uin
     return prefix;
 }
 
+// ------------------------------------------------------------------ exact order (csa2_topk and
+// csa2_block_candidates with an exact context)
+// The float32 scores s~ the indexer writes are within eps of the exact scores s (see
+// csa2_index_score: (H + 2) 2^-24 A + 2^-149 (sum|w| + H), A = sum_h |w_h| ReLU(d_h)).  With
+// tau~ the k-th largest s~ and a row-wide eps >= that bound:
+//   s~ < tau~ - 2 eps: at least k candidates (those with s~ >= tau~) have s >= tau~ - eps > s,
+//     so the candidate is out;
+//   s~ > tau~ + 2 eps: any candidate with s >= this one's s has s~ > tau~, and fewer than k
+//     do, so it is in;
+//   the rest (the band) are re-scored exactly and the k - (#in) best of them taken by
+//   (exact score desc, candidate asc).
+// eps: for rows with every w_h >= 0, A = s <= (max s~ + eta) / (1 - c); otherwise A is
+// bounded through |d_h| <= sum_b 12 sum_i |2 q_i| 2^(Xq_b + Xk_b - 2) with Xk_b the largest
+// key scale exponent of block b in the sequence (one pass over its scale bytes).  The
+// constants are rounded up by one more 2^-24 A and a factor 2 on eta, which covers the
+// float64 rounding of this arithmetic.
+struct ExactArgs {
+    int H, d;                      // indexer heads, head dim (32, 64 or 128)
+    int32_t n_q;                   // queries per sequence (row r belongs to sequence r / n_q)
+    int64_t n_keys;                // key rows per sequence
+    const uint16_t *q;             // [rows, H, d] bf16
+    const float *w;                // [rows, H]
+    const uint8_t *kc, *ks;        // [B, N, d/2], [B, N, d/32]
+    int unit;                      // 1: candidates are positions; > 1: blocks of `unit` positions
+    const float *pos_scores;       // unit > 1: position scores [rows, pos_n]
+    int64_t pos_n;
+    const int32_t *pos_len;        // unit > 1: valid positions per row
+    uint32_t *band;                // [gridDim.x][kLimbs][CSA2_EXACT_BAND_CAP] exact keys
+    uint32_t *d_status;
+};
+constexpr int kBandCap = CSA2_EXACT_BAND_CAP;
+static_assert(kBandCap <= 2 * kGThreads, "two band entries per thread at most");
+
+__device__ __forceinline__ float key_value(uint32_t key)
+{
+    return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
+}
+
+// Block-wide min and max of one value per thread (all threads call; ends with a barrier).
+__device__ __forceinline__ void block_minmax(uint32_t vmin, uint32_t vmax, uint32_t *s_red, uint32_t &mn, uint32_t &mx)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    vmin = __reduce_min_sync(0xffffffffu, vmin);
+    vmax = __reduce_max_sync(0xffffffffu, vmax);
+    if (lane == 0) { s_red[warp] = vmin; s_red[32 + warp] = vmax; }
+    __syncthreads();
+    mn = 0xffffffffu; mx = 0u;
+    for (int i = 0; i < nw; ++i) { mn = min(mn, s_red[i]); mx = max(mx, s_red[32 + i]); }
+    __syncthreads();
+}
+
+// Largest scale byte of each 32-value block over the n_keys key rows of one sequence
+// (byte b of the result = block b, nb in {1, 2, 4}); block-wide, ends with a barrier.
+__device__ __noinline__ uint32_t key_scale_max(const uint8_t *ks, int64_t n_keys, int nb, uint32_t *s_red)
+{
+    const int64_t nbytes = n_keys * nb;
+    uint32_t r = 0;                           // byte b: largest scale byte of block b
+    int64_t i0 = 0;
+    if (((uintptr_t)ks & 3u) == 0) {
+        // byte j of word v is byte 4v + j, of block (4v + j) % nb = j % nb
+        uint32_t m = 0;
+        const uint32_t *w4 = reinterpret_cast<const uint32_t *>(ks);
+        for (int64_t v = threadIdx.x; v < nbytes / 4; v += blockDim.x) m = __vmaxu4(m, w4[v]);
+        for (int j = 0; j < 4; ++j) r = __vmaxu4(r, ((m >> (8 * j)) & 255u) << (8 * (j % nb)));
+        i0 = nbytes / 4 * 4;
+    }
+    for (int64_t i = i0 + threadIdx.x; i < nbytes; i += blockDim.x)
+        r = __vmaxu4(r, (uint32_t)ks[i] << (8 * (int)(i % nb)));
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) r = __vmaxu4(r, __shfl_xor_sync(0xffffffffu, r, o));
+    if (lane == 0) s_red[warp] = r;
+    __syncthreads();
+    uint32_t t = 0;
+    for (int i = 0; i < nw; ++i) t = __vmaxu4(t, s_red[i]);
+    __syncthreads();
+    return t;
+}
+
+// eps of one row (see above); returns a negative value when the row's scores are not all
+// finite (then no exact pass is made: the indexer has flagged CSA2_DEV_SCORE_RANGE).
+__device__ __noinline__ double row_eps(const exact::QuantQuery &Q, const ExactArgs &X, int64_t seq, uint32_t max_key,
+                                       uint32_t *s_red)
+{
+    const float mval = key_value(max_key);
+    if (max_key == 0u || !(fabsf(mval) <= 3.4028234663852886e38f)) return -1.0;
+    double sumw = 0.0;
+    bool neg = false;
+    for (int h = 0; h < X.H; ++h) {
+        sumw += fabs((double)Q.w[h]);
+        neg |= Q.w[h] < 0.0f;
+    }
+    const double c = (double)(X.H + 3) * 0x1p-24;
+    const double eta = 0x1p-148 * (sumw + X.H);
+    double A;
+    if (!neg) {
+        A = ((double)fmaxf(mval, 0.0f) + eta) / (1.0 - c);
+    } else {
+        const int nb = X.d / 32;
+        const uint32_t km = key_scale_max(X.ks + seq * X.n_keys * nb, X.n_keys, nb, s_red);
+        A = 0.0;
+        for (int h = 0; h < X.H; ++h) {
+            double ah = 0.0;
+            for (int b = 0; b < nb; ++b)
+                ah += 12.0 * (double)Q.q1[h * 4 + b] *
+                      ldexp(1.0, Q.qx[h * 4 + b] + (int)((km >> (8 * b)) & 255u) - 127 - 2);
+            A += fabs((double)Q.w[h]) * ah;
+        }
+    }
+    return (c * A + eta) * (1.0 + 0x1p-40);
+}
+
+// Exact key (limb `lane`) of band candidate i of a row: a position (through the pool), or
+// the largest exact score of a block's positions whose float32 score could be its maximum.
+template <int D>
+__device__ __noinline__ uint32_t unit_key(const exact::QuantQuery &Q, const ExactArgs &X, int64_t row, int64_t seq,
+                                          const int32_t *pool_row, int32_t block, int64_t i, uint32_t unit_lo_key)
+{
+    const int64_t kbase = seq * X.n_keys;
+    if (X.unit == 1) {
+        int64_t p = cand_pos(pool_row, block, i);
+        p = p < 0 ? 0 : (p >= X.n_keys ? X.n_keys - 1 : p);
+        return exact::score_key_limb<D>(Q, X.H, X.kc + (kbase + p) * (D / 2), X.ks + (kbase + p) * (D / 32));
+    }
+    int64_t len = X.pos_len[row];
+    len = len < 0 ? 0 : (len > X.pos_n ? X.pos_n : len);
+    const float *ps = X.pos_scores + row * X.pos_n;
+    uint32_t best = 0;
+    bool have = false;
+#pragma unroll 1
+    for (int j = 0; j < X.unit; ++j) {
+        const int64_t p = i * X.unit + j;
+        if (p >= len || p >= X.n_keys) break;
+        if (score_key(ps[p]) < unit_lo_key) continue;          // cannot be the block's maximum
+        const uint32_t l = exact::score_key_limb<D>(Q, X.H, X.kc + (kbase + p) * (D / 2),
+                                                    X.ks + (kbase + p) * (D / 32));
+        if (!have || exact::compare_keys(l, best) > 0) best = l;
+        have = true;
+    }
+    return best;
+}
+
+// Among n_band band units whose exact keys are in bk (limb-major, stride kBandCap), sets
+// state[u] = 1 for the `take` best by (key desc, unit index asc): limb by limb from the top,
+// the take-th largest limb value among the units still tied splits them into taken, tied
+// and dropped.  Block-wide; act and vals are scratch of n_band entries in shared memory.
+__device__ __noinline__ void select_band(const uint32_t *bk, int n_band, uint32_t take, uint8_t *state,
+                                         uint32_t *act, uint32_t *vals, GSmem &S, uint32_t *s_red)
+{
+    const int tid = threadIdx.x;
+    for (int i = tid; i < n_band; i += kGThreads) { state[i] = 0; act[i] = (uint32_t)i; }
+    __syncthreads();
+    int n_act = n_band;
+    uint32_t remaining = take;
+#pragma unroll 1
+    for (int j = exact::kLimbs - 1; j >= 0; --j) {
+        if (remaining == 0 || remaining >= (uint32_t)n_act) break;
+        uint32_t vmin = 0xffffffffu, vmax = 0u;
+        for (int i = tid; i < n_act; i += kGThreads) {
+            const uint32_t v = bk[(size_t)j * kBandCap + act[i]];
+            vals[i] = v;
+            vmin = min(vmin, v);
+            vmax = max(vmax, v);
+        }
+        uint32_t mn, mx;
+        block_minmax(vmin, vmax, s_red, mn, mx);           // barrier: vals visible
+        if (mn == mx) continue;                             // this limb ties them all
+        uint32_t need_eq;
+        const uint32_t v = g_threshold(vals, n_act, remaining, S, need_eq, 3);
+        const int r0 = min(2 * tid, n_act), r1 = min(r0 + 2, n_act);
+        uint32_t keep0 = 0, keep1 = 0;
+        int nk = 0;
+        for (int i = r0; i < r1; ++i) {
+            if (vals[i] > v) state[act[i]] = 1;
+            else if (vals[i] == v) { if (nk == 0) keep0 = act[i]; else keep1 = act[i]; ++nk; }
+        }
+        uint32_t tot;
+        const uint32_t at = block_excl_count_sum((uint32_t)nk, S.warp, tot);   // all reads done
+        if (nk > 0) act[at] = keep0;
+        if (nk > 1) act[at + 1] = keep1;
+        __syncthreads();
+        n_act = (int)tot;
+        remaining = need_eq;
+    }
+    for (int i = tid; i < n_act && i < (int)remaining; i += kGThreads) state[act[i]] = 1;
+    __syncthreads();
+}
+
+template <bool EXACT, int D>
 __global__ void __launch_bounds__(kGThreads, 1)
-topk_gmax_kernel(const float *__restrict__ scores, int64_t n, const int32_t *__restrict__ row_len,
+topk_gmax_kernel(const float *__restrict__ scores, int64_t n, int64_t rows, const int32_t *__restrict__ row_len,
                  const int32_t *__restrict__ pool, int32_t block, int32_t k, int32_t *__restrict__ idx,
-                 float *__restrict__ out_scores, const uint32_t *__restrict__ gkeys, int32_t gs, int64_t G)
+                 float *__restrict__ out_scores, const uint32_t *__restrict__ gkeys, int32_t gs, int64_t G,
+                 const ExactArgs X)
 {
     extern __shared__ uint32_t g_sm[];
     uint32_t *s_g = g_sm;                                  // group keys, then candidate-group list
     uint32_t *s_ck = g_sm + kGroupCap;                     // candidate keys
     int32_t *s_cp = reinterpret_cast<int32_t *>(s_ck + kCandCap);   // candidate positions (index)
     __shared__ GSmem S;
+    __shared__ uint32_t s_red[64];
+    __shared__ exact::QuantQuery QQ;                       // exact order: the row's query
     const int tid = threadIdx.x;
-    const int64_t row = blockIdx.x;
     pdl_wait();                                            // scores come from the kernel before
     pdl_allow_dependents();
+#pragma unroll 1
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+    __syncthreads();                                       // the previous row is done with shared memory
     int64_t len = row_len ? (int64_t)row_len[row] : n;
     len = len < 0 ? 0 : (len > n ? n : len);
     const float *s = scores + row * n;
@@ -329,23 +525,42 @@ topk_gmax_kernel(const float *__restrict__ scores, int64_t n, const int32_t *__r
             out[i] = i < len ? (int32_t)cand_pos(pool_row, block, i) : -1;
             if (out_s) out_s[i] = i < len ? s[i] : 0.0f;
         }
-        return;
+        continue;
     }
     const int ng = (int)((len + gs - 1) / gs);
     if (ng > kGroupCap) {                                  // too long for the on-chip path
         radix_select_row(scores, n, row_len, pool, block, k, idx, out_scores, row);
-        return;
+        if (EXACT && tid == 0) dev_flag(X.d_status, CSA2_DEV_BAND_LIMIT);
+        continue;
     }
-    for (int g = tid; g < ng; g += kGThreads) s_g[g] = gkeys[row * G + g];
+    uint32_t gmx = 0;
+    for (int g = tid; g < ng; g += kGThreads) {
+        const uint32_t v = gkeys[row * G + g];
+        s_g[g] = v;
+        gmx = max(gmx, v);
+    }
     __syncthreads();
+    // exact order: the row's error bound of the float32 scores (negative: none made)
+    double eps = -1.0;
+    int64_t seq = 0;
+    if constexpr (EXACT) {
+        seq = row / X.n_q;
+        exact::quantise_query(QQ, X.q + row * (int64_t)X.H * D, X.w + row * (int64_t)X.H, X.H, D);
+        uint32_t mn, mx;
+        block_minmax(0xffffffffu, gmx, s_red, mn, mx);
+        eps = row_eps(QQ, X, seq, mx, s_red);
+    }
     // a lower bound of the k-th largest group key is enough to keep every top-k element
-    // (the groups above the bound are a superset of those above the exact key)
+    // (the groups above the bound are a superset of those above the exact key); in exact
+    // order the bound is lowered by 2 eps so the whole band is gathered
     uint32_t need0;
-    const uint32_t tau0 = ng > k ? g_threshold(s_g, ng, (uint32_t)k, S, need0, 2) : 0u;
+    uint32_t tau0 = ng > k ? g_threshold(s_g, ng, (uint32_t)k, S, need0, 2) : 0u;
+    if (EXACT && eps >= 0.0 && tau0 != 0u)
+        tau0 = score_key(__double2float_rd((double)key_value(tau0) - 2.0 * eps));
 
     // candidate groups (key >= tau0), compacted in place in ascending order: thread t owns
     // the run [t*run, (t+1)*run) and writes only below its own run after everyone has read
-    const int run = (ng + kGThreads - 1) / kGThreads;        // <= 32
+    const int run = (ng + kGThreads - 1) / kGThreads;        // <= 8
     const int r0 = min(tid * run, ng), r1 = min(r0 + run, ng);
     uint32_t mine = 0;                                      // bit j: group r0+j is a candidate
     for (int i = r0; i < r1; ++i) mine |= (s_g[i] >= tau0 ? 1u : 0u) << (i - r0);
@@ -357,7 +572,6 @@ topk_gmax_kernel(const float *__restrict__ scores, int64_t n, const int32_t *__r
             if ((mine >> (i - r0)) & 1u) s_g[o++] = (uint32_t)i;
     }
     __syncthreads();
-
     // gather candidates, in position order: one thread per candidate group reads its
     // scores (groups of 32 as eight 16-byte loads, all in flight at once) and keeps a bit
     // mask of its elements >= tau0; after a scan of the counts it walks the mask in a
@@ -365,6 +579,7 @@ topk_gmax_kernel(const float *__restrict__ scores, int64_t n, const int32_t *__r
     // code runs once per row, so it is kept small.
     const bool vec = gs == 32 && ((reinterpret_cast<uintptr_t>(s) & 15u) == 0);   // 16-byte rows
     uint32_t n_c = 0;
+    bool overflow = false;
 #pragma unroll 1
     for (uint32_t base = 0; base < n_cg; base += kGThreads) {
         const uint32_t j = base + tid;
@@ -395,8 +610,8 @@ topk_gmax_kernel(const float *__restrict__ scores, int64_t n, const int32_t *__r
         uint32_t tot;
         uint32_t o = n_c + block_excl_count_sum(cnt, S.warp, tot);
         if (n_c + tot > kCandCap) {                        // does not fit on chip: fall back
-            radix_select_row(scores, n, row_len, pool, block, k, idx, out_scores, row);
-            return;
+            overflow = true;
+            break;
         }
         if (j < n_cg) {
             if (vec && g0 + 32 <= n) {
@@ -419,11 +634,74 @@ topk_gmax_kernel(const float *__restrict__ scores, int64_t n, const int32_t *__r
         n_c += tot;
     }
     __syncthreads();
-    // exact selection among the candidates (n_c >= k), emitted in position order
+    if (overflow) {                                        // does not fit on chip: fall back
+        radix_select_row(scores, n, row_len, pool, block, k, idx, out_scores, row);
+        if (EXACT && tid == 0) dev_flag(X.d_status, CSA2_DEV_BAND_LIMIT);
+        continue;
+    }
+    // selection among the candidates (n_c >= k) in float order: the k-th key tau and how
+    // many candidates equal to it are taken
     uint32_t need;
-    const uint32_t tau = g_threshold(s_ck, (int)n_c, (uint32_t)k, S, need, 3);
+    uint32_t tau = g_threshold(s_ck, (int)n_c, (uint32_t)k, S, need, 3);
     const int crun = ((int)n_c + kGThreads - 1) / kGThreads;
     const int c0 = min(tid * crun, (int)n_c), c1 = min(c0 + crun, (int)n_c);
+    if constexpr (EXACT) {
+        if (eps >= 0.0 && tau != 0u) {
+            // the band [tau~ - 2 eps, tau~ + 2 eps] in key terms; above it: selected
+            const double tv = (double)key_value(tau);
+            const uint32_t lo_key = score_key(__double2float_rd(tv - 2.0 * eps));
+            const uint32_t hi_key = score_key(__double2float_ru(tv + 2.0 * eps));
+            uint32_t n_hi = 0, n_bd = 0;
+            for (int i = c0; i < c1; ++i) {
+                n_hi += s_ck[i] > hi_key;
+                n_bd += s_ck[i] >= lo_key && s_ck[i] <= hi_key;
+            }
+            uint32_t tot;
+            const uint32_t before = block_excl_count_sum((n_hi << 16) | n_bd, S.warp, tot);
+            const uint32_t n_in = tot >> 16, n_band = tot & 0xffffu;
+            const uint32_t take = (uint32_t)k > n_in ? (uint32_t)k - n_in : 0u;
+            uint32_t *s_band = s_g;                        // band candidates, in position order
+            uint32_t *s_act = s_g + kBandCap;
+            uint32_t *s_val = s_g + 2 * kBandCap;
+            uint8_t *s_state = reinterpret_cast<uint8_t *>(s_g + 3 * kBandCap);
+            if (n_band <= (uint32_t)kBandCap) {
+                uint32_t o = before & 0xffffu;
+                for (int i = c0; i < c1; ++i)
+                    if (s_ck[i] >= lo_key && s_ck[i] <= hi_key) s_band[o++] = (uint32_t)i;
+            }
+            __syncthreads();
+            if (n_band < take) {
+                // cannot happen (every candidate >= tau~ is above or in the band): float order
+            } else if (n_band > take && n_band > (uint32_t)kBandCap) {
+                if (tid == 0) dev_flag(X.d_status, CSA2_DEV_BAND_LIMIT);    // float order stays
+            } else {
+                if (n_band > take) {
+                    // exact keys of the band candidates, one warp each, into this CTA's slot
+                    uint32_t *bk = X.band + (size_t)blockIdx.x * exact::kLimbs * kBandCap;
+                    const int lane = tid & 31, warp = tid >> 5;
+#pragma unroll 1
+                    for (uint32_t u = warp; u < n_band; u += kGThreads / 32) {
+                        const uint32_t i = s_band[u];
+                        const uint32_t ulo = X.unit > 1
+                            ? score_key(__double2float_rd((double)key_value(s_ck[i]) - 2.0 * eps)) : 0u;
+                        const uint32_t limb = unit_key<D>(QQ, X, row, seq, pool_row, block, s_cp[i], ulo);
+                        if (lane < exact::kLimbs) bk[(size_t)lane * kBandCap + u] = limb;
+                    }
+                    __syncthreads();
+                    select_band(bk, (int)n_band, take, s_state, s_act, s_val, S, s_red);
+                } else {
+                    for (uint32_t u = tid; u < n_band; u += kGThreads) s_state[u] = 1;
+                    __syncthreads();
+                }
+                // band candidates taken rank above tau~ + 2 eps, the others below every
+                // candidate: the float-order emission below then takes exactly these
+                for (uint32_t u = tid; u < n_band; u += kGThreads) s_ck[s_band[u]] = s_state[u] ? 0xffffffffu : 0u;
+                __syncthreads();
+                tau = hi_key;
+                need = 0;
+            }
+        }
+    }
     uint32_t n_gt = 0, n_eq = 0;
     for (int i = c0; i < c1; ++i) {
         n_gt += s_ck[i] > tau;
@@ -446,6 +724,7 @@ topk_gmax_kernel(const float *__restrict__ scores, int64_t n, const int32_t *__r
             ++o;
         }
     }
+    }   // rows
 }
 
 int32_t group_size_for(int64_t n)
@@ -477,18 +756,50 @@ __global__ void block_max_kernel(const float *__restrict__ scores, int64_t n,
 
 } // namespace
 
-size_t topk_ws_bytes(int64_t rows, int64_t n, int32_t)
+namespace {
+
+constexpr int64_t kExactSlots = 160;      // per-CTA band slots of the exact pass
+
+size_t align256(size_t a) { return (a + 255) & ~(size_t)255; }
+
+int64_t exact_slots(int64_t rows) { return rows < kExactSlots ? rows : kExactSlots; }
+
+size_t group_keys_bytes(int64_t rows, int64_t n)
 {
     const int64_t G = (n + group_size_for(n) - 1) / group_size_for(n);
     return (size_t)rows * (size_t)(G > 0 ? G : 1) * sizeof(uint32_t);
 }
 
+// The selection kernel for float order, or exact order at the indexer head dim.
+template <bool EXACT, int D>
+cudaError_t launch_gmax(unsigned grid, size_t smem, cudaStream_t s, const float *scores, int64_t n, int64_t rows,
+                        const int32_t *row_len, const int32_t *pool, int32_t block, int32_t k, int32_t *idx,
+                        float *out_scores, const uint32_t *gkeys, int32_t gs, int64_t G, const ExactArgs &X)
+{
+    cudaError_t e = cudaFuncSetAttribute(topk_gmax_kernel<EXACT, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(topk_gmax_kernel<EXACT, D>, dim3(grid), dim3(kGThreads), smem, s, 1, scores, n, rows,
+                      row_len, pool, block, k, idx, out_scores, gkeys, gs, G, X);
+}
+
+} // namespace
+
+size_t topk_ws_bytes(int64_t rows, int64_t n, int32_t, bool exact)
+{
+    size_t a = group_keys_bytes(rows, n);
+    if (exact) a = align256(a) + (size_t)exact_slots(rows) * exact::kLimbs * kBandCap * sizeof(uint32_t);
+    return a;
+}
+
 cudaError_t launch_topk(const float *scores, int64_t rows, int64_t n, const int32_t *row_len,
                         const uint32_t *group_max, const int32_t *pool, int32_t block, int32_t k,
-                        int32_t *idx, float *out_scores, void *ws, uint32_t *, cudaStream_t s)
+                        int32_t *idx, float *out_scores, void *ws, uint32_t *d_status, cudaStream_t s,
+                        const csa2_index_args *ex, int32_t unit, const float *pos_scores, int64_t pos_n,
+                        const int32_t *pos_len)
 {
     if (rows == 0 || k == 0) return cudaSuccess;
-    if (rows > 0x7fffffffLL || !ws) {
+    if (!ex && (rows > 0x7fffffffLL || !ws)) {
         topk_radix_kernel<<<(unsigned)rows, kTopkThreads, 0, s>>>(scores, n, row_len, pool, block, k,
                                                                  idx, out_scores);
         return cudaGetLastError();
@@ -505,38 +816,62 @@ cudaError_t launch_topk(const float *scores, int64_t rows, int64_t n, const int3
             group_max32_kernel<<<(unsigned)blocks, 256, 0, s>>>(scores, n, row_len, rows, G, gk);
         } else {
             int64_t blocks = (rows * G * 32 + 255) / 256;
-            if (blocks > 152 * 16) blocks = 152 * 16;
+            const int64_t cap = (int64_t)device_sm_count() * 16;
+            if (blocks > cap) blocks = cap;
             group_max_kernel<<<(unsigned)blocks, 256, 0, s>>>(scores, n, row_len, rows, gs, G, gk);
         }
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     const size_t smem = (size_t)(kGroupCap + 2 * kCandCap) * sizeof(uint32_t);
-    cudaError_t e = cudaFuncSetAttribute(topk_gmax_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    return launch_pdl(topk_gmax_kernel, dim3((unsigned)rows), dim3(kGThreads), smem, s, 1, scores, n, row_len,
-                      pool, block, k, idx, out_scores, gkeys, gs, G);
+    ExactArgs X = {};
+    if (!ex) return launch_gmax<false, 0>((unsigned)rows, smem, s, scores, n, rows, row_len, pool, block, k, idx,
+                                          out_scores, gkeys, gs, G, X);
+    // exact order: persistent CTAs (at most one per SM and per band slot), rows strided
+    X.H = ex->n_heads;
+    X.d = ex->head_dim;
+    X.n_q = ex->n_q;
+    X.n_keys = ex->n_keys;
+    X.q = ex->q;
+    X.w = ex->w;
+    X.kc = ex->k_codes;
+    X.ks = ex->k_scales;
+    X.unit = unit;
+    X.pos_scores = pos_scores;
+    X.pos_n = pos_n;
+    X.pos_len = pos_len;
+    X.band = reinterpret_cast<uint32_t *>(static_cast<char *>(ws) + align256(group_keys_bytes(rows, n)));
+    X.d_status = d_status;
+    int64_t grid = exact_slots(rows);
+    if (grid > device_sm_count()) grid = device_sm_count();
+    switch (ex->head_dim) {
+    case 32: return launch_gmax<true, 32>((unsigned)grid, smem, s, scores, n, rows, row_len, pool, block, k, idx,
+                                          out_scores, gkeys, gs, G, X);
+    case 64: return launch_gmax<true, 64>((unsigned)grid, smem, s, scores, n, rows, row_len, pool, block, k, idx,
+                                          out_scores, gkeys, gs, G, X);
+    case 128: return launch_gmax<true, 128>((unsigned)grid, smem, s, scores, n, rows, row_len, pool, block, k,
+                                            idx, out_scores, gkeys, gs, G, X);
+    default: return cudaErrorInvalidValue;
+    }
 }
 
-size_t block_candidates_ws_bytes(int64_t rows, int64_t n, int32_t block, int32_t nb)
+size_t block_candidates_ws_bytes(int64_t rows, int64_t n, int32_t block, int32_t nb, bool exact)
 {
     const int64_t nbmax = (n + block - 1) / block;
-    size_t a = (size_t)rows * (size_t)nbmax * sizeof(float);
-    a = (a + 255) & ~(size_t)255;
-    a += (size_t)rows * sizeof(int32_t);
-    a = (a + 255) & ~(size_t)255;
-    return a + topk_ws_bytes(rows, nbmax, nb);
+    size_t a = align256((size_t)rows * (size_t)nbmax * sizeof(float));
+    a = align256(a + (size_t)rows * sizeof(int32_t));
+    return a + topk_ws_bytes(rows, nbmax, nb, exact);
 }
 
 cudaError_t launch_block_candidates(const float *scores, int64_t rows, int64_t n,
                                     const int32_t *row_len, int32_t block, int32_t nb,
                                     int32_t *block_ids, void *ws, uint32_t *d_status,
-                                    cudaStream_t s)
+                                    cudaStream_t s, const csa2_index_args *ex)
 {
     if (rows == 0 || nb == 0) return cudaSuccess;
     const int64_t nbmax = (n + block - 1) / block;
     float *bscores = static_cast<float *>(ws);
-    size_t off = ((size_t)rows * (size_t)nbmax * sizeof(float) + 255) & ~(size_t)255;
+    const size_t off = align256((size_t)rows * (size_t)nbmax * sizeof(float));
     int32_t *brow_len = reinterpret_cast<int32_t *>(static_cast<char *>(ws) + off);
     int64_t gx = (nbmax + 255) / 256;
     if (gx > 64) gx = 64;
@@ -545,9 +880,9 @@ cudaError_t launch_block_candidates(const float *scores, int64_t rows, int64_t n
                                                                         nbmax, bscores, brow_len);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const size_t off2 = (off + (size_t)rows * sizeof(int32_t) + 255) & ~(size_t)255;
+    const size_t off2 = align256(off + (size_t)rows * sizeof(int32_t));
     return launch_topk(bscores, rows, nbmax, brow_len, nullptr, nullptr, 1, nb, block_ids, nullptr,
-                       static_cast<char *>(ws) + off2, d_status, s);
+                       static_cast<char *>(ws) + off2, d_status, s, ex, block, scores, n, row_len);
 }
 
 } // namespace csa2

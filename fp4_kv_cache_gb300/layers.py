@@ -60,14 +60,16 @@ def _attend(cache: Cache, x: LayerInput, idx, window, d_v, sm_scale, d_status, s
 def full_layer(cache: Cache, x: LayerInput, k: int = 512, window: int = 128, d_v: int = 512,
                build_pool: bool = False, n_blocks: int = 2048, block: int = 8,
                sm_scale: Optional[float] = None, d_status=None, stream=None) -> LayerOutput:
-    """Full mode: score every visible entry, Top-K (and, for the decoder's first Full
-    layer, the block pool of report §2.3.2), then attend."""
+    """Full mode: score every visible entry, Top-K by the exact score (and, for the
+    decoder's first Full layer, the block pool of report §2.3.2), then attend."""
     n = cache.k_codes.shape[1]
     gmax = torch.empty(x.q_idx.shape[:2] + ((n + 31) // 32,), dtype=torch.int32, device=x.q_idx.device)
-    scores, row_len = csa2.index_score(x.q_idx, x.w_idx, cache.k_codes, cache.k_scales, x.q_pos,
-                                       cache.ratio_m, None, block, d_status, stream, group_max=gmax)
-    idx = csa2.topk(scores, k, row_len, None, block, False, d_status, stream, group_max=gmax)
-    pool = csa2.block_candidates(scores, n_blocks, row_len, block, d_status, stream) \
+    scores, row_len, args = csa2.index_score(x.q_idx, x.w_idx, cache.k_codes, cache.k_scales, x.q_pos,
+                                             cache.ratio_m, None, block, d_status, stream, group_max=gmax,
+                                             want_args=True)
+    idx = csa2.topk(scores, k, row_len, None, block, False, d_status, stream, group_max=gmax,
+                    exact=args)
+    pool = csa2.block_candidates(scores, n_blocks, row_len, block, d_status, stream, exact=args) \
         if build_pool else None
     out, lse = _attend(cache, x, idx, window, d_v, sm_scale, d_status, stream)
     return LayerOutput(out, lse, idx, pool, scores)
@@ -80,10 +82,11 @@ def reindex_layer(cache: Cache, x: LayerInput, pool_blocks: torch.Tensor, k: int
     at the positions of the pool; its own Top-K inside the pool; then attend."""
     n = pool_blocks.shape[-1] * block
     gmax = torch.empty(x.q_idx.shape[:2] + ((n + 31) // 32,), dtype=torch.int32, device=x.q_idx.device)
-    scores, row_len = csa2.index_score(x.q_idx, x.w_idx, cache.k_codes, cache.k_scales, x.q_pos,
-                                       cache.ratio_m, pool_blocks, block, d_status, stream,
-                                       group_max=gmax)
-    idx = csa2.topk(scores, k, row_len, pool_blocks, block, False, d_status, stream, group_max=gmax)
+    scores, row_len, args = csa2.index_score(x.q_idx, x.w_idx, cache.k_codes, cache.k_scales, x.q_pos,
+                                             cache.ratio_m, pool_blocks, block, d_status, stream,
+                                             group_max=gmax, want_args=True)
+    idx = csa2.topk(scores, k, row_len, pool_blocks, block, False, d_status, stream, group_max=gmax,
+                    exact=args)
     out, lse = _attend(cache, x, idx, window, d_v, sm_scale, d_status, stream)
     return LayerOutput(out, lse, idx, pool_blocks, scores)
 

@@ -70,6 +70,13 @@ typedef enum {
 #define CSA2_DEV_BAD_POOL 0x2u   /* pool block ids not ascending-unique, -1 padded, in range */
 #define CSA2_DEV_NONFINITE 0x4u  /* a quantiser block held Inf/NaN (its output unspecified) */
 #define CSA2_DEV_TIMEOUT 0x8u    /* a bounded device wait gave up; outputs unspecified      */
+#define CSA2_DEV_SCORE_RANGE 0x10u /* an indexer score left the float32 range (Inf/NaN): the */
+                                   /* exact-order guarantee of the selections made on these */
+                                   /* scores does not hold                                  */
+#define CSA2_DEV_BAND_LIMIT 0x20u  /* a selection row had more candidates within the float32 */
+                                   /* scores' error bound of its K-th score than the exact   */
+                                   /* pass holds (CSA2_EXACT_BAND_CAP); that row follows the */
+                                   /* float32 order                                          */
 
 typedef enum { CSA2_BF16 = 0, CSA2_F32 = 1 } csa2_dtype;
 
@@ -187,12 +194,17 @@ CSA2_API csa2_status csa2_rope_quant_fp4(const csa2_rope_quant_job *jobs, int32_
 /* csa2_index_score -- indexer scores (report §2.3: the indexer scores main-KV entries  */
 /* with indexer Q and indexer K; §2.3.2: Reindex layers score only the pool).           */
 /*                                                                                    */
-/* Score of a candidate position t for a query with heads h = 0..H-1:                 */
-/*   q_hat = MXFP4(q_h) (quantised inside the call, 32-value blocks, same rule as       */
-/*   csa2_quant_fp4), D_h = float32 round-to-nearest-even of the exact dot             */
-/*   q_hat_h . k_hat_t, and s = float32 fma chain s <- fma(w_h, max(D_h, 0), s) over     */
-/*   h = 0..H-1 from s = +0.  (The pages give no formula; the head-weighted ReLU sum is */
-/*   the workload's definition, and this precision is the one the kernels use.)        */
+/* Score of a candidate position t for a query with heads h = 0..H-1 (the pages give   */
+/* no formula; the head-weighted ReLU sum is the workload's definition):               */
+/*   s_t = sum_h w_h * max(0, q_hat_h . k_hat_t),  q_hat = MXFP4(q_h) (quantised inside */
+/*   the call, 32-value blocks, same rule as csa2_quant_fp4), w_h the exact value of    */
+/*   the float32 weight.  Selections (csa2_topk / csa2_block_candidates with `exact`)   */
+/*   rank positions by this exact value.  The float32 scores written out here are its  */
+/*   approximation: D_h = float32 round-to-nearest-even of the exact dot, s = float32   */
+/*   fma chain s <- fma(w_h, max(D_h, 0), s) over h = 0..H-1 from s = +0, which is      */
+/*   within (H + 2) 2^-24 A_t + 2^-149 (sum_h |w_h| + H) of s_t, A_t = sum_h |w_h| *    */
+/*   max(0, q_hat_h . k_hat_t), whenever it is finite.  A score that is not finite sets */
+/*   CSA2_DEV_SCORE_RANGE.                                                              */
 /* Visibility: entry j covers tokens [j*m, j*m+m-1] (no overlap, report §2.3) and a     */
 /* query at token position p sees entries with (j+1)*m - 1 <= p:                       */
 /*   n_vis = min(n_keys, (p + 1) / m).                                                  */
@@ -226,7 +238,8 @@ typedef struct {
  * candidate i is position i (FULL) or pool_blocks[i/block]*block + i%block (POOL).
  * row_len [B, T] int32: the candidates 0..row_len-1 of each row are the valid ones
  * (FULL: n_vis; POOL: the pool positions that exist and are visible -- a prefix because
- * the pool is ascending).  Entries at or beyond row_len are left unwritten. */
+ * the pool is ascending).  Entries at or beyond row_len are left unwritten.  row_len is
+ * required (not NULL) when the scores are to be selected with `exact`. */
 /* Workspace: per-row tile counters.  Zero-fill it before its first use; every call     */
 /* leaves it zero-filled again (a call that raised CSA2_DEV_TIMEOUT may not: zero it     */
 /* again before reusing it).                                                            */
@@ -237,37 +250,55 @@ CSA2_API csa2_status csa2_index_score(const csa2_index_args *a, float *scores, i
 /* ---------------------------------------------------------------------------------- */
 /* csa2_topk -- Top-K selection (report §2.3: Top-K entries per query; §4.2.1: K=512).  */
 /* For each of `rows` rows of n candidates: the k candidates with the largest scores,   */
-/* ties broken by the lower candidate index; float order (-0 == +0), NaN below every    */
-/* number.  Only candidates 0..row_len[r]-1 compete (row_len NULL: all n).             */
+/* ties broken by the lower candidate index.  Only candidates 0..row_len[r]-1 compete   */
+/* (row_len NULL: all n).                                                              */
+/*   exact == NULL: the scores are the given floats, in float order (-0 == +0, NaN     */
+/*     below every number).                                                            */
+/*   exact != NULL: scores, row_len and group_max are the outputs of csa2_index_score  */
+/*     called with *exact (rows = batch * n_q, n = its n_cand, row_len required), and   */
+/*     the candidates are ranked by their EXACT indexer scores (see csa2_index_score).  */
+/*     The float32 scores decide every candidate farther than their error bound from   */
+/*     the k-th score; the candidates within it are re-scored exactly on the GPU (wide  */
+/*     integers) and ordered by the exact values.  pool_blocks / block must be those of */
+/*     *exact (POOL) or NULL / any (FULL).  A row with more than CSA2_EXACT_BAND_CAP     */
+/*     such candidates sets CSA2_DEV_BAND_LIMIT and follows the float32 order.          */
 /* idx [rows, k] int32: the selected POSITIONS in ascending order, padded with -1 when  */
 /* fewer than k compete.  Position of candidate i: i, or with pool_blocks != NULL        */
 /* ([rows, n/block]) pool_blocks[i/block]*block + i%block -- ascending candidates map to */
 /* ascending positions, so the tie rule is the lower position.                         */
-/* out_scores (nullable) [rows, k]: the score of each selected entry (0 for padding).   */
+/* out_scores (nullable) [rows, k]: the float32 score of each selected entry (0 for     */
+/* padding).                                                                           */
 /* group_max (nullable) [rows, ceil(n/32)]: the group_max output of the csa2_index_score */
 /* call that wrote these scores and row_len; when given, the call skips computing it.  */
 /* (Used only while n <= 2^20; longer rows use wider groups and compute their own.)     */
+/* Workspace: csa2_topk_workspace_size(rows, n, k, exact) bytes.                        */
 /* ---------------------------------------------------------------------------------- */
-CSA2_API size_t csa2_topk_workspace_size(int64_t rows, int64_t n, int32_t k);
+#define CSA2_EXACT_BAND_CAP 2048
+CSA2_API size_t csa2_topk_workspace_size(int64_t rows, int64_t n, int32_t k, const csa2_index_args *exact);
 CSA2_API csa2_status csa2_topk(const float *scores, int64_t rows, int64_t n, const int32_t *row_len,
                       const uint32_t *group_max, const int32_t *pool_blocks, int32_t block,
-                      int32_t k, int32_t *idx, float *out_scores, void *ws, size_t ws_bytes,
-                      uint32_t *d_status, csa2_stream stream);
+                      const csa2_index_args *exact, int32_t k, int32_t *idx, float *out_scores,
+                      void *ws, size_t ws_bytes, uint32_t *d_status, csa2_stream stream);
 
 /* ---------------------------------------------------------------------------------- */
 /* csa2_block_candidates -- the hierarchical sparse indexer's block pool (report §2.3.2 */
 /* and Figure 5; review: block selection uses the global position scores directly).     */
 /* For each row of FULL-mode scores (candidate i = position i, valid i < row_len): block */
 /* b covers positions [b*block, b*block+block-1]; its score is the max of its valid     */
-/* positions' scores (NaN ignored; all-NaN -> NaN).  block_ids [rows, nb]: the nb best  */
-/* blocks by (score desc, block id asc), ascending, -1 padded (at most 2,048 blocks of  */
-/* 8 = 16,384 positions in the report's configuration, §4.2.1).                         */
+/* positions' scores.  block_ids [rows, nb]: the nb best blocks by (score desc, block   */
+/* id asc), ascending, -1 padded (at most 2,048 blocks of 8 = 16,384 positions in the   */
+/* report's configuration, §4.2.1).                                                     */
+/*   exact == NULL: scores are the given floats (NaN ignored; all-NaN -> NaN).          */
+/*   exact != NULL: scores and row_len are the outputs of csa2_index_score with *exact  */
+/*     (FULL mode; row_len required) and a block's score is the largest EXACT score of  */
+/*     its valid positions, resolved as in csa2_topk (CSA2_DEV_BAND_LIMIT likewise).    */
 /* ---------------------------------------------------------------------------------- */
-CSA2_API size_t csa2_block_candidates_workspace_size(int64_t rows, int64_t n, int32_t block, int32_t nb);
+CSA2_API size_t csa2_block_candidates_workspace_size(int64_t rows, int64_t n, int32_t block, int32_t nb,
+                                                     const csa2_index_args *exact);
 CSA2_API csa2_status csa2_block_candidates(const float *scores, int64_t rows, int64_t n,
                                   const int32_t *row_len, int32_t block, int32_t nb,
-                                  int32_t *block_ids, void *ws, size_t ws_bytes,
-                                  uint32_t *d_status, csa2_stream stream);
+                                  const csa2_index_args *exact, int32_t *block_ids, void *ws,
+                                  size_t ws_bytes, uint32_t *d_status, csa2_stream stream);
 
 /* ---------------------------------------------------------------------------------- */
 /* csa2_sparse_attn -- core attention (report §2.3 and §2.3.1: every mode attends the   */

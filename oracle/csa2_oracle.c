@@ -28,6 +28,7 @@
  * Build: gcc -O2 -std=c11 -fopenmp -ffp-contract=off -shared -fPIC.
  */
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 #include <math.h>
 #include <limits.h>
@@ -329,25 +330,34 @@ static float dyadic_sum_to_f32(int nb, const int64_t *I, const int *e)
     return big_round_f32(acc);
 }
 
-/* D = RN32(qhat . khat) for one head and one key row, both MXFP4 of dim d. */
-static float exact_dot_f32(int d, const uint8_t *qc, const uint8_t *qs,
-                           const uint8_t *kc, const uint8_t *ks)
+/* Twice the signed E2M1 value of each of the d codes of a packed row (element 2i in the
+ * low nibble of byte i). */
+static void decode_twice(int d, const uint8_t *codes, int *out)
 {
-    int nb = d / 32;
-    int64_t I[64];
-    int e[64];
-    for (int b = 0; b < nb; ++b) {
+    for (int j = 0; j < d; ++j)
+        out[j] = e2m1_twice_signed((j % 2 == 0) ? (codes[j / 2] & 15) : (codes[j / 2] >> 4));
+}
+
+/* Integer block dots I_b = sum_{i in b} (2 q_i)(2 k_i) and their exponents
+ * e_b = Xq_b + Xk_b - 2 of one head and one key row (twice-values tq, tk). */
+static void block_dots(int d, const int *tq, const uint8_t *qs, const int *tk, const uint8_t *ks,
+                       int64_t *I, int *e)
+{
+    for (int b = 0; b < d / 32; ++b) {
         int64_t acc = 0;
-        for (int i = 0; i < 32; ++i) {
-            int j = b * 32 + i;
-            int cq = (j % 2 == 0) ? (qc[j / 2] & 15) : (qc[j / 2] >> 4);
-            int ck = (j % 2 == 0) ? (kc[j / 2] & 15) : (kc[j / 2] >> 4);
-            acc += (int64_t)e2m1_twice_signed(cq) * e2m1_twice_signed(ck);
-        }
+        for (int i = 0; i < 32; ++i) acc += (int64_t)tq[b * 32 + i] * tk[b * 32 + i];
         I[b] = acc;
         e[b] = ((int)qs[b] - 127) + ((int)ks[b] - 127) - 2;
     }
-    return dyadic_sum_to_f32(nb, I, e);
+}
+
+/* D = RN32(qhat . khat) for one head and one key row, both MXFP4 of dim d (twice-values). */
+static float exact_dot_f32(int d, const int *tq, const uint8_t *qs, const int *tk, const uint8_t *ks)
+{
+    int64_t I[64];
+    int e[64];
+    block_dots(d, tq, qs, tk, ks, I, e);
+    return dyadic_sum_to_f32(d / 32, I, e);
 }
 
 /* Per-head dots D_h (float32) of one quantised query against listed key rows.
@@ -356,11 +366,17 @@ void orc_head_dots(int H, int d, const uint8_t *qc, const uint8_t *qs,
                    const uint8_t *kc, const uint8_t *ks, const int64_t *pos, int64_t npos,
                    float *out)
 {
+    int *tq = (int *)malloc(sizeof(int) * (size_t)H * (size_t)d);
+    if (!tq) return;
+    for (int h = 0; h < H; ++h) decode_twice(d, qc + (int64_t)h * (d / 2), tq + h * d);
 #pragma omp parallel for schedule(static)
-    for (int64_t i = 0; i < npos; ++i)
+    for (int64_t i = 0; i < npos; ++i) {
+        int tk[2048];
+        decode_twice(d, kc + pos[i] * (d / 2), tk);
         for (int h = 0; h < H; ++h)
-            out[i * H + h] = exact_dot_f32(d, qc + (int64_t)h * (d / 2), qs + (int64_t)h * (d / 32),
-                                           kc + pos[i] * (d / 2), ks + pos[i] * (d / 32));
+            out[i * H + h] = exact_dot_f32(d, tq + h * d, qs + (int64_t)h * (d / 32), tk, ks + pos[i] * (d / 32));
+    }
+    free(tq);
 }
 
 /* Indexer score of one query against listed key rows:
@@ -369,17 +385,22 @@ void orc_index_scores(int H, int d, const uint8_t *qc, const uint8_t *qs, const 
                       const uint8_t *kc, const uint8_t *ks, const int64_t *pos, int64_t npos,
                       float *out)
 {
+    int *tq = (int *)malloc(sizeof(int) * (size_t)H * (size_t)d);
+    if (!tq) return;
+    for (int h = 0; h < H; ++h) decode_twice(d, qc + (int64_t)h * (d / 2), tq + h * d);
 #pragma omp parallel for schedule(static)
     for (int64_t i = 0; i < npos; ++i) {
+        int tk[2048];
+        decode_twice(d, kc + pos[i] * (d / 2), tk);
         float s = 0.0f;
         for (int h = 0; h < H; ++h) {
-            float D = exact_dot_f32(d, qc + (int64_t)h * (d / 2), qs + (int64_t)h * (d / 32),
-                                    kc + pos[i] * (d / 2), ks + pos[i] * (d / 32));
+            float D = exact_dot_f32(d, tq + h * d, qs + (int64_t)h * (d / 32), tk, ks + pos[i] * (d / 32));
             float R = D > 0.0f ? D : 0.0f;
             s = fmaf(w[h], R, s);
         }
         out[i] = s;
     }
+    free(tq);
 }
 
 /* ------------------------------------------------------------------------- */
@@ -451,29 +472,23 @@ void orc_index_scores_exact(int H, int d, const uint8_t *qc, const uint8_t *qs, 
                             uint32_t *out)
 {
     int nb = d / 32;
+    int *tq = (int *)malloc(sizeof(int) * (size_t)H * (size_t)d);
+    if (!tq) return;
+    for (int h = 0; h < H; ++h) decode_twice(d, qc + (int64_t)h * (d / 2), tq + h * d);
 #pragma omp parallel for schedule(static)
     for (int64_t i = 0; i < npos; ++i) {
         uint32_t *S = out + i * EXACT_LIMBS;
         memset(S, 0, EXACT_LIMBS * sizeof(uint32_t));
-        const uint8_t *kr = kc + pos[i] * (d / 2), *kx = ks + pos[i] * (d / 32);
+        int tk[2048];
+        decode_twice(d, kc + pos[i] * (d / 2), tk);
+        const uint8_t *kx = ks + pos[i] * (d / 32);
         for (int h = 0; h < H; ++h) {
-            const uint8_t *qr = qc + (int64_t)h * (d / 2), *qx = qs + (int64_t)h * (d / 32);
             int64_t I[64];
             int eb[64];
             uint32_t dh[BIG_LIMBS];
             memset(dh, 0, sizeof dh);
-            for (int b = 0; b < nb; ++b) {
-                int64_t acc = 0;
-                for (int t = 0; t < 32; ++t) {
-                    int j = b * 32 + t;
-                    int cq = (j % 2 == 0) ? (qr[j / 2] & 15) : (qr[j / 2] >> 4);
-                    int ck = (j % 2 == 0) ? (kr[j / 2] & 15) : (kr[j / 2] >> 4);
-                    acc += (int64_t)e2m1_twice_signed(cq) * e2m1_twice_signed(ck);
-                }
-                I[b] = acc;
-                eb[b] = ((int)qx[b] - 127) + ((int)kx[b] - 127) - 2;
-                wide_add(dh, BIG_LIMBS, BIG_E0, I[b], eb[b]);
-            }
+            block_dots(d, tq + h * d, qs + (int64_t)h * (d / 32), tk, kx, I, eb);
+            for (int b = 0; b < nb; ++b) wide_add(dh, BIG_LIMBS, BIG_E0, I[b], eb[b]);
             if (wide_sign(dh, BIG_LIMBS) <= 0) continue;            /* ReLU */
             int64_t mw;
             int ew;
@@ -482,6 +497,7 @@ void orc_index_scores_exact(int H, int d, const uint8_t *qc, const uint8_t *qs, 
                 wide_add(S, EXACT_LIMBS, EXACT_E0, mw * I[b], ew + eb[b]);
         }
     }
+    free(tq);
 }
 
 /* ------------------------------------------------------------------------- */

@@ -162,16 +162,35 @@ def test_index_rejects_bad_args(lib):
 
 
 def test_select_and_attn_reject_bad_args(lib):
-    assert lib.csa2_topk(FAKE, -1, 10, None, None, None, 8, 4, FAKE, None, None, 0, None, None) == 1
-    assert lib.csa2_topk(FAKE, 2, 10, None, None, FAKE, 8, 4, FAKE, None, None, 0, None, None) == 1
-    assert lib.csa2_topk(FAKE, 0, 10, None, None, None, 8, 4, FAKE, None, None, 0, None, None) == 0
-    need = lib.csa2_topk_workspace_size(2, 64, 4)
-    assert lib.csa2_topk(FAKE, 2, 64, None, ctypes.c_void_p(258), None, 8, 4, FAKE, None, FAKE,
-                         need, None, None) == 1                                 # misaligned
-    need = lib.csa2_block_candidates_workspace_size(4, 1 << 20, 8, 2048)
+    T, B = lib.csa2_topk, lib.csa2_block_candidates
+    assert T(FAKE, -1, 10, None, None, None, 8, None, 4, FAKE, None, None, 0, None, None) == 1
+    assert T(FAKE, 2, 10, None, None, FAKE, 8, None, 4, FAKE, None, None, 0, None, None) == 1
+    assert T(FAKE, 0, 10, None, None, None, 8, None, 4, FAKE, None, None, 0, None, None) == 0
+    need = lib.csa2_topk_workspace_size(2, 64, 4, None)
+    assert T(FAKE, 2, 64, None, ctypes.c_void_p(258), None, 8, None, 4, FAKE, None, FAKE,
+             need, None, None) == 1                                             # misaligned
+    need = lib.csa2_block_candidates_workspace_size(4, 1 << 20, 8, 2048, None)
     assert need >= 4 * (1 << 17) * 4
-    assert lib.csa2_block_candidates(FAKE, 4, 1 << 20, None, 8, 2048, FAKE, FAKE, need - 1,
-                                     None, None) == 4
+    assert B(FAKE, 4, 1 << 20, None, 8, 2048, None, FAKE, FAKE, need - 1, None, None) == 4
+    # exact order: the context must describe these scores (rows, candidates, pool), and
+    # row_len is required; its band slots make the workspace larger
+    a = csa2.IndexArgs()
+    a.batch, a.n_q, a.n_heads, a.head_dim, a.ratio_m, a.n_keys = 2, 3, 32, 128, 1, 1000
+    a.q = a.w = a.k_codes = a.k_scales = FAKE
+    a.mode, a.block = 0, 8
+    ra = ctypes.byref(a)
+    ne = lib.csa2_topk_workspace_size(6, 1000, 512, ra)
+    assert ne > lib.csa2_topk_workspace_size(6, 1000, 512, None) + 6 * 26 * 2048 * 4 - 1
+    assert T(FAKE, 5, 1000, FAKE, None, None, 8, ra, 512, FAKE, None, FAKE, ne, None, None) == 1   # rows
+    assert T(FAKE, 6, 999, FAKE, None, None, 8, ra, 512, FAKE, None, FAKE, ne, None, None) == 1    # n
+    assert T(FAKE, 6, 1000, None, None, None, 8, ra, 512, FAKE, None, FAKE, ne, None, None) == 1   # row_len
+    assert T(FAKE, 6, 1000, FAKE, None, FAKE, 8, ra, 512, FAKE, None, FAKE, ne, None, None) == 1   # pool in FULL
+    assert T(FAKE, 6, 1000, FAKE, None, None, 8, ra, 512, FAKE, None, FAKE, ne - 1, None, None) == 4
+    a.mode, a.pool_blocks, a.n_pool_blocks = 1, FAKE, 100                           # POOL: 800 candidates
+    other = ctypes.c_void_p(4096)
+    assert T(FAKE, 6, 800, FAKE, None, other, 8, ra, 512, FAKE, None, FAKE, ne, None, None) == 1   # other pool
+    nb_ws = lib.csa2_block_candidates_workspace_size(6, 800, 8, 64, ra)
+    assert B(FAKE, 6, 800, FAKE, 8, 64, ra, FAKE, FAKE, nb_ws, None, None) == 1     # blocks need FULL
     a = csa2.AttnArgs()
     a.batch, a.n_q, a.n_heads, a.d_qk, a.d_v, a.topk, a.window = 1, 1, 64, 576, 600, 512, 128
     a.q = a.idx = a.kv_codes = a.kv_scales = FAKE

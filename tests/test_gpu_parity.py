@@ -1,7 +1,8 @@
 """GPU parity of every step of the CSA2 path against the CPU oracle (needs a GB300).
 
-The bar (workload definition): indices, block ids and FP4 codes bit-exact; indexer
-scores bit-exact too (both sides compute them in the same float32 precision); attention
+The bar (workload definition): indices, block ids and FP4 codes bit-exact, with
+selections ranked by the EXACT indexer score; the float32 scores the indexer writes out
+bit-exact too (both sides compute that approximation in the same float32 precision); attention
 within 1e-2 relative error per (query, head) row:
     max_c |o_gpu - o_ref| / max(max_c |o_ref|, 1e-6) <= 1e-2,
 a row-normwise reading of "max relative error" so that near-zero elements do not blow
@@ -269,12 +270,13 @@ def group_keys(s_valid):
 
 
 def _with_group_max(dw, w, pool=None, st=None):
-    """The indexer again with its group-maximum output, then Top-K fed from it."""
+    """The indexer again with its group-maximum output, then Top-K (exact order) fed from it."""
     n_cand = w.n_keys if pool is None else pool.shape[-1] * w.block
     gm = torch.full((w.batch, w.n_q, (n_cand + 31) // 32), -1, dtype=torch.int32, device=DEV)
-    scores, row_len = csa2.index_score(dw["q_idx"], dw["w_idx"], dw["k_codes"], dw["k_scales"],
-                                       dw["q_pos"], w.ratio_m, pool, w.block, st, group_max=gm)
-    idx = csa2.topk(scores, w.topk, row_len, pool, w.block, d_status=st, group_max=gm)
+    scores, row_len, args = csa2.index_score(dw["q_idx"], dw["w_idx"], dw["k_codes"], dw["k_scales"],
+                                             dw["q_pos"], w.ratio_m, pool, w.block, st, group_max=gm,
+                                             want_args=True)
+    idx = csa2.topk(scores, w.topk, row_len, pool, w.block, d_status=st, group_max=gm, exact=args)
     return scores, gm, idx
 
 
@@ -283,16 +285,23 @@ def _oracle_row_scores(w, b, t, qi, ww, kc, ks, pos):
     return oracle.index_scores(qc, qs, ww[t], kc, ks, pos)
 
 
+def _oracle_row_exact(w, b, t, qi, ww, kc, ks, pos):
+    qc, qs = oracle.quant_mxfp4(f32(qi[t]))
+    return oracle.index_scores_exact(qc, qs, ww[t], kc, ks, pos)
+
+
 @pytest.mark.parametrize("name", list(SCORE_CASES))
 def test_full_scores_topk_blocks(name):
     w = SCORE_CASES[name]
     st = status()
     dw = workload.build(w, kv=False, device=DEV, d_status=st)
-    scores, row_len = csa2.index_score(dw["q_idx"], dw["w_idx"], dw["k_codes"], dw["k_scales"],
-                                       dw["q_pos"], w.ratio_m, None, w.block, st)
-    idx = csa2.topk(scores, w.topk, row_len, d_status=st)
+    scores, row_len, args = csa2.index_score(dw["q_idx"], dw["w_idx"], dw["k_codes"], dw["k_scales"],
+                                             dw["q_pos"], w.ratio_m, None, w.block, st, want_args=True)
+    idx = csa2.topk(scores, w.topk, row_len, d_status=st, exact=args)
+    idx_f = csa2.topk(scores, w.topk, row_len, d_status=st)          # float order of the scores
     nb = min(w.n_blocks, 300)
-    blocks = csa2.block_candidates(scores, nb, row_len, w.block, st)
+    blocks = csa2.block_candidates(scores, nb, row_len, w.block, st, exact=args)
+    blocks_f = csa2.block_candidates(scores, nb, row_len, w.block, st)
     scores_g, gm, idx_g = _with_group_max(dw, w, None, st)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
@@ -306,10 +315,14 @@ def test_full_scores_topk_blocks(name):
             assert int(row_len[b, t]) == nvis
             pos = np.arange(nvis)
             s_ref = _oracle_row_scores(w, b, t, qi_all[b], ww_all[b], kc, ks, pos)
+            ex_ref = _oracle_row_exact(w, b, t, qi_all[b], ww_all[b], kc, ks, pos)
             s_gpu = scores[b, t, :nvis].cpu().numpy()
             assert same_f32(s_gpu, s_ref), f"{name} b={b} t={t}"
-            assert np.array_equal(idx[b, t].cpu().numpy(), oracle.topk(s_ref, pos, w.topk))
+            assert np.array_equal(idx[b, t].cpu().numpy(), oracle.topk_exact(ex_ref, pos, w.topk))
             assert np.array_equal(blocks[b, t].cpu().numpy(),
+                                  oracle.block_candidates_exact(ex_ref, nvis, w.block, nb))
+            assert np.array_equal(idx_f[b, t].cpu().numpy(), oracle.topk(s_ref, pos, w.topk))
+            assert np.array_equal(blocks_f[b, t].cpu().numpy(),
                                   oracle.block_candidates(s_ref, nvis, w.block, nb))
             # group-maximum output and Top-K fed from it
             assert same_f32(scores_g[b, t, :nvis].cpu().numpy(), s_ref)
@@ -358,9 +371,10 @@ def test_pool_scores_and_topk():
     dw = workload.build(w, kv=False, device=DEV, d_status=st)
     pool = dw["pool"].clone()
     pool[1, 0, 650:] = -1                              # -1 padding
-    scores, row_len = csa2.index_score(dw["q_idx"], dw["w_idx"], dw["k_codes"], dw["k_scales"],
-                                       dw["q_pos"], 1, pool, w.block, st)
-    idx = csa2.topk(scores, w.topk, row_len, pool, w.block, d_status=st)
+    scores, row_len, args = csa2.index_score(dw["q_idx"], dw["w_idx"], dw["k_codes"], dw["k_scales"],
+                                             dw["q_pos"], 1, pool, w.block, st, want_args=True)
+    idx = csa2.topk(scores, w.topk, row_len, pool, w.block, d_status=st, exact=args)
+    idx_f = csa2.topk(scores, w.topk, row_len, pool, w.block, d_status=st)
     _, gm, idx_g = _with_group_max(dw, w, pool, st)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
@@ -379,8 +393,84 @@ def test_pool_scores_and_topk():
             assert np.array_equal(gm[b, t, :ng].cpu().numpy().view(np.uint32), group_keys(s_ref))
             assert np.array_equal(idx_g[b, t].cpu().numpy(), idx[b, t].cpu().numpy())
             idx_ref, _, _ = oracle.reindex_indexer(f32(qi_all[b, t]), ww_all[b, t], kc, ks,
-                                                   int(qpos[b, t]), 1, pool_np[b, t], w.topk, w.block)
+                                                   int(qpos[b, t]), 1, pool_np[b, t], w.topk, w.block,
+                                                   want_f32=False)
             assert np.array_equal(idx[b, t].cpu().numpy(), idx_ref)
+            assert np.array_equal(idx_f[b, t].cpu().numpy(), oracle.topk(s_ref, pos, w.topk))
+
+
+def _near_tie_case(N, seed, neg=False):
+    """Keys whose float32 scores tie while their exact scores differ: two heads with
+    w = (1, 2^-30) (negative: (1, -2^-30)).  Every key has the same block-0 dot with head 0;
+    head 1 reads a block whose dot is a different small integer per key.  The float32
+    chain rounds 2^-30 * d_1 away, so the float order is the position order; the exact
+    order follows d_1."""
+    rng = np.random.default_rng(seed)
+    d = 128
+    q = np.zeros((1, 1, 2, d), np.float32)
+    q[0, 0, 0, :32] = 1.0                              # head 0: block 0
+    q[0, 0, 1, 32:64] = 1.0                            # head 1: block 1
+    k = np.zeros((1, N, d), np.float32)
+    k[0, :, :32] = 0.5                                 # d_0 = 16 for every key
+    k[0, :, 32:64] = rng.integers(0, 7, size=(N, 32)) * 0.5 * (rng.random((N, 32)) < 0.3)
+    k[0, :, 36] = 3.0                                  # block amax 3: scale 2^-1, values exact
+    wv = np.array([[[1.0, (-1.0 if neg else 1.0) * 2.0 ** -30]]], np.float32)
+    return q, k, wv
+
+
+@pytest.mark.parametrize("N,neg", [(1500, False), (2000, True), (700, False)])
+def test_exact_order_resolves_float32_ties(N, neg):
+    # the whole row is one float32 tie group within the error bound: the band holds every
+    # position (<= 2,048) and the exact pass orders them by their low-order limbs
+    q, k, wv = _near_tie_case(N, N + neg, neg)
+    qb, kb = synth.f32_to_bf16_bits(q), synth.f32_to_bf16_bits(k)
+    assert np.array_equal(f32(qb), q) and np.array_equal(f32(kb), k)
+    st = status()
+    kt = workload.bf16_tensor(kb, DEV)
+    kc, ks = csa2.quant_fp4(kt, st)
+    wt = torch.from_numpy(wv).to(DEV)
+    scores, row_len, args = csa2.index_score(workload.bf16_tensor(qb, DEV), wt, kc, ks, d_status=st,
+                                             want_args=True)
+    K = 512
+    idx = csa2.topk(scores, K, row_len, d_status=st, exact=args)
+    blocks = csa2.block_candidates(scores, 40, row_len, 8, st, exact=args)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    kc_o, ks_o = oracle.quant_mxfp4(k[0])
+    qc_o, qs_o = oracle.quant_mxfp4(q[0, 0])
+    pos = np.arange(N)
+    s_ref = oracle.index_scores(qc_o, qs_o, wv[0, 0], kc_o, ks_o, pos)
+    ex = oracle.index_scores_exact(qc_o, qs_o, wv[0, 0], kc_o, ks_o, pos)
+    assert np.all(s_ref == s_ref[0])                     # one float32 value for the whole row
+    ref = oracle.topk_exact(ex, pos, K)
+    assert not np.array_equal(ref, oracle.topk(s_ref, pos, K))
+    assert np.array_equal(idx[0, 0].cpu().numpy(), ref)
+    assert np.array_equal(blocks[0, 0].cpu().numpy(), oracle.block_candidates_exact(ex, N, 8, 40))
+
+
+def test_exact_order_negative_weights():
+    # realistic scales with head weights of both signs: the row bound comes from the key
+    # scale maxima; the selections equal the exact ones
+    w = W["full_decode_64k"].scaled(batch=2, n_q=3, n_keys=9000, q_pos0=8999, plant_frac=0.0, seed=23)
+    st = status()
+    dw = workload.build(w, kv=False, device=DEV, d_status=st)
+    wn = torch.randn(dw["w_idx"].shape, generator=torch.Generator().manual_seed(5)).to(DEV)
+    scores, row_len, args = csa2.index_score(dw["q_idx"], wn, dw["k_codes"], dw["k_scales"],
+                                             dw["q_pos"], 1, None, w.block, st, want_args=True)
+    idx = csa2.topk(scores, w.topk, row_len, d_status=st, exact=args)
+    blocks = csa2.block_candidates(scores, 300, row_len, w.block, st, exact=args)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    qi_all, ww_all, _ = synth.gen_queries(w)
+    wn_np = wn.cpu().numpy()
+    for b in range(w.batch):
+        kc, ks = oracle.quant_mxfp4(f32(synth.gen_index_keys(w, b, qi_all[b], ww_all[b])))
+        for t in range(w.n_q):
+            pos = np.arange(w.n_keys)
+            ex = _oracle_row_exact(w, b, t, qi_all[b], wn_np[b], kc, ks, pos)
+            assert np.array_equal(idx[b, t].cpu().numpy(), oracle.topk_exact(ex, pos, w.topk))
+            assert np.array_equal(blocks[b, t].cpu().numpy(),
+                                  oracle.block_candidates_exact(ex, w.n_keys, w.block, 300))
 
 
 def test_index_workspace_left_zeroed():

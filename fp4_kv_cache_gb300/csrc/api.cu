@@ -243,7 +243,7 @@ csa2_status csa2_index_score(const csa2_index_args *a, float *scores, int32_t *r
 bool exact_ctx_ok(const csa2_index_args *ex, int64_t rows, int64_t n, const int32_t *pool_blocks,
                   int32_t block, const int32_t *row_len, bool blocks)
 {
-    if (!index_args_ok(ex)) return false;
+    if (!index_args_ok(ex) || !aligned(ex->q, 16)) return false;
     if ((int64_t)ex->batch * ex->n_q != rows || index_candidates(ex) != n || !row_len) return false;
     if (ex->mode == CSA2_INDEX_POOL) {
         if (blocks || pool_blocks != ex->pool_blocks || block != ex->block) return false;

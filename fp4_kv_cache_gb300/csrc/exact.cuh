@@ -37,32 +37,50 @@ struct QuantQuery {
     float w[kMaxH];
 };
 
-// Quantise query row `q` ([H, d] bf16 bits) into Q: one warp per 32-value block, the same
-// block exponent and rounding as csa2_quant_fp4 and the indexer kernels.  All threads of
-// the block call; ends with a barrier.
+// Quantise query row `q` ([H, d] bf16 bits, 16-byte aligned) into Q with the block exponent
+// and rounding of csa2_quant_fp4 and the indexer kernels: thread t loads 8 values (one
+// 16-byte load; H * d / 8 <= blockDim threads), the 4 threads of a 32-value block agree on
+// its exponent by shuffles.  All threads of the block call; ends with a barrier.
 __device__ __forceinline__ void quantise_query(QuantQuery &Q, const uint16_t *q, const float *w, int H, int d)
 {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    const int t = threadIdx.x;
     const int nb = d / 32, nw = d / 4;
-    for (int blk = warp; blk < H * nb; blk += nwarps) {
-        const int h = blk / nb, b = blk % nb;
-        const float v = __uint_as_float((uint32_t)q[(int64_t)h * d + b * 32 + lane] << 16);
-        const uint32_t amax_bits = __reduce_max_sync(0xffffffffu, __float_as_uint(v) & 0x7fffffffu);
-        const int X = mx_block_exponent(__uint_as_float(amax_bits >= 0x7f800000u ? 0u : amax_bits));
-        const int t = e2m1_twice(e2m1_encode(v, pow2_neg(X)));
-        const uint32_t tb = (uint32_t)t & 0xffu;
-        uint32_t word = tb;
-        word |= __shfl_down_sync(0xffffffffu, tb, 1) << 8;
-        word |= __shfl_down_sync(0xffffffffu, tb, 2) << 16;
-        word |= __shfl_down_sync(0xffffffffu, tb, 3) << 24;
-        const int q1 = __reduce_add_sync(0xffffffffu, t < 0 ? -t : t);
-        if ((lane & 3) == 0) Q.qw[h * nw + b * 8 + (lane >> 2)] = (int32_t)word;
-        if (lane == 0) {
+    const int nchunks = H * d / 8;
+    uint4 raw = make_uint4(0, 0, 0, 0);
+    if (t < nchunks) raw = reinterpret_cast<const uint4 *>(q)[t];
+    const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+    float v[8];
+    uint32_t amax = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        v[2 * k] = __uint_as_float(w4[k] << 16);
+        v[2 * k + 1] = __uint_as_float(w4[k] & 0xffff0000u);
+        amax = max(amax, max(__float_as_uint(v[2 * k]) & 0x7fffffffu, __float_as_uint(v[2 * k + 1]) & 0x7fffffffu));
+    }
+    amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    const int X = mx_block_exponent(__uint_as_float(amax >= 0x7f800000u ? 0u : amax));
+    const float inv = pow2_neg(X);
+    uint32_t word[2] = {0u, 0u};
+    int q1 = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        const int tw = e2m1_twice(e2m1_encode(v[e], inv));
+        word[e >> 2] |= ((uint32_t)tw & 0xffu) << (8 * (e & 3));
+        q1 += tw < 0 ? -tw : tw;
+    }
+    q1 += __shfl_xor_sync(0xffffffffu, q1, 1);
+    q1 += __shfl_xor_sync(0xffffffffu, q1, 2);
+    if (t < nchunks) {
+        const int h = t / (nb * 4), b = (t / 4) % nb, part = t & 3;
+        Q.qw[h * nw + b * 8 + part * 2] = (int32_t)word[0];
+        Q.qw[h * nw + b * 8 + part * 2 + 1] = (int32_t)word[1];
+        if (part == 0) {
             Q.qx[h * 4 + b] = X;
             Q.q1[h * 4 + b] = q1;
         }
     }
-    for (int h = threadIdx.x; h < H; h += blockDim.x) {
+    for (int h = t; h < H; h += blockDim.x) {
         const float x = w[h];
         const uint32_t u = __float_as_uint(x);
         const int ef = (int)((u >> 23) & 0xffu);
@@ -185,6 +203,103 @@ __device__ __noinline__ uint32_t score_key_limb(const QuantQuery &Q, int H, cons
     }
     if (lane == kLimbs - 1) limb ^= 0x80000000u;
     return lane < kLimbs ? limb : 0u;
+}
+
+// Fixed-point form of the exact score for the common case: S = V * 2^E with V a signed
+// 128-bit integer and E the smallest exponent among the score's terms.  Each term is
+// m * 2^e with |m| < 2^37; a lane's terms (at most 8) are shifted to E by at most 80 bits,
+// so a lane's sum stays below 2^120 and the warp's below 2^125.  Returns false (nothing
+// decided) when a term lies more than 80 bits above E; the caller then takes the wide
+// path.  A score with no terms is V = 0 (E = kNoTerms).  Warp-collective; every lane gets
+// the result.
+constexpr int kNoTerms = 1 << 30;
+
+__device__ __forceinline__ __int128 shfl_xor_i128(__int128 v, int o)
+{
+    const unsigned long long lo = (unsigned long long)v, hi = (unsigned long long)(v >> 64);
+    const unsigned long long lo2 = __shfl_xor_sync(0xffffffffu, lo, o), hi2 = __shfl_xor_sync(0xffffffffu, hi, o);
+    return (__int128)(((unsigned __int128)hi2 << 64) | lo2);
+}
+
+// Significant bits of |v| (0 for v = 0).
+__device__ __forceinline__ int bits_i128(__int128 v)
+{
+    const unsigned __int128 a = v < 0 ? (unsigned __int128)(-v) : (unsigned __int128)v;
+    const unsigned long long hi = (unsigned long long)(a >> 64), lo = (unsigned long long)a;
+    return hi ? 128 - __clzll((long long)hi) : (lo ? 64 - __clzll((long long)lo) : 0);
+}
+
+template <int D>
+__device__ __noinline__ bool score_fixed(const QuantQuery &Q, int H, const uint8_t *kc, const uint8_t *ks,
+                                         __int128 &V, int &E)
+{
+    constexpr int NB = D / 32, NW = D / 4;
+    const int lane = threadIdx.x & 31;
+    const int32_t kw = lane < NW ? twice_codes4(*reinterpret_cast<const uint16_t *>(kc + 2 * lane)) : 0;
+    int E_k[NB];
+#pragma unroll
+    for (int b = 0; b < NB; ++b) E_k[b] = (int)ks[b] - 127;
+    long long tm[2][NB];
+    int te[2][NB];
+    int emin = kNoTerms;
+#pragma unroll
+    for (int slot = 0; slot < 2; ++slot) {
+        const int h = lane + 32 * slot;
+        const bool live = h < H;
+        const int hq = live ? h : 0;
+        int I[NB], Ex[NB];
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            int a = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) a = __dp4a(Q.qw[hq * NW + b * 8 + j], __shfl_sync(0xffffffffu, kw, b * 8 + j), a);
+            I[b] = a;
+            Ex[b] = Q.qx[hq * 4 + b] + E_k[b] - 2;
+        }
+        const bool pos = live && Q.m_w[hq] != 0 && dyadic_sign<NB>(I, Ex) > 0;
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            const bool has = pos && I[b] != 0;
+            tm[slot][b] = has ? (long long)Q.m_w[hq] * I[b] : 0;
+            te[slot][b] = Q.e_w[hq] + Ex[b];
+            if (has) emin = min(emin, te[slot][b]);
+        }
+        if (H <= 32) {
+#pragma unroll
+            for (int b = 0; b < NB; ++b) tm[1][b] = 0;
+            break;
+        }
+    }
+    E = __reduce_min_sync(0xffffffffu, emin);
+    V = 0;
+    if (E == kNoTerms) return true;
+    bool ok = true;
+    __int128 c = 0;
+#pragma unroll
+    for (int slot = 0; slot < 2; ++slot)
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            if (tm[slot][b] == 0) continue;
+            const int sh = te[slot][b] - E;
+            if (sh > 80) ok = false;
+            else c += (__int128)tm[slot][b] << sh;
+        }
+    if (!__all_sync(0xffffffffu, ok)) return false;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) c += shfl_xor_i128(c, o);
+    V = c;
+    return true;
+}
+
+// Brings (V, E) to exponent E_to <= E: V << (E - E_to); false when that would leave more
+// than 126 significant bits.
+__device__ __forceinline__ bool align_fixed(__int128 &V, int E, int E_to)
+{
+    if (V == 0) return true;
+    const int sh = E - E_to;
+    if (sh < 0 || bits_i128(V) + sh > 126) return false;
+    V = V << sh;
+    return true;
 }
 
 // Compares two keys held one limb per lane (as returned by score_key_limb): > 0 when a is

@@ -190,7 +190,8 @@ topk_radix_kernel(const float *__restrict__ scores, int64_t n, const int32_t *__
 // desc, position asc) gives the top-k, emitted in order.
 constexpr int kGThreads = 1024;
 constexpr int kGBins = 2048;
-constexpr int kGroupCap = 8192;         // group keys per row kept on chip (longer rows: wider groups)
+constexpr int kListCap = 8192;          // candidate groups per row listed on chip
+constexpr int kMaxGroups = 32768;       // group keys per row (on chip; longer rows: wider groups)
 constexpr int kCandCap = 16384;         // candidates per row kept on chip (a whole
                                         // 2,048-block pool of 8 positions fits)
 
@@ -307,20 +308,21 @@ __device__ __forceinline__ uint32_t g_threshold(const uint32_t *keys, int n, uin
 
 // ------------------------------------------------------------------ exact order (csa2_topk and
 // csa2_block_candidates with an exact context)
-// The float32 scores s~ the indexer writes are within eps of the exact scores s (see
-// csa2_index_score: (H + 2) 2^-24 A + 2^-149 (sum|w| + H), A = sum_h |w_h| ReLU(d_h)).  With
-// tau~ the k-th largest s~ and a row-wide eps >= that bound:
-//   s~ < tau~ - 2 eps: at least k candidates (those with s~ >= tau~) have s >= tau~ - eps > s,
-//     so the candidate is out;
-//   s~ > tau~ + 2 eps: any candidate with s >= this one's s has s~ > tau~, and fewer than k
-//     do, so it is in;
+// The float32 scores s~ the indexer writes are within (H + 2) 2^-24 A + 2^-149 (sum|w| + H)
+// of the exact scores s, A = sum_h |w_h| ReLU(d_h) (see csa2_index_score).  The kernel uses
+// a bound e(x) >= that error for a candidate whose s~ is x, non-decreasing in x and with
+// x - e(x) rising.  With tau~ the k-th largest s~:
+//   s~ < lo = tau~ - 2 e(tau~): at least k candidates (those with s~ >= tau~) have
+//     s >= tau~ - e(tau~) > s, so the candidate is out;
+//   s~ > hi = tau~ + e(tau~) + e(tau~ + 3 e(tau~)): such an s~ has s~ - e(s~) > tau~ + e(tau~);
+//     any candidate with s >= this one's s then has s~ > tau~, and fewer than k do, so it
+//     is in;
 //   the rest (the band) are re-scored exactly and the k - (#in) best of them taken by
 //   (exact score desc, candidate asc).
-// eps: for rows with every w_h >= 0, A = s <= (max s~ + eta) / (1 - c); otherwise A is
-// bounded through |d_h| <= sum_b 12 sum_i |2 q_i| 2^(Xq_b + Xk_b - 2) with Xk_b the largest
-// key scale exponent of block b in the sequence (one pass over its scale bytes).  The
-// constants are rounded up by one more 2^-24 A and a factor 2 on eta, which covers the
-// float64 rounding of this arithmetic.
+// e: for rows with every w_h >= 0, A_t = s_t <= (s~_t + eta) / (1 - c), so
+// e(x) = c (x + eta) / (1 - c) + eta; otherwise one row-wide A through |d_h| <= sum_b 12
+// sum_i |2 q_i| 2^(Xq_b + Xk_b - 2), Xk_b the largest key scale exponent of block b in the
+// sequence (one pass over its scale bytes).
 struct ExactArgs {
     int H, d;                      // indexer heads, head dim (32, 64 or 128)
     int32_t n_q;                   // queries per sequence (row r belongs to sequence r / n_q)
@@ -384,37 +386,57 @@ __device__ __noinline__ uint32_t key_scale_max(const uint8_t *ks, int64_t n_keys
     return t;
 }
 
-// eps of one row (see above); returns a negative value when the row's scores are not all
-// finite (then no exact pass is made: the indexer has flagged CSA2_DEV_SCORE_RANGE).
-__device__ __noinline__ double row_eps(const exact::QuantQuery &Q, const ExactArgs &X, int64_t seq, uint32_t max_key,
-                                       uint32_t *s_red)
+// The row's error bound of the float32 scores as an affine function of the score,
+// e(x) = c1 max(x, 0) + c0 (see above); it holds for finite scores (a row with another
+// score gets no exact pass: the indexer has flagged CSA2_DEV_SCORE_RANGE).
+//   every w_h >= 0: A_t = s_t <= (s~_t + eta) / (1 - c), so e(x) = c (x + eta) / (1 - c) + eta;
+//   otherwise: one row-wide A from the key scale maxima, e = c A + eta.
+// Evaluated in float32 with every operation rounded outward (a float64 unit this slow has
+// no place in a per-row prologue); c1 = (H + 4) 2^-24 covers c / (1 - c) and that rounding,
+// c0 >= eta = 2^-140 (sum|w| + H) covers the subnormal terms.
+struct RowBound {
+    float c1, c0;
+    __device__ float e(float x) const { return __fmaf_ru(c1, x > 0.0f ? x : 0.0f, c0); }
+    // below lo(tau): out; above hi(tau): in (x - e(x) and x + e(x) both rise with x)
+    __device__ float lo(float x) const { return __fsub_rd(x, __fmul_ru(2.0f, e(x))); }
+    __device__ float hi(float x) const
+    {
+        const float ex = e(x);
+        return __fadd_ru(__fadd_ru(x, ex), e(__fmaf_ru(3.0f, ex, x)));
+    }
+};
+
+__device__ __noinline__ RowBound row_bound(const exact::QuantQuery &Q, const ExactArgs &X, int64_t seq,
+                                           uint32_t *s_red)
 {
-    const float mval = key_value(max_key);
-    if (max_key == 0u || !(fabsf(mval) <= 3.4028234663852886e38f)) return -1.0;
-    double sumw = 0.0;
+    RowBound rb{0.0f, -1.0f};
+    float sumw = 0.0f;
     bool neg = false;
     for (int h = 0; h < X.H; ++h) {
-        sumw += fabs((double)Q.w[h]);
+        sumw = __fadd_ru(sumw, fabsf(Q.w[h]));
         neg |= Q.w[h] < 0.0f;
     }
-    const double c = (double)(X.H + 3) * 0x1p-24;
-    const double eta = 0x1p-148 * (sumw + X.H);
-    double A;
+    const float c = (float)(X.H + 4) * 0x1p-24f;
+    const float eta = __fmul_ru(__fadd_ru(sumw, (float)X.H), 0x1p-140f);
     if (!neg) {
-        A = ((double)fmaxf(mval, 0.0f) + eta) / (1.0 - c);
-    } else {
-        const int nb = X.d / 32;
-        const uint32_t km = key_scale_max(X.ks + seq * X.n_keys * nb, X.n_keys, nb, s_red);
-        A = 0.0;
-        for (int h = 0; h < X.H; ++h) {
-            double ah = 0.0;
-            for (int b = 0; b < nb; ++b)
-                ah += 12.0 * (double)Q.q1[h * 4 + b] *
-                      ldexp(1.0, Q.qx[h * 4 + b] + (int)((km >> (8 * b)) & 255u) - 127 - 2);
-            A += fabs((double)Q.w[h]) * ah;
-        }
+        rb.c1 = c;
+        rb.c0 = eta;
+        return rb;
     }
-    return (c * A + eta) * (1.0 + 0x1p-40);
+    const int nb = X.d / 32;
+    const uint32_t km = key_scale_max(X.ks + seq * X.n_keys * nb, X.n_keys, nb, s_red);
+    float A = 0.0f;
+    for (int h = 0; h < X.H; ++h) {
+        float ah = 0.0f;
+        for (int b = 0; b < nb; ++b) {
+            const int ex = Q.qx[h * 4 + b] + (int)((km >> (8 * b)) & 255u) - 127 - 2;
+            const float p2 = ex < -149 ? 0x1p-149f : ldexpf(1.0f, ex);      // rounded up
+            ah = __fmaf_ru(12.0f * (float)Q.q1[h * 4 + b], p2, ah);
+        }
+        A = __fmaf_ru(fabsf(Q.w[h]), ah, A);
+    }
+    rb.c0 = __fmaf_ru(c, A, eta);                     // an overflow to +inf puts every candidate in the band
+    return rb;
 }
 
 // Exact key (limb `lane`) of band candidate i of a row: a position (through the pool), or
@@ -447,11 +469,50 @@ __device__ __noinline__ uint32_t unit_key(const exact::QuantQuery &Q, const Exac
     return best;
 }
 
-// Among n_band band units whose exact keys are in bk (limb-major, stride kBandCap), sets
+// Fixed-point exact score (V, E) of band candidate i (see exact::score_fixed); for a block,
+// the largest over its positions that could be its maximum.  false: the 128-bit form does
+// not hold it (the caller takes the wide path).
+template <int D>
+__device__ __noinline__ bool unit_fixed(const exact::QuantQuery &Q, const ExactArgs &X, int64_t row, int64_t seq,
+                                        const int32_t *pool_row, int32_t block, int64_t i, uint32_t unit_lo_key,
+                                        __int128 &V, int &E)
+{
+    const int64_t kbase = seq * X.n_keys;
+    if (X.unit == 1) {
+        int64_t p = cand_pos(pool_row, block, i);
+        p = p < 0 ? 0 : (p >= X.n_keys ? X.n_keys - 1 : p);
+        return exact::score_fixed<D>(Q, X.H, X.kc + (kbase + p) * (D / 2), X.ks + (kbase + p) * (D / 32), V, E);
+    }
+    int64_t len = X.pos_len[row];
+    len = len < 0 ? 0 : (len > X.pos_n ? X.pos_n : len);
+    const float *ps = X.pos_scores + row * X.pos_n;
+    bool have = false;
+    V = 0;
+    E = exact::kNoTerms;
+#pragma unroll 1
+    for (int j = 0; j < X.unit; ++j) {
+        const int64_t p = i * X.unit + j;
+        if (p >= len || p >= X.n_keys) break;
+        if (score_key(ps[p]) < unit_lo_key) continue;          // cannot be the block's maximum
+        __int128 v;
+        int e;
+        if (!exact::score_fixed<D>(Q, X.H, X.kc + (kbase + p) * (D / 2), X.ks + (kbase + p) * (D / 32), v, e))
+            return false;
+        if (!have) { V = v; E = e; have = true; continue; }
+        const int em = min(E, e);
+        if (!exact::align_fixed(V, E, em) || !exact::align_fixed(v, e, em)) return false;
+        E = em;
+        if (v > V) V = v;
+    }
+    return true;
+}
+
+// Among n_band band units whose exact keys are in bk (nwords words each, most significant
+// last, word-major with stride kBandCap, compared as unsigned), sets
 // state[u] = 1 for the `take` best by (key desc, unit index asc): limb by limb from the top,
 // the take-th largest limb value among the units still tied splits them into taken, tied
 // and dropped.  Block-wide; act and vals are scratch of n_band entries in shared memory.
-__device__ __noinline__ void select_band(const uint32_t *bk, int n_band, uint32_t take, uint8_t *state,
+__device__ __noinline__ void select_band(const uint32_t *bk, int nwords, int n_band, uint32_t take, uint8_t *state,
                                          uint32_t *act, uint32_t *vals, GSmem &S, uint32_t *s_red)
 {
     const int tid = threadIdx.x;
@@ -460,7 +521,7 @@ __device__ __noinline__ void select_band(const uint32_t *bk, int n_band, uint32_
     int n_act = n_band;
     uint32_t remaining = take;
 #pragma unroll 1
-    for (int j = exact::kLimbs - 1; j >= 0; --j) {
+    for (int j = nwords - 1; j >= 0; --j) {
         if (remaining == 0 || remaining >= (uint32_t)n_act) break;
         uint32_t vmin = 0xffffffffu, vmax = 0u;
         for (int i = tid; i < n_act; i += kGThreads) {
@@ -493,6 +554,176 @@ __device__ __noinline__ void select_band(const uint32_t *bk, int n_band, uint32_
     __syncthreads();
 }
 
+// Block-wide exclusive max-scan of one value per thread in thread order (identity 0; all
+// threads call; ends with a barrier).
+__device__ __forceinline__ uint32_t block_excl_max(uint32_t v, uint32_t *s_warp)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    uint32_t incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl = max(incl, t);
+    }
+    uint32_t excl = __shfl_up_sync(0xffffffffu, incl, 1);
+    if (lane == 0) excl = 0u;
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const uint32_t wv = lane < nw ? s_warp[lane] : 0u;
+        uint32_t wi = wv;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t t = __shfl_up_sync(0xffffffffu, wi, o);
+            if (lane >= o) wi = max(wi, t);
+        }
+        uint32_t we = __shfl_up_sync(0xffffffffu, wi, 1);
+        if (lane == 0) we = 0u;
+        s_warp[lane] = we;
+    }
+    __syncthreads();
+    const uint32_t r = max(s_warp[warp], excl);
+    __syncthreads();
+    return r;
+}
+
+// Key rows p and q of one sequence hold the same bytes (codes and scales).
+template <int D>
+__device__ __forceinline__ bool same_key_row(const ExactArgs &X, int64_t kbase, int64_t p, int64_t q)
+{
+    const uint4 *a = reinterpret_cast<const uint4 *>(X.kc + (kbase + p) * (D / 2));
+    const uint4 *b = reinterpret_cast<const uint4 *>(X.kc + (kbase + q) * (D / 2));
+    bool eq = true;
+#pragma unroll
+    for (int i = 0; i < D / 32; ++i) {
+        const uint4 x = a[i], y = b[i];
+        eq = eq && x.x == y.x && x.y == y.y && x.z == y.z && x.w == y.w;
+    }
+#pragma unroll
+    for (int i = 0; i < D / 32; ++i) eq = eq && X.ks[(kbase + p) * (D / 32) + i] == X.ks[(kbase + q) * (D / 32) + i];
+    return eq;
+}
+
+// Exact pass over a row's band (n_band candidates s_band[u] into the candidate arrays, in
+// position order; take = how many of them are selected): sets s_state[u].  Runs of band
+// candidates with equal float keys and byte-identical key rows have equal exact scores, so
+// only the first of each run is scored.  Scores go first to 128-bit fixed point at one row
+// exponent (4-word keys); where that form does not hold them, every candidate is scored as
+// 26 limbs.  Either way the keys are selected word by word (select_band).  Block-wide.
+template <int D>
+__device__ __noinline__ void band_exact(const exact::QuantQuery &Q, const ExactArgs &X, const RowBound &rb,
+                                        int64_t row, int64_t seq, const int32_t *pool_row, int32_t block,
+                                        const uint32_t *s_band, const uint32_t *s_ck, const int32_t *s_cp,
+                                        uint32_t n_band, uint32_t take, uint8_t *s_state, uint32_t *s_act,
+                                        uint32_t *s_val, GSmem &S, uint32_t *s_red)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    uint32_t *bk = X.band + (size_t)blockIdx.x * exact::kLimbs * kBandCap;   // [word][kBandCap]
+    uint32_t *g_head = bk + 4 * kBandCap, *g_v = bk + 5 * kBandCap;          // rows 4 and 5..9
+    const int64_t kbase = seq * X.n_keys;
+    int32_t *s_pos = reinterpret_cast<int32_t *>(s_val);   // free until select_band
+    // the single position that can hold each candidate's score (-1: several)
+    for (uint32_t u = tid; u < n_band; u += kGThreads) {
+        const uint32_t i = s_band[u];
+        int64_t p = -1;
+        if (X.unit == 1) {
+            p = cand_pos(pool_row, block, s_cp[i]);
+            p = p < 0 ? 0 : (p >= X.n_keys ? X.n_keys - 1 : p);
+        } else {
+            int64_t len = X.pos_len[row];
+            len = len < 0 ? 0 : (len > X.pos_n ? X.pos_n : len);
+            const float *ps = X.pos_scores + row * X.pos_n;
+            const uint32_t ulo = score_key(rb.lo(key_value(s_ck[i])));
+            int cnt = 0;
+            for (int j = 0; j < X.unit; ++j) {
+                const int64_t q = (int64_t)s_cp[i] * X.unit + j;
+                if (q >= len || q >= X.n_keys) break;
+                if (score_key(ps[q]) >= ulo) { p = q; ++cnt; }
+            }
+            if (cnt != 1) p = -1;
+        }
+        s_pos[u] = (int32_t)p;
+    }
+    __syncthreads();
+    // run heads: thread t takes candidates 2t and 2t + 1
+    uint32_t a[2] = {0u, 0u};
+    for (int k = 0; k < 2; ++k) {
+        const uint32_t u = 2 * tid + k;
+        if (u >= n_band) continue;
+        bool same = false;
+        if (u > 0 && s_pos[u] >= 0 && s_pos[u - 1] >= 0 && s_ck[s_band[u]] == s_ck[s_band[u - 1]])
+            same = same_key_row<D>(X, kbase, s_pos[u], s_pos[u - 1]);
+        a[k] = same ? 0u : u;
+    }
+    const uint32_t pre = block_excl_max(max(a[0], a[1]), S.warp);
+    const uint32_t h0 = max(pre, a[0]), h1 = max(h0, a[1]);
+    uint32_t n_heads;
+    const int nh = (2 * tid < n_band && h0 == 2 * tid) + (2 * tid + 1 < n_band && h1 == 2 * tid + 1);
+    const uint32_t at = block_excl_count_sum((uint32_t)nh, S.warp, n_heads);
+    {
+        uint32_t o = at;
+        if (2 * tid < n_band) {
+            g_head[2 * tid] = h0;
+            if (h0 == 2 * tid) s_act[o++] = 2 * tid;
+        }
+        if (2 * tid + 1 < n_band) {
+            g_head[2 * tid + 1] = h1;
+            if (h1 == 2 * tid + 1) s_act[o++] = 2 * tid + 1;
+        }
+    }
+    __syncthreads();
+    // fixed point for the run heads
+    bool ok = true;
+#pragma unroll 1
+    for (uint32_t hi_ = warp; hi_ < n_heads; hi_ += kGThreads / 32) {
+        const uint32_t u = s_act[hi_], i = s_band[u];
+        const uint32_t ulo = X.unit > 1 ? score_key(rb.lo(key_value(s_ck[i]))) : 0u;
+        __int128 V;
+        int E;
+        ok = unit_fixed<D>(Q, X, row, seq, pool_row, block, s_cp[i], ulo, V, E) && ok;
+        if (lane < 4) g_v[(size_t)lane * kBandCap + u] = (uint32_t)(V >> (32 * lane));
+        if (lane == 4) g_v[(size_t)4 * kBandCap + u] = (uint32_t)E;
+    }
+    ok = __syncthreads_and(ok) != 0;
+    if (ok) {
+        int e_row = exact::kNoTerms;
+        for (uint32_t k = tid; k < n_heads; k += kGThreads) e_row = min(e_row, (int)g_v[(size_t)4 * kBandCap + s_act[k]]);
+        e_row = __reduce_min_sync(0xffffffffu, e_row);
+        if (lane == 0) s_red[warp] = (uint32_t)e_row;
+        __syncthreads();
+        e_row = exact::kNoTerms;
+        for (int k = 0; k < kGThreads / 32; ++k) e_row = min(e_row, (int)s_red[k]);
+        __syncthreads();
+        for (uint32_t u = tid; u < n_band; u += kGThreads) {
+            const uint32_t h = g_head[u];
+            unsigned __int128 w = 0;
+            for (int k = 3; k >= 0; --k) w = (w << 32) | g_v[(size_t)k * kBandCap + h];
+            __int128 V = (__int128)w;
+            ok = exact::align_fixed(V, (int)g_v[(size_t)4 * kBandCap + h], e_row) && ok;
+            for (int k = 0; k < 4; ++k) {
+                uint32_t word = (uint32_t)((unsigned __int128)V >> (32 * k));
+                if (k == 3) word ^= 0x80000000u;
+                bk[(size_t)k * kBandCap + u] = word;
+            }
+        }
+        ok = __syncthreads_and(ok) != 0;
+    }
+    if (ok) {
+        select_band(bk, 4, (int)n_band, take, s_state, s_act, s_val, S, s_red);
+        return;
+    }
+    // wide form: every band candidate as 26 limbs
+#pragma unroll 1
+    for (uint32_t u = warp; u < n_band; u += kGThreads / 32) {
+        const uint32_t i = s_band[u];
+        const uint32_t ulo = X.unit > 1 ? score_key(rb.lo(key_value(s_ck[i]))) : 0u;
+        const uint32_t limb = unit_key<D>(Q, X, row, seq, pool_row, block, s_cp[i], ulo);
+        if (lane < exact::kLimbs) bk[(size_t)lane * kBandCap + u] = limb;
+    }
+    __syncthreads();
+    select_band(bk, exact::kLimbs, (int)n_band, take, s_state, s_act, s_val, S, s_red);
+}
+
 template <bool EXACT, int D>
 __global__ void __launch_bounds__(kGThreads, 1)
 topk_gmax_kernel(const float *__restrict__ scores, int64_t n, int64_t rows, const int32_t *__restrict__ row_len,
@@ -500,14 +731,28 @@ topk_gmax_kernel(const float *__restrict__ scores, int64_t n, int64_t rows, cons
                  float *__restrict__ out_scores, const uint32_t *__restrict__ gkeys, int32_t gs, int64_t G,
                  const ExactArgs X)
 {
+    // shared memory: the candidate-group list (later the exact band), then the group keys,
+    // whose space the candidates' keys and positions take once the list is made
     extern __shared__ uint32_t g_sm[];
-    uint32_t *s_g = g_sm;                                  // group keys, then candidate-group list
-    uint32_t *s_ck = g_sm + kGroupCap;                     // candidate keys
+    uint32_t *s_g = g_sm;                                  // candidate-group list / exact band
+    uint32_t *s_gk = g_sm + kListCap;                      // group keys
+    uint32_t *s_ck = g_sm + kListCap;                      // candidate keys
     int32_t *s_cp = reinterpret_cast<int32_t *>(s_ck + kCandCap);   // candidate positions (index)
+    static_assert(2 * kCandCap >= kMaxGroups, "group keys and candidates share their space");
     __shared__ GSmem S;
     __shared__ uint32_t s_red[64];
     __shared__ exact::QuantQuery QQ;                       // exact order: the row's query
     const int tid = threadIdx.x;
+    // exact order: the first row's query and error bound come from inputs the kernel before
+    // does not write (csa2_topk), so they are prepared before the dependency wait
+    RowBound rb_first{0.0f, -1.0f};
+    if constexpr (EXACT) {
+        if ((int64_t)blockIdx.x < rows) {
+            const int64_t r = blockIdx.x;
+            exact::quantise_query(QQ, X.q + r * (int64_t)X.H * D, X.w + r * (int64_t)X.H, X.H, D);
+            rb_first = row_bound(QQ, X, r / X.n_q, s_red);
+        }
+    }
     pdl_wait();                                            // scores come from the kernel before
     pdl_allow_dependents();
 #pragma unroll 1
@@ -527,45 +772,49 @@ topk_gmax_kernel(const float *__restrict__ scores, int64_t n, int64_t rows, cons
         }
         continue;
     }
-    const int ng = (int)((len + gs - 1) / gs);
-    if (ng > kGroupCap) {                                  // too long for the on-chip path
+    const int ng = (int)((len + gs - 1) / gs);             // <= kMaxGroups
+    const uint32_t *gk = s_gk;
+    bool nonfinite = false;                                 // a group maximum of +-inf
+    for (int g = tid; g < ng; g += kGThreads) {
+        const uint32_t v = gkeys[row * G + g];
+        s_gk[g] = v;
+        nonfinite |= v >= 0xff800000u || v <= 0x007fffffu;
+    }
+    nonfinite = __syncthreads_or(nonfinite) != 0;
+    // exact order: the row's error bound of the float32 scores (c0 < 0: none made)
+    RowBound rb{0.0f, -1.0f};
+    int64_t seq = 0;
+    if constexpr (EXACT) {
+        seq = row / X.n_q;
+        if (row == (int64_t)blockIdx.x) {
+            rb = rb_first;
+        } else {
+            exact::quantise_query(QQ, X.q + row * (int64_t)X.H * D, X.w + row * (int64_t)X.H, X.H, D);
+            rb = row_bound(QQ, X, seq, s_red);
+        }
+        if (nonfinite) rb.c0 = -1.0f;
+    }
+    const bool exact_row = EXACT && rb.c0 >= 0.0f;
+    // a lower bound of the k-th largest group key is enough to keep every top-k element
+    // (the groups above the bound are a superset of those above the exact key); in exact
+    // order the bound is lowered to lo() of it, so the whole band is gathered
+    uint32_t need0;
+    uint32_t tau0 = ng > k ? g_threshold(gk, ng, (uint32_t)k, S, need0, 2) : 0u;
+    if (exact_row && tau0 != 0u) tau0 = score_key(rb.lo(key_value(tau0)));
+
+    // candidate groups (key >= tau0), listed in s_g in ascending order: thread t owns the
+    // run [t*run, (t+1)*run)
+    const int run = (ng + kGThreads - 1) / kGThreads;        // <= 32
+    const int r0 = min(tid * run, ng), r1 = min(r0 + run, ng);
+    uint32_t mine = 0;                                      // bit j: group r0+j is a candidate
+    for (int i = r0; i < r1; ++i) mine |= (gk[i] >= tau0 ? 1u : 0u) << (i - r0);
+    uint32_t n_cg;
+    const uint32_t at = block_excl_count_sum((uint32_t)__popc(mine), S.warp, n_cg);
+    if (n_cg > (uint32_t)kListCap) {                        // too many to list on chip
         radix_select_row(scores, n, row_len, pool, block, k, idx, out_scores, row);
         if (EXACT && tid == 0) dev_flag(X.d_status, CSA2_DEV_BAND_LIMIT);
         continue;
     }
-    uint32_t gmx = 0;
-    for (int g = tid; g < ng; g += kGThreads) {
-        const uint32_t v = gkeys[row * G + g];
-        s_g[g] = v;
-        gmx = max(gmx, v);
-    }
-    __syncthreads();
-    // exact order: the row's error bound of the float32 scores (negative: none made)
-    double eps = -1.0;
-    int64_t seq = 0;
-    if constexpr (EXACT) {
-        seq = row / X.n_q;
-        exact::quantise_query(QQ, X.q + row * (int64_t)X.H * D, X.w + row * (int64_t)X.H, X.H, D);
-        uint32_t mn, mx;
-        block_minmax(0xffffffffu, gmx, s_red, mn, mx);
-        eps = row_eps(QQ, X, seq, mx, s_red);
-    }
-    // a lower bound of the k-th largest group key is enough to keep every top-k element
-    // (the groups above the bound are a superset of those above the exact key); in exact
-    // order the bound is lowered by 2 eps so the whole band is gathered
-    uint32_t need0;
-    uint32_t tau0 = ng > k ? g_threshold(s_g, ng, (uint32_t)k, S, need0, 2) : 0u;
-    if (EXACT && eps >= 0.0 && tau0 != 0u)
-        tau0 = score_key(__double2float_rd((double)key_value(tau0) - 2.0 * eps));
-
-    // candidate groups (key >= tau0), compacted in place in ascending order: thread t owns
-    // the run [t*run, (t+1)*run) and writes only below its own run after everyone has read
-    const int run = (ng + kGThreads - 1) / kGThreads;        // <= 8
-    const int r0 = min(tid * run, ng), r1 = min(r0 + run, ng);
-    uint32_t mine = 0;                                      // bit j: group r0+j is a candidate
-    for (int i = r0; i < r1; ++i) mine |= (s_g[i] >= tau0 ? 1u : 0u) << (i - r0);
-    uint32_t n_cg;
-    const uint32_t at = block_excl_count_sum((uint32_t)__popc(mine), S.warp, n_cg);
     {
         uint32_t o = at;
         for (int i = r0; i < r1; ++i)
@@ -646,11 +895,11 @@ topk_gmax_kernel(const float *__restrict__ scores, int64_t n, int64_t rows, cons
     const int crun = ((int)n_c + kGThreads - 1) / kGThreads;
     const int c0 = min(tid * crun, (int)n_c), c1 = min(c0 + crun, (int)n_c);
     if constexpr (EXACT) {
-        if (eps >= 0.0 && tau != 0u) {
-            // the band [tau~ - 2 eps, tau~ + 2 eps] in key terms; above it: selected
-            const double tv = (double)key_value(tau);
-            const uint32_t lo_key = score_key(__double2float_rd(tv - 2.0 * eps));
-            const uint32_t hi_key = score_key(__double2float_ru(tv + 2.0 * eps));
+        if (exact_row && tau != 0u) {
+            // the band [lo(tau~), hi(tau~)] in key terms; above it: selected
+            const float tv = key_value(tau);
+            const uint32_t lo_key = score_key(rb.lo(tv));
+            const uint32_t hi_key = score_key(rb.hi(tv));
             uint32_t n_hi = 0, n_bd = 0;
             for (int i = c0; i < c1; ++i) {
                 n_hi += s_ck[i] > hi_key;
@@ -676,29 +925,20 @@ topk_gmax_kernel(const float *__restrict__ scores, int64_t n, int64_t rows, cons
                 if (tid == 0) dev_flag(X.d_status, CSA2_DEV_BAND_LIMIT);    // float order stays
             } else {
                 if (n_band > take) {
-                    // exact keys of the band candidates, one warp each, into this CTA's slot
-                    uint32_t *bk = X.band + (size_t)blockIdx.x * exact::kLimbs * kBandCap;
-                    const int lane = tid & 31, warp = tid >> 5;
-#pragma unroll 1
-                    for (uint32_t u = warp; u < n_band; u += kGThreads / 32) {
-                        const uint32_t i = s_band[u];
-                        const uint32_t ulo = X.unit > 1
-                            ? score_key(__double2float_rd((double)key_value(s_ck[i]) - 2.0 * eps)) : 0u;
-                        const uint32_t limb = unit_key<D>(QQ, X, row, seq, pool_row, block, s_cp[i], ulo);
-                        if (lane < exact::kLimbs) bk[(size_t)lane * kBandCap + u] = limb;
-                    }
+                    band_exact<D>(QQ, X, rb, row, seq, pool_row, block, s_band, s_ck, s_cp, n_band, take, s_state,
+                                  s_act, s_val, S, s_red);
+                    // band candidates taken rank above hi, the others below every
+                    // candidate: the float-order emission below then takes exactly these
+                    for (uint32_t u = tid; u < n_band; u += kGThreads)
+                        s_ck[s_band[u]] = s_state[u] ? 0xffffffffu : 0u;
                     __syncthreads();
-                    select_band(bk, (int)n_band, take, s_state, s_act, s_val, S, s_red);
+                    tau = hi_key;
+                    need = 0;
                 } else {
-                    for (uint32_t u = tid; u < n_band; u += kGThreads) s_state[u] = 1;
-                    __syncthreads();
+                    // the whole band is taken: every candidate >= lo is selected
+                    tau = lo_key;
+                    need = 0xffffffffu;
                 }
-                // band candidates taken rank above tau~ + 2 eps, the others below every
-                // candidate: the float-order emission below then takes exactly these
-                for (uint32_t u = tid; u < n_band; u += kGThreads) s_ck[s_band[u]] = s_state[u] ? 0xffffffffu : 0u;
-                __syncthreads();
-                tau = hi_key;
-                need = 0;
             }
         }
     }
@@ -730,7 +970,7 @@ topk_gmax_kernel(const float *__restrict__ scores, int64_t n, int64_t rows, cons
 int32_t group_size_for(int64_t n)
 {
     int32_t gs = 32;
-    while ((n + gs - 1) / gs > kGroupCap && gs < (1 << 20)) gs *= 2;
+    while ((n + gs - 1) / gs > kMaxGroups && gs < (1 << 20)) gs *= 2;
     return gs;
 }
 
@@ -823,7 +1063,7 @@ cudaError_t launch_topk(const float *scores, int64_t rows, int64_t n, const int3
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    const size_t smem = (size_t)(kGroupCap + 2 * kCandCap) * sizeof(uint32_t);
+    const size_t smem = (size_t)(kListCap + 2 * kCandCap) * sizeof(uint32_t);
     ExactArgs X = {};
     if (!ex) return launch_gmax<false, 0>((unsigned)rows, smem, s, scores, n, rows, row_len, pool, block, k, idx,
                                           out_scores, gkeys, gs, G, X);

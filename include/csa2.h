@@ -33,11 +33,13 @@
  *   - Kernels are launched with programmatic dependent launch: a kernel may start its
  *     set-up while the kernel before it on the stream drains, and waits for that kernel
  *     to complete before it reads what that kernel may write.  Every kernel of the
- *     library lets its dependents start only after that wait.  One exception:
+ *     library lets its dependents start only after that wait.  Two exceptions:
  *     csa2_sparse_attn reads q, q_pos, swa_pos0 and swa_start before its wait (only idx
- *     may come from the kernel just before it), so those must not be written by a kernel
- *     that lets its dependents start early (a plain kernel, or any call of this library,
- *     is fine).
+ *     may come from the kernel just before it), and csa2_topk / csa2_block_candidates
+ *     with an exact context read its q, w and k_scales before theirs (only the scores,
+ *     row lengths and group maxima may come from the kernel just before them); those
+ *     inputs must not be written by a kernel that lets its dependents start early (a
+ *     plain kernel, or any call of this library, is fine).
  */
 #ifndef CSA2_H
 #define CSA2_H
@@ -260,8 +262,9 @@ CSA2_API csa2_status csa2_index_score(const csa2_index_args *a, float *scores, i
 /*     The float32 scores decide every candidate farther than their error bound from   */
 /*     the k-th score; the candidates within it are re-scored exactly on the GPU (wide  */
 /*     integers) and ordered by the exact values.  pool_blocks / block must be those of */
-/*     *exact (POOL) or NULL / any (FULL).  A row with more than CSA2_EXACT_BAND_CAP     */
-/*     such candidates sets CSA2_DEV_BAND_LIMIT and follows the float32 order.          */
+/*     *exact (POOL) or NULL / any (FULL); exact->q must be 16-byte aligned.  A row     */
+/*     with more than CSA2_EXACT_BAND_CAP such candidates sets CSA2_DEV_BAND_LIMIT and  */
+/*     follows the float32 order.                                                      */
 /* idx [rows, k] int32: the selected POSITIONS in ascending order, padded with -1 when  */
 /* fewer than k compete.  Position of candidate i: i, or with pool_blocks != NULL        */
 /* ([rows, n/block]) pool_blocks[i/block]*block + i%block -- ascending candidates map to */
@@ -356,10 +359,12 @@ CSA2_API csa2_status csa2_sparse_attn(const csa2_attn_args *a, uint16_t *out, fl
 /* the scratch it uses with cudaMemsetAsync on `stream`.                                */
 /*                                                                                    */
 /* The first call on a device (with that device current) looks up the array's device   */
-/* address with cudaGetSymbolAddress and caches it; make that first call before any     */
-/* stream capture on that device.  All calls on a device share the one array and it    */
-/* keeps the last call's contents: calls whose GPU work overlaps (concurrent streams)   */
-/* race on it, so serialise them.                                                       */
+/* address with cudaGetSymbolAddress and caches it for the life of the process, keyed   */
+/* by device ordinal; make that first call before any stream capture on that device.   */
+/* The cached address belongs to the device's primary context: it does not survive a   */
+/* cudaDeviceReset, and a call with another context current must not be made.  All     */
+/* calls on a device share the one array and it keeps the last call's contents: calls  */
+/* whose GPU work overlaps (concurrent streams) race on it, so serialise them.          */
 /* ---------------------------------------------------------------------------------- */
 CSA2_API csa2_status csa2_index_score_noalloc(const csa2_index_args *a, float *scores,
                                               int32_t *row_len, uint32_t *d_status,

@@ -399,9 +399,9 @@ def test_pool_scores_and_topk():
             assert np.array_equal(idx_f[b, t].cpu().numpy(), oracle.topk(s_ref, pos, w.topk))
 
 
-def _near_tie_case(N, seed, neg=False):
+def _near_tie_case(N, seed, neg=False, tiny_exp=-30):
     """Keys whose float32 scores tie while their exact scores differ: two heads with
-    w = (1, 2^-30) (negative: (1, -2^-30)).  Every key has the same block-0 dot with head 0;
+    w = (1, 2^tiny_exp) (negative: (1, -2^tiny_exp)).  Every key has the same block-0 dot with head 0;
     head 1 reads a block whose dot is a different small integer per key.  The float32
     chain rounds 2^-30 * d_1 away, so the float order is the position order; the exact
     order follows d_1."""
@@ -414,15 +414,16 @@ def _near_tie_case(N, seed, neg=False):
     k[0, :, :32] = 0.5                                 # d_0 = 16 for every key
     k[0, :, 32:64] = rng.integers(0, 7, size=(N, 32)) * 0.5 * (rng.random((N, 32)) < 0.3)
     k[0, :, 36] = 3.0                                  # block amax 3: scale 2^-1, values exact
-    wv = np.array([[[1.0, (-1.0 if neg else 1.0) * 2.0 ** -30]]], np.float32)
+    wv = np.array([[[1.0, (-1.0 if neg else 1.0) * 2.0 ** tiny_exp]]], np.float32)
     return q, k, wv
 
 
-@pytest.mark.parametrize("N,neg", [(1500, False), (2000, True), (700, False)])
-def test_exact_order_resolves_float32_ties(N, neg):
+@pytest.mark.parametrize("N,neg,tiny_exp", [(1500, False, -30), (2000, True, -30), (700, False, -100),
+                                            (900, True, -100)])
+def test_exact_order_resolves_float32_ties(N, neg, tiny_exp):
     # the whole row is one float32 tie group within the error bound: the band holds every
-    # position (<= 2,048) and the exact pass orders them by their low-order limbs
-    q, k, wv = _near_tie_case(N, N + neg, neg)
+    # position (<= 2,048) and the exact pass orders them by their low-order bits
+    q, k, wv = _near_tie_case(N, N + neg, neg, tiny_exp)
     qb, kb = synth.f32_to_bf16_bits(q), synth.f32_to_bf16_bits(k)
     assert np.array_equal(f32(qb), q) and np.array_equal(f32(kb), k)
     st = status()

@@ -62,3 +62,25 @@ def test_noalloc_matches_workspace_entry_point(name, wl):
             for t in range(T):
                 L = int(ref_len[b, t])
                 assert _bits_equal(got[b, t, :L], ref[b, t, :L]), f"{name} call {call} row ({b},{t})"
+
+
+def test_noalloc_rejects_requests_beyond_its_scratch():
+    # 32,769 query rows on tensor-core-eligible arguments need 262,152 bytes of counters,
+    # one row more than the 256 KB array holds: CSA2_ERR_WORKSPACE before anything is
+    # launched, outputs untouched.  Every buffer is allocated at its full size anyway.
+    rows, H, d, N = 32769, 1, 128, 64
+    q = torch.zeros((1, rows, H, d), dtype=torch.bfloat16, device=DEV)
+    w = torch.ones((1, rows, H), dtype=torch.float32, device=DEV)
+    kc = torch.zeros((1, N, d // 2), dtype=torch.uint8, device=DEV)
+    ks = torch.full((1, N, d // 32), 127, dtype=torch.uint8, device=DEV)
+    args = csa2.make_index_args(q, w, kc, ks)
+    lib = csa2.load()
+    assert lib.csa2_index_score_workspace_size(ctypes.byref(args)) > 256 * 1024
+    scores = torch.full((1, rows, N), float("nan"), dtype=torch.float32, device=DEV)
+    row_len = torch.full((1, rows), -7, dtype=torch.int32, device=DEV)
+    status = lib.csa2_index_score_noalloc(ctypes.byref(args), ctypes.c_void_p(scores.data_ptr()),
+                                          ctypes.c_void_p(row_len.data_ptr()), None,
+                                          ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    torch.cuda.synchronize()
+    assert status == csa2.ERR_WORKSPACE
+    assert bool(torch.isnan(scores).all()) and bool((row_len == -7).all())

@@ -168,10 +168,12 @@ __device__ __forceinline__ float exact_head_dot(const uint8_t *kc, uint32_t sfw,
     return dyadic_sum_f32<4>(I, E);
 }
 
-// The warp re-scores its lanes flagged in `todo` exactly, one head per lane, chaining the
-// heads' terms in head order as the tensor-core path does; returns this lane's new score
+// The warp re-scores its lanes flagged in `todo` exactly, one head per lane, summing the
+// heads' terms in the order the calling kernel uses (split: the eight partial sums of the
+// prefill-chunk epilogue, else one chain in head order); returns this lane's new score
 // (or `score` when the lane was not flagged).  Out of line: the hot loop keeps only the
 // call.
+template <bool SPLIT>
 __device__ __noinline__ float rescore_flagged(uint32_t todo, float score, uint32_t sfw, int64_t cand0,
                                               const uint8_t *kc_row0, const int32_t *pool, int pool_mode,
                                               int64_t n_keys, const uint8_t *qb, const uint8_t *qsf,
@@ -191,9 +193,20 @@ __device__ __noinline__ float rescore_flagged(uint32_t todo, float score, uint32
         const uint32_t psfw = __shfl_sync(0xffffffffu, sfw, src);
         const float Dh = lane < H ? exact_head_dot(kc_row0 + pos * kRowBytes, psfw, qb, qsf, qi, lane) : 0.0f;
         float e = 0.0f;
-        for (int h = 0; h < H; ++h) {
-            const float d = __shfl_sync(0xffffffffu, Dh, h);
-            e = __fmaf_rn(w[h], d > 0.0f ? d : 0.0f, e);
+        if constexpr (SPLIT) {
+            float p[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+            for (int h = 0; h < kNPad; ++h) {
+                const float d = __shfl_sync(0xffffffffu, Dh, h);
+                p[h & 7] = __fmaf_rn(h < H ? w[h] : 0.0f, d > 0.0f ? d : 0.0f, p[h & 7]);
+            }
+            e = __fadd_rn(__fadd_rn(__fadd_rn(p[0], p[1]), __fadd_rn(p[2], p[3])),
+                          __fadd_rn(__fadd_rn(p[4], p[5]), __fadd_rn(p[6], p[7])));
+        } else {
+            for (int h = 0; h < H; ++h) {
+                const float d = __shfl_sync(0xffffffffu, Dh, h);
+                e = __fmaf_rn(w[h], d > 0.0f ? d : 0.0f, e);
+            }
         }
         if (lane == src) score = e;
     }
@@ -235,7 +248,7 @@ __device__ __noinline__ void recheck_stage(const TcParams &P, const TcSmem<QG> &
             if (!todo) continue;
             float *srow = P.scores + (row0 + qi) * P.n_cand;
             float sc = valid ? srow[p] : 0.0f;
-            sc = rescore_flagged(todo, sc, kw, g0, P.kc + kbase * kRowBytes, pool, P.pool_mode, P.n_keys, S.b,
+            sc = rescore_flagged<Cfg<QG>::kDeferred>(todo, sc, kw, g0, P.kc + kbase * kRowBytes, pool, P.pool_mode, P.n_keys, S.b,
                                  reinterpret_cast<const uint8_t *>(S.sfb), S.w[qi], qi, P.H);
             if ((todo >> lane) & 1u) srow[p] = sc;
             if (__any_sync(0xffffffffu, ((todo >> lane) & 1u) && !(fabsf(sc) <= 3.4028234663852886e38f)) &&
@@ -699,23 +712,57 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
             // (the chains of a warp's queries advance together: independent FMAs between
             // the dependent steps of each chain)
             float scs[kQPerWarp];
+            if constexpr (!C::kDeferred) {
+                // decode: one fma chain per query in head order
 #pragma unroll
-            for (int u = 0; u < kQPerWarp; ++u) scs[u] = 0.0f;
+                for (int u = 0; u < kQPerWarp; ++u) scs[u] = 0.0f;
 #pragma unroll
-            for (int h4 = 0; h4 < kNPad / 4; ++h4) {
-                float wh[kQPerWarp][4];
-#pragma unroll
-                for (int u = 0; u < kQPerWarp; ++u) {
-                    const float4 wv = reinterpret_cast<const float4 *>(S.w[q_lo + u])[h4];
-                    wh[u][0] = wv.x; wh[u][1] = wv.y; wh[u][2] = wv.z; wh[u][3] = wv.w;
-                }
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
+                for (int h4 = 0; h4 < kNPad / 4; ++h4) {
+                    float wh[kQPerWarp][4];
 #pragma unroll
                     for (int u = 0; u < kQPerWarp; ++u) {
-                        const float D = __uint_as_float(r[u][4 * h4 + j]);
-                        scs[u] = __fmaf_rn(wh[u][j], D > 0.0f ? D : 0.0f, scs[u]);
+                        const float4 wv = reinterpret_cast<const float4 *>(S.w[q_lo + u])[h4];
+                        wh[u][0] = wv.x; wh[u][1] = wv.y; wh[u][2] = wv.z; wh[u][3] = wv.w;
                     }
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+#pragma unroll
+                        for (int u = 0; u < kQPerWarp; ++u) {
+                            const float D = __uint_as_float(r[u][4 * h4 + j]);
+                            scs[u] = __fmaf_rn(wh[u][j], D > 0.0f ? D : 0.0f, scs[u]);
+                        }
+                    }
+                }
+            } else {
+                // prefill chunks: eight independent partial sums per query (head h goes to
+                // lane h % 2 of packed accumulator (h / 2) % 4), four fused steps deep, then a
+                // fixed tree -- the chain's latency no longer paces the epilogue.  Any order
+                // keeps the float score within the bound the exact selection uses.
+#pragma unroll
+                for (int u = 0; u < kQPerWarp; ++u) {
+                    unsigned long long acc[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+                    for (int h8 = 0; h8 < kNPad / 8; ++h8) {
+                        const float4 wa = reinterpret_cast<const float4 *>(S.w[q_lo + u])[2 * h8];
+                        const float4 wb = reinterpret_cast<const float4 *>(S.w[q_lo + u])[2 * h8 + 1];
+                        const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const float d0 = fmaxf(__uint_as_float(r[u][8 * h8 + 2 * j]), 0.0f);
+                            const float d1 = fmaxf(__uint_as_float(r[u][8 * h8 + 2 * j + 1]), 0.0f);
+                            asm("{\n\t.reg .b64 a, b;\n\tmov.b64 a, {%1, %2};\n\tmov.b64 b, {%3, %4};\n\t"
+                                "fma.rn.f32x2 %0, a, b, %0;\n\t}"
+                                : "+l"(acc[j]) : "f"(wv[2 * j]), "f"(wv[2 * j + 1]), "f"(d0), "f"(d1));
+                        }
+                    }
+                    float lo[4], hi[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        lo[j] = __uint_as_float((uint32_t)acc[j]);
+                        hi[j] = __uint_as_float((uint32_t)(acc[j] >> 32));
+                    }
+                    scs[u] = __fadd_rn(__fadd_rn(__fadd_rn(lo[0], hi[0]), __fadd_rn(lo[1], hi[1])),
+                                       __fadd_rn(__fadd_rn(lo[2], hi[2]), __fadd_rn(lo[3], hi[3])));
                 }
             }
 #pragma unroll
@@ -730,7 +777,7 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
                                                   qmax[u] + kmax - 2 > 100);
                     const uint32_t todo = __ballot_sync(0xffffffffu, unsafe);
                     if (todo)
-                        sc = rescore_flagged(todo, sc, sfw, g0, P.kc + kbase * kRowBytes, pool, P.pool_mode,
+                        sc = rescore_flagged<C::kDeferred>(todo, sc, sfw, g0, P.kc + kbase * kRowBytes, pool, P.pool_mode,
                                              P.n_keys, S.b, reinterpret_cast<const uint8_t *>(S.sfb), S.w[qi],
                                              qi, H);
                 }

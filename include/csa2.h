@@ -202,9 +202,13 @@ CSA2_API csa2_status csa2_rope_quant_fp4(const csa2_rope_quant_job *jobs, int32_
 /*   the call, 32-value blocks, same rule as csa2_quant_fp4), w_h the exact value of    */
 /*   the float32 weight.  Selections (csa2_topk / csa2_block_candidates with `exact`)   */
 /*   rank positions by this exact value.  The float32 scores written out here are its  */
-/*   approximation: D_h = float32 round-to-nearest-even of the exact dot, s = float32   */
-/*   fma chain s <- fma(w_h, max(D_h, 0), s) over h = 0..H-1 from s = +0, which is      */
-/*   within (H + 2) 2^-24 A_t + 2^-149 (sum_h |w_h| + H) of s_t, A_t = sum_h |w_h| *    */
+/*   approximation from D_h = float32 round-to-nearest-even of the exact dot and        */
+/*   R_h = max(D_h, 0): a float32 fma chain s <- fma(w_h, R_h, s) over h = 0..H-1 from  */
+/*   s = +0; except for a chunk of queries (FULL mode, n_q >= 8, head_dim 128,          */
+/*   n_heads <= 32, n_keys <= 2^21, batch * n_keys < 2^31, q 16-byte aligned), where    */
+/*   eight chains p_j run over the heads h = j mod 8 and                                */
+/*   s = ((p0 + p1) + (p2 + p3)) + ((p4 + p5) + (p6 + p7)).  Either is within           */
+/*   (H + 2) 2^-24 A_t + 2^-149 (sum_h |w_h| + H) of s_t, A_t = sum_h |w_h| *           */
 /*   max(0, q_hat_h . k_hat_t), whenever it is finite.  A score that is not finite sets */
 /*   CSA2_DEV_SCORE_RANGE.                                                              */
 /* Visibility: entry j covers tokens [j*m, j*m+m-1] (no overlap, report §2.3) and a     */

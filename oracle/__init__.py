@@ -67,7 +67,7 @@ def _L():
             lib.orc_quant_nvfp4.argtypes = [P, I64, I64, P, P]
             lib.orc_dequant_nvfp4.argtypes = [P, P, I64, I64, P]
             lib.orc_head_dots.argtypes = [I, I, P, P, P, P, P, I64, P]
-            lib.orc_index_scores.argtypes = [I, I, P, P, P, P, P, P, I64, P]
+            lib.orc_index_scores.argtypes = [I, I, P, P, P, P, P, P, I64, P, I]
             lib.orc_index_scores_exact.argtypes = [I, I, P, P, P, P, P, P, I64, P]
             lib.orc_exact_limbs.restype = I
             lib.orc_exact_e0.restype = I
@@ -189,8 +189,11 @@ def head_dots(qc, qs, kc, ks, pos) -> np.ndarray:
     return out
 
 
-def index_scores(qc, qs, w, kc, ks, pos) -> np.ndarray:
-    """float32 indexer scores of one quantised query at key rows ``pos``."""
+def index_scores(qc, qs, w, kc, ks, pos, order: str = "chain") -> np.ndarray:
+    """float32 indexer scores of one quantised query at key rows ``pos``, the head terms
+    summed in the library's order: "chain" (one fma chain in head order) or "split8" (the
+    prefill-chunk kernel's eight partial chains over heads h = j mod 8, then
+    ((p0 + p1) + (p2 + p3)) + ((p4 + p5) + (p6 + p7)))."""
     qc = np.ascontiguousarray(qc, np.uint8); qs = np.ascontiguousarray(qs, np.uint8)
     kc = np.ascontiguousarray(kc, np.uint8); ks = np.ascontiguousarray(ks, np.uint8)
     w = np.ascontiguousarray(w, np.float32)
@@ -198,7 +201,7 @@ def index_scores(qc, qs, w, kc, ks, pos) -> np.ndarray:
     H, d = qc.shape[0], qc.shape[1] * 2
     out = np.empty(pos.size, np.float32)
     _L().orc_index_scores(H, d, _p(qc), _p(qs), _p(w), _p(kc), _p(ks), _p(pos), pos.size,
-                          _p(out))
+                          _p(out), {"chain": 0, "split8": 1}[order])
     return out
 
 

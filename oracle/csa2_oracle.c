@@ -25,6 +25,7 @@
  * reproduced bit for bit by orc_index_scores:
  *   D_h = RN32(exact q_h . k)          one rounding of the exact dyadic dot
  *   s   = fma32(w_{H-1}, R_{H-1}, ... fma32(w_0, R_0, +0))     R_h = max(D_h, 0)
+ * or, for the chunk kernel's order, eight partial chains summed in a fixed tree.
  * Build: gcc -O2 -std=c11 -fopenmp -ffp-contract=off -shared -fPIC.
  */
 #include <stdint.h>
@@ -379,11 +380,13 @@ void orc_head_dots(int H, int d, const uint8_t *qc, const uint8_t *qs,
     free(tq);
 }
 
-/* Indexer score of one query against listed key rows:
- *   s = fma32 chain over h = 0..H-1 of (w_h, max(D_h, 0)), starting from +0. */
+/* float32 indexer score of one query against listed key rows, R_h = max(D_h, 0):
+ *   order 0: s = fma32 chain over h = 0..H-1 of (w_h, R_h), starting from +0;
+ *   order 1: eight partial sums p_j = fma32 chain over h = j, j+8, j+16, ... (from +0),
+ *            then s = ((p0 + p1) + (p2 + p3)) + ((p4 + p5) + (p6 + p7)) in float32. */
 void orc_index_scores(int H, int d, const uint8_t *qc, const uint8_t *qs, const float *w,
                       const uint8_t *kc, const uint8_t *ks, const int64_t *pos, int64_t npos,
-                      float *out)
+                      float *out, int order)
 {
     int *tq = (int *)malloc(sizeof(int) * (size_t)H * (size_t)d);
     if (!tq) return;
@@ -392,12 +395,14 @@ void orc_index_scores(int H, int d, const uint8_t *qc, const uint8_t *qs, const 
     for (int64_t i = 0; i < npos; ++i) {
         int tk[2048];
         decode_twice(d, kc + pos[i] * (d / 2), tk);
-        float s = 0.0f;
+        float s = 0.0f, p[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
         for (int h = 0; h < H; ++h) {
             float D = exact_dot_f32(d, tq + h * d, qs + (int64_t)h * (d / 32), tk, ks + pos[i] * (d / 32));
             float R = D > 0.0f ? D : 0.0f;
-            s = fmaf(w[h], R, s);
+            if (order == 0) s = fmaf(w[h], R, s);
+            else p[h % 8] = fmaf(w[h], R, p[h % 8]);
         }
+        if (order != 0) s = ((p[0] + p[1]) + (p[2] + p[3])) + ((p[4] + p[5]) + (p[6] + p[7]));
         out[i] = s;
     }
     free(tq);

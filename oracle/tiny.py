@@ -146,16 +146,25 @@ def exact_vector(codes_packed: np.ndarray, scales: np.ndarray) -> List[Fraction]
     return vals
 
 
-def score(qc, qs, w, kc, ks) -> np.float32:
-    """s = fma32 chain over heads of (w_h, max(RN32(q_h . k), 0))."""
+def score(qc, qs, w, kc, ks, order: str = "chain") -> np.float32:
+    """float32 score from R_h = max(RN32(q_h . k), 0): "chain" = fma32 chain over heads of
+    (w_h, R_h); "split8" = eight fma32 chains over the heads h = j mod 8, added as
+    ((p0 + p1) + (p2 + p3)) + ((p4 + p5) + (p6 + p7)) with float32 roundings."""
     kv = exact_vector(kc, ks)
     s = np.float32(0.0)
+    p = [np.float32(0.0)] * 8
     for h in range(qc.shape[0]):
         qv = exact_vector(qc[h], qs[h])
         D = rn32(sum((a * b for a, b in zip(qv, kv)), Fraction(0)))
         R = D if D > 0 else np.float32(0.0)
-        s = fma32(np.float32(w[h]), R, s)
-    return s
+        if order == "chain":
+            s = fma32(np.float32(w[h]), R, s)
+        else:
+            p[h % 8] = fma32(np.float32(w[h]), R, p[h % 8])
+    if order == "chain":
+        return s
+    add = lambda a, b: fma32(np.float32(1.0), a, b)           # one rounding of a + b
+    return add(add(add(p[0], p[1]), add(p[2], p[3])), add(add(p[4], p[5]), add(p[6], p[7])))
 
 
 def topk_positions(scores: Sequence[float], positions: Sequence[int], k: int) -> List[int]:

@@ -280,9 +280,17 @@ def _with_group_max(dw, w, pool=None, st=None):
     return scores, gm, idx
 
 
-def _oracle_row_scores(w, b, t, qi, ww, kc, ks, pos):
+def score_order(n_q, idx_dim, idx_heads, pool=False):
+    """Summation order of the float32 scores the indexer writes (include/csa2.h): the
+    chunk kernel (Full mode, >= 8 queries a sequence, head dim 128, <= 32 heads) adds the
+    heads in eight partial chains, every other kernel in one chain."""
+    return "split8" if (not pool and n_q >= 8 and idx_dim == 128 and idx_heads <= 32) else "chain"
+
+
+def _oracle_row_scores(w, b, t, qi, ww, kc, ks, pos, pool=False):
     qc, qs = oracle.quant_mxfp4(f32(qi[t]))
-    return oracle.index_scores(qc, qs, ww[t], kc, ks, pos)
+    return oracle.index_scores(qc, qs, ww[t], kc, ks, pos,
+                               order=score_order(w.n_q, w.idx_dim, w.idx_heads, pool))
 
 
 def _oracle_row_exact(w, b, t, qi, ww, kc, ks, pos):
@@ -358,7 +366,8 @@ def test_scores_wide_exponents(T, sparse):
     for b in range(B):
         for t in range(T):
             qc, qs = oracle.quant_mxfp4(f32(qbits[b, t]))
-            s_ref = oracle.index_scores(qc, qs, wv[b, t], kc[b], ks[b], np.arange(N))
+            s_ref = oracle.index_scores(qc, qs, wv[b, t], kc[b], ks[b], np.arange(N),
+                                        order=score_order(T, d, H))
             assert same_f32(scores[b, t].cpu().numpy(), s_ref)
             # groups re-scored by the exact pass carry the exact scores' maxima
             assert np.array_equal(gm[b, t].cpu().numpy().view(np.uint32), group_keys(s_ref))
@@ -387,7 +396,7 @@ def test_pool_scores_and_topk():
             nvis = oracle.n_visible(int(qpos[b, t]), 1, w.n_keys)
             pos = oracle.pool_positions(pool_np[b, t], w.block, nvis)
             assert int(row_len[b, t]) == pos.size
-            s_ref = _oracle_row_scores(w, b, t, qi_all[b], ww_all[b], kc, ks, pos)
+            s_ref = _oracle_row_scores(w, b, t, qi_all[b], ww_all[b], kc, ks, pos, pool=True)
             assert same_f32(scores[b, t, :pos.size].cpu().numpy(), s_ref)
             ng = (pos.size + 31) // 32
             assert np.array_equal(gm[b, t, :ng].cpu().numpy().view(np.uint32), group_keys(s_ref))

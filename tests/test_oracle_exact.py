@@ -170,17 +170,18 @@ def test_float32_scores_within_error_bound(H, lo, hi, wkind, seed):
     if wkind == "normal" and H >= 4:
         qc[1], qs[1], w[1] = qc[0], qs[0], -w[0] * np.float32(1.0000001)
     pos = np.arange(N)
-    f = oracle.index_scores(qc, qs, w, kc, ks, pos)
     ex = oracle.index_scores_exact(qc, qs, w, kc, ks, pos)
     A = oracle.index_scores_exact(qc, qs, np.abs(w), kc, ks, pos)
-    checked = 0
-    for t in range(N):
-        if not np.isfinite(f[t]):
-            continue                      # overflow: outside the bound's domain
-        err = abs(Fraction(float(f[t])) - _frac(ex[t]))
-        assert err <= _bound(w, _frac(A[t]), H), t
-        checked += 1
-    assert checked >= 20
+    for order in ("chain", "split8"):                 # both orders the library writes
+        f = oracle.index_scores(qc, qs, w, kc, ks, pos, order=order)
+        checked = 0
+        for t in range(N):
+            if not np.isfinite(f[t]):
+                continue                      # overflow: outside the bound's domain
+            err = abs(Fraction(float(f[t])) - _frac(ex[t]))
+            assert err <= _bound(w, _frac(A[t]), H), (order, t)
+            checked += 1
+        assert checked >= 20
 
 
 def test_exact_topk_and_blocks_match_sorted_bruteforce():

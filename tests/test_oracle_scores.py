@@ -4,7 +4,8 @@ Score (the workload definition; the report, aipaper.jasonlin.tech §2.3, says on
 the indexer scores main-KV entries from indexer Q and indexer K):
     s = sum_h w_h * ReLU(q_h . k)
 with q, k MXFP4 (report §2.4.4), each head dot rounded once to float32 and the head
-sum a float32 fma chain.  Pins: an exact Fraction brute force on tiny inputs
+sum a float32 fma chain (or, for the prefill-chunk kernel, eight partial chains over the
+heads h = j mod 8 added in a fixed tree).  Pins: an exact Fraction brute force on tiny inputs
 (typical and extreme scales, so both the double path and the wide-integer path of the
 C oracle run), hand-derived rounding cases where a tiny term breaks a tie, and the
 textbook case H = 1, w = 1 where the score is the plain dot product.
@@ -39,13 +40,15 @@ def test_scores_match_fraction_bruteforce(H, d, lo, hi, seed):
         w[2] = 0.0
     pos = np.arange(N, dtype=np.int64)
     got = oracle.index_scores(qc, qs, w, kc, ks, pos)
+    got8 = oracle.index_scores(qc, qs, w, kc, ks, pos, order="split8")
     dots = oracle.head_dots(qc, qs, kc, ks, pos)
     for t in range(N):
-        exp = np.float32(tiny.score(qc, qs, w, kc[t], ks[t]))
-        if np.isnan(exp):
-            assert np.isnan(got[t])          # NaN payloads differ between platforms
-        else:
-            assert got[t].view(np.uint32) == exp.view(np.uint32), (t, got[t], exp)
+        for g, order in ((got, "chain"), (got8, "split8")):
+            exp = np.float32(tiny.score(qc, qs, w, kc[t], ks[t], order))
+            if np.isnan(exp):
+                assert np.isnan(g[t])            # NaN payloads differ between platforms
+            else:
+                assert g[t].view(np.uint32) == exp.view(np.uint32), (order, t, g[t], exp)
         kv = tiny.exact_vector(kc[t], ks[t])
         for h in range(H):
             qv = tiny.exact_vector(qc[h], qs[h])

@@ -6,12 +6,13 @@
 //     D[t, h] = sum_d k_hat[t, d] * q_hat[h, d]      (t: 128-position tile, h: heads)
 // run as block-scaled MMA (kind::mxf4, E2M1 x E2M1, UE8M0 scale per 32) with M = 128
 // positions, N = 32 heads per query, K = 128 (two K = 64 steps).  The epilogue reads each
-// position's 32 head dots from tensor memory and forms s = fma32 chain of w_h * ReLU(D_h).
+// position's 32 head dots from tensor memory and sums w_h * ReLU(D_h) over the heads.
 //
-// Precision.  The float32 score written out is the fma chain over heads of w_h * max(D_h, 0)
-// with D_h = RN32(exact dot); the selection kernels rank by the exact score and use this
-// one through its error bound, which needs each D_h correctly rounded.  Non-finite scores
-// set CSA2_DEV_SCORE_RANGE.  The per-head dot D_h = RN32(exact dot).  Each K = 32 block adds an
+// Precision.  The float32 score written out sums w_h * max(D_h, 0) in one fma chain in head
+// order (decode) or in eight chains over the heads h = j mod 8 added in a fixed tree
+// (prefill chunks), with D_h = RN32(exact dot); the selection kernels rank by the exact
+// score and use this one through its error bound, which needs each D_h correctly rounded.
+// Non-finite scores set CSA2_DEV_SCORE_RANGE.  The per-head dot D_h = RN32(exact dot).  Each K = 32 block adds an
 // integer (< 2^13) times 2^(Xq + Xk - 2); when every term's exponent lies within 9 of the
 // others and in the normal range, every partial sum is exactly representable, so the MMA's
 // float32 accumulation returns the exact dot whatever its order.  That condition is checked

@@ -774,12 +774,14 @@ def indexer_rows(dev):
 
 
 def decode_workloads(dev):
-    """The two decode workloads the default line does not time, each on its own sizes:
-    the tiny Full decode layer (batch 1, 4,096 positions, indexer 4 x 64, 16 heads over a
-    128-dim latent; index score, exact Top-512, attention) as a latency, and the Reuse layer
-    at batch 64 x 131,072 (attention over the given Top-512 + SWA 128; no indexer work)
-    against the HBM copy rate with its algorithmic bytes (gathered main-KV rows, indices,
-    SWA, query, output).  Each is one CUDA graph, replayed after an L2 flush; median of 20."""
+    """The attention workloads the default line does not time, each on its own sizes: the
+    tiny Full decode layer (batch 1, 4,096 positions, indexer 4 x 64, 16 heads over a
+    128-dim latent; index score, exact Top-512, attention) as a latency; the Reuse layer at
+    batch 64 x 131,072 (attention over the given Top-512 + SWA 128; no indexer work); and
+    the decoder's SWA bounded replay (8 x 128 tokens from s = 131,072, SWA keys truncated at
+    s).  The last two against the HBM copy rate with their algorithmic bytes (gathered
+    main-KV rows, indices, SWA rows, query, output).  Each is one CUDA graph, replayed after
+    an L2 flush; median of 20."""
     import ctypes
     import torch
     from fp4_kv_cache_gb300 import csa2, workload
@@ -862,6 +864,36 @@ def decode_workloads(dev):
     flop = 2.0 * B * T * w.heads * (w.topk + w.window) * (w.d_qk + w.d_v)
     res["reuse_decode_128k"] = {
         "workload": w.name, "batch": B, "context": w.n_keys, "sparse_attn_ms": t,
+        "tokens_per_s": B * T / (t * 1e-3), "bytes": ab, "gbs": ab / (t * 1e-3) / 1e9,
+        "frac_hbm": ab / (t * 1e-3) / 1e9 / peak, "tflops": flop / (t * 1e-3) / 1e12,
+        "frac_bf16": flop / (t * 1e-3) / 1e12 / _bf16_peak()}
+    del dw, out, lse, ws_a
+    torch.cuda.empty_cache()
+
+    # ---- SWA bounded replay: 128 tokens from s through attention (given Top-512 each)
+    w = synth.WORKLOADS["swa_replay_prefill"]
+    dw = workload.build(w, device=dev, kidx=False, d_status=st)
+    B, T = w.batch, w.n_q
+    out = torch.empty((B, T, w.heads, w.d_v), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, T, w.heads), dtype=torch.float32, device=dev)
+    aargs = csa2.make_attn_args(dw["q_attn"], dw["kv_codes"], dw["kv_scales"], dw["reuse_idx"], dw["swa"],
+                                dw["swa_pos0"], dw["q_pos"], dw["swa_start"], w.window, dw.sm_scale, w.d_v)
+    ws_a = torch.empty(max(1, lib.csa2_sparse_attn_workspace_size(ctypes.byref(aargs))), dtype=torch.uint8,
+                       device=dev)
+
+    def replay():
+        csa2.csa2_sparse_attn(aargs, out, lse, st, workspace=ws_a)
+
+    t = graph_ms(replay)
+    if int(st.item()) != 0:
+        raise RuntimeError(f"device status {int(st.item())}")
+    n_swa_keys = sum(min(w.window, j + 1) for j in range(T))          # query s + j sees j + 1
+    # per sequence: every query's gathered rows, indices, query and output, and the T
+    # replayed SWA rows (tokens s .. s + T - 1), each needed once
+    ab = B * (T * (w.topk * (kv_row + 4) + w.heads * w.d_qk * 2 + w.heads * w.d_v * 2) + T * w.d_qk * 2)
+    flop = 2.0 * B * w.heads * (T * w.topk + n_swa_keys) * (w.d_qk + w.d_v)
+    res["swa_replay_prefill"] = {
+        "workload": w.name, "batch": B, "queries": T, "replay_start": w.swa_start, "sparse_attn_ms": t,
         "tokens_per_s": B * T / (t * 1e-3), "bytes": ab, "gbs": ab / (t * 1e-3) / 1e9,
         "frac_hbm": ab / (t * 1e-3) / 1e9 / peak, "tflops": flop / (t * 1e-3) / 1e12,
         "frac_bf16": flop / (t * 1e-3) / 1e12 / _bf16_peak()}
@@ -998,6 +1030,8 @@ def main():
                     help="skip the step over the E2M1 + E4M3/16 main-KV cache")
     ap.add_argument("--prefill-only", action="store_true",
                     help="time only the prefill indexer (for profiling it) and print its object")
+    ap.add_argument("--workloads-only", action="store_true",
+                    help="time only the tiny decode, Reuse and SWA-replay workloads and print their object")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -1005,6 +1039,11 @@ def main():
         import torch
         torch.cuda.set_device(0)
         print(json.dumps({"prefill_indexer": prefill_indexer(torch.device("cuda", 0), None, with_chunk=False)}))
+        return 0
+    if args.workloads_only:
+        import torch
+        torch.cuda.set_device(0)
+        print(json.dumps({"decode_workloads": decode_workloads(torch.device("cuda", 0))}))
         return 0
     if args.indexer_rows_only:
         import torch

@@ -93,6 +93,12 @@ WORKLOADS = {
     "prefill_chunk_m2": Workload("prefill_chunk_m2", batch=1, n_q=4096, n_keys=67584, ratio_m=2,
                                  q_pos0=131072, idx_heads=32, idx_dim=128, heads=64, d_qk=576,
                                  d_v=512, seed=4),
+    # decoder SWA bounded replay (report §3.2.2): the last 128 tokens of a 131,072-token
+    # context replayed from s = 131,072 through attention; query i attends its given
+    # Top-512 entries and the SWA keys [max(s, i - W + 1), i] (1 to 128 of them)
+    "swa_replay_prefill": Workload("swa_replay_prefill", batch=8, n_q=128, n_keys=131072, ratio_m=1,
+                                   q_pos0=131072, idx_heads=32, idx_dim=128, heads=64, d_qk=576,
+                                   d_v=512, seed=5, reuse_idx=True, swa_start=131072),
 }
 
 

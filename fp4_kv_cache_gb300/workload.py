@@ -77,6 +77,8 @@ def build(w: synth.Workload, rows=None, device="cuda:0", kv: bool = True, kidx: 
         out.t["pool"] = torch.from_numpy(np.stack([synth.gen_pool_blocks(w, b) for b in rows])).to(dev)
     if w.reuse_idx:
         out.t["reuse_idx"] = torch.from_numpy(np.stack([synth.gen_reuse_idx(w, b) for b in rows])).to(dev)
+    if w.swa_start:
+        out.t["swa_start"] = torch.full((B,), w.swa_start, dtype=torch.int32, device=dev)
     out.sm_scale = 1.0 / math.sqrt(w.d_qk)
     torch.cuda.synchronize(dev)
     return out

@@ -25,11 +25,16 @@ def _cache(dw, ratio_m=1):
     return Cache(dw["kv_codes"], dw["kv_scales"], dw["k_codes"], dw["k_scales"], ratio_m)
 
 
+def _cache_kv(dw, ratio_m=1):
+    """Cache view for a Reuse layer: main KV only (no indexer K needed)."""
+    return Cache(dw["kv_codes"], dw["kv_scales"], None, None, ratio_m)
+
+
 def _inp(dw):
     return LayerInput(dw["q_attn"], dw["swa"], dw["swa_pos0"], dw["q_pos"], dw["q_idx"], dw["w_idx"])
 
 
-def _check_attention_rows(w, out, lse, idx_np, rows_bt):
+def _check_attention_rows(w, out, lse, idx_np, rows_bt, swa_start=0):
     qpos = synth.q_positions(w)
     n_slots, pos0 = synth.swa_layout(w)
     _, _, qa = synth.gen_queries(w)
@@ -45,7 +50,7 @@ def _check_attention_rows(w, out, lse, idx_np, rows_bt):
             sel = sel[(sel >= 0) & (sel < w.n_keys)]
             kc, ks = oracle.quant_mxfp4(kv[sel])              # only the rows attention reads
             keys = oracle.gather_keys(np.arange(sel.size), kc, ks, swa, int(qpos[b, t]), pos0,
-                                      w.window, 0)
+                                      w.window, swa_start)
             o_ref, l_ref = oracle.attention_rows(f32(qa[b, t])[None].astype(np.float64), [keys],
                                                  1.0 / math.sqrt(w.d_qk), w.d_v)
             o = out[b, t].float().cpu().numpy().astype(np.float64)
@@ -152,3 +157,24 @@ def test_prefill_chunk_sampled():
         idx_ref, _, _ = _oracle_full(w, 0, t, qi, ww, kc, ks, qpos)
         assert np.array_equal(idx_gpu[0, t], idx_ref), t
     _check_attention_rows(w, res.out, res.lse, idx_gpu, [(0, t) for t in sample[::4]])
+
+
+def test_swa_replay_prefill():
+    """Decoder SWA bounded replay (report §3.2.2): 128 tokens replayed from s = 131,072, each
+    attending its given Top-512 entries and the SWA keys [max(s, i - W + 1), i] -- query
+    s + j sees j + 1 of them; the 127 buffered tokens before s are never attended."""
+    w = W["swa_replay_prefill"]
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    dw = workload.build(w, kidx=False, device=DEV, d_status=st)
+    x = LayerInput(dw["q_attn"], dw["swa"], dw["swa_pos0"], dw["q_pos"], swa_start=dw["swa_start"])
+    res = reuse_layer(_cache_kv(dw), x, dw["reuse_idx"], w.window, w.d_v, d_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    n_slots, pos0 = synth.swa_layout(w)
+    qpos = synth.q_positions(w)
+    for t in (0, 5, 127):
+        j0, j1 = oracle.swa_keys_range(int(qpos[0, t]), pos0, n_slots, w.window, w.swa_start)
+        assert j1 - j0 + 1 == min(w.window, t + 1)
+    rows = [(b, t) for b in (0, w.batch - 1) for t in list(range(0, 128, 2)) + [127]]
+    worst = _check_attention_rows(w, res.out, res.lse, dw["reuse_idx"].cpu().numpy(), rows, w.swa_start)
+    assert worst <= 1e-2

@@ -102,6 +102,14 @@ typedef enum { CSA2_BF16 = 0, CSA2_F32 = 1 } csa2_dtype;
  *   always MXFP4 (report §2.4.4). */
 typedef enum { CSA2_FMT_MXFP4 = 0, CSA2_FMT_NVFP4_E4M3_16 = 1 } csa2_fp4_format;
 
+/* SWA KV formats.  The report keeps the SWA cache in FP8 (§2.4.4: it is sensitive to
+ * quantisation) without saying which; MXFP8 is the OCP MX format with E4M3 elements: one
+ * E8M0 scale per 32 values, X = floor(log2(max|x|)) - 8 clamped to [-127, 127] (X = 0 for
+ * an all-zero block), element = round-half-even of x / 2^X onto the E4M3 grid (1 sign, 4
+ * exponent bits with bias 7, 3 mantissa bits, subnormals m x 2^-9), saturating at +-448,
+ * sign bit = sign bit of x.  Element x 2^X is exact in bf16 while it stays normal. */
+typedef enum { CSA2_SWA_BF16 = 0, CSA2_SWA_MXFP8 = 1 } csa2_swa_format;
+
 typedef enum {
     CSA2_INDEX_FULL = 0, /* every causally visible entry is a candidate (Full mode)     */
     CSA2_INDEX_POOL = 1  /* only the positions of the given block pool (Reindex mode)    */
@@ -132,6 +140,21 @@ CSA2_API csa2_status csa2_quant_fp4(const void *x, csa2_dtype xt, int64_t rows, 
 CSA2_API csa2_status csa2_dequant_fp4(const uint8_t *codes, int64_t ldc, const uint8_t *scales,
                              int64_t lds, int64_t rows, int64_t cols, csa2_fp4_format fmt,
                              void *y, csa2_dtype yt, int64_t ldy, csa2_stream stream);
+
+/* ---------------------------------------------------------------------------------- */
+/* csa2_quant_fp8 / csa2_dequant_fp8 -- the MXFP8 (E4M3 + E8M0 per 32) SWA cache codec  */
+/* (report §2.4.4: FP8 SWA KV; the format is the reading stated at csa2_swa_format).    */
+/* x: rows x cols values of type xt (BF16 or F32), row stride ldx elements, cols % 32  */
+/* == 0.  codes: rows x cols bytes, row stride ldc; scales: rows x cols/32 bytes, row  */
+/* stride lds.  Non-finite input sets CSA2_DEV_NONFINITE.  dequant writes y (BF16 or   */
+/* F32, row stride ldy): code value x 2^(scale byte - 127), exact in float32.          */
+/* ---------------------------------------------------------------------------------- */
+CSA2_API csa2_status csa2_quant_fp8(const void *x, csa2_dtype xt, int64_t rows, int64_t cols, int64_t ldx,
+                                    uint8_t *codes, int64_t ldc, uint8_t *scales, int64_t lds,
+                                    uint32_t *d_status, csa2_stream stream);
+CSA2_API csa2_status csa2_dequant_fp8(const uint8_t *codes, int64_t ldc, const uint8_t *scales, int64_t lds,
+                                      int64_t rows, int64_t cols, void *y, csa2_dtype yt, int64_t ldy,
+                                      csa2_stream stream);
 
 /* ---------------------------------------------------------------------------------- */
 /* csa2_quant_fp4_batch -- up to CSA2_QUANT_MAX_JOBS independent csa2_quant_fp4 calls  */
@@ -312,6 +335,7 @@ CSA2_API csa2_status csa2_block_candidates(const float *scores, int64_t rows, in
 /* selected main-KV entries together with the layer's SWA KV; review: the main KV is a  */
 /* latent shared by all query heads; report §3.2.2: SWA keys of a query at token i are   */
 /* [max(s, i-W+1), i] for a replay starting at s).                                      */
+/* SWA keys are bf16, or MXFP8 dequantised exactly (swa_fmt).                          */
 /* Key set of query (b, t): the main-KV rows idx[b,t,j] for j < topk with idx >= 0      */
 /* (dequantised exactly; duplicates kept; idx >= n_kv or < -1 sets CSA2_DEV_BAD_INDEX   */
 /* and is ignored), then the SWA slots j whose token swa_pos0[b] + j lies in            */
@@ -332,12 +356,17 @@ typedef struct {
     const uint8_t *kv_codes; /* [B, n_kv, d_qk/2]  main-KV codes (format kv_fmt)          */
     const uint8_t *kv_scales;/* [B, n_kv, d_qk/G]  main-KV scales, G = 32 (MXFP4) or 16   */
     const int32_t *idx;      /* [B, T, topk]                                              */
-    const uint16_t *swa;     /* bf16 [B, n_swa, d_qk]; NULL = no SWA keys                 */
+    const uint16_t *swa;     /* [B, n_swa, d_qk] bf16 (or E4M3 bytes, swa_fmt); NULL = no */
+                             /* SWA keys                                                  */
     int32_t n_swa;           /* SWA slots per sequence                                    */
     const int32_t *swa_pos0; /* [B] token position of slot 0 (required with swa)          */
     const int32_t *swa_start;/* [B] replay start s, or NULL for s = 0                     */
     const int32_t *q_pos;    /* [B, T] token position of each query (required with swa)   */
     csa2_fp4_format kv_fmt;  /* main-KV format: CSA2_FMT_MXFP4 (0) or NVFP4_E4M3_16 (1)   */
+    csa2_swa_format swa_fmt; /* SWA format: CSA2_SWA_BF16 (0): swa holds bf16 values;    */
+                             /* CSA2_SWA_MXFP8 (1): swa holds [B, n_swa, d_qk] E4M3 codes */
+                             /* (one byte each) and swa_scales their E8M0 scales          */
+    const uint8_t *swa_scales; /* MXFP8: [B, n_swa, d_qk/32] scale bytes, else unused      */
 } csa2_attn_args;
 
 CSA2_API size_t csa2_sparse_attn_workspace_size(const csa2_attn_args *a);

@@ -66,6 +66,8 @@ def _L():
             lib.orc_dequant_mxfp4.argtypes = [P, P, I64, I64, P]
             lib.orc_quant_nvfp4.argtypes = [P, I64, I64, P, P]
             lib.orc_dequant_nvfp4.argtypes = [P, P, I64, I64, P]
+            lib.orc_quant_mxfp8.argtypes = [P, I64, I64, P, P]
+            lib.orc_dequant_mxfp8.argtypes = [P, P, I64, I64, P]
             lib.orc_head_dots.argtypes = [I, I, P, P, P, P, P, I64, P]
             lib.orc_index_scores.argtypes = [I, I, P, P, P, P, P, P, I64, P, I]
             lib.orc_index_scores_exact.argtypes = [I, I, P, P, P, P, P, P, I64, P]
@@ -133,6 +135,32 @@ def dequant_nvfp4(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
     rows = codes.size // (D // 2)
     y = np.empty(codes.shape[:-1] + (D,), np.float64)
     _L().orc_dequant_nvfp4(_p(codes), _p(scales), rows, D, _p(y))
+    return y
+
+
+# ---------------------------------------------------------------- MXFP8 (E4M3) SWA codec
+def quant_mxfp8(x: np.ndarray):
+    """SWA KV in FP8 (report §2.4.4), read as OCP MXFP8 with E4M3 elements: one E8M0 scale
+    per 32 values, X = floor(log2 amax) - 8, elements rounded to nearest E4M3 (ties to even)
+    and saturated at 448.  x [..., D] (exact values), D % 32 == 0 ->
+    (codes uint8 [..., D], scales uint8 [..., D/32])."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    D = x.shape[-1]
+    assert D % 32 == 0
+    rows = x.size // D if D else 0
+    codes = np.empty(x.shape, np.uint8)
+    scales = np.empty(x.shape[:-1] + (D // 32,), np.uint8)
+    _L().orc_quant_mxfp8(_p(x), rows, D, _p(codes), _p(scales))
+    return codes, scales
+
+
+def dequant_mxfp8(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.uint8)
+    D = codes.shape[-1]
+    rows = codes.size // D if D else 0
+    y = np.empty(codes.shape, np.float64)
+    _L().orc_dequant_mxfp8(_p(codes), _p(scales), rows, D, _p(y))
     return y
 
 

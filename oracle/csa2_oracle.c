@@ -225,6 +225,68 @@ void orc_dequant_nvfp4(const uint8_t *codes, const uint8_t *scales, int64_t rows
 }
 
 /* ------------------------------------------------------------------------- */
+/* MXFP8 (E4M3) SWA codec.  Report §2.4.4 keeps the SWA KV cache in FP8; the   */
+/* reading is OCP MX v1.0 with E4M3 elements: per block of 32, X = floor(log2 */
+/* amax) - emax_elem with emax_elem = 8 (448 = 1.75 * 2^8), clamped to         */
+/* [-127, 127], X = 0 for an all-zero block; element = x / 2^X rounded to the */
+/* nearest E4M3 value (ties to the even code), saturating at 448; sign bit =  */
+/* sign bit of x.  Every decision is an exact comparison in double.           */
+/* ------------------------------------------------------------------------- */
+
+/* Nearest non-negative finite E4M3 code to v >= 0 (codes 0x00..0x7E ascend with their
+ * values), ties to the even code, saturating at 448 (0x7E). */
+static int e4m3_round_magnitude(double v)
+{
+    if (v >= 448.0) return 0x7E;
+    for (int c = 0; c < 0x7E; ++c) {
+        double lo = e4m3_value(c), hi = e4m3_value(c + 1);
+        if (v <= hi) {
+            double mid = 0.5 * (lo + hi);                 /* exact */
+            if (v < mid) return c;
+            if (v > mid) return c + 1;
+            return (c % 2 == 0) ? c : c + 1;
+        }
+    }
+    return 0x7E;
+}
+
+/* Quantise rows of doubles (exact bf16/fp32 values) to MXFP8.
+ * codes: [rows, cols] one E4M3 byte per value; scales: [rows, cols/32] = X + 127. */
+void orc_quant_mxfp8(const double *x, int64_t rows, int64_t cols, uint8_t *codes, uint8_t *scales)
+{
+    int64_t nblk = cols / 32;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t b = 0; b < nblk; ++b) {
+            const double *xb = x + r * cols + b * 32;
+            double amax = 0.0;
+            for (int i = 0; i < 32; ++i) amax = fmax(amax, fabs(xb[i]));
+            int X = 0;
+            if (amax > 0.0) {
+                X = floor_log2(amax) - 8;
+                if (X < -127) X = -127;
+                if (X > 127) X = 127;
+            }
+            scales[r * nblk + b] = (uint8_t)(X + 127);
+            for (int i = 0; i < 32; ++i) {
+                double v = ldexp(fabs(xb[i]), -X);        /* exact */
+                codes[r * cols + b * 32 + i] = (uint8_t)(e4m3_round_magnitude(v) | (signbit(xb[i]) ? 0x80 : 0));
+            }
+        }
+    }
+}
+
+/* Dequantise MXFP8 rows to doubles: E4M3 value of the code * 2^(scale - 127). */
+void orc_dequant_mxfp8(const uint8_t *codes, const uint8_t *scales, int64_t rows, int64_t cols, double *y)
+{
+    int64_t nblk = cols / 32;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t i = 0; i < cols; ++i)
+            y[r * cols + i] = ldexp(e4m3_value(codes[r * cols + i]), (int)scales[r * nblk + i / 32] - 127);
+}
+
+/* ------------------------------------------------------------------------- */
 /* Exact dot product of two MXFP4 vectors, rounded once to float32.           */
 /* Twice an E2M1 magnitude is an integer, so each block of 32 contributes     */
 /*   I_b * 2^(Xq_b + Xk_b - 2),  I_b = sum (2 q_i)(2 k_i)  (|I_b| <= 4608).     */

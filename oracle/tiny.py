@@ -192,3 +192,19 @@ def topk_exact_positions(values: Sequence[Fraction], positions: Sequence[int], k
     order = sorted(range(len(positions)), key=lambda i: (-values[i], positions[i]))
     sel = sorted(positions[i] for i in order[:k])
     return sel + [-1] * (k - len(sel))
+
+
+def quant_block_mxfp8(xs: Sequence[Fraction], signs: Sequence[bool]):
+    """OCP MXFP8 (E4M3 elements) of one block of 32 exact values -> (scale byte, [codes]):
+    X = floor(log2 amax) - 8 clamped to [-127, 127] (0 for a zero block); each element the
+    finite E4M3 magnitude nearest to |x| / 2^X (ties to the even code, beyond 448 the
+    nearest is 448), with the sign bit of x."""
+    amax = max(abs(x) for x in xs)
+    X = 0 if amax == 0 else min(127, max(-127, floor_log2(amax) - 8))
+    grid = [e4m3_value(c) for c in range(0x7F)]
+    codes = []
+    for x, neg in zip(xs, signs):
+        v = abs(x) / TWO ** X
+        c = min(range(0x7F), key=lambda c: (abs(v - grid[c]), c % 2))
+        codes.append(c | (0x80 if neg else 0))
+    return X + 127, codes

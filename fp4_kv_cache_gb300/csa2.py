@@ -28,6 +28,7 @@ DEV_SCORE_RANGE, DEV_BAND_LIMIT = 0x10, 0x20
 EXACT_BAND_CAP = 2048
 BF16, F32 = 0, 1
 FMT_MXFP4, FMT_NVFP4_E4M3_16 = 0, 1
+SWA_BF16, SWA_MXFP8 = 0, 1
 FMT_BLOCK = {FMT_MXFP4: 32, FMT_NVFP4_E4M3_16: 16}     # values per scale byte
 INDEX_FULL, INDEX_POOL = 0, 1
 
@@ -50,7 +51,7 @@ class AttnArgs(ctypes.Structure):
                 ("topk", _I32), ("window", _I32), ("sm_scale", ctypes.c_float), ("n_kv", _I64),
                 ("q", _P), ("kv_codes", _P), ("kv_scales", _P), ("idx", _P), ("swa", _P),
                 ("n_swa", _I32), ("swa_pos0", _P), ("swa_start", _P), ("q_pos", _P),
-                ("kv_fmt", ctypes.c_int)]
+                ("kv_fmt", ctypes.c_int), ("swa_fmt", ctypes.c_int), ("swa_scales", _P)]
 
 
 class Csa2Error(RuntimeError):
@@ -106,6 +107,10 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
             lib.csa2_quant_fp4_batch.argtypes = [ctypes.POINTER(QuantJob), _I32, S, _P, _P]
             lib.csa2_rope_quant_fp4.restype = S
             lib.csa2_rope_quant_fp4.argtypes = [ctypes.POINTER(RopeQuantJob), _I32, _P, _P]
+            lib.csa2_quant_fp8.restype = S
+            lib.csa2_quant_fp8.argtypes = [_P, S, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _P]
+            lib.csa2_dequant_fp8.restype = S
+            lib.csa2_dequant_fp8.argtypes = [_P, _I64, _P, _I64, _I64, _I64, _P, S, _I64, _P]
             lib.csa2_dequant_fp4.restype = S
             lib.csa2_dequant_fp4.argtypes = [_P, _I64, _P, _I64, _I64, _I64, S, _P, S, _I64, _P]
             lib.csa2_index_score_workspace_size.restype = sz
@@ -208,6 +213,41 @@ def csa2_quant_fp4(x: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor,
         raise ValueError("x, codes and scales must have the same number of rows")
     _check("csa2_quant_fp4", load().csa2_quant_fp4(
         px, xt, rows, cols, ldx, pc, ldc, ps, lds, fmt, _ptr(d_status), _stream(stream)))
+
+
+def csa2_quant_fp8(x: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor,
+                   d_status: Optional[torch.Tensor] = None, stream=None):
+    """MXFP8 (E4M3 + E8M0 per 32) rows: the SWA cache codec (csa2_quant_fp8)."""
+    cols = x.shape[-1]
+    xt = BF16 if x.dtype == torch.bfloat16 else F32 if x.dtype == torch.float32 else None
+    if xt is None:
+        raise ValueError("x must be bf16 or f32")
+    px, rows, ldx = _rows_view(x)
+    pc, rows_c, ldc = _rows_view(codes)
+    ps, rows_s, lds = _rows_view(scales)
+    if rows_c != rows or rows_s != rows:
+        raise ValueError("x, codes and scales must have the same number of rows")
+    _check("csa2_quant_fp8", load().csa2_quant_fp8(px, xt, rows, cols, ldx, pc, ldc, ps, lds,
+                                                   _ptr(d_status), _stream(stream)))
+
+
+def quant_fp8(x: torch.Tensor, d_status=None, stream=None):
+    """x [..., D] bf16/f32 -> (codes uint8 [..., D], scales uint8 [..., D/32]) in MXFP8."""
+    D = x.shape[-1]
+    codes = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    scales = torch.empty(x.shape[:-1] + (D // 32,), dtype=torch.uint8, device=x.device)
+    csa2_quant_fp8(x, codes, scales, d_status, stream)
+    return codes, scales
+
+
+def dequant_fp8(codes, scales, dtype=torch.float32, stream=None):
+    cols = codes.shape[-1]
+    rows = codes.numel() // cols if cols else 0
+    y = torch.empty(codes.shape, dtype=dtype, device=codes.device)
+    _check("csa2_dequant_fp8", load().csa2_dequant_fp8(
+        _ptr(codes), cols, _ptr(scales), cols // 32, rows, cols, _ptr(y),
+        BF16 if dtype == torch.bfloat16 else F32, cols, _stream(stream)))
+    return y
 
 
 def quant_jobs(triples) -> ctypes.Array:
@@ -356,8 +396,9 @@ def csa2_block_candidates(scores: torch.Tensor, nb: int, block_ids: torch.Tensor
 
 
 def make_attn_args(q, kv_codes, kv_scales, idx, swa=None, swa_pos0=None, q_pos=None,
-                   swa_start=None, window=128, sm_scale=None, d_v=None):
-    """csa2_attn_args; the main-KV format follows from the width of kv_scales."""
+                   swa_start=None, window=128, sm_scale=None, d_v=None, swa_scales=None):
+    """csa2_attn_args; the main-KV format follows from the width of kv_scales; the SWA is
+    bf16, or MXFP8 when swa holds uint8 codes and swa_scales their scales."""
     B, T, H, dqk = q.shape
     a = AttnArgs()
     a.kv_fmt = scales_format(dqk, kv_scales)
@@ -368,7 +409,13 @@ def make_attn_args(q, kv_codes, kv_scales, idx, swa=None, swa_pos0=None, q_pos=N
     a.sm_scale = (1.0 / math.sqrt(dqk)) if sm_scale is None else sm_scale
     a.n_kv = kv_codes.shape[1]
     a.q, a.kv_codes, a.kv_scales, a.idx = _ptr(_bits(q)), _ptr(kv_codes), _ptr(kv_scales), _ptr(idx)
-    a.swa = _ptr(_bits(swa)) if swa is not None else None
+    if swa is not None and swa.dtype == torch.uint8:
+        if swa_scales is None:
+            raise ValueError("MXFP8 SWA codes need swa_scales")
+        a.swa, a.swa_fmt, a.swa_scales = _ptr(swa), SWA_MXFP8, _ptr(swa_scales)
+    else:
+        a.swa = _ptr(_bits(swa)) if swa is not None else None
+        a.swa_fmt, a.swa_scales = SWA_BF16, None
     a.n_swa = swa.shape[1] if swa is not None else 0
     a.swa_pos0, a.swa_start, a.q_pos = _ptr(swa_pos0), _ptr(swa_start), _ptr(q_pos)
     return a
@@ -441,10 +488,11 @@ def block_candidates(scores, nb=2048, row_len=None, block=8, d_status=None, stre
 
 
 def sparse_attn(q, kv_codes, kv_scales, idx, swa=None, swa_pos0=None, q_pos=None, swa_start=None,
-                window=128, sm_scale=None, d_v=None, want_lse=True, d_status=None, stream=None):
+                window=128, sm_scale=None, d_v=None, want_lse=True, d_status=None, stream=None,
+                swa_scales=None):
     """-> (out bf16 [B, T, H, d_v], lse f32 [B, T, H] or None)."""
     args = make_attn_args(q, kv_codes, kv_scales, idx, swa, swa_pos0, q_pos, swa_start, window,
-                          sm_scale, d_v)
+                          sm_scale, d_v, swa_scales)
     B, T, H = q.shape[:3]
     out = torch.empty((B, T, H, args.d_v), dtype=torch.bfloat16, device=q.device)
     lse = torch.empty((B, T, H), dtype=torch.float32, device=q.device) if want_lse else None

@@ -90,8 +90,10 @@ bool attn_args_ok(const csa2_attn_args *a)
     if (empty) return true;
     if (!a->q) return false;
     if (a->topk > 0 && (!a->idx || (a->n_kv > 0 && (!a->kv_codes || !a->kv_scales)))) return false;
+    if (a->swa_fmt != CSA2_SWA_BF16 && a->swa_fmt != CSA2_SWA_MXFP8) return false;
     if (a->swa) {
         if (a->n_swa < 0 || !a->swa_pos0 || !a->q_pos) return false;
+        if (a->swa_fmt == CSA2_SWA_MXFP8 && !a->swa_scales) return false;
     }
     return true;
 }
@@ -203,6 +205,32 @@ csa2_status csa2_rope_quant_fp4(const csa2_rope_quant_job *jobs, int32_t n_jobs,
                 j.fmt == CSA2_FMT_NVFP4_E4M3_16};
     }
     return from_cuda(launch_rope_quant(d, n_jobs, d_status, as_stream(stream)));
+}
+
+csa2_status csa2_quant_fp8(const void *x, csa2_dtype xt, int64_t rows, int64_t cols, int64_t ldx,
+                           uint8_t *codes, int64_t ldc, uint8_t *scales, int64_t lds,
+                           uint32_t *d_status, csa2_stream stream)
+{
+    if (xt != CSA2_BF16 && xt != CSA2_F32) return CSA2_ERR_INVALID_ARG;
+    if (rows < 0 || cols < 0 || cols % 32) return CSA2_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0) return CSA2_OK;
+    if (!x || !codes || !scales) return CSA2_ERR_INVALID_ARG;
+    if (ldx < cols || ldc < cols || lds < cols / 32) return CSA2_ERR_INVALID_ARG;
+    return from_cuda(launch_quant_mxfp8(x, xt == CSA2_BF16, rows, cols, ldx, codes, ldc, scales, lds, d_status,
+                                        as_stream(stream)));
+}
+
+csa2_status csa2_dequant_fp8(const uint8_t *codes, int64_t ldc, const uint8_t *scales, int64_t lds,
+                             int64_t rows, int64_t cols, void *y, csa2_dtype yt, int64_t ldy,
+                             csa2_stream stream)
+{
+    if (yt != CSA2_BF16 && yt != CSA2_F32) return CSA2_ERR_INVALID_ARG;
+    if (rows < 0 || cols < 0 || cols % 32) return CSA2_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0) return CSA2_OK;
+    if (!y || !codes || !scales) return CSA2_ERR_INVALID_ARG;
+    if (ldy < cols || ldc < cols || lds < cols / 32) return CSA2_ERR_INVALID_ARG;
+    return from_cuda(launch_dequant_mxfp8(codes, ldc, scales, lds, rows, cols, y, yt == CSA2_BF16, ldy,
+                                          as_stream(stream)));
 }
 
 csa2_status csa2_dequant_fp4(const uint8_t *codes, int64_t ldc, const uint8_t *scales,

@@ -8,7 +8,7 @@
 //
 // One CTA = one query row x 8 heads.  Keys stream through shared memory in tiles of 32
 // (gathered FP4 rows -- MXFP4 or E2M1 + E4M3/16 -- dequantised exactly to float, then the
-// SWA slots), with an online
+// SWA slots, bf16 or MXFP8 (report §2.4.4 keeps the SWA KV in FP8)), with an online
 // softmax per head and fp32 accumulation.
 #include "common.cuh"
 #include "internal.h"
@@ -29,7 +29,9 @@ struct AttnParams {
     const uint16_t *q;
     const uint8_t *kvc, *kvs;
     const int32_t *idx;
-    const uint16_t *swa;
+    const uint16_t *swa;     // bf16 rows, or E4M3 bytes when swa8
+    const uint8_t *swa_scales;
+    int32_t swa8;            // SWA in MXFP8
     const int32_t *swa_pos0, *swa_start, *q_pos;
     uint16_t *out;
     float *lse;
@@ -125,7 +127,12 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_cc_kernel(AttnParams P)
                 if (code & 8u) v = -v;
             } else if (src <= -2) {
                 const int64_t slot = -src - 2;
-                v = __uint_as_float((uint32_t)P.swa[(b * P.n_swa + slot) * (int64_t)P.d_qk + c] << 16);
+                const int64_t r = b * P.n_swa + slot;
+                if (P.swa8)      // MXFP8: E4M3 value x 2^(e - 127), exact in float32
+                    v = e4m3_value(reinterpret_cast<const uint8_t *>(P.swa)[r * P.d_qk + c]) *
+                        e8m0_value(P.swa_scales[r * (P.d_qk / 32) + c / 32]);
+                else
+                    v = __uint_as_float((uint32_t)P.swa[r * (int64_t)P.d_qk + c] << 16);
             }
             s_k[j * ldk + c] = v;
         }
@@ -236,6 +243,8 @@ cudaError_t launch_sparse_attn(const csa2_attn_args &a, uint16_t *out, float *ls
     P.kvs = a.kv_scales;
     P.idx = a.idx;
     P.swa = a.swa;
+    P.swa_scales = a.swa_scales;
+    P.swa8 = a.swa_fmt == CSA2_SWA_MXFP8 ? 1 : 0;
     P.swa_pos0 = a.swa_pos0;
     P.swa_start = a.swa_start;
     P.q_pos = a.q_pos;

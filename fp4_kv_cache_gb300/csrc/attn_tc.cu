@@ -49,7 +49,9 @@ struct AttnTcParams {
     const uint16_t *q;
     const uint8_t *kvc, *kvs;
     const int32_t *idx;
-    const uint16_t *swa;
+    const uint16_t *swa;    // bf16 rows, or E4M3 bytes when swa8
+    const uint8_t *swa_scales;
+    int32_t swa8;           // SWA in MXFP8 (E4M3 + E8M0 per 32)
     const int32_t *swa_pos0, *swa_start, *q_pos;
     uint16_t *out;
     float *lse;
@@ -264,7 +266,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
         return sl < n_slots ? -(j0 + (sl - P.topk) + 2) : -1;
     };
     // Registers carry the next tile's FP4 half-row while the current tile computes; SWA rows
-    // (bf16, 4x the bytes) are pulled into L2 a tile ahead and copied with cp.async.
+    // (bf16, 4x the bytes, or MXFP8) are pulled into L2 a tile ahead, then copied with
+    // cp.async (bf16) or decoded (MXFP8).
     uint4 raw[9];
     uint32_t sb[9];          // scale byte(s) of each 32 codes: one E8M0, or two E4M3 (NV)
     auto issue = [&](int64_t src) {
@@ -283,10 +286,18 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
                 for (int i = 0; i < 9; ++i) sb[i] = scl[i];
             }
         } else if (src <= -2) {
-            const char *srow = reinterpret_cast<const char *>(P.swa + (b * P.n_swa + (-src - 2)) * (int64_t)kDqk);
+            const int64_t srw = b * P.n_swa + (-src - 2);
+            if (P.swa8) {          // MXFP8: 288 code bytes and 9 scale bytes per half row
+                const char *crow = reinterpret_cast<const char *>(P.swa) + srw * kDqk + part * 288;
 #pragma unroll
-            for (int i = 0; i < 5; ++i)
-                asm volatile("prefetch.global.L2 [%0];" ::"l"(srow + part * 576 + i * 128));
+                for (int i = 0; i < 3; ++i) asm volatile("prefetch.global.L2 [%0];" ::"l"(crow + i * 128));
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(P.swa_scales + srw * (kDqk / 32) + part * 9));
+            } else {
+                const char *srow = reinterpret_cast<const char *>(P.swa + srw * (int64_t)kDqk);
+#pragma unroll
+                for (int i = 0; i < 5; ++i)
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(srow + part * 576 + i * 128));
+            }
         }
     };
     int64_t src_cur = -1;
@@ -374,6 +385,32 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
                                 make_uint4(packed[0], packed[1], packed[2], packed[3]);
                         }
                     }
+                }
+            } else if (src <= -2 && P.swa8) {
+                // MXFP8 SWA row: 8 E4M3 codes per 16-byte piece, decoded exactly (the code's
+                // bits placed as a float's, times 2^120 to move the exponent bias from 7 to
+                // 127 -- subnormal codes included -- and times the block's 2^X)
+                const int64_t srw = b * P.n_swa + (-src - 2);
+                const uint8_t *crow = reinterpret_cast<const uint8_t *>(P.swa) + srw * kDqk;
+                const uint8_t *srow_s = P.swa_scales + srw * (kDqk / 32);
+#pragma unroll 2
+                for (int pc = part * 36; pc < part * 36 + 36; ++pc) {
+                    const int c = pc >> 3;
+                    uint8_t *base = sm + (c < 8 ? kOffK + c * kChunkBytes : kOffR);
+                    const uint2 w8 = *reinterpret_cast<const uint2 *>(crow + pc * 8);
+                    const float k2 = e8m0_value(srow_s[pc >> 2]);
+                    uint32_t packed[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const uint32_t x = k < 2 ? w8.x : w8.y, sh = 16 * (k & 1);
+                        const uint32_t b0 = x >> sh, b1 = x >> (sh + 8);
+                        const float f0 = __uint_as_float(((b0 & 0x7fu) << 20) | ((b0 & 0x80u) << 24)) * 0x1p120f * k2;
+                        const float f1 = __uint_as_float(((b1 & 0x7fu) << 20) | ((b1 & 0x80u) << 24)) * 0x1p120f * k2;
+                        const __nv_bfloat162 bb = __floats2bfloat162_rn(f0, f1);
+                        packed[k] = *reinterpret_cast<const uint32_t *>(&bb);
+                    }
+                    *reinterpret_cast<uint4 *>(base + sw128(r, pc & 7)) =
+                        make_uint4(packed[0], packed[1], packed[2], packed[3]);
                 }
             } else if (src <= -2) {
                 const uint16_t *srow = P.swa + (b * P.n_swa + (-src - 2)) * (int64_t)kDqk;
@@ -658,7 +695,8 @@ void attn_tc_split(const csa2_attn_args &a, int &splits, int &tiles_per_split)
 bool attn_tc_eligible(const csa2_attn_args &a)
 {
     return a.d_qk == kDqk && a.d_v == kDv && a.n_heads <= kH && ((uintptr_t)a.q & 15) == 0 &&
-           (!a.swa || ((uintptr_t)a.swa & 15) == 0) && ((uintptr_t)a.kv_codes & 15) == 0 &&
+           (!a.swa || ((uintptr_t)a.swa & (a.swa_fmt == CSA2_SWA_MXFP8 ? 7 : 15)) == 0) &&
+           ((uintptr_t)a.kv_codes & 15) == 0 &&
            (a.kv_fmt != CSA2_FMT_NVFP4_E4M3_16 || ((uintptr_t)a.kv_scales & 1) == 0);
 }
 
@@ -686,6 +724,8 @@ cudaError_t launch_attn_tc(const csa2_attn_args &a, uint16_t *out, float *lse, v
     P.kvs = a.kv_scales;
     P.idx = a.idx;
     P.swa = a.swa;
+    P.swa_scales = a.swa_scales;
+    P.swa8 = a.swa_fmt == CSA2_SWA_MXFP8 ? 1 : 0;
     P.swa_pos0 = a.swa_pos0;
     P.swa_start = a.swa_start;
     P.q_pos = a.q_pos;

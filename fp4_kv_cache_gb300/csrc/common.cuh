@@ -112,6 +112,26 @@ __device__ __forceinline__ uint32_t e4m3_block_scale(float amax)
     return (uint32_t)(d & 0xffu);
 }
 
+// ------------------------------------------------------------------ MXFP8 (E4M3) SWA
+// (report §2.4.4: the SWA KV cache stays in FP8; OCP MX with E4M3 elements.)
+// Shared exponent X of a 32-value block with maximum magnitude amax (finite, >= 0):
+// floor(log2 amax) - 8 clamped to [-127, 127]; 0 for an all-zero block.
+__device__ __forceinline__ int mx8_block_exponent(float amax)
+{
+    if (!(amax > 0.0f)) return 0;
+    const int x = floor_log2_f32(amax) - 8;
+    return x < -127 ? -127 : (x > 127 ? 127 : x);
+}
+
+// E4M3 code of an already scaled value by the hardware conversion: round to nearest, ties
+// to even, saturating at +-448, sign kept (also for results that round to zero).
+__device__ __forceinline__ uint32_t e4m3_cvt(float v)
+{
+    uint16_t d;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %1;" : "=h"(d) : "f"(v));
+    return (uint32_t)(d & 0xffu);
+}
+
 // Twice the signed E2M1 value of a code, an integer in [-12, 12].
 __device__ __forceinline__ int e2m1_twice(uint32_t c)
 {

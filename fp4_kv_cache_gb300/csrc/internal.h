@@ -42,6 +42,11 @@ struct RopeQuantJobDesc {
     bool nvfp4;
 };
 cudaError_t launch_rope_quant(const RopeQuantJobDesc *jobs, int n_jobs, uint32_t *d_status, cudaStream_t s);
+cudaError_t launch_quant_mxfp8(const void *x, bool x_bf16, int64_t rows, int64_t cols, int64_t ldx,
+                               uint8_t *codes, int64_t ldc, uint8_t *scales, int64_t lds,
+                               uint32_t *d_status, cudaStream_t s);
+cudaError_t launch_dequant_mxfp8(const uint8_t *codes, int64_t ldc, const uint8_t *scales, int64_t lds,
+                                 int64_t rows, int64_t cols, void *y, bool y_bf16, int64_t ldy, cudaStream_t s);
 cudaError_t launch_dequant_fp4(const uint8_t *codes, int64_t ldc, const uint8_t *scales,
                                int64_t lds, int64_t rows, int64_t cols, bool nvfp4, void *y,
                                bool y_bf16, int64_t ldy, cudaStream_t s);

@@ -311,6 +311,57 @@ __global__ void __launch_bounds__(256) dequant_fp4_kernel(const uint8_t *__restr
     }
 }
 
+// ---------------------------------------------------------------- MXFP8 (E4M3) SWA codec
+// One warp per 32-value block: the block maximum by a warp reduction, X = floor(log2 amax)
+// - 8, each lane's value times 2^-X (exact: a power of two, and any product below 2^-126
+// lies far below the first E4M3 rounding boundary 2^-10) converted by the hardware.
+template <bool BF16>
+__global__ void __launch_bounds__(256) quant_mxfp8_kernel(const void *__restrict__ x, int64_t rows,
+                                                          int64_t cols, int64_t ldx,
+                                                          uint8_t *__restrict__ codes, int64_t ldc,
+                                                          uint8_t *__restrict__ scales, int64_t lds,
+                                                          uint32_t *d_status)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t nblk_row = cols / 32;
+    const int64_t total = rows * nblk_row;
+    const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    pdl_wait();
+    pdl_allow_dependents();
+    for (int64_t blk = warp0; blk < total; blk += nwarps) {
+        const int64_t r = blk / nblk_row, kb = blk % nblk_row;
+        const int64_t col = kb * 32 + lane;
+        float v;
+        if (BF16) v = __uint_as_float((uint32_t)static_cast<const uint16_t *>(x)[r * ldx + col] << 16);
+        else v = static_cast<const float *>(x)[r * ldx + col];
+        const uint32_t amax_bits = __reduce_max_sync(0xffffffffu, __float_as_uint(v) & 0x7fffffffu);
+        if (amax_bits >= 0x7f800000u && lane == 0) dev_flag(d_status, CSA2_DEV_NONFINITE);
+        const int X = mx8_block_exponent(__uint_as_float(amax_bits >= 0x7f800000u ? 0u : amax_bits));
+        codes[r * ldc + col] = (uint8_t)e4m3_cvt(v * pow2_neg(X));
+        if (lane == 0) scales[r * lds + kb] = (uint8_t)(X + 127);
+    }
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(256) dequant_mxfp8_kernel(const uint8_t *__restrict__ codes, int64_t ldc,
+                                                            const uint8_t *__restrict__ scales, int64_t lds,
+                                                            int64_t rows, int64_t cols, void *__restrict__ y,
+                                                            int64_t ldy)
+{
+    const int64_t total = rows * cols;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = i / cols, c = i % cols;
+        // E4M3 value (at most 4 significant bits) x 2^(e - 127): exact in float32
+        const float v = e4m3_value(codes[r * ldc + c]) * e8m0_value(scales[r * lds + c / 32]);
+        if (BF16)
+            static_cast<uint16_t *>(y)[r * ldy + c] = (uint16_t)(__float_as_uint(v) >> 16);
+        else
+            static_cast<float *>(y)[r * ldy + c] = v;
+    }
+}
+
 // ---------------------------------------------------------------- RoPE + quantise
 // The cache write of report §2.4.4 (quantise after RoPE, one format for both parts): every
 // lane takes 8 values of one block (one 16-byte bf16 load), rotates the pairs that fall in
@@ -544,6 +595,29 @@ cudaError_t launch_rope_quant(const RopeQuantJobDesc *jobs, int n_jobs, uint32_t
     B.n = n;
     for (int k = n; k < 4; ++k) B.lanes_end[k] = acc;
     return launch_pdl(rope_quant_kernel, dim3(grid_for(acc, 256)), dim3(256), 0, s, 1, B, d_status);
+}
+
+cudaError_t launch_quant_mxfp8(const void *x, bool x_bf16, int64_t rows, int64_t cols, int64_t ldx,
+                               uint8_t *codes, int64_t ldc, uint8_t *scales, int64_t lds,
+                               uint32_t *d_status, cudaStream_t s)
+{
+    if (rows == 0 || cols == 0) return cudaSuccess;
+    const int grid = grid_for(rows * (cols / 32), 8);
+    if (x_bf16)
+        return launch_pdl(quant_mxfp8_kernel<true>, dim3(grid), dim3(256), 0, s, 1, x, rows, cols, ldx, codes,
+                          ldc, scales, lds, d_status);
+    return launch_pdl(quant_mxfp8_kernel<false>, dim3(grid), dim3(256), 0, s, 1, x, rows, cols, ldx, codes, ldc,
+                      scales, lds, d_status);
+}
+
+cudaError_t launch_dequant_mxfp8(const uint8_t *codes, int64_t ldc, const uint8_t *scales, int64_t lds,
+                                 int64_t rows, int64_t cols, void *y, bool y_bf16, int64_t ldy, cudaStream_t s)
+{
+    if (rows == 0 || cols == 0) return cudaSuccess;
+    const int grid = grid_for(rows * cols, 256);
+    if (y_bf16) dequant_mxfp8_kernel<true><<<grid, 256, 0, s>>>(codes, ldc, scales, lds, rows, cols, y, ldy);
+    else dequant_mxfp8_kernel<false><<<grid, 256, 0, s>>>(codes, ldc, scales, lds, rows, cols, y, ldy);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_dequant_fp4(const uint8_t *codes, int64_t ldc, const uint8_t *scales,

@@ -33,10 +33,11 @@ class DeviceWorkload:
 
 def build(w: synth.Workload, rows=None, device="cuda:0", kv: bool = True, kidx: bool = True,
           d_status: Optional[torch.Tensor] = None, kv_fmt: int = csa2.FMT_MXFP4,
-          also_nvfp4: bool = False) -> DeviceWorkload:
+          also_nvfp4: bool = False, swa_fp8: bool = False) -> DeviceWorkload:
     """kv_fmt: main-KV cache format (MXFP4, or E2M1 + E4M3/16 as the report stores it);
     the indexer keys are MXFP4 either way.  also_nvfp4: quantise the same main-KV rows a
-    second time into E2M1 + E4M3/16 ("kv_codes_nv", "kv_scales_nv")."""
+    second time into E2M1 + E4M3/16 ("kv_codes_nv", "kv_scales_nv").  swa_fp8: also the SWA
+    rows in MXFP8 ("swa8" codes, "swa8_scales"), the report's FP8 SWA cache."""
     rows = list(range(w.batch)) if rows is None else list(rows)
     B = len(rows)
     dev = torch.device(device)
@@ -73,6 +74,8 @@ def build(w: synth.Workload, rows=None, device="cuda:0", kv: bool = True, kidx: 
             del x
             swa[i] = bf16_tensor(synth.gen_swa(w, b), dev)
         out.t["kv_codes"], out.t["kv_scales"], out.t["swa"] = vc, vs, swa
+        if swa_fp8:
+            out.t["swa8"], out.t["swa8_scales"] = csa2.quant_fp8(swa, d_status)
     if w.pool_blocks:
         out.t["pool"] = torch.from_numpy(np.stack([synth.gen_pool_blocks(w, b) for b in rows])).to(dev)
     if w.reuse_idx:

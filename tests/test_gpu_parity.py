@@ -122,6 +122,34 @@ def test_quant_dequant_nvfp4_parity(cols, as_bf16):
     assert np.array_equal(c_u.cpu().numpy(), c_ref) and np.array_equal(s_u.cpu().numpy(), s_ref)
 
 
+@pytest.mark.parametrize("cols,as_bf16", [(576, True), (64, False), (32, True)])
+def test_quant_dequant_mxfp8_parity(cols, as_bf16):
+    # MXFP8 SWA codec (report §2.4.4 keeps the SWA cache in FP8): codes and scale bytes
+    # bit-exact, every dequantised value exact in float32 and bf16 (moderate scales)
+    raw, x = _codec_inputs(2001, cols, 300 + cols + as_bf16, as_bf16)
+    xt = workload.bf16_tensor(raw, DEV) if as_bf16 else torch.from_numpy(raw).to(DEV)
+    st = status()
+    codes, scales = csa2.quant_fp8(xt, st)
+    c_ref, s_ref = oracle.quant_mxfp8(x)
+    assert np.array_equal(scales.cpu().numpy(), s_ref)
+    assert np.array_equal(codes.cpu().numpy(), c_ref)
+    assert int(st.item()) == 0
+    y_ref = oracle.dequant_mxfp8(c_ref, s_ref).astype(np.float32)
+    y32 = csa2.dequant_fp8(codes, scales, torch.float32).cpu().numpy()
+    assert np.array_equal(y32.view(np.uint32), y_ref.view(np.uint32))
+    ok = (s_ref >= 127 - 100) & (s_ref <= 127 + 100)                # bf16-normal products
+    rows_ok = ok.all(axis=1)
+    y16 = csa2.dequant_fp8(codes, scales, torch.bfloat16).view(torch.int16).cpu().numpy()
+    assert np.array_equal(y16.view(np.uint16)[rows_ok],
+                          (y_ref.view(np.uint32) >> 16).astype(np.uint16)[rows_ok])
+    x[3] = np.float32(np.inf)
+    bad = torch.from_numpy(np.ascontiguousarray(x[:8], np.float32)).to(DEV)
+    st2 = status()
+    csa2.quant_fp8(bad, st2)
+    torch.cuda.synchronize()
+    assert int(st2.item()) & csa2.DEV_NONFINITE
+
+
 def test_nvfp4_scale_rounding_boundaries():
     # block maxima at, and one float32 step either side of, 6 x every E4M3 rounding midpoint,
     # plus the zero-scale and clamp edges: the GPU's scale bytes and codes match the oracle's
@@ -556,8 +584,9 @@ def _attn_check(o_gpu, lse_gpu, o_ref, lse_ref):
     return err.max()
 
 
-def _oracle_attention(w, dw_rows, idx_np, t_range, swa_start=None, kv_fmt="mxfp4"):
-    """fp64 oracle attention for rows (b, t) with the given idx."""
+def _oracle_attention(w, dw_rows, idx_np, t_range, swa_start=None, kv_fmt="mxfp4", swa8=False):
+    """fp64 oracle attention for rows (b, t) with the given idx (swa8: the SWA rows as their
+    MXFP8 values)."""
     qpos = synth.q_positions(w)
     n_slots, pos0 = synth.swa_layout(w)
     _, _, qa = synth.gen_queries(w)
@@ -565,6 +594,8 @@ def _oracle_attention(w, dw_rows, idx_np, t_range, swa_start=None, kv_fmt="mxfp4
     for b in dw_rows:
         kvc, kvs = oracle.quant_main_kv(f32(synth.gen_main_kv(w, b)), kv_fmt)
         swa = f32(synth.gen_swa(w, b)).astype(np.float64)
+        if swa8:
+            swa = oracle.dequant_mxfp8(*oracle.quant_mxfp8(swa))
         s0 = 0 if swa_start is None else int(swa_start[b])
         for t in t_range:
             keys = oracle.gather_keys(idx_np[b, t], kvc, kvs, swa, int(qpos[b, t]), pos0, w.window, s0)
@@ -582,28 +613,33 @@ ATTN_CASES = {
 }
 
 
-@pytest.mark.parametrize("name,kv_fmt", [(n, "mxfp4") for n in ATTN_CASES] +
-                         [("prod_dims_T3", "nvfp4"), ("replay_start", "nvfp4"), ("tiny", "nvfp4"),
-                          ("d_v_odd_heads", "nvfp4")])
-def test_attention_parity(name, kv_fmt):
+@pytest.mark.parametrize("name,kv_fmt,swa8", [(n, "mxfp4", False) for n in ATTN_CASES] +
+                         [("prod_dims_T3", "nvfp4", False), ("replay_start", "nvfp4", False),
+                          ("tiny", "nvfp4", False), ("d_v_odd_heads", "nvfp4", False),
+                          ("prod_dims_T3", "nvfp4", True), ("replay_start", "mxfp4", True),
+                          ("tiny", "mxfp4", True), ("d_v_odd_heads", "nvfp4", True)])
+def test_attention_parity(name, kv_fmt, swa8):
     # kv_fmt "nvfp4": the main KV in the report's E2M1 + E4M3/16 format (tensor-core kernel
-    # for the production dims, CUDA-core kernel for the others)
+    # for the production dims, CUDA-core kernel for the others); swa8: the SWA window in
+    # MXFP8, the report's FP8 SWA cache (with nvfp4: the pages' whole cache configuration)
     w, swa_start = ATTN_CASES[name]
     st = status()
     fmt = csa2.FMT_NVFP4_E4M3_16 if kv_fmt == "nvfp4" else csa2.FMT_MXFP4
-    dw = workload.build(w, kidx=False, device=DEV, d_status=st, kv_fmt=fmt)
+    dw = workload.build(w, kidx=False, device=DEV, d_status=st, kv_fmt=fmt, swa_fp8=swa8)
     rng = np.random.default_rng(3)
     idx = np.stack([np.stack([np.sort(rng.choice(w.n_keys, w.topk, replace=False)) for _ in range(w.n_q)])
                     for _ in range(w.batch)]).astype(np.int32)
     idx[0, 0, -7:] = -1                                  # padding
     idx[-1, -1, :3] = idx[-1, -1, 3]                     # duplicates are kept
     ss = None if swa_start is None else torch.tensor(swa_start, dtype=torch.int32, device=DEV)
+    swa = dw["swa8"] if swa8 else dw["swa"]
     out, lse = csa2.sparse_attn(dw["q_attn"], dw["kv_codes"], dw["kv_scales"],
-                                torch.from_numpy(idx).to(DEV), dw["swa"], dw["swa_pos0"], dw["q_pos"],
-                                ss, w.window, dw.sm_scale, w.d_v, d_status=st)
+                                torch.from_numpy(idx).to(DEV), swa, dw["swa_pos0"], dw["q_pos"],
+                                ss, w.window, dw.sm_scale, w.d_v, d_status=st,
+                                swa_scales=dw["swa8_scales"] if swa8 else None)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
-    o_ref, l_ref = _oracle_attention(w, range(w.batch), idx, range(w.n_q), swa_start, kv_fmt)
+    o_ref, l_ref = _oracle_attention(w, range(w.batch), idx, range(w.n_q), swa_start, kv_fmt, swa8)
     for (b, t), o in o_ref.items():
         _attn_check(out[b, t].float().cpu().numpy(), lse[b, t].cpu().numpy(), o, l_ref[(b, t)])
 

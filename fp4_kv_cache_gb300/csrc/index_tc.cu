@@ -441,19 +441,20 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
                     tc::mbar_arrive_expect_tx(&S.full[s], kSpan * kRowBytes + (sf_bulk ? kSpan * 4 : 0));
                     tc::tma_load_2d(S.a[s], &tmap, &S.full[s], 0, (int32_t)(kbase + t0));
                     if (sf_bulk) tc::bulk_load(S.sfa[s], ks_run, kSpan * 4, &S.full[s]);
-                } else {
-                    uint32_t bytes = 0;
-                    for (int j = 0; j < kSpan / 8; ++j)
-                        if (t0 + 8 * j < c1 && pool[(t0 >> 3) + j] >= 0) bytes += 8 * kRowBytes;
-                    tc::mbar_arrive_expect_tx(&S.full[s], bytes);
-                    for (int j = 0; j < kSpan / 8; ++j) {
-                        if (t0 + 8 * j >= c1) break;
-                        int64_t id = pool[(t0 >> 3) + j];
-                        if (id < 0) continue;
-                        id = id >= n_blk_all ? n_blk_all - 1 : id;
-                        tc::tma_load_2d(S.a[s] + j * 8 * kRowBytes, &tmap, &S.full[s], 0,
-                                        (int32_t)(kbase + id * 8));
-                    }
+                }
+            }
+            // pool mode: lane j reads the stage's block id j (all at once) and loads that
+            // block's 8 code rows with one TMA box
+            int64_t blk_id = -1;
+            if (P.pool_mode) {
+                static_assert(QG != 1 || kSpanOf<1> / 8 == 32, "one pool block per lane");
+                if (lane < kSpan / 8 && t0 + 8 * lane < c1) blk_id = pool[(t0 >> 3) + lane];
+                const uint32_t have = __ballot_sync(0xffffffffu, blk_id >= 0);
+                if (lane == 0) tc::mbar_arrive_expect_tx(&S.full[s], (uint32_t)__popc(have) * 8u * kRowBytes);
+                __syncwarp();
+                if (blk_id >= 0) {
+                    const int64_t id = blk_id >= n_blk_all ? n_blk_all - 1 : blk_id;
+                    tc::tma_load_2d(S.a[s] + lane * 8 * kRowBytes, &tmap, &S.full[s], 0, (int32_t)(kbase + id * 8));
                 }
             }
             // scale atom of block mb: word lane * 4 + j holds position mb * 128 + lane + 32 j
@@ -463,10 +464,11 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
                 const int m = lane + 32 * j;
                 const int64_t cand = t0 + m;
                 uint32_t *dst = &S.sfa[s][(j >> 2) * kTile + lane * 4 + (j & 3)];
+                const int64_t bid = P.pool_mode ? __shfl_sync(0xffffffffu, blk_id, (m >> 3) & 31) : 0;
                 if (cand < c1) {
                     int64_t pos = cand;
                     if (P.pool_mode) {
-                        int64_t id = pool[cand >> 3];
+                        int64_t id = bid;           // lane m / 8 read it above
                         id = id < 0 ? 0 : (id >= n_blk_all ? n_blk_all - 1 : id);
                         pos = id * 8 + (cand & 7);
                         if (pos >= P.n_keys) pos = P.n_keys - 1;

@@ -15,11 +15,15 @@
 // maxima and sums are reduced across the 128 threads with a halving shuffle reduction.
 // The softmax runs in base 2: logits are scaled by sm_scale * log2(e), so every exponential
 // is one exp2f, and lse = (m + log2 l) ln 2.
-// A CTA covers a contiguous span of tiles of one query row with an online softmax; when
-// a row is split over several CTAs, they form one thread-block cluster: (m, l) go
-// through distributed shared memory, O partials through L2, and each CTA merges a
-// quarter-slice of the output dims.  Each thread holds the next tile's FP4 half-row in
-// registers while the current tile is multiplied, so the gather latency overlaps the MMAs.
+// A CTA covers its share of one query row's SWA window and a contiguous span of the row's
+// index tiles with an online softmax.  The SWA share comes first and runs before the wait
+// for the kernel that writes the index entries (Top-K), so only the index tiles remain
+// once those arrive.  When a row is split over several CTAs (one index tile each while
+// the rows' tiles fit one wave), they form one thread-block cluster: (m, l) go through
+// distributed shared memory, O partials through L2 (bulk-copied into the merging CTA's
+// shared memory), and each CTA merges a quarter-slice of the output dims.  A tile is
+// staged with coalesced reads (consecutive threads, consecutive 8-value pieces of a row);
+// the next tile's rows are prefetched into L2 while the current one computes.
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -40,9 +44,12 @@ constexpr int kQChunkBytes = kH * 128;            // 8 KB: 64 heads x 64 bf16
 constexpr uint32_t kTmemCols = 512;   // S^T [0,64), O^T block m at [64 + 64m, 128 + 64m)
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kMaxSplits = 7;          // CTAs (one cluster) per split row
+constexpr int kPieces = kKeys * (kDqk / 8) / kThreads;   // 36 pieces of 8 values per thread and tile
+static_assert(kKeys * (kDqk / 8) == kPieces * kThreads, "pieces do not divide evenly");
 
 struct AttnTcParams {
     int32_t T, H, topk, window, n_swa, splits, tiles_per_split;
+    int32_t n_itiles;       // tiles of index slots (128 each); SWA tiles are numbered after them
     float log2_scale;       // logit scale x log2(e): the softmax runs in base 2
     float *part_o;          // split rows: [rows, splits, 4 blocks, H, 128] raw O^T partials
     int64_t n_kv;
@@ -63,6 +70,9 @@ constexpr int kOffK = 0;
 constexpr int kOffR = 8 * kChunkBytes;                    // 131072
 constexpr int kOffQ = kOffR + kChunkBytes;                // 147456
 constexpr int kSmemBytes = kOffQ + kChunks * kQChunkBytes; // 221184
+// the merge's bulk copies (at most 6 peer blocks of 64 heads x 128 dims, float) reuse it
+static_assert(6 * kH * kKeys * 4 <= kSmemBytes, "merge staging does not fit");
+static_assert(kMaxSplits <= 7, "merge staging holds at most 6 peer blocks");
 
 __device__ __forceinline__ int sw128(int row, int piece)   // byte offset of 16-byte piece
 {
@@ -190,6 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
     __shared__ int s_abort;
     __shared__ float s_mlx[kMaxSplits][2][kH];   // split row: every rank's (m, l) per head
     __shared__ float s_fac[kMaxSplits][kH];      // split row: e^(m_s - M)
+    __shared__ int64_t s_src[kKeys];             // the tile's source rows (see slot_src)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t row = blockIdx.y;
@@ -198,12 +209,11 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
     const int H = P.H;
     const int quad = warp & 3, hh0 = 32 * (warp >> 2);   // TMEM lane quadrant, first head
     const int key_row = 32 * quad + lane;                 // this thread's key / dim row
-    const int part = tid >> 7;                            // which half of the key row it gathers
     const int t_begin = split * P.tiles_per_split;
-    // index entry of slot `key_row` of a tile (idx slots come first; 0 past them)
+    // index entry of slot `key_row` of an index tile (0 past the entries and for SWA tiles)
     auto slot_id = [&](int tile) -> int32_t {
         const int64_t sl = (int64_t)tile * kKeys + key_row;
-        return sl < P.topk ? P.idx[row * P.topk + sl] : 0;
+        return tile < P.n_itiles && sl < P.topk ? P.idx[row * P.topk + sl] : 0;
     };
     if (tid == 0) {
         tc::mbar_init(&s_bar, 1);
@@ -240,202 +250,223 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
         j1 = j1 > P.n_swa - 1 ? P.n_swa - 1 : j1;
         n_sw = j1 >= j0 ? j1 - j0 + 1 : 0;
     }
-    const int64_t n_slots = P.topk + n_sw;
-    const int n_tiles = (int)((n_slots + kKeys - 1) / kKeys);
-    const int t_end = min(t_begin + P.tiles_per_split, n_tiles);
-    pdl_wait();
-    pdl_allow_dependents();
-    // the first two tiles' index entries are read first, so their latency overlaps the
-    // set-up below
-    const int32_t id_first = slot_id(t_begin);
-    int32_t id_next = slot_id(t_begin + 1);
+    // This CTA's tiles, in order: its share of the SWA window -- slots [sw_lo, sw_hi), an
+    // equal part for each of the row's CTAs -- which needs nothing from the kernel before, so
+    // it runs before the dependency wait (while Top-K still works, and with every CTA's code
+    // path warmed up by the time the index entries arrive), then its index tiles
+    // [t_begin, t_begin + tiles_per_split).
+    const int64_t sw_share = (n_sw + P.splits - 1) / P.splits;
+    const int64_t sw_lo = split * sw_share < n_sw ? split * sw_share : n_sw;
+    const int64_t sw_hi = sw_lo + sw_share < n_sw ? sw_lo + sw_share : n_sw;
+    const int n_sw_t = (int)((sw_hi - sw_lo + kKeys - 1) / kKeys);
+    const int n_it = max(0, min(t_begin + P.tiles_per_split, P.n_itiles) - t_begin);
+    const int n_v = n_sw_t + n_it;
+    auto gtile = [&](int v) -> int { return v < n_sw_t ? P.n_itiles + v : t_begin + (v - n_sw_t); };
+    bool waited = false;
+    auto wait_prev = [&]() {
+        if (!waited) {
+            pdl_wait();
+            pdl_allow_dependents();
+            waited = true;
+        }
+    };
     __syncthreads();
     const uint32_t tmem = s_tmem;
     uint32_t phase = 0;
     bool any_o = false;
 
-    // Key slot `key_row` of a tile: idx entries first, then the SWA window.  Returns the
-    // main-KV row (>= 0), -(SWA slot + 2), or -1 for an empty slot.
+    // Key slot `key_row` of a tile: an index tile's entry, or an SWA tile's slot of the
+    // window.  Returns the main-KV row (>= 0), -(SWA slot + 2), or -1 for an empty slot.
     auto slot_src = [&](int tile, int32_t id) -> int64_t {
-        const int64_t sl = (int64_t)tile * kKeys + key_row;
-        if (sl < P.topk) {
+        if (tile < P.n_itiles) {
+            const int64_t sl = (int64_t)tile * kKeys + key_row;
+            if (sl >= P.topk) return -1;
             if (id >= 0 && id < P.n_kv) return id;
             if (id != -1) dev_flag(P.d_status, CSA2_DEV_BAD_INDEX);
             return -1;
         }
-        return sl < n_slots ? -(j0 + (sl - P.topk) + 2) : -1;
+        const int64_t sl = sw_lo + (int64_t)(tile - P.n_itiles) * kKeys + key_row;
+        return sl < sw_hi ? -(j0 + sl + 2) : -1;
     };
-    // Registers carry the next tile's FP4 half-row while the current tile computes; SWA rows
-    // (bf16, 4x the bytes, or MXFP8) are pulled into L2 a tile ahead, then copied with
-    // cp.async (bf16) or decoded (MXFP8).
-    uint4 raw[9];
-    uint32_t sb[9];          // scale byte(s) of each 32 codes: one E8M0, or two E4M3 (NV)
-    auto issue = [&](int64_t src) {
-        if (src >= 0) {
-            const uint8_t *codes = P.kvc + (b * P.n_kv + src) * (kDqk / 2) + part * 9 * 16;
+    // Staging: thread t < 128 resolves key slot t of the tile to its source row (s_src).
+    // Main-KV tiles then go to the threads as 32-value blocks (16 code bytes, one scale)
+    // bi = t + 256 k, k < 9: consecutive threads take consecutive blocks of a row, so a
+    // warp's reads cover one or two rows' contiguous bytes.  Each block decodes to four
+    // 16-byte pieces of one chunk row; a thread writes them starting at piece (chunk & 3),
+    // so the eight threads of a store phase (four chunks, two blocks each) hit eight
+    // different bank groups.  SWA tiles go by 8-value pieces p = t + 256 k, k < 36.  The
+    // next tile's rows are prefetched into L2 while the current one computes.
+    const int64_t kv_row0 = b * P.n_kv, swa_row0 = b * P.n_swa;
+    auto piece_dst = [&](int r, int q) -> uint8_t * {
+        const int c = q >> 3;
+        return sm + (c < 8 ? kOffK + c * kChunkBytes : kOffR) + sw128(r, q & 7);
+    };
+    auto stage_fp4 = [&]() {
+        constexpr int kBlocks = kKeys * (kDqk / 32) / kThreads;      // 9 blocks per thread
+        uint4 cw[kBlocks];
+        uint32_t sc[kBlocks], ok = 0;
 #pragma unroll
-            for (int i = 0; i < 9; ++i) raw[i] = *reinterpret_cast<const uint4 *>(codes + i * 16);
-            if constexpr (NV) {
-                const uint16_t *scl = reinterpret_cast<const uint16_t *>(P.kvs + (b * P.n_kv + src) * (kDqk / 16) +
-                                                                         part * 18);
-#pragma unroll
-                for (int i = 0; i < 9; ++i) sb[i] = scl[i];
-            } else {
-                const uint8_t *scl = P.kvs + (b * P.n_kv + src) * (kDqk / 32) + part * 9;
-#pragma unroll
-                for (int i = 0; i < 9; ++i) sb[i] = scl[i];
-            }
-        } else if (src <= -2) {
-            const int64_t srw = b * P.n_swa + (-src - 2);
-            if (P.swa8) {          // MXFP8: 288 code bytes and 9 scale bytes per half row
-                const char *crow = reinterpret_cast<const char *>(P.swa) + srw * kDqk + part * 288;
-#pragma unroll
-                for (int i = 0; i < 3; ++i) asm volatile("prefetch.global.L2 [%0];" ::"l"(crow + i * 128));
-                asm volatile("prefetch.global.L2 [%0];" ::"l"(P.swa_scales + srw * (kDqk / 32) + part * 9));
-            } else {
-                const char *srow = reinterpret_cast<const char *>(P.swa + srw * (int64_t)kDqk);
-#pragma unroll
-                for (int i = 0; i < 5; ++i)
-                    asm volatile("prefetch.global.L2 [%0];" ::"l"(srow + part * 576 + i * 128));
+        for (int k = 0; k < kBlocks; ++k) {
+            const int bi = tid + kThreads * k, r = bi / 18, blk = bi - 18 * r;
+            const int64_t src = s_src[r];
+            cw[k] = make_uint4(0u, 0u, 0u, 0u);
+            sc[k] = 0u;
+            if (src >= 0) {
+                const int64_t g = kv_row0 + src;
+                cw[k] = *reinterpret_cast<const uint4 *>(P.kvc + g * (kDqk / 2) + blk * 16);
+                sc[k] = NV ? *reinterpret_cast<const uint16_t *>(P.kvs + g * (kDqk / 16) + blk * 2)
+                           : P.kvs[g * (kDqk / 32) + blk];
+                ok |= 1u << k;
             }
         }
-    };
-    int64_t src_cur = -1;
-    if (t_begin < t_end) {
-        src_cur = slot_src(t_begin, id_first);
-        issue(src_cur);
-    }
-    for (int tile = t_begin; tile < t_end; ++tile) {
-        // ---- dequantise the staged half-row into the key chunks (threads r and r+128 take
-        //      the two halves of key row r)
-        {
-            const int r = key_row;
-            const int64_t src = src_cur;
-            if (NV && src >= 0) {
-                // code value x E4M3 scale in bf16: exact (at most 6 significant bits, every
-                // product in [2^-10, 2688])
-#pragma unroll
-                for (int i = 0; i < 9; ++i) {
-                    const int blk = part * 9 + i;                 // 32-value block of the row
-                    const uint32_t w4[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
-                    const int c = blk >> 1;
-                    uint8_t *base = sm + (c < 8 ? kOffK + c * kChunkBytes : kOffR);
-                    const unsigned short s_lo = (unsigned short)(__float_as_uint(e4m3_value(sb[i] & 0xffu)) >> 16);
-                    const unsigned short s_hi = (unsigned short)(__float_as_uint(e4m3_value(sb[i] >> 8)) >> 16);
-#pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {             // 8 values -> one 16-byte piece
-                        const unsigned short sbits = q4 < 2 ? s_lo : s_hi;
-                        const __nv_bfloat162 sc2 =
-                            __halves2bfloat162(__ushort_as_bfloat16(sbits), __ushort_as_bfloat16(sbits));
-                        uint32_t packed[4];
-                        e2m1x8_to_bf16(w4[q4], sc2, packed);
-                        *reinterpret_cast<uint4 *>(base + sw128(r, (blk & 1) * 4 + q4)) =
-                            make_uint4(packed[0], packed[1], packed[2], packed[3]);
-                    }
-                }
-            } else if (src >= 0) {
-                bool fast = true;
-#pragma unroll
-                for (int i = 0; i < 9; ++i) fast = fast && sb[i] >= 8u && sb[i] <= 250u;
-                if (fast) {
-                    // code value x 2^(e-127) in bf16: exact, every product stays normal
-#pragma unroll
-                    for (int i = 0; i < 9; ++i) {
-                        const int blk = part * 9 + i;             // 32-value block of the row
-                        const uint32_t w4[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
-                        const int c = blk >> 1;
-                        uint8_t *base = sm + (c < 8 ? kOffK + c * kChunkBytes : kOffR);
-                        const __nv_bfloat162 sc2 = __halves2bfloat162(
-                            __ushort_as_bfloat16((unsigned short)(sb[i] << 7)),
-                            __ushort_as_bfloat16((unsigned short)(sb[i] << 7)));
-#pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) {         // 8 values -> one 16-byte piece
-                            uint32_t packed[4];
-                            e2m1x8_to_bf16(w4[q4], sc2, packed);
-                            *reinterpret_cast<uint4 *>(base + sw128(r, (blk & 1) * 4 + q4)) =
-                                make_uint4(packed[0], packed[1], packed[2], packed[3]);
-                        }
-                    }
-                } else {
-                    // a scale outside [2^-119, 2^123] (rare): exact float products, one block
-                    // at a time with the codes read again, so this path stays small
-                    const uint8_t *codes = P.kvc + (b * P.n_kv + src) * (kDqk / 2) + part * 9 * 16;
-                    const uint8_t *scl = P.kvs + (b * P.n_kv + src) * (kDqk / 32) + part * 9;
+        // decode block by block in a rolled loop (the block in hand is always cw[0]: the
+        // arrays shift down one place per block), so the code stays small -- it runs once
+        // per tile, and unrolled it costs more in instruction fetch than in execution
+        uint32_t slow = 0;
 #pragma unroll 1
-                    for (int i = 0; i < 9; ++i) {
-                        const int blk = part * 9 + i;
-                        const uint4 rw = *reinterpret_cast<const uint4 *>(codes + i * 16);
-                        const uint32_t w4[4] = {rw.x, rw.y, rw.z, rw.w};
-                        const int c = blk >> 1;
-                        uint8_t *base = sm + (c < 8 ? kOffK + c * kChunkBytes : kOffR);
-                        const float sc = e8m0_value(scl[i]);
+        for (int k = 0; k < kBlocks; ++k) {
+            const int bi = tid + kThreads * k, r = bi / 18, blk = bi - 18 * r, c = blk >> 1;
+            uint8_t *base = sm + (c < 8 ? kOffK + c * kChunkBytes : kOffR);
+            // code value x scale in bf16 is exact: an E4M3 scale has 4 significant bits and a
+            // code 2, with every product normal; an E8M0 scale in [2^-119, 2^123] keeps every
+            // product normal.  Other E8M0 scales (rare) take the exact float path below.
+            const bool have = (ok >> k) & 1u;
+            const bool use = have && (NV || (sc[0] >= 8u && sc[0] <= 250u));
+            if (have && !use) slow |= 1u << k;
+            const unsigned short s_lo = NV ? (unsigned short)(__float_as_uint(e4m3_value(sc[0] & 0xffu)) >> 16)
+                                           : (unsigned short)(sc[0] << 7);
+            const unsigned short s_hi = NV ? (unsigned short)(__float_as_uint(e4m3_value(sc[0] >> 8)) >> 16) : s_lo;
 #pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) {
-                            uint32_t packed[4];
+            for (int j = 0; j < 4; ++j) {
+                const int w = (j + c) & 3;
+                const uint32_t word = w == 0 ? cw[0].x : w == 1 ? cw[0].y : w == 2 ? cw[0].z : cw[0].w;
+                const unsigned short sbits = w < 2 ? s_lo : s_hi;
+                uint32_t o[4] = {0u, 0u, 0u, 0u};
+                if (use) {
+                    const __nv_bfloat162 sc2 =
+                        __halves2bfloat162(__ushort_as_bfloat16(sbits), __ushort_as_bfloat16(sbits));
+                    e2m1x8_to_bf16(word, sc2, o);
+                }
+                *reinterpret_cast<uint4 *>(base + sw128(r, (blk & 1) * 4 + w)) = make_uint4(o[0], o[1], o[2], o[3]);
+            }
 #pragma unroll
-                            for (int k = 0; k < 4; ++k) {
-                                const uint32_t byte = (w4[q4] >> (8 * k)) & 0xffu;
-                                float lo = e2m1_mag(byte & 7u) * sc, hi = e2m1_mag((byte >> 4) & 7u) * sc;
-                                if (byte & 8u) lo = -lo;
-                                if (byte & 0x80u) hi = -hi;
-                                const __nv_bfloat162 bb = __floats2bfloat162_rn(lo, hi);
-                                packed[k] = *reinterpret_cast<const uint32_t *>(&bb);
-                            }
-                            *reinterpret_cast<uint4 *>(base + sw128(r, (blk & 1) * 4 + q4)) =
-                                make_uint4(packed[0], packed[1], packed[2], packed[3]);
-                        }
+            for (int i = 0; i + 1 < kBlocks; ++i) {
+                cw[i] = cw[i + 1];
+                sc[i] = sc[i + 1];
+            }
+        }
+        if (slow) {
+            // exact float products rounded to bf16 once, the block's codes read again
+#pragma unroll 1
+            for (int k = 0; k < kBlocks; ++k) {
+                if (!((slow >> k) & 1u)) continue;
+                const int bi = tid + kThreads * k, r = bi / 18, blk = bi - 18 * r, c = blk >> 1;
+                uint8_t *base = sm + (c < 8 ? kOffK + c * kChunkBytes : kOffR);
+                const int64_t g = kv_row0 + s_src[r];
+                const uint8_t *codes = P.kvc + g * (kDqk / 2) + blk * 16;
+                const float sf = e8m0_value(P.kvs[g * (kDqk / 32) + blk]);
+#pragma unroll 1
+                for (int w = 0; w < 4; ++w) {
+                    const uint32_t word = *reinterpret_cast<const uint32_t *>(codes + 4 * w);
+                    uint32_t o[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const uint32_t byte = (word >> (8 * i)) & 0xffu;
+                        float lo = e2m1_mag(byte & 7u) * sf, hi = e2m1_mag((byte >> 4) & 7u) * sf;
+                        if (byte & 8u) lo = -lo;
+                        if (byte & 0x80u) hi = -hi;
+                        const __nv_bfloat162 bb = __floats2bfloat162_rn(lo, hi);
+                        o[i] = *reinterpret_cast<const uint32_t *>(&bb);
                     }
-                }
-            } else if (src <= -2 && P.swa8) {
-                // MXFP8 SWA row: 8 E4M3 codes per 16-byte piece, decoded exactly (the code's
-                // bits placed as a float's, times 2^120 to move the exponent bias from 7 to
-                // 127 -- subnormal codes included -- and times the block's 2^X)
-                const int64_t srw = b * P.n_swa + (-src - 2);
-                const uint8_t *crow = reinterpret_cast<const uint8_t *>(P.swa) + srw * kDqk;
-                const uint8_t *srow_s = P.swa_scales + srw * (kDqk / 32);
-#pragma unroll 2
-                for (int pc = part * 36; pc < part * 36 + 36; ++pc) {
-                    const int c = pc >> 3;
-                    uint8_t *base = sm + (c < 8 ? kOffK + c * kChunkBytes : kOffR);
-                    const uint2 w8 = *reinterpret_cast<const uint2 *>(crow + pc * 8);
-                    const float k2 = e8m0_value(srow_s[pc >> 2]);
-                    uint32_t packed[4];
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const uint32_t x = k < 2 ? w8.x : w8.y, sh = 16 * (k & 1);
-                        const uint32_t b0 = x >> sh, b1 = x >> (sh + 8);
-                        const float f0 = __uint_as_float(((b0 & 0x7fu) << 20) | ((b0 & 0x80u) << 24)) * 0x1p120f * k2;
-                        const float f1 = __uint_as_float(((b1 & 0x7fu) << 20) | ((b1 & 0x80u) << 24)) * 0x1p120f * k2;
-                        const __nv_bfloat162 bb = __floats2bfloat162_rn(f0, f1);
-                        packed[k] = *reinterpret_cast<const uint32_t *>(&bb);
-                    }
-                    *reinterpret_cast<uint4 *>(base + sw128(r, pc & 7)) =
-                        make_uint4(packed[0], packed[1], packed[2], packed[3]);
-                }
-            } else if (src <= -2) {
-                const uint16_t *srow = P.swa + (b * P.n_swa + (-src - 2)) * (int64_t)kDqk;
-#pragma unroll 4
-                for (int pc = part * 36; pc < part * 36 + 36; ++pc) {
-                    const int c = pc >> 3;
-                    uint8_t *base = sm + (c < 8 ? kOffK + c * kChunkBytes : kOffR);
-                    cp_async_16(base + sw128(r, pc & 7), srow + pc * 8);
-                }
-            } else {
-#pragma unroll 4
-                for (int pc = part * 36; pc < part * 36 + 36; ++pc) {
-                    const int c = pc >> 3;
-                    uint8_t *base = sm + (c < 8 ? kOffK + c * kChunkBytes : kOffR);
-                    *reinterpret_cast<uint4 *>(base + sw128(r, pc & 7)) = make_uint4(0, 0, 0, 0);
+                    *reinterpret_cast<uint4 *>(base + sw128(r, (blk & 1) * 4 + w)) = make_uint4(o[0], o[1], o[2], o[3]);
                 }
             }
         }
-        const bool valid = src_cur != -1;
-        // ---- stage the next tile (its index was read one tile earlier)
-        if (tile + 1 < t_end) {
-            src_cur = slot_src(tile + 1, id_next);
-            issue(src_cur);
-            id_next = tile + 2 < t_end ? slot_id(tile + 2) : 0;
+    };
+    // bf16 SWA rows: one 16-byte cp.async per piece
+    auto stage_swa16 = [&]() {
+#pragma unroll 4
+        for (int k = 0; k < kPieces; ++k) {
+            const int p = tid + kThreads * k, r = p / 72, q = p - 72 * r;
+            const int64_t src = s_src[r];
+            uint8_t *dst = piece_dst(r, q);
+            if (src <= -2) cp_async_16(dst, P.swa + (swa_row0 + (-src - 2)) * kDqk + q * 8);
+            else *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
         }
+    };
+    // MXFP8 SWA rows: 8 E4M3 code bytes and their scale byte per piece, decoded exactly (the
+    // code's bits placed as a float's, times 2^120 to move the exponent bias from 7 to 127 --
+    // subnormal codes included -- and times the block's 2^X)
+    auto stage_swa8 = [&]() {
+#pragma unroll 2
+        for (int k = 0; k < kPieces; ++k) {
+            const int p = tid + kThreads * k, r = p / 72, q = p - 72 * r;
+            const int64_t src = s_src[r];
+            uint32_t o[4] = {0u, 0u, 0u, 0u};
+            if (src <= -2) {
+                const int64_t srw = swa_row0 + (-src - 2);
+                const uint2 cw = *reinterpret_cast<const uint2 *>(reinterpret_cast<const uint8_t *>(P.swa) + srw * kDqk + q * 8);
+                const float k2 = e8m0_value(P.swa_scales[srw * (kDqk / 32) + (q >> 2)]);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t x = i < 2 ? cw.x : cw.y, sh = 16 * (i & 1);
+                    const uint32_t b0 = x >> sh, b1 = x >> (sh + 8);
+                    const float f0 = __uint_as_float(((b0 & 0x7fu) << 20) | ((b0 & 0x80u) << 24)) * 0x1p120f * k2;
+                    const float f1 = __uint_as_float(((b1 & 0x7fu) << 20) | ((b1 & 0x80u) << 24)) * 0x1p120f * k2;
+                    const __nv_bfloat162 bb = __floats2bfloat162_rn(f0, f1);
+                    o[i] = *reinterpret_cast<const uint32_t *>(&bb);
+                }
+            }
+            *reinterpret_cast<uint4 *>(piece_dst(r, q)) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+    };
+    // the next tile's source row of key slot `key_row` into L2 (threads < 128)
+    auto prefetch_row = [&](int tile, int32_t id) {
+        if (tile < P.n_itiles) {
+            const int64_t sl = (int64_t)tile * kKeys + key_row;
+            if (sl >= P.topk || id < 0 || id >= P.n_kv) return;
+            const uint8_t *c = P.kvc + (kv_row0 + id) * (kDqk / 2);
+#pragma unroll
+            for (int o = 0; o < kDqk / 2; o += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(c + o));
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(c + kDqk / 2 - 1));
+            const uint8_t *s = P.kvs + (kv_row0 + id) * (NV ? kDqk / 16 : kDqk / 32);
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(s));
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(s + (NV ? kDqk / 16 : kDqk / 32) - 1));
+        } else {
+            const int64_t sl = sw_lo + (int64_t)(tile - P.n_itiles) * kKeys + key_row;
+            if (sl >= sw_hi) return;
+            const int64_t srw = swa_row0 + j0 + sl;
+            const int row_bytes = P.swa8 ? kDqk : 2 * kDqk;
+            const uint8_t *c = reinterpret_cast<const uint8_t *>(P.swa) + srw * row_bytes;
+#pragma unroll 1
+            for (int o = 0; o < row_bytes; o += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(c + o));
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(c + row_bytes - 1));
+            if (P.swa8) asm volatile("prefetch.global.L2 [%0];" ::"l"(P.swa_scales + srw * (kDqk / 32)));
+        }
+    };
+    int32_t id_cur = 0;      // index entry of key slot key_row of the current tile (threads < 128)
+    bool have_id = false;
+#pragma unroll 1
+    for (int v = 0; v < n_v; ++v) {
+        const int tile = gtile(v);
+        if (tile < P.n_itiles) {
+            wait_prev();
+            if (!have_id && tid < kKeys) id_cur = slot_id(tile);
+        }
+        // the next tile's index entries are read a tile ahead (once the wait is behind)
+        const int tn = v + 1 < n_v ? gtile(v + 1) : -1;
+        const bool nx_idx = tn >= 0 && tn < P.n_itiles && waited;
+        const int32_t id_nx = nx_idx && tid < kKeys ? slot_id(tn) : 0;
+        if (tid < kKeys) s_src[tid] = slot_src(tile, id_cur);
+        __syncthreads();
+        // ---- stage the tile's keys into the chunks
+        if (tile < P.n_itiles) stage_fp4();
+        else if (P.swa8) stage_swa8();
+        else stage_swa16();
+        if (tid < kKeys && tn >= 0 && (tn >= P.n_itiles || nx_idx)) prefetch_row(tn, id_nx);
+        id_cur = id_nx;
+        have_id = nx_idx;
+        const bool valid = s_src[key_row] != -1;
         cp_async_wait_all();
         tc::fence_proxy_async_smem();
         __syncthreads();
@@ -558,6 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
         __syncthreads();
     }
 
+    wait_prev();             // a CTA with SWA tiles only has not waited yet
     // ---- epilogue: thread = (dim row of each O^T block, its 32 heads)
     const uint32_t lane_t = tmem + ((uint32_t)(quad * 32) << 16);
     if (P.splits == 1) {
@@ -585,7 +617,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
         // to every rank through distributed shared memory and its raw O^T blocks to the
         // workspace ([row][split][block][head][128 dims]); after one cluster barrier, O^T
         // block m is merged by rank m % S from its own copy (still in tensor memory) and
-        // the other ranks' copies, read through L2:
+        // the other ranks' copies, bulk-copied from L2 into its shared memory:
         //   o = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s,  lse = (M + log2 l) ln 2
         const int S = P.splits;
         const int64_t blk_floats = (int64_t)H * kKeys;                 // one block of a rank
@@ -618,6 +650,21 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
         cluster_sync();                   // (m, l) and partials visible to the whole cluster
         tc::tc_fence_after();
         const int n_own = (4 - split + S - 1) / S;                       // blocks m = split + kS
+        // The peers' copies of the owned blocks come into shared memory with one bulk copy
+        // each (the tiles' buffers are free now), slot k (S - 1) + (peer rank, this one skipped).
+        const uint32_t blk_bytes = (uint32_t)blk_floats * 4u;
+        const uint32_t n_in = (uint32_t)(n_own * (S - 1));
+        if (tid == 0 && n_in > 0) {
+            tc::mbar_arrive_expect_tx(&s_bar, n_in * blk_bytes);
+            uint32_t slot = 0;
+#pragma unroll 1
+            for (int k = 0; k < n_own; ++k)
+#pragma unroll 1
+                for (int sp = 0; sp < S; ++sp)
+                    if (sp != split)
+                        tc::bulk_load(sm + (slot++) * blk_bytes,
+                                      P.part_o + ((row * S + sp) * 4 + split + k * S) * blk_floats, blk_bytes, &s_bar);
+        }
         if (tid < kH) {
             float M = -INFINITY;
 #pragma unroll 1
@@ -633,9 +680,20 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
             s_corr[tid] = L > 0.0f ? 1.0f / L : 0.0f;                 // 1/l per head
             if (split == 0 && tid < H && P.lse) P.lse[row * H + tid] = L > 0.0f ? (M + log2f(L)) * kLn2 : -INFINITY;
         }
-        __syncthreads();
+        bool have = true;
+        if (n_in > 0) {
+            if (__syncthreads_or(!tc::mbar_wait(&s_bar, phase, &s_abort))) {
+                s_abort = 1;
+                tc::mbar_wait_bounded(&s_bar, phase);   // the copies in flight land before exit
+                have = false;
+            }
+            phase ^= 1u;
+        } else {
+            __syncthreads();
+        }
+        const float *peer = reinterpret_cast<const float *>(sm) + key_row;
 #pragma unroll 1
-        for (int k = 0; k < n_own; ++k) {
+        for (int k = 0; have && k < n_own; ++k) {
             const int m = split + k * S, d = 128 * m + key_row;
             uint32_t own[32];
             if (any_o) {
@@ -650,17 +708,11 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
             for (int j = 0; j < 32; ++j) acc[j] = 0.0f;
 #pragma unroll 1
             for (int sp = 0; sp < S; ++sp) {
-                if (sp == split) {
+                const float *src = peer + (int64_t)(k * (S - 1) + (sp < split ? sp : sp - 1)) * blk_floats;
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) acc[j] += s_fac[sp][hh0 + j] * __uint_as_float(own[j]);
-                } else {                  // the peer's copy of block m, read through L2
-                    const float *src = P.part_o + ((row * S + sp) * 4 + m) * blk_floats + key_row;
-                    float v[32];
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] = hh0 + j < H ? __ldcg(src + (hh0 + j) * kKeys) : 0.0f;
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) acc[j] += s_fac[sp][hh0 + j] * v[j];
-                }
+                for (int j = 0; j < 32; ++j)
+                    acc[j] += s_fac[sp][hh0 + j] * (sp == split ? __uint_as_float(own[j])
+                                                                : hh0 + j < H ? src[(hh0 + j) * kKeys] : 0.0f);
             }
 #pragma unroll
             for (int j = 0; j < 32; ++j)
@@ -676,18 +728,25 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
     if (tid == 0 && s_abort) dev_flag(P.d_status, CSA2_DEV_TIMEOUT);
 }
 
-void attn_tc_split(const csa2_attn_args &a, int &splits, int &tiles_per_split)
+// Index tiles per CTA and CTAs (one cluster) per row: one index tile per CTA while the rows'
+// index tiles fit one wave of the GPU's SMs, at most kMaxSplits CTAs a row; the row's SWA
+// window is shared out evenly among its CTAs, ahead of their index tiles.
+void attn_tc_split(const csa2_attn_args &a, int &splits, int &tiles_per_split, int &n_itiles)
 {
     const int64_t rows = (int64_t)a.batch * a.n_q;
-    const int64_t max_slots = (int64_t)a.topk + (a.swa ? (int64_t)(a.window < a.n_swa ? a.window : a.n_swa) : 0);
-    const int tiles = (int)((max_slots + kKeys - 1) / kKeys);
+    n_itiles = (int)((a.topk + kKeys - 1) / kKeys);
+    if (n_itiles == 0) {
+        splits = 1;
+        tiles_per_split = 0;
+        return;
+    }
     const int64_t sms = device_sm_count();
-    int64_t per = (tiles * rows + sms - 1) / sms;       // tiles per CTA to fill one wave
+    int64_t per = (n_itiles * rows + sms - 1) / sms;     // index tiles per CTA to fill one wave
     if (per < 1) per = 1;
-    if (per * kMaxSplits < tiles) per = (tiles + kMaxSplits - 1) / kMaxSplits;   // one cluster per row
-    if (per > tiles) per = tiles > 0 ? tiles : 1;
+    if (per * kMaxSplits < n_itiles) per = (n_itiles + kMaxSplits - 1) / kMaxSplits;   // one cluster per row
+    if (per > n_itiles) per = n_itiles;
     tiles_per_split = (int)per;
-    splits = tiles > 0 ? (int)((tiles + per - 1) / per) : 1;
+    splits = (int)((n_itiles + per - 1) / per);
 }
 
 } // namespace
@@ -702,8 +761,8 @@ bool attn_tc_eligible(const csa2_attn_args &a)
 
 size_t attn_tc_ws_bytes(const csa2_attn_args &a)
 {
-    int splits, per;
-    attn_tc_split(a, splits, per);
+    int splits, per, nit;
+    attn_tc_split(a, splits, per, nit);
     if (splits <= 1) return 0;
     return (size_t)a.batch * a.n_q * splits * a.n_heads * (size_t)kDv * sizeof(float);
 }
@@ -732,7 +791,7 @@ cudaError_t launch_attn_tc(const csa2_attn_args &a, uint16_t *out, float *lse, v
     P.out = out;
     P.lse = lse;
     P.d_status = d_status;
-    attn_tc_split(a, P.splits, P.tiles_per_split);
+    attn_tc_split(a, P.splits, P.tiles_per_split, P.n_itiles);
     P.part_o = static_cast<float *>(ws);
     const int64_t rows = (int64_t)a.batch * a.n_q;
     const int smem = kSmemBytes + 1024;

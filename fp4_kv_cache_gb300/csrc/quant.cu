@@ -57,7 +57,6 @@ __global__ void __launch_bounds__(256) quant_mxfp4_vec_kernel(const void *__rest
                                                               uint32_t *d_status)
 {
     pdl_wait();                                   // x may come from the kernel before
-    pdl_allow_dependents();
     const int64_t nblk_row = cols / 32;
     const int64_t total = rows * nblk_row * 4;                 // lanes of work
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -123,7 +122,6 @@ __global__ void __launch_bounds__(256) quant_mxfp4_batch_kernel(const __grid_con
                                                                 uint32_t *d_status)
 {
     pdl_wait();                                   // x may come from the kernel before
-    pdl_allow_dependents();
     const int64_t total = B.lanes_end[B.n - 1];
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     const int64_t total32 = (total + 31) & ~int64_t(31);
@@ -194,7 +192,6 @@ __global__ void __launch_bounds__(256) quant_nvfp4_vec_kernel(const void *__rest
                                                               uint32_t *d_status)
 {
     pdl_wait();                                   // x may come from the kernel before
-    pdl_allow_dependents();
     const int64_t nblk_row = cols / 16;
     const int64_t total = rows * nblk_row * 2;                 // lanes of work
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -328,7 +325,6 @@ __global__ void __launch_bounds__(256) quant_mxfp8_kernel(const void *__restrict
     const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
     pdl_wait();
-    pdl_allow_dependents();
     for (int64_t blk = warp0; blk < total; blk += nwarps) {
         const int64_t r = blk / nblk_row, kb = blk % nblk_row;
         const int64_t col = kb * 32 + lane;
@@ -383,7 +379,6 @@ __global__ void __launch_bounds__(256) rope_quant_kernel(const __grid_constant__
                                                          uint32_t *d_status)
 {
     pdl_wait();                                   // x and pos may come from the kernel before
-    pdl_allow_dependents();
     const int64_t total = B.lanes_end[B.n - 1];
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     const int64_t total32 = (total + 31) & ~int64_t(31);

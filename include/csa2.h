@@ -32,14 +32,17 @@
  *     library keeps no mutable global state.
  *   - Kernels are launched with programmatic dependent launch: a kernel may start its
  *     set-up while the kernel before it on the stream drains, and waits for that kernel
- *     to complete before it reads what that kernel may write.  Every kernel of the
- *     library lets its dependents start only after that wait.  Two exceptions:
- *     csa2_sparse_attn reads q, q_pos, swa_pos0 and swa_start before its wait (only idx
- *     may come from the kernel just before it), and csa2_topk / csa2_block_candidates
- *     with an exact context read its q, w and k_scales before theirs (only the scores,
- *     row lengths and group maxima may come from the kernel just before them); those
- *     inputs must not be written by a kernel that lets its dependents start early (a
- *     plain kernel, or any call of this library, is fine).
+ *     to complete before it reads what that kernel may write.  The indexer, Top-K and
+ *     attention kernels let their dependents start right after that wait; the conversion
+ *     and cache-write calls (csa2_quant_*, csa2_dequant_*, csa2_rope_quant_fp4) only when
+ *     they finish.  Two exceptions read inputs before the wait: csa2_sparse_attn reads q,
+ *     q_pos, swa_pos0, swa_start, swa and swa_scales (and works through the SWA window)
+ *     before it (only idx may come from the kernel just before it), and csa2_topk /
+ *     csa2_block_candidates with an exact context read its q, w and k_scales before
+ *     theirs (only the scores, row lengths and group maxima may come from the kernel just
+ *     before them).  Those inputs must not be written by a kernel that lets its
+ *     dependents start early: a plain kernel, or a conversion or cache-write call of this
+ *     library, is fine, and so is any call of this library whose outputs they are not.
  */
 #ifndef CSA2_H
 #define CSA2_H

@@ -34,7 +34,8 @@
 namespace csa2 {
 namespace {
 
-constexpr int kThreads = 256;          // two warps per TMEM lane quadrant
+constexpr int kThreads = 512;          // four warps per TMEM lane quadrant, 16 heads each
+constexpr int kHT = 16;               // heads per thread in the softmax and the epilogue
 constexpr int kKeys = 128;            // key slots per tile (MMA M)
 constexpr int kH = 64;                // heads (MMA N; fewer heads are zero-padded)
 constexpr int kDqk = 576, kDv = 512;
@@ -44,7 +45,7 @@ constexpr int kQChunkBytes = kH * 128;            // 8 KB: 64 heads x 64 bf16
 constexpr uint32_t kTmemCols = 512;   // S^T [0,64), O^T block m at [64 + 64m, 128 + 64m)
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kMaxSplits = 7;          // CTAs (one cluster) per split row
-constexpr int kPieces = kKeys * (kDqk / 8) / kThreads;   // 36 pieces of 8 values per thread and tile
+constexpr int kPieces = kKeys * (kDqk / 8) / kThreads;   // 18 pieces of 8 values per thread and tile
 static_assert(kKeys * (kDqk / 8) == kPieces * kThreads, "pieces do not divide evenly");
 
 struct AttnTcParams {
@@ -145,19 +146,6 @@ __device__ __forceinline__ void mma_f16(uint32_t d, uint64_t a, uint64_t b, uint
                  ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
 }
 
-__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32])
-{
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0],"
-                 " {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16,"
-                 " %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};"
-                 ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]),
-                   "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]),
-                   "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
-                   "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
-                   "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
-                 : "memory");
-}
-
 __device__ __forceinline__ void cp_async_16(void *dst, const void *src)
 {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_u32(dst)), "l"(src) : "memory");
@@ -167,13 +155,17 @@ __device__ __forceinline__ void cp_async_wait_all()
     asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
-// Reduce 32 per-thread values over the 32 lanes of a warp by halving: afterwards lane L
-// holds the reduction of value index L in v[0] (31 shuffles instead of 32 x 5).
-template <bool MAX>
-__device__ __forceinline__ float warp_halving_reduce32(float (&v)[32], int lane)
+// Reduce N per-thread values (N = 16 or 32) over the 32 lanes of a warp by halving: each
+// exchange sends half the values and keeps the other half, so afterwards lane L holds the
+// reduction of value index L N / 32 (for N = 16 lanes 2i and 2i + 1 both hold value i).
+template <bool MAX, int N>
+__device__ __forceinline__ float warp_halving_reduce(float (&v)[N], int lane)
 {
+    static_assert(N == 16 || N == 32, "16 or 32 values");
+    constexpr int kSteps = N == 32 ? 5 : 4;
 #pragma unroll
-    for (int o = 16, n = 32; o >= 1; o >>= 1, n >>= 1) {
+    for (int st = 0; st < kSteps; ++st) {
+        const int o = 16 >> st, n = N >> st;
         const bool upper = (lane & o) != 0;
 #pragma unroll
         for (int i = 0; i < n / 2; ++i) {
@@ -182,6 +174,10 @@ __device__ __forceinline__ float warp_halving_reduce32(float (&v)[32], int lane)
             const float recv = __shfl_xor_sync(0xffffffffu, send, o);
             v[i] = MAX ? fmaxf(keep, recv) : keep + recv;
         }
+    }
+    if (N == 16) {
+        const float recv = __shfl_xor_sync(0xffffffffu, v[0], 1);
+        v[0] = MAX ? fmaxf(v[0], recv) : v[0] + recv;
     }
     return v[0];
 }
@@ -207,7 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
     const int split = blockIdx.x;
     const int64_t b = row / P.T;
     const int H = P.H;
-    const int quad = warp & 3, hh0 = 32 * (warp >> 2);   // TMEM lane quadrant, first head
+    const int quad = warp & 3, hh0 = kHT * (warp >> 2);  // TMEM lane quadrant, first head
     const int key_row = 32 * quad + lane;                 // this thread's key / dim row
     const int t_begin = split * P.tiles_per_split;
     // index entry of slot `key_row` of an index tile (0 past the entries and for SWA tiles)
@@ -289,12 +285,12 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
         return sl < sw_hi ? -(j0 + sl + 2) : -1;
     };
     // Staging: thread t < 128 resolves key slot t of the tile to its source row (s_src).
-    // Main-KV tiles then go to the threads as 32-value blocks (16 code bytes, one scale)
-    // bi = t + 256 k, k < 9: consecutive threads take consecutive blocks of a row, so a
-    // warp's reads cover one or two rows' contiguous bytes.  Each block decodes to four
-    // 16-byte pieces of one chunk row; a thread writes them starting at piece (chunk & 3),
-    // so the eight threads of a store phase (four chunks, two blocks each) hit eight
-    // different bank groups.  SWA tiles go by 8-value pieces p = t + 256 k, k < 36.  The
+    // Main-KV tiles then go to the threads as 16-value half blocks (8 code bytes, one scale)
+    // hb = t + 512 k, k < 9: consecutive threads take consecutive half blocks of a row, so a
+    // warp's reads cover one or two rows' contiguous bytes.  A half block decodes to two
+    // 16-byte pieces of one chunk row, written in the order given by the chunk's parity,
+    // so the eight threads of a store phase (two chunks, four half blocks each) hit eight
+    // different bank groups.  SWA tiles go by 8-value pieces p = t + 512 k, k < 18.  The
     // next tile's rows are prefetched into L2 while the current one computes.
     const int64_t kv_row0 = b * P.n_kv, swa_row0 = b * P.n_swa;
     auto piece_dst = [&](int r, int q) -> uint8_t * {
@@ -302,71 +298,56 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
         return sm + (c < 8 ? kOffK + c * kChunkBytes : kOffR) + sw128(r, q & 7);
     };
     auto stage_fp4 = [&]() {
-        constexpr int kBlocks = kKeys * (kDqk / 32) / kThreads;      // 9 blocks per thread
-        uint4 cw[kBlocks];
-        uint32_t sc[kBlocks], ok = 0;
+        constexpr int kHalves = kKeys * (kDqk / 16) / kThreads;      // 9 half blocks per thread
+        uint2 cw[kHalves];
+        uint32_t sc[kHalves], ok = 0;
 #pragma unroll
-        for (int k = 0; k < kBlocks; ++k) {
-            const int bi = tid + kThreads * k, r = bi / 18, blk = bi - 18 * r;
+        for (int k = 0; k < kHalves; ++k) {
+            const int hb = tid + kThreads * k, r = hb / 36, hq = hb - 36 * r;
             const int64_t src = s_src[r];
-            cw[k] = make_uint4(0u, 0u, 0u, 0u);
+            cw[k] = make_uint2(0u, 0u);
             sc[k] = 0u;
             if (src >= 0) {
                 const int64_t g = kv_row0 + src;
-                cw[k] = *reinterpret_cast<const uint4 *>(P.kvc + g * (kDqk / 2) + blk * 16);
-                sc[k] = NV ? *reinterpret_cast<const uint16_t *>(P.kvs + g * (kDqk / 16) + blk * 2)
-                           : P.kvs[g * (kDqk / 32) + blk];
+                cw[k] = *reinterpret_cast<const uint2 *>(P.kvc + g * (kDqk / 2) + hq * 8);
+                sc[k] = NV ? P.kvs[g * (kDqk / 16) + hq] : P.kvs[g * (kDqk / 32) + (hq >> 1)];
                 ok |= 1u << k;
             }
         }
-        // decode block by block in a rolled loop (the block in hand is always cw[0]: the
-        // arrays shift down one place per block), so the code stays small -- it runs once
-        // per tile, and unrolled it costs more in instruction fetch than in execution
         uint32_t slow = 0;
-#pragma unroll 1
-        for (int k = 0; k < kBlocks; ++k) {
-            const int bi = tid + kThreads * k, r = bi / 18, blk = bi - 18 * r, c = blk >> 1;
+#pragma unroll
+        for (int k = 0; k < kHalves; ++k) {
+            const int hb = tid + kThreads * k, r = hb / 36, hq = hb - 36 * r, c = hq >> 2;
             uint8_t *base = sm + (c < 8 ? kOffK + c * kChunkBytes : kOffR);
             // code value x scale in bf16 is exact: an E4M3 scale has 4 significant bits and a
             // code 2, with every product normal; an E8M0 scale in [2^-119, 2^123] keeps every
             // product normal.  Other E8M0 scales (rare) take the exact float path below.
             const bool have = (ok >> k) & 1u;
-            const bool use = have && (NV || (sc[0] >= 8u && sc[0] <= 250u));
+            const bool use = have && (NV || (sc[k] >= 8u && sc[k] <= 250u));
             if (have && !use) slow |= 1u << k;
-            const unsigned short s_lo = NV ? (unsigned short)(__float_as_uint(e4m3_value(sc[0] & 0xffu)) >> 16)
-                                           : (unsigned short)(sc[0] << 7);
-            const unsigned short s_hi = NV ? (unsigned short)(__float_as_uint(e4m3_value(sc[0] >> 8)) >> 16) : s_lo;
+            const unsigned short sbits = NV ? (unsigned short)(__float_as_uint(e4m3_value(sc[k])) >> 16)
+                                            : (unsigned short)(sc[k] << 7);
+            const __nv_bfloat162 sc2 = __halves2bfloat162(__ushort_as_bfloat16(sbits), __ushort_as_bfloat16(sbits));
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int w = (j + c) & 3;
-                const uint32_t word = w == 0 ? cw[0].x : w == 1 ? cw[0].y : w == 2 ? cw[0].z : cw[0].w;
-                const unsigned short sbits = w < 2 ? s_lo : s_hi;
+            for (int j = 0; j < 2; ++j) {
+                const int w = (j + c) & 1;
                 uint32_t o[4] = {0u, 0u, 0u, 0u};
-                if (use) {
-                    const __nv_bfloat162 sc2 =
-                        __halves2bfloat162(__ushort_as_bfloat16(sbits), __ushort_as_bfloat16(sbits));
-                    e2m1x8_to_bf16(word, sc2, o);
-                }
-                *reinterpret_cast<uint4 *>(base + sw128(r, (blk & 1) * 4 + w)) = make_uint4(o[0], o[1], o[2], o[3]);
-            }
-#pragma unroll
-            for (int i = 0; i + 1 < kBlocks; ++i) {
-                cw[i] = cw[i + 1];
-                sc[i] = sc[i + 1];
+                if (use) e2m1x8_to_bf16(w ? cw[k].y : cw[k].x, sc2, o);
+                *reinterpret_cast<uint4 *>(base + sw128(r, 2 * (hq & 3) + w)) = make_uint4(o[0], o[1], o[2], o[3]);
             }
         }
         if (slow) {
-            // exact float products rounded to bf16 once, the block's codes read again
+            // exact float products rounded to bf16 once, the half block's codes read again
 #pragma unroll 1
-            for (int k = 0; k < kBlocks; ++k) {
+            for (int k = 0; k < kHalves; ++k) {
                 if (!((slow >> k) & 1u)) continue;
-                const int bi = tid + kThreads * k, r = bi / 18, blk = bi - 18 * r, c = blk >> 1;
+                const int hb = tid + kThreads * k, r = hb / 36, hq = hb - 36 * r, c = hq >> 2;
                 uint8_t *base = sm + (c < 8 ? kOffK + c * kChunkBytes : kOffR);
                 const int64_t g = kv_row0 + s_src[r];
-                const uint8_t *codes = P.kvc + g * (kDqk / 2) + blk * 16;
-                const float sf = e8m0_value(P.kvs[g * (kDqk / 32) + blk]);
+                const uint8_t *codes = P.kvc + g * (kDqk / 2) + hq * 8;
+                const float sf = e8m0_value(P.kvs[g * (kDqk / 32) + (hq >> 1)]);
 #pragma unroll 1
-                for (int w = 0; w < 4; ++w) {
+                for (int w = 0; w < 2; ++w) {
                     const uint32_t word = *reinterpret_cast<const uint32_t *>(codes + 4 * w);
                     uint32_t o[4];
 #pragma unroll
@@ -378,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
                         const __nv_bfloat162 bb = __floats2bfloat162_rn(lo, hi);
                         o[i] = *reinterpret_cast<const uint32_t *>(&bb);
                     }
-                    *reinterpret_cast<uint4 *>(base + sw128(r, (blk & 1) * 4 + w)) = make_uint4(o[0], o[1], o[2], o[3]);
+                    *reinterpret_cast<uint4 *>(base + sw128(r, 2 * (hq & 3) + w)) = make_uint4(o[0], o[1], o[2], o[3]);
                 }
             }
         }
@@ -489,21 +470,22 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
         if (__syncthreads_or(!tc::mbar_wait(&s_bar, phase, &s_abort))) { s_abort = 1; break; }
         phase ^= 1u;
         tc::tc_fence_after();
-        // ---- softmax numerators: thread = (key row, 32 heads)
-        float l[32];
+        // ---- softmax numerators: thread = (key row, 16 heads)
+        float l[kHT];
         {
-            uint32_t r[32];
-            tc::tc_ld_32x32b_x32(tmem + ((uint32_t)(quad * 32) << 16) + hh0, r);
+            uint32_t r[kHT];
+            tc::tc_ld_32x32b_x16(tmem + ((uint32_t)(quad * 32) << 16) + hh0, r);
             tc::tc_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
+            for (int j = 0; j < kHT; ++j)
                 l[j] = (valid && hh0 + j < H) ? __uint_as_float(r[j]) * P.log2_scale : -INFINITY;
         }
         {
-            float v[32];
+            float v[kHT];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = l[j];
-            s_red[quad][hh0 + lane] = warp_halving_reduce32<true>(v, lane);
+            for (int j = 0; j < kHT; ++j) v[j] = l[j];
+            const float red = warp_halving_reduce<true, kHT>(v, lane);
+            if ((lane & 1) == 0) s_red[quad][hh0 + (lane >> 1)] = red;
         }
         __syncthreads();
         if (tid < kH) {
@@ -515,12 +497,13 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
         }
         __syncthreads();
 #pragma unroll
-        for (int j = 0; j < 32; ++j) l[j] = (l[j] == -INFINITY) ? 0.0f : exp2f(l[j] - s_m[hh0 + j]);
+        for (int j = 0; j < kHT; ++j) l[j] = (l[j] == -INFINITY) ? 0.0f : exp2f(l[j] - s_m[hh0 + j]);
         {
-            float v[32];
+            float v[kHT];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = l[j];
-            s_red[quad][hh0 + lane] = warp_halving_reduce32<false>(v, lane);
+            for (int j = 0; j < kHT; ++j) v[j] = l[j];
+            const float red = warp_halving_reduce<false, kHT>(v, lane);
+            if ((lane & 1) == 0) s_red[quad][hh0 + (lane >> 1)] = red;
         }
         // ---- P^T (bf16) into the rope-chunk buffer: [64 heads x 128 keys], two 64-key halves
         {
@@ -528,13 +511,13 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
             const int col = key_row & 63;
             const bool odd = (lane & 1) != 0;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                // even lanes store heads hh0..hh0+15 for keys (row, row+1); odd lanes heads
-                // hh0+16..hh0+31 for keys (row-1, row)
-                const float mine = odd ? l[16 + i] : l[i];
-                const float send = odd ? l[i] : l[16 + i];
+            for (int i = 0; i < kHT / 2; ++i) {
+                // even lanes store heads hh0..hh0+7 for keys (row, row+1); odd lanes heads
+                // hh0+8..hh0+15 for keys (row-1, row)
+                const float mine = odd ? l[kHT / 2 + i] : l[i];
+                const float send = odd ? l[i] : l[kHT / 2 + i];
                 const float other = __shfl_xor_sync(0xffffffffu, send, 1);
-                const int h = hh0 + (odd ? 16 + i : i);
+                const int h = hh0 + (odd ? kHT / 2 + i : i);
                 const int c0 = odd ? col - 1 : col;
                 const __nv_bfloat162 pr = odd ? __floats2bfloat162_rn(other, mine)
                                               : __floats2bfloat162_rn(mine, other);
@@ -546,20 +529,20 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
             const float tsum = s_red[0][tid] + s_red[1][tid] + s_red[2][tid] + s_red[3][tid];
             s_l[tid] = s_l[tid] * s_corr[tid] + tsum;
         }
-        // ---- rescale the running O^T by the per-head correction (thread = dim row, 32 heads)
+        // ---- rescale the running O^T by the per-head correction (thread = dim row, 16 heads)
         if (any_o) {
 #pragma unroll 1
             for (int m = 0; m < 4; ++m) {
-                uint32_t r[32];
+                uint32_t r[kHT];
                 const uint32_t ta = tmem + ((uint32_t)(quad * 32) << 16) + 64 + 64 * m + hh0;
-                tc::tc_ld_32x32b_x32(ta, r);
+                tc::tc_ld_32x32b_x16(ta, r);
                 tc::tc_wait_ld();
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
+                for (int j = 0; j < kHT; ++j)
                     r[j] = __float_as_uint(__uint_as_float(r[j]) * s_corr[hh0 + j]);
-                tmem_st_32x32b_x32(ta, r);
+                tc::tc_st_32x32b_x16(ta, r);
             }
-            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            tc::tc_wait_st();
         }
         tc::fence_proxy_async_smem();
         tc::tc_fence_before();
@@ -590,7 +573,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
     }
 
     wait_prev();             // a CTA with SWA tiles only has not waited yet
-    // ---- epilogue: thread = (dim row of each O^T block, its 32 heads)
+    // ---- epilogue: thread = (dim row of each O^T block, its 16 heads)
     const uint32_t lane_t = tmem + ((uint32_t)(quad * 32) << 16);
     if (P.splits == 1) {
         if (tid < kH) s_corr[tid] = s_l[tid] > 0.0f ? 1.0f / s_l[tid] : 0.0f;   // 1/l per head
@@ -598,16 +581,16 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
 #pragma unroll 1
         for (int m = 0; m < 4; ++m) {
             const int d = 128 * m + key_row;
-            uint32_t r[32];
+            uint32_t r[kHT];
             if (any_o) {
-                tc::tc_ld_32x32b_x32(lane_t + 64 + 64 * m + hh0, r);
+                tc::tc_ld_32x32b_x16(lane_t + 64 + 64 * m + hh0, r);
                 tc::tc_wait_ld();
             } else {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) r[j] = 0u;
+                for (int j = 0; j < kHT; ++j) r[j] = 0u;
             }
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
+            for (int j = 0; j < kHT; ++j)
                 if (hh0 + j < H)
                     P.out[(row * H + hh0 + j) * (int64_t)kDv + d] = bf16_bits(__uint_as_float(r[j]) * s_corr[hh0 + j]);
         }
@@ -633,16 +616,16 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
         for (int m = 0; m < 4; ++m) {
             if (m % S == split) continue;
             float *dst = P.part_o + ((row * S + split) * 4 + m) * blk_floats + key_row;
-            uint32_t r[32];
-            if (any_o) {                  // one load of the 32 columns, one wait
-                tc::tc_ld_32x32b_x32(lane_t + 64 + 64 * m + hh0, r);
+            uint32_t r[kHT];
+            if (any_o) {                  // one load of the thread's columns, one wait
+                tc::tc_ld_32x32b_x16(lane_t + 64 + 64 * m + hh0, r);
                 tc::tc_wait_ld();
             } else {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) r[j] = 0u;
+                for (int j = 0; j < kHT; ++j) r[j] = 0u;
             }
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
+            for (int j = 0; j < kHT; ++j)
                 if (hh0 + j < H) dst[(hh0 + j) * kKeys] = __uint_as_float(r[j]);
         }
         __threadfence();
@@ -695,27 +678,27 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_tc_kernel(const AttnT
 #pragma unroll 1
         for (int k = 0; have && k < n_own; ++k) {
             const int m = split + k * S, d = 128 * m + key_row;
-            uint32_t own[32];
+            uint32_t own[kHT];
             if (any_o) {
-                tc::tc_ld_32x32b_x32(lane_t + 64 + 64 * m + hh0, own);
+                tc::tc_ld_32x32b_x16(lane_t + 64 + 64 * m + hh0, own);
                 tc::tc_wait_ld();
             } else {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) own[j] = 0u;
+                for (int j = 0; j < kHT; ++j) own[j] = 0u;
             }
-            float acc[32];
+            float acc[kHT];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) acc[j] = 0.0f;
+            for (int j = 0; j < kHT; ++j) acc[j] = 0.0f;
 #pragma unroll 1
             for (int sp = 0; sp < S; ++sp) {
                 const float *src = peer + (int64_t)(k * (S - 1) + (sp < split ? sp : sp - 1)) * blk_floats;
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
+                for (int j = 0; j < kHT; ++j)
                     acc[j] += s_fac[sp][hh0 + j] * (sp == split ? __uint_as_float(own[j])
                                                                 : hh0 + j < H ? src[(hh0 + j) * kKeys] : 0.0f);
             }
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
+            for (int j = 0; j < kHT; ++j)
                 if (hh0 + j < H) P.out[(row * H + hh0 + j) * (int64_t)kDv + d] = bf16_bits(acc[j] * s_corr[hh0 + j]);
         }
     }

@@ -6,10 +6,13 @@
 // SWA keys in [max(s, i-W+1), i].  Review page (papers.chlience.com, CSA2 section): the
 // main KV is a latent shared by every query head, so V is its leading d_v dims.
 //
-// One CTA = one query row x 8 heads.  Keys stream through shared memory in tiles of 32
-// (gathered FP4 rows -- MXFP4 or E2M1 + E4M3/16 -- dequantised exactly to float, then the
-// SWA slots, bf16 or MXFP8 (report §2.4.4 keeps the SWA KV in FP8)), with an online
-// softmax per head and fp32 accumulation.
+// One CTA = one query row x 8 heads x one span of its key slots.  Keys stream through
+// shared memory in tiles of 32 (gathered FP4 rows -- MXFP4 or E2M1 + E4M3/16 --
+// dequantised exactly to float, then the SWA slots, bf16 or MXFP8 (report §2.4.4 keeps
+// the SWA KV in FP8)), with an online softmax per head and fp32 accumulation.  When the
+// rows and head groups alone would leave most SMs idle, a row's slots are split over
+// several CTAs (flash-decoding style): each writes its (m, l, unnormalised output) to the
+// workspace and a second small kernel merges them.
 #include "common.cuh"
 #include "internal.h"
 #include <math.h>
@@ -23,6 +26,8 @@ constexpr int kKT = 32;   // keys per tile (one lane each for the logits)
 
 struct AttnParams {
     int32_t T, H, d_qk, d_v, topk, window, n_swa;
+    int32_t splits, tiles_per_split;   // spans of key tiles per row (splits > 1: partials to ws)
+    float *part;             // splits > 1: [rows, head groups, splits, kHG, d_v + 2] (m, l, acc)
     int32_t nv;              // main KV: 0 = MXFP4 (E8M0 / 32), 1 = E2M1 + E4M3 / 16
     float sm_scale;
     int64_t n_kv;
@@ -90,6 +95,9 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_cc_kernel(AttnParams P)
         n_sw = j1 >= j0 ? j1 - j0 + 1 : 0;
     }
     const int64_t n_slots = P.topk + n_sw;
+    const int64_t t_lo = (int64_t)blockIdx.z * P.tiles_per_split * kKT;
+    int64_t t_hi = t_lo + (int64_t)P.tiles_per_split * kKT;
+    t_hi = t_hi < n_slots ? t_hi : n_slots;
 
     float acc[kHG][CPT];
 #pragma unroll
@@ -99,7 +107,7 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_cc_kernel(AttnParams P)
     float m_run = -INFINITY, l_run = 0.0f;   // per-head state, held by the head's warp
     const int my_h = h0 + warp;
 
-    for (int64_t t0 = 0; t0 < n_slots; t0 += kKT) {
+    for (int64_t t0 = t_lo; t0 < t_hi; t0 += kKT) {
         if (tid < kKT) {
             const int64_t sl = t0 + tid;
             int64_t src = -1;
@@ -107,7 +115,7 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_cc_kernel(AttnParams P)
                 const int32_t id = P.idx[row * P.topk + sl];
                 if (id >= 0 && id < P.n_kv) src = id;
                 else if (id != -1) dev_flag(P.d_status, CSA2_DEV_BAD_INDEX);
-            } else if (sl < n_slots) {
+            } else if (sl < t_hi) {
                 src = -(j0 + (sl - P.topk) + 2);
             }
             s_src[tid] = src;
@@ -184,6 +192,24 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_cc_kernel(AttnParams P)
     }
     if (lane == 0) { s_m[warp] = m_run; s_l[warp] = l_run; }
     __syncthreads();
+    if (P.splits > 1) {
+        // this span's partial: m and l per head, then the output unnormalised (relative to m)
+        float *part = P.part + (((row * gridDim.x + blockIdx.x) * P.splits + blockIdx.z) * kHG) * (int64_t)(P.d_v + 2);
+#pragma unroll
+        for (int hh = 0; hh < kHG; ++hh) {
+            float *ph = part + hh * (int64_t)(P.d_v + 2);
+            if (tid == 0) {
+                ph[0] = s_m[hh];
+                ph[1] = s_l[hh];
+            }
+#pragma unroll
+            for (int u = 0; u < CPT; ++u) {
+                const int c = tid + kThreads * u;
+                if (c < P.d_v) ph[2 + c] = acc[hh][u];
+            }
+        }
+        return;
+    }
 #pragma unroll
     for (int hh = 0; hh < kHG; ++hh) {
         const int h = h0 + hh;
@@ -205,6 +231,60 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_cc_kernel(AttnParams P)
     }
 }
 
+// Merge of a split row: thread = output column, one CTA per (head group, row):
+//   o = sum_s e^(m_s - M) acc_s / sum_s e^(m_s - M) l_s,  lse = M + ln(sum_s e^(m_s - M) l_s)
+__global__ void __launch_bounds__(kThreads) sparse_attn_cc_merge_kernel(AttnParams P)
+{
+    const int64_t row = blockIdx.y;
+    const int S = P.splits;
+    const float *part = P.part + ((row * gridDim.x + blockIdx.x) * S * kHG) * (int64_t)(P.d_v + 2);
+#pragma unroll 1
+    for (int hh = 0; hh < kHG; ++hh) {
+        const int h = blockIdx.x * kHG + hh;
+        if (h >= P.H) break;
+        float M = -INFINITY;
+#pragma unroll 1
+        for (int z = 0; z < S; ++z) M = fmaxf(M, part[(z * kHG + hh) * (int64_t)(P.d_v + 2)]);
+        float L = 0.0f;
+#pragma unroll 1
+        for (int z = 0; z < S; ++z) {
+            const float *pz = part + (z * kHG + hh) * (int64_t)(P.d_v + 2);
+            if (pz[0] != -INFINITY) L += expf(pz[0] - M) * pz[1];
+        }
+        const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+#pragma unroll 1
+        for (int c = threadIdx.x; c < P.d_v; c += kThreads) {
+            float o = 0.0f;
+#pragma unroll 1
+            for (int z = 0; z < S; ++z) {
+                const float *pz = part + (z * kHG + hh) * (int64_t)(P.d_v + 2);
+                if (pz[0] != -INFINITY) o = fmaf(expf(pz[0] - M), pz[2 + c], o);
+            }
+            o *= inv;
+            uint32_t bits = __float_as_uint(o);       // round to nearest even bf16
+            bits += 0x7fffu + ((bits >> 16) & 1u);
+            P.out[(row * P.H + h) * (int64_t)P.d_v + c] = (uint16_t)(bits >> 16);
+        }
+        if (P.lse && threadIdx.x == 0) P.lse[row * P.H + h] = L > 0.0f ? M + logf(L) : -INFINITY;
+    }
+}
+
+// Spans per row: enough CTAs for about two per SM, at most one per 32-key tile of the
+// row's largest slot count (its Top-K entries and a full SWA window).
+void cc_split(const csa2_attn_args &a, int &splits, int &per)
+{
+    const int64_t rows = (int64_t)a.batch * a.n_q, hg = (a.n_heads + kHG - 1) / kHG;
+    int64_t sw = a.swa ? (a.window < a.n_swa ? a.window : a.n_swa) : 0;
+    const int64_t tiles = (a.topk + sw + kKT - 1) / kKT;
+    int64_t want = (2 * device_sm_count() + rows * hg - 1) / (rows * hg > 0 ? rows * hg : 1);
+    if (want > tiles) want = tiles;
+    if (want < 1) want = 1;
+    const int64_t p = (tiles + want - 1) / want;
+    per = (int)(p > 0 ? p : 1);
+    splits = (int)(tiles > 0 ? (tiles + per - 1) / per : 1);
+    if (splits < 1) splits = 1;
+}
+
 template <int CPT>
 cudaError_t launch_cc(const AttnParams &P, int64_t rows, cudaStream_t s)
 {
@@ -212,8 +292,13 @@ cudaError_t launch_cc(const AttnParams &P, int64_t rows, cudaStream_t s)
     cudaError_t e = cudaFuncSetAttribute(sparse_attn_cc_kernel<CPT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)((P.H + kHG - 1) / kHG), (unsigned)rows);
+    dim3 grid((unsigned)((P.H + kHG - 1) / kHG), (unsigned)rows, (unsigned)P.splits);
     sparse_attn_cc_kernel<CPT><<<grid, kThreads, smem, s>>>(P);
+    if (P.splits > 1) {
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        sparse_attn_cc_merge_kernel<<<dim3(grid.x, grid.y), kThreads, 0, s>>>(P);
+    }
     return cudaGetLastError();
 }
 
@@ -221,7 +306,12 @@ cudaError_t launch_cc(const AttnParams &P, int64_t rows, cudaStream_t s)
 
 size_t sparse_attn_ws_bytes(const csa2_attn_args &a)
 {
-    return attn_tc_eligible(a) ? attn_tc_ws_bytes(a) : 0;
+    if (attn_tc_eligible(a)) return attn_tc_ws_bytes(a);
+    int splits, per;
+    cc_split(a, splits, per);
+    if (splits <= 1) return 0;
+    const int64_t rows = (int64_t)a.batch * a.n_q, hg = (a.n_heads + kHG - 1) / kHG;
+    return (size_t)rows * hg * splits * kHG * (size_t)(a.d_v + 2) * sizeof(float);
 }
 
 cudaError_t launch_sparse_attn(const csa2_attn_args &a, uint16_t *out, float *lse, void *ws,
@@ -254,6 +344,8 @@ cudaError_t launch_sparse_attn(const csa2_attn_args &a, uint16_t *out, float *ls
     const int64_t rows = (int64_t)a.batch * a.n_q;
     if (rows == 0 || a.n_heads == 0) return cudaSuccess;
     if (attn_tc_eligible(a)) return launch_attn_tc(a, out, lse, ws, d_status, s);
+    cc_split(a, P.splits, P.tiles_per_split);
+    P.part = static_cast<float *>(ws);
     const int cpt = (a.d_v + kThreads - 1) / kThreads;
     switch (cpt <= 1 ? 1 : cpt <= 2 ? 2 : 4) {
     case 1: return launch_cc<1>(P, rows, s);

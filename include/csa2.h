@@ -372,6 +372,9 @@ typedef struct {
     const uint8_t *swa_scales; /* MXFP8: [B, n_swa, d_qk/32] scale bytes, else unused      */
 } csa2_attn_args;
 
+/* Workspace: split rows keep their partial outputs there.  Its size depends on the    */
+/* arguments and on the current device (its SM count sets how finely rows are split),  */
+/* so query it with that device current; 0 means ws may be NULL.                       */
 CSA2_API size_t csa2_sparse_attn_workspace_size(const csa2_attn_args *a);
 CSA2_API csa2_status csa2_sparse_attn(const csa2_attn_args *a, uint16_t *out, float *lse, void *ws,
                              size_t ws_bytes, uint32_t *d_status, csa2_stream stream);

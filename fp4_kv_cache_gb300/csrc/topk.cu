@@ -196,6 +196,7 @@ constexpr int kCandCap = 16384;         // candidates per row kept on chip (a wh
                                         // 2,048-block pool of 8 positions fits)
 
 struct GSmem {
+    uint32_t coarse[2][kGBins / 32];   // the same counts per 32 consecutive bins
     uint32_t hist[2][kGBins];    // double buffer: the next digit pass clears one while
     uint32_t warp[33];           // the current one counts into the other
     uint32_t pick[2];
@@ -251,24 +252,36 @@ __global__ void __launch_bounds__(256) group_max_kernel(const float *__restrict_
 // With all three passes: the exact key tau, and in need how many keys equal to tau belong
 // to the top k.  With the first `passes` only: tau with its unresolved low bits zero, a
 // lower bound of the exact key (need is then meaningless).
-// Each pass: one histogram of the keys that match the digits found so far (the other
-// buffer is cleared meanwhile for the next pass), then a block-wide scan finds the digit:
-// thread t owns nb / kGThreads consecutive bins from the top, an exclusive prefix sum of
-// their counts in thread order is the count above them, and the thread whose bins reach
-// `remaining` names the digit.
+// Each pass: one histogram of the keys that match the digits found so far, counted per
+// bin and per 32 consecutive bins (the other buffers are cleared meanwhile for the next
+// pass), then warp 0 alone finds the digit in two warp scans from the top -- over the
+// coarse counts, then over the 32 bins of the coarse bin that reaches `remaining` -- so a
+// pass costs two block barriers.
+__device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v, int lane)
+{
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += t;
+    }
+    return v;
+}
 __device__ __forceinline__ uint32_t g_threshold(const uint32_t *keys, int n, uint32_t k, GSmem &S,
                                              uint32_t &need, int passes)
 {
     const int tid = threadIdx.x, lane = tid & 31;
     uint32_t prefix = 0, mask = 0, remaining = k;
     for (int i = tid; i < kGBins; i += kGThreads) S.hist[0][i] = 0;
+    if (tid < kGBins / 32) S.coarse[0][tid] = 0;
     __syncthreads();
 #pragma unroll 1
     for (int pass = 0; pass < passes; ++pass) {
         const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0), nb = pass < 2 ? 2048 : 1024;
-        uint32_t *h = S.hist[pass & 1];
-        if (pass + 1 < passes)
+        uint32_t *h = S.hist[pass & 1], *hc = S.coarse[pass & 1];
+        if (pass + 1 < passes) {
             for (int i = tid; i < kGBins; i += kGThreads) S.hist[(pass + 1) & 1][i] = 0;
+            if (tid < kGBins / 32) S.coarse[(pass + 1) & 1][tid] = 0;
+        }
         for (int base = 0; base < n; base += kGThreads) {
             const int i = base + tid;
             uint32_t key = 0;
@@ -281,21 +294,42 @@ __device__ __forceinline__ uint32_t g_threshold(const uint32_t *keys, int n, uin
             if (act) {
                 const uint32_t digit = (key >> shift) & (uint32_t)(nb - 1);
                 const uint32_t peers = __match_any_sync(am, digit);
-                if (lane == __ffs(peers) - 1) atomicAdd(&h[digit], (uint32_t)__popc(peers));
+                if (lane == __ffs(peers) - 1) {
+                    atomicAdd(&h[digit], (uint32_t)__popc(peers));
+                    atomicAdd(&hc[digit >> 5], (uint32_t)__popc(peers));
+                }
             }
         }
         __syncthreads();
-        const int c = nb / kGThreads;                       // 2 or 1 bins per thread
-        const int top = nb - 1 - tid * c;
-        const uint32_t v0 = h[top], v1 = c > 1 ? h[top - 1] : 0u;
-        uint32_t total;
-        const uint32_t above = block_excl_count_sum(v0 + v1, S.warp, total);   // ends with a barrier
-        if (above < remaining && above + v0 >= remaining) {
-            S.pick[0] = (uint32_t)top;
-            S.pick[1] = remaining - above;
-        } else if (c > 1 && above + v0 < remaining && above + v0 + v1 >= remaining) {
-            S.pick[0] = (uint32_t)(top - 1);
-            S.pick[1] = remaining - above - v0;
+        if (tid < 32) {
+            // coarse bins from the top: lane L holds bin ncb-1-L, and bin 31-L when ncb = 64
+            const int ncb = nb >> 5;
+            const uint32_t c0 = hc[ncb - 1 - lane], c1 = ncb == 64 ? hc[31 - lane] : 0u;
+            const uint32_t i0 = warp_incl_scan(c0, lane);
+            const uint32_t i1 = warp_incl_scan(c1, lane) + __shfl_sync(0xffffffffu, i0, 31);
+            const uint32_t b0 = __ballot_sync(0xffffffffu, i0 >= remaining);
+            const uint32_t b1 = __ballot_sync(0xffffffffu, i1 >= remaining);
+            int cb;
+            uint32_t above;
+            if (b0) {
+                const int L = __ffs(b0) - 1;
+                cb = ncb - 1 - L;
+                above = __shfl_sync(0xffffffffu, i0 - c0, L);
+            } else {
+                const int L = b1 ? __ffs(b1) - 1 : 31;
+                cb = 31 - L;
+                above = __shfl_sync(0xffffffffu, i1 - c1, L);
+            }
+            // the 32 bins of coarse bin cb, from the top
+            const uint32_t f = h[cb * 32 + 31 - lane];
+            const uint32_t fi = warp_incl_scan(f, lane) + above;
+            const uint32_t bf = __ballot_sync(0xffffffffu, fi >= remaining);
+            const int Lf = bf ? __ffs(bf) - 1 : 31;
+            const uint32_t fabove = __shfl_sync(0xffffffffu, fi - f, Lf);
+            if (lane == 0) {
+                S.pick[0] = (uint32_t)(cb * 32 + 31 - Lf);
+                S.pick[1] = remaining - fabove;
+            }
         }
         __syncthreads();
         prefix |= S.pick[0] << shift;

@@ -706,6 +706,13 @@ __device__ __noinline__ void band_exact(const exact::QuantQuery &Q, const ExactA
         }
     }
     __syncthreads();
+    if (n_heads == 1) {
+        // one run: every band candidate has the same exact score, so the lowest positions
+        // (the band is in position order) are the ones taken
+        for (uint32_t u = tid; u < n_band; u += kGThreads) s_state[u] = u < take ? 1 : 0;
+        __syncthreads();
+        return;
+    }
     // fixed point for the run heads
     bool ok = true;
 #pragma unroll 1

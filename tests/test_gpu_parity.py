@@ -486,6 +486,64 @@ def test_exact_order_resolves_float32_ties(N, neg, tiny_exp):
     assert np.array_equal(blocks[0, 0].cpu().numpy(), oracle.block_candidates_exact(ex, N, 8, 40))
 
 
+def test_exact_order_long_row_spread_tie_group():
+    # a row of 70,001 positions: a float32 tie group of 1,000 positions spread over the
+    # whole row holds the top 512, whose exact order comes from the tiny second head; the
+    # filler keys (one float32 value too) score lower
+    N = 70001
+    q, k, wv = _near_tie_case(N, 77)
+    rng = np.random.default_rng(78)
+    tie = np.zeros(N, bool)
+    tie[rng.choice(N, 1000, replace=False)] = True
+    k[0, ~tie, :32] = 0.25                             # d_0 = 8 for the filler keys
+    qb, kb = synth.f32_to_bf16_bits(q), synth.f32_to_bf16_bits(k)
+    assert np.array_equal(f32(kb), k)
+    st = status()
+    kc, ks = csa2.quant_fp4(workload.bf16_tensor(kb, DEV), st)
+    wt = torch.from_numpy(wv).to(DEV)
+    scores, row_len, args = csa2.index_score(workload.bf16_tensor(qb, DEV), wt, kc, ks, d_status=st,
+                                             want_args=True)
+    K = 512
+    idx = csa2.topk(scores, K, row_len, d_status=st, exact=args)
+    idx_f = csa2.topk(scores, K, row_len, d_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    kc_o, ks_o = oracle.quant_mxfp4(k[0])
+    qc_o, qs_o = oracle.quant_mxfp4(q[0, 0])
+    pos = np.arange(N)
+    s_ref = oracle.index_scores(qc_o, qs_o, wv[0, 0], kc_o, ks_o, pos)
+    ex = oracle.index_scores_exact(qc_o, qs_o, wv[0, 0], kc_o, ks_o, pos)
+    assert np.all(s_ref[tie] == s_ref[tie][0]) and s_ref[~tie].max() < s_ref[tie][0]
+    ref = oracle.topk_exact(ex, pos, K)
+    assert not np.array_equal(ref, oracle.topk(s_ref, pos, K))
+    assert np.array_equal(idx[0, 0].cpu().numpy(), ref)
+    assert np.array_equal(idx_f[0, 0].cpu().numpy(), oracle.topk(s_ref, pos, K))
+
+
+def test_exact_order_long_rows_negative_weights():
+    # three rows of 100,003 positions with head weights of both signs, one row shortened to
+    # 40,000 positions and one to K + 1
+    w = W["full_decode_64k"].scaled(batch=3, n_q=1, n_keys=100003, q_pos0=100002, plant_frac=0.01, seed=29)
+    st = status()
+    dw = workload.build(w, kv=False, device=DEV, d_status=st)
+    wn = torch.randn(dw["w_idx"].shape, generator=torch.Generator().manual_seed(6)).to(DEV)
+    scores, row_len, args = csa2.index_score(dw["q_idx"], wn, dw["k_codes"], dw["k_scales"],
+                                             dw["q_pos"], 1, None, w.block, st, want_args=True)
+    lens = torch.tensor([[100003], [40000], [w.topk + 1]], dtype=torch.int32, device=DEV)
+    row_len = torch.minimum(row_len, lens)
+    idx = csa2.topk(scores, w.topk, row_len, d_status=st, exact=args)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    qi_all, ww_all, _ = synth.gen_queries(w)
+    wn_np = wn.cpu().numpy()
+    for b in range(w.batch):
+        kc, ks = oracle.quant_mxfp4(f32(synth.gen_index_keys(w, b, qi_all[b], ww_all[b])))
+        L = int(row_len[b, 0])
+        pos = np.arange(L)
+        ex = _oracle_row_exact(w, b, 0, qi_all[b], wn_np[b], kc, ks, pos)
+        assert np.array_equal(idx[b, 0].cpu().numpy(), oracle.topk_exact(ex, pos, w.topk)), b
+
+
 def test_exact_order_negative_weights():
     # realistic scales with head weights of both signs: the row bound comes from the key
     # scale maxima; the selections equal the exact ones

@@ -528,6 +528,7 @@ def run_gpu(args):
     #      graph, L2 flushed between steps; the attention call alone is timed for both formats
     nv = None
     pages_cfg = None
+    fused_cfg = None
     if want_nv and graph is not None:
         nv_c, nv_s = dw["kv_codes_nv"], dw["kv_scales_nv"]
         aargs_nv = csa2.make_attn_args(dw["q_attn"], nv_c, nv_s, idx, dw["swa"], dw["swa_pos0"],
@@ -598,6 +599,34 @@ def run_gpu(args):
                      "ms_per_step": t_pc, "tokens_per_s": B * T / (t_pc * 1e-3), "launches": 5,
                      "calls": "RoPE + cache write (main KV, indexer K), SWA row write (MXFP8), indexer, "
                               "exact Top-512, attention"}
+        # the same step with the selection fused into the indexer (csa2_index_topk: its CTAs
+        # keep their scores on chip and write candidate lists; no score matrix)
+        iargs_f = csa2.make_index_args(dw["q_idx"], dw["w_idx"], dw["k_codes"], dw["k_scales"], dw["q_pos"],
+                                       w.ratio_m)
+        ws_f = torch.zeros(max(1, lib.csa2_index_topk_workspace_size(ctypes.byref(iargs_f), w.topk)),
+                           dtype=torch.uint8, device=dev)
+        idx_f = torch.empty_like(idx)
+        aargs_f = csa2.make_attn_args(dw["q_attn"], dw["kv_codes"], dw["kv_scales"], idx_f, dw["swa"],
+                                      dw["swa_pos0"], dw["q_pos"], None, w.window, dw.sm_scale, w.d_v)
+        out_f, lse_f = torch.empty_like(out), torch.empty_like(lse)
+
+        def step_fused():
+            csa2.csa2_rope_quant_fp4(cache_rows, st, jobs=cache_jobs)
+            csa2.csa2_index_topk(iargs_f, w.topk, idx_f, None, row_len, st, workspace=ws_f)
+            csa2.csa2_sparse_attn(aargs_f, out_f, lse_f, st, workspace=ws_attn)
+
+        for _ in range(args.warmup):
+            step_fused()
+        g_f = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_f):
+            step_fused()
+        t_f = timed(g_f)
+        if int(st.item()) != 0:
+            raise RuntimeError(f"device status {int(st.item())}")
+        fused_cfg = {"calls": "RoPE + cache write, csa2_index_topk (indexer CTAs keep their scores on chip "
+                              "and write candidate lists; a merge selects), attention",
+                     "ms_per_step": t_f, "tokens_per_s": B * T / (t_f * 1e-3), "launches": 4,
+                     "score_bytes_written": 0, "same_idx": bool(torch.equal(idx_f, idx))}
         row_nv = w.d_qk // 2 + w.d_qk // 16
         nv = {"format": "E2M1 + E4M3 per 16, no global scale (report §2.4.4)",
               "ms_per_step": t_nv, "tokens_per_s": B * T / (t_nv * 1e-3), "launches": launches_per_step,
@@ -657,6 +686,8 @@ def run_gpu(args):
         line["main_kv_e4m3_16"] = nv
     if pages_cfg is not None:
         line["pages_cache_config"] = pages_cfg
+    if fused_cfg is not None:
+        line["fused_selection"] = fused_cfg
     if not args.no_prefill:
         line["prefill_indexer"] = prefill_indexer(dev, line["clocks"].get("sm_mhz"))
     if not args.no_indexer_rows:

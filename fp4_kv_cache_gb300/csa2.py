@@ -122,6 +122,10 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
             lib.csa2_topk_workspace_size.argtypes = [_I64, _I64, _I32, IA]
             lib.csa2_topk.restype = S
             lib.csa2_topk.argtypes = [_P, _I64, _I64, _P, _P, _P, _I32, IA, _I32, _P, _P, _P, sz, _P, _P]
+            lib.csa2_index_topk_workspace_size.restype = sz
+            lib.csa2_index_topk_workspace_size.argtypes = [ctypes.POINTER(IndexArgs), _I32]
+            lib.csa2_index_topk.restype = S
+            lib.csa2_index_topk.argtypes = [ctypes.POINTER(IndexArgs), _I32, _P, _P, _P, _P, sz, _P, _P]
             lib.csa2_block_candidates_workspace_size.restype = sz
             lib.csa2_block_candidates_workspace_size.argtypes = [_I64, _I64, _I32, _I32, IA]
             lib.csa2_block_candidates.restype = S
@@ -382,6 +386,16 @@ def csa2_topk(scores: torch.Tensor, k: int, idx: torch.Tensor, row_len=None, poo
                                       _ptr(out_scores), ws, wsb, _ptr(d_status), _stream(stream)))
 
 
+def csa2_index_topk(args: IndexArgs, k: int, idx: torch.Tensor, out_scores=None, row_len=None,
+                    d_status=None, stream=None, workspace=None):
+    """The indexer and the exact Top-K in one call (no score matrix on the decode path)."""
+    lib = load()
+    need = lib.csa2_index_topk_workspace_size(ctypes.byref(args), k)
+    ws, wsb = _ws(need, idx.device, workspace, stream)
+    _check("csa2_index_topk", lib.csa2_index_topk(ctypes.byref(args), k, _ptr(idx), _ptr(out_scores),
+                                                  _ptr(row_len), ws, wsb, _ptr(d_status), _stream(stream)))
+
+
 def csa2_block_candidates(scores: torch.Tensor, nb: int, block_ids: torch.Tensor, row_len=None,
                           block: int = 8, d_status=None, stream=None, workspace=None,
                           exact: Optional[IndexArgs] = None):
@@ -479,6 +493,19 @@ def topk(scores, k=512, row_len=None, pool_blocks=None, block=8, want_scores=Fal
     csa2_topk(scores, k, idx, row_len, pool_blocks, block, out_s, d_status, stream,
               group_max=group_max, exact=exact)
     return (idx, out_s) if want_scores else idx
+
+
+def index_topk(q, w, k_codes, k_scales, k=512, q_pos=None, ratio_m=1, pool_blocks=None, block=8,
+               d_status=None, stream=None, want_scores=False):
+    """-> (idx int32 [B, T, k], row_len int32 [B, T]) [+ their float32 scores]: the exact
+    Top-K of the indexer scores from one csa2_index_topk call."""
+    B, T = q.shape[:2]
+    idx = torch.empty((B, T, k), dtype=torch.int32, device=q.device)
+    row_len = torch.empty((B, T), dtype=torch.int32, device=q.device)
+    out_s = torch.empty((B, T, k), dtype=torch.float32, device=q.device) if want_scores else None
+    args = make_index_args(q, w, k_codes, k_scales, q_pos, ratio_m, pool_blocks, block)
+    csa2_index_topk(args, k, idx, out_s, row_len, d_status, stream)
+    return (idx, row_len, out_s) if want_scores else (idx, row_len)
 
 
 def block_candidates(scores, nb=2048, row_len=None, block=8, d_status=None, stream=None, exact=None):

@@ -305,6 +305,84 @@ csa2_status csa2_topk(const float *scores, int64_t rows, int64_t n, const int32_
                                  out_scores, ws, d_status, as_stream(stream), exact));
 }
 
+// csa2_index_topk workspace.  Tensor-core FULL mode with one query per CTA (the decode
+// shape): the indexer's tile counters | candidate keys | positions | list meta | band slots.
+// Otherwise: the indexer's workspace | scores | row lengths | csa2_topk's workspace.
+namespace {
+struct FusedLayout {
+    bool fused;
+    int64_t ctas, cap;            // fused: lists per row, entries per list
+    size_t idx_ws, a, b, c, d, total;
+};
+FusedLayout fused_layout(const csa2_index_args &a, int32_t k)
+{
+    FusedLayout L = {};
+    const int64_t rows = (int64_t)a.batch * a.n_q;
+    L.idx_ws = index_score_ws_bytes(a);
+    L.fused = index_tc_fusable(a);
+    size_t off = (L.idx_ws + 255) & ~(size_t)255;
+    if (L.fused) {
+        int stages;
+        index_fused_shape(a, L.ctas, stages);
+        L.cap = (int64_t)stages * 256;
+        const size_t lst = (size_t)rows * L.ctas * L.cap * sizeof(uint32_t);
+        L.a = off;
+        L.b = L.a + ((lst + 255) & ~(size_t)255);
+        L.c = L.b + ((lst + 255) & ~(size_t)255);
+        L.d = L.c + (((size_t)rows * L.ctas * 4 * sizeof(uint32_t) + 255) & ~(size_t)255);
+        L.total = L.d + topk_lists_ws_bytes(rows);
+    } else {
+        const int64_t n = index_candidates(&a);
+        L.a = off;                                          // scores
+        L.b = L.a + (((size_t)rows * n * sizeof(float) + 255) & ~(size_t)255);   // row lengths
+        L.c = L.b + (((size_t)rows * sizeof(int32_t) + 255) & ~(size_t)255);     // Top-K workspace
+        L.total = L.c + topk_ws_bytes(rows, n, k, true);
+    }
+    return L;
+}
+} // namespace
+
+size_t csa2_index_topk_workspace_size(const csa2_index_args *a, int32_t k)
+{
+    if (!index_args_ok(a) || k < 0) return 0;
+    return fused_layout(*a, k).total;
+}
+
+csa2_status csa2_index_topk(const csa2_index_args *a, int32_t k, int32_t *idx, float *out_scores,
+                            int32_t *row_len, void *ws, size_t ws_bytes, uint32_t *d_status,
+                            csa2_stream stream)
+{
+    if (!index_args_ok(a) || k < 0 || !aligned(a->q, 16)) return CSA2_ERR_INVALID_ARG;
+    const int64_t rows = (int64_t)a->batch * a->n_q;
+    if (rows == 0) return CSA2_OK;
+    if (k > 0 && !idx) return CSA2_ERR_INVALID_ARG;
+    const FusedLayout L = fused_layout(*a, k);
+    if (ws_bytes < L.total) return CSA2_ERR_WORKSPACE;
+    if (!ws || !aligned(ws, 16)) return CSA2_ERR_INVALID_ARG;
+    char *w = static_cast<char *>(ws);
+    const cudaStream_t s = as_stream(stream);
+    uint32_t *tile_ctr = L.idx_ws ? reinterpret_cast<uint32_t *>(w) : nullptr;
+    if (L.fused) {
+        FusedOut fo;
+        fo.key = reinterpret_cast<uint32_t *>(w + L.a);
+        fo.pos = reinterpret_cast<int32_t *>(w + L.b);
+        fo.meta = reinterpret_cast<uint32_t *>(w + L.c);
+        fo.k = k > 0 ? k : 1;
+        cudaError_t e = launch_index_tc(*a, nullptr, row_len, tile_ctr, d_status, s, &fo);
+        if (e != cudaSuccess || k == 0) return from_cuda(e);
+        return from_cuda(launch_topk_lists(*a, k, fo.key, fo.pos, fo.meta, (int)L.ctas, L.cap, idx, out_scores,
+                                           w + L.d, d_status, s));
+    }
+    float *scores = reinterpret_cast<float *>(w + L.a);
+    int32_t *rl = row_len ? row_len : reinterpret_cast<int32_t *>(w + L.b);
+    cudaError_t e = launch_index_score(*a, scores, rl, tile_ctr, d_status, s);
+    if (e != cudaSuccess || k == 0) return from_cuda(e);
+    const int64_t n = index_candidates(a);
+    const bool pool = a->mode == CSA2_INDEX_POOL;
+    return from_cuda(launch_topk(scores, rows, n, rl, nullptr, pool ? a->pool_blocks : nullptr, a->block, k, idx,
+                                 out_scores, w + L.c, d_status, s, a));
+}
+
 size_t csa2_block_candidates_workspace_size(int64_t rows, int64_t n, int32_t block, int32_t nb,
                                             const csa2_index_args *exact)
 {

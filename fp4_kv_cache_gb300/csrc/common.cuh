@@ -149,6 +149,11 @@ __device__ __forceinline__ uint32_t score_key(float s)
     if (u == 0x80000000u) u = 0u;
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
+// The float a key stands for (the inverse of score_key on numbers).
+__device__ __forceinline__ float key_value(uint32_t key)
+{
+    return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
+}
 
 // ------------------------------------------------------------------ exact rounding
 // float32 round-to-nearest-even of sum_b I[b] * 2^E[b] (|I[b]| < 2^20, E in [-300, 260]).

@@ -314,4 +314,42 @@ __device__ __forceinline__ int compare_keys(uint32_t a, uint32_t b)
 }
 
 } // namespace exact
+
+// The row's error bound of the float32 scores as an affine function of the score,
+// e(x) = c1 max(x, 0) + c0 (see above); it holds for finite scores (a row with another
+// score gets no exact pass: the indexer has flagged CSA2_DEV_SCORE_RANGE).
+//   every w_h >= 0: A_t = s_t <= (s~_t + eta) / (1 - c), so e(x) = c (x + eta) / (1 - c) + eta;
+//   otherwise: one row-wide A from the key scale maxima, e = c A + eta.
+// Evaluated in float32 with every operation rounded outward (a float64 unit this slow has
+// no place in a per-row prologue); c1 = (H + 4) 2^-24 covers c / (1 - c) and that rounding,
+// c0 >= eta = 2^-140 (sum|w| + H) covers the subnormal terms.
+struct RowBound {
+    float c1, c0;
+    __device__ float e(float x) const { return __fmaf_ru(c1, x > 0.0f ? x : 0.0f, c0); }
+    // below lo(tau): out; above hi(tau): in (x - e(x) and x + e(x) both rise with x)
+    __device__ float lo(float x) const { return __fsub_rd(x, __fmul_ru(2.0f, e(x))); }
+    __device__ float hi(float x) const
+    {
+        const float ex = e(x);
+        return __fadd_ru(__fadd_ru(x, ex), e(__fmaf_ru(3.0f, ex, x)));
+    }
+};
+
+// The bound of a row whose head weights w[0..H) are all >= 0 (neg = false); with a negative
+// weight neg = true and the bound needs the key scale maxima (see csa2_topk).  The same
+// evaluation serves every kernel that cuts candidates by it, so their cuts agree.
+__device__ __forceinline__ RowBound row_bound_nonneg(const float *w, int H, bool &neg)
+{
+    float sumw = 0.0f;
+    neg = false;
+    for (int h = 0; h < H; ++h) {
+        sumw = __fadd_ru(sumw, fabsf(w[h]));
+        neg |= w[h] < 0.0f;
+    }
+    RowBound rb;
+    rb.c1 = (float)(H + 4) * 0x1p-24f;
+    rb.c0 = __fmul_ru(__fadd_ru(sumw, (float)H), 0x1p-140f);
+    return rb;
+}
+
 } // namespace csa2

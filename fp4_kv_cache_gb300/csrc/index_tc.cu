@@ -34,6 +34,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "exact.cuh"
 #include "tc_util.cuh"
 
 namespace csa2 {
@@ -87,11 +88,20 @@ struct TcParams {
     uint32_t *tile_ctr;      // [units]: claims from each unit's shared tiles (zero at launch)
     uint32_t *tile_done;     // [units]: CTAs of the unit done (zero at launch)
     uint32_t *d_status;
+    // fused selection (one query per CTA, FULL mode): the CTA keeps its scores' selection
+    // keys on chip and writes a candidate list instead of scores (see fused_list)
+    uint32_t *lst_key;       // [rows, CTAs per row, lst_cap] keys (null: write scores)
+    int32_t *lst_pos;        // [rows, CTAs per row, lst_cap] positions
+    uint32_t *lst_meta;      // [rows, CTAs per row, 4]: count, K-th key (0: K or fewer), non-finite
+    int32_t lst_k;           // K
+    int32_t lst_stages;      // stages per CTA (lst_cap = lst_stages x span)
 };
 
+constexpr int kFuseStages = 32;        // fused selection: stages a CTA keeps on chip
 template <int QG>
 struct TcSmem {
     static constexpr int kStages = Cfg<QG>::kStages, kAcc = Cfg<QG>::kAcc, kSpan = kSpanOf<QG>;
+    static constexpr int kFuseKeys = QG == 1 ? kFuseStages * kSpanOf<1> : 1;
     uint8_t a[kStages][kSpan * kRowBytes];     // K codes, 64-byte swizzle, 1024-aligned
     uint8_t b[QG * kNPad * kRowBytes];         // q codes (row = query x 32 + head), same layout
     uint32_t sfa[kStages][kSpan];              // scale-factor atoms of the K tiles (one per block)
@@ -109,6 +119,7 @@ struct TcSmem {
     uint32_t tmem_base;
     int abort_flag, bad;
     int q_span[QG], q_min[QG], q_max[QG];
+    uint32_t fkeys[kFuseKeys];                 // fused selection: the CTA's keys in position order
 };
 
 // instruction descriptor, kind::mxf4: A = B = E2M1 (1), UE8M0 scales, K-major A and B,
@@ -266,6 +277,166 @@ __device__ __noinline__ void recheck_stage(const TcParams &P, const TcSmem<QG> &
 // Registers: with QG = 1, two resident CTAs of 320 threads need every warp within its
 // sub-partition's share of the register file (20 warps over 4 sub-partitions: at most 102
 // registers a thread, 96 after rounding); the launch bound makes the compiler keep to it.
+// Block-wide exclusive prefix sum of one value per thread (any multiple of 32 threads).
+__device__ __forceinline__ uint32_t fused_scan(uint32_t v, uint32_t *s_warp, uint32_t &total)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    uint32_t incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const uint32_t w = lane < nw ? s_warp[lane] : 0u;
+        uint32_t wi = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t t = __shfl_up_sync(0xffffffffu, wi, o);
+            if (lane >= o) wi += t;
+        }
+        s_warp[lane] = wi - w;
+        if (lane == 31) s_warp[32] = wi;
+    }
+    __syncthreads();
+    const uint32_t r = s_warp[warp] + incl - v;
+    total = s_warp[32];
+    __syncthreads();
+    return r;
+}
+
+// Fused selection at the end of a CTA: its V selection keys (positions pos0 .. pos0 + V - 1 of
+// `row`, in S.fkeys) become its candidate list, in position order.  With K or fewer keys the
+// list is all of them; otherwise tau is a lower bound of the K-th largest key (its top 22
+// bits) and the list holds every key whose score is at least lo(tau), lo as in the exact
+// Top-K's band (report §2.3 Top-K by the exact score): the row's K-th score is at least
+// tau, so every candidate of the row's exact top K and of its band is here.  A row with a
+// negative head weight (its bound needs the whole sequence's key scales) keeps every key; a
+// CTA that met a non-finite score keeps the keys >= tau and says so (its row then goes by
+// the float order, for which those suffice).
+template <int QG>
+__device__ __noinline__ void fused_list(const TcParams &P, TcSmem<QG> &S, int64_t row, int64_t pos0, int V)
+{
+    const int tid = threadIdx.x, lane = tid & 31;
+    constexpr int NT = kThreadsOf<QG>;
+    __shared__ uint32_t s_pick[2], s_warp[33];
+    const uint32_t *keys = S.fkeys;
+    const int64_t slot = row * gridDim.x + blockIdx.x;
+    uint32_t *meta = P.lst_meta + slot * 4;
+    const int64_t lbase = slot * (int64_t)P.lst_stages * kSpanOf<QG>;
+    const uint32_t K = (uint32_t)P.lst_k;
+    bool nf = false;
+    for (int i = tid; i < V; i += NT) {
+        const uint32_t k = keys[i];
+        nf |= k >= 0xff800000u || k <= 0x007fffffu;
+    }
+    nf = __syncthreads_or(nf) != 0;
+    uint32_t tau = 0u, lo_key = 0u;
+    if ((uint32_t)V > K) {
+        // tau: the top 22 bits of the K-th largest key, its low bits zero -- a lower bound,
+        // enough to cut the list (lo rises with its argument): two digit passes of 11 bits,
+        // one atomic per distinct digit and warp, in the stage buffers (free now)
+        uint32_t *hist = reinterpret_cast<uint32_t *>(&S.a[0][0]);
+        uint32_t *coarse = hist + 2048;
+        uint32_t prefix = 0u, mask = 0u, remaining = K;
+#pragma unroll 1
+        for (int pass = 0; pass < 2; ++pass) {
+            const int shift = pass == 0 ? 21 : 10;
+            for (int i = tid; i < 2048 + 64; i += NT) hist[i] = 0u;
+            __syncthreads();
+            for (int base = 0; base < V; base += NT) {
+                const int i = base + tid;
+                uint32_t key = 0u;
+                bool act = false;
+                if (i < V) {
+                    key = keys[i];
+                    act = (key & mask) == prefix;
+                }
+                const uint32_t am = __ballot_sync(0xffffffffu, act);
+                if (act) {
+                    const uint32_t digit = (key >> shift) & 2047u;
+                    const uint32_t peers = __match_any_sync(am, digit);
+                    if (lane == __ffs(peers) - 1) {
+                        atomicAdd(&hist[digit], (uint32_t)__popc(peers));
+                        atomicAdd(&coarse[digit >> 5], (uint32_t)__popc(peers));
+                    }
+                }
+            }
+            __syncthreads();
+            if (tid < 32) {                      // the digit, from the top: coarse bins, then 32 bins
+                const uint32_t c0 = coarse[63 - lane], c1 = coarse[31 - lane];
+                uint32_t i0 = c0, i1 = c1;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const uint32_t x = __shfl_up_sync(0xffffffffu, i0, o), y = __shfl_up_sync(0xffffffffu, i1, o);
+                    if (lane >= o) { i0 += x; i1 += y; }
+                }
+                i1 += __shfl_sync(0xffffffffu, i0, 31);
+                const uint32_t b0 = __ballot_sync(0xffffffffu, i0 >= remaining);
+                const uint32_t b1 = __ballot_sync(0xffffffffu, i1 >= remaining);
+                int cb;
+                uint32_t above;
+                if (b0) {
+                    const int L = __ffs(b0) - 1;
+                    cb = 63 - L;
+                    above = __shfl_sync(0xffffffffu, i0 - c0, L);
+                } else {
+                    const int L = b1 ? __ffs(b1) - 1 : 31;
+                    cb = 31 - L;
+                    above = __shfl_sync(0xffffffffu, i1 - c1, L);
+                }
+                const uint32_t f = hist[cb * 32 + 31 - lane];
+                uint32_t fi = f;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const uint32_t x = __shfl_up_sync(0xffffffffu, fi, o);
+                    if (lane >= o) fi += x;
+                }
+                fi += above;
+                const uint32_t bf = __ballot_sync(0xffffffffu, fi >= remaining);
+                const int Lf = bf ? __ffs(bf) - 1 : 31;
+                const uint32_t fabove = __shfl_sync(0xffffffffu, fi - f, Lf);
+                if (lane == 0) {
+                    s_pick[0] = (uint32_t)(cb * 32 + 31 - Lf);
+                    s_pick[1] = remaining - fabove;
+                }
+            }
+            __syncthreads();
+            prefix |= s_pick[0] << shift;
+            mask |= 2047u << shift;
+            remaining = s_pick[1];
+            __syncthreads();                     // s_pick is read before the next pass writes it
+        }
+        tau = prefix;
+        bool neg;
+        const RowBound rb = row_bound_nonneg(S.w[0], P.H, neg);
+        lo_key = neg ? 0u : (nf ? tau : score_key(rb.lo(key_value(tau))));
+    }
+    // the list: keys >= lo_key, each thread a contiguous run of positions
+    const int run = (V + NT - 1) / NT;
+    const int i0 = min(tid * run, V), i1 = min(i0 + run, V);
+    uint32_t cnt = 0;
+    for (int i = i0; i < i1; ++i) cnt += keys[i] >= lo_key;
+    uint32_t total;
+    uint32_t o = fused_scan(cnt, s_warp, total);
+    for (int i = i0; i < i1; ++i) {
+        const uint32_t key = keys[i];
+        if (key >= lo_key) {
+            P.lst_key[lbase + o] = key;
+            P.lst_pos[lbase + o] = (int32_t)(pos0 + i);
+            ++o;
+        }
+    }
+    if (tid == 0) {
+        meta[0] = total;
+        meta[1] = tau;
+        meta[2] = nf ? 1u : 0u;
+        meta[3] = 0u;
+    }
+}
+
 template <int QG>
 __global__ void __launch_bounds__(kThreadsOf<QG>, Cfg<QG>::kCtasPerSm)
 index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P)
@@ -356,7 +527,9 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
     // epilogue.
     const int ntr = len > 0 ? (int)((len + kSpan - 1) / kSpan) : 0;
     const int CT = (int)gridDim.x;
-    const int R = ntr / CT > 2 ? ntr / CT - 2 : 0;
+    // fused selection: CTA c takes the fixed run [c F, c F + F) of lst_stages stages
+    const bool fused = QG == 1 && P.lst_key != nullptr;
+    const int R = fused ? P.lst_stages : (ntr / CT > 2 ? ntr / CT - 2 : 0);
     const int64_t c1 = len;
     const uint32_t tmem = S.tmem_base;
     const int64_t kbase = b * P.n_keys;
@@ -399,7 +572,7 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
         };
         int issued = 0;
         uint32_t claim = 0;                       // lane 0: the next claim from the counter
-        if (lane == 0 && R == 0) claim = atomicAdd(&P.tile_ctr[unit], 1u);
+        if (lane == 0 && R == 0 && !fused) claim = atomicAdd(&P.tile_ctr[unit], 1u);
         for (int i = 0;; ++i) {
             const int s = i % kStages;
             const uint32_t ph = (uint32_t)(i / kStages) & 1u;
@@ -409,7 +582,9 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
             }
             if (C::kDeferred && i >= kStages && !S.abort_flag) check_stage(s, S.tile[s]);   // its previous tile
             int t = 0;
-            if (i < R) {
+            if (fused) {
+                t = i < R ? (int)blockIdx.x * R + i : ntr;
+            } else if (i < R) {
                 t = (int)blockIdx.x * R + i;
                 if (lane == 0 && i == R - 1) claim = atomicAdd(&P.tile_ctr[unit], 1u);
             } else {
@@ -785,11 +960,12 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
                                              qi, H);
                 }
                 if (valid) {
-                    P.scores[(row0 + qi) * P.n_cand + cand] = sc;
                     key = score_key(sc);
                     out_of_range |= !(fabsf(sc) <= 3.4028234663852886e38f);
+                    if (fused) S.fkeys[(t - (int)blockIdx.x * R) * kSpan + m] = key;
+                    else P.scores[(row0 + qi) * P.n_cand + cand] = sc;
                 }
-                if (P.gmax) {            // this warp's 32 candidates are one aligned group
+                if (P.gmax && !fused) {  // this warp's 32 candidates are one aligned group
                     const uint32_t gk = __reduce_max_sync(0xffffffffu, key);
                     if (lane == 0 && g0 < qlen[u]) P.gmax[(row0 + qi) * P.G + (g0 >> 5)] = gk;
                 }
@@ -824,6 +1000,14 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
     if (warp == 1) {
         tc::tc_fence_after();
         tc::tmem_dealloc(tmem, C::kTmemCols);
+    }
+    if constexpr (QG == 1) {
+        if (fused && !S.abort_flag) {
+            const int64_t pos0 = (int64_t)blockIdx.x * R * kSpan;
+            int64_t v = S.qlen[0] - pos0;
+            v = v < 0 ? 0 : (v > (int64_t)R * kSpan ? (int64_t)R * kSpan : v);
+            fused_list<QG>(P, S, row0, pos0, (int)v);
+        }
     }
     if (tid == 0) {
         if (S.abort_flag) dev_flag(P.d_status, CSA2_DEV_TIMEOUT);
@@ -908,11 +1092,30 @@ int64_t index_tc_ctas_per_row(const csa2_index_args &a)
                    : tc_splits(units, n_cand, Cfg<1>::kCtasPerSm, kSpanOf<1>);
 }
 
+// Fused selection (csa2_index_topk): one query per CTA in FULL mode, each CTA a fixed run
+// of at most kFuseStages stages, so the row takes at least stages / kFuseStages CTAs.
+bool index_tc_fusable(const csa2_index_args &a)
+{
+    return index_tc_eligible(a) && a.mode != CSA2_INDEX_POOL && tc_query_group(a) == 1;
+}
+
+void index_fused_shape(const csa2_index_args &a, int64_t &ctas, int &stages)
+{
+    const int64_t ntr = ((int64_t)a.n_keys + kSpanOf<1> - 1) / kSpanOf<1>;
+    int64_t c = index_tc_ctas_per_row(a);
+    const int64_t need = (ntr + kFuseStages - 1) / kFuseStages;
+    if (c < need) c = need;
+    if (c < 1) c = 1;
+    stages = (int)(ntr > 0 ? (ntr + c - 1) / c : 1);
+    if (stages < 1) stages = 1;
+    ctas = ntr > 0 ? (ntr + stages - 1) / stages : 1;
+}
+
 cudaError_t launch_index_tc(const csa2_index_args &a, float *scores, int32_t *row_len,
-                            uint32_t *tile_ctr, uint32_t *d_status, cudaStream_t s)
+                            uint32_t *tile_ctr, uint32_t *d_status, cudaStream_t s, const FusedOut *fo)
 {
     const int qg = tc_query_group(a);
-    const int64_t splits = index_tc_ctas_per_row(a);
+    int64_t splits = index_tc_ctas_per_row(a);
     const int64_t rows = (int64_t)a.batch * a.n_q;
     const int64_t units = (int64_t)a.batch * ((a.n_q + qg - 1) / qg);
     TcParams P;
@@ -937,6 +1140,25 @@ cudaError_t launch_index_tc(const csa2_index_args &a, float *scores, int32_t *ro
     P.tile_ctr = tile_ctr;
     P.tile_done = tile_ctr + rows;
     P.d_status = d_status;
+    P.lst_key = nullptr;
+    P.lst_pos = nullptr;
+    P.lst_meta = nullptr;
+    P.lst_k = 0;
+    P.lst_stages = 0;
+    if (fo) {                                  // no scores, no group maxima: candidate lists
+        if (qg != 1 || P.pool_mode) return cudaErrorInvalidValue;
+        int64_t ctas;
+        int stages;
+        index_fused_shape(a, ctas, stages);
+        splits = ctas;
+        P.scores = nullptr;
+        P.gmax = nullptr;
+        P.lst_key = fo->key;
+        P.lst_pos = fo->pos;
+        P.lst_meta = fo->meta;
+        P.lst_k = fo->k;
+        P.lst_stages = stages;
+    }
 
     CUtensorMap map;
     cuuint64_t dims[2] = {(cuuint64_t)kRowBytes, (cuuint64_t)((int64_t)a.batch * a.n_keys)};

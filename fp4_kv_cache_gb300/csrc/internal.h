@@ -61,8 +61,26 @@ cudaError_t launch_index_exact(const csa2_index_args &a, float *scores, int32_t 
                                uint32_t *d_status, cudaStream_t s);
 bool index_tc_eligible(const csa2_index_args &a);
 int64_t index_tc_ctas_per_row(const csa2_index_args &a);
+// Candidate lists of the fused selection (csa2_index_topk): per row, `ctas` lists of
+// stages x 256 entries (key, position) in position order, and per list (count, K-th key,
+// non-finite flag, 0).
+struct FusedOut {
+    uint32_t *key;
+    int32_t *pos;
+    uint32_t *meta;
+    int32_t k;
+};
+bool index_tc_fusable(const csa2_index_args &a);
+void index_fused_shape(const csa2_index_args &a, int64_t &ctas, int &stages);
 cudaError_t launch_index_tc(const csa2_index_args &a, float *scores, int32_t *row_len,
-                            uint32_t *tile_ctr, uint32_t *d_status, cudaStream_t s);
+                            uint32_t *tile_ctr, uint32_t *d_status, cudaStream_t s,
+                            const FusedOut *fo = nullptr);
+// The exact Top-K of every row from its candidate lists (see TopkLists in topk.cu);
+// ws: topk_lists_ws_bytes(rows).
+size_t topk_lists_ws_bytes(int64_t rows);
+cudaError_t launch_topk_lists(const csa2_index_args &ex, int32_t k, const uint32_t *key, const int32_t *pos,
+                              const uint32_t *meta, int n_lists, int64_t cap, int32_t *idx, float *out_scores,
+                              void *ws, uint32_t *d_status, cudaStream_t s);
 
 // Top-K over rows of float scores (see csa2_topk).  ws: topk_ws_bytes(rows, n, k, ex != 0).
 // ex != NULL: exact order for the scores of csa2_index_score(*ex); candidates are positions

@@ -266,8 +266,9 @@ __device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v, int lane)
     }
     return v;
 }
-__device__ __forceinline__ uint32_t g_threshold(const uint32_t *keys, int n, uint32_t k, GSmem &S,
-                                             uint32_t &need, int passes)
+template <class KeyAt>
+__device__ __forceinline__ uint32_t g_threshold_at(KeyAt key_at, int n, uint32_t k, GSmem &S, uint32_t &need,
+                                                int passes)
 {
     const int tid = threadIdx.x, lane = tid & 31;
     uint32_t prefix = 0, mask = 0, remaining = k;
@@ -287,7 +288,7 @@ __device__ __forceinline__ uint32_t g_threshold(const uint32_t *keys, int n, uin
             uint32_t key = 0;
             bool act = false;
             if (i < n) {
-                key = keys[i];
+                key = key_at(i);
                 act = (key & mask) == prefix;
             }
             const uint32_t am = __ballot_sync(0xffffffffu, act);
@@ -339,6 +340,11 @@ __device__ __forceinline__ uint32_t g_threshold(const uint32_t *keys, int n, uin
     need = remaining;
     return prefix;
 }
+__device__ __forceinline__ uint32_t g_threshold(const uint32_t *keys, int n, uint32_t k, GSmem &S,
+                                             uint32_t &need, int passes)
+{
+    return g_threshold_at([keys](int i) { return keys[i]; }, n, k, S, need, passes);
+}
 
 // ------------------------------------------------------------------ exact order (csa2_topk and
 // csa2_block_candidates with an exact context)
@@ -373,11 +379,6 @@ struct ExactArgs {
 };
 constexpr int kBandCap = CSA2_EXACT_BAND_CAP;
 static_assert(kBandCap <= 2 * kGThreads, "two band entries per thread at most");
-
-__device__ __forceinline__ float key_value(uint32_t key)
-{
-    return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
-}
 
 // Block-wide min and max of one value per thread (all threads call; ends with a barrier).
 __device__ __forceinline__ void block_minmax(uint32_t vmin, uint32_t vmax, uint32_t *s_red, uint32_t &mn, uint32_t &mx)
@@ -420,43 +421,14 @@ __device__ __noinline__ uint32_t key_scale_max(const uint8_t *ks, int64_t n_keys
     return t;
 }
 
-// The row's error bound of the float32 scores as an affine function of the score,
-// e(x) = c1 max(x, 0) + c0 (see above); it holds for finite scores (a row with another
-// score gets no exact pass: the indexer has flagged CSA2_DEV_SCORE_RANGE).
-//   every w_h >= 0: A_t = s_t <= (s~_t + eta) / (1 - c), so e(x) = c (x + eta) / (1 - c) + eta;
-//   otherwise: one row-wide A from the key scale maxima, e = c A + eta.
-// Evaluated in float32 with every operation rounded outward (a float64 unit this slow has
-// no place in a per-row prologue); c1 = (H + 4) 2^-24 covers c / (1 - c) and that rounding,
-// c0 >= eta = 2^-140 (sum|w| + H) covers the subnormal terms.
-struct RowBound {
-    float c1, c0;
-    __device__ float e(float x) const { return __fmaf_ru(c1, x > 0.0f ? x : 0.0f, c0); }
-    // below lo(tau): out; above hi(tau): in (x - e(x) and x + e(x) both rise with x)
-    __device__ float lo(float x) const { return __fsub_rd(x, __fmul_ru(2.0f, e(x))); }
-    __device__ float hi(float x) const
-    {
-        const float ex = e(x);
-        return __fadd_ru(__fadd_ru(x, ex), e(__fmaf_ru(3.0f, ex, x)));
-    }
-};
-
 __device__ __noinline__ RowBound row_bound(const exact::QuantQuery &Q, const ExactArgs &X, int64_t seq,
                                            uint32_t *s_red)
 {
-    RowBound rb{0.0f, -1.0f};
-    float sumw = 0.0f;
-    bool neg = false;
-    for (int h = 0; h < X.H; ++h) {
-        sumw = __fadd_ru(sumw, fabsf(Q.w[h]));
-        neg |= Q.w[h] < 0.0f;
-    }
-    const float c = (float)(X.H + 4) * 0x1p-24f;
-    const float eta = __fmul_ru(__fadd_ru(sumw, (float)X.H), 0x1p-140f);
-    if (!neg) {
-        rb.c1 = c;
-        rb.c0 = eta;
-        return rb;
-    }
+    bool neg;
+    RowBound rb = row_bound_nonneg(Q.w, X.H, neg);
+    if (!neg) return rb;
+    const float c = rb.c1;
+    const float eta = rb.c0;
     const int nb = X.d / 32;
     const uint32_t km = key_scale_max(X.ks + seq * X.n_keys * nb, X.n_keys, nb, s_red);
     float A = 0.0f;
@@ -765,12 +737,26 @@ __device__ __noinline__ void band_exact(const exact::QuantQuery &Q, const ExactA
     select_band(bk, exact::kLimbs, (int)n_band, take, s_state, s_act, s_val, S, s_red);
 }
 
-template <bool EXACT, int D>
+// Candidate lists (csa2_index_topk): the scoring kernel's CTAs of a row each wrote a list
+// of (key, position) in position order, with the list's K-th key (0 when it holds K or
+// fewer: then it holds them all) and whether it met a non-finite score.  Each list holds
+// every entry at or above lo(its K-th key), so the row's exact top K and its band are in
+// their union; the row's K-th score is at least the largest list K-th key.
+struct TopkLists {
+    int n_lists;                   // lists per row (in position order)
+    int64_t cap;                   // entries per list
+    const uint32_t *key;           // [rows, n_lists, cap]
+    const int32_t *pos;            // [rows, n_lists, cap]
+    const uint32_t *meta;          // [rows, n_lists, 4]: count, K-th key, non-finite, 0
+};
+constexpr int kMaxLists = 1024;
+
+template <bool EXACT, int D, bool LISTS>
 __global__ void __launch_bounds__(kGThreads, 1)
 topk_gmax_kernel(const float *__restrict__ scores, int64_t n, int64_t rows, const int32_t *__restrict__ row_len,
                  const int32_t *__restrict__ pool, int32_t block, int32_t k, int32_t *__restrict__ idx,
                  float *__restrict__ out_scores, const uint32_t *__restrict__ gkeys, int32_t gs, int64_t G,
-                 const ExactArgs X)
+                 const ExactArgs X, const TopkLists Ls)
 {
     // shared memory: the candidate-group list (later the exact band), then the group keys,
     // whose space the candidates' keys and positions take once the list is made
@@ -783,6 +769,8 @@ topk_gmax_kernel(const float *__restrict__ scores, int64_t n, int64_t rows, cons
     __shared__ GSmem S;
     __shared__ uint32_t s_red[64];
     __shared__ exact::QuantQuery QQ;                       // exact order: the row's query
+    __shared__ uint32_t s_lpre[LISTS ? kMaxLists + 1 : 1];   // lists: offsets of the row's lists
+    __shared__ uint32_t s_tmax;                           // lists: the largest list K-th key
     const int tid = threadIdx.x;
     // exact order: the first row's query and error bound come from inputs the kernel before
     // does not write (csa2_topk), so they are prepared before the dependency wait
@@ -794,7 +782,7 @@ topk_gmax_kernel(const float *__restrict__ scores, int64_t n, int64_t rows, cons
             rb_first = row_bound(QQ, X, r / X.n_q, s_red);
         }
     }
-    pdl_wait();                                            // scores come from the kernel before
+    pdl_wait();                                            // scores / lists come from the kernel before
     pdl_allow_dependents();
 #pragma unroll 1
     for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
@@ -806,135 +794,276 @@ topk_gmax_kernel(const float *__restrict__ scores, int64_t n, int64_t rows, cons
     int32_t *out = idx + row * (int64_t)k;
     float *out_s = out_scores ? out_scores + row * (int64_t)k : nullptr;
 
-    if (len <= k) {                                        // everything competes and wins
+    if (!LISTS && len <= k) {                              // everything competes and wins
         for (int64_t i = tid; i < k; i += kGThreads) {
             out[i] = i < len ? (int32_t)cand_pos(pool_row, block, i) : -1;
             if (out_s) out_s[i] = i < len ? s[i] : 0.0f;
         }
         continue;
     }
-    const int ng = (int)((len + gs - 1) / gs);             // <= kMaxGroups
-    const uint32_t *gk = s_gk;
-    bool nonfinite = false;                                 // a group maximum of +-inf
-    for (int g = tid; g < ng; g += kGThreads) {
-        const uint32_t v = gkeys[row * G + g];
-        s_gk[g] = v;
-        nonfinite |= v >= 0xff800000u || v <= 0x007fffffu;
-    }
-    nonfinite = __syncthreads_or(nonfinite) != 0;
-    // exact order: the row's error bound of the float32 scores (c0 < 0: none made)
-    RowBound rb{0.0f, -1.0f};
-    int64_t seq = 0;
-    if constexpr (EXACT) {
-        seq = row / X.n_q;
-        if (row == (int64_t)blockIdx.x) {
-            rb = rb_first;
-        } else {
-            exact::quantise_query(QQ, X.q + row * (int64_t)X.H * D, X.w + row * (int64_t)X.H, X.H, D);
-            rb = row_bound(QQ, X, seq, s_red);
-        }
-        if (nonfinite) rb.c0 = -1.0f;
-    }
-    const bool exact_row = EXACT && rb.c0 >= 0.0f;
-    // a lower bound of the k-th largest group key is enough to keep every top-k element
-    // (the groups above the bound are a superset of those above the exact key); in exact
-    // order the bound is lowered to lo() of it, so the whole band is gathered
-    uint32_t need0;
-    uint32_t tau0 = ng > k ? g_threshold(gk, ng, (uint32_t)k, S, need0, 2) : 0u;
-    if (exact_row && tau0 != 0u) tau0 = score_key(rb.lo(key_value(tau0)));
-
-    // candidate groups (key >= tau0), listed in s_g in ascending order: thread t owns the
-    // run [t*run, (t+1)*run)
-    const int run = (ng + kGThreads - 1) / kGThreads;        // <= 32
-    const int r0 = min(tid * run, ng), r1 = min(r0 + run, ng);
-    uint32_t mine = 0;                                      // bit j: group r0+j is a candidate
-    for (int i = r0; i < r1; ++i) mine |= (gk[i] >= tau0 ? 1u : 0u) << (i - r0);
-    uint32_t n_cg;
-    const uint32_t at = block_excl_count_sum((uint32_t)__popc(mine), S.warp, n_cg);
-    if (n_cg > (uint32_t)kListCap) {                        // too many to list on chip
-        radix_select_row(scores, n, row_len, pool, block, k, idx, out_scores, row);
-        if (EXACT && tid == 0) dev_flag(X.d_status, CSA2_DEV_BAND_LIMIT);
-        continue;
-    }
-    {
-        uint32_t o = at;
-        for (int i = r0; i < r1; ++i)
-            if ((mine >> (i - r0)) & 1u) s_g[o++] = (uint32_t)i;
-    }
-    __syncthreads();
-    // gather candidates, in position order: one thread per candidate group reads its
-    // scores (groups of 32 as eight 16-byte loads, all in flight at once) and keeps a bit
-    // mask of its elements >= tau0; after a scan of the counts it walks the mask in a
-    // rolled loop, reading each selected score again (the lines are in L1 by then).  This
-    // code runs once per row, so it is kept small.
-    const bool vec = gs == 32 && ((reinterpret_cast<uintptr_t>(s) & 15u) == 0);   // 16-byte rows
     uint32_t n_c = 0;
     bool overflow = false;
-#pragma unroll 1
-    for (uint32_t base = 0; base < n_cg; base += kGThreads) {
-        const uint32_t j = base + tid;
-        uint32_t sel = 0;                                  // groups of 32: bit e = element e
-        uint32_t cnt = 0;
-        int64_t g0 = 0;
-        if (j < n_cg) {
-            g0 = (int64_t)s_g[j] * gs;
-            if (vec && g0 + 32 <= n) {
-                float4 f[8];
-                const float4 *src = reinterpret_cast<const float4 *>(s + g0);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) f[e] = src[e];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    sel |= (uint32_t)(score_key(f[e].x) >= tau0) << (4 * e);
-                    sel |= (uint32_t)(score_key(f[e].y) >= tau0) << (4 * e + 1);
-                    sel |= (uint32_t)(score_key(f[e].z) >= tau0) << (4 * e + 2);
-                    sel |= (uint32_t)(score_key(f[e].w) >= tau0) << (4 * e + 3);
-                }
-                if (g0 + 32 > len) sel &= len > g0 ? (1u << (len - g0)) - 1u : 0u;
-                cnt = __popc(sel);
+    RowBound rb{0.0f, -1.0f};
+    int64_t seq = 0;
+    bool nonfinite = false;
+    if constexpr (LISTS) {
+        // ---- the row's lists: counts, the largest list K-th key, non-finite flags
+        const uint32_t *meta = Ls.meta + row * Ls.n_lists * 4;
+        uint32_t cnt = 0, tk = 0;
+        if (tid < Ls.n_lists) {
+            cnt = meta[tid * 4];
+            tk = meta[tid * 4 + 1];
+            nonfinite = meta[tid * 4 + 2] != 0u;
+        }
+        if (tid == 0) s_tmax = 0u;
+        nonfinite = __syncthreads_or(nonfinite) != 0;
+        if (tid < Ls.n_lists && tk) atomicMax(&s_tmax, tk);
+        uint32_t total;
+        const uint32_t pre = block_excl_count_sum(cnt, S.warp, total);
+        if (tid < Ls.n_lists) s_lpre[tid] = pre;
+        if (tid == 0) s_lpre[Ls.n_lists] = total;
+        __syncthreads();
+        if constexpr (EXACT) {
+            seq = row / X.n_q;
+            if (row == (int64_t)blockIdx.x) {
+                rb = rb_first;
             } else {
+                exact::quantise_query(QQ, X.q + row * (int64_t)X.H * D, X.w + row * (int64_t)X.H, X.H, D);
+                rb = row_bound(QQ, X, seq, s_red);
+            }
+            if (nonfinite) rb.c0 = -1.0f;
+        }
+        const bool ex_row = EXACT && rb.c0 >= 0.0f;
+        const uint32_t *lk = Ls.key + row * Ls.n_lists * Ls.cap;
+        const int32_t *lp = Ls.pos + row * Ls.n_lists * Ls.cap;
+        const int nls = Ls.n_lists;
+        const int64_t cap = Ls.cap;
+        const uint32_t *lpre = s_lpre;
+        // entry i of the row's lists, in list order (= position order)
+        auto list_at = [lpre, nls, cap](uint32_t i) -> int64_t {
+            int lo = 0, hi = nls;                           // the list c with lpre[c] <= i < lpre[c+1]
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (lpre[mid] <= i) lo = mid; else hi = mid;
+            }
+            return (int64_t)lo * cap + (i - lpre[lo]);
+        };
+        // entries at or above lo_key into shared memory, in list order; false: they do not
+        // fit.  Thread t reads entries 4t .. 4t + 3 of each round of 4,096.
+        auto load_lists = [&](uint32_t lo_key) -> bool {
+            n_c = 0;
 #pragma unroll 1
-                for (int e = 0; e < gs && g0 + e < len; ++e) cnt += score_key(s[g0 + e]) >= tau0;
+            for (uint32_t base = 0; base < total; base += 4 * kGThreads) {
+                const uint32_t i0 = base + 4u * tid;
+                uint32_t key[4];
+                int32_t cd[4];
+                uint32_t keep = 0;
+                if (i0 < total) {
+                    int64_t at = list_at(i0);
+                    int c = (int)(at / cap);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const uint32_t i = i0 + u;
+                        key[u] = 0u;
+                        cd[u] = 0;
+                        if (i < total) {
+                            while (i >= lpre[c + 1]) ++c;      // the next non-empty list
+                            at = (int64_t)c * cap + (i - lpre[c]);
+                            key[u] = lk[at];
+                            cd[u] = lp[at];
+                            keep |= (uint32_t)(key[u] >= lo_key) << u;
+                        }
+                    }
+                }
+                uint32_t tot;
+                uint32_t o = n_c + block_excl_count_sum((uint32_t)__popc(keep), S.warp, tot);
+                if (n_c + tot > (uint32_t)kCandCap) return false;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    if ((keep >> u) & 1u) {
+                        s_ck[o] = key[u];
+                        s_cp[o] = cd[u];
+                        ++o;
+                    }
+                }
+                n_c += tot;
+            }
+            return true;
+        };
+        // The row's K-th score is at least s_tmax, so the entries at or above lo(s_tmax) hold
+        // the row's candidates and band.  When those do not fit on chip (a list's own K-th
+        // key was a weak bound), the row's K-th float key is found over the lists where they
+        // are and the load repeated at lo() of it; if even that does not fit (more than
+        // kCandCap candidates tie with it), the row is selected in float order from the
+        // lists directly and CSA2_DEV_BAND_LIMIT is set.
+        const uint32_t tfl = s_tmax;
+        uint32_t lo_t = tfl == 0u ? 0u : (ex_row ? score_key(rb.lo(key_value(tfl))) : tfl);
+        if (!load_lists(lo_t)) {
+            uint32_t need_g;
+            const uint32_t tau_g = g_threshold_at([&](int i) { return lk[list_at((uint32_t)i)]; }, (int)total,
+                                                  (uint32_t)k, S, need_g, 3);
+            lo_t = ex_row ? score_key(rb.lo(key_value(tau_g))) : tau_g;
+            if (!load_lists(lo_t)) {
+                // float order straight from the lists: above tau_g, then the first need_g at it
+                uint32_t n_gt = 0, n_eq = 0;
+#pragma unroll 1
+                for (uint32_t base = 0; base < total; base += kGThreads) {
+                    const uint32_t i = base + tid;
+                    uint32_t key = 0u;
+                    int32_t ps = 0;
+                    if (i < total) {
+                        const int64_t at = list_at(i);
+                        key = lk[at];
+                        ps = lp[at];
+                    }
+                    uint32_t tg, te;
+                    const uint32_t og = block_excl_count(i < total && key > tau_g, S.warp, tg);
+                    const uint32_t oe = block_excl_count(i < total && key == tau_g, S.warp, te);
+                    bool sel = i < total && key > tau_g;
+                    if (i < total && key == tau_g) sel = n_eq + oe < need_g;
+                    if (sel) {
+                        const uint32_t o = n_gt + og + min(n_eq + oe, need_g);
+                        if (o < (uint32_t)k) {
+                            out[o] = (int32_t)cand_pos(pool_row, block, ps);
+                            if (out_s) out_s[o] = key_value(key);
+                        }
+                    }
+                    n_gt += tg;
+                    n_eq += te;
+                }
+                if (tid == 0) dev_flag(X.d_status, CSA2_DEV_BAND_LIMIT);
+                continue;
             }
         }
-        uint32_t tot;
-        uint32_t o = n_c + block_excl_count_sum(cnt, S.warp, tot);
-        if (n_c + tot > kCandCap) {                        // does not fit on chip: fall back
-            overflow = true;
-            break;
+        __syncthreads();
+        if (n_c <= (uint32_t)k) {                          // everything listed wins
+            for (uint32_t i = tid; i < (uint32_t)k; i += kGThreads) {
+                out[i] = i < n_c ? (int32_t)cand_pos(pool_row, block, s_cp[i]) : -1;
+                if (out_s) out_s[i] = i < n_c ? key_value(s_ck[i]) : 0.0f;
+            }
+            continue;
         }
-        if (j < n_cg) {
-            if (vec && g0 + 32 <= n) {
-#pragma unroll 1
-                while (sel) {
-                    const int e = __ffs(sel) - 1;
-                    sel &= sel - 1u;
-                    s_ck[o] = score_key(s[g0 + e]);
-                    s_cp[o] = (int32_t)(g0 + e);
-                    ++o;
-                }
+    } else {
+        const int ng = (int)((len + gs - 1) / gs);             // <= kMaxGroups
+        const uint32_t *gk = s_gk;
+        for (int g = tid; g < ng; g += kGThreads) {
+            const uint32_t v = gkeys[row * G + g];
+            s_gk[g] = v;
+            nonfinite |= v >= 0xff800000u || v <= 0x007fffffu;
+        }
+        nonfinite = __syncthreads_or(nonfinite) != 0;
+        // exact order: the row's error bound of the float32 scores (c0 < 0: none made)
+        if constexpr (EXACT) {
+            seq = row / X.n_q;
+            if (row == (int64_t)blockIdx.x) {
+                rb = rb_first;
             } else {
-#pragma unroll 1
-                for (int e = 0; e < gs && g0 + e < len; ++e) {
-                    const uint32_t key = score_key(s[g0 + e]);
-                    if (key >= tau0) { s_ck[o] = key; s_cp[o] = (int32_t)(g0 + e); ++o; }
+                exact::quantise_query(QQ, X.q + row * (int64_t)X.H * D, X.w + row * (int64_t)X.H, X.H, D);
+                rb = row_bound(QQ, X, seq, s_red);
+            }
+            if (nonfinite) rb.c0 = -1.0f;
+        }
+        const bool ex_row = EXACT && rb.c0 >= 0.0f;
+        // a lower bound of the k-th largest group key is enough to keep every top-k element
+        // (the groups above the bound are a superset of those above the exact key); in exact
+        // order the bound is lowered to lo() of it, so the whole band is gathered
+        uint32_t need0;
+        uint32_t tau0 = ng > k ? g_threshold(gk, ng, (uint32_t)k, S, need0, 2) : 0u;
+        if (ex_row && tau0 != 0u) tau0 = score_key(rb.lo(key_value(tau0)));
+
+        // candidate groups (key >= tau0), listed in s_g in ascending order: thread t owns the
+        // run [t*run, (t+1)*run)
+        const int run = (ng + kGThreads - 1) / kGThreads;        // <= 32
+        const int r0 = min(tid * run, ng), r1 = min(r0 + run, ng);
+        uint32_t mine = 0;                                      // bit j: group r0+j is a candidate
+        for (int i = r0; i < r1; ++i) mine |= (gk[i] >= tau0 ? 1u : 0u) << (i - r0);
+        uint32_t n_cg;
+        const uint32_t at = block_excl_count_sum((uint32_t)__popc(mine), S.warp, n_cg);
+        if (n_cg > (uint32_t)kListCap) {                        // too many to list on chip
+            radix_select_row(scores, n, row_len, pool, block, k, idx, out_scores, row);
+            if (EXACT && tid == 0) dev_flag(X.d_status, CSA2_DEV_BAND_LIMIT);
+            continue;
+        }
+        {
+            uint32_t o = at;
+            for (int i = r0; i < r1; ++i)
+                if ((mine >> (i - r0)) & 1u) s_g[o++] = (uint32_t)i;
+        }
+        __syncthreads();
+        // gather candidates, in position order: one thread per candidate group reads its
+        // scores (groups of 32 as eight 16-byte loads, all in flight at once) and keeps a bit
+        // mask of its elements >= tau0; after a scan of the counts it walks the mask in a
+        // rolled loop, reading each selected score again (the lines are in L1 by then).  This
+        // code runs once per row, so it is kept small.
+        const bool vec = gs == 32 && ((reinterpret_cast<uintptr_t>(s) & 15u) == 0);   // 16-byte rows
+    #pragma unroll 1
+        for (uint32_t base = 0; base < n_cg; base += kGThreads) {
+            const uint32_t j = base + tid;
+            uint32_t sel = 0;                                  // groups of 32: bit e = element e
+            uint32_t cnt = 0;
+            int64_t g0 = 0;
+            if (j < n_cg) {
+                g0 = (int64_t)s_g[j] * gs;
+                if (vec && g0 + 32 <= n) {
+                    float4 f[8];
+                    const float4 *src = reinterpret_cast<const float4 *>(s + g0);
+    #pragma unroll
+                    for (int e = 0; e < 8; ++e) f[e] = src[e];
+    #pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        sel |= (uint32_t)(score_key(f[e].x) >= tau0) << (4 * e);
+                        sel |= (uint32_t)(score_key(f[e].y) >= tau0) << (4 * e + 1);
+                        sel |= (uint32_t)(score_key(f[e].z) >= tau0) << (4 * e + 2);
+                        sel |= (uint32_t)(score_key(f[e].w) >= tau0) << (4 * e + 3);
+                    }
+                    if (g0 + 32 > len) sel &= len > g0 ? (1u << (len - g0)) - 1u : 0u;
+                    cnt = __popc(sel);
+                } else {
+    #pragma unroll 1
+                    for (int e = 0; e < gs && g0 + e < len; ++e) cnt += score_key(s[g0 + e]) >= tau0;
                 }
             }
+            uint32_t tot;
+            uint32_t o = n_c + block_excl_count_sum(cnt, S.warp, tot);
+            if (n_c + tot > kCandCap) {                        // does not fit on chip: fall back
+                overflow = true;
+                break;
+            }
+            if (j < n_cg) {
+                if (vec && g0 + 32 <= n) {
+    #pragma unroll 1
+                    while (sel) {
+                        const int e = __ffs(sel) - 1;
+                        sel &= sel - 1u;
+                        s_ck[o] = score_key(s[g0 + e]);
+                        s_cp[o] = (int32_t)(g0 + e);
+                        ++o;
+                    }
+                } else {
+    #pragma unroll 1
+                    for (int e = 0; e < gs && g0 + e < len; ++e) {
+                        const uint32_t key = score_key(s[g0 + e]);
+                        if (key >= tau0) { s_ck[o] = key; s_cp[o] = (int32_t)(g0 + e); ++o; }
+                    }
+                }
+            }
+            n_c += tot;
         }
-        n_c += tot;
+        __syncthreads();
+        if (overflow) {                                        // does not fit on chip: fall back
+            radix_select_row(scores, n, row_len, pool, block, k, idx, out_scores, row);
+            if (EXACT && tid == 0) dev_flag(X.d_status, CSA2_DEV_BAND_LIMIT);
+            continue;
+        }
     }
-    __syncthreads();
-    if (overflow) {                                        // does not fit on chip: fall back
-        radix_select_row(scores, n, row_len, pool, block, k, idx, out_scores, row);
-        if (EXACT && tid == 0) dev_flag(X.d_status, CSA2_DEV_BAND_LIMIT);
-        continue;
-    }
+    const bool exact_row = EXACT && rb.c0 >= 0.0f;
     // selection among the candidates (n_c >= k) in float order: the k-th key tau and how
     // many candidates equal to it are taken
     uint32_t need;
     uint32_t tau = g_threshold(s_ck, (int)n_c, (uint32_t)k, S, need, 3);
     const int crun = ((int)n_c + kGThreads - 1) / kGThreads;
     const int c0 = min(tid * crun, (int)n_c), c1 = min(c0 + crun, (int)n_c);
+    uint32_t band_n = 0;                                   // lists: band entries re-scored exactly
     if constexpr (EXACT) {
         if (exact_row && tau != 0u) {
             // the band [lo(tau~), hi(tau~)] in key terms; above it: selected
@@ -970,11 +1099,15 @@ topk_gmax_kernel(const float *__restrict__ scores, int64_t n, int64_t rows, cons
                                   s_act, s_val, S, s_red);
                     // band candidates taken rank above hi, the others below every
                     // candidate: the float-order emission below then takes exactly these
-                    for (uint32_t u = tid; u < n_band; u += kGThreads)
+                    // (lists: the band's own keys are kept by band index for the scores out)
+                    for (uint32_t u = tid; u < n_band; u += kGThreads) {
+                        if (LISTS) s_act[u] = s_ck[s_band[u]];
                         s_ck[s_band[u]] = s_state[u] ? 0xffffffffu : 0u;
+                    }
                     __syncthreads();
                     tau = hi_key;
                     need = 0;
+                    band_n = n_band;
                 } else {
                     // the whole band is taken: every candidate >= lo is selected
                     tau = lo_key;
@@ -1001,7 +1134,22 @@ topk_gmax_kernel(const float *__restrict__ scores, int64_t n, int64_t rows, cons
         if (key == tau) sel = ties++ < need;
         if (sel && o < (uint32_t)k) {
             out[o] = (int32_t)cand_pos(pool_row, block, s_cp[i]);
-            if (out_s) out_s[o] = s[s_cp[i]];
+            if (out_s) {
+                if constexpr (LISTS) {
+                    uint32_t kk = key;
+                    if (key == 0xffffffffu) {          // a band candidate taken: its own key
+                        uint32_t lo = 0, hi = band_n;
+                        while (lo < hi) {
+                            const uint32_t mid = (lo + hi) >> 1;
+                            if (s_g[mid] < (uint32_t)i) lo = mid + 1; else hi = mid;
+                        }
+                        kk = s_g[kBandCap + lo];               // s_act (band index order)
+                    }
+                    out_s[o] = key_value(kk);
+                } else {
+                    out_s[o] = s[s_cp[i]];
+                }
+            }
             ++o;
         }
     }
@@ -1052,16 +1200,17 @@ size_t group_keys_bytes(int64_t rows, int64_t n)
 }
 
 // The selection kernel for float order, or exact order at the indexer head dim.
-template <bool EXACT, int D>
+template <bool EXACT, int D, bool LISTS = false>
 cudaError_t launch_gmax(unsigned grid, size_t smem, cudaStream_t s, const float *scores, int64_t n, int64_t rows,
                         const int32_t *row_len, const int32_t *pool, int32_t block, int32_t k, int32_t *idx,
-                        float *out_scores, const uint32_t *gkeys, int32_t gs, int64_t G, const ExactArgs &X)
+                        float *out_scores, const uint32_t *gkeys, int32_t gs, int64_t G, const ExactArgs &X,
+                        const TopkLists &L = TopkLists{})
 {
-    cudaError_t e = cudaFuncSetAttribute(topk_gmax_kernel<EXACT, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(topk_gmax_kernel<EXACT, D, LISTS>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(topk_gmax_kernel<EXACT, D>, dim3(grid), dim3(kGThreads), smem, s, 1, scores, n, rows,
-                      row_len, pool, block, k, idx, out_scores, gkeys, gs, G, X);
+    return launch_pdl(topk_gmax_kernel<EXACT, D, LISTS>, dim3(grid), dim3(kGThreads), smem, s, 1, scores, n, rows,
+                      row_len, pool, block, k, idx, out_scores, gkeys, gs, G, X, L);
 }
 
 } // namespace
@@ -1132,6 +1281,51 @@ cudaError_t launch_topk(const float *scores, int64_t rows, int64_t n, const int3
                                           out_scores, gkeys, gs, G, X);
     case 128: return launch_gmax<true, 128>((unsigned)grid, smem, s, scores, n, rows, row_len, pool, block, k,
                                             idx, out_scores, gkeys, gs, G, X);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+size_t topk_lists_ws_bytes(int64_t rows)
+{
+    return (size_t)exact_slots(rows) * exact::kLimbs * kBandCap * sizeof(uint32_t);
+}
+
+cudaError_t launch_topk_lists(const csa2_index_args &ex, int32_t k, const uint32_t *key, const int32_t *pos,
+                              const uint32_t *meta, int n_lists, int64_t cap, int32_t *idx, float *out_scores,
+                              void *ws, uint32_t *d_status, cudaStream_t s)
+{
+    const int64_t rows = (int64_t)ex.batch * ex.n_q;
+    if (rows == 0 || k == 0) return cudaSuccess;
+    if (n_lists < 1 || n_lists > kMaxLists) return cudaErrorInvalidValue;
+    TopkLists L;
+    L.n_lists = n_lists;
+    L.cap = cap;
+    L.key = key;
+    L.pos = pos;
+    L.meta = meta;
+    ExactArgs X = {};
+    X.H = ex.n_heads;
+    X.d = ex.head_dim;
+    X.n_q = ex.n_q;
+    X.n_keys = ex.n_keys;
+    X.q = ex.q;
+    X.w = ex.w;
+    X.kc = ex.k_codes;
+    X.ks = ex.k_scales;
+    X.unit = 1;
+    X.band = static_cast<uint32_t *>(ws);
+    X.d_status = d_status;
+    int64_t grid = exact_slots(rows);
+    if (grid > device_sm_count()) grid = device_sm_count();
+    const size_t smem = (size_t)(kListCap + 2 * kCandCap) * sizeof(uint32_t);
+    const int64_t n = ex.n_keys;
+    switch (ex.head_dim) {
+    case 32: return launch_gmax<true, 32, true>((unsigned)grid, smem, s, nullptr, n, rows, nullptr, nullptr, 1, k,
+                                                idx, out_scores, nullptr, 32, 0, X, L);
+    case 64: return launch_gmax<true, 64, true>((unsigned)grid, smem, s, nullptr, n, rows, nullptr, nullptr, 1, k,
+                                                idx, out_scores, nullptr, 32, 0, X, L);
+    case 128: return launch_gmax<true, 128, true>((unsigned)grid, smem, s, nullptr, n, rows, nullptr, nullptr, 1,
+                                                  k, idx, out_scores, nullptr, 32, 0, X, L);
     default: return cudaErrorInvalidValue;
     }
 }

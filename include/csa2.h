@@ -334,6 +334,29 @@ CSA2_API csa2_status csa2_block_candidates(const float *scores, int64_t rows, in
                                   size_t ws_bytes, uint32_t *d_status, csa2_stream stream);
 
 /* ---------------------------------------------------------------------------------- */
+/* csa2_index_topk -- the indexer and the exact Top-K in one call, with no score matrix  */
+/* (report §2.3: each query keeps the Top-K of its indexer scores; report §1 / §3.2 run   */
+/* the selection fused with the scoring).  Computes exactly what csa2_index_score(a)    */
+/* followed by csa2_topk(scores, ..., exact = a, k) computes: idx [B, T, k] the exact    */
+/* top-k positions of each query (ascending, -1 padded; in POOL mode positions through  */
+/* the pool), out_scores (nullable) [B, T, k] their float32 scores (-0 is returned as   */
+/* +0), row_len (nullable) [B, T] the candidates of each row.                           */
+/* Where the tensor-core indexer takes the call with one query per CTA (FULL mode, head  */
+/* dim 128, at most 32 heads: the decode shape), each of its CTAs keeps its scores in    */
+/* shared memory and writes only a candidate list -- every score at least lo(its own    */
+/* k-th), lo the exact selection's band bound -- and a second kernel selects each row    */
+/* from its lists.  Other shapes run csa2_index_score into the workspace, then          */
+/* csa2_topk.  a->q must be 16-byte aligned.                                            */
+/* Workspace: csa2_index_topk_workspace_size(a, k) bytes, 16-byte aligned, zero-filled   */
+/* before its first use (its first part holds the indexer's counters, which every call  */
+/* leaves zero).  The size depends on the current device's SM count.                    */
+/* ---------------------------------------------------------------------------------- */
+CSA2_API size_t csa2_index_topk_workspace_size(const csa2_index_args *a, int32_t k);
+CSA2_API csa2_status csa2_index_topk(const csa2_index_args *a, int32_t k, int32_t *idx, float *out_scores,
+                                     int32_t *row_len, void *ws, size_t ws_bytes, uint32_t *d_status,
+                                     csa2_stream stream);
+
+/* ---------------------------------------------------------------------------------- */
 /* csa2_sparse_attn -- core attention (report §2.3 and §2.3.1: every mode attends the   */
 /* selected main-KV entries together with the layer's SWA KV; review: the main KV is a  */
 /* latent shared by all query heads; report §3.2.2: SWA keys of a query at token i are   */

@@ -29,7 +29,7 @@ def lib():
 
 def test_exports_every_declared_symbol(lib):
     syms = _declared_symbols()
-    assert len(syms) == 19
+    assert len(syms) == 21
     for s in syms:
         assert hasattr(lib, s), s
     out = os.popen(f"nm -D --defined-only {libbuild.LIB}").read()

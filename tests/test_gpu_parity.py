@@ -486,6 +486,64 @@ def test_exact_order_resolves_float32_ties(N, neg, tiny_exp):
     assert np.array_equal(blocks[0, 0].cpu().numpy(), oracle.block_candidates_exact(ex, N, 8, 40))
 
 
+FUSED_CASES = dict(SCORE_CASES)
+FUSED_CASES.update({
+    # more candidates than the 32 stages x 256 positions one CTA keeps: the row takes
+    # at least 9 CTAs whatever the SM count
+    "decode_70k": W["full_decode_64k"].scaled(batch=2, n_q=1, n_keys=70001, q_pos0=70000, seed=31),
+    # fewer visible positions than K: every list holds all of its positions
+    "short_rows": W["full_decode_64k"].scaled(batch=3, n_q=1, n_keys=900, q_pos0=300, seed=32),
+    "ties_decode": W["hier_indexer_1m"].scaled(batch=2, n_keys=30000, q_pos0=29999, palette=32),
+})
+
+
+@pytest.mark.parametrize("name", list(FUSED_CASES))
+def test_index_topk_equals_scores_then_topk(name):
+    # csa2_index_topk (no score matrix where the indexer takes one query per CTA) gives
+    # exactly what csa2_index_score + exact csa2_topk give
+    w = FUSED_CASES[name]
+    st = status()
+    dw = workload.build(w, kv=False, device=DEV, d_status=st)
+    scores, row_len, args = csa2.index_score(dw["q_idx"], dw["w_idx"], dw["k_codes"], dw["k_scales"],
+                                             dw["q_pos"], w.ratio_m, None, w.block, st, want_args=True)
+    ref, ref_s = csa2.topk(scores, w.topk, row_len, d_status=st, exact=args, want_scores=True)
+    idx, rl, out_s = csa2.index_topk(dw["q_idx"], dw["w_idx"], dw["k_codes"], dw["k_scales"], w.topk,
+                                     dw["q_pos"], w.ratio_m, d_status=st, want_scores=True)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.equal(rl, row_len)
+    assert torch.equal(idx, ref)
+    # scores of the selected entries (the fused call returns -0 as +0)
+    assert torch.equal(out_s, ref_s + 0.0)
+
+
+def test_index_topk_negative_weights_and_near_ties():
+    # head weights of both signs (the CTAs keep every position: the bound needs the whole
+    # sequence) and a float32 tie group resolved by the exact order
+    w = W["full_decode_64k"].scaled(batch=2, n_q=3, n_keys=9000, q_pos0=8999, plant_frac=0.0, seed=23)
+    st = status()
+    dw = workload.build(w, kv=False, device=DEV, d_status=st)
+    wn = torch.randn(dw["w_idx"].shape, generator=torch.Generator().manual_seed(5)).to(DEV)
+    scores, row_len, args = csa2.index_score(dw["q_idx"], wn, dw["k_codes"], dw["k_scales"],
+                                             dw["q_pos"], 1, None, w.block, st, want_args=True)
+    ref = csa2.topk(scores, w.topk, row_len, d_status=st, exact=args)
+    idx, rl = csa2.index_topk(dw["q_idx"], wn, dw["k_codes"], dw["k_scales"], w.topk, dw["q_pos"], 1,
+                              d_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.equal(idx, ref) and torch.equal(rl, row_len)
+    q, k, wv = _near_tie_case(1500, 41)
+    qb, kb = synth.f32_to_bf16_bits(q), synth.f32_to_bf16_bits(k)
+    kc, ks = csa2.quant_fp4(workload.bf16_tensor(kb, DEV), st)
+    qt, wt = workload.bf16_tensor(qb, DEV), torch.from_numpy(wv).to(DEV)
+    scores, row_len, args = csa2.index_score(qt, wt, kc, ks, d_status=st, want_args=True)
+    ref = csa2.topk(scores, 512, row_len, d_status=st, exact=args)
+    idx, _ = csa2.index_topk(qt, wt, kc, ks, 512, d_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.equal(idx, ref)
+
+
 def test_exact_order_long_row_spread_tie_group():
     # a row of 70,001 positions: a float32 tie group of 1,000 positions spread over the
     # whole row holds the top 512, whose exact order comes from the tiny second head; the

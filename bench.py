@@ -298,6 +298,9 @@ def run_gpu(args):
     gmax = csa2.group_max_buffer(scores)     # per-32 group maxima: indexer -> Top-K
     iargs = csa2.make_index_args(dw["q_idx"], dw["w_idx"], dw["k_codes"], dw["k_scales"],
                                  dw["q_pos"], w.ratio_m, group_max=gmax)
+    # only the decoded token's row (position N - 1) comes from the cache write just before the
+    # indexer: the older positions stream while that write runs
+    iargs.fresh_from = w.n_keys - 1
     aargs = csa2.make_attn_args(dw["q_attn"], dw["kv_codes"], dw["kv_scales"], idx, dw["swa"],
                                 dw["swa_pos0"], dw["q_pos"], None, w.window, dw.sm_scale, w.d_v)
     lib = csa2.load()
@@ -427,6 +430,7 @@ def run_gpu(args):
     h_in[n_qi:].copy_(dw["w_idx"].cpu().view(torch.uint8).reshape(-1))
     iargs_e2e = csa2.make_index_args(e_qi, e_w, dw["k_codes"], dw["k_scales"], dw["q_pos"], w.ratio_m,
                                      group_max=gmax)
+    iargs_e2e.fresh_from = w.n_keys - 1
     h_qa = dw["q_attn"].cpu().pin_memory()
     h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     h2d = h_in.numel() + h_qa.numel() * 2
@@ -603,6 +607,7 @@ def run_gpu(args):
         # keep their scores on chip and write candidate lists; no score matrix)
         iargs_f = csa2.make_index_args(dw["q_idx"], dw["w_idx"], dw["k_codes"], dw["k_scales"], dw["q_pos"],
                                        w.ratio_m)
+        iargs_f.fresh_from = w.n_keys - 1
         ws_f = torch.zeros(max(1, lib.csa2_index_topk_workspace_size(ctypes.byref(iargs_f), w.topk)),
                            dtype=torch.uint8, device=dev)
         idx_f = torch.empty_like(idx)

@@ -42,7 +42,7 @@ class IndexArgs(ctypes.Structure):
     _fields_ = [("batch", _I32), ("n_q", _I32), ("n_heads", _I32), ("head_dim", _I32),
                 ("ratio_m", _I32), ("n_keys", _I64), ("q", _P), ("w", _P), ("k_codes", _P),
                 ("k_scales", _P), ("q_pos", _P), ("mode", ctypes.c_int), ("pool_blocks", _P),
-                ("n_pool_blocks", _I32), ("block", _I32), ("group_max", _P)]
+                ("n_pool_blocks", _I32), ("block", _I32), ("group_max", _P), ("fresh_from", _I64)]
 
 
 class AttnArgs(ctypes.Structure):

@@ -60,6 +60,7 @@ bool index_args_ok(const csa2_index_args *a)
     if (a->ratio_m < 1) return false;
     if (a->mode != CSA2_INDEX_FULL && a->mode != CSA2_INDEX_POOL) return false;
     if (a->block < 1 || a->block > 32) return false;
+    if (a->fresh_from < 0) return false;
     const bool empty = (int64_t)a->batch * a->n_q == 0;
     if (!empty && (!a->q || !a->w || (a->n_keys > 0 && (!a->k_codes || !a->k_scales)))) return false;
     if (a->k_codes && !aligned(a->k_codes, 16)) return false;

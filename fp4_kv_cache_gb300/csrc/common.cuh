@@ -266,9 +266,9 @@ __device__ __forceinline__ float dyadic_sum_f32(const int (&I)[NB], const int (&
 // A kernel launched with programmatic dependent launch waits here until the previous
 // kernel in the stream has completed and its writes are visible (immediately, when there
 // is no such kernel); pdl_allow_dependents lets the next kernel in the stream start its
-// own set-up early.  Only the indexer, Top-K and attention kernels call it: a conversion
-// or cache-write kernel lets the next kernel start only when it has finished, so nothing
-// it writes is read early by a kernel that reads some inputs before its wait.
+// own set-up early.  The indexer, Top-K, attention and RoPE cache-write kernels call it
+// (the indexer then streams the cache rows written before this step while the cache write
+// runs); the other conversion kernels let the next kernel start only when they finish.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 

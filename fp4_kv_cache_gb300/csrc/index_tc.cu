@@ -95,6 +95,7 @@ struct TcParams {
     uint32_t *lst_meta;      // [rows, CTAs per row, 4]: count, K-th key (0: K or fewer), non-finite
     int32_t lst_k;           // K
     int32_t lst_stages;      // stages per CTA (lst_cap = lst_stages x span)
+    int64_t fresh_from;      // > 0: only positions >= fresh_from may come from the kernel before
 };
 
 constexpr int kFuseStages = 32;        // fused selection: stages a CTA keeps on chip
@@ -480,8 +481,12 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
         tc::tmem_alloc(&S.tmem_base, C::kTmemCols);
         tc::tmem_relinquish();
     }
-    // everything above touched no input: it overlaps the previous kernel's tail
-    pdl_wait();
+    // everything above touched no input: it overlaps the previous kernel's tail.  With
+    // fresh_from, the positions below it (and q, w, q_pos) are not written by the kernel
+    // before: the dependency wait is taken only before the first stage that holds a newer
+    // position, before the first claim from the shared counters, and before the CTA ends.
+    const bool early = !P.pool_mode && P.fresh_from > 0;
+    if (!early) pdl_wait();
     pdl_allow_dependents();
     // ---- valid candidates of the group's rows (and pool checks): needed before streaming
     const int32_t *pool = P.pool_mode ? P.pool + row0 * (int64_t)P.n_pool_blocks : nullptr;
@@ -572,6 +577,14 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
         };
         int issued = 0;
         uint32_t claim = 0;                       // lane 0: the next claim from the counter
+        bool waited = !early;
+        auto wait_prev = [&]() {
+            if (!waited) {
+                pdl_wait();
+                waited = true;
+            }
+        };
+        if (R == 0 && !fused) wait_prev();
         if (lane == 0 && R == 0 && !fused) claim = atomicAdd(&P.tile_ctr[unit], 1u);
         for (int i = 0;; ++i) {
             const int s = i % kStages;
@@ -586,6 +599,7 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
                 t = i < R ? (int)blockIdx.x * R + i : ntr;
             } else if (i < R) {
                 t = (int)blockIdx.x * R + i;
+                if (i == R - 1) wait_prev();
                 if (lane == 0 && i == R - 1) claim = atomicAdd(&P.tile_ctr[unit], 1u);
             } else {
                 if (lane == 0) {
@@ -604,6 +618,7 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
                 break;
             }
             const int64_t t0 = (int64_t)t * kSpan;
+            if (t0 + kSpan > P.fresh_from) wait_prev();   // the stage holds a newer position
             // a whole stage of consecutive positions: its scale bytes are one contiguous run,
             // copied in position order by one bulk copy (the MMA warp rearranges them into
             // the scale-factor atoms); otherwise each lane copies its atom words
@@ -841,6 +856,7 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
         int64_t qlen[kQPerWarp];
         int qspan[kQPerWarp], qmin[kQPerWarp], qmax[kQPerWarp];
         bool out_of_range = false;            // a score this warp wrote is not finite
+        bool ewaited = !early;
         for (int i = 0;; ++i) {
             const int acc = i % kAcc;
             // the stage itself is not touched here: the MMA's completion frees it
@@ -851,6 +867,10 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
             }
             const int t = S.acc_tile[acc];
             if (t < 0) break;                     // end marker (the same for the whole warp)
+            if (!ewaited && (int64_t)(t + 1) * kSpan > P.fresh_from) {   // newer positions: re-scores read them
+                pdl_wait();
+                ewaited = true;
+            }
             if (i == 0) {
 #pragma unroll
                 for (int u = 0; u < kQPerWarp; ++u) {
@@ -975,6 +995,7 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
         //      position is checked per query and re-scored exactly where the MMA result may
         //      be rounded; the group maxima around re-scored positions are recomputed
         if constexpr (C::kDeferred) {
+            if (!ewaited) pdl_wait();             // the re-checks read key rows of any position
             asm volatile("bar.sync 3, %0;" ::"r"((kEpiWarps + 1) * 32) : "memory");
             if (!S.abort_flag) {
                 const int nwords = (ntr + 31) >> 5;
@@ -997,6 +1018,7 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
 
     tc::tc_fence_before();
     __syncthreads();
+    if (early) pdl_wait();                         // before the counters and lists are touched
     if (warp == 1) {
         tc::tc_fence_after();
         tc::tmem_dealloc(tmem, C::kTmemCols);
@@ -1145,6 +1167,7 @@ cudaError_t launch_index_tc(const csa2_index_args &a, float *scores, int32_t *ro
     P.lst_meta = nullptr;
     P.lst_k = 0;
     P.lst_stages = 0;
+    P.fresh_from = a.mode == CSA2_INDEX_POOL ? 0 : a.fresh_from;
     if (fo) {                                  // no scores, no group maxima: candidate lists
         if (qg != 1 || P.pool_mode) return cudaErrorInvalidValue;
         int64_t ctas;

@@ -379,6 +379,7 @@ __global__ void __launch_bounds__(256) rope_quant_kernel(const __grid_constant__
                                                          uint32_t *d_status)
 {
     pdl_wait();                                   // x and pos may come from the kernel before
+    pdl_allow_dependents();                       // the indexer streams older rows meanwhile
     const int64_t total = B.lanes_end[B.n - 1];
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     const int64_t total32 = (total + 31) & ~int64_t(31);

@@ -32,17 +32,23 @@
  *     library keeps no mutable global state.
  *   - Kernels are launched with programmatic dependent launch: a kernel may start its
  *     set-up while the kernel before it on the stream drains, and waits for that kernel
- *     to complete before it reads what that kernel may write.  The indexer, Top-K and
- *     attention kernels let their dependents start right after that wait; the conversion
- *     and cache-write calls (csa2_quant_*, csa2_dequant_*, csa2_rope_quant_fp4) only when
- *     they finish.  Two exceptions read inputs before the wait: csa2_sparse_attn reads q,
- *     q_pos, swa_pos0, swa_start, swa and swa_scales (and works through the SWA window)
- *     before it (only idx may come from the kernel just before it), and csa2_topk /
+ *     to complete before it reads what that kernel may write.  The indexer, Top-K,
+ *     attention and csa2_rope_quant_fp4 kernels let their dependents start right after
+ *     that wait; the other conversion calls (csa2_quant_*, csa2_dequant_*) only when they
+ *     finish.  Three read inputs before the wait: csa2_sparse_attn reads q, q_pos,
+ *     swa_pos0, swa_start, swa and swa_scales (and works through the SWA window) before
+ *     it (only idx may come from the kernel just before it); csa2_topk /
  *     csa2_block_candidates with an exact context read its q, w and k_scales before
  *     theirs (only the scores, row lengths and group maxima may come from the kernel just
- *     before them).  Those inputs must not be written by a kernel that lets its
- *     dependents start early: a plain kernel, or a conversion or cache-write call of this
- *     library, is fine, and so is any call of this library whose outputs they are not.
+ *     before them); and csa2_index_score / csa2_index_topk with fresh_from > 0 read q, w,
+ *     q_pos and the cache positions below fresh_from before theirs.  Those inputs must not
+ *     be written by a kernel that lets its dependents start early and runs just before
+ *     the call: a plain kernel, a csa2_quant_* / csa2_dequant_* call, or a call of this
+ *     library whose outputs they are not is fine (so a csa2_rope_quant_fp4 that writes
+ *     the decoded token's cache rows may come just before the indexer with fresh_from set
+ *     to that token's position, not just before an exact csa2_topk on the same cache).
+ *     With fresh_from > 0 the kernel just before must not use this call's outputs or
+ *     workspace either.
  */
 #ifndef CSA2_H
 #define CSA2_H
@@ -264,6 +270,14 @@ typedef struct {
                                 /* order csa2_topk uses): 0 for NaN; with u = the bits of  */
                                 /* s and -0 read as +0, u | 0x80000000 for s >= 0 and ~u   */
                                 /* for s < 0 (so keys rise with the score).                */
+    int64_t fresh_from;         /* 0: the scoring kernel waits for the kernel just before  */
+                                /* it on the stream before it reads any input.  > 0 (FULL  */
+                                /* mode): only the positions >= fresh_from of each         */
+                                /* sequence may be written by that kernel (e.g. it is the  */
+                                /* cache write of the decoded token): the kernel streams   */
+                                /* the positions below it, and reads q, w and q_pos,       */
+                                /* before its wait, which it takes only before the first   */
+                                /* stage that holds a position >= fresh_from.              */
 } csa2_index_args;
 
 /* Outputs: scores [B, T, n_cand] float32, n_cand = N (FULL) or n_pool_blocks*block (POOL);

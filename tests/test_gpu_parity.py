@@ -517,6 +517,45 @@ def test_index_topk_equals_scores_then_topk(name):
     assert torch.equal(out_s, ref_s + 0.0)
 
 
+def test_index_after_cache_write_with_fresh_from():
+    # the cache write of the decoded token (csa2_rope_quant_fp4, which lets the next kernel
+    # start early) directly followed by the indexer with fresh_from = that token's
+    # position: the indexer streams the older positions before its dependency wait and must
+    # still see the new row.  Each round writes a different row; the scores equal those of
+    # a call made after a full synchronisation.
+    w = W["full_decode_64k"].scaled(batch=4, n_q=1, n_keys=20000, q_pos0=19999, seed=43)
+    st = status()
+    dw = workload.build(w, kv=False, device=DEV, d_status=st)
+    last = w.n_keys - 1
+    kc, ks = dw["k_codes"], dw["k_scales"]
+    gen = torch.Generator().manual_seed(44)
+    scores = torch.empty((w.batch, 1, w.n_keys), dtype=torch.float32, device=DEV)
+    row_len = torch.empty((w.batch, 1), dtype=torch.int32, device=DEV)
+    args = csa2.make_index_args(dw["q_idx"], dw["w_idx"], kc, ks, dw["q_pos"], 1)
+    args.fresh_from = last
+    ref_args = csa2.make_index_args(dw["q_idx"], dw["w_idx"], kc, ks, dw["q_pos"], 1)
+    ws = torch.zeros(max(1, csa2.load().csa2_index_score_workspace_size(ctypes.byref(args))), dtype=torch.uint8,
+                     device=DEV)
+    idx = torch.empty((w.batch, 1, w.topk), dtype=torch.int32, device=DEV)
+    wsf = torch.zeros(csa2.load().csa2_index_topk_workspace_size(ctypes.byref(args), w.topk), dtype=torch.uint8,
+                      device=DEV)
+    for r in range(4):
+        new_k = (torch.randn((w.batch, w.idx_dim), generator=gen) * (2.0 + 10 * r)).to(torch.bfloat16).to(DEV)
+        jobs = [(new_k, kc[:, last], ks[:, last], 0, None, None, csa2.FMT_MXFP4)]
+        csa2.csa2_rope_quant_fp4(jobs, st)
+        csa2.csa2_index_score(args, scores, row_len, st, workspace=ws)
+        csa2.csa2_rope_quant_fp4(jobs, st)                 # the same row again, then the fused call
+        csa2.csa2_index_topk(args, w.topk, idx, None, None, st, workspace=wsf)
+        torch.cuda.synchronize()
+        ref_s, ref_l = csa2.index_score(dw["q_idx"], dw["w_idx"], kc, ks, dw["q_pos"], 1)
+        ref_idx = csa2.topk(ref_s, w.topk, ref_l, d_status=st, exact=ref_args)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        assert torch.equal(row_len, ref_l)
+        assert np.array_equal(scores.cpu().numpy().view(np.uint32), ref_s.cpu().numpy().view(np.uint32)), r
+        assert torch.equal(idx, ref_idx), r
+
+
 def test_index_topk_negative_weights_and_near_ties():
     # head weights of both signs (the CTAs keep every position: the bound needs the whole
     # sequence) and a float32 tie group resolved by the exact order

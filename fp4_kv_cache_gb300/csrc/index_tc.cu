@@ -61,7 +61,7 @@ template <int QG> struct Cfg;
 // otherwise the epilogue checks each position's bounds and re-scores in place (decode).
 template <> struct Cfg<1> {
     static constexpr bool kDeferred = false;
-    static constexpr int kStages = 4, kAcc = 3, kMB = 2, kEpiPerQuad = 2, kCtasPerSm = 2;
+    static constexpr int kStages = 5, kAcc = 3, kMB = 2, kEpiPerQuad = 2, kCtasPerSm = 2;
     static constexpr uint32_t kTmemCols = 256, kColSfa = 192, kColSfb = 216;
 };
 template <> struct Cfg<4> {
@@ -98,7 +98,7 @@ struct TcParams {
     int64_t fresh_from;      // > 0: only positions >= fresh_from may come from the kernel before
 };
 
-constexpr int kFuseStages = 32;        // fused selection: stages a CTA keeps on chip
+constexpr int kFuseStages = 20;        // fused selection: stages a CTA keeps on chip
 template <int QG>
 struct TcSmem {
     static constexpr int kStages = Cfg<QG>::kStages, kAcc = Cfg<QG>::kAcc, kSpan = kSpanOf<QG>;
@@ -121,7 +121,11 @@ struct TcSmem {
     int abort_flag, bad;
     int q_span[QG], q_min[QG], q_max[QG];
     uint32_t fkeys[kFuseKeys];                 // fused selection: the CTA's keys in position order
+                                               // (last: launches without it leave it out)
 };
+// Two decode CTAs per SM, also with the fused selection's keys (the SM's 228 KB, less 1 KB
+// reserved per CTA and the 1 KB alignment slack of each)
+static_assert(2 * (sizeof(TcSmem<1>) + 1024 + 1024) <= 228 * 1024, "two decode CTAs per SM");
 
 // instruction descriptor, kind::mxf4: A = B = E2M1 (1), UE8M0 scales, K-major A and B,
 // N at bits 17-22 (N/8), M at bits 24-28 (M/16), scale-factor ids at bits 4-5 (B) and
@@ -1081,6 +1085,8 @@ cudaError_t launch_tc(const CUtensorMap &map, const TcParams &P, int64_t units, 
                       cudaStream_t s)
 {
     const size_t smem = sizeof(TcSmem<QG>) + 1024;
+    // without the fused selection the key buffer at the end is not needed
+    const size_t smem_launch = P.lst_key ? smem : offsetof(TcSmem<QG>, fkeys) + 1024;
     cudaError_t e = cudaFuncSetAttribute(index_score_tc_kernel<QG>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -1089,7 +1095,7 @@ cudaError_t launch_tc(const CUtensorMap &map, const TcParams &P, int64_t units, 
                              (int)cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     return launch_pdl(index_score_tc_kernel<QG>, dim3((unsigned)splits, (unsigned)units),
-                      dim3(kThreadsOf<QG>), smem, s, 1, map, P);
+                      dim3(kThreadsOf<QG>), smem_launch, s, 1, map, P);
 }
 
 } // namespace

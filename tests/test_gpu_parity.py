@@ -275,6 +275,9 @@ SCORE_CASES = {
     "chunk_groups": W["prefill_chunk_m2"].scaled(batch=2, n_q=11, n_keys=2100, q_pos0=4090, seed=11),
     "d32_h1": W["tiny_full_decode"].scaled(batch=2, n_keys=777, q_pos0=776, idx_heads=1, idx_dim=32),
     "ties": W["hier_indexer_1m"].scaled(batch=2, n_keys=20000, q_pos0=19999, palette=64),
+    # decode stages are loaded through a view of the key rows in groups of four; a whole
+    # stage that reaches into the last (B * n_keys) mod 4 rows is loaded plain instead
+    "tensor_end": W["full_decode_64k"].scaled(batch=2, n_q=1, n_keys=257, q_pos0=256, seed=5),
 }
 
 
@@ -367,15 +370,16 @@ def test_full_scores_topk_blocks(name):
             assert np.array_equal(idx_g[b, t].cpu().numpy(), idx[b, t].cpu().numpy())
 
 
-@pytest.mark.parametrize("T,sparse", [(2, False), (9, False), (9, True)])
-def test_scores_wide_exponents(T, sparse):
+@pytest.mark.parametrize("T,sparse,N", [(2, False, 3000), (2, True, 3001), (9, False, 3000), (9, True, 3000)])
+def test_scores_wide_exponents(T, sparse, N):
     # random FP4 codes with scale bytes over the whole E8M0 range and queries spanning
     # 2^-60 .. 2^60 per block: the kernels' wide-sum and overflow paths.  T = 9 takes the
     # four-queries-per-CTA kernel (stages flagged and re-checked after its main loop);
     # `sparse` keeps ordinary scales except at 1% of the positions, so only some stages
-    # are flagged and only some positions of those need re-scoring.
+    # are flagged and only some positions of those need re-scoring.  N = 3,001 puts the
+    # second sequence's rows and scale words off the 4-row grid.
     rng = np.random.default_rng(17 + T + int(sparse))
-    B, H, d, N = 2, 8, 128, 3000
+    B, H, d = 2, 8, 128
     kc = rng.integers(0, 256, size=(B, N, d // 2), dtype=np.uint8)
     ks = rng.integers(0, 255, size=(B, N, d // 32)).astype(np.uint8)
     if sparse:

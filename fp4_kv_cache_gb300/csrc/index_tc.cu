@@ -98,11 +98,13 @@ struct TcParams {
     int64_t fresh_from;      // > 0: only positions >= fresh_from may come from the kernel before
 };
 
-constexpr int kFuseStages = 20;        // fused selection: stages a CTA keeps on chip
-template <int QG>
+constexpr int kFuseStages = 32;        // fused selection: stages a CTA keeps on chip
+constexpr int kFuseRing = 4;           // fused selection: stage ring (its keys take the room)
+// FU: the fused selection's layout (QG = 1 only): a shorter stage ring and the key buffer
+template <int QG, bool FU = false>
 struct TcSmem {
-    static constexpr int kStages = Cfg<QG>::kStages, kAcc = Cfg<QG>::kAcc, kSpan = kSpanOf<QG>;
-    static constexpr int kFuseKeys = QG == 1 ? kFuseStages * kSpanOf<1> : 1;
+    static constexpr int kStages = FU ? kFuseRing : Cfg<QG>::kStages, kAcc = Cfg<QG>::kAcc, kSpan = kSpanOf<QG>;
+    static constexpr int kFuseKeys = FU ? kFuseStages * kSpanOf<1> : 1;
     uint8_t a[kStages][kSpan * kRowBytes];     // K codes, 64-byte swizzle, 1024-aligned
     uint8_t b[QG * kNPad * kRowBytes];         // q codes (row = query x 32 + head), same layout
     uint32_t sfa[kStages][kSpan];              // scale-factor atoms of the K tiles (one per block)
@@ -121,11 +123,11 @@ struct TcSmem {
     int abort_flag, bad;
     int q_span[QG], q_min[QG], q_max[QG];
     uint32_t fkeys[kFuseKeys];                 // fused selection: the CTA's keys in position order
-                                               // (last: launches without it leave it out)
 };
-// Two decode CTAs per SM, also with the fused selection's keys (the SM's 228 KB, less 1 KB
-// reserved per CTA and the 1 KB alignment slack of each)
+// Two decode CTAs per SM in either layout (the SM's 228 KB, less 1 KB reserved per CTA and
+// the 1 KB alignment slack of each)
 static_assert(2 * (sizeof(TcSmem<1>) + 1024 + 1024) <= 228 * 1024, "two decode CTAs per SM");
+static_assert(2 * (sizeof(TcSmem<1, true>) + 1024 + 1024) <= 228 * 1024, "two fused decode CTAs per SM");
 
 // instruction descriptor, kind::mxf4: A = B = E2M1 (1), UE8M0 scales, K-major A and B,
 // N at bits 17-22 (N/8), M at bits 24-28 (M/16), scale-factor ids at bits 4-5 (B) and
@@ -234,8 +236,8 @@ __device__ __noinline__ float rescore_flagged(uint32_t todo, float score, uint32
 // positions whose key exponents break that query's exactness bounds are re-scored on CUDA
 // cores (rescore_flagged) and their score and group maximum rewritten.  Runs after the main
 // loop, so the loop itself carries no re-scoring code.
-template <int QG>
-__device__ __noinline__ void recheck_stage(const TcParams &P, const TcSmem<QG> &S, int t, int span, int64_t row0,
+template <int QG, bool FU>
+__device__ __noinline__ void recheck_stage(const TcParams &P, const TcSmem<QG, FU> &S, int t, int span, int64_t row0,
                                            int t0q, int64_t kbase, const int32_t *pool, int64_t n_blk_all)
 {
     const int lane = threadIdx.x & 31;
@@ -321,8 +323,8 @@ __device__ __forceinline__ uint32_t fused_scan(uint32_t v, uint32_t *s_warp, uin
 // negative head weight (its bound needs the whole sequence's key scales) keeps every key; a
 // CTA that met a non-finite score keeps the keys >= tau and says so (its row then goes by
 // the float order, for which those suffice).
-template <int QG>
-__device__ __noinline__ void fused_list(const TcParams &P, TcSmem<QG> &S, int64_t row, int64_t pos0, int V)
+template <int QG, bool FU>
+__device__ __noinline__ void fused_list(const TcParams &P, TcSmem<QG, FU> &S, int64_t row, int64_t pos0, int V)
 {
     const int tid = threadIdx.x, lane = tid & 31;
     constexpr int NT = kThreadsOf<QG>;
@@ -442,16 +444,16 @@ __device__ __noinline__ void fused_list(const TcParams &P, TcSmem<QG> &S, int64_
     }
 }
 
-template <int QG>
+template <int QG, bool FU>
 __global__ void __launch_bounds__(kThreadsOf<QG>, Cfg<QG>::kCtasPerSm)
 index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P)
 {
     using C = Cfg<QG>;
-    constexpr int kStages = C::kStages, kAcc = C::kAcc, kN = QG * kNPad, kMB = C::kMB;
+    constexpr int kStages = TcSmem<QG, FU>::kStages, kAcc = C::kAcc, kN = QG * kNPad, kMB = C::kMB;
     constexpr int kSpan = kSpanOf<QG>;
     constexpr int kEpiWarps = 4 * C::kEpiPerQuad, kQPerWarp = QG * kMB / C::kEpiPerQuad;
     extern __shared__ uint8_t smem_raw[];
-    TcSmem<QG> &S = *reinterpret_cast<TcSmem<QG> *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+    TcSmem<QG, FU> &S = *reinterpret_cast<TcSmem<QG, FU> *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                     ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // unit = the QG consecutive queries of one sequence this CTA scores (rows row0 ..)
@@ -537,7 +539,7 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
     const int ntr = len > 0 ? (int)((len + kSpan - 1) / kSpan) : 0;
     const int CT = (int)gridDim.x;
     // fused selection: CTA c takes the fixed run [c F, c F + F) of lst_stages stages
-    const bool fused = QG == 1 && P.lst_key != nullptr;
+    constexpr bool fused = QG == 1 && FU;
     const int R = fused ? P.lst_stages : (ntr / CT > 2 ? ntr / CT - 2 : 0);
     const int64_t c1 = len;
     const uint32_t tmem = S.tmem_base;
@@ -1012,7 +1014,7 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
                         const int bit = __ffs(bits) - 1;
                         bits &= bits - 1u;
                         if (seen++ % kEpiWarps != ew) continue;
-                        recheck_stage<QG>(P, S, wi * 32 + bit, kSpan, row0, t0q, kbase, pool, n_blk_all);
+                        recheck_stage<QG, FU>(P, S, wi * 32 + bit, kSpan, row0, t0q, kbase, pool, n_blk_all);
                     }
                 }
             }
@@ -1032,7 +1034,7 @@ index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap, const TcParams P
             const int64_t pos0 = (int64_t)blockIdx.x * R * kSpan;
             int64_t v = S.qlen[0] - pos0;
             v = v < 0 ? 0 : (v > (int64_t)R * kSpan ? (int64_t)R * kSpan : v);
-            fused_list<QG>(P, S, row0, pos0, (int)v);
+            fused_list<QG, FU>(P, S, row0, pos0, (int)v);
         }
     }
     if (tid == 0) {
@@ -1080,22 +1082,20 @@ int64_t tc_splits(int64_t units, int64_t n_cand, int ctas_per_sm, int span)
     return s;
 }
 
-template <int QG>
+template <int QG, bool FU>
 cudaError_t launch_tc(const CUtensorMap &map, const TcParams &P, int64_t units, int64_t splits,
                       cudaStream_t s)
 {
-    const size_t smem = sizeof(TcSmem<QG>) + 1024;
-    // without the fused selection the key buffer at the end is not needed
-    const size_t smem_launch = P.lst_key ? smem : offsetof(TcSmem<QG>, fkeys) + 1024;
-    cudaError_t e = cudaFuncSetAttribute(index_score_tc_kernel<QG>,
+    const size_t smem = sizeof(TcSmem<QG, FU>) + 1024;
+    cudaError_t e = cudaFuncSetAttribute(index_score_tc_kernel<QG, FU>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     // the whole unified L1 as shared memory, so the resident CTAs fit on every SM
-    e = cudaFuncSetAttribute(index_score_tc_kernel<QG>, cudaFuncAttributePreferredSharedMemoryCarveout,
+    e = cudaFuncSetAttribute(index_score_tc_kernel<QG, FU>, cudaFuncAttributePreferredSharedMemoryCarveout,
                              (int)cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
-    return launch_pdl(index_score_tc_kernel<QG>, dim3((unsigned)splits, (unsigned)units),
-                      dim3(kThreadsOf<QG>), smem_launch, s, 1, map, P);
+    return launch_pdl(index_score_tc_kernel<QG, FU>, dim3((unsigned)splits, (unsigned)units),
+                      dim3(kThreadsOf<QG>), smem, s, 1, map, P);
 }
 
 } // namespace
@@ -1201,7 +1201,8 @@ cudaError_t launch_index_tc(const csa2_index_args &a, float *scores, int32_t *ro
                              CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    return qg == 4 ? launch_tc<4>(map, P, units, splits, s) : launch_tc<1>(map, P, units, splits, s);
+    if (qg == 4) return launch_tc<4, false>(map, P, units, splits, s);
+    return fo ? launch_tc<1, true>(map, P, units, splits, s) : launch_tc<1, false>(map, P, units, splits, s);
 }
 
 } // namespace csa2

@@ -751,7 +751,7 @@ struct TopkLists {
 };
 constexpr int kMaxLists = 1024;
 
-template <bool EXACT, int D, bool LISTS>
+template <bool EXACT, int D, bool LISTS, bool SHORT>
 __global__ void __launch_bounds__(kGThreads, 1)
 topk_gmax_kernel(const float *__restrict__ scores, int64_t n, int64_t rows, const int32_t *__restrict__ row_len,
                  const int32_t *__restrict__ pool, int32_t block, int32_t k, int32_t *__restrict__ idx,
@@ -766,6 +766,7 @@ topk_gmax_kernel(const float *__restrict__ scores, int64_t n, int64_t rows, cons
     uint32_t *s_ck = g_sm + kListCap;                      // candidate keys
     int32_t *s_cp = reinterpret_cast<int32_t *>(s_ck + kCandCap);   // candidate positions (index)
     static_assert(2 * kCandCap >= kMaxGroups, "group keys and candidates share their space");
+    static_assert(16 * kGThreads <= kCandCap && 2 * kGThreads <= 2 * kCandCap, "short rows fit on chip");
     __shared__ GSmem S;
     __shared__ uint32_t s_red[64];
     __shared__ exact::QuantQuery QQ;                       // exact order: the row's query
@@ -943,6 +944,79 @@ topk_gmax_kernel(const float *__restrict__ scores, int64_t n, int64_t rows, cons
             }
             continue;
         }
+    } else if constexpr (SHORT) {
+        // ---- short rows (a Reindex pool, a short context): thread t holds the keys of
+        //      candidates [16 t, 16 t + 16) in registers.  Each of the k blocks of 8 with the
+        //      largest maxima holds an element >= the k-th largest block maximum, so a lower
+        //      bound of that maximum keeps every top-k element; only the elements at or above
+        //      it are listed.  (Groups of 32 cannot prune a row of 16,384 at k = 512.)
+        const int64_t b0 = 16 * (int64_t)tid;
+        uint32_t kv[16];
+        if (b0 >= len) {
+    #pragma unroll
+            for (int i = 0; i < 16; ++i) kv[i] = 0u;
+        } else if (b0 + 16 <= n && (reinterpret_cast<uintptr_t>(s) & 15u) == 0) {
+            const float4 *src = reinterpret_cast<const float4 *>(s + b0);
+            float4 f[4];
+    #pragma unroll
+            for (int e = 0; e < 4; ++e) f[e] = src[e];
+    #pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                kv[4 * e] = score_key(f[e].x);
+                kv[4 * e + 1] = score_key(f[e].y);
+                kv[4 * e + 2] = score_key(f[e].z);
+                kv[4 * e + 3] = score_key(f[e].w);
+            }
+        } else {
+    #pragma unroll
+            for (int i = 0; i < 16; ++i) kv[i] = b0 + i < len ? score_key(s[b0 + i]) : 0u;
+        }
+    #pragma unroll
+        for (int i = 0; i < 16; ++i)
+            if (b0 + i >= len) kv[i] = 0u;
+        uint32_t bm0 = 0, bm1 = 0;                             // maxima of the thread's two blocks
+    #pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            bm0 = max(bm0, kv[i]);
+            bm1 = max(bm1, kv[8 + i]);
+        }
+        s_gk[2 * tid] = bm0;
+        s_gk[2 * tid + 1] = bm1;
+        // a group of 32 (two threads) whose maximum is not finite: as in the grouped path
+        uint32_t g32 = max(bm0, bm1);
+        g32 = max(g32, __shfl_xor_sync(0xffffffffu, g32, 1));
+        nonfinite = (tid & 1) == 0 && b0 < len && (g32 >= 0xff800000u || g32 <= 0x007fffffu);
+        nonfinite = __syncthreads_or(nonfinite) != 0;
+        if constexpr (EXACT) {
+            seq = row / X.n_q;
+            if (row == (int64_t)blockIdx.x) {
+                rb = rb_first;
+            } else {
+                exact::quantise_query(QQ, X.q + row * (int64_t)X.H * D, X.w + row * (int64_t)X.H, X.H, D);
+                rb = row_bound(QQ, X, seq, s_red);
+            }
+            if (nonfinite) rb.c0 = -1.0f;
+        }
+        const bool ex_row = EXACT && rb.c0 >= 0.0f;
+        const int nb = (int)((len + 7) / 8);
+        uint32_t need0;
+        uint32_t tau0 = nb > k ? g_threshold(s_gk, nb, (uint32_t)k, S, need0, 2) : 0u;
+        if (ex_row && tau0 != 0u) tau0 = score_key(rb.lo(key_value(tau0)));
+        uint32_t sel = 0;
+    #pragma unroll
+        for (int i = 0; i < 16; ++i) sel |= (uint32_t)(b0 + i < len && kv[i] >= tau0) << i;
+        uint32_t tot;
+        uint32_t o = block_excl_count_sum((uint32_t)__popc(sel), S.warp, tot);   // block maxima read
+    #pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            if ((sel >> i) & 1u) {
+                s_ck[o] = kv[i];
+                s_cp[o] = (int32_t)(b0 + i);
+                ++o;
+            }
+        }
+        n_c = tot;                                         // <= 16 kGThreads = kCandCap
+        __syncthreads();
     } else {
         const int ng = (int)((len + gs - 1) / gs);             // <= kMaxGroups
         const uint32_t *gk = s_gk;
@@ -1200,16 +1274,16 @@ size_t group_keys_bytes(int64_t rows, int64_t n)
 }
 
 // The selection kernel for float order, or exact order at the indexer head dim.
-template <bool EXACT, int D, bool LISTS = false>
+template <bool EXACT, int D, bool LISTS = false, bool SHORT = false>
 cudaError_t launch_gmax(unsigned grid, size_t smem, cudaStream_t s, const float *scores, int64_t n, int64_t rows,
                         const int32_t *row_len, const int32_t *pool, int32_t block, int32_t k, int32_t *idx,
                         float *out_scores, const uint32_t *gkeys, int32_t gs, int64_t G, const ExactArgs &X,
                         const TopkLists &L = TopkLists{})
 {
-    cudaError_t e = cudaFuncSetAttribute(topk_gmax_kernel<EXACT, D, LISTS>,
+    cudaError_t e = cudaFuncSetAttribute(topk_gmax_kernel<EXACT, D, LISTS, SHORT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(topk_gmax_kernel<EXACT, D, LISTS>, dim3(grid), dim3(kGThreads), smem, s, 1, scores, n, rows,
+    return launch_pdl(topk_gmax_kernel<EXACT, D, LISTS, SHORT>, dim3(grid), dim3(kGThreads), smem, s, 1, scores, n, rows,
                       row_len, pool, block, k, idx, out_scores, gkeys, gs, G, X, L);
 }
 
@@ -1237,8 +1311,11 @@ cudaError_t launch_topk(const float *scores, int64_t rows, int64_t n, const int3
     const int32_t gs = group_size_for(n);
     const int64_t G = (n + gs - 1) / gs;
     const uint32_t *gkeys = static_cast<const uint32_t *>(ws);
-    if (group_max && gs == 32) {
-        gkeys = group_max;                                 // written by the indexer
+    // rows of at most 16 candidates a thread: the short-row instance (its bound comes from
+    // maxima of blocks of 8 it takes itself, no group keys)
+    const bool short_rows = n <= 16 * kGThreads;
+    if (short_rows || (group_max && gs == 32)) {
+        if (!short_rows) gkeys = group_max;                // written by the indexer
     } else if (G > 0) {
         uint32_t *gk = static_cast<uint32_t *>(ws);
         if (gs == 32 && ((uintptr_t)scores % 16) == 0 && n % 4 == 0) {
@@ -1255,8 +1332,11 @@ cudaError_t launch_topk(const float *scores, int64_t rows, int64_t n, const int3
     }
     const size_t smem = (size_t)(kListCap + 2 * kCandCap) * sizeof(uint32_t);
     ExactArgs X = {};
-    if (!ex) return launch_gmax<false, 0>((unsigned)rows, smem, s, scores, n, rows, row_len, pool, block, k, idx,
-                                          out_scores, gkeys, gs, G, X);
+    if (!ex)
+        return short_rows ? launch_gmax<false, 0, false, true>((unsigned)rows, smem, s, scores, n, rows, row_len, pool,
+                                                               block, k, idx, out_scores, gkeys, gs, G, X)
+                          : launch_gmax<false, 0>((unsigned)rows, smem, s, scores, n, rows, row_len, pool, block, k,
+                                                  idx, out_scores, gkeys, gs, G, X);
     // exact order: persistent CTAs (at most one per SM and per band slot), rows strided
     X.H = ex->n_heads;
     X.d = ex->head_dim;
@@ -1274,13 +1354,17 @@ cudaError_t launch_topk(const float *scores, int64_t rows, int64_t n, const int3
     X.d_status = d_status;
     int64_t grid = exact_slots(rows);
     if (grid > device_sm_count()) grid = device_sm_count();
+#define CSA2_TOPK_CASE(DIM)                                                                                  \
+    case DIM:                                                                                                \
+        return short_rows ? launch_gmax<true, DIM, false, true>((unsigned)grid, smem, s, scores, n, rows, row_len, \
+                                                                pool, block, k, idx, out_scores, gkeys, gs, G, X)    \
+                          : launch_gmax<true, DIM>((unsigned)grid, smem, s, scores, n, rows, row_len, pool, block,  \
+                                                   k, idx, out_scores, gkeys, gs, G, X);
     switch (ex->head_dim) {
-    case 32: return launch_gmax<true, 32>((unsigned)grid, smem, s, scores, n, rows, row_len, pool, block, k, idx,
-                                          out_scores, gkeys, gs, G, X);
-    case 64: return launch_gmax<true, 64>((unsigned)grid, smem, s, scores, n, rows, row_len, pool, block, k, idx,
-                                          out_scores, gkeys, gs, G, X);
-    case 128: return launch_gmax<true, 128>((unsigned)grid, smem, s, scores, n, rows, row_len, pool, block, k,
-                                            idx, out_scores, gkeys, gs, G, X);
+    CSA2_TOPK_CASE(32)
+    CSA2_TOPK_CASE(64)
+    CSA2_TOPK_CASE(128)
+#undef CSA2_TOPK_CASE
     default: return cudaErrorInvalidValue;
     }
 }

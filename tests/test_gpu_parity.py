@@ -712,7 +712,8 @@ def test_pool_flags_bad_order():
 
 # ------------------------------------------------------------------ selection on given scores
 @pytest.mark.parametrize("rows,n,k,levels", [(3, 300000, 512, 7), (5, 1000, 512, 3), (2, 70000, 2048, 100000),
-                                             (4, 4097, 1, 2), (1, 1 << 20, 512, 1 << 20)])
+                                             (4, 4097, 1, 2), (1, 1 << 20, 512, 1 << 20),
+                                             (2, 600000, 2048, 50000)])
 def test_topk_on_given_scores(rows, n, k, levels):
     rng = np.random.default_rng(rows * n + k)
     s = (rng.integers(0, levels, size=(rows, n)).astype(np.float32) - levels // 2) * np.float32(0.5)

@@ -56,6 +56,98 @@ __device__ __forceinline__ float warp_sum(float v)
     return v;
 }
 
+// One 16-value chunk of a tile's key row (values 16 q .. 16 q + 15): its raw bytes are
+// loaded first (every load of a thread's chunks in flight together), then widened to float.
+struct KvChunk {
+    uint4 a, b;              // main KV: a.x, a.y = the 8 code bytes; SWA: the 16 values' bytes
+    uint32_t scale;          // the chunk's scale byte (main KV, MXFP8 SWA)
+    int kind;                // 0: none (zeros), 1: main KV, 2: bf16 SWA, 3: MXFP8 SWA
+};
+
+__device__ __forceinline__ KvChunk load_chunk(const AttnParams &P, int64_t b, int64_t src, int q)
+{
+    KvChunk k;
+    k.a = make_uint4(0u, 0u, 0u, 0u);
+    k.b = k.a;
+    k.scale = 0u;
+    k.kind = 0;
+    if (src >= 0) {
+        const int64_t r = b * P.n_kv + src;
+        const uint8_t *cp = P.kvc + r * (P.d_qk / 2) + q * 8;
+        if ((reinterpret_cast<uintptr_t>(cp) & 7u) == 0) {
+            const uint2 v = *reinterpret_cast<const uint2 *>(cp);
+            k.a.x = v.x;
+            k.a.y = v.y;
+        } else {
+            uint32_t w[2] = {0u, 0u};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) w[i >> 2] |= (uint32_t)cp[i] << (8 * (i & 3));
+            k.a.x = w[0];
+            k.a.y = w[1];
+        }
+        k.scale = P.nv ? P.kvs[r * (P.d_qk / 16) + q] : P.kvs[r * (P.d_qk / 32) + q / 2];
+        k.kind = 1;
+    } else if (src <= -2) {
+        const int64_t r = b * P.n_swa + (-src - 2);
+        if (P.swa8) {        // 16 E4M3 bytes and the block's E8M0 scale
+            const uint8_t *vp = reinterpret_cast<const uint8_t *>(P.swa) + r * P.d_qk + q * 16;
+            if ((reinterpret_cast<uintptr_t>(vp) & 15u) == 0) {
+                k.a = *reinterpret_cast<const uint4 *>(vp);
+            } else {
+                uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+                for (int i = 0; i < 16; ++i) w[i >> 2] |= (uint32_t)vp[i] << (8 * (i & 3));
+                k.a = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+            k.scale = P.swa_scales[r * (P.d_qk / 32) + q / 2];
+            k.kind = 3;
+        } else {             // 16 bf16
+            const uint16_t *vp = P.swa + r * (int64_t)P.d_qk + q * 16;
+            if ((reinterpret_cast<uintptr_t>(vp) & 15u) == 0) {
+                k.a = reinterpret_cast<const uint4 *>(vp)[0];
+                k.b = reinterpret_cast<const uint4 *>(vp)[1];
+            } else {
+                uint32_t w[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) w[i] = (uint32_t)vp[2 * i] | ((uint32_t)vp[2 * i + 1] << 16);
+                k.a = make_uint4(w[0], w[1], w[2], w[3]);
+                k.b = make_uint4(w[4], w[5], w[6], w[7]);
+            }
+            k.kind = 2;
+        }
+    }
+    return k;
+}
+
+__device__ __forceinline__ void store_chunk(const AttnParams &P, const KvChunk &k, float *dst)
+{
+    if (k.kind == 1) {                   // E2M1 codes (low nibble first) times the block scale
+        const float sc = P.nv ? e4m3_value(k.scale) : e8m0_value(k.scale);
+        const uint32_t w[2] = {k.a.x, k.a.y};
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const uint32_t code = (w[i >> 3] >> (4 * (i & 7))) & 15u;
+            const float v = e2m1_mag(code & 7u) * sc;
+            dst[i] = (code & 8u) ? -v : v;
+        }
+    } else if (k.kind == 2) {
+        const uint32_t w[8] = {k.a.x, k.a.y, k.a.z, k.a.w, k.b.x, k.b.y, k.b.z, k.b.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            dst[2 * i] = __uint_as_float(w[i] << 16);
+            dst[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    } else if (k.kind == 3) {            // MXFP8: E4M3 value x 2^(e - 127), exact in float32
+        const float sc = e8m0_value(k.scale);
+        const uint32_t w[4] = {k.a.x, k.a.y, k.a.z, k.a.w};
+#pragma unroll
+        for (int i = 0; i < 16; ++i) dst[i] = e4m3_value((w[i >> 2] >> (8 * (i & 3))) & 255u) * sc;
+    } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) dst[i] = 0.0f;
+    }
+}
+
 template <int CPT>
 __global__ void __launch_bounds__(kThreads) sparse_attn_cc_kernel(AttnParams P)
 {
@@ -72,11 +164,29 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_cc_kernel(AttnParams P)
     const int64_t b = row / P.T;
     const int h0 = blockIdx.x * kHG;
 
-    for (int e = tid; e < kHG * P.d_qk; e += kThreads) {
-        const int hh = e / P.d_qk, c = e % P.d_qk;
-        s_q[e] = (h0 + hh < P.H)
-                     ? __uint_as_float((uint32_t)P.q[(row * P.H + h0 + hh) * (int64_t)P.d_qk + c] << 16)
-                     : 0.0f;
+    // the head group's query rows, 8 bf16 a load where the rows are 16-byte aligned
+    if ((reinterpret_cast<uintptr_t>(P.q) & 15u) == 0) {
+        const int n8 = P.d_qk / 8;
+        for (int e = tid; e < kHG * n8; e += kThreads) {
+            const int hh = e / n8, c8 = e - hh * n8;
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (h0 + hh < P.H)
+                v = *reinterpret_cast<const uint4 *>(P.q + (row * P.H + h0 + hh) * (int64_t)P.d_qk + c8 * 8);
+            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+            float *dst = s_q + hh * P.d_qk + c8 * 8;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                dst[2 * i] = __uint_as_float(w4[i] << 16);
+                dst[2 * i + 1] = __uint_as_float(w4[i] & 0xffff0000u);
+            }
+        }
+    } else {
+        for (int e = tid; e < kHG * P.d_qk; e += kThreads) {
+            const int hh = e / P.d_qk, c = e % P.d_qk;
+            s_q[e] = (h0 + hh < P.H)
+                         ? __uint_as_float((uint32_t)P.q[(row * P.H + h0 + hh) * (int64_t)P.d_qk + c] << 16)
+                         : 0.0f;
+        }
     }
 
     // SWA slots of this query: tokens [max(s, p - W + 1, 0), p] of a buffer whose slot 0
@@ -121,28 +231,24 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_cc_kernel(AttnParams P)
             s_src[tid] = src;
         }
         __syncthreads();
-        // gather + dequantise (main KV) or widen (SWA) the tile's keys
-        for (int e = tid; e < kKT * P.d_qk; e += kThreads) {
-            const int j = e / P.d_qk, c = e % P.d_qk;
-            const int64_t src = s_src[j];
-            float v = 0.0f;
-            if (src >= 0) {
-                const int64_t r = b * P.n_kv + src;
-                const uint32_t byte = P.kvc[r * (P.d_qk / 2) + c / 2];
-                const uint32_t code = (c & 1) ? (byte >> 4) : (byte & 15u);
-                v = e2m1_mag(code & 7u) * (P.nv ? e4m3_value(P.kvs[r * (P.d_qk / 16) + c / 16])
-                                                : e8m0_value(P.kvs[r * (P.d_qk / 32) + c / 32]));
-                if (code & 8u) v = -v;
-            } else if (src <= -2) {
-                const int64_t slot = -src - 2;
-                const int64_t r = b * P.n_swa + slot;
-                if (P.swa8)      // MXFP8: E4M3 value x 2^(e - 127), exact in float32
-                    v = e4m3_value(reinterpret_cast<const uint8_t *>(P.swa)[r * P.d_qk + c]) *
-                        e8m0_value(P.swa_scales[r * (P.d_qk / 32) + c / 32]);
-                else
-                    v = __uint_as_float((uint32_t)P.swa[r * (int64_t)P.d_qk + c] << 16);
+        // gather + dequantise (main KV) or widen (SWA) the tile's keys: 16-value chunks, two
+        // per thread and pass, both loaded before either is widened (d_qk = 128: one pass)
+        {
+            const int nch = P.d_qk / 16, nchunk = kKT * nch;
+            for (int c0 = 0; c0 < nchunk; c0 += 2 * kThreads) {
+                KvChunk kc[2];
+                int at[2];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int ch = c0 + u * kThreads + tid;
+                    const int j = ch / nch, q = ch - j * nch;
+                    kc[u] = load_chunk(P, b, ch < nchunk ? s_src[j] : -1, q);
+                    at[u] = ch < nchunk ? j * ldk + q * 16 : -1;
+                }
+#pragma unroll
+                for (int u = 0; u < 2; ++u)
+                    if (at[u] >= 0) store_chunk(P, kc[u], s_k + at[u]);
             }
-            s_k[j * ldk + c] = v;
         }
         __syncthreads();
         // logits: warp = head, lane = key
@@ -231,42 +337,50 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_cc_kernel(AttnParams P)
     }
 }
 
-// Merge of a split row: thread = output column, one CTA per (head group, row):
+// Merge of a split row, one CTA per (head group, row) and one warp per head (at most
+// 2 x 152 spans a row: the weights take at most 9.7 KB of shared memory):
 //   o = sum_s e^(m_s - M) acc_s / sum_s e^(m_s - M) l_s,  lse = M + ln(sum_s e^(m_s - M) l_s)
 __global__ void __launch_bounds__(kThreads) sparse_attn_cc_merge_kernel(AttnParams P)
 {
+    // warp hh merges head blockIdx.x * kHG + hh: lanes take the spans for M and the sum L,
+    // the spans' weights e^(m_s - M) go to shared memory, then lanes take output columns
+    static_assert(kThreads == 32 * kHG, "one warp per head");
+    extern __shared__ float s_e[];                         // [kHG][splits]
     const int64_t row = blockIdx.y;
     const int S = P.splits;
-    const float *part = P.part + ((row * gridDim.x + blockIdx.x) * S * kHG) * (int64_t)(P.d_v + 2);
-#pragma unroll 1
-    for (int hh = 0; hh < kHG; ++hh) {
-        const int h = blockIdx.x * kHG + hh;
-        if (h >= P.H) break;
-        float M = -INFINITY;
-#pragma unroll 1
-        for (int z = 0; z < S; ++z) M = fmaxf(M, part[(z * kHG + hh) * (int64_t)(P.d_v + 2)]);
-        float L = 0.0f;
-#pragma unroll 1
-        for (int z = 0; z < S; ++z) {
-            const float *pz = part + (z * kHG + hh) * (int64_t)(P.d_v + 2);
-            if (pz[0] != -INFINITY) L += expf(pz[0] - M) * pz[1];
-        }
-        const float inv = L > 0.0f ? 1.0f / L : 0.0f;
-#pragma unroll 1
-        for (int c = threadIdx.x; c < P.d_v; c += kThreads) {
-            float o = 0.0f;
-#pragma unroll 1
-            for (int z = 0; z < S; ++z) {
-                const float *pz = part + (z * kHG + hh) * (int64_t)(P.d_v + 2);
-                if (pz[0] != -INFINITY) o = fmaf(expf(pz[0] - M), pz[2 + c], o);
-            }
-            o *= inv;
-            uint32_t bits = __float_as_uint(o);       // round to nearest even bf16
-            bits += 0x7fffu + ((bits >> 16) & 1u);
-            P.out[(row * P.H + h) * (int64_t)P.d_v + c] = (uint16_t)(bits >> 16);
-        }
-        if (P.lse && threadIdx.x == 0) P.lse[row * P.H + h] = L > 0.0f ? M + logf(L) : -INFINITY;
+    const int lane = threadIdx.x & 31, hh = threadIdx.x >> 5;
+    const int h = blockIdx.x * kHG + hh;
+    if (h >= P.H) return;                                  // whole warps; no block barrier follows
+    const int64_t stride = kHG * (int64_t)(P.d_v + 2);     // from one span's partial to the next
+    const float *ph = P.part + ((row * gridDim.x + blockIdx.x) * S * kHG + hh) * (int64_t)(P.d_v + 2);
+    float *se = s_e + hh * S;
+    float M = -INFINITY;
+    for (int z = lane; z < S; z += 32) M = fmaxf(M, ph[z * stride]);
+    M = warp_max(M);
+    float L = 0.0f;
+    for (int z = lane; z < S; z += 32) {
+        const float m = ph[z * stride];
+        const float e = m != -INFINITY ? expf(m - M) : 0.0f;   // a span without keys adds nothing
+        se[z] = e;
+        if (e != 0.0f) L += e * ph[z * stride + 1];
     }
+    L = warp_sum(L);
+    __syncwarp();
+    const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+    for (int c = lane; c < P.d_v; c += 32) {
+        float o = 0.0f;
+#pragma unroll 4
+        for (int z = 0; z < S; ++z) {
+            const float e = se[z];
+            const float v = ph[z * stride + 2 + c];
+            if (e != 0.0f) o = fmaf(e, v, o);
+        }
+        o *= inv;
+        uint32_t bits = __float_as_uint(o);                // round to nearest even bf16
+        bits += 0x7fffu + ((bits >> 16) & 1u);
+        P.out[(row * P.H + h) * (int64_t)P.d_v + c] = (uint16_t)(bits >> 16);
+    }
+    if (P.lse && lane == 0) P.lse[row * P.H + h] = L > 0.0f ? M + logf(L) : -INFINITY;
 }
 
 // Spans per row: enough CTAs for about two per SM, at most one per 32-key tile of the
@@ -297,7 +411,7 @@ cudaError_t launch_cc(const AttnParams &P, int64_t rows, cudaStream_t s)
     if (P.splits > 1) {
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
-        sparse_attn_cc_merge_kernel<<<dim3(grid.x, grid.y), kThreads, 0, s>>>(P);
+        sparse_attn_cc_merge_kernel<<<dim3(grid.x, grid.y), kThreads, sizeof(float) * kHG * P.splits, s>>>(P);
     }
     return cudaGetLastError();
 }

@@ -216,6 +216,10 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_cc_kernel(AttnParams P)
         for (int u = 0; u < CPT; ++u) acc[hh][u] = 0.0f;
     float m_run = -INFINITY, l_run = 0.0f;   // per-head state, held by the head's warp
     const int my_h = h0 + warp;
+    // the query, positions and SWA range above come from inputs the kernel before does not
+    // write; the indices (and the keys they select) from here on may
+    pdl_wait();
+    pdl_allow_dependents();
 
     for (int64_t t0 = t_lo; t0 < t_hi; t0 += kKT) {
         if (tid < kKT) {
@@ -350,6 +354,8 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_cc_merge_kernel(AttnPara
     const int S = P.splits;
     const int lane = threadIdx.x & 31, hh = threadIdx.x >> 5;
     const int h = blockIdx.x * kHG + hh;
+    pdl_wait();                                            // the spans' partials
+    pdl_allow_dependents();
     if (h >= P.H) return;                                  // whole warps; no block barrier follows
     const int64_t stride = kHG * (int64_t)(P.d_v + 2);     // from one span's partial to the next
     const float *ph = P.part + ((row * gridDim.x + blockIdx.x) * S * kHG + hh) * (int64_t)(P.d_v + 2);
@@ -407,13 +413,10 @@ cudaError_t launch_cc(const AttnParams &P, int64_t rows, cudaStream_t s)
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)((P.H + kHG - 1) / kHG), (unsigned)rows, (unsigned)P.splits);
-    sparse_attn_cc_kernel<CPT><<<grid, kThreads, smem, s>>>(P);
-    if (P.splits > 1) {
-        e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-        sparse_attn_cc_merge_kernel<<<dim3(grid.x, grid.y), kThreads, sizeof(float) * kHG * P.splits, s>>>(P);
-    }
-    return cudaGetLastError();
+    e = launch_pdl(sparse_attn_cc_kernel<CPT>, grid, dim3(kThreads), smem, s, 1, P);
+    if (e != cudaSuccess || P.splits <= 1) return e;
+    return launch_pdl(sparse_attn_cc_merge_kernel, dim3(grid.x, grid.y), dim3(kThreads),
+                      sizeof(float) * kHG * P.splits, s, 1, P);
 }
 
 } // namespace

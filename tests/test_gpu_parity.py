@@ -405,8 +405,11 @@ def test_scores_wide_exponents(T, sparse, N):
             assert np.array_equal(gm[b, t].cpu().numpy().view(np.uint32), group_keys(s_ref))
 
 
-def test_pool_scores_and_topk():
-    w = W["reuse_reindex_decode_128k"].scaled(batch=3, n_q=2, n_keys=40000, q_pos0=30000,
+@pytest.mark.parametrize("n_keys,q_pos0", [(40000, 30000), (40003, 40001)])
+def test_pool_scores_and_topk(n_keys, q_pos0):
+    # 40,003 rows a sequence put the second and third sequences' scale words off the
+    # 16-byte grid (their blocks' words are copied one by one) and end in a partial block
+    w = W["reuse_reindex_decode_128k"].scaled(batch=3, n_q=2, n_keys=n_keys, q_pos0=q_pos0,
                                               n_blocks=700)
     st = status()
     dw = workload.build(w, kv=False, device=DEV, d_status=st)

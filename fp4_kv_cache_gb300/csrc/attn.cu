@@ -344,6 +344,7 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_cc_kernel(AttnParams P)
 // Merge of a split row, one CTA per (head group, row) and one warp per head (at most
 // 2 x 152 spans a row: the weights take at most 9.7 KB of shared memory):
 //   o = sum_s e^(m_s - M) acc_s / sum_s e^(m_s - M) l_s,  lse = M + ln(sum_s e^(m_s - M) l_s)
+template <int NC>           // output columns per lane (d_v <= 32 NC)
 __global__ void __launch_bounds__(kThreads) sparse_attn_cc_merge_kernel(AttnParams P)
 {
     // warp hh merges head blockIdx.x * kHG + hh: lanes take the spans for M and the sum L,
@@ -373,16 +374,35 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_cc_merge_kernel(AttnPara
     L = warp_sum(L);
     __syncwarp();
     const float inv = L > 0.0f ? 1.0f / L : 0.0f;
-    for (int c = lane; c < P.d_v; c += 32) {
-        float o = 0.0f;
-#pragma unroll 4
-        for (int z = 0; z < S; ++z) {
-            const float e = se[z];
-            const float v = ph[z * stride + 2 + c];
-            if (e != 0.0f) o = fmaf(e, v, o);
+    // lane columns c = lane + 32 k; four spans' values of all of them loaded together, then
+    // each column's chain advances over those spans in order
+    float o[NC];
+#pragma unroll
+    for (int k = 0; k < NC; ++k) o[k] = 0.0f;
+    for (int z0 = 0; z0 < S; z0 += 4) {
+        float v[4][NC], e[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int z = z0 + u;
+            e[u] = z < S ? se[z] : 0.0f;
+#pragma unroll
+            for (int k = 0; k < NC; ++k) {
+                const int c = lane + 32 * k;
+                v[u][k] = (z < S && c < P.d_v) ? ph[z * stride + 2 + c] : 0.0f;
+            }
         }
-        o *= inv;
-        uint32_t bits = __float_as_uint(o);                // round to nearest even bf16
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (e[u] != 0.0f) {
+#pragma unroll
+                for (int k = 0; k < NC; ++k) o[k] = fmaf(e[u], v[u][k], o[k]);
+            }
+    }
+#pragma unroll
+    for (int k = 0; k < NC; ++k) {
+        const int c = lane + 32 * k;
+        if (c >= P.d_v) break;
+        uint32_t bits = __float_as_uint(o[k] * inv);       // round to nearest even bf16
         bits += 0x7fffu + ((bits >> 16) & 1u);
         P.out[(row * P.H + h) * (int64_t)P.d_v + c] = (uint16_t)(bits >> 16);
     }
@@ -415,8 +435,15 @@ cudaError_t launch_cc(const AttnParams &P, int64_t rows, cudaStream_t s)
     dim3 grid((unsigned)((P.H + kHG - 1) / kHG), (unsigned)rows, (unsigned)P.splits);
     e = launch_pdl(sparse_attn_cc_kernel<CPT>, grid, dim3(kThreads), smem, s, 1, P);
     if (e != cudaSuccess || P.splits <= 1) return e;
-    return launch_pdl(sparse_attn_cc_merge_kernel, dim3(grid.x, grid.y), dim3(kThreads),
-                      sizeof(float) * kHG * P.splits, s, 1, P);
+    const dim3 mg(grid.x, grid.y);
+    const size_t msm = sizeof(float) * kHG * P.splits;
+    const int nc = (P.d_v + 31) / 32;                    // d_v <= d_qk <= 1024
+    if (nc <= 1) return launch_pdl(sparse_attn_cc_merge_kernel<1>, mg, dim3(kThreads), msm, s, 1, P);
+    if (nc <= 2) return launch_pdl(sparse_attn_cc_merge_kernel<2>, mg, dim3(kThreads), msm, s, 1, P);
+    if (nc <= 4) return launch_pdl(sparse_attn_cc_merge_kernel<4>, mg, dim3(kThreads), msm, s, 1, P);
+    if (nc <= 8) return launch_pdl(sparse_attn_cc_merge_kernel<8>, mg, dim3(kThreads), msm, s, 1, P);
+    if (nc <= 16) return launch_pdl(sparse_attn_cc_merge_kernel<16>, mg, dim3(kThreads), msm, s, 1, P);
+    return launch_pdl(sparse_attn_cc_merge_kernel<32>, mg, dim3(kThreads), msm, s, 1, P);
 }
 
 } // namespace

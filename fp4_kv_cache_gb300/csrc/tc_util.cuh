@@ -35,13 +35,6 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
 {
     asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
-// Arrive without release semantics: for a barrier that only hands a resource back (the
-// waiter reads nothing this thread wrote), so the arrive need not wait for this thread's
-// earlier global stores to be performed.
-__device__ __forceinline__ void mbar_arrive_relaxed(uint64_t *bar)
-{
-    asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
 {
     asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;"

@@ -155,6 +155,15 @@ def test_index_rejects_bad_args(lib):
     a.k_codes = ctypes.c_void_p(257)                                       # misaligned
     assert f(ctypes.byref(a), FAKE, FAKE, None, 0, None, None) == 1
     a.k_codes = FAKE
+    a.fresh_from = -1                                                      # no such position
+    assert f(ctypes.byref(a), FAKE, FAKE, None, 0, None, None) == 1
+    a.fresh_from = 0
+    g = lib.csa2_index_topk                                                # (args, k, idx, out_scores, row_len, ws, bytes, status, stream)
+    assert g(ctypes.byref(a), -1, FAKE, None, None, FAKE, 1 << 20, None, None) == 1      # k < 0
+    assert g(ctypes.byref(a), 512, None, None, None, FAKE, 1 << 20, None, None) == 1     # idx missing
+    a.q = ctypes.c_void_p(4104)                                            # q not 16-byte aligned
+    assert g(ctypes.byref(a), 512, FAKE, None, None, FAKE, 1 << 20, None, None) == 1
+    a.q = FAKE
     a.mode, a.n_pool_blocks, a.pool_blocks = 1, 16, None                   # pool missing
     assert f(ctypes.byref(a), FAKE, FAKE, None, 0, None, None) == 1
     a.batch = 0

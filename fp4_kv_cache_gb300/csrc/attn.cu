@@ -361,28 +361,36 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_cc_merge_kernel(AttnPara
     const int64_t stride = kHG * (int64_t)(P.d_v + 2);     // from one span's partial to the next
     const float *ph = P.part + ((row * gridDim.x + blockIdx.x) * S * kHG + hh) * (int64_t)(P.d_v + 2);
     float *se = s_e + hh * S;
-    float M = -INFINITY;
-    for (int z = lane; z < S; z += 32) M = fmaxf(M, ph[z * stride]);
+    // lane z's first span's (m, l) are read once and kept (spans from 32 on are read again)
+    float m0 = -INFINITY, l0 = 0.0f;
+    if (lane < S) {
+        m0 = ph[lane * stride];
+        l0 = ph[lane * stride + 1];
+    }
+    float M = m0;
+    for (int z = lane + 32; z < S; z += 32) M = fmaxf(M, ph[z * stride]);
     M = warp_max(M);
     float L = 0.0f;
     for (int z = lane; z < S; z += 32) {
-        const float m = ph[z * stride];
+        const float m = z == lane ? m0 : ph[z * stride];
+        const float l = z == lane ? l0 : ph[z * stride + 1];
         const float e = m != -INFINITY ? expf(m - M) : 0.0f;   // a span without keys adds nothing
         se[z] = e;
-        if (e != 0.0f) L += e * ph[z * stride + 1];
+        if (e != 0.0f) L += e * l;
     }
     L = warp_sum(L);
     __syncwarp();
     const float inv = L > 0.0f ? 1.0f / L : 0.0f;
-    // lane columns c = lane + 32 k; four spans' values of all of them loaded together, then
-    // each column's chain advances over those spans in order
+    // lane columns c = lane + 32 k; CH spans' values of all of them loaded together (CH x NC
+    // registers), then each column's chain advances over those spans in order
+    constexpr int CH = NC <= 4 ? 8 : (NC <= 16 ? 4 : 2);
     float o[NC];
 #pragma unroll
     for (int k = 0; k < NC; ++k) o[k] = 0.0f;
-    for (int z0 = 0; z0 < S; z0 += 4) {
-        float v[4][NC], e[4];
+    for (int z0 = 0; z0 < S; z0 += CH) {
+        float v[CH][NC], e[CH];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < CH; ++u) {
             const int z = z0 + u;
             e[u] = z < S ? se[z] : 0.0f;
 #pragma unroll
@@ -392,7 +400,7 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_cc_merge_kernel(AttnPara
             }
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
+        for (int u = 0; u < CH; ++u)
             if (e[u] != 0.0f) {
 #pragma unroll
                 for (int k = 0; k < NC; ++k) o[k] = fmaf(e[u], v[u][k], o[k]);
